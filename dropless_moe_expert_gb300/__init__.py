@@ -1,0 +1,342 @@
+"""Dropless MoE SwiGLU layer forward on one GB300 -- Python binding.
+
+Thin ctypes binding over the C ABI in ``include/moe.h`` (library
+``libmoe_gb300.so`` built in-tree by ``build.py``).  Functions carry the C
+names without the ``moe_`` prefix, take torch tensors (device memory only,
+any stream), check dtypes/shapes/contiguity, and pass raw pointers plus the
+current CUDA stream.  Every step of the layer runs in the library's kernels;
+there is no fallback: if the library is missing, importing this package
+raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "MoEError", "lib", "router_logits", "route", "route_workspace_size", "permute", "grouped_mlp",
+    "grouped_gemm1_swiglu", "grouped_gemm2", "unpermute", "forward", "forward_workspace_size",
+    "forward_views", "forward_host", "device_status", "launch_count", "MoELayer",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
+           4: "MOE_ERR_CUDA", 5: "MOE_ERR_DEVICE_TIMEOUT"}
+
+
+class MoEError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        msg = lib.moe_status_string(code).decode() if _LIB is not None else _STATUS.get(code, str(code))
+        super().__init__(f"{where}: {msg}")
+
+
+class _Layout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in (
+        "logits", "topk_idx", "topk_w", "counts", "offsets", "row_of", "src_tok", "route_ws",
+        "x_perm", "h", "y_perm", "x_dev", "y_dev", "total")]
+
+
+def _load():
+    path = _build.lib_path()
+    if not os.path.exists(path):
+        raise ImportError(
+            f"{path} is missing: build the CUDA library first "
+            "(python -c 'import __graft_entry__ as g; g.build()')")
+    L = ctypes.CDLL(path)
+    P, I, S, U64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_uint64
+    sig = {
+        "moe_status_string": (ctypes.c_char_p, [I]),
+        "moe_abi_version": (I, []),
+        "moe_launch_count": (U64, []),
+        "moe_router_logits": (I, [P, P, P, I, I, I, P, P]),
+        "moe_route_workspace_size": (S, [I, I, I]),
+        "moe_route": (I, [P, I, I, I, P, P, P, P, P, P, P, S, P]),
+        "moe_permute": (I, [P, P, I, I, I, P, P]),
+        "moe_grouped_mlp": (I, [P, P, I, I, I, I, P, P, P, P, P]),
+        "moe_grouped_gemm1_swiglu": (I, [P, P, I, I, I, I, P, P, P]),
+        "moe_grouped_gemm2": (I, [P, P, I, I, I, I, P, P, P]),
+        "moe_unpermute": (I, [P, P, P, I, I, I, P, P]),
+        "moe_forward_workspace_size": (S, [I, I, I, I, I]),
+        "moe_forward_views": (I, [I, I, I, I, I, ctypes.POINTER(_Layout)]),
+        "moe_forward": (I, [P, P, P, P, P, I, I, I, I, I, P, P, S, P]),
+        "moe_forward_host": (I, [P, P, P, P, P, I, I, I, I, I, P, P, S, P]),
+        "moe_device_status": (I, [ctypes.POINTER(I)]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(L, name)
+        fn.restype = res
+        fn.argtypes = args
+    return L
+
+
+_LIB = _load()
+lib = _LIB
+
+
+# ------------------------------------------------------------------ helpers
+def _stream(stream=None) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _check(code: int, where: str):
+    if code != 0:
+        raise MoEError(code, where)
+
+
+def _need(t, dtype, shape, name):
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (the library has no CPU path)")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _empty(shape, dtype, like):
+    return torch.empty(shape, dtype=dtype, device=like.device)
+
+
+# ------------------------------------------------------------------ a0
+def router_logits(x, Wr, bias=None, out=None, stream=None):
+    """logits[T,E] fp32 = index-ordered FMA chain of x[t,:] . Wr[:,e], + bias[e]."""
+    T, d = x.shape
+    E = Wr.shape[1]
+    _need(x, torch.bfloat16, (T, d), "x")
+    _need(Wr, torch.float32, (d, E), "Wr")
+    if bias is not None:
+        _need(bias, torch.float32, (E,), "bias")
+    out = _empty((T, E), torch.float32, x) if out is None else _need(out, torch.float32, (T, E), "logits")
+    _check(lib.moe_router_logits(_ptr(x), _ptr(Wr), _ptr(bias), T, d, E, _ptr(out), _stream(stream)),
+           "moe_router_logits")
+    return out
+
+
+# ------------------------------------------------------------------ a1 + a2
+@dataclass
+class Routing:
+    topk_idx: torch.Tensor   # [T, K] int32
+    topk_w: torch.Tensor     # [T, K] fp32
+    counts: torch.Tensor     # [E] int32
+    offsets: torch.Tensor    # [E+1] int32
+    row_of: torch.Tensor     # [T, K] int32
+    src_tok: torch.Tensor    # [TK] int32
+
+
+def route_workspace_size(T: int, E: int, K: int) -> int:
+    return int(lib.moe_route_workspace_size(T, E, K))
+
+
+def route(logits, K: int, workspace=None, stream=None) -> Routing:
+    T, E = logits.shape
+    _need(logits, torch.float32, (T, E), "logits")
+    i32 = torch.int32
+    r = Routing(_empty((T, K), i32, logits), _empty((T, K), torch.float32, logits), _empty((E,), i32, logits),
+                _empty((E + 1,), i32, logits), _empty((T, K), i32, logits), _empty((T * K,), i32, logits))
+    nbytes = route_workspace_size(T, E, K)
+    if workspace is None:
+        workspace = _empty((max(nbytes, 4),), torch.uint8, logits)
+    _check(lib.moe_route(_ptr(logits), T, E, K, _ptr(r.topk_idx), _ptr(r.topk_w), _ptr(r.counts),
+                         _ptr(r.offsets), _ptr(r.row_of), _ptr(r.src_tok), _ptr(workspace),
+                         workspace.numel() * workspace.element_size(), _stream(stream)), "moe_route")
+    return r
+
+
+# ------------------------------------------------------------------ a3
+def permute(x, row_of, out=None, stream=None):
+    """x_perm[row_of[t,k]] = x[t]."""
+    T, d = x.shape
+    K = row_of.shape[1]
+    _need(x, torch.bfloat16, (T, d), "x")
+    _need(row_of, torch.int32, (T, K), "row_of")
+    out = _empty((T * K, d), torch.bfloat16, x) if out is None else _need(out, torch.bfloat16, (T * K, d), "x_perm")
+    _check(lib.moe_permute(_ptr(x), _ptr(row_of), T, K, d, _ptr(out), _stream(stream)), "moe_permute")
+    return out
+
+
+# ------------------------------------------------------------------ a4 + a5
+def _mlp_shapes(x_perm, offsets, W1=None, W2=None):
+    TK, d = x_perm.shape
+    E = offsets.shape[0] - 1
+    f = W1.shape[1] // 2 if W1 is not None else W2.shape[2]
+    return TK, d, E, f
+
+
+def grouped_gemm1_swiglu(x_perm, offsets, W1, h=None, stream=None):
+    TK, d, E, f = _mlp_shapes(x_perm, offsets, W1=W1)
+    _need(x_perm, torch.bfloat16, (TK, d), "x_perm")
+    _need(offsets, torch.int32, (E + 1,), "offsets")
+    _need(W1, torch.bfloat16, (E, 2 * f, d), "W1")
+    h = _empty((TK, f), torch.bfloat16, x_perm) if h is None else _need(h, torch.bfloat16, (TK, f), "h")
+    _check(lib.moe_grouped_gemm1_swiglu(_ptr(x_perm), _ptr(offsets), E, TK, d, f, _ptr(W1), _ptr(h),
+                                        _stream(stream)), "moe_grouped_gemm1_swiglu")
+    return h
+
+
+def grouped_gemm2(h, offsets, W2, y_perm=None, stream=None):
+    TK, f = h.shape
+    E = offsets.shape[0] - 1
+    d = W2.shape[1]
+    _need(h, torch.bfloat16, (TK, f), "h")
+    _need(offsets, torch.int32, (E + 1,), "offsets")
+    _need(W2, torch.bfloat16, (E, d, f), "W2")
+    y_perm = _empty((TK, d), torch.bfloat16, h) if y_perm is None else _need(y_perm, torch.bfloat16, (TK, d), "y_perm")
+    _check(lib.moe_grouped_gemm2(_ptr(h), _ptr(offsets), E, TK, d, f, _ptr(W2), _ptr(y_perm), _stream(stream)),
+           "moe_grouped_gemm2")
+    return y_perm
+
+
+def grouped_mlp(x_perm, offsets, W1, W2, h=None, y_perm=None, stream=None):
+    TK, d, E, f = _mlp_shapes(x_perm, offsets, W1=W1)
+    _need(x_perm, torch.bfloat16, (TK, d), "x_perm")
+    _need(offsets, torch.int32, (E + 1,), "offsets")
+    _need(W1, torch.bfloat16, (E, 2 * f, d), "W1")
+    _need(W2, torch.bfloat16, (E, d, f), "W2")
+    h = _empty((TK, f), torch.bfloat16, x_perm) if h is None else _need(h, torch.bfloat16, (TK, f), "h")
+    y_perm = _empty((TK, d), torch.bfloat16, x_perm) if y_perm is None else _need(y_perm, torch.bfloat16, (TK, d), "y_perm")
+    _check(lib.moe_grouped_mlp(_ptr(x_perm), _ptr(offsets), E, TK, d, f, _ptr(W1), _ptr(W2), _ptr(h), _ptr(y_perm),
+                               _stream(stream)), "moe_grouped_mlp")
+    return h, y_perm
+
+
+# ------------------------------------------------------------------ a6
+def unpermute(y_perm, row_of, topk_w, out=None, stream=None):
+    """y[t] = bf16(sum_k topk_w[t,k] * y_perm[row_of[t,k]]), fp32 accumulate."""
+    T, K = row_of.shape
+    d = y_perm.shape[1]
+    _need(y_perm, torch.bfloat16, (T * K, d), "y_perm")
+    _need(row_of, torch.int32, (T, K), "row_of")
+    _need(topk_w, torch.float32, (T, K), "topk_w")
+    out = _empty((T, d), torch.bfloat16, y_perm) if out is None else _need(out, torch.bfloat16, (T, d), "y")
+    _check(lib.moe_unpermute(_ptr(y_perm), _ptr(row_of), _ptr(topk_w), T, K, d, _ptr(out), _stream(stream)),
+           "moe_unpermute")
+    return out
+
+
+# ------------------------------------------------------------------ whole layer
+def forward_workspace_size(T, d, E, K, f) -> int:
+    return int(lib.moe_forward_workspace_size(T, d, E, K, f))
+
+
+def forward_views(T, d, E, K, f) -> dict:
+    lay = _Layout()
+    _check(lib.moe_forward_views(T, d, E, K, f, ctypes.byref(lay)), "moe_forward_views")
+    return {n: getattr(lay, n) for n, _ in _Layout._fields_}
+
+
+def _weights_check(x, Wr, bias, W1, W2, K):
+    T, d = x.shape
+    E = Wr.shape[1]
+    f = W1.shape[1] // 2
+    _need(Wr, torch.float32, (d, E), "Wr")
+    if bias is not None:
+        _need(bias, torch.float32, (E,), "bias")
+    _need(W1, torch.bfloat16, (E, 2 * f, d), "W1")
+    _need(W2, torch.bfloat16, (E, d, f), "W2")
+    return T, d, E, f
+
+
+def forward(x, Wr, bias, W1, W2, K: int, out=None, workspace=None, stream=None):
+    """The whole layer in one C-ABI call (8 kernel launches, no host sync)."""
+    T, d, E, f = _weights_check(x, Wr, bias, W1, W2, K)
+    _need(x, torch.bfloat16, (T, d), "x")
+    nbytes = forward_workspace_size(T, d, E, K, f)
+    if nbytes == 0:
+        raise MoEError(2, "moe_forward_workspace_size")
+    if workspace is None:
+        workspace = _empty((nbytes,), torch.uint8, x)
+    out = _empty((T, d), torch.bfloat16, x) if out is None else _need(out, torch.bfloat16, (T, d), "y")
+    _check(lib.moe_forward(_ptr(x), _ptr(Wr), _ptr(bias), _ptr(W1), _ptr(W2), T, d, E, K, f, _ptr(out),
+                           _ptr(workspace), workspace.numel(), _stream(stream)), "moe_forward")
+    return out
+
+
+def forward_host(x_host, Wr, bias, W1, W2, K: int, y_host=None, workspace=None, stream=None):
+    """The layer with activations in host memory (pinned for async copies):
+    x_host [T,d] bf16 (CPU) -> y_host [T,d] bf16 (CPU).  Copies happen on the
+    stream inside the C call; synchronize the stream before reading y_host."""
+    if x_host.is_cuda or x_host.dtype != torch.bfloat16 or not x_host.is_contiguous():
+        raise ValueError("x_host must be a contiguous CPU bf16 tensor")
+    T, d = x_host.shape
+    _, _, E, f = _weights_check(x_host, Wr, bias, W1, W2, K)
+    nbytes = forward_workspace_size(T, d, E, K, f)
+    if workspace is None:
+        workspace = torch.empty((nbytes,), dtype=torch.uint8, device=W1.device)
+    if y_host is None:
+        y_host = torch.empty((T, d), dtype=torch.bfloat16, pin_memory=x_host.is_pinned())
+    _check(lib.moe_forward_host(_ptr(x_host), _ptr(Wr), _ptr(bias), _ptr(W1), _ptr(W2), T, d, E, K, f,
+                                _ptr(y_host), _ptr(workspace), workspace.numel(), _stream(stream)),
+           "moe_forward_host")
+    return y_host
+
+
+def device_status() -> int:
+    v = ctypes.c_int(0)
+    _check(lib.moe_device_status(ctypes.byref(v)), "moe_device_status")
+    return v.value
+
+
+def launch_count() -> int:
+    return int(lib.moe_launch_count())
+
+
+class MoELayer:
+    """Holds one layer's weights and a persistent workspace; ``__call__(x)``
+    runs the forward with one C call.  Intermediates can be read back with
+    ``views()`` after a call (they live in the workspace)."""
+
+    def __init__(self, Wr, bias, W1, W2, K: int, T_max: int):
+        self.Wr, self.bias, self.W1, self.W2, self.K = Wr, bias, W1, W2, K
+        self.d = W1.shape[2]
+        self.E = Wr.shape[1]
+        self.f = W1.shape[1] // 2
+        self.T_max = T_max
+        n = forward_workspace_size(T_max, self.d, self.E, K, self.f)
+        if n == 0:
+            raise MoEError(2, "moe_forward_workspace_size")
+        self.workspace = torch.empty((n,), dtype=torch.uint8, device=W1.device)
+
+    def __call__(self, x, out=None, stream=None):
+        if x.shape[0] > self.T_max:
+            raise ValueError("more tokens than the workspace was sized for")
+        return forward(x, self.Wr, self.bias, self.W1, self.W2, self.K, out=out, workspace=self.workspace,
+                       stream=stream)
+
+    def views(self, T: int) -> dict:
+        """Typed tensor views of the intermediates of the last call with T tokens."""
+        lay = forward_views(T, self.d, self.E, self.K, self.f)
+        ws = self.workspace
+        K, E, d, f = self.K, self.E, self.d, self.f
+        TK = T * K
+
+        def v(name, n, dtype, shape):
+            return ws[lay[name]:lay[name] + n * torch.tensor([], dtype=dtype).element_size()].view(dtype).view(shape)
+
+        return dict(
+            logits=v("logits", T * E, torch.float32, (T, E)),
+            topk_idx=v("topk_idx", TK, torch.int32, (T, K)),
+            topk_w=v("topk_w", TK, torch.float32, (T, K)),
+            counts=v("counts", E, torch.int32, (E,)),
+            offsets=v("offsets", E + 1, torch.int32, (E + 1,)),
+            row_of=v("row_of", TK, torch.int32, (T, K)),
+            src_tok=v("src_tok", TK, torch.int32, (TK,)),
+            x_perm=v("x_perm", TK * d, torch.bfloat16, (TK, d)),
+            h=v("h", TK * f, torch.bfloat16, (TK, f)),
+            y_perm=v("y_perm", TK * d, torch.bfloat16, (TK, d)),
+        )

@@ -1,0 +1,40 @@
+// Internal launchers of the sm_103a kernels (not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime_api.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace moe {
+
+// Tokens per routing chunk: the unit of the per-chunk histograms that make the
+// dispatch order deterministic.
+constexpr int kRouteChunk = 256;
+
+inline int route_num_chunks(int T) { return (T + kRouteChunk - 1) / kRouteChunk; }
+// chunk_counts [C, E] and chunk_base [C, E], int32
+inline size_t route_workspace_bytes(int T, int E) {
+    return static_cast<size_t>(route_num_chunks(T)) * static_cast<size_t>(E) * 2 * sizeof(int32_t);
+}
+
+cudaError_t launch_router_logits(const uint16_t *x, const float *Wr, const float *bias, int T, int d, int E,
+                                 float *logits, cudaStream_t stream);
+
+cudaError_t launch_route(const float *logits, int T, int E, int K, int32_t *topk_idx, float *topk_w,
+                         int32_t *counts, int32_t *offsets, int32_t *row_of, int32_t *src_tok, int32_t *workspace,
+                         cudaStream_t stream);
+
+cudaError_t launch_permute(const uint16_t *x, const int32_t *row_of, int T, int K, int d, uint16_t *x_perm,
+                           cudaStream_t stream);
+
+cudaError_t launch_unpermute(const uint16_t *y_perm, const int32_t *row_of, const float *topk_w, int T, int K,
+                             int d, uint16_t *y, cudaStream_t stream);
+
+int grouped_gemm_smem_bytes();
+cudaError_t grouped_gemm_set_attributes();
+// swiglu: GEMM1 (out [TK, n_out=f], W [E, 2f, Kdim=d]); else GEMM2 (out [TK, n_out=d], W [E, d, Kdim=f]).
+cudaError_t launch_grouped_gemm(bool swiglu, const void *A, int TK, int Kdim, const void *W, int E, int n_out,
+                                const int32_t *offsets, void *out, int num_sms, int *status, uint64_t timeout_ns,
+                                cudaStream_t stream);
+
+}  // namespace moe

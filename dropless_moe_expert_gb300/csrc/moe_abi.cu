@@ -1,0 +1,290 @@
+// C ABI of the dropless MoE layer forward (declared in include/moe.h).
+//
+// Host-side argument checks run before anything touches CUDA, so a bad call
+// returns an error and launches nothing.  The library allocates nothing: every
+// buffer, scratch included, is the caller's.
+#include "../../include/moe.h"
+#include "kernels.h"
+
+#include <atomic>
+#include <mutex>
+
+namespace {
+
+constexpr int kMaxE = 256;
+constexpr int kMaxK = 16;
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // bounded device waits: 1 s
+
+std::atomic<uint64_t> g_launches{0};
+
+__device__ int g_device_status = 0;
+
+struct DeviceState {
+    bool ready = false;
+    int num_sms = 0;
+    int *status = nullptr;
+};
+constexpr int kMaxDevices = 64;
+DeviceState g_dev[kMaxDevices];
+std::mutex g_mu;
+
+// Per-device one-time set-up: SM count, kernel attributes, status word address.
+moe_status_t device_state(DeviceState **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState &s = g_dev[dev];
+    if (!s.ready) {
+        if (cudaDeviceGetAttribute(&s.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MOE_ERR_CUDA;
+        int major = 0, minor = 0;
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        if (major != 10) return MOE_ERR_UNSUPPORTED;  // built for sm_103a only
+        if (moe::grouped_gemm_set_attributes() != cudaSuccess) return MOE_ERR_CUDA;
+        if (cudaGetSymbolAddress(reinterpret_cast<void **>(&s.status), g_device_status) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        s.ready = true;
+    }
+    *out = &s;
+    return MOE_OK;
+}
+
+inline bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+moe_status_t check_shape(int T, int d, int E, int K, int f, bool need_d, bool need_f) {
+    if (T < 1 || E < 1 || K < 1 || K > E) return MOE_ERR_INVALID_ARG;
+    if (E > kMaxE || K > kMaxK) return MOE_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(T) * K >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
+    if (need_d && (d < 64 || d % 64 != 0)) return d < 1 ? MOE_ERR_INVALID_ARG : MOE_ERR_UNSUPPORTED;
+    if (need_f && (f < 64 || f % 64 != 0)) return f < 1 ? MOE_ERR_INVALID_ARG : MOE_ERR_UNSUPPORTED;
+    if (need_d && need_f && static_cast<int64_t>(E) * 2 * f >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
+    if (need_d && need_f && static_cast<int64_t>(E) * d >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+inline moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+bool forward_layout(int T, int d, int E, int K, int f, moe_forward_layout_t *L) {
+    const size_t TK = static_cast<size_t>(T) * K;
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = o;
+        o = align_up(o + bytes, 256);
+        return at;
+    };
+    L->logits = take(static_cast<size_t>(T) * E * 4);
+    L->topk_idx = take(TK * 4);
+    L->topk_w = take(TK * 4);
+    L->counts = take(static_cast<size_t>(E) * 4);
+    L->offsets = take(static_cast<size_t>(E + 1) * 4);
+    L->row_of = take(TK * 4);
+    L->src_tok = take(TK * 4);
+    L->route_ws = take(moe::route_workspace_bytes(T, E));
+    L->x_perm = take(TK * d * 2);
+    L->h = take(TK * f * 2);
+    L->y_perm = take(TK * d * 2);
+    L->x_dev = take(static_cast<size_t>(T) * d * 2);
+    L->y_dev = take(static_cast<size_t>(T) * d * 2);
+    L->total = o;
+    return true;
+}
+
+moe_status_t run_gemm(bool swiglu, const void *A, const int32_t *offsets, int E, int TK, int d, int f,
+                      const void *W, void *out, cudaStream_t stream) {
+    DeviceState *ds = nullptr;
+    moe_status_t st = device_state(&ds);
+    if (st != MOE_OK) return st;
+    const int Kdim = swiglu ? d : f;
+    const int n_out = swiglu ? f : d;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return cuda_status(moe::launch_grouped_gemm(swiglu, A, TK, Kdim, W, E, n_out, offsets, out, ds->num_sms,
+                                                ds->status, kWaitLimitNs, stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *moe_status_string(int status) {
+    switch (status) {
+        case MOE_OK: return "MOE_OK";
+        case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG: null or misaligned pointer, or size out of range";
+        case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED: sizes outside what the kernels cover";
+        case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE: workspace smaller than required";
+        case MOE_ERR_CUDA: return "MOE_ERR_CUDA: a CUDA call or kernel launch failed";
+        case MOE_ERR_DEVICE_TIMEOUT: return "MOE_ERR_DEVICE_TIMEOUT: a bounded device-side wait expired";
+        default: return "unknown moe_status_t";
+    }
+}
+
+int moe_abi_version(void) { return 100; }
+
+uint64_t moe_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+moe_status_t moe_router_logits(const uint16_t *x, const float *Wr, const float *bias, int T, int d, int E,
+                               float *logits, cudaStream_t stream) {
+    if (!x || !Wr || !logits) return MOE_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(Wr, 4) || !aligned(logits, 4) || (bias && !aligned(bias, 4)))
+        return MOE_ERR_INVALID_ARG;
+    moe_status_t st = check_shape(T, d, E, 1, 64, true, false);
+    if (st != MOE_OK) return st;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return cuda_status(moe::launch_router_logits(x, Wr, bias, T, d, E, logits, stream));
+}
+
+size_t moe_route_workspace_size(int T, int E, int K) {
+    if (T < 1 || E < 1 || K < 1) return 0;
+    return moe::route_workspace_bytes(T, E);
+}
+
+moe_status_t moe_route(const float *logits, int T, int E, int K, int32_t *topk_idx, float *topk_w,
+                       int32_t *counts, int32_t *offsets, int32_t *row_of, int32_t *src_tok, void *workspace,
+                       size_t workspace_bytes, cudaStream_t stream) {
+    if (!logits || !topk_idx || !topk_w || !counts || !offsets || !row_of || !src_tok || !workspace)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned(logits, 4) || !aligned(topk_idx, 4) || !aligned(topk_w, 4) || !aligned(counts, 4) ||
+        !aligned(offsets, 4) || !aligned(row_of, 4) || !aligned(src_tok, 4) || !aligned(workspace, 4))
+        return MOE_ERR_INVALID_ARG;
+    moe_status_t st = check_shape(T, 64, E, K, 64, false, false);
+    if (st != MOE_OK) return st;
+    if (workspace_bytes < moe::route_workspace_bytes(T, E)) return MOE_ERR_WORKSPACE;
+    g_launches.fetch_add(3, std::memory_order_relaxed);
+    return cuda_status(moe::launch_route(logits, T, E, K, topk_idx, topk_w, counts, offsets, row_of, src_tok,
+                                         static_cast<int32_t *>(workspace), stream));
+}
+
+moe_status_t moe_permute(const uint16_t *x, const int32_t *row_of, int T, int K, int d, uint16_t *x_perm,
+                         cudaStream_t stream) {
+    if (!x || !row_of || !x_perm) return MOE_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(x_perm, 16) || !aligned(row_of, 4)) return MOE_ERR_INVALID_ARG;
+    moe_status_t st = check_shape(T, d, K, K, 64, true, false);
+    if (st != MOE_OK) return st;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return cuda_status(moe::launch_permute(x, row_of, T, K, d, x_perm, stream));
+}
+
+moe_status_t moe_grouped_gemm1_swiglu(const uint16_t *x_perm, const int32_t *offsets, int E, int TK, int d, int f,
+                                      const uint16_t *W1, uint16_t *h, cudaStream_t stream) {
+    if (!x_perm || !offsets || !W1 || !h) return MOE_ERR_INVALID_ARG;
+    if (!aligned(x_perm, 16) || !aligned(W1, 16) || !aligned(h, 16) || !aligned(offsets, 4))
+        return MOE_ERR_INVALID_ARG;
+    moe_status_t st = check_shape(TK, d, E, 1, f, true, true);
+    if (st != MOE_OK) return st;
+    return run_gemm(true, x_perm, offsets, E, TK, d, f, W1, h, stream);
+}
+
+moe_status_t moe_grouped_gemm2(const uint16_t *h, const int32_t *offsets, int E, int TK, int d, int f,
+                               const uint16_t *W2, uint16_t *y_perm, cudaStream_t stream) {
+    if (!h || !offsets || !W2 || !y_perm) return MOE_ERR_INVALID_ARG;
+    if (!aligned(h, 16) || !aligned(W2, 16) || !aligned(y_perm, 16) || !aligned(offsets, 4))
+        return MOE_ERR_INVALID_ARG;
+    moe_status_t st = check_shape(TK, d, E, 1, f, true, true);
+    if (st != MOE_OK) return st;
+    return run_gemm(false, h, offsets, E, TK, d, f, W2, y_perm, stream);
+}
+
+moe_status_t moe_grouped_mlp(const uint16_t *x_perm, const int32_t *offsets, int E, int TK, int d, int f,
+                             const uint16_t *W1, const uint16_t *W2, uint16_t *h, uint16_t *y_perm,
+                             cudaStream_t stream) {
+    if (!W2 || !y_perm || !aligned(W2, 16) || !aligned(y_perm, 16)) return MOE_ERR_INVALID_ARG;
+    moe_status_t st = moe_grouped_gemm1_swiglu(x_perm, offsets, E, TK, d, f, W1, h, stream);
+    if (st != MOE_OK) return st;
+    return moe_grouped_gemm2(h, offsets, E, TK, d, f, W2, y_perm, stream);
+}
+
+moe_status_t moe_unpermute(const uint16_t *y_perm, const int32_t *row_of, const float *topk_w, int T, int K, int d,
+                           uint16_t *y, cudaStream_t stream) {
+    if (!y_perm || !row_of || !topk_w || !y) return MOE_ERR_INVALID_ARG;
+    if (!aligned(y_perm, 16) || !aligned(y, 16) || !aligned(row_of, 4) || !aligned(topk_w, 4))
+        return MOE_ERR_INVALID_ARG;
+    moe_status_t st = check_shape(T, d, K, K, 64, true, false);
+    if (st != MOE_OK) return st;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return cuda_status(moe::launch_unpermute(y_perm, row_of, topk_w, T, K, d, y, stream));
+}
+
+size_t moe_forward_workspace_size(int T, int d, int E, int K, int f) {
+    if (check_shape(T, d, E, K, f, true, true) != MOE_OK) return 0;
+    moe_forward_layout_t L;
+    forward_layout(T, d, E, K, f, &L);
+    return L.total;
+}
+
+moe_status_t moe_forward_views(int T, int d, int E, int K, int f, moe_forward_layout_t *layout) {
+    if (!layout) return MOE_ERR_INVALID_ARG;
+    moe_status_t st = check_shape(T, d, E, K, f, true, true);
+    if (st != MOE_OK) return st;
+    forward_layout(T, d, E, K, f, layout);
+    return MOE_OK;
+}
+
+moe_status_t moe_forward(const uint16_t *x, const float *Wr, const float *bias, const uint16_t *W1,
+                         const uint16_t *W2, int T, int d, int E, int K, int f, uint16_t *y, void *workspace,
+                         size_t workspace_bytes, cudaStream_t stream) {
+    if (!x || !Wr || !W1 || !W2 || !y || !workspace) return MOE_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(W1, 16) || !aligned(W2, 16) || !aligned(y, 16) || !aligned(workspace, 16) ||
+        !aligned(Wr, 4) || (bias && !aligned(bias, 4)))
+        return MOE_ERR_INVALID_ARG;
+    moe_status_t st = check_shape(T, d, E, K, f, true, true);
+    if (st != MOE_OK) return st;
+    moe_forward_layout_t L;
+    forward_layout(T, d, E, K, f, &L);
+    if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    auto at = [&](size_t off) { return static_cast<void *>(ws + off); };
+    const int TK = T * K;
+    float *logits = static_cast<float *>(at(L.logits));
+    int32_t *idx = static_cast<int32_t *>(at(L.topk_idx));
+    float *w = static_cast<float *>(at(L.topk_w));
+    int32_t *counts = static_cast<int32_t *>(at(L.counts));
+    int32_t *offsets = static_cast<int32_t *>(at(L.offsets));
+    int32_t *row_of = static_cast<int32_t *>(at(L.row_of));
+    int32_t *src_tok = static_cast<int32_t *>(at(L.src_tok));
+    uint16_t *x_perm = static_cast<uint16_t *>(at(L.x_perm));
+    uint16_t *h = static_cast<uint16_t *>(at(L.h));
+    uint16_t *y_perm = static_cast<uint16_t *>(at(L.y_perm));
+    if ((st = moe_router_logits(x, Wr, bias, T, d, E, logits, stream)) != MOE_OK) return st;
+    if ((st = moe_route(logits, T, E, K, idx, w, counts, offsets, row_of, src_tok, at(L.route_ws),
+                        L.x_perm - L.route_ws, stream)) != MOE_OK)
+        return st;
+    if ((st = moe_permute(x, row_of, T, K, d, x_perm, stream)) != MOE_OK) return st;
+    if ((st = moe_grouped_mlp(x_perm, offsets, E, TK, d, f, W1, W2, h, y_perm, stream)) != MOE_OK) return st;
+    return moe_unpermute(y_perm, row_of, w, T, K, d, y, stream);
+}
+
+moe_status_t moe_forward_host(const uint16_t *x_host, const float *Wr, const float *bias, const uint16_t *W1,
+                              const uint16_t *W2, int T, int d, int E, int K, int f, uint16_t *y_host,
+                              void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    if (!x_host || !y_host || !workspace) return MOE_ERR_INVALID_ARG;
+    moe_status_t st = check_shape(T, d, E, K, f, true, true);
+    if (st != MOE_OK) return st;
+    moe_forward_layout_t L;
+    forward_layout(T, d, E, K, f, &L);
+    if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    uint16_t *x_dev = reinterpret_cast<uint16_t *>(ws + L.x_dev);
+    uint16_t *y_dev = reinterpret_cast<uint16_t *>(ws + L.y_dev);
+    const size_t bytes = static_cast<size_t>(T) * d * 2;
+    if (cudaMemcpyAsync(x_dev, x_host, bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess) return MOE_ERR_CUDA;
+    if ((st = moe_forward(x_dev, Wr, bias, W1, W2, T, d, E, K, f, y_dev, workspace, workspace_bytes, stream)) !=
+        MOE_OK)
+        return st;
+    return cuda_status(cudaMemcpyAsync(y_host, y_dev, bytes, cudaMemcpyDeviceToHost, stream));
+}
+
+moe_status_t moe_device_status(int *status_out) {
+    if (!status_out) return MOE_ERR_INVALID_ARG;
+    DeviceState *ds = nullptr;
+    moe_status_t st = device_state(&ds);
+    if (st != MOE_OK) return st;
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_device_status, sizeof(int)) != cudaSuccess) return MOE_ERR_CUDA;
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int)) != cudaSuccess) return MOE_ERR_CUDA;
+    *status_out = v;
+    return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,133 @@
+// Steps a3 and a6: permute (local dispatch) and weighted unpermute (local
+// combine).  Both are HBM-bound row moves with 16-byte vectors.
+//
+// Figure 3 caption of "Accelerating dropless MoE training in JAX with NVIDIA
+// Transformer Engine": dispatch moves each token to its experts, combine
+// reverses the exchange and restores the original token order; "Optimization
+// 2" notes that a naive dispatch/combine reads and writes the data many times.
+//
+// permute : x_perm[row_of[t,k], :] = x[t, :] -- each token row is read once
+//           and written K times (scatter form: T*d reads, T*K*d writes).
+// combine : y[t, :] = bf16( sum_k w[t,k] * y_perm[row_of[t,k], :] ), fp32
+//           fused multiply-add in ascending k.
+// One warp per token, lanes own 16-byte column vectors; a lane keeps UV
+// vectors in flight per load round.
+#include "kernels.h"
+
+#include <cuda_bf16.h>
+
+namespace moe {
+namespace pm {
+
+constexpr int THREADS = 256;
+constexpr int UV = 4;
+
+__global__ void __launch_bounds__(THREADS)
+permute_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ row_of, int T, int K, int nvec,
+               uint4 *__restrict__ x_perm) {
+    const int lane = threadIdx.x & 31;
+    const int gw = (blockIdx.x * THREADS + threadIdx.x) >> 5;
+    const int nw = (gridDim.x * THREADS) >> 5;
+    for (int t = gw; t < T; t += nw) {
+        const int my_row = lane < K ? row_of[static_cast<size_t>(t) * K + lane] : 0;
+        const uint4 *src = x + static_cast<size_t>(t) * nvec;
+        for (int v0 = 0; v0 < nvec; v0 += 32 * UV) {
+            uint4 buf[UV];
+#pragma unroll
+            for (int u = 0; u < UV; ++u) {
+                const int v = v0 + u * 32 + lane;
+                if (v < nvec) buf[u] = __ldg(src + v);
+            }
+            for (int k = 0; k < K; ++k) {
+                const int r = __shfl_sync(0xffffffffu, my_row, k);
+                uint4 *dst = x_perm + static_cast<size_t>(r) * nvec;
+#pragma unroll
+                for (int u = 0; u < UV; ++u) {
+                    const int v = v0 + u * 32 + lane;
+                    if (v < nvec) dst[v] = buf[u];
+                }
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void fma_bf16x8(float (&acc)[8], float w, const uint4 &v) {
+    const uint32_t p[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        acc[2 * i] = __fmaf_rn(w, __uint_as_float(p[i] << 16), acc[2 * i]);
+        acc[2 * i + 1] = __fmaf_rn(w, __uint_as_float(p[i] & 0xffff0000u), acc[2 * i + 1]);
+    }
+}
+
+__device__ __forceinline__ uint4 to_bf16x8(const float (&acc)[8]) {
+    uint32_t p[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+        p[i] = *reinterpret_cast<const uint32_t *>(&b);
+    }
+    return make_uint4(p[0], p[1], p[2], p[3]);
+}
+
+__global__ void __launch_bounds__(THREADS)
+unpermute_kernel(const uint4 *__restrict__ y_perm, const int32_t *__restrict__ row_of,
+                 const float *__restrict__ topk_w, int T, int K, int nvec, uint4 *__restrict__ y) {
+    const int lane = threadIdx.x & 31;
+    const int gw = (blockIdx.x * THREADS + threadIdx.x) >> 5;
+    const int nw = (gridDim.x * THREADS) >> 5;
+    for (int t = gw; t < T; t += nw) {
+        const int my_row = lane < K ? row_of[static_cast<size_t>(t) * K + lane] : 0;
+        const float my_w = lane < K ? topk_w[static_cast<size_t>(t) * K + lane] : 0.0f;
+        for (int v0 = 0; v0 < nvec; v0 += 32 * UV) {
+            float acc[UV][8];
+#pragma unroll
+            for (int u = 0; u < UV; ++u)
+#pragma unroll
+                for (int i = 0; i < 8; ++i) acc[u][i] = 0.0f;
+            for (int k = 0; k < K; ++k) {
+                const int r = __shfl_sync(0xffffffffu, my_row, k);
+                const float w = __shfl_sync(0xffffffffu, my_w, k);
+                const uint4 *src = y_perm + static_cast<size_t>(r) * nvec;
+                uint4 buf[UV];
+#pragma unroll
+                for (int u = 0; u < UV; ++u) {
+                    const int v = v0 + u * 32 + lane;
+                    buf[u] = v < nvec ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
+                }
+#pragma unroll
+                for (int u = 0; u < UV; ++u) fma_bf16x8(acc[u], w, buf[u]);
+            }
+            uint4 *dst = y + static_cast<size_t>(t) * nvec;
+#pragma unroll
+            for (int u = 0; u < UV; ++u) {
+                const int v = v0 + u * 32 + lane;
+                if (v < nvec) dst[v] = to_bf16x8(acc[u]);
+            }
+        }
+    }
+}
+
+int grid_for(int T) {
+    const int warps_per_block = THREADS / 32;
+    const int blocks = (T + warps_per_block - 1) / warps_per_block;
+    return blocks < 1 ? 1 : blocks;
+}
+
+}  // namespace pm
+
+cudaError_t launch_permute(const uint16_t *x, const int32_t *row_of, int T, int K, int d, uint16_t *x_perm,
+                           cudaStream_t stream) {
+    pm::permute_kernel<<<pm::grid_for(T), pm::THREADS, 0, stream>>>(
+        reinterpret_cast<const uint4 *>(x), row_of, T, K, d / 8, reinterpret_cast<uint4 *>(x_perm));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_unpermute(const uint16_t *y_perm, const int32_t *row_of, const float *topk_w, int T, int K,
+                             int d, uint16_t *y, cudaStream_t stream) {
+    pm::unpermute_kernel<<<pm::grid_for(T), pm::THREADS, 0, stream>>>(
+        reinterpret_cast<const uint4 *>(y_perm), row_of, topk_w, T, K, d / 8, reinterpret_cast<uint4 *>(y));
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,168 @@
+/*
+ * moe.h -- C ABI of a dropless Mixture-of-Experts SwiGLU FFN layer forward on
+ * one NVIDIA GB300 (sm_103a).
+ *
+ * The operation follows "Accelerating dropless MoE training in JAX with NVIDIA
+ * Transformer Engine" (aihot.vn/items/70e24b30eb05130d):
+ *   - introduction: a learned router activates the Top-K experts per token;
+ *   - "How is dropless MoE different from capacity-based MoE?": every token is
+ *     processed by its chosen experts whatever the load (no drop, no padding);
+ *   - "What specialized optimizations are needed for dropless MoE?": per-expert
+ *     token counts are data dependent and must stay invisible to the CPU, so
+ *     that CUDA graphs work without recompiling;
+ *   - Figure 3 caption: dispatch moves tokens to their experts, the grouped MLP
+ *     runs two grouped GEMMs over the variable-length groups, combine restores
+ *     the original token order;
+ *   - "Optimization 1: Grouped GEMM": all expert matmuls in one kernel call,
+ *     each with its actual token count, computing only valid-token rows; a
+ *     device-to-host copy of the counts would break CUDA graphs.
+ *
+ * Notation: T tokens, d model dim, E experts, K experts per token, f expert
+ * FFN dim, TK = T*K.  Layouts are row-major and dense:
+ *   x      [T, d]      bf16        token activations
+ *   Wr     [d, E]      fp32        router weights;  bias [E] fp32 (nullable)
+ *   logits [T, E]      fp32
+ *   W1     [E, 2f, d]  bf16        rows 0..f-1 gate, rows f..2f-1 up (out x in)
+ *   W2     [E, d, f]   bf16        (out x in)
+ *   topk_idx [T, K] int32, topk_w [T, K] fp32   (descending logit; equal
+ *                                   logits -> lower expert index)
+ *   counts [E], offsets [E+1] int32 (offsets[E] = TK)
+ *   row_of [T, K] int32: row of x_perm holding token t's k-th choice
+ *   src_tok [TK] int32: token held by each row of x_perm
+ *   x_perm, y_perm [TK, d] bf16, h [TK, f] bf16: rows grouped by expert,
+ *                                   ascending token index inside a group
+ *   y      [T, d]      bf16        layer output
+ * bf16 buffers are passed as uint16_t* (bit patterns).
+ *
+ * Conventions for every entry point:
+ *   - All pointers except those of *_host calls are device pointers owned by
+ *     the caller.  The library allocates no memory and performs no
+ *     host<->device copy, except moe_forward_host (stated there).
+ *   - Calls are asynchronous on `stream` and never synchronize; no value flows
+ *     from device to host, so a sequence of calls can be captured in a CUDA
+ *     graph and replayed for any routing.  (The first call on a device also
+ *     sets kernel attributes; make it once before capturing.)
+ *   - Arguments are checked on the host before anything is launched; a bad
+ *     argument returns an error and launches nothing.  Sizes: T >= 1,
+ *     1 <= K <= E <= 256, K <= 16, d and f multiples of 64, T*K < 2^31.
+ *     bf16 matrices must be 16-byte aligned; fp32/int32 arrays 4-byte aligned.
+ *   - Device-side waits are bounded (about one second).  A kernel whose wait
+ *     expires records MOE_ERR_DEVICE_TIMEOUT in a device status word, drains
+ *     its own copies, frees its tensor memory and returns; read the word with
+ *     moe_device_status().
+ *   - Inputs are assumed finite; NaN or Inf logits are outside the contract.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,    /* null/misaligned pointer, size out of range    */
+    MOE_ERR_UNSUPPORTED = 2,    /* sizes the kernels do not cover (E>256, ...)   */
+    MOE_ERR_WORKSPACE = 3,      /* workspace smaller than *_workspace_size()     */
+    MOE_ERR_CUDA = 4,           /* a CUDA runtime/driver call or launch failed   */
+    MOE_ERR_DEVICE_TIMEOUT = 5  /* a bounded device-side wait expired            */
+} moe_status_t;
+
+/* Static, human-readable name of a status code. */
+const char *moe_status_string(int status);
+
+/* ABI version: 100 * major + minor. */
+int moe_abi_version(void);
+
+/* Step a0 -- router logits (introduction: the learned router).
+ * logits[t,e] = fp32 dot product of x[t,:] and Wr[:,e], accumulated in index
+ * order with one fused multiply-add per term, then + bias[e] (if bias is not
+ * NULL).  That order makes the logits bit-reproducible.  */
+moe_status_t moe_router_logits(const uint16_t *x, const float *Wr, const float *bias,
+                               int T, int d, int E, float *logits, cudaStream_t stream);
+
+/* Steps a1 + a2 -- top-K softmax routing, expert histogram, offsets and the
+ * stable dispatch order (introduction: Top-K experts; "What specialized
+ * optimizations are needed for dropless MoE?": counts stay on the device).
+ *   topk_idx[t,:]: the K largest logits of token t, descending, equal logits
+ *                  in ascending expert order (-0.0 equals +0.0);
+ *   topk_w[t,k]  : exp(l_k - l_0) / sum_j exp(l_j - l_0) over the K selected;
+ *   counts, offsets (exclusive scan, E+1 entries), row_of, src_tok as above.
+ * Every output is bit-deterministic.  `workspace` must hold
+ * moe_route_workspace_size(T, E, K) bytes (4-byte aligned).  */
+size_t moe_route_workspace_size(int T, int E, int K);
+moe_status_t moe_route(const float *logits, int T, int E, int K,
+                       int32_t *topk_idx, float *topk_w, int32_t *counts, int32_t *offsets,
+                       int32_t *row_of, int32_t *src_tok,
+                       void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Step a3 -- permute (local part of dispatch, Figure 3 caption):
+ * x_perm[row_of[t,k], :] = x[t, :] for every (t, k).  */
+moe_status_t moe_permute(const uint16_t *x, const int32_t *row_of, int T, int K, int d,
+                         uint16_t *x_perm, cudaStream_t stream);
+
+/* Steps a4 + a5 -- the grouped MLP ("Optimization 1: Grouped GEMM"; Figure 3
+ * caption: two grouped GEMMs over the variable-length groups).  For each
+ * expert e and each row r in offsets[e]..offsets[e+1]-1:
+ *   g = x_perm[r] . W1[e, 0:f]^T,  u = x_perm[r] . W1[e, f:2f]^T  (fp32 accumulate)
+ *   h[r] = bf16(silu(g) * u)                                    (GEMM1 epilogue)
+ *   y_perm[r] = bf16(h[r] . W2[e]^T)                            (fp32 accumulate)
+ * The kernels read `offsets` on the device; empty experts cost nothing and
+ * their weights are not read.  `h` is caller-owned scratch [TK, f].  */
+moe_status_t moe_grouped_mlp(const uint16_t *x_perm, const int32_t *offsets, int E, int TK,
+                             int d, int f, const uint16_t *W1, const uint16_t *W2,
+                             uint16_t *h, uint16_t *y_perm, cudaStream_t stream);
+/* The two halves of moe_grouped_mlp, one kernel launch each. */
+moe_status_t moe_grouped_gemm1_swiglu(const uint16_t *x_perm, const int32_t *offsets, int E,
+                                      int TK, int d, int f, const uint16_t *W1, uint16_t *h,
+                                      cudaStream_t stream);
+moe_status_t moe_grouped_gemm2(const uint16_t *h, const int32_t *offsets, int E, int TK,
+                               int d, int f, const uint16_t *W2, uint16_t *y_perm,
+                               cudaStream_t stream);
+
+/* Step a6 -- unpermute + combine (Figure 3 caption: restore token order):
+ * y[t,:] = bf16( sum_{k=0..K-1} topk_w[t,k] * y_perm[row_of[t,k], :] ),
+ * fp32 accumulation in ascending k.  */
+moe_status_t moe_unpermute(const uint16_t *y_perm, const int32_t *row_of, const float *topk_w,
+                           int T, int K, int d, uint16_t *y, cudaStream_t stream);
+
+/* The whole layer, a0..a6 in order on `stream` (8 kernel launches).
+ * `workspace` (16-byte aligned, moe_forward_workspace_size() bytes) holds
+ * every intermediate; moe_forward_views() gives their byte offsets so that a
+ * caller can inspect them after the call.  */
+size_t moe_forward_workspace_size(int T, int d, int E, int K, int f);
+typedef struct {
+    size_t logits, topk_idx, topk_w, counts, offsets, row_of, src_tok, route_ws,
+           x_perm, h, y_perm, x_dev, y_dev, total;
+} moe_forward_layout_t;
+moe_status_t moe_forward_views(int T, int d, int E, int K, int f, moe_forward_layout_t *layout);
+moe_status_t moe_forward(const uint16_t *x, const float *Wr, const float *bias,
+                         const uint16_t *W1, const uint16_t *W2, int T, int d, int E, int K,
+                         int f, uint16_t *y, void *workspace, size_t workspace_bytes,
+                         cudaStream_t stream);
+
+/* moe_forward with the activations in HOST memory (pinned memory makes the
+ * copies asynchronous): copies x_host [T, d] bf16 into the workspace,
+ * runs the layer, copies y back to y_host [T, d] bf16, all on `stream`.
+ * The weights stay device pointers.  y_host is valid after the stream
+ * has been synchronized.  */
+moe_status_t moe_forward_host(const uint16_t *x_host, const float *Wr, const float *bias,
+                              const uint16_t *W1, const uint16_t *W2, int T, int d, int E,
+                              int K, int f, uint16_t *y_host, void *workspace,
+                              size_t workspace_bytes, cudaStream_t stream);
+
+/* Reads and clears the device status word of the current device (0 = OK, or
+ * a moe_status_t a kernel recorded).  Synchronous: call outside capture. */
+moe_status_t moe_device_status(int *status_out);
+
+/* Number of kernels this library has launched in this process. */
+uint64_t moe_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

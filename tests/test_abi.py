@@ -1,0 +1,116 @@
+"""The C ABI: the library loads, exports every symbol include/moe.h declares,
+and rejects bad arguments on the host before anything is launched (so these
+run without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe.h")
+
+
+@pytest.fixture(scope="module")
+def moe():
+    import __graft_entry__
+    __graft_entry__.build()
+    import dropless_moe_expert_gb300 as m
+    return m
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for n in ["moe_router_logits", "moe_route", "moe_permute", "moe_grouped_mlp", "moe_unpermute",
+              "moe_route_workspace_size", "moe_status_string", "moe_forward", "moe_device_status"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(moe):
+    lib = ctypes.CDLL(moe.build.lib_path())
+    missing = [n for n in _declared() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings(moe):
+    for code in range(6):
+        s = moe.lib.moe_status_string(code).decode()
+        assert s.startswith("MOE_")
+    assert moe.lib.moe_status_string(99).decode() == "unknown moe_status_t"
+    assert moe.lib.moe_abi_version() == 100
+
+
+def test_workspace_sizes(moe):
+    # two int32 [chunks, E] tables, 256 tokens per chunk
+    assert moe.route_workspace_size(256, 8, 2) == 1 * 8 * 2 * 4
+    assert moe.route_workspace_size(257, 8, 2) == 2 * 8 * 2 * 4
+    assert moe.route_workspace_size(32768, 64, 6) == 128 * 64 * 2 * 4
+    v = moe.forward_views(8192, 4096, 8, 2, 14336)
+    TK = 8192 * 2
+    assert v["h"] - v["x_perm"] >= TK * 4096 * 2 and v["y_perm"] - v["h"] >= TK * 14336 * 2
+    offs = [v[k] for k in ("logits", "topk_idx", "topk_w", "counts", "offsets", "row_of", "src_tok",
+                           "route_ws", "x_perm", "h", "y_perm", "x_dev", "y_dev", "total")]
+    assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
+    assert moe.forward_workspace_size(8192, 4096, 8, 2, 14336) == v["total"]
+    assert moe.forward_workspace_size(8, 100, 8, 2, 64) == 0      # d not a multiple of 64
+
+
+FAKE = 1 << 20  # a 16-byte aligned non-null address; never dereferenced (rejected first)
+
+
+@pytest.mark.parametrize("args,code", [
+    # T, d, E, K, f
+    ((0, 64, 8, 2, 64), 1),       # T < 1
+    ((8, 64, 8, 9, 64), 1),       # K > E
+    ((8, 64, 8, 0, 64), 1),       # K < 1
+    ((8, 64, 300, 2, 64), 2),     # E > 256
+    ((8, 64, 32, 17, 64), 2),     # K > 16
+    ((8, 96, 8, 2, 64), 2),       # d % 64
+    ((8, 64, 8, 2, 96), 2),       # f % 64
+])
+def test_forward_rejects_bad_shapes(moe, args, code):
+    T, d, E, K, f = args
+    r = moe.lib.moe_forward(FAKE, FAKE, None, FAKE, FAKE, T, d, E, K, f, FAKE, FAKE, 1 << 40, None)
+    assert r == code
+
+
+def test_null_and_misaligned_pointers_rejected(moe):
+    L = moe.lib
+    assert L.moe_forward(None, FAKE, None, FAKE, FAKE, 8, 64, 8, 2, 64, FAKE, FAKE, 1 << 40, None) == 1
+    assert L.moe_forward(FAKE + 2, FAKE, None, FAKE, FAKE, 8, 64, 8, 2, 64, FAKE, FAKE, 1 << 40, None) == 1
+    assert L.moe_router_logits(FAKE, FAKE, None, 8, 64, 8, None, None) == 1
+    assert L.moe_router_logits(FAKE + 8, FAKE, None, 8, 64, 8, FAKE, None) == 1
+    assert L.moe_permute(FAKE, FAKE, 8, 2, 64, FAKE + 4, None) == 1
+    assert L.moe_unpermute(FAKE, FAKE, None, 8, 2, 64, FAKE, None) == 1
+    assert L.moe_grouped_mlp(FAKE, FAKE, 8, 16, 64, 64, FAKE, None, FAKE, FAKE, None) == 1
+    assert L.moe_grouped_gemm1_swiglu(FAKE, FAKE, 8, 16, 64, 64, FAKE, FAKE + 1, None) == 1
+    assert L.moe_device_status(None) == 1
+    assert L.moe_forward_views(8, 64, 8, 2, 64, None) == 1
+
+
+def test_route_workspace_too_small(moe):
+    L = moe.lib
+    need = moe.route_workspace_size(1000, 16, 4)
+    r = L.moe_route(FAKE, 1000, 16, 4, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, need - 4, None)
+    assert r == 3
+    r = L.moe_forward(FAKE, FAKE, None, FAKE, FAKE, 64, 64, 8, 2, 64, FAKE, FAKE, 1024, None)
+    assert r == 3
+
+
+def test_no_launch_happened(moe):
+    # every call above was rejected on the host
+    assert moe.launch_count() == 0
+
+
+def test_package_refuses_cpu_tensors(moe):
+    import torch
+    x = torch.zeros(4, 64, dtype=torch.bfloat16)
+    Wr = torch.zeros(64, 8)
+    with pytest.raises(ValueError, match="CUDA"):
+        moe.router_logits(x, Wr)
