@@ -156,9 +156,8 @@ def _oracle_inputs(s, x, w):
     """Host copies of the layer (weights in fp64 when host memory allows, which
     the oracle then uses as they are)."""
     try:
-        import psutil
-        avail = psutil.virtual_memory().available
-    except Exception:
+        avail = os.sysconf("SC_AVPHYS_PAGES") * os.sysconf("SC_PAGE_SIZE")
+    except (ValueError, OSError, AttributeError):
         avail = 0
     f64_bytes = 8 * s.E * 3 * s.d * s.f
     wdtype = np.float64 if avail > 3 * f64_bytes else np.float32
@@ -178,10 +177,12 @@ def _oracle_rate(s, inputs, budget_s: float, nthreads: int):
     x_np, Wr_np, bias_np, W1_np, W2_np, _ = inputs
     n = min(16, s.T)
     t = _oracle_sample_run(s, x_np, Wr_np, bias_np, W1_np, W2_np, n, nthreads)
-    per_tok = t / n
-    n2 = int(max(n, min(s.T, budget_s / max(per_tok, 1e-9))))
-    t2 = _oracle_sample_run(s, x_np, Wr_np, bias_np, W1_np, W2_np, n2, nthreads)
-    return n2, t2
+    # grow the sample until one run takes about the budget (the oracle has a
+    # fixed cost per expert, so a single small run underestimates the rate)
+    while t < 0.5 * budget_s and n < s.T:
+        n = int(min(s.T, max(2 * n, n * 0.8 * budget_s / max(t, 1e-9))))
+        t = _oracle_sample_run(s, x_np, Wr_np, bias_np, W1_np, W2_np, n, nthreads)
+    return n, t
 
 
 def run_reference(args):
@@ -396,8 +397,8 @@ def run_gpu(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--config", default="mixtral")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
