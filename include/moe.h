@@ -100,6 +100,30 @@ moe_status_t moe_route(const float *logits, int T, int E, int K,
                        int32_t *row_of, int32_t *src_tok,
                        void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* moe_route without a workspace argument, for callers that cannot allocate
+ * device memory where they route: an inference-engine plugin whose enqueue
+ * step must not allocate, code running while a stream is captured in global
+ * capture mode (cudaMalloc is not permitted there), or a runtime that owns
+ * all device memory in a fixed pool.  The page has no counterpart: this is
+ * a packaging variant of moe_route, with identical outputs.
+ *   - Scratch lives in a library-owned static device array of
+ *     MOE_ROUTE_STATIC_MAX_SCRATCH_BYTES (256 KiB) on every GPU that loads
+ *     the library, held until the process exits.  Sizes whose scratch,
+ *     moe_route_workspace_size(T, E, K), exceeds it return
+ *     MOE_ERR_UNSUPPORTED with nothing launched (e.g. E = 256 allows up to
+ *     32768 tokens).
+ *   - The call allocates and frees nothing.  Its first call on a device looks
+ *     up the array's device address (cudaGetSymbolAddress) with that device
+ *     current; make that first call before any stream capture.
+ *   - Every call shares the one array and leaves its contents behind; nothing
+ *     in it needs to start at zero.  Calls whose kernels overlap on the GPU
+ *     (several streams, or several host threads) race on it: serialize them.
+ *   - Kernel launches of this call are not counted by moe_launch_count(). */
+#define MOE_ROUTE_STATIC_MAX_SCRATCH_BYTES (256u * 1024u)
+moe_status_t moe_route_static(const float *logits, int T, int E, int K,
+                              int32_t *topk_idx, float *topk_w, int32_t *counts, int32_t *offsets,
+                              int32_t *row_of, int32_t *src_tok, cudaStream_t stream);
+
 /* Step a3 -- permute (local part of dispatch, Figure 3 caption):
  * x_perm[row_of[t,k], :] = x[t, :] for every (t, k).  */
 moe_status_t moe_permute(const uint16_t *x, const int32_t *row_of, int T, int K, int d,
