@@ -10,27 +10,39 @@
 //   GEMM2 (SWIGLU = false): y_perm[r, n] = bf16( h[r].W2[e,n] )
 // for every row r of expert e's group offsets[e]..offsets[e+1]-1.
 //
-// Design:
-//  * One CTA per SM, persistent over a device-side tile list.  Every CTA reads
-//    offsets[] (E+1 ints) and builds the tile prefix itself, so the host never
-//    sees a count and the launch is the same for every routing.
-//  * Tile = 128 rows x 256 accumulator columns.  GEMM1 stacks the gate rows
-//    n0..n0+127 and the up rows f+n0..f+n0+127 of W1[e] into one 256-row B tile,
-//    so one MMA produces both halves of SwiGLU for 128 output columns; GEMM2
-//    uses 256 consecutive rows of W2[e].  A tile that runs past its group
-//    reads neighbouring rows (or TMA zero fill); the epilogue masks them.
+// Design (both variants):
+//  * Persistent over a device-side tile list.  Every CTA reads offsets[] (E+1
+//    ints) and builds the tile prefix itself, so the host never sees a count
+//    and the launch is the same for every routing.
+//  * Accumulator tile: rows x 256 columns.  GEMM1 stacks the gate rows
+//    n0..n0+127 and the up rows f+n0..f+n0+127 of W1[e] into one 256-column
+//    B operand, so one MMA yields both SwiGLU halves of 128 output columns;
+//    GEMM2 uses 256 consecutive rows of W2[e].  A tile that runs past its
+//    group reads neighbouring rows (or TMA zero fill); the epilogue masks them.
 //  * Warp roles: warp 0 = TMA producer, warp 1 = tcgen05.mma issuer (and TMEM
 //    owner), warps 2..5 = epilogue (TMEM -> registers -> global).
-//  * 4-stage smem ring (48 KB per stage: A 128x64, B 256x64 bf16, 128-byte
-//    swizzle) with full/empty mbarriers; two 256-column fp32 accumulators in
-//    TMEM (512 columns) so the epilogue of tile i overlaps the mainloop of
-//    tile i+1.
-//  * Tiles are ordered expert by expert; inside an expert, bands of 16 row
-//    blocks sweep all column blocks, so concurrent CTAs share the weight tile
+//  * Shared-memory ring of bf16 tiles (64-wide K slices, 128-byte swizzle)
+//    with full/empty mbarriers; two 256-column fp32 accumulators in TMEM (512
+//    columns) so the epilogue of tile i overlaps the mainloop of tile i+1.
+//  * Tiles are ordered expert by expert; inside an expert, bands of row
+//    blocks sweep all column blocks, so concurrent CTAs share each weight tile
 //    through L2 and the band's activation rows stay L2-resident.
 //  * Every wait is bounded: on expiry the kernel records a timeout, drains its
 //    copies and MMAs, frees TMEM and returns.
+//
+// Single-CTA variant (grouped_gemm_kernel): 128-row tiles, M=128 x N=256 MMAs,
+// 4 stages of 48 KB.  Used when groups are small (about one row block).
+//
+// CTA-pair variant (grouped_gemm_pair_kernel): clusters of 2 CTAs on 2 SMs
+// share a 256-row tile through cta_group::2 MMAs (M=256 x N=256).  Each CTA
+// loads its 128 A rows and half of the B columns (GEMM1: CTA 0 the gate rows,
+// CTA 1 the up rows), so each SM moves 32 KB per K slice instead of 48 KB and
+// the ring holds 6 stages.  The even CTA issues the MMAs; both CTAs' copies
+// signal its full barrier, its commits free both CTAs' stages, and both CTAs'
+// epilogues release its accumulator.
 #include <cudaTypedefs.h>
+
+#include <algorithm>
 
 #include "kernels.h"
 #include "ptx.cuh"
@@ -38,28 +50,49 @@
 namespace moe {
 namespace gg {
 
-constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int BN_ACC = 256;
+constexpr int UMMA_K = 16;
+constexpr int TMEM_COLS = 2 * BN_ACC;
+constexpr int THREADS = 192;
+constexpr int MAX_E = 256;
+constexpr int BOX_ROWS = 128;  // every TMA box is 128 rows x 64 bf16
+
+// single-CTA variant
+constexpr int BM = 128;
+constexpr int BAND = 16;       // row blocks per raster band
 constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN_ACC * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int UMMA_K = 16;
-constexpr int TMEM_COLS = 2 * BN_ACC;
-constexpr int BAND = 16;
-constexpr int THREADS = 192;
-constexpr int MAX_E = 256;
 
-constexpr int OFF_BARS = STAGES * STAGE_BYTES;
-constexpr int NUM_BARS = 2 * STAGES + 5;  // full, empty, tfull[2], tempty[2], drain
-constexpr int OFF_TMEM = OFF_BARS + NUM_BARS * 8;
-constexpr int OFF_ABORT = OFF_TMEM + 4;
-constexpr int OFF_OFFS = OFF_ABORT + 4;
-constexpr int OFF_ENDS = OFF_OFFS + MAX_E * 4;
-constexpr int OFF_PRE = OFF_ENDS + MAX_E * 4;
-constexpr int SMEM_USED = OFF_PRE + (MAX_E + 1) * 4;
-constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack for 1024-byte alignment
+// CTA-pair variant (per CTA)
+constexpr int P_BM = 256;      // rows of a pair tile (128 per CTA)
+constexpr int P_BAND = 8;
+constexpr int P_STAGES = 6;
+constexpr int P_A_BYTES = 128 * BK * 2;
+constexpr int P_B_BYTES = 128 * BK * 2;
+constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
+
+// shared-memory layout after the ring: barriers, TMEM address, abort flag,
+// group bounds and tile prefix
+template <int NSTAGES, int STAGE>
+struct Layout {
+    static constexpr int OFF_BARS = NSTAGES * STAGE;
+    static constexpr int NUM_BARS = 2 * NSTAGES + 5;  // full, empty, tfull[2], tempty[2], drain
+    static constexpr int OFF_TMEM = OFF_BARS + NUM_BARS * 8;
+    static constexpr int OFF_ABORT = OFF_TMEM + 4;
+    static constexpr int OFF_OFFS = OFF_ABORT + 4;
+    static constexpr int OFF_ENDS = OFF_OFFS + MAX_E * 4;
+    static constexpr int OFF_PRE = OFF_ENDS + MAX_E * 4;
+    static constexpr int USED = OFF_PRE + (MAX_E + 1) * 4;
+    static constexpr int BYTES = USED + 1024;  // slack for 1024-byte alignment
+};
+using L1 = Layout<STAGES, STAGE_BYTES>;
+using L2 = Layout<P_STAGES, P_STAGE_BYTES>;
+constexpr int SMEM_BYTES = L1::BYTES;
+constexpr int P_SMEM_BYTES = L2::BYTES;
+static_assert(SMEM_BYTES <= 227 * 1024 && P_SMEM_BYTES <= 227 * 1024, "shared memory budget");
 
 struct Params {
     const int32_t *offsets;  // [E+1] device
@@ -75,9 +108,37 @@ struct Params {
 };
 
 struct Tile {
-    int e, m_blk, n_blk, row0, rows, grp_end;
+    int e, m_blk, n_blk, row0, grp_end;
 };
 
+// Group bounds [s_off[e], s_end[e]), clamped to [0, TK] so that no content of
+// offsets[] can send a store out of bounds, and the per-expert tile prefix
+// s_pre (tiles of experts < e) for row blocks of RB rows.  One warp.
+template <int RB>
+__device__ __forceinline__ void build_groups(const Params &p, int lane, int *s_off, int *s_end, int *s_pre) {
+    int carry = 0;
+    for (int base = 0; base < p.E; base += 32) {
+        const int e = base + lane;
+        int v = 0;
+        if (e < p.E) {
+            const int o0 = min(max(p.offsets[e], 0), p.TK);
+            const int o1 = min(max(p.offsets[e + 1], o0), p.TK);
+            s_off[e] = o0;
+            s_end[e] = o1;
+            v = ((o1 - o0 + RB - 1) / RB) * p.NT;
+        }
+#pragma unroll
+        for (int s = 1; s < 32; s <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, v, s);
+            if (lane >= s) v += n;
+        }
+        if (e < p.E) s_pre[e + 1] = carry + v;
+        carry += __shfl_sync(0xffffffffu, v, 31);
+    }
+    if (lane == 0) s_pre[0] = 0;
+}
+
+template <int RB, int NBAND>
 __device__ __forceinline__ Tile decode_tile(int tile, const int *s_pre, const int *s_off, const int *s_end, int E,
                                             int NT) {
     int lo = 0, hi = E - 1;
@@ -89,16 +150,14 @@ __device__ __forceinline__ Tile decode_tile(int tile, const int *s_pre, const in
     t.e = lo;
     const int local = tile - s_pre[lo];
     const int g0 = s_off[lo], g1 = s_end[lo];
-    const int cnt = g1 - g0;
-    const int MT = (cnt + BM - 1) / BM;
-    const int band = local / (BAND * NT);
-    const int within = local - band * BAND * NT;
-    const int mb0 = band * BAND;
-    const int bm = min(BAND, MT - mb0);
+    const int MT = (g1 - g0 + RB - 1) / RB;
+    const int band = local / (NBAND * NT);
+    const int within = local - band * NBAND * NT;
+    const int mb0 = band * NBAND;
+    const int bm = min(NBAND, MT - mb0);
     t.n_blk = within / bm;
     t.m_blk = mb0 + (within - t.n_blk * bm);
-    t.row0 = g0 + t.m_blk * BM;
-    t.rows = min(BM, cnt - t.m_blk * BM);
+    t.row0 = g0 + t.m_blk * RB;
     t.grp_end = g1;
     return t;
 }
@@ -108,23 +167,83 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<const uint32_t *>(&v);
 }
 
+__device__ __forceinline__ void store_row32(__nv_bfloat16 *dst_row, const uint32_t (&packed)[16]) {
+    uint4 *dst = reinterpret_cast<uint4 *>(dst_row);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+}
+
+// Epilogue of one accumulator: this thread owns TMEM lane `row_local` of the
+// warp's quarter (tbase already points at it) and output row `grow`.
+template <bool SWIGLU>
+__device__ __forceinline__ void epilogue_tile(const Params &p, uint32_t tbase, int n_blk, int grow, bool row_ok) {
+    if (SWIGLU) {
+#pragma unroll 1
+        for (int c = 0; c < BN_ACC / 2; c += 32) {
+            uint32_t g[32], u[32];
+            tmem_ld_32x32b_x32(tbase + c, g);
+            tmem_ld_32x32b_x32(tbase + BN_ACC / 2 + c, u);
+            tmem_ld_wait();
+            const int col = n_blk * (BN_ACC / 2) + c;
+            if (row_ok && col < p.n_out) {
+                uint32_t packed[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    float h2[2];
+#pragma unroll
+                    for (int k = 0; k < 2; ++k) {
+                        const float gv = __uint_as_float(g[2 * i + k]);
+                        const float uv = __uint_as_float(u[2 * i + k]);
+                        h2[k] = gv * __frcp_rn(1.0f + __expf(-gv)) * uv;
+                    }
+                    packed[i] = pack_bf16x2(h2[0], h2[1]);
+                }
+                store_row32(p.out + static_cast<size_t>(grow) * p.n_out + col, packed);
+            }
+        }
+    } else {
+        // two 32-column loads per wait, so TMEM latency is paid 4 times per tile, not 8
+#pragma unroll 1
+        for (int c = 0; c < BN_ACC; c += 64) {
+            uint32_t v[2][32];
+            tmem_ld_32x32b_x32(tbase + c, v[0]);
+            tmem_ld_32x32b_x32(tbase + c + 32, v[1]);
+            tmem_ld_wait();
+#pragma unroll
+            for (int hlf = 0; hlf < 2; ++hlf) {
+                const int col = n_blk * BN_ACC + c + 32 * hlf;
+                if (row_ok && col < p.n_out) {
+                    uint32_t packed[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        packed[i] = pack_bf16x2(__uint_as_float(v[hlf][2 * i]), __uint_as_float(v[hlf][2 * i + 1]));
+                    store_row32(p.out + static_cast<size_t>(grow) * p.n_out + col, packed);
+                }
+            }
+        }
+    }
+}
+
+// ======================================================================
+// single-CTA variant
+// ======================================================================
 template <bool SWIGLU>
 __global__ void __launch_bounds__(THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_BARS);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L1::OFF_BARS);
     uint64_t *full = bars;
     uint64_t *empty = bars + STAGES;
     uint64_t *tfull = bars + 2 * STAGES;
     uint64_t *tempty = bars + 2 * STAGES + 2;
     uint64_t *drain = bars + 2 * STAGES + 4;
-    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(smem + OFF_TMEM);
-    volatile int *s_abort = reinterpret_cast<volatile int *>(smem + OFF_ABORT);
-    int *s_off = reinterpret_cast<int *>(smem + OFF_OFFS);
-    int *s_end = reinterpret_cast<int *>(smem + OFF_ENDS);
-    int *s_pre = reinterpret_cast<int *>(smem + OFF_PRE);
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(smem + L1::OFF_TMEM);
+    volatile int *s_abort = reinterpret_cast<volatile int *>(smem + L1::OFF_ABORT);
+    int *s_off = reinterpret_cast<int *>(smem + L1::OFF_OFFS);
+    int *s_end = reinterpret_cast<int *>(smem + L1::OFF_ENDS);
+    int *s_pre = reinterpret_cast<int *>(smem + L1::OFF_PRE);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -150,31 +269,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         tmem_alloc(s_tmem, TMEM_COLS);
         tmem_relinquish();
     }
-    if (warp == 2) {
-        // Group bounds [s_off[e], s_end[e]), clamped to [0, TK] so that no
-        // content of offsets[] can send a store out of bounds, and the
-        // per-expert tile prefix s_pre (tiles of experts < e).
-        int carry = 0;
-        for (int base = 0; base < E; base += 32) {
-            const int e = base + lane;
-            int v = 0;
-            if (e < E) {
-                const int o0 = min(max(p.offsets[e], 0), p.TK);
-                const int o1 = min(max(p.offsets[e + 1], o0), p.TK);
-                s_off[e] = o0;
-                s_end[e] = o1;
-                v = ((o1 - o0 + BM - 1) / BM) * NT;
-            }
-#pragma unroll
-            for (int s = 1; s < 32; s <<= 1) {
-                const int n = __shfl_up_sync(0xffffffffu, v, s);
-                if (lane >= s) v += n;
-            }
-            if (e < E) s_pre[e + 1] = carry + v;
-            carry += __shfl_sync(0xffffffffu, v, 31);
-        }
-        if (lane == 0) s_pre[0] = 0;
-    }
+    if (warp == 2) build_groups<BM>(p, lane, s_off, s_end, s_pre);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -191,7 +286,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             uint32_t stage = 0, phase = 0;
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
-                const Tile t = decode_tile(tile, s_pre, s_off, s_end, E, NT);
+                const Tile t = decode_tile<BM, BAND>(tile, s_pre, s_off, s_end, E, NT);
                 int brow0, brow1;
                 if (SWIGLU) {
                     brow0 = t.e * p.w_rows + t.n_blk * (BN_ACC / 2);
@@ -261,58 +356,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         const int row_local = q * 32 + lane;
         uint32_t acc = 0, acc_phase = 0;
         for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
-            const Tile t = decode_tile(tile, s_pre, s_off, s_end, E, NT);
+            const Tile t = decode_tile<BM, BAND>(tile, s_pre, s_off, s_end, E, NT);
             if (!mbar_wait(&tfull[acc], acc_phase, s_abort, p.status, p.timeout_ns)) break;
             tc_fence_after();
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN_ACC;
             const int grow = t.row0 + row_local;
-            const bool row_ok = row_local < t.rows && grow < t.grp_end;
-            if (SWIGLU) {
-#pragma unroll 1
-                for (int c = 0; c < BN_ACC / 2; c += 32) {
-                    uint32_t g[32], u[32];
-                    tmem_ld_32x32b_x32(tbase + c, g);
-                    tmem_ld_32x32b_x32(tbase + BN_ACC / 2 + c, u);
-                    tmem_ld_wait();
-                    const int col = t.n_blk * (BN_ACC / 2) + c;
-                    if (row_ok && col < p.n_out) {
-                        uint32_t packed[16];
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            float h2[2];
-#pragma unroll
-                            for (int k = 0; k < 2; ++k) {
-                                const float gv = __uint_as_float(g[2 * i + k]);
-                                const float uv = __uint_as_float(u[2 * i + k]);
-                                h2[k] = gv * __frcp_rn(1.0f + __expf(-gv)) * uv;
-                            }
-                            packed[i] = pack_bf16x2(h2[0], h2[1]);
-                        }
-                        uint4 *dst = reinterpret_cast<uint4 *>(p.out + static_cast<size_t>(grow) * p.n_out + col);
-#pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
-                    }
-                }
-            } else {
-#pragma unroll 1
-                for (int c = 0; c < BN_ACC; c += 32) {
-                    uint32_t v[32];
-                    tmem_ld_32x32b_x32(tbase + c, v);
-                    tmem_ld_wait();
-                    const int col = t.n_blk * BN_ACC + c;
-                    if (row_ok && col < p.n_out) {
-                        uint32_t packed[16];
-#pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            packed[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-                        uint4 *dst = reinterpret_cast<uint4 *>(p.out + static_cast<size_t>(grow) * p.n_out + col);
-#pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
-                    }
-                }
-            }
+            epilogue_tile<SWIGLU>(p, tbase, t.n_blk, grow, grow < t.grp_end);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[acc]);
@@ -326,6 +375,174 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+// ======================================================================
+// CTA-pair variant (cluster of 2)
+// ======================================================================
+template <bool SWIGLU>
+__global__ void __launch_bounds__(THREADS, 1)
+grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                         const Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L2::OFF_BARS);
+    uint64_t *full = bars;                       // used in CTA 0 only
+    uint64_t *empty = bars + P_STAGES;           // both CTAs
+    uint64_t *tfull = bars + 2 * P_STAGES;       // both CTAs
+    uint64_t *tempty = bars + 2 * P_STAGES + 2;  // CTA 0 only: 4 warps x 2 CTAs arrive
+    uint64_t *drain = bars + 2 * P_STAGES + 4;
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(smem + L2::OFF_TMEM);
+    volatile int *s_abort = reinterpret_cast<volatile int *>(smem + L2::OFF_ABORT);
+    int *s_off = reinterpret_cast<int *>(smem + L2::OFF_OFFS);
+    int *s_end = reinterpret_cast<int *>(smem + L2::OFF_ENDS);
+    int *s_pre = reinterpret_cast<int *>(smem + L2::OFF_PRE);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int E = p.E;
+    const int NT = p.NT;
+    const uint32_t rank = cluster_ctarank();  // 0 issues the MMAs
+    const int pair = blockIdx.x >> 1;
+    const int npairs = gridDim.x >> 1;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < P_STAGES; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&tfull[i], 1);
+            mbar_init(&tempty[i], 8);
+        }
+        mbar_init(drain, 1);
+        *s_abort = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 2) build_groups<P_BM>(p, lane, s_off, s_end, s_pre);
+    __syncthreads();
+    // both CTAs' barriers are initialised (and both CTAs are running) before
+    // any copy, commit or arrive crosses the pair, and before the collective
+    // TMEM allocation
+    cluster_sync();
+    if (warp == 1) {
+        tmem_alloc_pair(s_tmem, TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    const uint32_t tmem_base = *s_tmem;
+    const int total_tiles = s_pre[E];
+    const int KB = p.Kdim / BK;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // both CTAs' copies signal CTA 0's full barriers
+            const uint32_t full0 = mapa_shared(smem_u32(&full[0]), 0);
+            int armed_phase[P_STAGES];
+#pragma unroll
+            for (int i = 0; i < P_STAGES; ++i) armed_phase[i] = -1;
+            uint32_t stage = 0, phase = 0;
+            bool ok = true;
+            for (int tile = pair; ok && tile < total_tiles; tile += npairs) {
+                const Tile t = decode_tile<P_BM, P_BAND>(tile, s_pre, s_off, s_end, E, NT);
+                const int a_row = t.row0 + 128 * static_cast<int>(rank);
+                // GEMM1: CTA 0 loads the gate rows, CTA 1 the up rows (f rows later);
+                // GEMM2: CTA r loads rows 128r..128r+127 of the 256-row column block
+                const int brow = SWIGLU ? t.e * p.w_rows + static_cast<int>(rank) * p.n_out + t.n_blk * (BN_ACC / 2)
+                                        : t.e * p.w_rows + t.n_blk * BN_ACC + static_cast<int>(rank) * (BN_ACC / 2);
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!mbar_wait<true>(&empty[stage], phase ^ 1u, s_abort, p.status, p.timeout_ns)) { ok = false; break; }
+                    uint8_t *sa = smem + stage * P_STAGE_BYTES;
+                    uint8_t *sb = sa + P_A_BYTES;
+                    if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * P_STAGE_BYTES);
+                    tma_load_2d_pair(sa, &tmA, full0 + 8u * stage, kb * BK, a_row);
+                    tma_load_2d_pair(sb, &tmB, full0 + 8u * stage, kb * BK, brow);
+                    armed_phase[stage] = static_cast<int>(phase);
+                    if (++stage == P_STAGES) { stage = 0; phase ^= 1u; }
+                }
+            }
+            if (!ok) {
+                volatile int no_abort = 0;
+                if (rank == 0) {
+                    for (int i = 0; i < P_STAGES; ++i)
+                        if (armed_phase[i] >= 0)
+                            mbar_wait<true>(&full[i], static_cast<uint32_t>(armed_phase[i]), &no_abort, p.status,
+                                            p.timeout_ns);
+                } else {
+                    // this CTA's copies signal CTA 0's barriers: give them time to land
+                    const uint64_t t0 = global_timer_ns();
+                    while (global_timer_ns() - t0 < 200000ull) __nanosleep(1000);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && rank == 0) {
+            constexpr uint32_t idesc = idesc_bf16_f32(P_BM, BN_ACC);
+            uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+            bool ok = true;
+            bool issued = false;
+            for (int tile = pair; ok && tile < total_tiles; tile += npairs) {
+                if (!mbar_wait<true>(&tempty[acc], acc_phase ^ 1u, s_abort, p.status, p.timeout_ns)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * BN_ACC;
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!mbar_wait<true>(&full[stage], phase, s_abort, p.status, p.timeout_ns)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(smem + stage * P_STAGE_BYTES);
+                    const uint64_t adesc = smem_desc_kmajor_sw128(sa);
+                    const uint64_t bdesc = smem_desc_kmajor_sw128(sa + P_A_BYTES);
+#pragma unroll
+                    for (int j = 0; j < BK / UMMA_K; ++j)
+                        umma_bf16_pair(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, (kb | j) != 0);
+                    issued = true;
+                    umma_commit_pair_multicast(&empty[stage], 0x3);
+                    if (++stage == P_STAGES) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                umma_commit_pair_multicast(&tfull[acc], 0x3);
+                acc ^= 1u;
+                if (acc == 0) acc_phase ^= 1u;
+            }
+            if (!ok && issued) {
+                volatile int no_abort = 0;
+                umma_commit_pair_multicast(drain, 0x1);
+                mbar_wait<true>(drain, 0, &no_abort, p.status, p.timeout_ns);
+            }
+        }
+    } else {
+        const int q = warp & 3;
+        const int row_local = q * 32 + lane;
+        const uint32_t tempty0 = mapa_shared(smem_u32(&tempty[0]), 0);
+        uint32_t acc = 0, acc_phase = 0;
+        for (int tile = pair; tile < total_tiles; tile += npairs) {
+            const Tile t = decode_tile<P_BM, P_BAND>(tile, s_pre, s_off, s_end, E, NT);
+            if (!mbar_wait<true>(&tfull[acc], acc_phase, s_abort, p.status, p.timeout_ns)) break;
+            tc_fence_after();
+            const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN_ACC;
+            const int grow = t.row0 + 128 * static_cast<int>(rank) + row_local;
+            epilogue_tile<SWIGLU>(p, tbase, t.n_blk, grow, grow < t.grp_end);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(tempty0 + 8u * acc);
+            acc ^= 1u;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    // neither CTA leaves (or frees TMEM) while its peer may still touch its
+    // shared memory or tensor memory
+    cluster_sync();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, TMEM_COLS);
     }
 }
 
@@ -363,17 +580,57 @@ bool make_tmap(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, u
     return r == CUDA_SUCCESS;
 }
 
+template <bool SWIGLU>
+cudaError_t launch_pair(const CUtensorMap &tmA, const CUtensorMap &tmB, const gg::Params &p, int grid,
+                        cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(gg::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = gg::P_SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gg::grouped_gemm_pair_kernel<SWIGLU>, tmA, tmB, p);
+}
+
+template <bool SWIGLU>
+int max_pairs() {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(gg::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = gg::P_SMEM_BYTES;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gg::grouped_gemm_pair_kernel<SWIGLU>, &cfg) != cudaSuccess) return 0;
+    return n;
+}
+
 }  // namespace
 
-int grouped_gemm_smem_bytes() { return gg::SMEM_BYTES; }
+bool grouped_gemm_use_pair(int TK, int E) {
+    // a 256-row pair tile pays off once the average group holds a few of them
+    return static_cast<int64_t>(TK) >= static_cast<int64_t>(E) * 384;
+}
 
 cudaError_t launch_grouped_gemm(bool swiglu, const void *A, int TK, int Kdim, const void *W, int E, int n_out,
-                                const int32_t *offsets, void *out, int num_sms, int *status, uint64_t timeout_ns,
-                                cudaStream_t stream) {
+                                const int32_t *offsets, void *out, const GemmLaunch &cfg, int *status,
+                                uint64_t timeout_ns, cudaStream_t stream) {
     CUtensorMap tmA, tmB;
     const int w_rows = swiglu ? 2 * n_out : n_out;
-    if (!make_tmap(&tmA, A, static_cast<uint64_t>(TK), static_cast<uint64_t>(Kdim), gg::BM)) return cudaErrorInvalidValue;
-    if (!make_tmap(&tmB, W, static_cast<uint64_t>(E) * w_rows, static_cast<uint64_t>(Kdim), gg::BN_ACC / 2))
+    if (!make_tmap(&tmA, A, static_cast<uint64_t>(TK), static_cast<uint64_t>(Kdim), gg::BOX_ROWS))
+        return cudaErrorInvalidValue;
+    if (!make_tmap(&tmB, W, static_cast<uint64_t>(E) * w_rows, static_cast<uint64_t>(Kdim), gg::BOX_ROWS))
         return cudaErrorInvalidValue;
     gg::Params p;
     p.offsets = offsets;
@@ -386,19 +643,39 @@ cudaError_t launch_grouped_gemm(bool swiglu, const void *A, int TK, int Kdim, co
     p.out = static_cast<__nv_bfloat16 *>(out);
     p.status = status;
     p.timeout_ns = timeout_ns;
+    const int pairs = swiglu ? cfg.pairs_swiglu : cfg.pairs_plain;
+    if (grouped_gemm_use_pair(TK, E) && pairs > 0) {
+        return swiglu ? launch_pair<true>(tmA, tmB, p, 2 * pairs, stream)
+                      : launch_pair<false>(tmA, tmB, p, 2 * pairs, stream);
+    }
     if (swiglu)
-        gg::grouped_gemm_kernel<true><<<num_sms, gg::THREADS, gg::SMEM_BYTES, stream>>>(tmA, tmB, p);
+        gg::grouped_gemm_kernel<true><<<cfg.num_sms, gg::THREADS, gg::SMEM_BYTES, stream>>>(tmA, tmB, p);
     else
-        gg::grouped_gemm_kernel<false><<<num_sms, gg::THREADS, gg::SMEM_BYTES, stream>>>(tmA, tmB, p);
+        gg::grouped_gemm_kernel<false><<<cfg.num_sms, gg::THREADS, gg::SMEM_BYTES, stream>>>(tmA, tmB, p);
     return cudaGetLastError();
 }
 
-cudaError_t grouped_gemm_set_attributes() {
-    cudaError_t e = cudaFuncSetAttribute(gg::grouped_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         gg::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(gg::grouped_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                gg::SMEM_BYTES);
+cudaError_t grouped_gemm_setup(int num_sms, GemmLaunch *cfg) {
+    cudaError_t e;
+    if ((e = cudaFuncSetAttribute(gg::grouped_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  gg::SMEM_BYTES)) != cudaSuccess)
+        return e;
+    if ((e = cudaFuncSetAttribute(gg::grouped_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  gg::SMEM_BYTES)) != cudaSuccess)
+        return e;
+    if ((e = cudaFuncSetAttribute(gg::grouped_gemm_pair_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  gg::P_SMEM_BYTES)) != cudaSuccess)
+        return e;
+    if ((e = cudaFuncSetAttribute(gg::grouped_gemm_pair_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  gg::P_SMEM_BYTES)) != cudaSuccess)
+        return e;
+    cfg->num_sms = num_sms;
+    // every pair must be resident at once (the kernel is persistent): never
+    // launch more pairs than fit, nor more CTAs than SMs
+    cfg->pairs_swiglu = std::min(max_pairs<true>(), num_sms / 2);
+    cfg->pairs_plain = std::min(max_pairs<false>(), num_sms / 2);
+    cudaGetLastError();  // a failed occupancy query leaves pairs = 0: single-CTA kernels only
+    return cudaSuccess;
 }
 
 }  // namespace moe

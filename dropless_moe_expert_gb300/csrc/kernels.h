@@ -30,11 +30,21 @@ cudaError_t launch_permute(const uint16_t *x, const int32_t *row_of, int T, int 
 cudaError_t launch_unpermute(const uint16_t *y_perm, const int32_t *row_of, const float *topk_w, int T, int K,
                              int d, uint16_t *y, cudaStream_t stream);
 
-int grouped_gemm_smem_bytes();
-cudaError_t grouped_gemm_set_attributes();
+// Per-device launch shape of the grouped GEMM: SM count, and how many CTA
+// pairs of the pair kernel can be resident at once (0: single-CTA only).
+struct GemmLaunch {
+    int num_sms = 0;
+    int pairs_swiglu = 0;
+    int pairs_plain = 0;
+};
+// Kernel attributes and occupancy queries; once per device, before any capture.
+cudaError_t grouped_gemm_setup(int num_sms, GemmLaunch *cfg);
+// True when the CTA-pair kernel is used for this shape (decided on host
+// sizes only, so the choice is the same for every routing).
+bool grouped_gemm_use_pair(int TK, int E);
 // swiglu: GEMM1 (out [TK, n_out=f], W [E, 2f, Kdim=d]); else GEMM2 (out [TK, n_out=d], W [E, d, Kdim=f]).
 cudaError_t launch_grouped_gemm(bool swiglu, const void *A, int TK, int Kdim, const void *W, int E, int n_out,
-                                const int32_t *offsets, void *out, int num_sms, int *status, uint64_t timeout_ns,
-                                cudaStream_t stream);
+                                const int32_t *offsets, void *out, const GemmLaunch &cfg, int *status,
+                                uint64_t timeout_ns, cudaStream_t stream);
 
 }  // namespace moe

@@ -23,6 +23,7 @@ struct DeviceState {
     bool ready = false;
     int num_sms = 0;
     int *status = nullptr;
+    moe::GemmLaunch gemm;
 };
 constexpr int kMaxDevices = 64;
 DeviceState g_dev[kMaxDevices];
@@ -40,7 +41,7 @@ moe_status_t device_state(DeviceState **out) {
         cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
         if (major != 10) return MOE_ERR_UNSUPPORTED;  // built for sm_103a only
-        if (moe::grouped_gemm_set_attributes() != cudaSuccess) return MOE_ERR_CUDA;
+        if (moe::grouped_gemm_setup(s.num_sms, &s.gemm) != cudaSuccess) return MOE_ERR_CUDA;
         if (cudaGetSymbolAddress(reinterpret_cast<void **>(&s.status), g_device_status) != cudaSuccess)
             return MOE_ERR_CUDA;
         s.ready = true;
@@ -99,7 +100,7 @@ moe_status_t run_gemm(bool swiglu, const void *A, const int32_t *offsets, int E,
     const int Kdim = swiglu ? d : f;
     const int n_out = swiglu ? f : d;
     g_launches.fetch_add(1, std::memory_order_relaxed);
-    return cuda_status(moe::launch_grouped_gemm(swiglu, A, TK, Kdim, W, E, n_out, offsets, out, ds->num_sms,
+    return cuda_status(moe::launch_grouped_gemm(swiglu, A, TK, Kdim, W, E, n_out, offsets, out, ds->gemm,
                                                 ds->status, kWaitLimitNs, stream));
 }
 

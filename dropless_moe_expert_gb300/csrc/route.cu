@@ -8,10 +8,11 @@
 // optimizations are needed for dropless MoE?", "Optimization 1: Grouped GEMM").
 //
 // Three kernels, no atomics whose order could show in a result:
-//  1. route_topk: one warp per token; each lane holds E/32 logits as 64-bit
-//     keys (order-preserving float bits << 32 | ~expert), K rounds of warp
-//     max via shuffles pick the experts (descending, lower index on ties,
-//     -0.0 == +0.0); softmax over the K picks.  The CTA then marks, per
+//  1. route_topk: a group of G lanes per token (G = 8, 16 or 32; 32/G tokens
+//     per warp); each lane holds E/G logits as 64-bit keys (order-preserving
+//     float bits << 32 | ~expert), K rounds of group max via shuffles pick the
+//     experts (descending, lower index on ties, -0.0 == +0.0); softmax over
+//     the K picks.  The CTA then marks, per
 //     expert, which of its 256 tokens chose it in a shared bitmap (atomicOr:
 //     the final bitmap does not depend on order), and from it writes the
 //     chunk's per-expert count and every pair's rank inside the chunk.
@@ -34,7 +35,6 @@ constexpr int THREADS = 256;
 constexpr int WARPS = THREADS / 32;
 constexpr int MAX_E = 256;
 constexpr int MAX_K = 16;
-constexpr int EPL = MAX_E / 32;  // logits per lane
 
 __device__ __forceinline__ uint32_t order_key(float v) {
     if (v == 0.0f) v = 0.0f;  // -0.0 and +0.0 compare equal: give them one key
@@ -46,26 +46,33 @@ __device__ __forceinline__ float key_value(uint32_t k) {
     return __uint_as_float(u);
 }
 
+// G lanes per token (a power of two, G >= E / EPL), EPL logits per lane, so
+// that few experts do not leave most of a warp idle: 32/G tokens per warp.
+template <int G, int EPL>
 __global__ void __launch_bounds__(THREADS)
 route_topk_kernel(const float *__restrict__ L, int T, int E, int K, int32_t *__restrict__ topk_idx,
                   float *__restrict__ topk_w, int32_t *__restrict__ row_rank, int32_t *__restrict__ chunk_counts) {
+    constexpr int TPW = 32 / G;  // tokens per warp at a time
     __shared__ uint32_t bits[MAX_E][CH / 32];
     __shared__ int32_t s_idx[CH * MAX_K];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const int glane = lane % G;                 // lane inside the token's group
+    const int group = lane / G;
+    const unsigned gmask = (G == 32) ? 0xffffffffu : (((1u << G) - 1u) << (group * G));
     const int t0 = blockIdx.x * CH;
     const int nt = min(CH, T - t0);
 
     for (int i = threadIdx.x; i < E * (CH / 32); i += THREADS) (&bits[0][0])[i] = 0u;
     __syncthreads();
 
-    for (int tl = warp; tl < nt; tl += WARPS) {
+    for (int tl = warp * TPW + group; tl < nt; tl += WARPS * TPW) {
         const int t = t0 + tl;
         const float *row = L + static_cast<size_t>(t) * E;
         unsigned long long key[EPL];
 #pragma unroll
         for (int j = 0; j < EPL; ++j) {
-            const int e = lane + 32 * j;
+            const int e = glane + G * j;
             key[j] = (e < E) ? ((static_cast<unsigned long long>(order_key(row[e])) << 32) |
                                 static_cast<unsigned long long>(0xffffffffu - static_cast<uint32_t>(e)))
                              : 0ull;  // below every real key
@@ -78,26 +85,24 @@ route_topk_kernel(const float *__restrict__ L, int T, int E, int K, int32_t *__r
 #pragma unroll
             for (int j = 1; j < EPL; ++j) best = key[j] > best ? key[j] : best;
 #pragma unroll
-            for (int s = 16; s >= 1; s >>= 1) {
-                const unsigned long long o = __shfl_xor_sync(0xffffffffu, best, s);
+            for (int s = G / 2; s >= 1; s >>= 1) {
+                const unsigned long long o = __shfl_xor_sync(gmask, best, s, G);
                 best = o > best ? o : best;
             }
             const int e = static_cast<int>(0xffffffffu - static_cast<uint32_t>(best & 0xffffffffull));
             const float v = key_value(static_cast<uint32_t>(best >> 32));
-            if ((e & 31) == lane) {
+            const bool mine = (e % G) == glane;
 #pragma unroll
-                for (int j = 0; j < EPL; ++j)
-                    if (j == (e >> 5)) key[j] = 0ull;
-            }
+            for (int j = 0; j < EPL; ++j) key[j] = (mine && j == e / G) ? 0ull : key[j];
             if (k == 0) v0 = v;
             const float z = expf(v - v0);
             sum += z;
-            if (lane == k) { my_e = e; my_z = z; }
+            if (glane == k) { my_e = e; my_z = z; }
         }
-        if (lane < K) {
-            topk_idx[static_cast<size_t>(t) * K + lane] = my_e;
-            topk_w[static_cast<size_t>(t) * K + lane] = my_z / sum;
-            s_idx[tl * K + lane] = my_e;
+        if (glane < K) {
+            topk_idx[static_cast<size_t>(t) * K + glane] = my_e;
+            topk_w[static_cast<size_t>(t) * K + glane] = my_z / sum;
+            s_idx[tl * K + glane] = my_e;
             atomicOr(&bits[my_e][tl >> 5], 1u << (tl & 31));
         }
     }
@@ -127,8 +132,10 @@ route_scan_kernel(const int32_t *__restrict__ chunk_counts, int C, int E, int32_
     const int e = threadIdx.x;
     const int lane = e & 31, warp = e >> 5;
     int cnt = 0;
-    if (e < E)
+    if (e < E) {
+#pragma unroll 8
         for (int c = 0; c < C; ++c) cnt += chunk_counts[static_cast<size_t>(c) * E + e];
+    }
     // exclusive scan of cnt over experts
     int v = cnt;
 #pragma unroll
@@ -146,6 +153,7 @@ route_scan_kernel(const int32_t *__restrict__ chunk_counts, int C, int E, int32_
         offsets[e] = excl;
         if (e == E - 1) offsets[E] = excl + cnt;
         int run = excl;
+#pragma unroll 8
         for (int c = 0; c < C; ++c) {
             chunk_base[static_cast<size_t>(c) * E + e] = run;
             run += chunk_counts[static_cast<size_t>(c) * E + e];
@@ -175,7 +183,18 @@ cudaError_t launch_route(const float *logits, int T, int E, int K, int32_t *topk
     const int C = route_num_chunks(T);
     int32_t *chunk_counts = workspace;
     int32_t *chunk_base = workspace + static_cast<size_t>(C) * E;
-    rt::route_topk_kernel<<<C, rt::THREADS, 0, stream>>>(logits, T, E, K, topk_idx, topk_w, row_of, chunk_counts);
+    if (E <= 8)
+        rt::route_topk_kernel<8, 1><<<C, rt::THREADS, 0, stream>>>(logits, T, E, K, topk_idx, topk_w, row_of, chunk_counts);
+    else if (E <= 16)
+        rt::route_topk_kernel<16, 1><<<C, rt::THREADS, 0, stream>>>(logits, T, E, K, topk_idx, topk_w, row_of, chunk_counts);
+    else if (E <= 32)
+        rt::route_topk_kernel<32, 1><<<C, rt::THREADS, 0, stream>>>(logits, T, E, K, topk_idx, topk_w, row_of, chunk_counts);
+    else if (E <= 64)
+        rt::route_topk_kernel<32, 2><<<C, rt::THREADS, 0, stream>>>(logits, T, E, K, topk_idx, topk_w, row_of, chunk_counts);
+    else if (E <= 128)
+        rt::route_topk_kernel<32, 4><<<C, rt::THREADS, 0, stream>>>(logits, T, E, K, topk_idx, topk_w, row_of, chunk_counts);
+    else
+        rt::route_topk_kernel<32, 8><<<C, rt::THREADS, 0, stream>>>(logits, T, E, K, topk_idx, topk_w, row_of, chunk_counts);
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     rt::route_scan_kernel<<<1, rt::MAX_E, 0, stream>>>(chunk_counts, C, E, counts, offsets, chunk_base);
