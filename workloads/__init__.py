@@ -45,6 +45,9 @@ CONFIGS = {
     "dsv3": dict(T=4096, d=7168, E=256, K=8, f=2048, bias="zipf_1.1"),
     "qwen": dict(T=16384, d=2048, E=128, K=8, f=768, bias="zero"),
     "skew": dict(T=32768, d=4096, E=64, K=6, f=1536, bias="skew"),
+    # profiling-size stand-in for dsv3: the same d, f, K and rows per expert
+    # (T*K/E = 128) with 32 experts, so a full ncu capture holds ~3 GB
+    "dsv3_e32": dict(T=512, d=7168, E=32, K=8, f=2048, bias="zipf_1.1"),
 }
 
 DESCRIPTIONS = {
@@ -53,6 +56,7 @@ DESCRIPTIONS = {
     "dsv3": "DeepSeek-V3-shaped routed-expert layer fwd T=4096 d=7168 E=256 K=8 f=2048",
     "qwen": "Qwen-MoE-shaped layer fwd T=16384 d=2048 E=128 K=8 f=768",
     "skew": "Extreme-skew MoE layer fwd T=32768 d=4096 E=64 K=6 f=1536",
+    "dsv3_e32": "DeepSeek-V3-shaped layer, 32 experts (profiling size) T=512 d=7168 E=32 K=8 f=2048",
 }
 
 
