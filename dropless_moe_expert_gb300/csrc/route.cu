@@ -31,7 +31,7 @@ namespace moe {
 namespace rt {
 
 constexpr int CH = kRouteChunk;  // tokens per CTA
-constexpr int THREADS = 256;
+constexpr int THREADS = 1024;    // 32 warps: each ranks 8 of the chunk's tokens
 constexpr int WARPS = THREADS / 32;
 constexpr int MAX_E = 256;
 constexpr int MAX_K = 16;
@@ -66,17 +66,29 @@ route_topk_kernel(const float *__restrict__ L, int T, int E, int K, int32_t *__r
     for (int i = threadIdx.x; i < E * (CH / 32); i += THREADS) (&bits[0][0])[i] = 0u;
     __syncthreads();
 
+    // the logits of the group's next token are loaded while the current one is
+    // ranked, so a warp does not pay one global-load latency per token
+    float nxt[EPL];
+    auto load_logits = [&](int tl) {
+        const float *row = L + static_cast<size_t>(t0 + tl) * E;
+#pragma unroll
+        for (int j = 0; j < EPL; ++j) {
+            const int e = glane + G * j;
+            nxt[j] = (tl < nt && e < E) ? row[e] : 0.0f;
+        }
+    };
+    load_logits(warp * TPW + group);
     for (int tl = warp * TPW + group; tl < nt; tl += WARPS * TPW) {
         const int t = t0 + tl;
-        const float *row = L + static_cast<size_t>(t) * E;
         unsigned long long key[EPL];
 #pragma unroll
         for (int j = 0; j < EPL; ++j) {
             const int e = glane + G * j;
-            key[j] = (e < E) ? ((static_cast<unsigned long long>(order_key(row[e])) << 32) |
+            key[j] = (e < E) ? ((static_cast<unsigned long long>(order_key(nxt[j])) << 32) |
                                 static_cast<unsigned long long>(0xffffffffu - static_cast<uint32_t>(e)))
                              : 0ull;  // below every real key
         }
+        load_logits(tl + WARPS * TPW);
         int my_e = 0;
         float my_z = 0.0f;
         float v0 = 0.0f, sum = 0.0f;
