@@ -20,7 +20,9 @@
 //    GEMM2 uses 256 consecutive rows of W2[e].  A tile that runs past its
 //    group reads neighbouring rows (or TMA zero fill); the epilogue masks them.
 //  * Warp roles: warp 0 = TMA producer, warp 1 = tcgen05.mma issuer (and TMEM
-//    owner), warps 2..5 = epilogue (TMEM -> registers -> global).
+//    owner), warps 2..5 = epilogue (TMEM -> registers -> bf16 -> shared memory
+//    -> TMA store of full lines; masked row stores where a warp's 32 rows
+//    cross the end of the group).
 //  * Shared-memory ring of bf16 tiles (64-wide K slices, 128-byte swizzle)
 //    with full/empty mbarriers; two 256-column fp32 accumulators in TMEM (512
 //    columns) so the epilogue of tile i overlaps the mainloop of tile i+1.
@@ -76,9 +78,16 @@ constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
 
 // shared-memory layout after the ring: barriers, TMEM address, abort flag,
 // group bounds and tile prefix
+// Epilogue staging for TMA stores: per epilogue warp two 32-row x 32-column
+// bf16 buffers (2 KB each, 64-byte swizzle).
+constexpr int EPI_WARPS = 4;
+constexpr int EPI_BUF = 32 * 32 * 2;
+constexpr int EPI_BYTES = EPI_WARPS * 2 * EPI_BUF;
+
 template <int NSTAGES, int STAGE>
 struct Layout {
-    static constexpr int OFF_BARS = NSTAGES * STAGE;
+    static constexpr int OFF_EPI = NSTAGES * STAGE;  // 1024-aligned: the ring is whole KBs
+    static constexpr int OFF_BARS = OFF_EPI + EPI_BYTES;
     static constexpr int NUM_BARS = 2 * NSTAGES + 5;  // full, empty, tfull[2], tempty[2], drain
     static constexpr int OFF_TMEM = OFF_BARS + NUM_BARS * 8;
     static constexpr int OFF_ABORT = OFF_TMEM + 4;
@@ -173,52 +182,82 @@ __device__ __forceinline__ void store_row32(__nv_bfloat16 *dst_row, const uint32
     for (int i = 0; i < 4; ++i) dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
 }
 
-// Epilogue of one accumulator: this thread owns TMEM lane `row_local` of the
-// warp's quarter (tbase already points at it) and output row `grow`.
+// Epilogue of one accumulator for one warp: 32 TMEM lanes = 32 output rows
+// wrow0..wrow0+31 (this thread's row is wrow0 + lane), tbase points at the
+// warp's lane quarter of the accumulator.  Each 32-column chunk is converted
+// to bf16 and, when all 32 rows belong to the group, staged in shared memory
+// (64-byte swizzle) and written by one TMA store of full lines; a slice that
+// crosses the group's end falls back to masked 16-byte stores per row.
+// `sbuf` alternates the warp's two staging buffers across chunks and tiles.
 template <bool SWIGLU>
-__device__ __forceinline__ void epilogue_tile(const Params &p, uint32_t tbase, int n_blk, int grow, bool row_ok) {
+__device__ __forceinline__ void epilogue_tile(const Params &p, const CUtensorMap *tm_out, uint8_t *stage,
+                                              uint32_t &sbuf, uint32_t tbase, int n_blk, int wrow0, int lane,
+                                              int grp_end) {
+    if (wrow0 >= grp_end) return;  // whole slice outside the group (warp-uniform)
+    const bool full = wrow0 + 31 < grp_end;
+    const int grow = wrow0 + lane;
+    const bool row_ok = grow < grp_end;
+    constexpr int NCOL = SWIGLU ? BN_ACC / 2 : BN_ACC;
+    auto emit = [&](int c, const uint32_t (&packed)[16]) {
+        const int col = n_blk * NCOL + c;
+        if (col >= p.n_out) return;  // column tail (uniform)
+        if (full) {
+            uint8_t *buf = stage + sbuf * EPI_BUF;
+            if (lane == 0) bulk_wait_read<1>();  // this buffer's store from two chunks ago has read it
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int jj = j ^ ((lane >> 1) & 3);
+                *reinterpret_cast<uint4 *>(buf + lane * 64 + jj * 16) =
+                    make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                tma_store_2d(tm_out, buf, col, wrow0);
+                bulk_commit();
+            }
+            sbuf ^= 1u;
+        } else if (row_ok) {
+            store_row32(p.out + static_cast<size_t>(grow) * p.n_out + col, packed);
+        }
+    };
     if (SWIGLU) {
 #pragma unroll 1
-        for (int c = 0; c < BN_ACC / 2; c += 32) {
+        for (int c = 0; c < NCOL; c += 32) {
             uint32_t g[32], u[32];
             tmem_ld_32x32b_x32(tbase + c, g);
             tmem_ld_32x32b_x32(tbase + BN_ACC / 2 + c, u);
             tmem_ld_wait();
-            const int col = n_blk * (BN_ACC / 2) + c;
-            if (row_ok && col < p.n_out) {
-                uint32_t packed[16];
+            uint32_t packed[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    float h2[2];
+            for (int i = 0; i < 16; ++i) {
+                float h2[2];
 #pragma unroll
-                    for (int k = 0; k < 2; ++k) {
-                        const float gv = __uint_as_float(g[2 * i + k]);
-                        const float uv = __uint_as_float(u[2 * i + k]);
-                        h2[k] = gv * __frcp_rn(1.0f + __expf(-gv)) * uv;
-                    }
-                    packed[i] = pack_bf16x2(h2[0], h2[1]);
+                for (int k = 0; k < 2; ++k) {
+                    const float gv = __uint_as_float(g[2 * i + k]);
+                    const float uv = __uint_as_float(u[2 * i + k]);
+                    h2[k] = gv * __frcp_rn(1.0f + __expf(-gv)) * uv;
                 }
-                store_row32(p.out + static_cast<size_t>(grow) * p.n_out + col, packed);
+                packed[i] = pack_bf16x2(h2[0], h2[1]);
             }
+            emit(c, packed);
         }
     } else {
         // two 32-column loads per wait, so TMEM latency is paid 4 times per tile, not 8
 #pragma unroll 1
-        for (int c = 0; c < BN_ACC; c += 64) {
+        for (int c = 0; c < NCOL; c += 64) {
             uint32_t v[2][32];
             tmem_ld_32x32b_x32(tbase + c, v[0]);
             tmem_ld_32x32b_x32(tbase + c + 32, v[1]);
             tmem_ld_wait();
 #pragma unroll
             for (int hlf = 0; hlf < 2; ++hlf) {
-                const int col = n_blk * BN_ACC + c + 32 * hlf;
-                if (row_ok && col < p.n_out) {
-                    uint32_t packed[16];
+                uint32_t packed[16];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        packed[i] = pack_bf16x2(__uint_as_float(v[hlf][2 * i]), __uint_as_float(v[hlf][2 * i + 1]));
-                    store_row32(p.out + static_cast<size_t>(grow) * p.n_out + col, packed);
-                }
+                for (int i = 0; i < 16; ++i)
+                    packed[i] = pack_bf16x2(__uint_as_float(v[hlf][2 * i]), __uint_as_float(v[hlf][2 * i + 1]));
+                emit(c + 32 * hlf, packed);
             }
         }
     }
@@ -230,7 +269,7 @@ __device__ __forceinline__ void epilogue_tile(const Params &p, uint32_t tbase, i
 template <bool SWIGLU>
 __global__ void __launch_bounds__(THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const Params p) {
+                    const __grid_constant__ CUtensorMap tmOut, const Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L1::OFF_BARS);
@@ -353,21 +392,22 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         }
     } else {
         const int q = warp & 3;  // TMEM lane quarter this warp may access
-        const int row_local = q * 32 + lane;
+        uint8_t *stage = smem + L1::OFF_EPI + (warp - 2) * 2 * EPI_BUF;
+        uint32_t sbuf = 0;
         uint32_t acc = 0, acc_phase = 0;
         for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
             const Tile t = decode_tile<BM, BAND>(tile, s_pre, s_off, s_end, E, NT);
             if (!mbar_wait(&tfull[acc], acc_phase, s_abort, p.status, p.timeout_ns)) break;
             tc_fence_after();
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN_ACC;
-            const int grow = t.row0 + row_local;
-            epilogue_tile<SWIGLU>(p, tbase, t.n_blk, grow, grow < t.grp_end);
+            epilogue_tile<SWIGLU>(p, &tmOut, stage, sbuf, tbase, t.n_blk, t.row0 + q * 32, lane, t.grp_end);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[acc]);
             acc ^= 1u;
             if (acc == 0) acc_phase ^= 1u;
         }
+        if (lane == 0) bulk_wait_all();  // stores done before the CTA's shared memory goes away
     }
 
     tc_fence_before();
@@ -384,7 +424,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 template <bool SWIGLU>
 __global__ void __launch_bounds__(THREADS, 1)
 grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                         const Params p) {
+                         const __grid_constant__ CUtensorMap tmOut, const Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L2::OFF_BARS);
@@ -517,7 +557,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
         }
     } else {
         const int q = warp & 3;
-        const int row_local = q * 32 + lane;
+        uint8_t *stage = smem + L2::OFF_EPI + (warp - 2) * 2 * EPI_BUF;
+        uint32_t sbuf = 0;
         const uint32_t tempty0 = mapa_shared(smem_u32(&tempty[0]), 0);
         uint32_t acc = 0, acc_phase = 0;
         for (int tile = pair; tile < total_tiles; tile += npairs) {
@@ -525,14 +566,15 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
             if (!mbar_wait<true>(&tfull[acc], acc_phase, s_abort, p.status, p.timeout_ns)) break;
             tc_fence_after();
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN_ACC;
-            const int grow = t.row0 + 128 * static_cast<int>(rank) + row_local;
-            epilogue_tile<SWIGLU>(p, tbase, t.n_blk, grow, grow < t.grp_end);
+            const int wrow0 = t.row0 + 128 * static_cast<int>(rank) + q * 32;
+            epilogue_tile<SWIGLU>(p, &tmOut, stage, sbuf, tbase, t.n_blk, wrow0, lane, t.grp_end);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(tempty0 + 8u * acc);
             acc ^= 1u;
             if (acc == 0) acc_phase ^= 1u;
         }
+        if (lane == 0) bulk_wait_all();
     }
 
     tc_fence_before();
@@ -566,23 +608,26 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// 2D bf16 row-major [rows, cols] with a (box_rows x 64) box and 128-byte swizzle.
-bool make_tmap(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+// 2D bf16 row-major [rows, cols] with a (box_rows x box_cols) box: operand
+// loads use 64-column boxes with 128-byte swizzle, the epilogue's stores
+// 32 x 32 boxes with 64-byte swizzle.
+bool make_tmap(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+               uint32_t box_cols = gg::BK, CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {cols, rows};
     cuuint64_t strides[1] = {cols * 2};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(gg::BK), box_rows};
+    cuuint32_t box[2] = {box_cols, box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
 template <bool SWIGLU>
-cudaError_t launch_pair(const CUtensorMap &tmA, const CUtensorMap &tmB, const gg::Params &p, int grid,
-                        cudaStream_t stream) {
+cudaError_t launch_pair(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmOut,
+                        const gg::Params &p, int grid, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);
     cfg.blockDim = dim3(gg::THREADS, 1, 1);
@@ -595,7 +640,7 @@ cudaError_t launch_pair(const CUtensorMap &tmA, const CUtensorMap &tmB, const gg
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gg::grouped_gemm_pair_kernel<SWIGLU>, tmA, tmB, p);
+    return cudaLaunchKernelEx(&cfg, gg::grouped_gemm_pair_kernel<SWIGLU>, tmA, tmB, tmOut, p);
 }
 
 template <bool SWIGLU>
@@ -632,6 +677,10 @@ cudaError_t launch_grouped_gemm(bool swiglu, const void *A, int TK, int Kdim, co
         return cudaErrorInvalidValue;
     if (!make_tmap(&tmB, W, static_cast<uint64_t>(E) * w_rows, static_cast<uint64_t>(Kdim), gg::BOX_ROWS))
         return cudaErrorInvalidValue;
+    CUtensorMap tmOut;
+    if (!make_tmap(&tmOut, out, static_cast<uint64_t>(TK), static_cast<uint64_t>(n_out), 32, 32,
+                   CU_TENSOR_MAP_SWIZZLE_64B))
+        return cudaErrorInvalidValue;
     gg::Params p;
     p.offsets = offsets;
     p.E = E;
@@ -645,13 +694,13 @@ cudaError_t launch_grouped_gemm(bool swiglu, const void *A, int TK, int Kdim, co
     p.timeout_ns = timeout_ns;
     const int pairs = swiglu ? cfg.pairs_swiglu : cfg.pairs_plain;
     if (grouped_gemm_use_pair(TK, E) && pairs > 0) {
-        return swiglu ? launch_pair<true>(tmA, tmB, p, 2 * pairs, stream)
-                      : launch_pair<false>(tmA, tmB, p, 2 * pairs, stream);
+        return swiglu ? launch_pair<true>(tmA, tmB, tmOut, p, 2 * pairs, stream)
+                      : launch_pair<false>(tmA, tmB, tmOut, p, 2 * pairs, stream);
     }
     if (swiglu)
-        gg::grouped_gemm_kernel<true><<<cfg.num_sms, gg::THREADS, gg::SMEM_BYTES, stream>>>(tmA, tmB, p);
+        gg::grouped_gemm_kernel<true><<<cfg.num_sms, gg::THREADS, gg::SMEM_BYTES, stream>>>(tmA, tmB, tmOut, p);
     else
-        gg::grouped_gemm_kernel<false><<<cfg.num_sms, gg::THREADS, gg::SMEM_BYTES, stream>>>(tmA, tmB, p);
+        gg::grouped_gemm_kernel<false><<<cfg.num_sms, gg::THREADS, gg::SMEM_BYTES, stream>>>(tmA, tmB, tmOut, p);
     return cudaGetLastError();
 }
 

@@ -10,8 +10,9 @@
 //           and written K times (scatter form: T*d reads, T*K*d writes).
 // combine : y[t, :] = bf16( sum_k w[t,k] * y_perm[row_of[t,k], :] ), fp32
 //           fused multiply-add in ascending k.
-// One warp per token, lanes own 16-byte column vectors; a lane keeps UV
-// vectors in flight per load round.
+// One warp per token, lanes own 16-byte column vectors.  permute keeps UV
+// vectors in flight per lane; combine loads all K rows of a round before
+// accumulating them (for the common K), so K*UVK loads are in flight.
 #include "kernels.h"
 
 #include <cuda_bf16.h>
@@ -70,6 +71,9 @@ __device__ __forceinline__ uint4 to_bf16x8(const float (&acc)[8]) {
     return make_uint4(p[0], p[1], p[2], p[3]);
 }
 
+// KT > 0: K is KT, and all K rows' vectors of a round are loaded before any
+// is accumulated, so a lane keeps KT*UVK loads in flight.  KT == 0: any K.
+template <int KT, int UVK>
 __global__ void __launch_bounds__(THREADS)
 unpermute_kernel(const uint4 *__restrict__ y_perm, const int32_t *__restrict__ row_of,
                  const float *__restrict__ topk_w, int T, int K, int nvec, uint4 *__restrict__ y) {
@@ -79,28 +83,47 @@ unpermute_kernel(const uint4 *__restrict__ y_perm, const int32_t *__restrict__ r
     for (int t = gw; t < T; t += nw) {
         const int my_row = lane < K ? row_of[static_cast<size_t>(t) * K + lane] : 0;
         const float my_w = lane < K ? topk_w[static_cast<size_t>(t) * K + lane] : 0.0f;
-        for (int v0 = 0; v0 < nvec; v0 += 32 * UV) {
-            float acc[UV][8];
+        for (int v0 = 0; v0 < nvec; v0 += 32 * UVK) {
+            float acc[UVK][8];
 #pragma unroll
-            for (int u = 0; u < UV; ++u)
+            for (int u = 0; u < UVK; ++u)
 #pragma unroll
                 for (int i = 0; i < 8; ++i) acc[u][i] = 0.0f;
-            for (int k = 0; k < K; ++k) {
-                const int r = __shfl_sync(0xffffffffu, my_row, k);
-                const float w = __shfl_sync(0xffffffffu, my_w, k);
-                const uint4 *src = y_perm + static_cast<size_t>(r) * nvec;
-                uint4 buf[UV];
+            if (KT > 0) {
+                uint4 buf[KT > 0 ? KT : 1][UVK];
 #pragma unroll
-                for (int u = 0; u < UV; ++u) {
-                    const int v = v0 + u * 32 + lane;
-                    buf[u] = v < nvec ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
+                for (int k = 0; k < KT; ++k) {
+                    const uint4 *src = y_perm + static_cast<size_t>(__shfl_sync(0xffffffffu, my_row, k)) * nvec;
+#pragma unroll
+                    for (int u = 0; u < UVK; ++u) {
+                        const int v = v0 + u * 32 + lane;
+                        buf[k][u] = v < nvec ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
+                    }
                 }
 #pragma unroll
-                for (int u = 0; u < UV; ++u) fma_bf16x8(acc[u], w, buf[u]);
+                for (int k = 0; k < KT; ++k) {
+                    const float w = __shfl_sync(0xffffffffu, my_w, k);
+#pragma unroll
+                    for (int u = 0; u < UVK; ++u) fma_bf16x8(acc[u], w, buf[k][u]);
+                }
+            } else {
+                for (int k = 0; k < K; ++k) {
+                    const int r = __shfl_sync(0xffffffffu, my_row, k);
+                    const float w = __shfl_sync(0xffffffffu, my_w, k);
+                    const uint4 *src = y_perm + static_cast<size_t>(r) * nvec;
+                    uint4 buf[UVK];
+#pragma unroll
+                    for (int u = 0; u < UVK; ++u) {
+                        const int v = v0 + u * 32 + lane;
+                        buf[u] = v < nvec ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
+                    }
+#pragma unroll
+                    for (int u = 0; u < UVK; ++u) fma_bf16x8(acc[u], w, buf[u]);
+                }
             }
             uint4 *dst = y + static_cast<size_t>(t) * nvec;
 #pragma unroll
-            for (int u = 0; u < UV; ++u) {
+            for (int u = 0; u < UVK; ++u) {
                 const int v = v0 + u * 32 + lane;
                 if (v < nvec) dst[v] = to_bf16x8(acc[u]);
             }
@@ -125,8 +148,20 @@ cudaError_t launch_permute(const uint16_t *x, const int32_t *row_of, int T, int 
 
 cudaError_t launch_unpermute(const uint16_t *y_perm, const int32_t *row_of, const float *topk_w, int T, int K,
                              int d, uint16_t *y, cudaStream_t stream) {
-    pm::unpermute_kernel<<<pm::grid_for(T), pm::THREADS, 0, stream>>>(
-        reinterpret_cast<const uint4 *>(y_perm), row_of, topk_w, T, K, d / 8, reinterpret_cast<uint4 *>(y));
+    const uint4 *src = reinterpret_cast<const uint4 *>(y_perm);
+    uint4 *dst = reinterpret_cast<uint4 *>(y);
+    const int g = pm::grid_for(T), nvec = d / 8;
+#define MOE_UNPERMUTE(KT, UVK) \
+    pm::unpermute_kernel<KT, UVK><<<g, pm::THREADS, 0, stream>>>(src, row_of, topk_w, T, K, nvec, dst)
+    switch (K) {
+        case 1: MOE_UNPERMUTE(1, 4); break;
+        case 2: MOE_UNPERMUTE(2, 4); break;
+        case 4: MOE_UNPERMUTE(4, 2); break;
+        case 6: MOE_UNPERMUTE(6, 2); break;
+        case 8: MOE_UNPERMUTE(8, 2); break;
+        default: MOE_UNPERMUTE(0, 4); break;
+    }
+#undef MOE_UNPERMUTE
     return cudaGetLastError();
 }
 
