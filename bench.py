@@ -135,13 +135,25 @@ def _barrier(ws):
         dist.barrier()
 
 
-def _max_over_ranks(v: float, ws: int) -> float:
+def _max_over_ranks(v: float, ws: int, device="cuda") -> float:
+    """The slowest rank's time: the whole job is done when every replica is."""
     if ws == 1:
         return v
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    t = torch.tensor([v], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def replica_seed(rank: int) -> int:
+    """Token seed of a replica: every rank forwards its own batch of T tokens
+    (the weights, seed 0, are the same on every rank)."""
+    return rank
+
+
+def aggregate(work_per_step: float, ws: int, steps: int, elapsed_ms_max: float) -> float:
+    """Whole-job rate: the work of all ranks' steps over the slowest rank's time."""
+    return work_per_step * ws * steps / (elapsed_ms_max * 1e-3)
 
 
 # ------------------------------------------------------------------ oracle timing
@@ -249,7 +261,7 @@ def run_gpu(args):
     TK = T * K
     dev = torch.device("cuda", local)
     w = make_weights(s, seed=0, device=dev)
-    x = make_tokens(s, seed=rank, device=dev)
+    x = make_tokens(s, seed=replica_seed(rank), device=dev)
 
     # persistent buffers of the step (granular C-ABI calls so that each
     # kernel can be bracketed by events on the launching stream)
@@ -320,8 +332,8 @@ def run_gpu(args):
     kmean = {n: sum(v) / len(v) for n, v in per_kernel.items()}
     ms_per_step = elapsed_ms / args.steps
     flops_step = 6.0 * TK * d * f
-    value = flops_step * ws * args.steps / (elapsed_ms * 1e-3) / 1e12
-    tokens_s = T * ws * args.steps / (elapsed_ms * 1e-3)
+    value = aggregate(flops_step, ws, args.steps, elapsed_ms) / 1e12
+    tokens_s = aggregate(T, ws, args.steps, elapsed_ms)
 
     # ---- end to end through the C ABI with host buffers (pinned)
     layer = moe.MoELayer(w.Wr, w.bias, w.W1, w.W2, K, T)
@@ -339,7 +351,7 @@ def run_gpu(args):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = _max_over_ranks(e0.elapsed_time(e1), ws)
-    e2e_value = flops_step * ws * args.steps / (e2e_ms * 1e-3) / 1e12
+    e2e_value = aggregate(flops_step, ws, args.steps, e2e_ms) / 1e12
 
     # ---- roofline of the dominant kernel
     peaks, peak_src = _peaks()

@@ -67,6 +67,7 @@ def _load():
         "moe_forward": (I, [P, P, P, P, P, I, I, I, I, I, P, P, S, P]),
         "moe_forward_host": (I, [P, P, P, P, P, I, I, I, I, I, P, P, S, P]),
         "moe_device_status": (I, [ctypes.POINTER(I)]),
+        "moe_check_bounded_wait": (I, [U64, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -290,6 +291,12 @@ def device_status() -> int:
     v = ctypes.c_int(0)
     _check(lib.moe_device_status(ctypes.byref(v)), "moe_device_status")
     return v.value
+
+
+def check_bounded_wait(limit_ns: int = 2_000_000, stream=None) -> None:
+    """Launches a kernel whose only wait never completes; it times out after
+    limit_ns and records MOE_ERR_DEVICE_TIMEOUT (see device_status())."""
+    _check(lib.moe_check_bounded_wait(limit_ns, _stream(stream)), "moe_check_bounded_wait")
 
 
 def launch_count() -> int:

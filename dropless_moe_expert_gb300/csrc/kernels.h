@@ -47,4 +47,8 @@ cudaError_t launch_grouped_gemm(bool swiglu, const void *A, int TK, int Kdim, co
                                 const int32_t *offsets, void *out, const GemmLaunch &cfg, int *status,
                                 uint64_t timeout_ns, cudaStream_t stream);
 
+// A kernel whose only wait never completes: it times out after limit_ns and
+// records MOE_ERR_DEVICE_TIMEOUT in *status.
+cudaError_t launch_bounded_wait_probe(int *status, uint64_t limit_ns, cudaStream_t stream);
+
 }  // namespace moe

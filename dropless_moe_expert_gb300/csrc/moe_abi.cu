@@ -275,6 +275,15 @@ moe_status_t moe_forward_host(const uint16_t *x_host, const float *Wr, const flo
     return cuda_status(cudaMemcpyAsync(y_host, y_dev, bytes, cudaMemcpyDeviceToHost, stream));
 }
 
+moe_status_t moe_check_bounded_wait(uint64_t limit_ns, cudaStream_t stream) {
+    if (limit_ns < 1000ull || limit_ns > kWaitLimitNs) return MOE_ERR_INVALID_ARG;
+    DeviceState *ds = nullptr;
+    moe_status_t st = device_state(&ds);
+    if (st != MOE_OK) return st;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return cuda_status(moe::launch_bounded_wait_probe(ds->status, limit_ns, stream));
+}
+
 moe_status_t moe_device_status(int *status_out) {
     if (!status_out) return MOE_ERR_INVALID_ARG;
     DeviceState *ds = nullptr;

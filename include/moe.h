@@ -183,6 +183,13 @@ moe_status_t moe_forward_host(const uint16_t *x_host, const float *Wr, const flo
  * a moe_status_t a kernel recorded).  Synchronous: call outside capture. */
 moe_status_t moe_device_status(int *status_out);
 
+/* Exercises the failure path of the device-side waits: launches one kernel
+ * whose single wait can never complete.  After limit_ns (1 us .. 1 s) it
+ * gives up, records MOE_ERR_DEVICE_TIMEOUT in the device status word (read
+ * it with moe_device_status()) and returns; the CUDA context stays usable.
+ * Returns MOE_OK when the launch succeeded.  */
+moe_status_t moe_check_bounded_wait(uint64_t limit_ns, cudaStream_t stream);
+
 /* Number of kernels this library has launched in this process. */
 uint64_t moe_launch_count(void);
 
