@@ -94,7 +94,8 @@ struct Layout {
     static constexpr int OFF_OFFS = OFF_ABORT + 4;
     static constexpr int OFF_ENDS = OFF_OFFS + MAX_E * 4;
     static constexpr int OFF_PRE = OFF_ENDS + MAX_E * 4;
-    static constexpr int USED = OFF_PRE + (MAX_E + 1) * 4;
+    static constexpr int OFF_MIX = OFF_PRE + (MAX_E + 1) * 4;
+    static constexpr int USED = OFF_MIX + 4;
     static constexpr int BYTES = USED + 1024;  // slack for 1024-byte alignment
 };
 using L1 = Layout<STAGES, STAGE_BYTES>;
@@ -123,9 +124,13 @@ struct Tile {
 // Group bounds [s_off[e], s_end[e]), clamped to [0, TK] so that no content of
 // offsets[] can send a store out of bounds, and the per-expert tile prefix
 // s_pre (tiles of experts < e) for row blocks of RB rows.  One warp.
+//
+// Also decides the visit order (s_mix): when the largest group holds more
+// than 4x the average, heavy and light groups' tiles are interleaved.
 template <int RB>
-__device__ __forceinline__ void build_groups(const Params &p, int lane, int *s_off, int *s_end, int *s_pre) {
-    int carry = 0;
+__device__ __forceinline__ void build_groups(const Params &p, int lane, int *s_off, int *s_end, int *s_pre,
+                                             int *s_mix) {
+    int carry = 0, cmax = 0, csum = 0;
     for (int base = 0; base < p.E; base += 32) {
         const int e = base + lane;
         int v = 0;
@@ -135,6 +140,8 @@ __device__ __forceinline__ void build_groups(const Params &p, int lane, int *s_o
             s_off[e] = o0;
             s_end[e] = o1;
             v = ((o1 - o0 + RB - 1) / RB) * p.NT;
+            cmax = max(cmax, o1 - o0);
+            csum += o1 - o0;
         }
 #pragma unroll
         for (int s = 1; s < 32; s <<= 1) {
@@ -144,7 +151,15 @@ __device__ __forceinline__ void build_groups(const Params &p, int lane, int *s_o
         if (e < p.E) s_pre[e + 1] = carry + v;
         carry += __shfl_sync(0xffffffffu, v, 31);
     }
-    if (lane == 0) s_pre[0] = 0;
+#pragma unroll
+    for (int s = 16; s >= 1; s >>= 1) {
+        cmax = max(cmax, __shfl_xor_sync(0xffffffffu, cmax, s));
+        csum += __shfl_xor_sync(0xffffffffu, csum, s);
+    }
+    if (lane == 0) {
+        s_pre[0] = 0;
+        *s_mix = static_cast<int64_t>(cmax) * p.E > 4ll * csum ? 1 : 0;
+    }
 }
 
 template <int RB, int NBAND>
@@ -170,6 +185,23 @@ __device__ __forceinline__ Tile decode_tile(int tile, const int *s_pre, const in
     t.grp_end = g1;
     return t;
 }
+
+// Order in which the persistent CTAs visit the tile list.  Under a skewed
+// load (mix), positions alternate between the front and the back of the list,
+// so every wave mixes tiles of the experts at both ends: the heavy groups'
+// tiles, whose weight tiles are shared by many row blocks and so are bounded
+// by the tensor pipe, run beside the light groups' tiles, which only stream
+// weights.  A bijection of [0, N); neighbours in each half stay neighbours,
+// so tiles that share operands through L2 still run together.
+__device__ __forceinline__ int visit_order(int p, int N, int mix) {
+    return mix ? ((p & 1) ? N - 1 - (p >> 1) : (p >> 1)) : p;
+}
+
+// Position of round k for worker c of G: rounds cover consecutive blocks of
+// G positions, and the workers sweep them in alternating direction, so a
+// worker alternates between even and odd positions (the two ends of the list
+// under the interleaved order).
+__device__ __forceinline__ int round_position(int k, int c, int G) { return k * G + ((k & 1) ? G - 1 - c : c); }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -283,6 +315,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     int *s_off = reinterpret_cast<int *>(smem + L1::OFF_OFFS);
     int *s_end = reinterpret_cast<int *>(smem + L1::OFF_ENDS);
     int *s_pre = reinterpret_cast<int *>(smem + L1::OFF_PRE);
+    int *s_mix = reinterpret_cast<int *>(smem + L1::OFF_MIX);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -308,13 +341,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         tmem_alloc(s_tmem, TMEM_COLS);
         tmem_relinquish();
     }
-    if (warp == 2) build_groups<BM>(p, lane, s_off, s_end, s_pre);
+    if (warp == 2) build_groups<BM>(p, lane, s_off, s_end, s_pre, s_mix);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
 
     const uint32_t tmem_base = *s_tmem;
     const int total_tiles = s_pre[E];
+    const int mix = *s_mix;
     const int KB = p.Kdim / BK;
 
     if (warp == 0) {
@@ -324,8 +358,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             for (int i = 0; i < STAGES; ++i) armed_phase[i] = -1;
             uint32_t stage = 0, phase = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
-                const Tile t = decode_tile<BM, BAND>(tile, s_pre, s_off, s_end, E, NT);
+            for (int k = 0, tile = round_position(0, blockIdx.x, gridDim.x); ok && tile < total_tiles;
+                 ++k, tile = round_position(k, blockIdx.x, gridDim.x)) {
+                const Tile t = decode_tile<BM, BAND>(visit_order(tile, total_tiles, mix), s_pre, s_off, s_end, E, NT);
                 int brow0, brow1;
                 if (SWIGLU) {
                     brow0 = t.e * p.w_rows + t.n_blk * (BN_ACC / 2);
@@ -360,7 +395,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
             bool ok = true;
             bool issued = false;
-            for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+            for (int k = 0, tile = round_position(0, blockIdx.x, gridDim.x); ok && tile < total_tiles;
+                 ++k, tile = round_position(k, blockIdx.x, gridDim.x)) {
                 if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, s_abort, p.status, p.timeout_ns)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN_ACC;
@@ -395,8 +431,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         uint8_t *stage = smem + L1::OFF_EPI + (warp - 2) * 2 * EPI_BUF;
         uint32_t sbuf = 0;
         uint32_t acc = 0, acc_phase = 0;
-        for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
-            const Tile t = decode_tile<BM, BAND>(tile, s_pre, s_off, s_end, E, NT);
+        for (int k = 0, tile = round_position(0, blockIdx.x, gridDim.x); tile < total_tiles;
+             ++k, tile = round_position(k, blockIdx.x, gridDim.x)) {
+            const Tile t = decode_tile<BM, BAND>(visit_order(tile, total_tiles, mix), s_pre, s_off, s_end, E, NT);
             if (!mbar_wait(&tfull[acc], acc_phase, s_abort, p.status, p.timeout_ns)) break;
             tc_fence_after();
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN_ACC;
@@ -438,6 +475,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
     int *s_off = reinterpret_cast<int *>(smem + L2::OFF_OFFS);
     int *s_end = reinterpret_cast<int *>(smem + L2::OFF_ENDS);
     int *s_pre = reinterpret_cast<int *>(smem + L2::OFF_PRE);
+    int *s_mix = reinterpret_cast<int *>(smem + L2::OFF_MIX);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -462,7 +500,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
     }
-    if (warp == 2) build_groups<P_BM>(p, lane, s_off, s_end, s_pre);
+    if (warp == 2) build_groups<P_BM>(p, lane, s_off, s_end, s_pre, s_mix);
     __syncthreads();
     // both CTAs' barriers are initialised (and both CTAs are running) before
     // any copy, commit or arrive crosses the pair, and before the collective
@@ -478,6 +516,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
 
     const uint32_t tmem_base = *s_tmem;
     const int total_tiles = s_pre[E];
+    const int mix = *s_mix;
     const int KB = p.Kdim / BK;
 
     if (warp == 0) {
@@ -489,8 +528,9 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
             for (int i = 0; i < P_STAGES; ++i) armed_phase[i] = -1;
             uint32_t stage = 0, phase = 0;
             bool ok = true;
-            for (int tile = pair; ok && tile < total_tiles; tile += npairs) {
-                const Tile t = decode_tile<P_BM, P_BAND>(tile, s_pre, s_off, s_end, E, NT);
+            for (int k = 0, tile = round_position(0, pair, npairs); ok && tile < total_tiles;
+                 ++k, tile = round_position(k, pair, npairs)) {
+                const Tile t = decode_tile<P_BM, P_BAND>(visit_order(tile, total_tiles, mix), s_pre, s_off, s_end, E, NT);
                 const int a_row = t.row0 + 128 * static_cast<int>(rank);
                 // GEMM1: CTA 0 loads the gate rows, CTA 1 the up rows (f rows later);
                 // GEMM2: CTA r loads rows 128r..128r+127 of the 256-row column block
@@ -527,7 +567,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
             bool ok = true;
             bool issued = false;
-            for (int tile = pair; ok && tile < total_tiles; tile += npairs) {
+            for (int k = 0, tile = round_position(0, pair, npairs); ok && tile < total_tiles;
+                 ++k, tile = round_position(k, pair, npairs)) {
                 if (!mbar_wait<true>(&tempty[acc], acc_phase ^ 1u, s_abort, p.status, p.timeout_ns)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN_ACC;
@@ -561,8 +602,9 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
         uint32_t sbuf = 0;
         const uint32_t tempty0 = mapa_shared(smem_u32(&tempty[0]), 0);
         uint32_t acc = 0, acc_phase = 0;
-        for (int tile = pair; tile < total_tiles; tile += npairs) {
-            const Tile t = decode_tile<P_BM, P_BAND>(tile, s_pre, s_off, s_end, E, NT);
+        for (int k = 0, tile = round_position(0, pair, npairs); tile < total_tiles;
+             ++k, tile = round_position(k, pair, npairs)) {
+            const Tile t = decode_tile<P_BM, P_BAND>(visit_order(tile, total_tiles, mix), s_pre, s_off, s_end, E, NT);
             if (!mbar_wait<true>(&tfull[acc], acc_phase, s_abort, p.status, p.timeout_ns)) break;
             tc_fence_after();
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN_ACC;
