@@ -198,10 +198,14 @@ __device__ __forceinline__ int visit_order(int p, int N, int mix) {
 }
 
 // Position of round k for worker c of G: rounds cover consecutive blocks of
-// G positions, and the workers sweep them in alternating direction, so a
-// worker alternates between even and odd positions (the two ends of the list
-// under the interleaved order).
-__device__ __forceinline__ int round_position(int k, int c, int G) { return k * G + ((k & 1) ? G - 1 - c : c); }
+// G positions.  Under the interleaved order (mix) the workers sweep them in
+// alternating direction, so a worker alternates between even and odd
+// positions (the two ends of the list); otherwise every round keeps the same
+// direction, which keeps the tiles in flight at one time (and their shared
+// operands in L2) close together even when workers drift apart.
+__device__ __forceinline__ int round_position(int k, int c, int G, int mix) {
+    return k * G + ((mix && (k & 1)) ? G - 1 - c : c);
+}
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -358,8 +362,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             for (int i = 0; i < STAGES; ++i) armed_phase[i] = -1;
             uint32_t stage = 0, phase = 0;
             bool ok = true;
-            for (int k = 0, tile = round_position(0, blockIdx.x, gridDim.x); ok && tile < total_tiles;
-                 ++k, tile = round_position(k, blockIdx.x, gridDim.x)) {
+            for (int k = 0, tile = round_position(0, blockIdx.x, gridDim.x, mix); ok && tile < total_tiles;
+                 ++k, tile = round_position(k, blockIdx.x, gridDim.x, mix)) {
                 const Tile t = decode_tile<BM, BAND>(visit_order(tile, total_tiles, mix), s_pre, s_off, s_end, E, NT);
                 int brow0, brow1;
                 if (SWIGLU) {
@@ -395,8 +399,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
             bool ok = true;
             bool issued = false;
-            for (int k = 0, tile = round_position(0, blockIdx.x, gridDim.x); ok && tile < total_tiles;
-                 ++k, tile = round_position(k, blockIdx.x, gridDim.x)) {
+            for (int k = 0, tile = round_position(0, blockIdx.x, gridDim.x, mix); ok && tile < total_tiles;
+                 ++k, tile = round_position(k, blockIdx.x, gridDim.x, mix)) {
                 if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, s_abort, p.status, p.timeout_ns)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN_ACC;
@@ -431,8 +435,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         uint8_t *stage = smem + L1::OFF_EPI + (warp - 2) * 2 * EPI_BUF;
         uint32_t sbuf = 0;
         uint32_t acc = 0, acc_phase = 0;
-        for (int k = 0, tile = round_position(0, blockIdx.x, gridDim.x); tile < total_tiles;
-             ++k, tile = round_position(k, blockIdx.x, gridDim.x)) {
+        for (int k = 0, tile = round_position(0, blockIdx.x, gridDim.x, mix); tile < total_tiles;
+             ++k, tile = round_position(k, blockIdx.x, gridDim.x, mix)) {
             const Tile t = decode_tile<BM, BAND>(visit_order(tile, total_tiles, mix), s_pre, s_off, s_end, E, NT);
             if (!mbar_wait(&tfull[acc], acc_phase, s_abort, p.status, p.timeout_ns)) break;
             tc_fence_after();
@@ -528,8 +532,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
             for (int i = 0; i < P_STAGES; ++i) armed_phase[i] = -1;
             uint32_t stage = 0, phase = 0;
             bool ok = true;
-            for (int k = 0, tile = round_position(0, pair, npairs); ok && tile < total_tiles;
-                 ++k, tile = round_position(k, pair, npairs)) {
+            for (int k = 0, tile = round_position(0, pair, npairs, mix); ok && tile < total_tiles;
+                 ++k, tile = round_position(k, pair, npairs, mix)) {
                 const Tile t = decode_tile<P_BM, P_BAND>(visit_order(tile, total_tiles, mix), s_pre, s_off, s_end, E, NT);
                 const int a_row = t.row0 + 128 * static_cast<int>(rank);
                 // GEMM1: CTA 0 loads the gate rows, CTA 1 the up rows (f rows later);
@@ -567,8 +571,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
             bool ok = true;
             bool issued = false;
-            for (int k = 0, tile = round_position(0, pair, npairs); ok && tile < total_tiles;
-                 ++k, tile = round_position(k, pair, npairs)) {
+            for (int k = 0, tile = round_position(0, pair, npairs, mix); ok && tile < total_tiles;
+                 ++k, tile = round_position(k, pair, npairs, mix)) {
                 if (!mbar_wait<true>(&tempty[acc], acc_phase ^ 1u, s_abort, p.status, p.timeout_ns)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN_ACC;
@@ -602,8 +606,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
         uint32_t sbuf = 0;
         const uint32_t tempty0 = mapa_shared(smem_u32(&tempty[0]), 0);
         uint32_t acc = 0, acc_phase = 0;
-        for (int k = 0, tile = round_position(0, pair, npairs); tile < total_tiles;
-             ++k, tile = round_position(k, pair, npairs)) {
+        for (int k = 0, tile = round_position(0, pair, npairs, mix); tile < total_tiles;
+             ++k, tile = round_position(k, pair, npairs, mix)) {
             const Tile t = decode_tile<P_BM, P_BAND>(visit_order(tile, total_tiles, mix), s_pre, s_off, s_end, E, NT);
             if (!mbar_wait<true>(&tfull[acc], acc_phase, s_abort, p.status, p.timeout_ns)) break;
             tc_fence_after();
