@@ -250,7 +250,9 @@ __device__ __forceinline__ void epilogue_tile(const Params &p, const CUtensorMap
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-                tma_store_2d(tm_out, buf, col, wrow0);
+                // the output is not read again by this kernel: let L2 evict it
+                // before the operand tiles that other CTAs still share
+                tma_store_2d_evict_first(tm_out, buf, col, wrow0, l2_policy_evict_first());
                 bulk_commit();
             }
             sbuf ^= 1u;

@@ -111,6 +111,20 @@ __device__ __forceinline__ void tma_store_2d(const void *tmap, const void *src, 
                  "r"(smem_u32(src)), "r"(c_inner), "r"(c_outer)
                  : "memory");
 }
+// L2 policy that marks lines first in line for eviction.
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+// TMA store whose lines L2 evicts first (output that is not read again soon).
+__device__ __forceinline__ void tma_store_2d_evict_first(const void *tmap, const void *src, int c_inner, int c_outer,
+                                                         uint64_t policy) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%2, %3}], [%1], %4;" ::"l"(
+                     tmap),
+                 "r"(smem_u32(src)), "r"(c_inner), "r"(c_outer), "l"(policy)
+                 : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until at most N committed store groups still read shared memory.
 template <int N>
