@@ -267,6 +267,7 @@ def run_gpu(args):
     # kernel can be bracketed by events on the launching stream)
     logits = torch.empty((T, E), dtype=torch.float32, device=dev)
     route_ws = torch.empty((max(4, moe.route_workspace_size(T, E, K)),), dtype=torch.uint8, device=dev)
+    router_ws = torch.empty((moe.router_workspace_size(d, E),), dtype=torch.uint8, device=dev)
     i32 = dict(dtype=torch.int32, device=dev)
     topk_idx, row_of = torch.empty((T, K), **i32), torch.empty((T, K), **i32)
     topk_w = torch.empty((T, K), dtype=torch.float32, device=dev)
@@ -286,7 +287,7 @@ def run_gpu(args):
             if ev is not None:
                 ev[i].record(stream)
         rec(0)
-        st = L.moe_router_logits(P(x), P(w.Wr), bias_p, T, d, E, P(logits), sp)
+        st = L.moe_router_logits(P(x), P(w.Wr), bias_p, T, d, E, P(logits), P(router_ws), router_ws.numel(), sp)
         rec(1)
         st |= L.moe_route(P(logits), T, E, K, P(topk_idx), P(topk_w), P(counts), P(offsets), P(row_of),
                           P(src_tok), P(route_ws), route_ws.numel(), sp)
@@ -373,6 +374,8 @@ def run_gpu(args):
     for n, b in hbm_bytes.items():
         kernels[n]["GB/s"] = b / (kmean[n] * 1e-3) / 1e9
         kernels[n]["frac_of_hbm"] = kernels[n]["GB/s"] / float(peaks["hbm_gbs"])
+    # router: bf16 tensor-core work of the three-piece split, 3 x 2*T*d*E
+    kernels["router_logits"]["TFLOP/s"] = 6.0 * T * d * E / (kmean["router_logits"] * 1e-3) / 1e12
     for n in ("grouped_gemm1_swiglu", "grouped_gemm2"):
         fl = (4.0 if n == "grouped_gemm1_swiglu" else 2.0) * TK * d * f
         kernels[n]["TFLOP/s"] = fl / (kmean[n] * 1e-3) / 1e12

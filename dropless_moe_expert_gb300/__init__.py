@@ -19,7 +19,8 @@ import torch
 from . import build as _build
 
 __all__ = [
-    "MoEError", "lib", "router_logits", "route", "route_workspace_size", "permute", "grouped_mlp",
+    "MoEError", "lib", "router_logits", "router_workspace_size", "route", "route_workspace_size", "permute",
+    "grouped_mlp",
     "grouped_gemm1_swiglu", "grouped_gemm2", "unpermute", "forward", "forward_workspace_size",
     "forward_views", "forward_host", "device_status", "launch_count", "MoELayer",
 ]
@@ -39,7 +40,7 @@ class MoEError(RuntimeError):
 class _Layout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in (
         "logits", "topk_idx", "topk_w", "counts", "offsets", "row_of", "src_tok", "route_ws",
-        "x_perm", "h", "y_perm", "x_dev", "y_dev", "total")]
+        "router_ws", "x_perm", "h", "y_perm", "x_dev", "y_dev", "total")]
 
 
 def _load():
@@ -54,7 +55,8 @@ def _load():
         "moe_status_string": (ctypes.c_char_p, [I]),
         "moe_abi_version": (I, []),
         "moe_launch_count": (U64, []),
-        "moe_router_logits": (I, [P, P, P, I, I, I, P, P]),
+        "moe_router_workspace_size": (S, [I, I]),
+        "moe_router_logits": (I, [P, P, P, I, I, I, P, P, S, P]),
         "moe_route_workspace_size": (S, [I, I, I]),
         "moe_route": (I, [P, I, I, I, P, P, P, P, P, P, P, S, P]),
         "moe_permute": (I, [P, P, I, I, I, P, P]),
@@ -115,8 +117,13 @@ def _empty(shape, dtype, like):
 
 
 # ------------------------------------------------------------------ a0
-def router_logits(x, Wr, bias=None, out=None, stream=None):
-    """logits[T,E] fp32 = index-ordered FMA chain of x[t,:] . Wr[:,e], + bias[e]."""
+def router_workspace_size(d, E) -> int:
+    return int(lib.moe_router_workspace_size(d, E))
+
+
+def router_logits(x, Wr, bias=None, out=None, workspace=None, stream=None):
+    """logits[T,E] fp32 = x[t,:] . Wr[:,e] + bias[e]: exact products (Wr split
+    into three bf16 pieces) summed in fp32 on the tensor cores."""
     T, d = x.shape
     E = Wr.shape[1]
     _need(x, torch.bfloat16, (T, d), "x")
@@ -124,8 +131,13 @@ def router_logits(x, Wr, bias=None, out=None, stream=None):
     if bias is not None:
         _need(bias, torch.float32, (E,), "bias")
     out = _empty((T, E), torch.float32, x) if out is None else _need(out, torch.float32, (T, E), "logits")
-    _check(lib.moe_router_logits(_ptr(x), _ptr(Wr), _ptr(bias), T, d, E, _ptr(out), _stream(stream)),
-           "moe_router_logits")
+    nbytes = router_workspace_size(d, E)
+    if nbytes == 0:
+        raise MoEError(2, "moe_router_workspace_size")
+    if workspace is None:
+        workspace = _empty((nbytes,), torch.uint8, x)
+    _check(lib.moe_router_logits(_ptr(x), _ptr(Wr), _ptr(bias), T, d, E, _ptr(out), _ptr(workspace),
+                                 workspace.numel(), _stream(stream)), "moe_router_logits")
     return out
 
 
@@ -254,7 +266,7 @@ def _weights_check(x, Wr, bias, W1, W2, K):
 
 
 def forward(x, Wr, bias, W1, W2, K: int, out=None, workspace=None, stream=None):
-    """The whole layer in one C-ABI call (8 kernel launches, no host sync)."""
+    """The whole layer in one C-ABI call (9 kernel launches, no host sync)."""
     T, d, E, f = _weights_check(x, Wr, bias, W1, W2, K)
     _need(x, torch.bfloat16, (T, d), "x")
     nbytes = forward_workspace_size(T, d, E, K, f)

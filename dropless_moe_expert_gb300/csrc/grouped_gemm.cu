@@ -42,12 +42,11 @@
 // the ring holds 6 stages.  The even CTA issues the MMAs; both CTAs' copies
 // signal its full barrier, its commits free both CTAs' stages, and both CTAs'
 // epilogues release its accumulator.
-#include <cudaTypedefs.h>
-
 #include <algorithm>
 
 #include "kernels.h"
 #include "ptx.cuh"
+#include "tmap.h"
 
 namespace moe {
 namespace gg {
@@ -641,38 +640,6 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
 // ------------------------------------------------------------------ host side
 namespace {
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    }
-    return fn;
-}
-
-// 2D bf16 row-major [rows, cols] with a (box_rows x box_cols) box: operand
-// loads use 64-column boxes with 128-byte swizzle, the epilogue's stores
-// 32 x 32 boxes with 64-byte swizzle.
-bool make_tmap(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows,
-               uint32_t box_cols = gg::BK, CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
-    auto fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[2] = {cols, rows};
-    cuuint64_t strides[1] = {cols * 2};
-    cuuint32_t box[2] = {box_cols, box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
-
 template <bool SWIGLU>
 cudaError_t launch_pair(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmOut,
                         const gg::Params &p, int grid, cudaStream_t stream) {
@@ -721,9 +688,9 @@ cudaError_t launch_grouped_gemm(bool swiglu, const void *A, int TK, int Kdim, co
                                 uint64_t timeout_ns, cudaStream_t stream) {
     CUtensorMap tmA, tmB;
     const int w_rows = swiglu ? 2 * n_out : n_out;
-    if (!make_tmap(&tmA, A, static_cast<uint64_t>(TK), static_cast<uint64_t>(Kdim), gg::BOX_ROWS))
+    if (!make_tmap(&tmA, A, static_cast<uint64_t>(TK), static_cast<uint64_t>(Kdim), gg::BOX_ROWS, gg::BK))
         return cudaErrorInvalidValue;
-    if (!make_tmap(&tmB, W, static_cast<uint64_t>(E) * w_rows, static_cast<uint64_t>(Kdim), gg::BOX_ROWS))
+    if (!make_tmap(&tmB, W, static_cast<uint64_t>(E) * w_rows, static_cast<uint64_t>(Kdim), gg::BOX_ROWS, gg::BK))
         return cudaErrorInvalidValue;
     CUtensorMap tmOut;
     if (!make_tmap(&tmOut, out, static_cast<uint64_t>(TK), static_cast<uint64_t>(n_out), 32, 32,

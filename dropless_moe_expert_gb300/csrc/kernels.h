@@ -17,8 +17,16 @@ inline size_t route_workspace_bytes(int T, int E) {
     return static_cast<size_t>(route_num_chunks(T)) * static_cast<size_t>(E) * 2 * sizeof(int32_t);
 }
 
+// Router: the exact three-piece bf16 split of Wr [3][E][d] lives in caller
+// scratch of router_workspace_bytes(d, E) bytes (16-byte aligned).
+size_t router_workspace_bytes(int d, int E);
+// Kernel attributes; once per device, before any capture.
+cudaError_t router_setup();
+// Width (experts) of one router tile for this shape: 32, 64 or 128.
+int router_tile_n(int T, int E);
 cudaError_t launch_router_logits(const uint16_t *x, const float *Wr, const float *bias, int T, int d, int E,
-                                 float *logits, cudaStream_t stream);
+                                 float *logits, void *workspace, int *status, uint64_t timeout_ns,
+                                 cudaStream_t stream);
 
 cudaError_t launch_route(const float *logits, int T, int E, int K, int32_t *topk_idx, float *topk_w,
                          int32_t *counts, int32_t *offsets, int32_t *row_of, int32_t *src_tok, int32_t *workspace,

@@ -42,6 +42,7 @@ moe_status_t device_state(DeviceState **out) {
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
         if (major != 10) return MOE_ERR_UNSUPPORTED;  // built for sm_103a only
         if (moe::grouped_gemm_setup(s.num_sms, &s.gemm) != cudaSuccess) return MOE_ERR_CUDA;
+        if (moe::router_setup() != cudaSuccess) return MOE_ERR_CUDA;
         if (cudaGetSymbolAddress(reinterpret_cast<void **>(&s.status), g_device_status) != cudaSuccess)
             return MOE_ERR_CUDA;
         s.ready = true;
@@ -83,6 +84,7 @@ bool forward_layout(int T, int d, int E, int K, int f, moe_forward_layout_t *L) 
     L->row_of = take(TK * 4);
     L->src_tok = take(TK * 4);
     L->route_ws = take(moe::route_workspace_bytes(T, E));
+    L->router_ws = take(moe::router_workspace_bytes(d, E));
     L->x_perm = take(TK * d * 2);
     L->h = take(TK * f * 2);
     L->y_perm = take(TK * d * 2);
@@ -120,19 +122,30 @@ const char *moe_status_string(int status) {
     }
 }
 
-int moe_abi_version(void) { return 100; }
+int moe_abi_version(void) { return 200; }
 
 uint64_t moe_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
+size_t moe_router_workspace_size(int d, int E) {
+    if (d < 64 || d % 64 != 0 || E < 1 || E > kMaxE) return 0;
+    return moe::router_workspace_bytes(d, E);
+}
+
 moe_status_t moe_router_logits(const uint16_t *x, const float *Wr, const float *bias, int T, int d, int E,
-                               float *logits, cudaStream_t stream) {
-    if (!x || !Wr || !logits) return MOE_ERR_INVALID_ARG;
-    if (!aligned(x, 16) || !aligned(Wr, 4) || !aligned(logits, 4) || (bias && !aligned(bias, 4)))
+                               float *logits, void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    if (!x || !Wr || !logits || !workspace) return MOE_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(Wr, 4) || !aligned(logits, 4) || (bias && !aligned(bias, 4)) ||
+        !aligned(workspace, 16))
         return MOE_ERR_INVALID_ARG;
     moe_status_t st = check_shape(T, d, E, 1, 64, true, false);
     if (st != MOE_OK) return st;
-    g_launches.fetch_add(1, std::memory_order_relaxed);
-    return cuda_status(moe::launch_router_logits(x, Wr, bias, T, d, E, logits, stream));
+    if (static_cast<int64_t>(E) * d >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
+    if (workspace_bytes < moe::router_workspace_bytes(d, E)) return MOE_ERR_WORKSPACE;
+    DeviceState *ds = nullptr;
+    if ((st = device_state(&ds)) != MOE_OK) return st;
+    g_launches.fetch_add(2, std::memory_order_relaxed);
+    return cuda_status(
+        moe::launch_router_logits(x, Wr, bias, T, d, E, logits, workspace, ds->status, kWaitLimitNs, stream));
 }
 
 size_t moe_route_workspace_size(int T, int E, int K) {
@@ -246,9 +259,11 @@ moe_status_t moe_forward(const uint16_t *x, const float *Wr, const float *bias, 
     uint16_t *x_perm = static_cast<uint16_t *>(at(L.x_perm));
     uint16_t *h = static_cast<uint16_t *>(at(L.h));
     uint16_t *y_perm = static_cast<uint16_t *>(at(L.y_perm));
-    if ((st = moe_router_logits(x, Wr, bias, T, d, E, logits, stream)) != MOE_OK) return st;
+    if ((st = moe_router_logits(x, Wr, bias, T, d, E, logits, at(L.router_ws), L.x_perm - L.router_ws,
+                                stream)) != MOE_OK)
+        return st;
     if ((st = moe_route(logits, T, E, K, idx, w, counts, offsets, row_of, src_tok, at(L.route_ws),
-                        L.x_perm - L.route_ws, stream)) != MOE_OK)
+                        L.router_ws - L.route_ws, stream)) != MOE_OK)
         return st;
     if ((st = moe_permute(x, row_of, T, K, d, x_perm, stream)) != MOE_OK) return st;
     if ((st = moe_grouped_mlp(x_perm, offsets, E, TK, d, f, W1, W2, h, y_perm, stream)) != MOE_OK) return st;

@@ -1,254 +1,323 @@
-// Step a0: router logits, strict fp32 on the CUDA cores.
+// Step a0: router logits on the tensor cores, with fp32-exact products.
 //
 // Introduction of "Accelerating dropless MoE training in JAX with NVIDIA
 // Transformer Engine": a learned router scores the experts of every token and
-// activates the Top-K.  The score is the fp32 dot product of the token (bf16,
-// converted exactly) with the expert's router column, accumulated in index
-// order with one fused multiply-add per term, plus the expert's bias added
-// once at the end.  Every output is one sequential FMA chain, so the logits
-// are bit-reproducible, and the routing decisions taken on them are too.
+// activates the Top-K.  The score is the fp32 dot product of the token with
+// the expert's router column, plus the expert's bias:
+//     L[t, e] = sum_i x[t, i] * Wr[i, e] + bias[e]
+// with x bf16 and Wr, bias and L fp32.
 //
-// Two kernels: one for few experts (one chain per thread) and a register-tiled
-// SIMT GEMM for many experts; both walk the reduction in index order.
+// Exact split of the fp32 weights.  Every fp32 value w is the exact sum of
+// three bf16 values, w = hi + mid + lo, with hi = bf16(w), mid = bf16(w - hi),
+// lo = bf16(w - hi - mid): each difference is exact in fp32 (the operands are
+// within a factor of two), the first residual has at most 16 significant bits
+// and the second at most 8, so lo takes it without rounding.  A bf16 x bf16
+// product has at most 16 significant bits, so it is exact in fp32.  Hence
+//     L[t, e] = sum_p sum_i x[t, i] * Wp[e, i],   p in {hi, mid, lo},
+// is one bf16 contraction of depth 3d with exact products and fp32
+// accumulation: the same operands and precision as the fp32 dot product,
+// summed in the tensor core's order instead of index order.  The result is
+// deterministic (fixed tile shapes, no atomics, no split reduction).
+//
+// Two kernels:
+//   router_split_kernel : Wr [d, E] fp32 -> Ws [3][E][d] bf16 (hi, mid, lo,
+//                         each K-major, i.e. transposed) in caller scratch;
+//   router_gemm_kernel  : one 128-token x BN-expert tile per CTA; per 64-wide
+//                         K slice TMA brings the x tile and the three weight
+//                         pieces' tiles (128-byte swizzle), one thread issues
+//                         3 x 4 tcgen05.mma (M=128, N=BN, K=16) into one fp32
+//                         TMEM accumulator, and four warps add the bias and
+//                         store fp32 rows.  Expert rows past E and token rows
+//                         past T come from TMA zero fill and are not stored.
 #include "kernels.h"
+#include "ptx.cuh"
+#include "tmap.h"
 
 #include <cuda_bf16.h>
 
 namespace moe {
-namespace rl {
+namespace rt {
 
-// Many experts: register-tiled SIMT GEMM.  A CTA of NTH = (BE/TN)*(BT/TM)
-// threads owns BT tokens x BE experts, each thread TM tokens x TN experts
-// (TM x TN independent FMA chains).  The reduction walks 64-wide chunks
-// staged in shared memory: x transposed to [k][token] as fp32 (consecutive
-// lanes write consecutive tokens: no bank conflicts), Wr as [k][expert].  The
-// next chunk is loaded into registers while the current one is consumed.
-// Per k a warp reads TM/4 + 1 float4 per lane from shared memory for TM*TN
-// FMAs, which keeps the FMA pipe, not the shared-memory pipe, the limit.
-template <int BE, int BT, int TM, int TN>
-__global__ void __launch_bounds__((BE / TN) * (BT / TM))
-router_logits_kernel(const uint16_t *__restrict__ x, const float *__restrict__ Wr, const float *__restrict__ bias,
-                     int T, int d, int E, float *__restrict__ L) {
-    constexpr int BK = 64;
-    constexpr int GX = BE / TN;
-    constexpr int GY = BT / TM;
-    constexpr int NTH = GX * GY;
-    constexpr int XPAD = BT + 4;
-    constexpr int XV = (BT * BK / 8 + NTH - 1) / NTH;   // 16-byte x vectors per thread per chunk
-    constexpr int WV4 = (BK * BE / 4 + NTH - 1) / NTH;  // float4 of Wr per thread per chunk
-    static_assert(TM % 4 == 0 && TN == 4, "float4 fragments");
-    __shared__ __align__(16) float xs[BK][XPAD];
-    __shared__ __align__(16) float ws[BK][BE];
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int UMMA_K = 16;
+constexpr int THREADS = 128;
+constexpr int A_BYTES = BM * BK * 2;
 
-    const int tid = threadIdx.x;
-    const int tx = tid % GX;
-    const int ty = tid / GX;
-    const int t0 = blockIdx.x * BT;
-    const int e0 = blockIdx.y * BE;
-    const bool w_vec = (E % 4) == 0;  // Wr rows are 16-byte aligned: float4 loads
+template <int BN>
+struct Cfg {
+    static constexpr int B_PIECE = BN * BK * 2;
+    static constexpr int STAGE = A_BYTES + 3 * B_PIECE;
+    static constexpr int STAGES = (200 * 1024) / STAGE < 8 ? (200 * 1024) / STAGE : 8;
+    static constexpr int OFF_BARS = STAGES * STAGE;  // whole KBs: tiles stay 1024-aligned
+    static constexpr int NUM_BARS = 2 * STAGES + 2;  // full, empty, accumulator full, drain
+    static constexpr int OFF_TMEM = OFF_BARS + NUM_BARS * 8;
+    static constexpr int OFF_ABORT = OFF_TMEM + 4;
+    static constexpr int BYTES = OFF_ABORT + 4 + 1024;  // slack for 1024-byte alignment
+    static constexpr int TMEM_COLS = BN;                // a power of two >= 32
+    static_assert(BN == 32 || BN == 64 || BN == 128, "accumulator width");
+    static_assert(STAGES >= 2 && BYTES <= 227 * 1024, "shared memory budget");
+    static_assert(B_PIECE % 1024 == 0, "swizzled tiles must stay 1024-byte aligned");
+};
 
-    uint4 xr[XV];
-    float4 wr[WV4];
-    auto load_chunk = [&](int k0) {
-#pragma unroll
-        for (int i = 0; i < XV; ++i) {
-            const int v = tid + i * NTH;
-            const int tl = v % BT, kv = (v / BT) * 8;
-            const int t = t0 + tl;
-            xr[i] = (v < BT * (BK / 8) && t < T)
-                        ? *reinterpret_cast<const uint4 *>(x + static_cast<size_t>(t) * d + k0 + kv)
-                        : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int i = 0; i < WV4; ++i) {
-            const int v = tid + i * NTH;
-            const int kk = v / (BE / 4), e = e0 + (v % (BE / 4)) * 4;
-            float4 w = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (v < BK * BE / 4) {
-                const float *row = Wr + static_cast<size_t>(k0 + kk) * E;
-                if (w_vec && e + 3 < E) {
-                    w = *reinterpret_cast<const float4 *>(row + e);
-                } else {
-                    if (e < E) w.x = row[e];
-                    if (e + 1 < E) w.y = row[e + 1];
-                    if (e + 2 < E) w.z = row[e + 2];
-                    if (e + 3 < E) w.w = row[e + 3];
-                }
-            }
-            wr[i] = w;
-        }
-    };
+struct Params {
+    int T, d, E, NT;         // NT: expert tiles per token tile
+    const float *bias;       // [E] or null
+    float *L;                // [T, E]
+    int vec4;                // rows of L are 16-byte aligned (E % 4 == 0 and L aligned)
+    int *status;
+    uint64_t timeout_ns;
+};
 
-    float acc[TM][TN];
-#pragma unroll
-    for (int i = 0; i < TM; ++i)
-#pragma unroll
-        for (int j = 0; j < TN; ++j) acc[i][j] = 0.0f;
-
-    load_chunk(0);
-    for (int k0 = 0; k0 < d; k0 += BK) {
-#pragma unroll
-        for (int i = 0; i < XV; ++i) {
-            const int v = tid + i * NTH;
-            if (v < BT * (BK / 8)) {
-                const int tl = v % BT, kv = (v / BT) * 8;
-                const uint32_t w4[4] = {xr[i].x, xr[i].y, xr[i].z, xr[i].w};
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    xs[kv + 2 * q][tl] = __uint_as_float(w4[q] << 16);
-                    xs[kv + 2 * q + 1][tl] = __uint_as_float(w4[q] & 0xffff0000u);
-                }
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < WV4; ++i) {
-            const int v = tid + i * NTH;
-            if (v < BK * BE / 4) *reinterpret_cast<float4 *>(&ws[v / (BE / 4)][(v % (BE / 4)) * 4]) = wr[i];
-        }
-        __syncthreads();
-        if (k0 + BK < d) load_chunk(k0 + BK);  // in flight during this chunk's FMAs
-#pragma unroll 8
-        for (int kk = 0; kk < BK; ++kk) {
-            float a[TM];
-#pragma unroll
-            for (int i = 0; i < TM; i += 4) {
-                const float4 a4 = *reinterpret_cast<const float4 *>(&xs[kk][ty * TM + i]);
-                a[i] = a4.x; a[i + 1] = a4.y; a[i + 2] = a4.z; a[i + 3] = a4.w;
-            }
-            const float4 b4 = *reinterpret_cast<const float4 *>(&ws[kk][tx * TN]);
-            const float b[4] = {b4.x, b4.y, b4.z, b4.w};
-#pragma unroll
-            for (int i = 0; i < TM; ++i)
-#pragma unroll
-                for (int j = 0; j < TN; ++j) acc[i][j] = __fmaf_rn(a[i], b[j], acc[i][j]);
-        }
-        __syncthreads();
-    }
-
-#pragma unroll
-    for (int i = 0; i < TM; ++i) {
-        const int t = t0 + ty * TM + i;
-        if (t >= T) continue;
-#pragma unroll
-        for (int j = 0; j < TN; ++j) {
-            const int e = e0 + tx * TN + j;
-            if (e >= E) continue;
-            const float v = bias ? __fadd_rn(acc[i][j], bias[e]) : acc[i][j];
-            L[static_cast<size_t>(t) * E + e] = v;
-        }
-    }
-}
-
-// Few experts (E <= 16): one thread per (token, expert) pair, so there are
-// T*E chains in flight instead of T*E/16; EP lanes of a warp share one token.
-// Each 128-wide reduction chunk is staged in shared memory as fp32 (x once per
-// token, Wr transposed to [expert][k]) while the next chunk is already being
-// loaded into registers.
-template <int EP>
+// Wr [d, E] fp32 -> Ws[p][e][k] bf16, p = 0 (hi), 1 (mid), 2 (lo); 32 x 32
+// tiles transposed through shared memory.
 __global__ void __launch_bounds__(256)
-router_logits_small_e_kernel(const uint16_t *__restrict__ x, const float *__restrict__ Wr,
-                             const float *__restrict__ bias, int T, int d, int E, float *__restrict__ L) {
-    constexpr int SK = 128;               // reduction chunk
-    constexpr int TPW = 32 / EP;          // tokens per warp
-    constexpr int TPC = 8 * TPW;          // tokens per CTA
-    constexpr int XV = TPC * SK / 8 / 256; // 16-byte x vectors per thread per chunk
-    constexpr int WV = SK * EP / 256;      // Wr values per thread per chunk
-    static_assert(XV >= 1 && WV >= 1, "tile does not cover the CTA");
-    __shared__ __align__(16) float xs[TPC][SK + 4];
-    __shared__ __align__(16) float ws[EP][SK + 4];
-
-    const int tid = threadIdx.x;
-    const int lane = tid & 31;
-    const int tl = (tid >> 5) * TPW + lane / EP;
-    const int e = lane % EP;
-    const int t0 = blockIdx.x * TPC;
-
-    uint4 xr[XV];
-    float wr[WV];
-    auto load_chunk = [&](int k0) {
+router_split_kernel(const float *__restrict__ Wr, int d, int E, __nv_bfloat16 *__restrict__ Ws) {
+    __shared__ float tile[32][33];
+    const int k0 = blockIdx.x * 32, e0 = blockIdx.y * 32;
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
 #pragma unroll
-        for (int i = 0; i < XV; ++i) {
-            const int v = tid + i * 256;
-            const int r = v / (SK / 8), c = (v % (SK / 8)) * 8;
-            const int t = t0 + r;
-            xr[i] = (t < T) ? *reinterpret_cast<const uint4 *>(x + static_cast<size_t>(t) * d + k0 + c)
-                            : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int i = 0; i < WV; ++i) {
-            const int v = tid + i * 256;
-            const int kk = v / EP, ee = v % EP;
-            wr[i] = (ee < E) ? Wr[static_cast<size_t>(k0 + kk) * E + ee] : 0.0f;
-        }
-    };
-
-    float acc = 0.0f;
-    load_chunk(0);
-    for (int k0 = 0; k0 < d; k0 += SK) {
-#pragma unroll
-        for (int i = 0; i < XV; ++i) {
-            const int v = tid + i * 256;
-            const int r = v / (SK / 8), c = (v % (SK / 8)) * 8;
-            const uint32_t w4[4] = {xr[i].x, xr[i].y, xr[i].z, xr[i].w};
-            float4 lo, hi;
-            lo.x = __uint_as_float(w4[0] << 16); lo.y = __uint_as_float(w4[0] & 0xffff0000u);
-            lo.z = __uint_as_float(w4[1] << 16); lo.w = __uint_as_float(w4[1] & 0xffff0000u);
-            hi.x = __uint_as_float(w4[2] << 16); hi.y = __uint_as_float(w4[2] & 0xffff0000u);
-            hi.z = __uint_as_float(w4[3] << 16); hi.w = __uint_as_float(w4[3] & 0xffff0000u);
-            *reinterpret_cast<float4 *>(&xs[r][c]) = lo;
-            *reinterpret_cast<float4 *>(&xs[r][c + 4]) = hi;
-        }
-#pragma unroll
-        for (int i = 0; i < WV; ++i) {
-            const int v = tid + i * 256;
-            ws[v % EP][v / EP] = wr[i];
-        }
-        __syncthreads();
-        if (k0 + SK < d) load_chunk(k0 + SK);  // in flight during this chunk's FMAs
-#pragma unroll
-        for (int kk = 0; kk < SK; kk += 4) {
-            const float4 a = *reinterpret_cast<const float4 *>(&xs[tl][kk]);
-            const float4 b = *reinterpret_cast<const float4 *>(&ws[e][kk]);
-            acc = __fmaf_rn(a.x, b.x, acc);
-            acc = __fmaf_rn(a.y, b.y, acc);
-            acc = __fmaf_rn(a.z, b.z, acc);
-            acc = __fmaf_rn(a.w, b.w, acc);
-        }
-        __syncthreads();
+    for (int r = ty; r < 32; r += 8) {
+        const int k = k0 + r, e = e0 + tx;
+        tile[r][tx] = (k < d && e < E) ? Wr[static_cast<size_t>(k) * E + e] : 0.0f;
     }
-    const int t = t0 + tl;
-    if (t < T && e < E) L[static_cast<size_t>(t) * E + e] = bias ? __fadd_rn(acc, bias[e]) : acc;
+    __syncthreads();
+    const size_t piece = static_cast<size_t>(E) * d;
+#pragma unroll
+    for (int r = ty; r < 32; r += 8) {
+        const int e = e0 + r, k = k0 + tx;
+        if (e >= E || k >= d) continue;
+        const float w = tile[tx][r];
+        const __nv_bfloat16 hi = __float2bfloat16_rn(w);
+        const float r1 = w - __bfloat162float(hi);
+        const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+        const float r2 = r1 - __bfloat162float(mid);
+        const __nv_bfloat16 lo = __float2bfloat16_rn(r2);
+        const size_t o = static_cast<size_t>(e) * d + k;
+        Ws[o] = hi;
+        Ws[piece + o] = mid;
+        Ws[2 * piece + o] = lo;
+    }
 }
 
-template <int EP>
-cudaError_t launch_small_e(const uint16_t *x, const float *Wr, const float *bias, int T, int d, int E, float *L,
-                           cudaStream_t s) {
-    constexpr int TPC = 8 * (32 / EP);
-    router_logits_small_e_kernel<EP><<<(T + TPC - 1) / TPC, 256, 0, s>>>(x, Wr, bias, T, d, E, L);
+template <int BN>
+__global__ void __launch_bounds__(THREADS, 1)
+router_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW0,
+                   const __grid_constant__ CUtensorMap tmW1, const __grid_constant__ CUtensorMap tmW2,
+                   const Params p) {
+    using C = Cfg<BN>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BARS);
+    uint64_t *full = bars;
+    uint64_t *empty = bars + C::STAGES;
+    uint64_t *accfull = bars + 2 * C::STAGES;
+    uint64_t *drain = accfull + 1;
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(smem + C::OFF_TMEM);
+    volatile int *s_abort = reinterpret_cast<volatile int *>(smem + C::OFF_ABORT);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int n_blk = blockIdx.x % p.NT;
+    const int m_blk = blockIdx.x / p.NT;  // expert tiles of one token tile are neighbours: x tile shared in L2
+    const int n0 = n_blk * BN;
+    const int m0 = m_blk * BM;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < C::STAGES; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        mbar_init(accfull, 1);
+        mbar_init(drain, 1);
+        *s_abort = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmX);
+        tma_prefetch_desc(&tmW0);
+        tma_prefetch_desc(&tmW1);
+        tma_prefetch_desc(&tmW2);
+    }
+    if (warp == 1) {
+        tmem_alloc(s_tmem, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *s_tmem;
+    const int KB = p.d / BK;
+    bool committed = false;  // MMA thread: the accumulator commit was issued
+
+    if (warp == 0 && lane == 0) {
+        // TMA producer
+        int armed_phase[C::STAGES];
+#pragma unroll
+        for (int i = 0; i < C::STAGES; ++i) armed_phase[i] = -1;
+        uint32_t stage = 0, phase = 0;
+        bool ok = true;
+        for (int kb = 0; kb < KB; ++kb) {
+            if (!mbar_wait(&empty[stage], phase ^ 1u, s_abort, p.status, p.timeout_ns)) { ok = false; break; }
+            uint8_t *sa = smem + stage * C::STAGE;
+            uint8_t *sb = sa + A_BYTES;
+            mbar_arrive_expect_tx(&full[stage], C::STAGE);
+            tma_load_2d(sa, &tmX, &full[stage], kb * BK, m0);
+            tma_load_2d(sb, &tmW0, &full[stage], kb * BK, n0);
+            tma_load_2d(sb + C::B_PIECE, &tmW1, &full[stage], kb * BK, n0);
+            tma_load_2d(sb + 2 * C::B_PIECE, &tmW2, &full[stage], kb * BK, n0);
+            armed_phase[stage] = static_cast<int>(phase);
+            if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) {
+            // every armed stage completes once its bytes have landed
+            volatile int no_abort = 0;
+            for (int i = 0; i < C::STAGES; ++i)
+                if (armed_phase[i] >= 0)
+                    mbar_wait(&full[i], static_cast<uint32_t>(armed_phase[i]), &no_abort, p.status, p.timeout_ns);
+        }
+    } else if (warp == 1 && lane == 0) {
+        // MMA issuer: per K slice, the hi, mid and lo pieces in turn
+        constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+        uint32_t stage = 0, phase = 0;
+        bool ok = true, issued = false;
+        for (int kb = 0; kb < KB; ++kb) {
+            if (!mbar_wait(&full[stage], phase, s_abort, p.status, p.timeout_ns)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t sa = smem_u32(smem + stage * C::STAGE);
+            const uint64_t adesc = smem_desc_kmajor_sw128(sa);
+#pragma unroll
+            for (int pc = 0; pc < 3; ++pc) {
+                const uint64_t bdesc = smem_desc_kmajor_sw128(sa + A_BYTES + pc * C::B_PIECE);
+#pragma unroll
+                for (int j = 0; j < BK / UMMA_K; ++j)
+                    umma_bf16(tmem_base, adesc + 2 * j, bdesc + 2 * j, idesc, (kb | pc | j) != 0);
+            }
+            issued = true;
+            umma_commit(&empty[stage]);
+            if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+        }
+        committed = ok;
+        if (ok) {
+            umma_commit(accfull);
+        } else if (issued) {
+            volatile int no_abort = 0;
+            umma_commit(drain);
+            mbar_wait(drain, 0, &no_abort, p.status, p.timeout_ns);
+        }
+    }
+    __syncwarp();
+
+    // epilogue: warp w owns TMEM lanes 32w..32w+31 = token rows m0+32w..
+    const bool acc_ready = __all_sync(0xffffffffu, mbar_wait(accfull, 0, s_abort, p.status, p.timeout_ns));
+    tc_fence_after();
+    if (acc_ready) {
+        const int row = m0 + warp * 32 + lane;
+        const uint32_t tbase = tmem_base + (static_cast<uint32_t>(warp * 32) << 16);
+        float *Lrow = p.L + static_cast<size_t>(row) * p.E;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(tbase + c, v);
+            tmem_ld_wait();
+            const int e0 = n0 + c;
+            if (row < p.T && e0 < p.E) {
+            float o[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const int e = e0 + i;
+                const float a = __uint_as_float(v[i]);
+                o[i] = (p.bias && e < p.E) ? __fadd_rn(a, p.bias[e]) : a;
+            }
+            if (p.vec4) {
+#pragma unroll
+                for (int i = 0; i < 32; i += 4)
+                    if (e0 + i < p.E) *reinterpret_cast<float4 *>(Lrow + e0 + i) = make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    if (e0 + i < p.E) Lrow[e0 + i] = o[i];
+            }
+            }
+            __syncwarp();  // converged before the next tcgen05.ld
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        if (lane == 0 && committed && !acc_ready) {
+            // the epilogue gave up: the MMAs still finish before TMEM is freed
+            volatile int no_abort = 0;
+            mbar_wait(accfull, 0, &no_abort, p.status, p.timeout_ns);
+        }
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
+}
+
+template <int BN>
+cudaError_t launch_gemm(const CUtensorMap &tmX, const CUtensorMap (&tmW)[3], const Params &p, int tiles,
+                        cudaStream_t s) {
+    router_gemm_kernel<BN><<<tiles, THREADS, Cfg<BN>::BYTES, s>>>(tmX, tmW[0], tmW[1], tmW[2], p);
     return cudaGetLastError();
 }
 
-template <int BE, int BT, int TM, int TN>
-cudaError_t launch(const uint16_t *x, const float *Wr, const float *bias, int T, int d, int E, float *L,
-                   cudaStream_t s) {
-    dim3 grid((T + BT - 1) / BT, (E + BE - 1) / BE);
-    router_logits_kernel<BE, BT, TM, TN><<<grid, (BE / TN) * (BT / TM), 0, s>>>(x, Wr, bias, T, d, E, L);
-    return cudaGetLastError();
+}  // namespace rt
+
+size_t router_workspace_bytes(int d, int E) { return static_cast<size_t>(3) * E * d * 2; }
+
+int router_tile_n(int T, int E) {
+    // widest accumulator that still gives about one wave of tiles
+    const int mt = (T + rt::BM - 1) / rt::BM;
+    int bn = E <= 32 ? 32 : (E <= 64 ? 64 : 128);
+    while (bn > 32 && static_cast<int64_t>(mt) * ((E + bn - 1) / bn) < 120) bn /= 2;
+    return bn;
 }
 
-}  // namespace rl
+cudaError_t router_setup() {
+    cudaError_t e;
+    if ((e = cudaFuncSetAttribute(rt::router_gemm_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  rt::Cfg<32>::BYTES)) != cudaSuccess)
+        return e;
+    if ((e = cudaFuncSetAttribute(rt::router_gemm_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  rt::Cfg<64>::BYTES)) != cudaSuccess)
+        return e;
+    return cudaFuncSetAttribute(rt::router_gemm_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                rt::Cfg<128>::BYTES);
+}
 
 cudaError_t launch_router_logits(const uint16_t *x, const float *Wr, const float *bias, int T, int d, int E,
-                                 float *logits, cudaStream_t stream) {
-    // d is a multiple of 64 (checked by the caller); the small-E kernel walks
-    // the reduction in 128-wide chunks
-    if (d % 128 == 0) {
-        if (E <= 8) return rl::launch_small_e<8>(x, Wr, bias, T, d, E, logits, stream);
-        if (E <= 16) return rl::launch_small_e<16>(x, Wr, bias, T, d, E, logits, stream);
+                                 float *logits, void *workspace, int *status, uint64_t timeout_ns,
+                                 cudaStream_t stream) {
+    __nv_bfloat16 *Ws = static_cast<__nv_bfloat16 *>(workspace);
+    rt::router_split_kernel<<<dim3((d + 31) / 32, (E + 31) / 32), 256, 0, stream>>>(Wr, d, E, Ws);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+
+    const int bn = router_tile_n(T, E);
+    CUtensorMap tmX, tmW[3];
+    if (!make_tmap(&tmX, x, static_cast<uint64_t>(T), static_cast<uint64_t>(d), rt::BM, rt::BK))
+        return cudaErrorInvalidValue;
+    const size_t piece = static_cast<size_t>(E) * d;
+    for (int pc = 0; pc < 3; ++pc)
+        if (!make_tmap(&tmW[pc], Ws + pc * piece, static_cast<uint64_t>(E), static_cast<uint64_t>(d),
+                       static_cast<uint32_t>(bn), rt::BK))
+            return cudaErrorInvalidValue;
+    rt::Params p;
+    p.T = T;
+    p.d = d;
+    p.E = E;
+    p.NT = (E + bn - 1) / bn;
+    p.bias = bias;
+    p.L = logits;
+    p.vec4 = (E % 4 == 0) && (reinterpret_cast<uintptr_t>(logits) % 16 == 0);
+    p.status = status;
+    p.timeout_ns = timeout_ns;
+    const int tiles = ((T + rt::BM - 1) / rt::BM) * p.NT;
+    switch (bn) {
+        case 32: return rt::launch_gemm<32>(tmX, tmW, p, tiles, stream);
+        case 64: return rt::launch_gemm<64>(tmX, tmW, p, tiles, stream);
+        default: return rt::launch_gemm<128>(tmX, tmW, p, tiles, stream);
     }
-    if (E <= 16) return rl::launch<16, 64, 4, 4>(x, Wr, bias, T, d, E, logits, stream);
-    if (E <= 32) return rl::launch<32, 64, 8, 4>(x, Wr, bias, T, d, E, logits, stream);
-    return rl::launch<64, 64, 8, 4>(x, Wr, bias, T, d, E, logits, stream);
 }
 
 }  // namespace moe

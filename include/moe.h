@@ -79,11 +79,19 @@ const char *moe_status_string(int status);
 int moe_abi_version(void);
 
 /* Step a0 -- router logits (introduction: the learned router).
- * logits[t,e] = fp32 dot product of x[t,:] and Wr[:,e], accumulated in index
- * order with one fused multiply-add per term, then + bias[e] (if bias is not
- * NULL).  That order makes the logits bit-reproducible.  */
+ * logits[t,e] = fp32 dot product of x[t,:] and Wr[:,e], + bias[e] (if bias
+ * is not NULL).  Computed on the tensor cores with exact products: Wr is
+ * split exactly into three bf16 pieces (hi + mid + lo == Wr), every
+ * bf16 x bf16 product is exact in fp32, and the 3d products are summed in
+ * fp32 in the tensor core's order (not index order).  The logits are
+ * deterministic for a given shape and device, and within fp32 summation
+ * error of the exact dot product.
+ * `workspace` (16-byte aligned, moe_router_workspace_size(d, E) bytes)
+ * receives the split weights [3][E][d] bf16; 2 kernel launches.  */
+size_t moe_router_workspace_size(int d, int E);
 moe_status_t moe_router_logits(const uint16_t *x, const float *Wr, const float *bias,
-                               int T, int d, int E, float *logits, cudaStream_t stream);
+                               int T, int d, int E, float *logits,
+                               void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* Steps a1 + a2 -- top-K softmax routing, expert histogram, offsets and the
  * stable dispatch order (introduction: Top-K experts; "What specialized
@@ -154,14 +162,14 @@ moe_status_t moe_grouped_gemm2(const uint16_t *h, const int32_t *offsets, int E,
 moe_status_t moe_unpermute(const uint16_t *y_perm, const int32_t *row_of, const float *topk_w,
                            int T, int K, int d, uint16_t *y, cudaStream_t stream);
 
-/* The whole layer, a0..a6 in order on `stream` (8 kernel launches).
+/* The whole layer, a0..a6 in order on `stream` (9 kernel launches).
  * `workspace` (16-byte aligned, moe_forward_workspace_size() bytes) holds
  * every intermediate; moe_forward_views() gives their byte offsets so that a
  * caller can inspect them after the call.  */
 size_t moe_forward_workspace_size(int T, int d, int E, int K, int f);
 typedef struct {
     size_t logits, topk_idx, topk_w, counts, offsets, row_of, src_tok, route_ws,
-           x_perm, h, y_perm, x_dev, y_dev, total;
+           router_ws, x_perm, h, y_perm, x_dev, y_dev, total;
 } moe_forward_layout_t;
 moe_status_t moe_forward_views(int T, int d, int E, int K, int f, moe_forward_layout_t *layout);
 moe_status_t moe_forward(const uint16_t *x, const float *Wr, const float *bias,

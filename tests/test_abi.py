@@ -27,7 +27,8 @@ def _declared():
 
 def test_header_declares_the_boundary():
     names = _declared()
-    for n in ["moe_router_logits", "moe_route", "moe_permute", "moe_grouped_mlp", "moe_unpermute",
+    for n in ["moe_router_logits", "moe_router_workspace_size", "moe_route", "moe_permute", "moe_grouped_mlp",
+              "moe_unpermute",
               "moe_route_workspace_size", "moe_status_string", "moe_forward", "moe_device_status"]:
         assert n in names
 
@@ -43,7 +44,7 @@ def test_status_strings(moe):
         s = moe.lib.moe_status_string(code).decode()
         assert s.startswith("MOE_")
     assert moe.lib.moe_status_string(99).decode() == "unknown moe_status_t"
-    assert moe.lib.moe_abi_version() == 100
+    assert moe.lib.moe_abi_version() == 200
 
 
 def test_workspace_sizes(moe):
@@ -55,10 +56,14 @@ def test_workspace_sizes(moe):
     TK = 8192 * 2
     assert v["h"] - v["x_perm"] >= TK * 4096 * 2 and v["y_perm"] - v["h"] >= TK * 14336 * 2
     offs = [v[k] for k in ("logits", "topk_idx", "topk_w", "counts", "offsets", "row_of", "src_tok",
-                           "route_ws", "x_perm", "h", "y_perm", "x_dev", "y_dev", "total")]
+                           "route_ws", "router_ws", "x_perm", "h", "y_perm", "x_dev", "y_dev", "total")]
+    assert v["x_perm"] - v["router_ws"] >= moe.router_workspace_size(4096, 8)
     assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
     assert moe.forward_workspace_size(8192, 4096, 8, 2, 14336) == v["total"]
     assert moe.forward_workspace_size(8, 100, 8, 2, 64) == 0      # d not a multiple of 64
+    # three bf16 pieces of Wr, [3][E][d]
+    assert moe.router_workspace_size(7168, 256) == 3 * 256 * 7168 * 2
+    assert moe.router_workspace_size(100, 8) == 0 and moe.router_workspace_size(64, 257) == 0
 
 
 FAKE = 1 << 20  # a 16-byte aligned non-null address; never dereferenced (rejected first)
@@ -84,8 +89,10 @@ def test_null_and_misaligned_pointers_rejected(moe):
     L = moe.lib
     assert L.moe_forward(None, FAKE, None, FAKE, FAKE, 8, 64, 8, 2, 64, FAKE, FAKE, 1 << 40, None) == 1
     assert L.moe_forward(FAKE + 2, FAKE, None, FAKE, FAKE, 8, 64, 8, 2, 64, FAKE, FAKE, 1 << 40, None) == 1
-    assert L.moe_router_logits(FAKE, FAKE, None, 8, 64, 8, None, None) == 1
-    assert L.moe_router_logits(FAKE + 8, FAKE, None, 8, 64, 8, FAKE, None) == 1
+    assert L.moe_router_logits(FAKE, FAKE, None, 8, 64, 8, None, FAKE, 1 << 20, None) == 1
+    assert L.moe_router_logits(FAKE + 8, FAKE, None, 8, 64, 8, FAKE, FAKE, 1 << 20, None) == 1
+    assert L.moe_router_logits(FAKE, FAKE, None, 8, 64, 8, FAKE, None, 1 << 20, None) == 1
+    assert L.moe_router_logits(FAKE, FAKE, None, 8, 64, 8, FAKE, FAKE + 8, 1 << 20, None) == 1
     assert L.moe_permute(FAKE, FAKE, 8, 2, 64, FAKE + 4, None) == 1
     assert L.moe_unpermute(FAKE, FAKE, None, 8, 2, 64, FAKE, None) == 1
     assert L.moe_grouped_mlp(FAKE, FAKE, 8, 16, 64, 64, FAKE, None, FAKE, FAKE, None) == 1
@@ -96,6 +103,8 @@ def test_null_and_misaligned_pointers_rejected(moe):
 
 def test_route_workspace_too_small(moe):
     L = moe.lib
+    need = moe.router_workspace_size(128, 16)
+    assert L.moe_router_logits(FAKE, FAKE, None, 8, 128, 16, FAKE, FAKE, need - 16, None) == 3
     need = moe.route_workspace_size(1000, 16, 4)
     r = L.moe_route(FAKE, 1000, 16, 4, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, need - 4, None)
     assert r == 3

@@ -13,7 +13,8 @@ import torch
 import oracle
 from workloads import LayerWeights, Shape, make_tokens, make_weights, random_shape_cases, shape
 
-from _helpers import W_TOL, check_output, check_rounded, compare_small, run_layer, to_np
+from _helpers import (W_TOL, check_dispatch_valid, check_logits, check_output, check_rounded, check_routing,
+                      compare_small, run_layer, to_np, weight_tol)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -69,6 +70,43 @@ def test_every_token_to_one_expert(K):
     w.bias = torch.zeros(8, device=DEV)
     w.bias[3] = 50.0            # expert 3 wins every token: one long group, 7 empty
     compare_small(x, w, K)
+
+
+@pytest.mark.parametrize("E", [8, 64, 200])
+def test_router_one_hot_tokens_are_exact(E):
+    """x[t] = 2^s e_i makes the dot product a single product: the logits must
+    be exactly fp32(2^s Wr[i, e]) + bias[e], which holds only if all three
+    bf16 pieces of Wr are added back exactly and each lands on its expert."""
+    import dropless_moe_expert_gb300 as moe
+    T, d = 300, 256
+    g = np.random.default_rng(E)
+    Wr = (g.standard_normal((d, E)) / math.sqrt(d)).astype(np.float32)
+    bias = g.standard_normal(E).astype(np.float32)
+    x = np.zeros((T, d), np.float32)
+    i = (np.arange(T) * 7) % d
+    scale = np.float32(2.0) ** (np.arange(T) % 5 - 2).astype(np.float32)
+    x[np.arange(T), i] = scale
+    xt = torch.from_numpy(x).to(torch.bfloat16).to(DEV)
+    L = to_np(moe.router_logits(xt, torch.from_numpy(Wr).to(DEV), torch.from_numpy(bias).to(DEV)))
+    torch.cuda.synchronize()
+    ref = (scale[:, None] * Wr[i]).astype(np.float32) + bias[None, :]
+    assert np.array_equal(L.view(np.uint32), ref.view(np.uint32))
+    L0 = to_np(moe.router_logits(xt, torch.from_numpy(Wr).to(DEV), None))
+    assert np.array_equal(L0.view(np.uint32), (scale[:, None] * Wr[i]).astype(np.float32).view(np.uint32))
+
+
+@pytest.mark.parametrize("s", [Shape(T=1000, d=512, E=8, K=2, f=64), Shape(T=300, d=1024, E=256, K=8, f=64),
+                               Shape(T=129, d=64, E=100, K=4, f=64)],
+                         ids=lambda s: f"T{s.T}_d{s.d}_E{s.E}")
+def test_router_logits_bound_and_deterministic(s):
+    import dropless_moe_expert_gb300 as moe
+    x, w = _cpu_case(s, seed=11)
+    L1 = moe.router_logits(x, w.Wr, w.bias)
+    L2 = moe.router_logits(x, w.Wr, w.bias)
+    torch.cuda.synchronize()
+    assert torch.equal(L1.view(torch.int32), L2.view(torch.int32))
+    err = check_logits(to_np(L1), to_np(x), to_np(w.Wr), to_np(w.bias))[0]
+    print(f"router T={s.T} d={s.d} E={s.E}: max error / scale {err:.2e}")
 
 
 def test_equal_logits_route_to_first_k_experts():
@@ -153,37 +191,57 @@ def _sample_tokens(T, v, K, n=24, seed=0):
 
 @pytest.mark.parametrize("name", ["mixtral", "dsv3", "qwen", "skew"])
 def test_full_size_workload(name):
+    import dropless_moe_expert_gb300 as moe
     s = shape(name)
     torch.manual_seed(0)
     w = make_weights(s, seed=0, device=DEV)
     x = make_tokens(s, seed=0, device=DEV)
     y, v, layer = run_layer(x, w, s.K)
 
-    # routing of every token, bit-exact
+    # logits of every token against fp64
     xs = to_np(x)
-    L = oracle.router_logits_fp32(xs, to_np(w.Wr), to_np(w.bias))
-    assert np.array_equal(to_np(v["logits"]).view(np.uint32), L.view(np.uint32)), "logits"
+    Wr, bias = to_np(w.Wr), to_np(w.bias)
+    lerr, scale, L64 = check_logits(to_np(v["logits"]), xs, Wr, bias)
+    # routing given identical fp32 logits: the GPU route kernel on the
+    # oracle's logits, every output bit-exact
+    L = oracle.router_logits_fp32(xs, Wr, bias)
     idx, wref = oracle.topk_route(L, s.K)
     counts, offsets = oracle.expert_counts(idx, s.E)
     src_tok, row_of = oracle.dispatch_order(idx, s.E)
-    assert np.array_equal(to_np(v["topk_idx"]), idx)
-    assert np.max(np.abs(to_np(v["topk_w"]) - wref)) <= W_TOL
-    assert np.array_equal(to_np(v["counts"]), counts)
-    assert np.array_equal(to_np(v["offsets"]), offsets)
-    assert np.array_equal(to_np(v["row_of"]), row_of)
-    assert np.array_equal(to_np(v["src_tok"]), src_tok)
+    r = moe.route(torch.from_numpy(L).to(DEV), s.K)
+    torch.cuda.synchronize()
+    assert np.array_equal(to_np(r.topk_idx), idx)
+    assert np.max(np.abs(to_np(r.topk_w) - wref)) <= W_TOL
+    assert np.array_equal(to_np(r.counts), counts)
+    assert np.array_equal(to_np(r.offsets), offsets)
+    assert np.array_equal(to_np(r.row_of), row_of)
+    assert np.array_equal(to_np(r.src_tok), src_tok)
+    del r
+    # the layer's own routing (from its logits) against the oracle's
+    gidx = to_np(v["topk_idx"])
+    same = check_routing(gidx, idx, L64, scale, s.K)
+    dw = np.abs(to_np(v["topk_w"]) - wref).max(axis=1)
+    assert np.all(dw[same] <= weight_tol(scale, gidx)[same]), "topk_w"
+    if same.all():
+        assert np.array_equal(to_np(v["counts"]), counts)
+        assert np.array_equal(to_np(v["offsets"]), offsets)
+        assert np.array_equal(to_np(v["row_of"]), row_of)
+        assert np.array_equal(to_np(v["src_tok"]), src_tok)
+    else:
+        check_dispatch_valid(v, s.T, s.K, s.E)
     # every permuted row is its token's row (checked on the device, bit patterns)
-    st = torch.from_numpy(src_tok).to(DEV)
+    st = v["src_tok"].long()
     assert torch.equal(v["x_perm"].view(torch.int16), x.view(torch.int16)[st])
     del st
 
     # sampled tokens through the oracle, one by one
     toks = _sample_tokens(s.T, v, s.K)
+    toks = toks[same[toks]]
     W1, W2 = w.W1, w.W2
     ridx, rw, rh, ryk, ry = oracle.forward_tokens(
         toks, xs[toks], L[toks], s.K, lambda e: (to_np(W1[e]), to_np(W2[e])))
     assert np.array_equal(ridx, idx[toks])
-    rows = torch.from_numpy(row_of[toks].reshape(-1)).to(DEV)
+    rows = torch.from_numpy(to_np(v["row_of"])[toks].reshape(-1)).to(DEV)
     h_rows = to_np(v["h"][rows]).reshape(len(toks), s.K, s.f)
     yp_rows = to_np(v["y_perm"][rows]).reshape(len(toks), s.K, s.d)
     check_rounded(h_rows, rh, "h (sampled rows)")
@@ -191,5 +249,6 @@ def test_full_size_workload(name):
     r = check_output(to_np(y[torch.from_numpy(toks).to(DEV)]), ry, "y (sampled tokens)")
     # every output row was written and is finite
     assert bool(torch.isfinite(y.float()).all())
-    print(f"{name}: sampled {len(toks)} tokens rel_l2={r[0]:.2e} max/rms={r[1]:.2e}; "
+    print(f"{name}: logits err/scale {lerr:.2e}, tokens routed differently (near ties) {int((~same).sum())}; "
+          f"sampled {len(toks)} tokens rel_l2={r[0]:.2e} max/rms={r[1]:.2e}; "
           f"experts with no token: {(counts == 0).sum()}, largest group {counts.max()}")
