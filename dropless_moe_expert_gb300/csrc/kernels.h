@@ -9,7 +9,7 @@ namespace moe {
 
 // Tokens per routing chunk: the unit of the per-chunk histograms that make the
 // dispatch order deterministic.
-constexpr int kRouteChunk = 256;
+constexpr int kRouteChunk = 64;
 
 inline int route_num_chunks(int T) { return (T + kRouteChunk - 1) / kRouteChunk; }
 // chunk_counts [C, E] and chunk_base [C, E], int32

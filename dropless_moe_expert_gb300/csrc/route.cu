@@ -8,17 +8,21 @@
 // optimizations are needed for dropless MoE?", "Optimization 1: Grouped GEMM").
 //
 // Three kernels, no atomics whose order could show in a result:
-//  1. route_topk: a group of G lanes per token (G = 8, 16 or 32; 32/G tokens
-//     per warp); each lane holds E/G logits as 64-bit keys (order-preserving
-//     float bits << 32 | ~expert), K rounds of group max via shuffles pick the
-//     experts (descending, lower index on ties, -0.0 == +0.0); softmax over
-//     the K picks.  The CTA then marks, per
-//     expert, which of its 256 tokens chose it in a shared bitmap (atomicOr:
-//     the final bitmap does not depend on order), and from it writes the
-//     chunk's per-expert count and every pair's rank inside the chunk.
-//  2. route_scan: one CTA; counts = sum over chunks, offsets = exclusive
-//     scan over experts, chunk_base[c][e] = offsets[e] + rows of expert e in
-//     earlier chunks.
+//  1. route_topk: one CTA per chunk of 64 tokens.  A group of G lanes per
+//     token (G = 8, 16 or 32; 32/G tokens per warp); each lane holds E/G
+//     logits as order-preserving 32-bit keys (-0.0 == +0.0).  K rounds pick
+//     the experts, descending, lower index on ties.  With G = 32 a round is
+//     two warp reductions (redux.sync): the largest key, then the lowest
+//     expert among the lanes whose best key equals it; with G < 32 a round is
+//     a group max of 64-bit (key << 32 | ~expert) values via shuffles.
+//     Softmax over the K picks.  The CTA then marks, per expert, which of its
+//     tokens chose it in a shared bitmap (atomicOr: the final bitmap does not
+//     depend on order), and from it writes the chunk's per-expert count and
+//     every pair's rank inside the chunk.
+//  2. route_scan: one CTA of 1024 threads, each owning one expert and a slice
+//     of chunks; counts = sum over chunks, offsets = exclusive scan over
+//     experts, chunk_base[c][e] = offsets[e] + rows of expert e in earlier
+//     chunks.
 //  3. route_scatter: row_of[t,k] = chunk_base[chunk(t)][e] + rank;
 //     src_tok[row] = t.  Rows of a group are thus in ascending token order.
 #include "kernels.h"
@@ -31,8 +35,9 @@ namespace moe {
 namespace rt {
 
 constexpr int CH = kRouteChunk;  // tokens per CTA
-constexpr int THREADS = 1024;    // 32 warps: each ranks 8 of the chunk's tokens
+constexpr int THREADS = 256;     // 8 warps: with G = 32 each ranks 8 of the chunk's tokens
 constexpr int WARPS = THREADS / 32;
+constexpr int SCAN_THREADS = 1024;
 constexpr int MAX_E = 256;
 constexpr int MAX_K = 16;
 
@@ -80,36 +85,70 @@ route_topk_kernel(const float *__restrict__ L, int T, int E, int K, int32_t *__r
     load_logits(warp * TPW + group);
     for (int tl = warp * TPW + group; tl < nt; tl += WARPS * TPW) {
         const int t = t0 + tl;
-        unsigned long long key[EPL];
-#pragma unroll
-        for (int j = 0; j < EPL; ++j) {
-            const int e = glane + G * j;
-            key[j] = (e < E) ? ((static_cast<unsigned long long>(order_key(nxt[j])) << 32) |
-                                static_cast<unsigned long long>(0xffffffffu - static_cast<uint32_t>(e)))
-                             : 0ull;  // below every real key
-        }
-        load_logits(tl + WARPS * TPW);
         int my_e = 0;
         float my_z = 0.0f;
         float v0 = 0.0f, sum = 0.0f;
-        for (int k = 0; k < K; ++k) {
-            unsigned long long best = key[0];
+        if constexpr (G == 32) {
+            // keys of experts lane + 32 j; 0 is below every real key
+            uint32_t vk[EPL];
 #pragma unroll
-            for (int j = 1; j < EPL; ++j) best = key[j] > best ? key[j] : best;
+            for (int j = 0; j < EPL; ++j) vk[j] = (glane + 32 * j < E) ? order_key(nxt[j]) : 0u;
+            load_logits(tl + WARPS * TPW);
+            // this lane's best key; the lowest j (lowest expert) on ties
+            uint32_t bv = vk[0];
+            int bj = 0;
 #pragma unroll
-            for (int s = G / 2; s >= 1; s >>= 1) {
-                const unsigned long long o = __shfl_xor_sync(gmask, best, s, G);
-                best = o > best ? o : best;
+            for (int j = 1; j < EPL; ++j)
+                if (vk[j] > bv) { bv = vk[j]; bj = j; }
+            for (int k = 0; k < K; ++k) {
+                const uint32_t vmax = __reduce_max_sync(0xffffffffu, bv);
+                const uint32_t cand = (bv == vmax) ? static_cast<uint32_t>(glane + 32 * bj) : 0xffffffffu;
+                const int e = static_cast<int>(__reduce_min_sync(0xffffffffu, cand));
+                if ((e & 31) == glane) {
+                    // the winner is this lane's best key: drop it, find the next
+#pragma unroll
+                    for (int j = 0; j < EPL; ++j) vk[j] = (j == bj) ? 0u : vk[j];
+                    bv = vk[0];
+                    bj = 0;
+#pragma unroll
+                    for (int j = 1; j < EPL; ++j)
+                        if (vk[j] > bv) { bv = vk[j]; bj = j; }
+                }
+                const float v = key_value(vmax);
+                if (k == 0) v0 = v;
+                const float z = expf(v - v0);
+                sum += z;
+                if (glane == k) { my_e = e; my_z = z; }
             }
-            const int e = static_cast<int>(0xffffffffu - static_cast<uint32_t>(best & 0xffffffffull));
-            const float v = key_value(static_cast<uint32_t>(best >> 32));
-            const bool mine = (e % G) == glane;
+        } else {
+            unsigned long long key[EPL];
 #pragma unroll
-            for (int j = 0; j < EPL; ++j) key[j] = (mine && j == e / G) ? 0ull : key[j];
-            if (k == 0) v0 = v;
-            const float z = expf(v - v0);
-            sum += z;
-            if (glane == k) { my_e = e; my_z = z; }
+            for (int j = 0; j < EPL; ++j) {
+                const int e = glane + G * j;
+                key[j] = (e < E) ? ((static_cast<unsigned long long>(order_key(nxt[j])) << 32) |
+                                    static_cast<unsigned long long>(0xffffffffu - static_cast<uint32_t>(e)))
+                                 : 0ull;  // below every real key
+            }
+            load_logits(tl + WARPS * TPW);
+            for (int k = 0; k < K; ++k) {
+                unsigned long long best = key[0];
+#pragma unroll
+                for (int j = 1; j < EPL; ++j) best = key[j] > best ? key[j] : best;
+#pragma unroll
+                for (int s = G / 2; s >= 1; s >>= 1) {
+                    const unsigned long long o = __shfl_xor_sync(gmask, best, s, G);
+                    best = o > best ? o : best;
+                }
+                const int e = static_cast<int>(0xffffffffu - static_cast<uint32_t>(best & 0xffffffffull));
+                const float v = key_value(static_cast<uint32_t>(best >> 32));
+                const bool mine = (e % G) == glane;
+#pragma unroll
+                for (int j = 0; j < EPL; ++j) key[j] = (mine && j == e / G) ? 0ull : key[j];
+                if (k == 0) v0 = v;
+                const float z = expf(v - v0);
+                sum += z;
+                if (glane == k) { my_e = e; my_z = z; }
+            }
         }
         if (glane < K) {
             topk_idx[static_cast<size_t>(t) * K + glane] = my_e;
@@ -137,36 +176,62 @@ route_topk_kernel(const float *__restrict__ L, int T, int E, int K, int32_t *__r
     }
 }
 
-__global__ void __launch_bounds__(MAX_E)
+// Thread (e, s): expert e < EP (E rounded up to a multiple of 32), slice s of
+// S = SCAN_THREADS / EP consecutive chunk ranges.  Loads of one chunk row are
+// coalesced across the experts of a warp.
+__global__ void __launch_bounds__(SCAN_THREADS)
 route_scan_kernel(const int32_t *__restrict__ chunk_counts, int C, int E, int32_t *__restrict__ counts,
                   int32_t *__restrict__ offsets, int32_t *__restrict__ chunk_base) {
+    __shared__ int32_t part[SCAN_THREADS];   // [s][e]: rows of expert e in slice s
     __shared__ int32_t warp_tot[MAX_E / 32];
-    const int e = threadIdx.x;
-    const int lane = e & 31, warp = e >> 5;
-    int cnt = 0;
-    if (e < E) {
+    const int EP = (E + 31) & ~31;
+    const int S = SCAN_THREADS / EP;
+    const int e = threadIdx.x % EP;
+    const int sl = threadIdx.x / EP;
+    const int CS = (C + S - 1) / S;
+    const int c0 = min(C, sl * CS), c1 = min(C, c0 + CS);
+    int sum = 0;
+    if (sl < S && e < E) {
 #pragma unroll 8
-        for (int c = 0; c < C; ++c) cnt += chunk_counts[static_cast<size_t>(c) * E + e];
+        for (int c = c0; c < c1; ++c) sum += chunk_counts[static_cast<size_t>(c) * E + e];
     }
-    // exclusive scan of cnt over experts
-    int v = cnt;
-#pragma unroll
-    for (int s = 1; s < 32; s <<= 1) {
-        const int n = __shfl_up_sync(0xffffffffu, v, s);
-        if (lane >= s) v += n;
-    }
-    if (lane == 31) warp_tot[warp] = v;
+    if (sl < S) part[sl * EP + e] = sum;
     __syncthreads();
-    int before = 0;
-    for (int w = 0; w < warp; ++w) before += warp_tot[w];
-    const int excl = before + v - cnt;
-    if (e < E) {
-        counts[e] = cnt;
-        offsets[e] = excl;
-        if (e == E - 1) offsets[E] = excl + cnt;
+    if (sl == 0) {
+        int cnt = 0;
+        for (int q = 0; q < S; ++q) cnt += part[q * EP + e];
+        // exclusive scan of cnt over experts
+        const int lane = e & 31, warp = e >> 5;
+        int v = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, v, o);
+            if (lane >= o) v += n;
+        }
+        if (lane == 31) warp_tot[warp] = v;
+        __syncwarp();
+        asm volatile("bar.sync 1, %0;" ::"r"(EP) : "memory");  // the EP threads of slice 0
+        int before = 0;
+        for (int w = 0; w < warp; ++w) before += warp_tot[w];
+        const int excl = before + v - cnt;
+        if (e < E) {
+            counts[e] = cnt;
+            offsets[e] = excl;
+            if (e == E - 1) offsets[E] = excl + cnt;
+        }
+        // turn the slice sums into slice bases
         int run = excl;
+        for (int q = 0; q < S; ++q) {
+            const int pq = part[q * EP + e];
+            part[q * EP + e] = run;
+            run += pq;
+        }
+    }
+    __syncthreads();
+    if (sl < S && e < E) {
+        int run = part[sl * EP + e];
 #pragma unroll 8
-        for (int c = 0; c < C; ++c) {
+        for (int c = c0; c < c1; ++c) {
             chunk_base[static_cast<size_t>(c) * E + e] = run;
             run += chunk_counts[static_cast<size_t>(c) * E + e];
         }
@@ -209,7 +274,7 @@ cudaError_t launch_route(const float *logits, int T, int E, int K, int32_t *topk
         rt::route_topk_kernel<32, 8><<<C, rt::THREADS, 0, stream>>>(logits, T, E, K, topk_idx, topk_w, row_of, chunk_counts);
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
-    rt::route_scan_kernel<<<1, rt::MAX_E, 0, stream>>>(chunk_counts, C, E, counts, offsets, chunk_base);
+    rt::route_scan_kernel<<<1, rt::SCAN_THREADS, 0, stream>>>(chunk_counts, C, E, counts, offsets, chunk_base);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     const size_t TK = static_cast<size_t>(T) * K;

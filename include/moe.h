@@ -101,7 +101,8 @@ moe_status_t moe_router_logits(const uint16_t *x, const float *Wr, const float *
  *   topk_w[t,k]  : exp(l_k - l_0) / sum_j exp(l_j - l_0) over the K selected;
  *   counts, offsets (exclusive scan, E+1 entries), row_of, src_tok as above.
  * Every output is bit-deterministic.  `workspace` must hold
- * moe_route_workspace_size(T, E, K) bytes (4-byte aligned).  */
+ * moe_route_workspace_size(T, E, K) bytes (4-byte aligned): two int32
+ * tables of [ceil(T / 64), E].  */
 size_t moe_route_workspace_size(int T, int E, int K);
 moe_status_t moe_route(const float *logits, int T, int E, int K,
                        int32_t *topk_idx, float *topk_w, int32_t *counts, int32_t *offsets,
@@ -115,7 +116,7 @@ moe_status_t moe_route(const float *logits, int T, int E, int K,
  * all device memory in a fixed pool.  The page has no counterpart: this is
  * a packaging variant of moe_route, with identical outputs.
  *   - Scratch lives in a library-owned static device array of
- *     MOE_ROUTE_STATIC_MAX_SCRATCH_BYTES (256 KiB) on every GPU that loads
+ *     MOE_ROUTE_STATIC_MAX_SCRATCH_BYTES (1 MiB) on every GPU that loads
  *     the library, held until the process exits.  Sizes whose scratch,
  *     moe_route_workspace_size(T, E, K), exceeds it return
  *     MOE_ERR_UNSUPPORTED with nothing launched (e.g. E = 256 allows up to
@@ -127,7 +128,7 @@ moe_status_t moe_route(const float *logits, int T, int E, int K,
  *     in it needs to start at zero.  Calls whose kernels overlap on the GPU
  *     (several streams, or several host threads) race on it: serialize them.
  *   - Kernel launches of this call are not counted by moe_launch_count(). */
-#define MOE_ROUTE_STATIC_MAX_SCRATCH_BYTES (256u * 1024u)
+#define MOE_ROUTE_STATIC_MAX_SCRATCH_BYTES (1024u * 1024u)
 moe_status_t moe_route_static(const float *logits, int T, int E, int K,
                               int32_t *topk_idx, float *topk_w, int32_t *counts, int32_t *offsets,
                               int32_t *row_of, int32_t *src_tok, cudaStream_t stream);

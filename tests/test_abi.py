@@ -48,10 +48,10 @@ def test_status_strings(moe):
 
 
 def test_workspace_sizes(moe):
-    # two int32 [chunks, E] tables, 256 tokens per chunk
-    assert moe.route_workspace_size(256, 8, 2) == 1 * 8 * 2 * 4
-    assert moe.route_workspace_size(257, 8, 2) == 2 * 8 * 2 * 4
-    assert moe.route_workspace_size(32768, 64, 6) == 128 * 64 * 2 * 4
+    # two int32 [chunks, E] tables, 64 tokens per chunk
+    assert moe.route_workspace_size(64, 8, 2) == 1 * 8 * 2 * 4
+    assert moe.route_workspace_size(65, 8, 2) == 2 * 8 * 2 * 4
+    assert moe.route_workspace_size(32768, 64, 6) == 512 * 64 * 2 * 4
     v = moe.forward_views(8192, 4096, 8, 2, 14336)
     TK = 8192 * 2
     assert v["h"] - v["x_perm"] >= TK * 4096 * 2 and v["y_perm"] - v["h"] >= TK * 14336 * 2

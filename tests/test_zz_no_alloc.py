@@ -74,9 +74,10 @@ def test_route_static_matches_route_on_two_calls(T, E, K):
 
 def test_route_static_rejects_sizes_beyond_its_scratch():
     fn = _static_fn()
-    # 129 chunks of 256 tokens x 256 experts x 2 tables x 4 bytes > 256 KiB
-    T, E, K = 256 * 129, 256, 8
-    assert moe.route_workspace_size(T, E, K) > 256 * 1024
+    # 513 chunks of 64 tokens x 256 experts x 2 tables x 4 bytes > 1 MiB
+    T, E, K = 64 * 513, 256, 8
+    assert moe.route_workspace_size(T, E, K) > 1024 * 1024
+    assert moe.route_workspace_size(64 * 512, E, K) == 1024 * 1024
     dummy = torch.empty(16, dtype=torch.int32, device="cuda")
     p = dummy.data_ptr()
     before = torch.cuda.current_stream().cuda_stream
