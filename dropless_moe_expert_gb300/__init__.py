@@ -23,6 +23,8 @@ __all__ = [
     "grouped_mlp",
     "grouped_gemm1_swiglu", "grouped_gemm2", "unpermute", "forward", "forward_workspace_size",
     "forward_views", "forward_host", "device_status", "launch_count", "MoELayer",
+    "mxfp8_quantize", "mxfp8_scales_size", "mxfp8_act_scales_size", "permute_mxfp8",
+    "grouped_gemm1_swiglu_mxfp8", "grouped_gemm2_mxfp8", "forward_mxfp8", "forward_mxfp8_views", "MoELayerMXFP8",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -41,6 +43,12 @@ class _Layout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in (
         "logits", "topk_idx", "topk_w", "counts", "offsets", "row_of", "src_tok", "route_ws",
         "router_ws", "x_perm", "h", "y_perm", "x_dev", "y_dev", "total")]
+
+
+class _LayoutMX(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in (
+        "logits", "topk_idx", "topk_w", "counts", "offsets", "row_of", "src_tok", "route_ws", "router_ws",
+        "xq_perm", "sfa", "hq", "sfh", "y_perm", "total")]
 
 
 def _load():
@@ -68,6 +76,15 @@ def _load():
         "moe_forward_views": (I, [I, I, I, I, I, ctypes.POINTER(_Layout)]),
         "moe_forward": (I, [P, P, P, P, P, I, I, I, I, I, P, P, S, P]),
         "moe_forward_host": (I, [P, P, P, P, P, I, I, I, I, I, P, P, S, P]),
+        "moe_mxfp8_scales_size": (S, [I, I]),
+        "moe_mxfp8_quantize": (I, [P, I, I, P, P, P]),
+        "moe_mxfp8_act_scales_size": (S, [I, I, I]),
+        "moe_permute_mxfp8": (I, [P, P, P, P, I, I, I, I, P, P, S, P]),
+        "moe_grouped_gemm1_swiglu_mxfp8": (I, [P, P, S, P, I, I, I, I, P, P, P, P, S, P]),
+        "moe_grouped_gemm2_mxfp8": (I, [P, P, S, P, I, I, I, I, P, P, P, P]),
+        "moe_forward_mxfp8_workspace_size": (S, [I, I, I, I, I]),
+        "moe_forward_mxfp8_views": (I, [I, I, I, I, I, ctypes.POINTER(_LayoutMX)]),
+        "moe_forward_mxfp8": (I, [P, P, P, P, P, P, P, I, I, I, I, I, P, P, S, P]),
         "moe_device_status": (I, [ctypes.POINTER(I)]),
         "moe_check_bounded_wait": (I, [U64, P]),
     }
@@ -357,5 +374,148 @@ class MoELayer:
             src_tok=v("src_tok", TK, torch.int32, (TK,)),
             x_perm=v("x_perm", TK * d, torch.bfloat16, (TK, d)),
             h=v("h", TK * f, torch.bfloat16, (TK, f)),
+            y_perm=v("y_perm", TK * d, torch.bfloat16, (TK, d)),
+        )
+
+
+# ------------------------------------------------------------------ MXFP8 path
+def mxfp8_scales_size(rows: int, K: int) -> int:
+    return int(lib.moe_mxfp8_scales_size(rows, K))
+
+
+def mxfp8_act_scales_size(TK: int, E: int, K: int) -> int:
+    return int(lib.moe_mxfp8_act_scales_size(TK, E, K))
+
+
+def mxfp8_quantize(src, stream=None):
+    """bf16 [..., K] (K a multiple of 128) -> (codes uint8 [..., K], scale
+    atoms uint8 [moe_mxfp8_scales_size(rows, K)]), rows = src.numel() / K."""
+    if not src.is_cuda or src.dtype != torch.bfloat16 or not src.is_contiguous():
+        raise ValueError("src must be a contiguous CUDA bf16 tensor")
+    K = src.shape[-1]
+    rows = src.numel() // K
+    n = mxfp8_scales_size(rows, K)
+    if n == 0:
+        raise MoEError(2, "moe_mxfp8_scales_size")
+    codes = torch.empty(src.shape, dtype=torch.uint8, device=src.device)
+    scales = torch.empty((n,), dtype=torch.uint8, device=src.device)
+    _check(lib.moe_mxfp8_quantize(_ptr(src), rows, K, _ptr(codes), _ptr(scales), _stream(stream)),
+           "moe_mxfp8_quantize")
+    return codes, scales
+
+
+def permute_mxfp8(x, r: "Routing", stream=None):
+    """(xq_perm uint8 [TK, d], sfa scale atoms) of the routed tokens."""
+    T, d = x.shape
+    K = r.topk_idx.shape[1]
+    E = r.counts.shape[0]
+    _need(x, torch.bfloat16, (T, d), "x")
+    n = mxfp8_act_scales_size(T * K, E, d)
+    if n == 0:
+        raise MoEError(2, "moe_mxfp8_act_scales_size")
+    xq = torch.empty((T * K, d), dtype=torch.uint8, device=x.device)
+    sfa = torch.empty((n,), dtype=torch.uint8, device=x.device)
+    _check(lib.moe_permute_mxfp8(_ptr(x), _ptr(r.topk_idx), _ptr(r.row_of), _ptr(r.offsets), T, K, d, E, _ptr(xq),
+                                 _ptr(sfa), sfa.numel(), _stream(stream)), "moe_permute_mxfp8")
+    return xq, sfa
+
+
+def grouped_gemm1_swiglu_mxfp8(xq, sfa, offsets, W1q, W1s, stream=None):
+    """(hq uint8 [TK, f], sfh scale atoms)."""
+    TK, d = xq.shape
+    E, two_f, _ = W1q.shape
+    f = two_f // 2
+    n = mxfp8_act_scales_size(TK, E, f)
+    hq = torch.empty((TK, f), dtype=torch.uint8, device=xq.device)
+    sfh = torch.empty((n,), dtype=torch.uint8, device=xq.device)
+    _check(lib.moe_grouped_gemm1_swiglu_mxfp8(_ptr(xq), _ptr(sfa), sfa.numel(), _ptr(offsets), E, TK, d, f,
+                                              _ptr(W1q), _ptr(W1s), _ptr(hq), _ptr(sfh), sfh.numel(),
+                                              _stream(stream)), "moe_grouped_gemm1_swiglu_mxfp8")
+    return hq, sfh
+
+
+def grouped_gemm2_mxfp8(hq, sfh, offsets, W2q, W2s, out=None, stream=None):
+    """y_perm bf16 [TK, d]."""
+    TK, f = hq.shape
+    E, d, _ = W2q.shape
+    out = _empty((TK, d), torch.bfloat16, hq) if out is None else _need(out, torch.bfloat16, (TK, d), "y_perm")
+    _check(lib.moe_grouped_gemm2_mxfp8(_ptr(hq), _ptr(sfh), sfh.numel(), _ptr(offsets), E, TK, d, f, _ptr(W2q),
+                                       _ptr(W2s), _ptr(out), _stream(stream)), "moe_grouped_gemm2_mxfp8")
+    return out
+
+
+def forward_mxfp8_views(T, d, E, K, f) -> dict:
+    lay = _LayoutMX()
+    _check(lib.moe_forward_mxfp8_views(T, d, E, K, f, ctypes.byref(lay)), "moe_forward_mxfp8_views")
+    return {n: getattr(lay, n) for n, _ in _LayoutMX._fields_}
+
+
+def forward_mxfp8(x, Wr, bias, W1q, W1s, W2q, W2s, K: int, out=None, workspace=None, stream=None):
+    """The whole layer with MXFP8 expert matmuls in one C-ABI call."""
+    T, d = x.shape
+    E, two_f, _ = W1q.shape
+    f = two_f // 2
+    _need(x, torch.bfloat16, (T, d), "x")
+    _need(Wr, torch.float32, (d, E), "Wr")
+    if bias is not None:
+        _need(bias, torch.float32, (E,), "bias")
+    _need(W1q, torch.uint8, (E, 2 * f, d), "W1q")
+    _need(W2q, torch.uint8, (E, d, f), "W2q")
+    nbytes = int(lib.moe_forward_mxfp8_workspace_size(T, d, E, K, f))
+    if nbytes == 0:
+        raise MoEError(2, "moe_forward_mxfp8_workspace_size")
+    if workspace is None:
+        workspace = _empty((nbytes,), torch.uint8, x)
+    out = _empty((T, d), torch.bfloat16, x) if out is None else _need(out, torch.bfloat16, (T, d), "y")
+    _check(lib.moe_forward_mxfp8(_ptr(x), _ptr(Wr), _ptr(bias), _ptr(W1q), _ptr(W1s), _ptr(W2q), _ptr(W2s), T, d,
+                                 E, K, f, _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream)),
+           "moe_forward_mxfp8")
+    return out
+
+
+class MoELayerMXFP8:
+    """A layer whose expert weights are quantised to MXFP8 once at
+    construction; ``__call__(x)`` runs the MXFP8 forward with one C call."""
+
+    def __init__(self, Wr, bias, W1, W2, K: int, T_max: int):
+        self.Wr, self.bias, self.K = Wr, bias, K
+        self.E, two_f, self.d = W1.shape
+        self.f = two_f // 2
+        self.W1q, self.W1s = mxfp8_quantize(W1)
+        self.W2q, self.W2s = mxfp8_quantize(W2)
+        self.T_max = T_max
+        n = int(lib.moe_forward_mxfp8_workspace_size(T_max, self.d, self.E, K, self.f))
+        if n == 0:
+            raise MoEError(2, "moe_forward_mxfp8_workspace_size")
+        self.workspace = torch.empty((n,), dtype=torch.uint8, device=W1.device)
+
+    def __call__(self, x, out=None, stream=None):
+        if x.shape[0] > self.T_max:
+            raise ValueError("more tokens than the workspace was sized for")
+        return forward_mxfp8(x, self.Wr, self.bias, self.W1q, self.W1s, self.W2q, self.W2s, self.K, out=out,
+                             workspace=self.workspace, stream=stream)
+
+    def views(self, T: int) -> dict:
+        """Typed views of the intermediates of the last call with T tokens."""
+        lay = forward_mxfp8_views(T, self.d, self.E, self.K, self.f)
+        ws = self.workspace
+        K, E, d, f = self.K, self.E, self.d, self.f
+        TK = T * K
+
+        def v(name, n, dtype, shape):
+            return ws[lay[name]:lay[name] + n * torch.tensor([], dtype=dtype).element_size()].view(dtype).view(shape)
+
+        return dict(
+            logits=v("logits", T * E, torch.float32, (T, E)),
+            topk_idx=v("topk_idx", TK, torch.int32, (T, K)),
+            topk_w=v("topk_w", TK, torch.float32, (T, K)),
+            counts=v("counts", E, torch.int32, (E,)),
+            offsets=v("offsets", E + 1, torch.int32, (E + 1,)),
+            row_of=v("row_of", TK, torch.int32, (T, K)),
+            src_tok=v("src_tok", TK, torch.int32, (TK,)),
+            xq_perm=v("xq_perm", TK * d, torch.uint8, (TK, d)),
+            sfa=ws[lay["sfa"]:lay["hq"]],
+            hq=v("hq", TK * f, torch.uint8, (TK, f)),
+            sfh=ws[lay["sfh"]:lay["y_perm"]],
             y_perm=v("y_perm", TK * d, torch.bfloat16, (TK, d)),
         )

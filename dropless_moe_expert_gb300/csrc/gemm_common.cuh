@@ -1,0 +1,222 @@
+// Pieces shared by the bf16 and the MXFP8 grouped GEMMs: the parameters,
+// the device-side tile scheduler over ragged expert groups and the bf16
+// epilogue (TMEM -> registers -> bf16 -> shared memory -> TMA store).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "ptx.cuh"
+
+namespace moe {
+namespace gg {
+
+constexpr int BN_ACC = 256;   // accumulator columns of one tile
+constexpr int MAX_E = 256;
+
+// Epilogue staging for TMA stores: per epilogue warp two 32-row x 32-column
+// bf16 buffers (2 KB each, 64-byte swizzle).
+constexpr int EPI_WARPS = 4;
+constexpr int EPI_BUF = 32 * 32 * 2;
+constexpr int EPI_BYTES = EPI_WARPS * 2 * EPI_BUF;
+
+struct Params {
+    const int32_t *offsets;  // [E+1] device
+    int E;
+    int TK;         // rows of the activation matrix
+    int Kdim;       // reduction length (d for GEMM1, f for GEMM2)
+    int n_out;      // output columns (f for GEMM1, d for GEMM2)
+    int w_rows;     // weight rows per expert (2f or d)
+    int NT;         // column blocks per row block
+    __nv_bfloat16 *out;  // [TK, n_out]
+    int *status;
+    uint64_t timeout_ns;
+};
+
+struct Tile {
+    int e, m_blk, n_blk, row0, grp_end;
+};
+
+// Group bounds [s_off[e], s_end[e]), clamped to [0, TK] so that no content of
+// offsets[] can send a store out of bounds, and the per-expert tile prefix
+// s_pre (tiles of experts < e) for row blocks of RB rows.  One warp.
+//
+// Also decides the visit order (s_mix): when the largest group holds more
+// than 4x the average, heavy and light groups' tiles are interleaved.
+template <int RB>
+__device__ __forceinline__ void build_groups(const Params &p, int lane, int *s_off, int *s_end, int *s_pre,
+                                             int *s_mix) {
+    int carry = 0, cmax = 0, csum = 0;
+    for (int base = 0; base < p.E; base += 32) {
+        const int e = base + lane;
+        int v = 0;
+        if (e < p.E) {
+            const int o0 = min(max(p.offsets[e], 0), p.TK);
+            const int o1 = min(max(p.offsets[e + 1], o0), p.TK);
+            s_off[e] = o0;
+            s_end[e] = o1;
+            v = ((o1 - o0 + RB - 1) / RB) * p.NT;
+            cmax = max(cmax, o1 - o0);
+            csum += o1 - o0;
+        }
+#pragma unroll
+        for (int s = 1; s < 32; s <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, v, s);
+            if (lane >= s) v += n;
+        }
+        if (e < p.E) s_pre[e + 1] = carry + v;
+        carry += __shfl_sync(0xffffffffu, v, 31);
+    }
+#pragma unroll
+    for (int s = 16; s >= 1; s >>= 1) {
+        cmax = max(cmax, __shfl_xor_sync(0xffffffffu, cmax, s));
+        csum += __shfl_xor_sync(0xffffffffu, csum, s);
+    }
+    if (lane == 0) {
+        s_pre[0] = 0;
+        *s_mix = static_cast<int64_t>(cmax) * p.E > 4ll * csum ? 1 : 0;
+    }
+}
+
+template <int RB, int NBAND>
+__device__ __forceinline__ Tile decode_tile(int tile, const int *s_pre, const int *s_off, const int *s_end, int E,
+                                            int NT) {
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_pre[mid] <= tile) lo = mid; else hi = mid - 1;
+    }
+    Tile t;
+    t.e = lo;
+    const int local = tile - s_pre[lo];
+    const int g0 = s_off[lo], g1 = s_end[lo];
+    const int MT = (g1 - g0 + RB - 1) / RB;
+    const int band = local / (NBAND * NT);
+    const int within = local - band * NBAND * NT;
+    const int mb0 = band * NBAND;
+    const int bm = min(NBAND, MT - mb0);
+    t.n_blk = within / bm;
+    t.m_blk = mb0 + (within - t.n_blk * bm);
+    t.row0 = g0 + t.m_blk * RB;
+    t.grp_end = g1;
+    return t;
+}
+
+// Order in which the persistent CTAs visit the tile list.  Under a skewed
+// load (mix), positions alternate between the front and the back of the list,
+// so every wave mixes tiles of the experts at both ends: the heavy groups'
+// tiles, whose weight tiles are shared by many row blocks and so are bounded
+// by the tensor pipe, run beside the light groups' tiles, which only stream
+// weights.  A bijection of [0, N); neighbours in each half stay neighbours,
+// so tiles that share operands through L2 still run together.
+__device__ __forceinline__ int visit_order(int p, int N, int mix) {
+    return mix ? ((p & 1) ? N - 1 - (p >> 1) : (p >> 1)) : p;
+}
+
+// Position of round k for worker c of G: rounds cover consecutive blocks of
+// G positions.  Under the interleaved order (mix) the workers sweep them in
+// alternating direction, so a worker alternates between even and odd
+// positions (the two ends of the list); otherwise every round keeps the same
+// direction, which keeps the tiles in flight at one time (and their shared
+// operands in L2) close together even when workers drift apart.
+__device__ __forceinline__ int round_position(int k, int c, int G, int mix) {
+    return k * G + ((mix && (k & 1)) ? G - 1 - c : c);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+__device__ __forceinline__ void store_row32(__nv_bfloat16 *dst_row, const uint32_t (&packed)[16]) {
+    uint4 *dst = reinterpret_cast<uint4 *>(dst_row);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+}
+
+// Epilogue of one accumulator for one warp: 32 TMEM lanes = 32 output rows
+// wrow0..wrow0+31 (this thread's row is wrow0 + lane), tbase points at the
+// warp's lane quarter of the accumulator.  Each 32-column chunk is converted
+// to bf16 and, when all 32 rows belong to the group, staged in shared memory
+// (64-byte swizzle) and written by one TMA store of full lines; a slice that
+// crosses the group's end falls back to masked 16-byte stores per row.
+// `sbuf` alternates the warp's two staging buffers across chunks and tiles.
+template <bool SWIGLU>
+__device__ __forceinline__ void epilogue_tile(const Params &p, const CUtensorMap *tm_out, uint8_t *stage,
+                                              uint32_t &sbuf, uint32_t tbase, int n_blk, int wrow0, int lane,
+                                              int grp_end) {
+    if (wrow0 >= grp_end) return;  // whole slice outside the group (warp-uniform)
+    const bool full = wrow0 + 31 < grp_end;
+    const int grow = wrow0 + lane;
+    const bool row_ok = grow < grp_end;
+    constexpr int NCOL = SWIGLU ? BN_ACC / 2 : BN_ACC;
+    auto emit = [&](int c, const uint32_t (&packed)[16]) {
+        const int col = n_blk * NCOL + c;
+        if (col >= p.n_out) return;  // column tail (uniform)
+        if (full) {
+            uint8_t *buf = stage + sbuf * EPI_BUF;
+            if (lane == 0) bulk_wait_read<1>();  // this buffer's store from two chunks ago has read it
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int jj = j ^ ((lane >> 1) & 3);
+                *reinterpret_cast<uint4 *>(buf + lane * 64 + jj * 16) =
+                    make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                // the output is not read again by this kernel: let L2 evict it
+                // before the operand tiles that other CTAs still share
+                tma_store_2d_evict_first(tm_out, buf, col, wrow0, l2_policy_evict_first());
+                bulk_commit();
+            }
+            sbuf ^= 1u;
+        } else if (row_ok) {
+            store_row32(p.out + static_cast<size_t>(grow) * p.n_out + col, packed);
+        }
+    };
+    if (SWIGLU) {
+#pragma unroll 1
+        for (int c = 0; c < NCOL; c += 32) {
+            uint32_t g[32], u[32];
+            tmem_ld_32x32b_x32(tbase + c, g);
+            tmem_ld_32x32b_x32(tbase + BN_ACC / 2 + c, u);
+            tmem_ld_wait();
+            uint32_t packed[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                float h2[2];
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const float gv = __uint_as_float(g[2 * i + k]);
+                    const float uv = __uint_as_float(u[2 * i + k]);
+                    h2[k] = gv * __frcp_rn(1.0f + __expf(-gv)) * uv;
+                }
+                packed[i] = pack_bf16x2(h2[0], h2[1]);
+            }
+            emit(c, packed);
+        }
+    } else {
+        // two 32-column loads per wait, so TMEM latency is paid 4 times per tile, not 8
+#pragma unroll 1
+        for (int c = 0; c < NCOL; c += 64) {
+            uint32_t v[2][32];
+            tmem_ld_32x32b_x32(tbase + c, v[0]);
+            tmem_ld_32x32b_x32(tbase + c + 32, v[1]);
+            tmem_ld_wait();
+#pragma unroll
+            for (int hlf = 0; hlf < 2; ++hlf) {
+                uint32_t packed[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    packed[i] = pack_bf16x2(__uint_as_float(v[hlf][2 * i]), __uint_as_float(v[hlf][2 * i + 1]));
+                emit(c + 32 * hlf, packed);
+            }
+        }
+    }
+}
+
+}  // namespace gg
+}  // namespace moe

@@ -1,0 +1,360 @@
+// MXFP8 block-scaled persistent grouped GEMM over ragged expert groups, sm_103a.
+//
+// "Optimization 1: Grouped GEMM" of "Accelerating dropless MoE training in JAX
+// with NVIDIA Transformer Engine": all expert matmuls in one kernel call with
+// their actual token counts, and on Blackwell with MXFP8 block scaling.
+//
+//   GEMM1 (SWIGLU = true):  h = silu(xq . W1q_gate^T) * (xq . W1q_up^T), then
+//                           h is quantised to MXFP8 (blocks of 32 along f):
+//                           codes hq [TK, f] and scale atoms for GEMM2's A
+//   GEMM2 (SWIGLU = false): y_perm = bf16(hq . W2q^T)
+// Operands are E4M3 codes with one UE8M0 scale per 32 elements of K; the
+// products of the dequantised values are accumulated in fp32 in TMEM.
+//
+// Design (single CTA per tile, 128 rows x 256 accumulator columns; the tile
+// scheduler, raster order and bf16 epilogue are the bf16 kernel's):
+//  * Stage = one 128-element K slice: the A tile (128 rows x 128 B), the B
+//    tile (two 128-row boxes: GEMM1 gate and up rows, GEMM2 256 rows), both
+//    by TMA with 128-byte swizzle, and three 512-byte scale atoms (A, two B
+//    row blocks) by bulk copies.  4 stages of 50 KB.
+//  * The MMA thread copies a stage's atoms into that stage's slot of a TMEM
+//    scale ring (tcgen05.cp 32x128b.warpx4: A at columns +0..3, B at
+//    +4..11), then issues four tcgen05.mma kind::mxf8f6f4 block_scale
+//    (M=128, N=256, K=32), the k-th reading scale byte k.  The copies and the
+//    MMAs of one thread execute in issue order, and a slot is rewritten only
+//    after its stage's MMAs completed (the shared-memory stage was freed by
+//    their commit), so the ring needs no further synchronisation.
+//  * One accumulator (256 columns); the other 256 TMEM columns hold the
+//    scale ring.  The epilogue of a tile therefore runs between mainloops;
+//    the TMA producer keeps filling the ring meanwhile.
+//  * Scale atoms are addressed by 128-row blocks: A and h by the tile's row
+//    block (rb = row blocks of earlier experts + the tile's block inside its
+//    expert), the weights by their global row / 128.  Every atom index is
+//    clamped to its buffer, so no content of offsets[] can send a bulk copy
+//    out of bounds.
+//  * Bounded waits as in the bf16 kernel.
+#include <algorithm>
+
+#include "gemm_common.cuh"
+#include "kernels.h"
+#include "mxfp8.cuh"
+#include "ptx.cuh"
+#include "tmap.h"
+
+namespace moe {
+namespace gmx {
+
+using gg::BN_ACC;
+using gg::EPI_BUF;
+using gg::EPI_BYTES;
+using gg::MAX_E;
+
+constexpr int BM = 128;
+constexpr int BK = 128;          // elements (= bytes) of K per stage
+constexpr int UMMA_K = 32;
+constexpr int BAND = 16;
+constexpr int THREADS = 192;
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK;
+constexpr int B_BYTES = BN_ACC * BK;
+constexpr int SF_OFF = A_BYTES + B_BYTES;
+constexpr int SF_BYTES = 3 * 512;
+constexpr int STAGE = 51200;     // 1024-aligned
+constexpr int TX_BYTES = A_BYTES + B_BYTES + SF_BYTES;
+constexpr int TMEM_COLS = 512;
+constexpr int SF_COL0 = BN_ACC;  // scale ring after the accumulator
+constexpr int SF_SLOT = 16;
+static_assert(SF_OFF + SF_BYTES <= STAGE && STAGE % 1024 == 0, "stage layout");
+static_assert(SF_COL0 + STAGES * SF_SLOT <= TMEM_COLS, "TMEM budget");
+
+constexpr int OFF_EPI = STAGES * STAGE;
+constexpr int OFF_BARS = OFF_EPI + EPI_BYTES;
+constexpr int NUM_BARS = 2 * STAGES + 3;  // full, empty, tfull, tempty, drain
+constexpr int OFF_TMEM = OFF_BARS + NUM_BARS * 8;
+constexpr int OFF_ABORT = OFF_TMEM + 4;
+constexpr int OFF_OFFS = OFF_ABORT + 4;
+constexpr int OFF_ENDS = OFF_OFFS + MAX_E * 4;
+constexpr int OFF_PRE = OFF_ENDS + MAX_E * 4;
+constexpr int OFF_MIX = OFF_PRE + (MAX_E + 1) * 4;
+constexpr int SMEM_BYTES = OFF_MIX + 4 + 1024;
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+
+struct MxParams {
+    gg::Params g;
+    const uint8_t *sfa;   // A scale atoms (row blocks of the expert groups)
+    size_t sfa_atoms;
+    const uint8_t *sfb;   // weight scale atoms (row blocks of the weight matrix)
+    size_t sfb_atoms;
+    uint8_t *hq;          // GEMM1: h codes [TK, n_out]
+    uint32_t *sfh;        // GEMM1: h scale atoms, as words
+    size_t sfh_atoms;
+};
+
+__device__ __forceinline__ size_t clamp_atom(size_t a, size_t n) { return a < n ? a : n - 1; }
+
+// GEMM1 epilogue of one warp: 32 rows, the tile's 128 output columns of h
+// (gate columns 0..127 and up columns 128..255 of the accumulator).  Each
+// thread owns one row: per 32-column block it forms h, quantises it and
+// stores 32 code bytes; the four blocks' scale bytes are one word of the h
+// atom for this row block and column slice.
+__device__ __forceinline__ void epilogue_swiglu_mx(const MxParams &mp, uint32_t tbase, const gg::Tile &t, int q,
+                                                   int lane, int rb) {
+    const gg::Params &p = mp.g;
+    const int wrow0 = t.row0 + q * 32;
+    if (wrow0 >= t.grp_end) return;  // warp-uniform
+    const int grow = wrow0 + lane;
+    const bool row_ok = grow < t.grp_end;
+    uint32_t scales = 0;
+#pragma unroll 1
+    for (int c = 0; c < BN_ACC / 2; c += 32) {
+        uint32_t g[32], u[32];
+        tmem_ld_32x32b_x32(tbase + c, g);
+        tmem_ld_32x32b_x32(tbase + BN_ACC / 2 + c, u);
+        tmem_ld_wait();
+        float h[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const float gv = __uint_as_float(g[i]);
+            h[i] = gv * __frcp_rn(1.0f + __expf(-gv)) * __uint_as_float(u[i]);
+        }
+        uint32_t packed[8];
+        scales |= mx::quant_block(h, packed) << (8 * (c / 32));
+        if (row_ok) {
+            uint4 *dst = reinterpret_cast<uint4 *>(mp.hq + static_cast<size_t>(grow) * p.n_out + t.n_blk * 128 + c);
+            dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+            dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+        }
+    }
+    if (row_ok) {
+        const int ns = p.n_out / 128;
+        const size_t atom = clamp_atom(static_cast<size_t>(rb) * ns + t.n_blk, mp.sfh_atoms);
+        mp.sfh[atom * 128 + ((grow - t.row0) & 31) * 4 + ((grow - t.row0) >> 5)] = scales;
+    }
+}
+
+template <bool SWIGLU>
+__global__ void __launch_bounds__(THREADS, 1)
+grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                       const __grid_constant__ CUtensorMap tmOut, const MxParams mp) {
+    const gg::Params &p = mp.g;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_BARS);
+    uint64_t *full = bars;
+    uint64_t *empty = bars + STAGES;
+    uint64_t *tfull = bars + 2 * STAGES;
+    uint64_t *tempty = tfull + 1;
+    uint64_t *drain = tfull + 2;
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(smem + OFF_TMEM);
+    volatile int *s_abort = reinterpret_cast<volatile int *>(smem + OFF_ABORT);
+    int *s_off = reinterpret_cast<int *>(smem + OFF_OFFS);
+    int *s_end = reinterpret_cast<int *>(smem + OFF_ENDS);
+    int *s_pre = reinterpret_cast<int *>(smem + OFF_PRE);
+    int *s_mix = reinterpret_cast<int *>(smem + OFF_MIX);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int E = p.E;
+    const int NT = p.NT;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < STAGES; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        mbar_init(tfull, 1);
+        mbar_init(tempty, 4);
+        mbar_init(drain, 1);
+        *s_abort = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(s_tmem, TMEM_COLS);
+        tmem_relinquish();
+    }
+    if (warp == 2) gg::build_groups<BM>(p, lane, s_off, s_end, s_pre, s_mix);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    const uint32_t tmem_base = *s_tmem;
+    const int total_tiles = s_pre[E];
+    const int mix = *s_mix;
+    const int KB = p.Kdim / BK;
+    const size_t wrows_total = static_cast<size_t>(E) * p.w_rows;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int armed_phase[STAGES];
+#pragma unroll
+            for (int i = 0; i < STAGES; ++i) armed_phase[i] = -1;
+            uint32_t stage = 0, phase = 0;
+            bool ok = true;
+            for (int k = 0, tile = gg::round_position(0, blockIdx.x, gridDim.x, mix); ok && tile < total_tiles;
+                 ++k, tile = gg::round_position(k, blockIdx.x, gridDim.x, mix)) {
+                const gg::Tile t =
+                    gg::decode_tile<BM, BAND>(gg::visit_order(tile, total_tiles, mix), s_pre, s_off, s_end, E, NT);
+                const int rb = s_pre[t.e] / NT + t.m_blk;
+                int brow0, brow1;
+                if (SWIGLU) {
+                    brow0 = t.e * p.w_rows + t.n_blk * (BN_ACC / 2);
+                    brow1 = brow0 + p.n_out;  // the up half starts f rows later
+                } else {
+                    brow0 = t.e * p.w_rows + t.n_blk * BN_ACC;
+                    brow1 = brow0 + BN_ACC / 2;
+                }
+                // a B block past the last weight row only feeds masked columns:
+                // take any valid atom for it
+                const size_t wb0 = static_cast<size_t>(brow0) / 128;
+                const size_t wb1 = static_cast<size_t>(brow1) < wrows_total ? static_cast<size_t>(brow1) / 128 : wb0;
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, s_abort, p.status, p.timeout_ns)) { ok = false; break; }
+                    uint8_t *sa = smem + stage * STAGE;
+                    uint8_t *sb = sa + A_BYTES;
+                    uint8_t *ssf = sa + SF_OFF;
+                    mbar_arrive_expect_tx(&full[stage], TX_BYTES);
+                    tma_load_2d(sa, &tmA, &full[stage], kb * BK, t.row0);
+                    tma_load_2d(sb, &tmB, &full[stage], kb * BK, brow0);
+                    tma_load_2d(sb + B_BYTES / 2, &tmB, &full[stage], kb * BK, brow1);
+                    bulk_load(ssf, mp.sfa + clamp_atom(static_cast<size_t>(rb) * KB + kb, mp.sfa_atoms) * 512, 512,
+                              &full[stage]);
+                    bulk_load(ssf + 512, mp.sfb + clamp_atom(wb0 * KB + kb, mp.sfb_atoms) * 512, 512, &full[stage]);
+                    bulk_load(ssf + 1024, mp.sfb + clamp_atom(wb1 * KB + kb, mp.sfb_atoms) * 512, 512, &full[stage]);
+                    armed_phase[stage] = static_cast<int>(phase);
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+            }
+            if (!ok) {
+                volatile int no_abort = 0;
+                for (int i = 0; i < STAGES; ++i)
+                    if (armed_phase[i] >= 0)
+                        mbar_wait(&full[i], static_cast<uint32_t>(armed_phase[i]), &no_abort, p.status, p.timeout_ns);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0, acc_phase = 0;
+            bool ok = true, issued = false;
+            for (int k = 0, tile = gg::round_position(0, blockIdx.x, gridDim.x, mix); ok && tile < total_tiles;
+                 ++k, tile = gg::round_position(k, blockIdx.x, gridDim.x, mix)) {
+                if (!mbar_wait(tempty, acc_phase ^ 1u, s_abort, p.status, p.timeout_ns)) { ok = false; break; }
+                tc_fence_after();
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!mbar_wait(&full[stage], phase, s_abort, p.status, p.timeout_ns)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(smem + stage * STAGE);
+                    const uint32_t t_sfa = tmem_base + SF_COL0 + stage * SF_SLOT;
+                    const uint32_t t_sfb = t_sfa + 4;
+                    tmem_cp_32x128b_warpx4(t_sfa, smem_desc_rows16(sa + SF_OFF));
+                    tmem_cp_32x128b_warpx4(t_sfb, smem_desc_rows16(sa + SF_OFF + 512));
+                    tmem_cp_32x128b_warpx4(t_sfb + 4, smem_desc_rows16(sa + SF_OFF + 1024));
+                    const uint64_t adesc = smem_desc_kmajor_sw128(sa);
+                    const uint64_t bdesc = smem_desc_kmajor_sw128(sa + A_BYTES);
+#pragma unroll
+                    for (int j = 0; j < BK / UMMA_K; ++j)
+                        umma_mxf8(tmem_base, adesc + 2 * j, bdesc + 2 * j, idesc_mxf8(BM, BN_ACC, j), t_sfa, t_sfb,
+                                  (kb | j) != 0);
+                    issued = true;
+                    umma_commit(&empty[stage]);
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                umma_commit(tfull);
+                acc_phase ^= 1u;
+            }
+            if (!ok && issued) {
+                volatile int no_abort = 0;
+                umma_commit(drain);
+                mbar_wait(drain, 0, &no_abort, p.status, p.timeout_ns);
+            }
+        }
+    } else {
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        uint8_t *stage_buf = smem + OFF_EPI + (warp - 2) * 2 * EPI_BUF;
+        uint32_t sbuf = 0;
+        uint32_t acc_phase = 0;
+        for (int k = 0, tile = gg::round_position(0, blockIdx.x, gridDim.x, mix); tile < total_tiles;
+             ++k, tile = gg::round_position(k, blockIdx.x, gridDim.x, mix)) {
+            const gg::Tile t =
+                gg::decode_tile<BM, BAND>(gg::visit_order(tile, total_tiles, mix), s_pre, s_off, s_end, E, NT);
+            if (!mbar_wait(tfull, acc_phase, s_abort, p.status, p.timeout_ns)) break;
+            tc_fence_after();
+            const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+            if (SWIGLU)
+                epilogue_swiglu_mx(mp, tbase, t, q, lane, s_pre[t.e] / NT + t.m_blk);
+            else
+                gg::epilogue_tile<false>(p, &tmOut, stage_buf, sbuf, tbase, t.n_blk, t.row0 + q * 32, lane,
+                                         t.grp_end);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty);
+            acc_phase ^= 1u;
+        }
+        if (lane == 0) bulk_wait_all();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+}  // namespace gmx
+
+cudaError_t grouped_gemm_mx_setup() {
+    cudaError_t e;
+    if ((e = cudaFuncSetAttribute(gmx::grouped_gemm_mx_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  gmx::SMEM_BYTES)) != cudaSuccess)
+        return e;
+    return cudaFuncSetAttribute(gmx::grouped_gemm_mx_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                gmx::SMEM_BYTES);
+}
+
+cudaError_t launch_grouped_gemm_mx(bool swiglu, const uint8_t *A, const uint8_t *sfa, size_t sfa_bytes, int TK,
+                                   int Kdim, const uint8_t *W, const uint8_t *sfw, size_t sfw_bytes, int E, int n_out,
+                                   const int32_t *offsets, void *out, uint8_t *sfo, size_t sfo_bytes,
+                                   const GemmLaunch &cfg, int *status, uint64_t timeout_ns, cudaStream_t stream) {
+    const int w_rows = swiglu ? 2 * n_out : n_out;
+    CUtensorMap tmA, tmB, tmOut;
+    if (!make_tmap_u8(&tmA, A, static_cast<uint64_t>(TK), static_cast<uint64_t>(Kdim), gmx::BM))
+        return cudaErrorInvalidValue;
+    if (!make_tmap_u8(&tmB, W, static_cast<uint64_t>(E) * w_rows, static_cast<uint64_t>(Kdim), 128))
+        return cudaErrorInvalidValue;
+    if (swiglu) {
+        tmOut = tmA;  // unused: GEMM1 stores h codes directly
+    } else if (!make_tmap(&tmOut, out, static_cast<uint64_t>(TK), static_cast<uint64_t>(n_out), 32, 32,
+                          CU_TENSOR_MAP_SWIZZLE_64B)) {
+        return cudaErrorInvalidValue;
+    }
+    gmx::MxParams mp;
+    gg::Params &p = mp.g;
+    p.offsets = offsets;
+    p.E = E;
+    p.TK = TK;
+    p.Kdim = Kdim;
+    p.n_out = n_out;
+    p.w_rows = w_rows;
+    p.NT = swiglu ? n_out / (gg::BN_ACC / 2) : (n_out + gg::BN_ACC - 1) / gg::BN_ACC;
+    p.out = swiglu ? nullptr : static_cast<__nv_bfloat16 *>(out);
+    p.status = status;
+    p.timeout_ns = timeout_ns;
+    mp.sfa = sfa;
+    mp.sfa_atoms = sfa_bytes / 512;
+    mp.sfb = sfw;
+    mp.sfb_atoms = sfw_bytes / 512;
+    mp.hq = swiglu ? static_cast<uint8_t *>(out) : nullptr;
+    mp.sfh = reinterpret_cast<uint32_t *>(sfo);
+    mp.sfh_atoms = sfo_bytes / 512;
+    if (mp.sfa_atoms == 0 || mp.sfb_atoms == 0 || (swiglu && mp.sfh_atoms == 0)) return cudaErrorInvalidValue;
+    if (swiglu)
+        gmx::grouped_gemm_mx_kernel<true><<<cfg.num_sms, gmx::THREADS, gmx::SMEM_BYTES, stream>>>(tmA, tmB, tmOut, mp);
+    else
+        gmx::grouped_gemm_mx_kernel<false><<<cfg.num_sms, gmx::THREADS, gmx::SMEM_BYTES, stream>>>(tmA, tmB, tmOut, mp);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -38,6 +38,25 @@ cudaError_t launch_permute(const uint16_t *x, const int32_t *row_of, int T, int 
 cudaError_t launch_unpermute(const uint16_t *y_perm, const int32_t *row_of, const float *topk_w, int T, int K,
                              int d, uint16_t *y, cudaStream_t stream);
 
+// MXFP8 (E4M3 codes, one power-of-two scale byte per 32 elements along K,
+// scales stored as 512-byte atoms of 128 rows x one 128-wide K slice).
+size_t mxfp8_scales_bytes(int rows, int K);
+size_t mxfp8_perm_scales_bytes(int TK, int E, int K);
+cudaError_t launch_mxfp8_quantize(const uint16_t *src, int rows, int K, uint8_t *codes, uint8_t *scales,
+                                  cudaStream_t stream);
+cudaError_t launch_permute_mxfp8(const uint16_t *x, const int32_t *topk_idx, const int32_t *row_of,
+                                 const int32_t *offsets, int T, int K, int d, int E, uint8_t *xq, uint8_t *sfa,
+                                 cudaStream_t stream);
+
+// MXFP8 grouped GEMMs (single-CTA tiles).  swiglu: GEMM1 (A = x codes [TK, d],
+// W = W1 codes [E, 2f, d], out = h codes [TK, f], sfo = h scale atoms);
+// else GEMM2 (A = h codes [TK, f], W = W2 codes [E, d, f], out = y_perm bf16).
+cudaError_t grouped_gemm_mx_setup();
+cudaError_t launch_grouped_gemm_mx(bool swiglu, const uint8_t *A, const uint8_t *sfa, size_t sfa_bytes, int TK,
+                                   int Kdim, const uint8_t *W, const uint8_t *sfw, size_t sfw_bytes, int E, int n_out,
+                                   const int32_t *offsets, void *out, uint8_t *sfo, size_t sfo_bytes,
+                                   const struct GemmLaunch &cfg, int *status, uint64_t timeout_ns, cudaStream_t stream);
+
 // Per-device launch shape of the grouped GEMM: SM count, and how many CTA
 // pairs of the pair kernel can be resident at once (0: single-CTA only).
 struct GemmLaunch {

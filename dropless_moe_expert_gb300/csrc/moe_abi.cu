@@ -43,6 +43,7 @@ moe_status_t device_state(DeviceState **out) {
         if (major != 10) return MOE_ERR_UNSUPPORTED;  // built for sm_103a only
         if (moe::grouped_gemm_setup(s.num_sms, &s.gemm) != cudaSuccess) return MOE_ERR_CUDA;
         if (moe::router_setup() != cudaSuccess) return MOE_ERR_CUDA;
+        if (moe::grouped_gemm_mx_setup() != cudaSuccess) return MOE_ERR_CUDA;
         if (cudaGetSymbolAddress(reinterpret_cast<void **>(&s.status), g_device_status) != cudaSuccess)
             return MOE_ERR_CUDA;
         s.ready = true;
@@ -92,6 +93,39 @@ bool forward_layout(int T, int d, int E, int K, int f, moe_forward_layout_t *L) 
     L->y_dev = take(static_cast<size_t>(T) * d * 2);
     L->total = o;
     return true;
+}
+
+bool forward_mxfp8_layout(int T, int d, int E, int K, int f, moe_forward_mxfp8_layout_t *L) {
+    const size_t TK = static_cast<size_t>(T) * K;
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = o;
+        o = align_up(o + bytes, 256);
+        return at;
+    };
+    L->logits = take(static_cast<size_t>(T) * E * 4);
+    L->topk_idx = take(TK * 4);
+    L->topk_w = take(TK * 4);
+    L->counts = take(static_cast<size_t>(E) * 4);
+    L->offsets = take(static_cast<size_t>(E + 1) * 4);
+    L->row_of = take(TK * 4);
+    L->src_tok = take(TK * 4);
+    L->route_ws = take(moe::route_workspace_bytes(T, E));
+    L->router_ws = take(moe::router_workspace_bytes(d, E));
+    L->xq_perm = take(TK * d);
+    L->sfa = take(moe::mxfp8_perm_scales_bytes(static_cast<int>(TK), E, d));
+    L->hq = take(TK * f);
+    L->sfh = take(moe::mxfp8_perm_scales_bytes(static_cast<int>(TK), E, f));
+    L->y_perm = take(TK * d * 2);
+    L->total = o;
+    return true;
+}
+
+moe_status_t check_mx_shape(int T, int d, int E, int K, int f) {
+    moe_status_t st = check_shape(T, d, E, K, f, true, true);
+    if (st != MOE_OK) return st;
+    if (d % 128 != 0 || f % 128 != 0) return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
 }
 
 moe_status_t run_gemm(bool swiglu, const void *A, const int32_t *offsets, int E, int TK, int d, int f,
@@ -288,6 +322,138 @@ moe_status_t moe_forward_host(const uint16_t *x_host, const float *Wr, const flo
         MOE_OK)
         return st;
     return cuda_status(cudaMemcpyAsync(y_host, y_dev, bytes, cudaMemcpyDeviceToHost, stream));
+}
+
+size_t moe_mxfp8_scales_size(int rows, int K) {
+    if (rows < 1 || K < 128 || K % 128 != 0) return 0;
+    return moe::mxfp8_scales_bytes(rows, K);
+}
+
+moe_status_t moe_mxfp8_quantize(const uint16_t *src, int rows, int K, uint8_t *codes, uint8_t *scales,
+                                cudaStream_t stream) {
+    if (!src || !codes || !scales) return MOE_ERR_INVALID_ARG;
+    if (!aligned(src, 16) || !aligned(codes, 16) || !aligned(scales, 16)) return MOE_ERR_INVALID_ARG;
+    if (rows < 1 || K < 1) return MOE_ERR_INVALID_ARG;
+    if (K % 128 != 0) return MOE_ERR_UNSUPPORTED;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return cuda_status(moe::launch_mxfp8_quantize(src, rows, K, codes, scales, stream));
+}
+
+size_t moe_mxfp8_act_scales_size(int TK, int E, int K) {
+    if (TK < 1 || E < 1 || E > kMaxE || K < 128 || K % 128 != 0) return 0;
+    return moe::mxfp8_perm_scales_bytes(TK, E, K);
+}
+
+moe_status_t moe_permute_mxfp8(const uint16_t *x, const int32_t *topk_idx, const int32_t *row_of,
+                               const int32_t *offsets, int T, int K, int d, int E, uint8_t *xq_perm, uint8_t *sfa,
+                               size_t sfa_bytes, cudaStream_t stream) {
+    if (!x || !topk_idx || !row_of || !offsets || !xq_perm || !sfa) return MOE_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(xq_perm, 16) || !aligned(sfa, 16) || !aligned(topk_idx, 4) ||
+        !aligned(row_of, 4) || !aligned(offsets, 4))
+        return MOE_ERR_INVALID_ARG;
+    moe_status_t st = check_shape(T, d, E, K, 64, true, false);
+    if (st != MOE_OK) return st;
+    if (d % 128 != 0) return MOE_ERR_UNSUPPORTED;
+    if (sfa_bytes < moe::mxfp8_perm_scales_bytes(T * K, E, d)) return MOE_ERR_WORKSPACE;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return cuda_status(moe::launch_permute_mxfp8(x, topk_idx, row_of, offsets, T, K, d, E, xq_perm, sfa, stream));
+}
+
+moe_status_t moe_grouped_gemm1_swiglu_mxfp8(const uint8_t *xq_perm, const uint8_t *sfa, size_t sfa_bytes,
+                                            const int32_t *offsets, int E, int TK, int d, int f, const uint8_t *W1q,
+                                            const uint8_t *W1s, uint8_t *hq, uint8_t *sfh, size_t sfh_bytes,
+                                            cudaStream_t stream) {
+    if (!xq_perm || !sfa || !offsets || !W1q || !W1s || !hq || !sfh) return MOE_ERR_INVALID_ARG;
+    if (!aligned(xq_perm, 16) || !aligned(sfa, 16) || !aligned(W1q, 16) || !aligned(W1s, 16) || !aligned(hq, 16) ||
+        !aligned(sfh, 16) || !aligned(offsets, 4))
+        return MOE_ERR_INVALID_ARG;
+    moe_status_t st = check_mx_shape(TK, d, E, 1, f);
+    if (st != MOE_OK) return st;
+    if (sfa_bytes < moe::mxfp8_perm_scales_bytes(TK, E, d) || sfh_bytes < moe::mxfp8_perm_scales_bytes(TK, E, f))
+        return MOE_ERR_WORKSPACE;
+    DeviceState *ds = nullptr;
+    if ((st = device_state(&ds)) != MOE_OK) return st;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return cuda_status(moe::launch_grouped_gemm_mx(true, xq_perm, sfa, sfa_bytes, TK, d, W1q, W1s,
+                                                   moe::mxfp8_scales_bytes(E * 2 * f, d), E, f, offsets, hq, sfh,
+                                                   sfh_bytes, ds->gemm, ds->status, kWaitLimitNs, stream));
+}
+
+moe_status_t moe_grouped_gemm2_mxfp8(const uint8_t *hq, const uint8_t *sfh, size_t sfh_bytes, const int32_t *offsets,
+                                     int E, int TK, int d, int f, const uint8_t *W2q, const uint8_t *W2s,
+                                     uint16_t *y_perm, cudaStream_t stream) {
+    if (!hq || !sfh || !offsets || !W2q || !W2s || !y_perm) return MOE_ERR_INVALID_ARG;
+    if (!aligned(hq, 16) || !aligned(sfh, 16) || !aligned(W2q, 16) || !aligned(W2s, 16) || !aligned(y_perm, 16) ||
+        !aligned(offsets, 4))
+        return MOE_ERR_INVALID_ARG;
+    moe_status_t st = check_mx_shape(TK, d, E, 1, f);
+    if (st != MOE_OK) return st;
+    if (sfh_bytes < moe::mxfp8_perm_scales_bytes(TK, E, f)) return MOE_ERR_WORKSPACE;
+    DeviceState *ds = nullptr;
+    if ((st = device_state(&ds)) != MOE_OK) return st;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return cuda_status(moe::launch_grouped_gemm_mx(false, hq, sfh, sfh_bytes, TK, f, W2q, W2s,
+                                                   moe::mxfp8_scales_bytes(E * d, f), E, d, offsets, y_perm, nullptr,
+                                                   0, ds->gemm, ds->status, kWaitLimitNs, stream));
+}
+
+size_t moe_forward_mxfp8_workspace_size(int T, int d, int E, int K, int f) {
+    if (check_mx_shape(T, d, E, K, f) != MOE_OK) return 0;
+    moe_forward_mxfp8_layout_t L;
+    forward_mxfp8_layout(T, d, E, K, f, &L);
+    return L.total;
+}
+
+moe_status_t moe_forward_mxfp8_views(int T, int d, int E, int K, int f, moe_forward_mxfp8_layout_t *layout) {
+    if (!layout) return MOE_ERR_INVALID_ARG;
+    moe_status_t st = check_mx_shape(T, d, E, K, f);
+    if (st != MOE_OK) return st;
+    forward_mxfp8_layout(T, d, E, K, f, layout);
+    return MOE_OK;
+}
+
+moe_status_t moe_forward_mxfp8(const uint16_t *x, const float *Wr, const float *bias, const uint8_t *W1q,
+                               const uint8_t *W1s, const uint8_t *W2q, const uint8_t *W2s, int T, int d, int E, int K,
+                               int f, uint16_t *y, void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    if (!x || !Wr || !W1q || !W1s || !W2q || !W2s || !y || !workspace) return MOE_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(y, 16) || !aligned(workspace, 16) || !aligned(Wr, 4) ||
+        (bias && !aligned(bias, 4)))
+        return MOE_ERR_INVALID_ARG;
+    moe_status_t st = check_mx_shape(T, d, E, K, f);
+    if (st != MOE_OK) return st;
+    moe_forward_mxfp8_layout_t L;
+    forward_mxfp8_layout(T, d, E, K, f, &L);
+    if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    auto at = [&](size_t off) { return static_cast<void *>(ws + off); };
+    const int TK = T * K;
+    float *logits = static_cast<float *>(at(L.logits));
+    int32_t *idx = static_cast<int32_t *>(at(L.topk_idx));
+    float *w = static_cast<float *>(at(L.topk_w));
+    int32_t *counts = static_cast<int32_t *>(at(L.counts));
+    int32_t *offsets = static_cast<int32_t *>(at(L.offsets));
+    int32_t *row_of = static_cast<int32_t *>(at(L.row_of));
+    int32_t *src_tok = static_cast<int32_t *>(at(L.src_tok));
+    uint8_t *xq = static_cast<uint8_t *>(at(L.xq_perm));
+    uint8_t *sfa = static_cast<uint8_t *>(at(L.sfa));
+    uint8_t *hq = static_cast<uint8_t *>(at(L.hq));
+    uint8_t *sfh = static_cast<uint8_t *>(at(L.sfh));
+    uint16_t *y_perm = static_cast<uint16_t *>(at(L.y_perm));
+    if ((st = moe_router_logits(x, Wr, bias, T, d, E, logits, at(L.router_ws), L.xq_perm - L.router_ws, stream)) !=
+        MOE_OK)
+        return st;
+    if ((st = moe_route(logits, T, E, K, idx, w, counts, offsets, row_of, src_tok, at(L.route_ws),
+                        L.router_ws - L.route_ws, stream)) != MOE_OK)
+        return st;
+    if ((st = moe_permute_mxfp8(x, idx, row_of, offsets, T, K, d, E, xq, sfa, L.hq - L.sfa, stream)) != MOE_OK)
+        return st;
+    if ((st = moe_grouped_gemm1_swiglu_mxfp8(xq, sfa, L.hq - L.sfa, offsets, E, TK, d, f, W1q, W1s, hq, sfh,
+                                             L.y_perm - L.sfh, stream)) != MOE_OK)
+        return st;
+    if ((st = moe_grouped_gemm2_mxfp8(hq, sfh, L.y_perm - L.sfh, offsets, E, TK, d, f, W2q, W2s, y_perm, stream)) !=
+        MOE_OK)
+        return st;
+    return moe_unpermute(y_perm, row_of, w, T, K, d, y, stream);
 }
 
 moe_status_t moe_check_bounded_wait(uint64_t limit_ns, cudaStream_t stream) {

@@ -1,0 +1,40 @@
+// MXFP8 block quantiser and scale-atom addressing, shared by the
+// quantisation kernels and the GEMM1 epilogue (which quantises h).
+// Format and layout: see mxfp8.cu.
+#pragma once
+
+#include <cuda_fp8.h>
+#include <stdint.h>
+
+namespace moe {
+namespace mx {
+
+// 32 fp32 values -> 32 E4M3 codes packed little-endian in 8 words; returns
+// the scale byte e + 127.
+__device__ __forceinline__ uint32_t quant_block(const float (&v)[32], uint32_t (&packed)[8]) {
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    const uint32_t bits = __float_as_uint(amax);
+    const int be = static_cast<int>(bits >> 23);
+    int e = be == 0 ? -127 : (be - 127) - 8 + ((bits & 0x7fffffu) > 0x600000u ? 1 : 0);
+    e = max(e, -127);
+    const float inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);  // 2^-e, exact
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+        const __nv_fp8x2_storage_t lo =
+            __nv_cvt_float2_to_fp8x2(make_float2(v[4 * w] * inv, v[4 * w + 1] * inv), __NV_SATFINITE, __NV_E4M3);
+        const __nv_fp8x2_storage_t hi =
+            __nv_cvt_float2_to_fp8x2(make_float2(v[4 * w + 2] * inv, v[4 * w + 3] * inv), __NV_SATFINITE, __NV_E4M3);
+        packed[w] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+    }
+    return static_cast<uint32_t>(e + 127);
+}
+
+__device__ __forceinline__ size_t atom_word(int rb, int ks, int nslices, int i) {
+    // byte offset of row i (0..127) of atom (rb, ks), as a 4-byte word index
+    return (static_cast<size_t>(rb) * nslices + ks) * 128 + (i & 31) * 4 + (i >> 5);
+}
+
+}  // namespace mx
+}  // namespace moe

@@ -100,6 +100,15 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const void *tmap, uint64_
         : "memory");
 }
 
+// Non-tensor bulk copy global -> shared (both 16-byte aligned, bytes a
+// multiple of 16) that completes `bytes` of transaction on an mbarrier.
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // Makes this thread's generic-proxy shared-memory writes visible to the
 // async proxy (TMA stores, tensor-core operand reads).
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -252,6 +261,50 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
 }
 __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Block-scaled MMA: D[tmem] (+)= (A * scale_A) * (B * scale_B)^T with A and B
+// E4M3 (kind::mxf8f6f4), one UE8M0 scale per 32 elements of K read from
+// TMEM at sfa / sfb (the byte selected by the scale-factor ids of idesc).
+__device__ __forceinline__ void umma_mxf8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+        : "memory");
+}
+
+// Copies a 512-byte shared-memory block (32 rows x 16 bytes) into TMEM
+// columns taddr..taddr+3 of all four 32-lane quarters (row i -> lane i of
+// each quarter).  Ordered with this thread's later tcgen05.mma.
+__device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// Descriptor of 32 contiguous 16-byte shared-memory rows, no swizzle: 8-row
+// core matrices 128 bytes apart.
+__device__ __forceinline__ uint64_t smem_desc_rows16(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(128u >> 4) << 16;
+    d |= static_cast<uint64_t>(128u >> 4) << 32;
+    d |= static_cast<uint64_t>(1u) << 46;
+    return d;
+}
+
+// Instruction descriptor of tcgen05.mma kind::mxf8f6f4 with block scaling:
+// A and B E4M3, K-major, UE8M0 scales, shape M x N, scale-factor id `sfid`
+// (which byte of the scale columns) for both A and B.
+__host__ __device__ constexpr uint32_t idesc_mxf8(int M, int N, int sfid) {
+    return (static_cast<uint32_t>(sfid) << 4)          // B scale factor id
+           | (0u << 7) | (0u << 10)                    // A, B: E4M3
+           | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
+           | (1u << 23)                                // scales: UE8M0
+           | (static_cast<uint32_t>(M >> 4) << 24)     // M / 16
+           | (static_cast<uint32_t>(sfid) << 29);      // A scale factor id
 }
 
 // Shared-memory matrix descriptor of a K-major bf16 tile stored as rows of

@@ -188,6 +188,68 @@ moe_status_t moe_forward_host(const uint16_t *x_host, const float *Wr, const flo
                               int K, int f, uint16_t *y_host, void *workspace,
                               size_t workspace_bytes, cudaStream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * MXFP8 path ("Optimization 1: Grouped GEMM": on Blackwell the expert
+ * matmuls run with MXFP8 block scaling, fed by grouped quantisation).
+ * Format: E4M3 element codes (uint8), one scale byte s (value 2^(s-127)) per
+ * 32 consecutive elements along the reduction dimension; s is the smallest
+ * power of two with 448 * 2^(s-127) >= the block's largest magnitude, and
+ * each code is the element / 2^(s-127) rounded to nearest E4M3, ties to
+ * even.  Scales are stored as 512-byte atoms of 128 rows x 128 columns
+ * (4 blocks), byte (row % 32) * 16 + ((row % 128) / 32) * 4 + block.
+ * Requires d and f to be multiples of 128.  Codes and scale buffers are
+ * 16-byte aligned device memory owned by the caller.
+ * ------------------------------------------------------------------------ */
+
+/* Quantises a row-major bf16 matrix [rows, K] (K a multiple of 128) along K:
+ * codes [rows, K]; scale atoms for row block rb = row / 128 and column slice
+ * ks = k / 128 at byte offset (rb * (K / 128) + ks) * 512 of `scales`, which
+ * must hold moe_mxfp8_scales_size(rows, K) bytes.  The expert weights are
+ * quantised with this once: W1 as [E * 2f, d], W2 as [E * d, f].  */
+size_t moe_mxfp8_scales_size(int rows, int K);
+moe_status_t moe_mxfp8_quantize(const uint16_t *src, int rows, int K, uint8_t *codes, uint8_t *scales,
+                                cudaStream_t stream);
+
+/* Scale atoms of the permuted activations [TK, K] (rows grouped by expert
+ * by `offsets`): the rows of each expert group are cut into 128-row blocks
+ * from the group's first row; block b of expert e is row block
+ * rb = sum_{e'<e} ceil(count[e'] / 128) + b.  Size bound: */
+size_t moe_mxfp8_act_scales_size(int TK, int E, int K);
+
+/* Step a3 with quantisation: every token row of x [T, d] bf16 is quantised
+ * once and its codes written to the K rows of xq_perm [TK, d] it occupies
+ * (row_of), with its scales into those rows' atoms of `sfa`.  */
+moe_status_t moe_permute_mxfp8(const uint16_t *x, const int32_t *topk_idx, const int32_t *row_of,
+                               const int32_t *offsets, int T, int K, int d, int E, uint8_t *xq_perm,
+                               uint8_t *sfa, size_t sfa_bytes, cudaStream_t stream);
+
+/* Steps a4 and a5 in MXFP8.  GEMM1: h = silu(x.W1g^T) * (x.W1u^T) from the
+ * dequantised operands with fp32 accumulation, then quantised along f into
+ * hq [TK, f] and the atoms `sfh` (grouped layout).  GEMM2: y_perm [TK, d]
+ * bf16 = hq.W2q^T (fp32 accumulation).  W1s / W2s are the weight scales from
+ * moe_mxfp8_quantize.  */
+moe_status_t moe_grouped_gemm1_swiglu_mxfp8(const uint8_t *xq_perm, const uint8_t *sfa, size_t sfa_bytes,
+                                            const int32_t *offsets, int E, int TK, int d, int f,
+                                            const uint8_t *W1q, const uint8_t *W1s, uint8_t *hq, uint8_t *sfh,
+                                            size_t sfh_bytes, cudaStream_t stream);
+moe_status_t moe_grouped_gemm2_mxfp8(const uint8_t *hq, const uint8_t *sfh, size_t sfh_bytes,
+                                     const int32_t *offsets, int E, int TK, int d, int f, const uint8_t *W2q,
+                                     const uint8_t *W2s, uint16_t *y_perm, cudaStream_t stream);
+
+/* The whole layer with MXFP8 expert matmuls (router, routing and combine as
+ * in moe_forward; 9 kernel launches), weights pre-quantised by
+ * moe_mxfp8_quantize.  */
+size_t moe_forward_mxfp8_workspace_size(int T, int d, int E, int K, int f);
+typedef struct {
+    size_t logits, topk_idx, topk_w, counts, offsets, row_of, src_tok, route_ws, router_ws,
+           xq_perm, sfa, hq, sfh, y_perm, total;
+} moe_forward_mxfp8_layout_t;
+moe_status_t moe_forward_mxfp8_views(int T, int d, int E, int K, int f, moe_forward_mxfp8_layout_t *layout);
+moe_status_t moe_forward_mxfp8(const uint16_t *x, const float *Wr, const float *bias, const uint8_t *W1q,
+                               const uint8_t *W1s, const uint8_t *W2q, const uint8_t *W2s, int T, int d,
+                               int E, int K, int f, uint16_t *y, void *workspace, size_t workspace_bytes,
+                               cudaStream_t stream);
+
 /* Reads and clears the device status word of the current device (0 = OK, or
  * a moe_status_t a kernel recorded).  Synchronous: call outside capture. */
 moe_status_t moe_device_status(int *status_out);

@@ -112,6 +112,24 @@ def test_route_workspace_too_small(moe):
     assert r == 3
 
 
+def test_mxfp8_entry_points_reject_bad_arguments(moe):
+    L = moe.lib
+    assert moe.mxfp8_scales_size(300, 256) == 3 * 2 * 512          # 3 row blocks x 2 K slices
+    assert moe.mxfp8_act_scales_size(1000, 8, 256) == (8 + 8) * 2 * 512
+    assert L.moe_mxfp8_quantize(FAKE, 8, 192, FAKE, FAKE, None) == 2          # K % 128
+    assert L.moe_mxfp8_quantize(FAKE + 8, 8, 256, FAKE, FAKE, None) == 1      # misaligned
+    assert L.moe_permute_mxfp8(FAKE, FAKE, FAKE, FAKE, 8, 2, 192, 8, FAKE, FAKE, 1 << 30, None) == 2
+    assert L.moe_permute_mxfp8(FAKE, FAKE, FAKE, FAKE, 8, 2, 256, 8, FAKE, FAKE, 16, None) == 3
+    assert L.moe_grouped_gemm1_swiglu_mxfp8(FAKE, FAKE, 1 << 30, FAKE, 8, 16, 256, 192, FAKE, FAKE, FAKE, FAKE,
+                                           1 << 30, None) == 2                # f % 128
+    assert L.moe_grouped_gemm2_mxfp8(None, FAKE, 1 << 30, FAKE, 8, 16, 256, 256, FAKE, FAKE, FAKE, None) == 1
+    assert L.moe_forward_mxfp8(FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, 64, 256, 8, 2, 256, FAKE, FAKE, 16,
+                               None) == 3
+    v = moe.forward_mxfp8_views(8192, 4096, 8, 2, 14336)
+    assert v["hq"] - v["xq_perm"] >= 8192 * 2 * 4096
+    assert list(v.values()) == sorted(v.values())
+
+
 def test_no_launch_happened(moe):
     # every call above was rejected on the host
     assert moe.launch_count() == 0

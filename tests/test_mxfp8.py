@@ -1,0 +1,154 @@
+"""GPU parity of the MXFP8 path against the MXFP8 oracle (oracle/mxfp8.py).
+
+Integer work is bit-exact: the E4M3 codes and scale bytes of the weight
+quantiser and of the fused permute + quantise (both sides quantise the same
+bf16 values).  h is computed in fp32 on the GPU and in fp64 by the oracle
+before each is quantised, so the GPU's dequantised h is checked against the
+oracle's unquantised h within the E4M3 rounding bound of its block (half an
+ulp: 2^-4 relative in the normal range, 2^-10 of the block scale below it,
+with the scale allowed to be one binade above the oracle's).  y_perm and y
+have the bf16 path's tolerances against the oracle's MXFP8 forward.  Routing
+follows the rules of the bf16 tests (each side routes on its own fp32
+logits)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from workloads import Shape, make_tokens, make_weights
+
+from _helpers import check_logits, check_output, check_routing, to_np
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def unpack_plain_atoms(buf, R, K):
+    """Scale bytes [R, K/32] of a plain matrix from its 512-byte atoms."""
+    ns = K // 128
+    r = np.arange(R)
+    out = np.zeros((R, K // 32), np.uint8)
+    for ks in range(ns):
+        base = ((r // 128) * ns + ks) * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4
+        for b in range(4):
+            out[:, ks * 4 + b] = buf[base + b]
+    return out
+
+
+def unpack_group_atoms(buf, offsets, K):
+    """Scale bytes [TK, K/32] of rows grouped by expert (row blocks from each
+    group's first row)."""
+    ns = K // 128
+    counts = np.diff(offsets)
+    rbp = np.concatenate([[0], np.cumsum((counts + 127) // 128)])[:-1]
+    TK = int(offsets[-1])
+    r = np.arange(TK)
+    e = np.searchsorted(offsets, r, side="right") - 1
+    i = r - offsets[e]
+    rb = rbp[e] + i // 128
+    j = i % 128
+    out = np.zeros((TK, K // 32), np.uint8)
+    for ks in range(ns):
+        base = (rb * ns + ks) * 512 + (j % 32) * 16 + (j // 32) * 4
+        for b in range(4):
+            out[:, ks * 4 + b] = buf[base + b]
+    return out
+
+
+@pytest.mark.parametrize("R,K", [(300, 256), (128, 128), (1, 384), (257, 512)])
+def test_quantize_matches_oracle_bit_for_bit(R, K):
+    import dropless_moe_expert_gb300 as moe
+    g = torch.Generator().manual_seed(R + K)
+    x = torch.randn(R, K, generator=g) * torch.exp(3 * torch.randn(R, 1, generator=g))
+    x[0, :32] = 0.0                                   # a block of zeros
+    x[0, 32:64] = torch.linspace(-14.0, 14.0, 32)     # amax 14 = 1.75 * 2^3: lands exactly on 448
+    if K >= 128:
+        x[0, 64:96] = 0.5
+        x[0, 64] = 1.796875                           # mantissa above 1.75: one binade up
+    x = x.to(torch.bfloat16)
+    codes, sf = moe.mxfp8_quantize(x.to(DEV))
+    torch.cuda.synchronize()
+    rc, rs, _ = oracle.mx_quantize(x.float().numpy())
+    assert np.array_equal(codes.cpu().numpy(), rc)
+    assert np.array_equal(unpack_plain_atoms(sf.cpu().numpy(), R, K), rs)
+
+
+CASES = [
+    Shape(T=256, d=128, E=8, K=2, f=256),
+    Shape(T=300, d=256, E=64, K=8, f=128),
+    Shape(T=1000, d=384, E=8, K=1, f=384),
+    Shape(T=517, d=256, E=16, K=4, f=512, bias="normal_0.5"),
+    Shape(T=129, d=128, E=256, K=8, f=128),
+    Shape(T=2048, d=256, E=4, K=1, f=256),     # groups of several 128-row blocks
+    Shape(T=1500, d=128, E=3, K=2, f=640, bias="skew"),
+]
+
+
+def _run(s, seed):
+    import dropless_moe_expert_gb300 as moe
+    w = make_weights(s, seed=seed, device="cpu")
+    x = make_tokens(s, seed=seed, device="cpu")
+    wd = [t.to(DEV) for t in (w.Wr, w.bias, w.W1, w.W2)]
+    layer = moe.MoELayerMXFP8(*wd, s.K, s.T)
+    layer.workspace.fill_(0xFF)
+    y = layer(x.to(DEV))
+    torch.cuda.synchronize()
+    assert moe.device_status() == 0
+    return x, w, y, layer
+
+
+@pytest.mark.parametrize("s", CASES, ids=lambda s: f"T{s.T}_d{s.d}_E{s.E}_K{s.K}_f{s.f}")
+def test_layer_matches_mxfp8_oracle(s):
+    x, w, y, layer = _run(s, seed=s.T)
+    v = layer.views(s.T)
+    xs, Wr, bias = x.float().numpy(), w.Wr.numpy(), w.bias.numpy()
+    ref = oracle.forward_mxfp8(xs, Wr, bias, w.W1.float().numpy(), w.W2.float().numpy(), s.K)
+    _, scale, L64 = check_logits(to_np(v["logits"]), xs, Wr, bias)
+    same = check_routing(to_np(v["topk_idx"]), ref["idx"], L64, scale, s.K)
+    offs = to_np(v["offsets"])
+    rg = to_np(v["row_of"])[same].ravel()      # GPU rows of the equally routed tokens
+    ro = ref["row_of"][same].ravel()           # the oracle's rows of the same (token, slot)
+    tok = np.repeat(np.nonzero(same)[0], s.K)
+    # permute + quantise: codes and scales bit-exact
+    xq = to_np(v["xq_perm"])
+    assert np.array_equal(xq[rg], ref["xq"][tok])
+    sfa = unpack_group_atoms(to_np(v["sfa"]), offs, s.d)
+    assert np.array_equal(sfa[rg], ref["xs"][tok])
+    # h: dequantised GPU h against the oracle's unquantised h
+    hs = unpack_group_atoms(to_np(v["sfh"]), offs, s.f)
+    hd = oracle.mx_dequantize(to_np(v["hq"]), hs)[rg]
+    h = ref["h"][ro]
+    assert np.all(np.isfinite(hd))
+    X = np.repeat(np.ldexp(1.0, ref["hs"][ro].astype(np.int64) - 127), 32, axis=1)
+    bound = 2.0 ** -4 * np.abs(h) * (1 + 1e-4) + 2.0 ** -9 * X + 1e-6 * np.sqrt(np.mean(h ** 2))
+    excess = np.abs(hd - h) - bound
+    assert np.all(excess <= 0), f"h: {int((excess > 0).sum())} elements beyond the E4M3 rounding bound"
+    codes_equal = np.mean(to_np(v["hq"])[rg] == ref["hq"][ro])
+    check_output(to_np(v["y_perm"])[rg], ref["y_perm"][ro], "y_perm")
+    r = check_output(to_np(y)[same], ref["y"][same], "y")
+    y_bf16 = oracle.forward(xs, Wr, bias, w.W1.float().numpy(), w.W2.float().numpy(), s.K)["y"]
+    q_err = np.linalg.norm(to_np(y)[same] - y_bf16[same]) / np.linalg.norm(y_bf16[same])
+    print(f"{s}: h codes equal {codes_equal:.5f}; y rel_l2 {r[0]:.2e} vs the MXFP8 oracle, "
+          f"{q_err:.2e} vs the bf16 oracle")
+
+
+def test_step_by_step_api_matches_single_call():
+    import dropless_moe_expert_gb300 as moe
+    s = CASES[3]
+    x, w, y_one, layer = _run(s, seed=7)
+    xd = x.to(DEV)
+    L = moe.router_logits(xd, layer.Wr, layer.bias)
+    r = moe.route(L, s.K)
+    xq, sfa = moe.permute_mxfp8(xd, r)
+    hq, sfh = moe.grouped_gemm1_swiglu_mxfp8(xq, sfa, r.offsets, layer.W1q, layer.W1s)
+    yp = moe.grouped_gemm2_mxfp8(hq, sfh, r.offsets, layer.W2q, layer.W2s)
+    y = moe.unpermute(yp, r.row_of, r.topk_w)
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int16), y_one.view(torch.int16))
+
+
+def test_rejects_dims_not_multiple_of_128():
+    import dropless_moe_expert_gb300 as moe
+    assert moe.lib.moe_forward_mxfp8_workspace_size(64, 192, 8, 2, 256) == 0
+    assert moe.lib.moe_forward_mxfp8_workspace_size(64, 256, 8, 2, 192) == 0
+    assert moe.mxfp8_scales_size(10, 64) == 0
