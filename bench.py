@@ -2,7 +2,7 @@
 """Benchmark of the dropless MoE layer forward on GB300.
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
-                [--config mixtral|dsv3|qwen|skew|tiny]
+                [--config mixtral|dsv3|qwen|skew|tiny] [--precision bf16|mxfp8]
 
 One step = one pass of the whole forward (router logits, top-K routing +
 histogram/scan/dispatch order, permute, grouped GEMM1 + SwiGLU, grouped GEMM2,
@@ -17,6 +17,13 @@ step (only the valid rows of the two grouped GEMMs count), aggregated over
 ranks; per-kernel durations come from CUDA events on the launching stream
 inside the timed region.  `--impl reference` times the oracle (plain CPU
 implementation, fp64) on a bounded sample of the same workload.
+
+`--precision mxfp8` runs the expert matmuls with MXFP8 block scaling (E4M3
+elements, one UE8M0 scale per 32 along K): the expert weights are quantised
+once before the timed region (as a training step reuses them), the token
+activations inside every step (fused into the permute), and h inside GEMM1's
+epilogue.  Its roofline peak is the measured bf16 peak times the nominal
+fp8 / bf16 tensor ratio (2).
 """
 from __future__ import annotations
 
@@ -39,7 +46,7 @@ import torch  # noqa: E402
 from workloads import DESCRIPTIONS, make_tokens, make_weights, shape  # noqa: E402
 
 STEP_NAMES = ["router_logits", "route", "permute", "grouped_gemm1_swiglu", "grouped_gemm2", "unpermute"]
-KERNELS_PER_STEP = 8
+KERNELS_PER_STEP = 9
 
 
 def _peaks():
@@ -272,8 +279,17 @@ def run_gpu(args):
     topk_idx, row_of = torch.empty((T, K), **i32), torch.empty((T, K), **i32)
     topk_w = torch.empty((T, K), dtype=torch.float32, device=dev)
     counts, offsets, src_tok = torch.empty((E,), **i32), torch.empty((E + 1,), **i32), torch.empty((TK,), **i32)
-    x_perm = torch.empty((TK, d), dtype=torch.bfloat16, device=dev)
-    h = torch.empty((TK, f), dtype=torch.bfloat16, device=dev)
+    mxfp8 = args.precision == "mxfp8"
+    if mxfp8:
+        W1q, W1s = moe.mxfp8_quantize(w.W1)
+        W2q, W2s = moe.mxfp8_quantize(w.W2)
+        x_perm = torch.empty((TK, d), dtype=torch.uint8, device=dev)
+        sfa = torch.empty((moe.mxfp8_act_scales_size(TK, E, d),), dtype=torch.uint8, device=dev)
+        h = torch.empty((TK, f), dtype=torch.uint8, device=dev)
+        sfh = torch.empty((moe.mxfp8_act_scales_size(TK, E, f),), dtype=torch.uint8, device=dev)
+    else:
+        x_perm = torch.empty((TK, d), dtype=torch.bfloat16, device=dev)
+        h = torch.empty((TK, f), dtype=torch.bfloat16, device=dev)
     y_perm = torch.empty((TK, d), dtype=torch.bfloat16, device=dev)
     y = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
     L = moe.lib
@@ -292,12 +308,23 @@ def run_gpu(args):
         st |= L.moe_route(P(logits), T, E, K, P(topk_idx), P(topk_w), P(counts), P(offsets), P(row_of),
                           P(src_tok), P(route_ws), route_ws.numel(), sp)
         rec(2)
-        st |= L.moe_permute(P(x), P(row_of), T, K, d, P(x_perm), sp)
-        rec(3)
-        st |= L.moe_grouped_gemm1_swiglu(P(x_perm), P(offsets), E, TK, d, f, P(w.W1), P(h), sp)
-        rec(4)
-        st |= L.moe_grouped_gemm2(P(h), P(offsets), E, TK, d, f, P(w.W2), P(y_perm), sp)
-        rec(5)
+        if mxfp8:
+            st |= L.moe_permute_mxfp8(P(x), P(topk_idx), P(row_of), P(offsets), T, K, d, E, P(x_perm), P(sfa),
+                                      sfa.numel(), sp)
+            rec(3)
+            st |= L.moe_grouped_gemm1_swiglu_mxfp8(P(x_perm), P(sfa), sfa.numel(), P(offsets), E, TK, d, f, P(W1q),
+                                                   P(W1s), P(h), P(sfh), sfh.numel(), sp)
+            rec(4)
+            st |= L.moe_grouped_gemm2_mxfp8(P(h), P(sfh), sfh.numel(), P(offsets), E, TK, d, f, P(W2q), P(W2s),
+                                            P(y_perm), sp)
+            rec(5)
+        else:
+            st |= L.moe_permute(P(x), P(row_of), T, K, d, P(x_perm), sp)
+            rec(3)
+            st |= L.moe_grouped_gemm1_swiglu(P(x_perm), P(offsets), E, TK, d, f, P(w.W1), P(h), sp)
+            rec(4)
+            st |= L.moe_grouped_gemm2(P(h), P(offsets), E, TK, d, f, P(w.W2), P(y_perm), sp)
+            rec(5)
         st |= L.moe_unpermute(P(y_perm), P(row_of), P(topk_w), T, K, d, P(y), sp)
         rec(6)
         if st != 0:
@@ -336,19 +363,34 @@ def run_gpu(args):
     value = aggregate(flops_step, ws, args.steps, elapsed_ms) / 1e12
     tokens_s = aggregate(T, ws, args.steps, elapsed_ms)
 
-    # ---- end to end through the C ABI with host buffers (pinned)
-    layer = moe.MoELayer(w.Wr, w.bias, w.W1, w.W2, K, T)
+    # ---- end to end through the public API with host buffers (pinned): the
+    # host->device copy of x and the device->host copy of y inside the timed region
     x_host = x.cpu().pin_memory()
     y_host = torch.empty((T, d), dtype=torch.bfloat16, pin_memory=True)
+    if mxfp8:
+        del x_perm, h, sfa, sfh
+        nbytes = int(L.moe_forward_mxfp8_workspace_size(T, d, E, K, f))
+        ws_mx = torch.empty((nbytes,), dtype=torch.uint8, device=dev)
+        x_dev = torch.empty_like(x)
+
+        def e2e_step():
+            x_dev.copy_(x_host, non_blocking=True)
+            moe.forward_mxfp8(x_dev, w.Wr, w.bias, W1q, W1s, W2q, W2s, K, out=y, workspace=ws_mx)
+            y_host.copy_(y, non_blocking=True)
+    else:
+        layer = moe.MoELayer(w.Wr, w.bias, w.W1, w.W2, K, T)
+
+        def e2e_step():
+            moe.forward_host(x_host, w.Wr, w.bias, w.W1, w.W2, K, y_host=y_host, workspace=layer.workspace)
     for _ in range(max(1, args.warmup)):
-        moe.forward_host(x_host, w.Wr, w.bias, w.W1, w.W2, K, y_host=y_host, workspace=layer.workspace)
+        e2e_step()
     torch.cuda.synchronize()
     _barrier(ws)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
-        moe.forward_host(x_host, w.Wr, w.bias, w.W1, w.W2, K, y_host=y_host, workspace=layer.workspace)
+        e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = _max_over_ranks(e0.elapsed_time(e1), ws)
@@ -360,9 +402,13 @@ def run_gpu(args):
     dom_flops = (4.0 if dom == "grouped_gemm1_swiglu" else 2.0) * TK * d * f
     achieved = dom_flops / (kmean[dom] * 1e-3) / 1e12
     peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
-    tr = _traffic_record(dom)
-    roofline = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "peak_source": f"{peak_src} bf16_tflops_sustained",
+    peak_src_note = f"{peak_src} bf16_tflops_sustained"
+    if mxfp8:
+        peak *= 2.0
+        peak_src_note += " x 2 (nominal fp8 / bf16 dense tensor ratio, 4.5 / 2.25 PFLOP/s)"
+    tr = _traffic_record(dom + ("_mxfp8" if mxfp8 else ""))
+    roofline = {"kernel": dom + ("_mxfp8" if mxfp8 else ""), "bound": "tensor", "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak, "peak_source": peak_src_note,
                 "traffic": (tr["dram_bytes_per_launch"] if tr else None),
                 "traffic_note": (tr.get("note") if tr else "no ncu counters for the current source")}
     share = {n: kmean[n] / sum(kmean.values()) for n in STEP_NAMES}
@@ -376,13 +422,18 @@ def run_gpu(args):
         kernels[n]["frac_of_hbm"] = kernels[n]["GB/s"] / float(peaks["hbm_gbs"])
     # router: bf16 tensor-core work of the three-piece split, 3 x 2*T*d*E
     kernels["router_logits"]["TFLOP/s"] = 6.0 * T * d * E / (kmean["router_logits"] * 1e-3) / 1e12
+    if mxfp8:
+        # E4M3 codes: x read as bf16 once, codes written K times, scales beside them
+        hbm_bytes["permute"] = 2.0 * T * d + 1.0 * TK * d + TK * d / 32.0 + 8.0 * TK
+        kernels["permute"]["GB/s"] = hbm_bytes["permute"] / (kmean["permute"] * 1e-3) / 1e9
+        kernels["permute"]["frac_of_hbm"] = kernels["permute"]["GB/s"] / float(peaks["hbm_gbs"])
     for n in ("grouped_gemm1_swiglu", "grouped_gemm2"):
         fl = (4.0 if n == "grouped_gemm1_swiglu" else 2.0) * TK * d * f
         kernels[n]["TFLOP/s"] = fl / (kmean[n] * 1e-3) / 1e12
 
     # ---- CPU baseline: the oracle on a bounded sample (rank 0, N=1 only)
     cpu = None
-    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline and not mxfp8:
         import oracle
         inputs = _oracle_inputs(s, x, w)
         nthreads = oracle.host_threads()
@@ -395,8 +446,11 @@ def run_gpu(args):
         line = {
             "metric": _metric(s), "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) tokens, N(0,1/fan_in) weights)",
-            "config": _config(s_name, s, ws),
+            "vs_baseline": None, "dtype": "mxfp8" if mxfp8 else "bf16",
+            "data": "synthetic (seeded N(0,1) tokens, N(0,1/fan_in) weights)",
+            "config": dict(_config(s_name, s, ws), precision=(
+                "mxfp8: E4M3 elements, UE8M0 scale per 32 along K, fp32 accumulate; expert weights quantised "
+                "once before the timed region" if mxfp8 else "bf16, fp32 accumulate")),
             "tokens_per_s": tokens_s, "kernels": kernels, "roofline": roofline, "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": T * d * 2,
                     "d2h_bytes_per_step": T * d * 2, "ms_per_step": e2e_ms / args.steps},
@@ -418,6 +472,8 @@ def main():
     ap.add_argument("--config", default="mixtral")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--precision", default="bf16", choices=["bf16", "mxfp8"],
+                    help="expert matmuls in bf16 or MXFP8 (E4M3, UE8M0 scale per 32)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

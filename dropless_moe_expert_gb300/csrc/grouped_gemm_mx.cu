@@ -25,8 +25,9 @@
 //    after its stage's MMAs completed (the shared-memory stage was freed by
 //    their commit), so the ring needs no further synchronisation.
 //  * One accumulator (256 columns); the other 256 TMEM columns hold the
-//    scale ring.  The epilogue of a tile therefore runs between mainloops;
-//    the TMA producer keeps filling the ring meanwhile.
+//    scale ring.  The epilogue of a tile therefore runs between mainloops
+//    (the TMA producer keeps filling the ring meanwhile), and GEMM1's, which
+//    forms and quantises h, is spread over eight warps.
 //  * Scale atoms are addressed by 128-row blocks: A and h by the tile's row
 //    block (rb = row blocks of earlier experts + the tile's block inside its
 //    expert), the weights by their global row / 128.  Every atom index is
@@ -53,7 +54,18 @@ constexpr int BM = 128;
 constexpr int BK = 128;          // elements (= bytes) of K per stage
 constexpr int UMMA_K = 32;
 constexpr int BAND = 16;
-constexpr int THREADS = 192;
+// warps 0 and 1: TMA producer and MMA issuer; then the epilogue warps: GEMM1
+// (whose tiles are short and whose epilogue forms and quantises h) uses two
+// per TMEM lane quarter, each owning half of the tile's h columns), GEMM2
+// one (bf16 rows written by TMA stores of full lines, which measured faster
+// than eight warps of direct 16-byte row stores).  With a single accumulator
+// the epilogue is not overlapped with the next mainloop, so its length
+// counts in full.
+template <bool SWIGLU>
+struct Roles {
+    static constexpr int EPI_WARPS = SWIGLU ? 8 : 4;
+    static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+};
 constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK;
 constexpr int B_BYTES = BN_ACC * BK;
@@ -92,13 +104,13 @@ struct MxParams {
 
 __device__ __forceinline__ size_t clamp_atom(size_t a, size_t n) { return a < n ? a : n - 1; }
 
-// GEMM1 epilogue of one warp: 32 rows, the tile's 128 output columns of h
-// (gate columns 0..127 and up columns 128..255 of the accumulator).  Each
-// thread owns one row: per 32-column block it forms h, quantises it and
-// stores 32 code bytes; the four blocks' scale bytes are one word of the h
-// atom for this row block and column slice.
+// GEMM1 epilogue of one warp: 32 rows and half (64) of the tile's 128 output
+// columns of h (gate columns 0..127 and up columns 128..255 of the
+// accumulator).  Each thread owns one row: per 32-column block it forms h,
+// quantises it and stores 32 code bytes; its two blocks' scale bytes are one
+// half-word of the row's word in the h atom for this row block and slice.
 __device__ __forceinline__ void epilogue_swiglu_mx(const MxParams &mp, uint32_t tbase, const gg::Tile &t, int q,
-                                                   int lane, int rb) {
+                                                   int half, int lane, int rb) {
     const gg::Params &p = mp.g;
     const int wrow0 = t.row0 + q * 32;
     if (wrow0 >= t.grp_end) return;  // warp-uniform
@@ -106,7 +118,7 @@ __device__ __forceinline__ void epilogue_swiglu_mx(const MxParams &mp, uint32_t 
     const bool row_ok = grow < t.grp_end;
     uint32_t scales = 0;
 #pragma unroll 1
-    for (int c = 0; c < BN_ACC / 2; c += 32) {
+    for (int c = half * 64; c < half * 64 + 64; c += 32) {
         uint32_t g[32], u[32];
         tmem_ld_32x32b_x32(tbase + c, g);
         tmem_ld_32x32b_x32(tbase + BN_ACC / 2 + c, u);
@@ -115,10 +127,10 @@ __device__ __forceinline__ void epilogue_swiglu_mx(const MxParams &mp, uint32_t 
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
             const float gv = __uint_as_float(g[i]);
-            h[i] = gv * __frcp_rn(1.0f + __expf(-gv)) * __uint_as_float(u[i]);
+            h[i] = __fdividef(gv, 1.0f + __expf(-gv)) * __uint_as_float(u[i]);  // silu(g) * u
         }
         uint32_t packed[8];
-        scales |= mx::quant_block(h, packed) << (8 * (c / 32));
+        scales |= mx::quant_block(h, packed) << (8 * ((c / 32) & 1));
         if (row_ok) {
             uint4 *dst = reinterpret_cast<uint4 *>(mp.hq + static_cast<size_t>(grow) * p.n_out + t.n_blk * 128 + c);
             dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
@@ -128,12 +140,13 @@ __device__ __forceinline__ void epilogue_swiglu_mx(const MxParams &mp, uint32_t 
     if (row_ok) {
         const int ns = p.n_out / 128;
         const size_t atom = clamp_atom(static_cast<size_t>(rb) * ns + t.n_blk, mp.sfh_atoms);
-        mp.sfh[atom * 128 + ((grow - t.row0) & 31) * 4 + ((grow - t.row0) >> 5)] = scales;
+        const size_t word = atom * 128 + ((grow - t.row0) & 31) * 4 + ((grow - t.row0) >> 5);
+        reinterpret_cast<uint16_t *>(mp.sfh)[2 * word + half] = static_cast<uint16_t>(scales);
     }
 }
 
 template <bool SWIGLU>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(Roles<SWIGLU>::THREADS, 1)
 grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmOut, const MxParams mp) {
     const gg::Params &p = mp.g;
@@ -163,7 +176,7 @@ grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
             mbar_init(&empty[i], 1);
         }
         mbar_init(tfull, 1);
-        mbar_init(tempty, 4);
+        mbar_init(tempty, Roles<SWIGLU>::EPI_WARPS);
         mbar_init(drain, 1);
         *s_abort = 0;
         fence_mbar_init();
@@ -272,7 +285,8 @@ grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
         }
     } else {
         const int q = warp & 3;  // TMEM lane quarter this warp may access
-        uint8_t *stage_buf = smem + OFF_EPI + (warp - 2) * 2 * EPI_BUF;
+        const int half = (warp - 2) / 4;  // GEMM1: which 64 of the tile's 128 h columns
+        uint8_t *stage_buf = smem + OFF_EPI + ((warp - 2) & 3) * 2 * EPI_BUF;
         uint32_t sbuf = 0;
         uint32_t acc_phase = 0;
         for (int k = 0, tile = gg::round_position(0, blockIdx.x, gridDim.x, mix); tile < total_tiles;
@@ -283,7 +297,7 @@ grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
             tc_fence_after();
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
             if (SWIGLU)
-                epilogue_swiglu_mx(mp, tbase, t, q, lane, s_pre[t.e] / NT + t.m_blk);
+                epilogue_swiglu_mx(mp, tbase, t, q, half, lane, s_pre[t.e] / NT + t.m_blk);
             else
                 gg::epilogue_tile<false>(p, &tmOut, stage_buf, sbuf, tbase, t.n_blk, t.row0 + q * 32, lane,
                                          t.grp_end);
@@ -292,7 +306,7 @@ grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
             if (lane == 0) mbar_arrive(tempty);
             acc_phase ^= 1u;
         }
-        if (lane == 0) bulk_wait_all();
+        if (lane == 0) bulk_wait_all();  // stores done before the CTA's shared memory goes away
     }
 
     tc_fence_before();
@@ -351,9 +365,11 @@ cudaError_t launch_grouped_gemm_mx(bool swiglu, const uint8_t *A, const uint8_t 
     mp.sfh_atoms = sfo_bytes / 512;
     if (mp.sfa_atoms == 0 || mp.sfb_atoms == 0 || (swiglu && mp.sfh_atoms == 0)) return cudaErrorInvalidValue;
     if (swiglu)
-        gmx::grouped_gemm_mx_kernel<true><<<cfg.num_sms, gmx::THREADS, gmx::SMEM_BYTES, stream>>>(tmA, tmB, tmOut, mp);
+        gmx::grouped_gemm_mx_kernel<true><<<cfg.num_sms, gmx::Roles<true>::THREADS, gmx::SMEM_BYTES, stream>>>(
+            tmA, tmB, tmOut, mp);
     else
-        gmx::grouped_gemm_mx_kernel<false><<<cfg.num_sms, gmx::THREADS, gmx::SMEM_BYTES, stream>>>(tmA, tmB, tmOut, mp);
+        gmx::grouped_gemm_mx_kernel<false><<<cfg.num_sms, gmx::Roles<false>::THREADS, gmx::SMEM_BYTES, stream>>>(
+            tmA, tmB, tmOut, mp);
     return cudaGetLastError();
 }
 

@@ -48,6 +48,10 @@ CONFIGS = {
     # profiling-size stand-in for dsv3: the same d, f, K and rows per expert
     # (T*K/E = 128) with 32 experts, so a full ncu capture holds ~3 GB
     "dsv3_e32": dict(T=512, d=7168, E=32, K=8, f=2048, bias="zipf_1.1"),
+    # profiling-size stand-in for the Mixtral-shaped GEMMs: the same d and f
+    # (so the same tile shapes and K lengths) with 2 experts and 2048 rows
+    # each, about 1 GB of weights
+    "mixtral_e2": dict(T=2048, d=4096, E=2, K=1, f=14336, bias="zero"),
 }
 
 DESCRIPTIONS = {
@@ -57,6 +61,7 @@ DESCRIPTIONS = {
     "qwen": "Qwen-MoE-shaped layer fwd T=16384 d=2048 E=128 K=8 f=768",
     "skew": "Extreme-skew MoE layer fwd T=32768 d=4096 E=64 K=6 f=1536",
     "dsv3_e32": "DeepSeek-V3-shaped layer, 32 experts (profiling size) T=512 d=7168 E=32 K=8 f=2048",
+    "mixtral_e2": "Mixtral-shaped expert GEMMs, 2 experts (profiling size) T=2048 d=4096 E=2 K=1 f=14336",
 }
 
 
