@@ -104,12 +104,16 @@ __device__ __forceinline__ void row_block_prefix(const int32_t *__restrict__ off
     }
 }
 
-// Permute + quantise: one warp per token; each lane quantises 128-wide K
-// slices of the token's row once and writes them to the K rows of x_perm
-// the token occupies, with the scales into those rows' atoms.
+// Permute + quantise: one warp per token.  The warp walks the row in chunks
+// of 256 elements, lane l holding elements 8l..8l+7 (one 16-byte load, so the
+// warp reads 512 contiguous bytes); a block of 32 elements is 4 lanes, which
+// combine their maxima with two shuffles.  Each lane writes its 8 codes (8
+// bytes: 256 contiguous bytes per warp) to every row of x_perm the token
+// occupies, and lane 16 s (s = 0, 1) gathers the 4 scale bytes of the chunk's
+// s-th 128-element slice and writes them as one word of that row's atom.
 __global__ void __launch_bounds__(256)
 permute_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ topk_idx, const int32_t *__restrict__ row_of,
-               const int32_t *__restrict__ offsets, int T, int K, int d, int E, uint4 *__restrict__ xq,
+               const int32_t *__restrict__ offsets, int T, int K, int d, int E, uint2 *__restrict__ xq,
                uint32_t *__restrict__ sf) {
     __shared__ int s_off[MAX_E];
     __shared__ int s_rb[MAX_E];
@@ -121,19 +125,46 @@ permute_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ topk_idx
     const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int nw = (gridDim.x * blockDim.x) >> 5;
     for (int t = gw; t < T; t += nw) {
-        for (int ks = lane; ks < ns; ks += 32) {
-            uint4 c[8];
-            const uint32_t s = quant_slice(x + (static_cast<size_t>(t) * d + ks * 128) / 8, c);
-            for (int k = 0; k < K; ++k) {
-                const int r = __ldg(row_of + static_cast<size_t>(t) * K + k);
-                const int e = __ldg(topk_idx + static_cast<size_t>(t) * K + k);
-                if (r < 0 || r >= TK || e < 0 || e >= E) continue;  // outside the contract: skip
-                uint4 *dst = xq + (static_cast<size_t>(r) * d + ks * 128) / 16;
+        // lanes k < K hold the token's k-th row and expert
+        int my_r = -1, my_e = -1;
+        if (lane < K) {
+            my_r = __ldg(row_of + static_cast<size_t>(t) * K + lane);
+            my_e = __ldg(topk_idx + static_cast<size_t>(t) * K + lane);
+        }
+        for (int c0 = 0; c0 < d; c0 += 256) {
+            const bool valid = c0 + 8 * lane < d;  // d is a multiple of 128: whole blocks
+            float v[8];
+            if (valid) {
+                unpack_bf16x8(__ldg(x + (static_cast<size_t>(t) * d + c0 + 8 * lane) / 8), v);
+            } else {
 #pragma unroll
-                for (int i = 0; i < 8; ++i) dst[i] = c[i];
+                for (int i = 0; i < 8; ++i) v[i] = 0.0f;
+            }
+            float amax = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+            const uint32_t sbyte = scale_byte(amax);
+            const float inv = __uint_as_float((254u - sbyte) << 23);  // 2^-(s-127)
+            uint2 code;
+            code.x = pack4(v[0] * inv, v[1] * inv, v[2] * inv, v[3] * inv);
+            code.y = pack4(v[4] * inv, v[5] * inv, v[6] * inv, v[7] * inv);
+            // the chunk's two slices: bytes of blocks 0..3 from lanes 0, 4, 8, 12
+            // (slice 0) and 16, 20, 24, 28 (slice 1)
+            const uint32_t b1 = __shfl_down_sync(0xffffffffu, sbyte, 4);
+            const uint32_t b2 = __shfl_down_sync(0xffffffffu, sbyte, 8);
+            const uint32_t b3 = __shfl_down_sync(0xffffffffu, sbyte, 12);
+            const uint32_t word = sbyte | (b1 << 8) | (b2 << 16) | (b3 << 24);
+            const int ks = c0 / 128 + (lane >> 4);
+            for (int k = 0; k < K; ++k) {
+                const int r = __shfl_sync(0xffffffffu, my_r, k);
+                const int e = __shfl_sync(0xffffffffu, my_e, k);
+                if (r < 0 || r >= TK || e < 0 || e >= E) continue;  // outside the contract: skip (warp-uniform)
                 const int local = r - s_off[e];
-                if (local < 0) continue;  // row_of inconsistent with offsets: outside the contract
-                sf[atom_word(s_rb[e] + local / 128, ks, ns, local % 128)] = s;
+                if (local < 0) continue;
+                if (valid) xq[(static_cast<size_t>(r) * d + c0 + 8 * lane) / 8] = code;
+                if ((lane & 15) == 0 && valid) sf[atom_word(s_rb[e] + local / 128, ks, ns, local % 128)] = word;
             }
         }
     }
@@ -165,7 +196,7 @@ cudaError_t launch_permute_mxfp8(const uint16_t *x, const int32_t *topk_idx, con
     const int warps = 8;
     const int blocks = std::max(1, std::min((T + warps - 1) / warps, 152 * 8));
     mx::permute_kernel<<<blocks, 32 * warps, 0, stream>>>(reinterpret_cast<const uint4 *>(x), topk_idx, row_of,
-                                                         offsets, T, K, d, E, reinterpret_cast<uint4 *>(xq),
+                                                         offsets, T, K, d, E, reinterpret_cast<uint2 *>(xq),
                                                          reinterpret_cast<uint32_t *>(sfa));
     return cudaGetLastError();
 }
