@@ -69,10 +69,13 @@ def _traffic_record(kernel: str):
     rec = d.get(kernel)
     if not rec:
         return None
-    src = os.path.join(ROOT, rec["source"])
-    with open(src, "rb") as fh:
-        h = hashlib.sha256(fh.read()).hexdigest()[:16]
-    if h != rec.get("source_sha256_16"):
+    # the hash covers every source file the kernel is built from
+    srcs = rec["source"] if isinstance(rec["source"], list) else [rec["source"]]
+    digest = hashlib.sha256()
+    for src in srcs:
+        with open(os.path.join(ROOT, src), "rb") as fh:
+            digest.update(fh.read())
+    if digest.hexdigest()[:16] != rec.get("source_sha256_16"):
         return None
     return rec
 
@@ -292,6 +295,10 @@ def run_gpu(args):
         h = torch.empty((TK, f), dtype=torch.bfloat16, device=dev)
     y_perm = torch.empty((TK, d), dtype=torch.bfloat16, device=dev)
     y = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
+    counters = torch.empty((max(1, int(moe.lib.moe_combine_counters_size(T, d)) // 4),), dtype=torch.int32,
+                           device=dev)
+    if args.fused_combine and args.precision != "bf16":
+        raise SystemExit("--fused-combine is a bf16-path option")
     L = moe.lib
     stream = torch.cuda.current_stream()
     sp = stream.cuda_stream
@@ -323,9 +330,16 @@ def run_gpu(args):
             rec(3)
             st |= L.moe_grouped_gemm1_swiglu(P(x_perm), P(offsets), E, TK, d, f, P(w.W1), P(h), sp)
             rec(4)
-            st |= L.moe_grouped_gemm2(P(h), P(offsets), E, TK, d, f, P(w.W2), P(y_perm), sp)
+            if args.fused_combine:
+                # GEMM2 and the combine in one kernel; the combine step below is empty
+                st |= L.moe_grouped_gemm2_combine(P(h), P(offsets), E, TK, d, f, P(w.W2), P(src_tok), P(row_of),
+                                                  P(topk_w), T, K, P(y_perm), P(counters), counters.numel() * 4,
+                                                  P(y), sp)
+            else:
+                st |= L.moe_grouped_gemm2(P(h), P(offsets), E, TK, d, f, P(w.W2), P(y_perm), sp)
             rec(5)
-        st |= L.moe_unpermute(P(y_perm), P(row_of), P(topk_w), T, K, d, P(y), sp)
+        if not args.fused_combine:
+            st |= L.moe_unpermute(P(y_perm), P(row_of), P(topk_w), T, K, d, P(y), sp)
         rec(6)
         if st != 0:
             raise RuntimeError(f"C ABI returned {st}")
@@ -448,7 +462,7 @@ def run_gpu(args):
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "mxfp8" if mxfp8 else "bf16",
             "data": "synthetic (seeded N(0,1) tokens, N(0,1/fan_in) weights)",
-            "config": dict(_config(s_name, s, ws), precision=(
+            "config": dict(_config(s_name, s, ws), fused_combine=bool(args.fused_combine), precision=(
                 "mxfp8: E4M3 elements, UE8M0 scale per 32 along K, fp32 accumulate; expert weights quantised "
                 "once before the timed region" if mxfp8 else "bf16, fp32 accumulate")),
             "tokens_per_s": tokens_s, "kernels": kernels, "roofline": roofline, "cpu_baseline": cpu,
@@ -472,6 +486,8 @@ def main():
     ap.add_argument("--config", default="mixtral")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fused-combine", action="store_true",
+                    help="fuse the combine into GEMM2's epilogue (bf16 path)")
     ap.add_argument("--precision", default="bf16", choices=["bf16", "mxfp8"],
                     help="expert matmuls in bf16 or MXFP8 (E4M3, UE8M0 scale per 32)")
     args = ap.parse_args()

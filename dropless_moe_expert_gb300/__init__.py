@@ -25,6 +25,7 @@ __all__ = [
     "forward_views", "forward_host", "device_status", "launch_count", "MoELayer",
     "mxfp8_quantize", "mxfp8_scales_size", "mxfp8_act_scales_size", "permute_mxfp8",
     "grouped_gemm1_swiglu_mxfp8", "grouped_gemm2_mxfp8", "forward_mxfp8", "forward_mxfp8_views", "MoELayerMXFP8",
+    "grouped_gemm2_combine",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -85,6 +86,8 @@ def _load():
         "moe_forward_mxfp8_workspace_size": (S, [I, I, I, I, I]),
         "moe_forward_mxfp8_views": (I, [I, I, I, I, I, ctypes.POINTER(_LayoutMX)]),
         "moe_forward_mxfp8": (I, [P, P, P, P, P, P, P, I, I, I, I, I, P, P, S, P]),
+        "moe_combine_counters_size": (S, [I, I]),
+        "moe_grouped_gemm2_combine": (I, [P, P, I, I, I, I, P, P, P, P, I, I, P, P, S, P, P]),
         "moe_device_status": (I, [ctypes.POINTER(I)]),
         "moe_check_bounded_wait": (I, [U64, P]),
     }
@@ -256,6 +259,27 @@ def unpermute(y_perm, row_of, topk_w, out=None, stream=None):
     out = _empty((T, d), torch.bfloat16, y_perm) if out is None else _need(out, torch.bfloat16, (T, d), "y")
     _check(lib.moe_unpermute(_ptr(y_perm), _ptr(row_of), _ptr(topk_w), T, K, d, _ptr(out), _stream(stream)),
            "moe_unpermute")
+    return out
+
+
+def grouped_gemm2_combine(h, r: "Routing", W2, out=None, y_perm=None, counters=None, stream=None):
+    """GEMM2 with the combine fused into its epilogue: y [T, d] bf16, equal
+    bit for bit to unpermute(grouped_gemm2(h)).  y_perm and counters are
+    scratch (allocated when not given)."""
+    TK, f = h.shape
+    E, d, _ = W2.shape
+    T, K = r.row_of.shape
+    _need(h, torch.bfloat16, (TK, f), "h")
+    _need(W2, torch.bfloat16, (E, d, f), "W2")
+    if y_perm is None:
+        y_perm = _empty((TK, d), torch.bfloat16, h)
+    if counters is None:
+        counters = _empty((max(1, int(lib.moe_combine_counters_size(T, d)) // 4),), torch.int32, h)
+    out = _empty((T, d), torch.bfloat16, h) if out is None else _need(out, torch.bfloat16, (T, d), "y")
+    _check(lib.moe_grouped_gemm2_combine(_ptr(h), _ptr(r.offsets), E, TK, d, f, _ptr(W2), _ptr(r.src_tok),
+                                         _ptr(r.row_of), _ptr(r.topk_w), T, K, _ptr(y_perm), _ptr(counters),
+                                         counters.numel() * 4, _ptr(out), _stream(stream)),
+           "moe_grouped_gemm2_combine")
     return out
 
 

@@ -21,6 +21,18 @@ constexpr int EPI_WARPS = 4;
 constexpr int EPI_BUF = 32 * 32 * 2;
 constexpr int EPI_BYTES = EPI_WARPS * 2 * EPI_BUF;
 
+// GEMM2 with the combine fused into its epilogue (counters == nullptr: not
+// fused).  counters [T, nb] count, per token and 256-column block of y, the
+// token's rows already stored; they are zero at launch.
+struct Combine {
+    const int32_t *src_tok;   // [TK] token of each row
+    const int32_t *row_of;    // [T, K]
+    const float *topk_w;      // [T, K]
+    int T, K, nb;
+    int *counters;
+    __nv_bfloat16 *y;         // [T, n_out]
+};
+
 struct Params {
     const int32_t *offsets;  // [E+1] device
     int E;
@@ -32,6 +44,7 @@ struct Params {
     __nv_bfloat16 *out;  // [TK, n_out]
     int *status;
     uint64_t timeout_ns;
+    Combine comb;
 };
 
 struct Tile {
@@ -135,6 +148,70 @@ __device__ __forceinline__ void store_row32(__nv_bfloat16 *dst_row, const uint32
     for (int i = 0; i < 4; ++i) dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
 }
 
+__device__ __forceinline__ void fma_bf16x8(float (&acc)[8], float w, const uint4 &v) {
+    const uint32_t q[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        acc[2 * i] = __fmaf_rn(w, __uint_as_float(q[i] << 16), acc[2 * i]);
+        acc[2 * i + 1] = __fmaf_rn(w, __uint_as_float(q[i] & 0xffff0000u), acc[2 * i + 1]);
+    }
+}
+
+// Fused combine, after this warp's 32 rows of y_perm (columns of block
+// n_blk) are stored.  Each row's lane makes its stores visible and counts
+// the row for its token; the lane that brings the count to K is the
+// token's last row in this column block, and the warp then forms
+//   y[t, cols] = bf16( sum_{k=0..K-1} w[t,k] * y_perm[row_of[t,k], cols] )
+// (fp32 fused multiply-add in ascending k, the unfused combine's
+// arithmetic) from the K stored rows, 8 columns per lane.  Which row comes
+// last does not change the sum, so the result is deterministic.
+__device__ __forceinline__ void combine_arrive(const Params &p, int n_blk, int grow, bool row_ok, int lane) {
+    const Combine &cb = p.comb;
+    __threadfence();  // this row's stores before its count
+    int tok = -1;
+    bool last = false;
+    if (row_ok) {
+        tok = cb.src_tok[grow];
+        if (tok >= 0 && tok < cb.T)
+            last = atomicAdd(&cb.counters[static_cast<size_t>(tok) * cb.nb + n_blk], 1) == cb.K - 1;
+    }
+    unsigned m = __ballot_sync(0xffffffffu, last);
+    if (m == 0) return;
+    __threadfence();  // the token's other rows, seen through the count, before reading them
+    const int n0 = n_blk * BN_ACC + 8 * lane;
+    while (m) {
+        const int j = __ffs(m) - 1;
+        m &= m - 1;
+        const int t = __shfl_sync(0xffffffffu, tok, j);
+        if (n0 >= p.n_out) continue;
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        // up to 8 of the token's rows in flight, then added in ascending k
+        for (int k0 = 0; k0 < cb.K; k0 += 8) {
+            uint4 v[8];
+            float w[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int k = k0 + i;
+                v[i] = make_uint4(0, 0, 0, 0);
+                w[i] = 0.0f;
+                if (k < cb.K) {
+                    const int r = cb.row_of[static_cast<size_t>(t) * cb.K + k];
+                    w[i] = cb.topk_w[static_cast<size_t>(t) * cb.K + k];
+                    if (r >= 0 && r < p.TK)  // else outside the contract
+                        v[i] = __ldcg(reinterpret_cast<const uint4 *>(p.out + static_cast<size_t>(r) * p.n_out + n0));
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if (k0 + i < cb.K) fma_bf16x8(acc, w[i], v[i]);
+        }
+        uint32_t q[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) q[i] = pack_bf16x2(acc[2 * i], acc[2 * i + 1]);
+        *reinterpret_cast<uint4 *>(cb.y + static_cast<size_t>(t) * p.n_out + n0) = make_uint4(q[0], q[1], q[2], q[3]);
+    }
+}
+
 // Epilogue of one accumulator for one warp: 32 TMEM lanes = 32 output rows
 // wrow0..wrow0+31 (this thread's row is wrow0 + lane), tbase points at the
 // warp's lane quarter of the accumulator.  Each 32-column chunk is converted
@@ -150,6 +227,30 @@ __device__ __forceinline__ void epilogue_tile(const Params &p, const CUtensorMap
     const bool full = wrow0 + 31 < grp_end;
     const int grow = wrow0 + lane;
     const bool row_ok = grow < grp_end;
+    if (!SWIGLU && p.comb.counters != nullptr) {
+        // fused combine: rows stored directly (generic proxy), so that a fence
+        // orders them before the token's count
+#pragma unroll 1
+        for (int c = 0; c < BN_ACC; c += 64) {
+            const int col = n_blk * BN_ACC + c;
+            if (col >= p.n_out) break;  // column tail (uniform)
+            uint32_t v[2][32];
+            tmem_ld_32x32b_x32(tbase + c, v[0]);
+            tmem_ld_32x32b_x32(tbase + c + 32, v[1]);
+            tmem_ld_wait();
+#pragma unroll
+            for (int hlf = 0; hlf < 2; ++hlf) {
+                if (col + 32 * hlf >= p.n_out) break;
+                uint32_t packed[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    packed[i] = pack_bf16x2(__uint_as_float(v[hlf][2 * i]), __uint_as_float(v[hlf][2 * i + 1]));
+                if (row_ok) store_row32(p.out + static_cast<size_t>(grow) * p.n_out + col + 32 * hlf, packed);
+            }
+        }
+        combine_arrive(p, n_blk, grow, row_ok, lane);
+        return;
+    }
     constexpr int NCOL = SWIGLU ? BN_ACC / 2 : BN_ACC;
     auto emit = [&](int c, const uint32_t (&packed)[16]) {
         const int col = n_blk * NCOL + c;

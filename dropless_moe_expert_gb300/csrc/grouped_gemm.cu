@@ -482,7 +482,7 @@ bool grouped_gemm_use_pair(int TK, int E) {
 
 cudaError_t launch_grouped_gemm(bool swiglu, const void *A, int TK, int Kdim, const void *W, int E, int n_out,
                                 const int32_t *offsets, void *out, const GemmLaunch &cfg, int *status,
-                                uint64_t timeout_ns, cudaStream_t stream) {
+                                uint64_t timeout_ns, cudaStream_t stream, const CombineArgs *comb) {
     CUtensorMap tmA, tmB;
     const int w_rows = swiglu ? 2 * n_out : n_out;
     if (!make_tmap(&tmA, A, static_cast<uint64_t>(TK), static_cast<uint64_t>(Kdim), gg::BOX_ROWS, gg::BK))
@@ -493,7 +493,17 @@ cudaError_t launch_grouped_gemm(bool swiglu, const void *A, int TK, int Kdim, co
     if (!make_tmap(&tmOut, out, static_cast<uint64_t>(TK), static_cast<uint64_t>(n_out), 32, 32,
                    CU_TENSOR_MAP_SWIZZLE_64B))
         return cudaErrorInvalidValue;
-    gg::Params p;
+    gg::Params p = {};
+    if (comb && !swiglu) {
+        p.comb.src_tok = comb->src_tok;
+        p.comb.row_of = comb->row_of;
+        p.comb.topk_w = comb->topk_w;
+        p.comb.T = comb->T;
+        p.comb.K = comb->K;
+        p.comb.nb = (n_out + gg::BN_ACC - 1) / gg::BN_ACC;
+        p.comb.counters = comb->counters;
+        p.comb.y = static_cast<__nv_bfloat16 *>(comb->y);
+    }
     p.offsets = offsets;
     p.E = E;
     p.TK = TK;

@@ -344,7 +344,7 @@ cudaError_t launch_grouped_gemm_mx(bool swiglu, const uint8_t *A, const uint8_t 
                           CU_TENSOR_MAP_SWIZZLE_64B)) {
         return cudaErrorInvalidValue;
     }
-    gmx::MxParams mp;
+    gmx::MxParams mp = {};  // comb.counters == nullptr: no fused combine
     gg::Params &p = mp.g;
     p.offsets = offsets;
     p.E = E;

@@ -69,10 +69,21 @@ cudaError_t grouped_gemm_setup(int num_sms, GemmLaunch *cfg);
 // True when the CTA-pair kernel is used for this shape (decided on host
 // sizes only, so the choice is the same for every routing).
 bool grouped_gemm_use_pair(int TK, int E);
+// GEMM2 with the combine fused into its epilogue: y [T, n_out] bf16 from the
+// rows it stores in `out` (then scratch); counters [T, ceil(n_out / 256)]
+// int32 must be zero at launch.
+struct CombineArgs {
+    const int32_t *src_tok;
+    const int32_t *row_of;
+    const float *topk_w;
+    int T, K;
+    int *counters;
+    void *y;
+};
 // swiglu: GEMM1 (out [TK, n_out=f], W [E, 2f, Kdim=d]); else GEMM2 (out [TK, n_out=d], W [E, d, Kdim=f]).
 cudaError_t launch_grouped_gemm(bool swiglu, const void *A, int TK, int Kdim, const void *W, int E, int n_out,
                                 const int32_t *offsets, void *out, const GemmLaunch &cfg, int *status,
-                                uint64_t timeout_ns, cudaStream_t stream);
+                                uint64_t timeout_ns, cudaStream_t stream, const CombineArgs *comb = nullptr);
 
 // A kernel whose only wait never completes: it times out after limit_ns and
 // records MOE_ERR_DEVICE_TIMEOUT in *status.

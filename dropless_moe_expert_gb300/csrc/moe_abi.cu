@@ -233,6 +233,34 @@ moe_status_t moe_grouped_gemm2(const uint16_t *h, const int32_t *offsets, int E,
     return run_gemm(false, h, offsets, E, TK, d, f, W2, y_perm, stream);
 }
 
+size_t moe_combine_counters_size(int T, int d) {
+    if (T < 1 || d < 64 || d % 64 != 0) return 0;
+    return static_cast<size_t>(T) * ((d + 255) / 256) * sizeof(int32_t);
+}
+
+moe_status_t moe_grouped_gemm2_combine(const uint16_t *h, const int32_t *offsets, int E, int TK, int d, int f,
+                                       const uint16_t *W2, const int32_t *src_tok, const int32_t *row_of,
+                                       const float *topk_w, int T, int K, uint16_t *y_perm, int32_t *counters,
+                                       size_t counters_bytes, uint16_t *y, cudaStream_t stream) {
+    if (!h || !offsets || !W2 || !src_tok || !row_of || !topk_w || !y_perm || !counters || !y)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned(h, 16) || !aligned(W2, 16) || !aligned(y_perm, 16) || !aligned(y, 16) || !aligned(offsets, 4) ||
+        !aligned(src_tok, 4) || !aligned(row_of, 4) || !aligned(topk_w, 4) || !aligned(counters, 4))
+        return MOE_ERR_INVALID_ARG;
+    moe_status_t st = check_shape(T, d, E, K, f, true, true);
+    if (st != MOE_OK) return st;
+    if (static_cast<int64_t>(T) * K != TK) return MOE_ERR_INVALID_ARG;
+    const size_t need = moe_combine_counters_size(T, d);
+    if (counters_bytes < need) return MOE_ERR_WORKSPACE;
+    DeviceState *ds = nullptr;
+    if ((st = device_state(&ds)) != MOE_OK) return st;
+    if (cudaMemsetAsync(counters, 0, need, stream) != cudaSuccess) return MOE_ERR_CUDA;
+    moe::CombineArgs cb{src_tok, row_of, topk_w, T, K, counters, y};
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return cuda_status(moe::launch_grouped_gemm(false, h, TK, f, W2, E, d, offsets, y_perm, ds->gemm, ds->status,
+                                                kWaitLimitNs, stream, &cb));
+}
+
 moe_status_t moe_grouped_mlp(const uint16_t *x_perm, const int32_t *offsets, int E, int TK, int d, int f,
                              const uint16_t *W1, const uint16_t *W2, uint16_t *h, uint16_t *y_perm,
                              cudaStream_t stream) {

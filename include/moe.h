@@ -157,6 +157,23 @@ moe_status_t moe_grouped_gemm2(const uint16_t *h, const int32_t *offsets, int E,
                                int d, int f, const uint16_t *W2, uint16_t *y_perm,
                                cudaStream_t stream);
 
+/* Steps a5 + a6 in one kernel (the combine fused into GEMM2's epilogue;
+ * "Optimization 2": a naive dispatch/combine reads and writes the data many
+ * times, TE fuses them into one pipeline).  Computes y exactly as
+ * moe_grouped_gemm2 followed by moe_unpermute (bit-identical): each stored
+ * row of y_perm (scratch [TK, d]) is counted per token and 256-column block
+ * in `counters`, and the row that completes a token's K rows forms y for
+ * that block from the K stored rows, fp32 in ascending k.  No floating-point
+ * atomics: the result does not depend on which row comes last.
+ * `counters` holds moe_combine_counters_size(T, d) bytes and is zeroed by
+ * the call (cudaMemsetAsync on `stream`).  TK must equal T * K.  */
+size_t moe_combine_counters_size(int T, int d);
+moe_status_t moe_grouped_gemm2_combine(const uint16_t *h, const int32_t *offsets, int E, int TK, int d,
+                                       int f, const uint16_t *W2, const int32_t *src_tok,
+                                       const int32_t *row_of, const float *topk_w, int T, int K,
+                                       uint16_t *y_perm, int32_t *counters, size_t counters_bytes,
+                                       uint16_t *y, cudaStream_t stream);
+
 /* Step a6 -- unpermute + combine (Figure 3 caption: restore token order):
  * y[t,:] = bf16( sum_{k=0..K-1} topk_w[t,k] * y_perm[row_of[t,k], :] ),
  * fp32 accumulation in ascending k.  */
