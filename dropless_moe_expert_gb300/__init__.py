@@ -46,6 +46,12 @@ class _Layout(ctypes.Structure):
         "router_ws", "x_perm", "h", "y_perm", "x_dev", "y_dev", "total")]
 
 
+class _LayoutBW(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in (
+        "dw", "dl", "dl_row", "dy_perm", "dh", "a", "da", "dx_perm", "W1T", "W2T", "WrT", "dyT", "hT", "daT",
+        "xT", "total")]
+
+
 class _LayoutMX(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in (
         "logits", "topk_idx", "topk_w", "counts", "offsets", "row_of", "src_tok", "route_ws", "router_ws",
@@ -86,6 +92,9 @@ def _load():
         "moe_forward_mxfp8_workspace_size": (S, [I, I, I, I, I]),
         "moe_forward_mxfp8_views": (I, [I, I, I, I, I, ctypes.POINTER(_LayoutMX)]),
         "moe_forward_mxfp8": (I, [P, P, P, P, P, P, P, I, I, I, I, I, P, P, S, P]),
+        "moe_backward_workspace_size": (S, [I, I, I, I, I]),
+        "moe_backward_views": (I, [I, I, I, I, I, ctypes.POINTER(_LayoutBW)]),
+        "moe_backward": (I, [P, P, P, P, P, I, I, I, I, I, P, P, S, P, P, P, P, P, P, S, P]),
         "moe_combine_counters_size": (S, [I, I]),
         "moe_grouped_gemm2_combine": (I, [P, P, I, I, I, I, P, P, P, P, I, I, P, P, S, P, P]),
         "moe_device_status": (I, [ctypes.POINTER(I)]),
@@ -377,6 +386,48 @@ class MoELayer:
             raise ValueError("more tokens than the workspace was sized for")
         return forward(x, self.Wr, self.bias, self.W1, self.W2, self.K, out=out, workspace=self.workspace,
                        stream=stream)
+
+    def backward(self, x, dy, grads=None, workspace=None, stream=None):
+        """Gradients of sum(dy * y) for the last call (same x): dict of dx
+        [T,d] bf16 and dWr, dbias, dW1, dW2 (fp32, shaped like the weights)."""
+        T, d = x.shape
+        _need(x, torch.bfloat16, (T, d), "x")
+        _need(dy, torch.bfloat16, (T, d), "dy")
+        n = int(lib.moe_backward_workspace_size(T, d, self.E, self.K, self.f))
+        if n == 0:
+            raise MoEError(2, "moe_backward_workspace_size")
+        if workspace is None:
+            workspace = torch.empty((n,), dtype=torch.uint8, device=x.device)
+        if grads is None:
+            f32 = dict(dtype=torch.float32, device=x.device)
+            grads = dict(dx=torch.empty((T, d), dtype=torch.bfloat16, device=x.device),
+                         dWr=torch.empty(self.Wr.shape, **f32), dbias=torch.empty((self.E,), **f32),
+                         dW1=torch.empty(self.W1.shape, **f32), dW2=torch.empty(self.W2.shape, **f32))
+        _check(lib.moe_backward(_ptr(x), _ptr(self.Wr), _ptr(self.bias), _ptr(self.W1), _ptr(self.W2), T, d, self.E,
+                                self.K, self.f, _ptr(dy), _ptr(self.workspace), self.workspace.numel(),
+                                _ptr(grads["dx"]), _ptr(grads["dWr"]), _ptr(grads["dbias"]), _ptr(grads["dW1"]),
+                                _ptr(grads["dW2"]), _ptr(workspace), workspace.numel(), _stream(stream)),
+               "moe_backward")
+        self.bw_workspace = workspace
+        return grads
+
+    def backward_views(self, T: int) -> dict:
+        """Typed views of the backward's intermediates (after backward())."""
+        lay = _LayoutBW()
+        _check(lib.moe_backward_views(T, self.d, self.E, self.K, self.f, ctypes.byref(lay)), "moe_backward_views")
+        ws = self.bw_workspace
+        TK = T * self.K
+
+        def v(name, n, dtype, shape):
+            off = getattr(lay, name)
+            return ws[off:off + n * torch.tensor([], dtype=dtype).element_size()].view(dtype).view(shape)
+
+        return dict(dw=v("dw", TK, torch.float32, (T, self.K)), dl=v("dl", TK, torch.float32, (T, self.K)),
+                    dy_perm=v("dy_perm", TK * self.d, torch.bfloat16, (TK, self.d)),
+                    dh=v("dh", TK * self.f, torch.bfloat16, (TK, self.f)),
+                    a=v("a", TK * 2 * self.f, torch.bfloat16, (TK, 2 * self.f)),
+                    da=v("da", TK * 2 * self.f, torch.bfloat16, (TK, 2 * self.f)),
+                    dx_perm=v("dx_perm", TK * self.d, torch.bfloat16, (TK, self.d)))
 
     def views(self, T: int) -> dict:
         """Typed tensor views of the intermediates of the last call with T tokens."""

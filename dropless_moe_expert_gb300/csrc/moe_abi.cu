@@ -44,6 +44,7 @@ moe_status_t device_state(DeviceState **out) {
         if (moe::grouped_gemm_setup(s.num_sms, &s.gemm) != cudaSuccess) return MOE_ERR_CUDA;
         if (moe::router_setup() != cudaSuccess) return MOE_ERR_CUDA;
         if (moe::grouped_gemm_mx_setup() != cudaSuccess) return MOE_ERR_CUDA;
+        if (moe::wgrad_setup() != cudaSuccess) return MOE_ERR_CUDA;
         if (cudaGetSymbolAddress(reinterpret_cast<void **>(&s.status), g_device_status) != cudaSuccess)
             return MOE_ERR_CUDA;
         s.ready = true;
@@ -117,6 +118,34 @@ bool forward_mxfp8_layout(int T, int d, int E, int K, int f, moe_forward_mxfp8_l
     L->hq = take(TK * f);
     L->sfh = take(moe::mxfp8_perm_scales_bytes(static_cast<int>(TK), E, f));
     L->y_perm = take(TK * d * 2);
+    L->total = o;
+    return true;
+}
+
+bool backward_layout(int T, int d, int E, int K, int f, moe_backward_layout_t *L) {
+    const size_t TK = static_cast<size_t>(T) * K;
+    const size_t Rp = moe::wgrad_padded_rows(static_cast<int>(TK), E);
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = o;
+        o = align_up(o + bytes, 256);
+        return at;
+    };
+    L->dw = take(TK * 4);
+    L->dl = take(TK * 4);
+    L->dl_row = take(TK * 4);
+    L->dy_perm = take(TK * d * 2);
+    L->dh = take(TK * f * 2);
+    L->a = take(TK * 2 * f * 2);
+    L->da = take(TK * 2 * f * 2);
+    L->dx_perm = take(TK * d * 2);
+    L->W1T = take(static_cast<size_t>(E) * 2 * f * d * 2);
+    L->W2T = take(static_cast<size_t>(E) * f * d * 2);
+    L->WrT = take(static_cast<size_t>(E) * d * 4);
+    L->dyT = take(static_cast<size_t>(d) * Rp * 2);
+    L->hT = take(static_cast<size_t>(f) * Rp * 2);
+    L->daT = take(static_cast<size_t>(2 * f) * Rp * 2);
+    L->xT = take(static_cast<size_t>(d) * Rp * 2);
     L->total = o;
     return true;
 }
@@ -482,6 +511,106 @@ moe_status_t moe_forward_mxfp8(const uint16_t *x, const float *Wr, const float *
         MOE_OK)
         return st;
     return moe_unpermute(y_perm, row_of, w, T, K, d, y, stream);
+}
+
+size_t moe_backward_workspace_size(int T, int d, int E, int K, int f) {
+    if (check_shape(T, d, E, K, f, true, true) != MOE_OK) return 0;
+    moe_backward_layout_t L;
+    backward_layout(T, d, E, K, f, &L);
+    return L.total;
+}
+
+moe_status_t moe_backward_views(int T, int d, int E, int K, int f, moe_backward_layout_t *layout) {
+    if (!layout) return MOE_ERR_INVALID_ARG;
+    moe_status_t st = check_shape(T, d, E, K, f, true, true);
+    if (st != MOE_OK) return st;
+    backward_layout(T, d, E, K, f, layout);
+    return MOE_OK;
+}
+
+moe_status_t moe_backward(const uint16_t *x, const float *Wr, const float *bias, const uint16_t *W1,
+                          const uint16_t *W2, int T, int d, int E, int K, int f, const uint16_t *dy,
+                          const void *fwd_workspace, size_t fwd_workspace_bytes, uint16_t *dx, float *dWr,
+                          float *dbias, float *dW1, float *dW2, void *workspace, size_t workspace_bytes,
+                          cudaStream_t stream) {
+    (void)bias;  // the bias enters the gradients only through the routing recorded by the forward
+    if (!x || !Wr || !W1 || !W2 || !dy || !fwd_workspace || !dx || !dWr || !dbias || !dW1 || !dW2 || !workspace)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(W1, 16) || !aligned(W2, 16) || !aligned(dy, 16) || !aligned(dx, 16) ||
+        !aligned(fwd_workspace, 16) || !aligned(workspace, 16) || !aligned(Wr, 4) || !aligned(dWr, 4) ||
+        !aligned(dbias, 4) || !aligned(dW1, 16) || !aligned(dW2, 16))
+        return MOE_ERR_INVALID_ARG;
+    moe_status_t st = check_shape(T, d, E, K, f, true, true);
+    if (st != MOE_OK) return st;
+    moe_forward_layout_t F;
+    forward_layout(T, d, E, K, f, &F);
+    moe_backward_layout_t B;
+    backward_layout(T, d, E, K, f, &B);
+    if (fwd_workspace_bytes < F.total || workspace_bytes < B.total) return MOE_ERR_WORKSPACE;
+    DeviceState *ds = nullptr;
+    if ((st = device_state(&ds)) != MOE_OK) return st;
+    const uint8_t *fw = static_cast<const uint8_t *>(fwd_workspace);
+    uint8_t *bw = static_cast<uint8_t *>(workspace);
+    auto fv = [&](size_t off) { return fw + off; };
+    auto bv = [&](size_t off) { return bw + off; };
+    const int32_t *topk_idx = reinterpret_cast<const int32_t *>(fv(F.topk_idx));
+    const float *topk_w = reinterpret_cast<const float *>(fv(F.topk_w));
+    const int32_t *offsets = reinterpret_cast<const int32_t *>(fv(F.offsets));
+    const int32_t *row_of = reinterpret_cast<const int32_t *>(fv(F.row_of));
+    const uint16_t *x_perm = reinterpret_cast<const uint16_t *>(fv(F.x_perm));
+    const uint16_t *h = reinterpret_cast<const uint16_t *>(fv(F.h));
+    const uint16_t *y_perm = reinterpret_cast<const uint16_t *>(fv(F.y_perm));
+    float *dw = reinterpret_cast<float *>(bv(B.dw));
+    float *dl = reinterpret_cast<float *>(bv(B.dl));
+    float *dl_row = reinterpret_cast<float *>(bv(B.dl_row));
+    uint16_t *dy_perm = reinterpret_cast<uint16_t *>(bv(B.dy_perm));
+    uint16_t *dh = reinterpret_cast<uint16_t *>(bv(B.dh));
+    uint16_t *a = reinterpret_cast<uint16_t *>(bv(B.a));
+    uint16_t *da = reinterpret_cast<uint16_t *>(bv(B.da));
+    uint16_t *dx_perm = reinterpret_cast<uint16_t *>(bv(B.dx_perm));
+    uint16_t *W1T = reinterpret_cast<uint16_t *>(bv(B.W1T));
+    uint16_t *W2T = reinterpret_cast<uint16_t *>(bv(B.W2T));
+    float *WrT = reinterpret_cast<float *>(bv(B.WrT));
+    uint16_t *dyT = reinterpret_cast<uint16_t *>(bv(B.dyT));
+    uint16_t *hT = reinterpret_cast<uint16_t *>(bv(B.hT));
+    uint16_t *daT = reinterpret_cast<uint16_t *>(bv(B.daT));
+    uint16_t *xT = reinterpret_cast<uint16_t *>(bv(B.xT));
+    const int TK = T * K;
+    const int Rp = static_cast<int>(moe::wgrad_padded_rows(TK, E));
+    const moe::GemmLaunch &g = ds->gemm;
+    cudaError_t e = cudaSuccess;
+    auto go = [&](cudaError_t r, int launches) {
+        if (e == cudaSuccess) e = r;
+        g_launches.fetch_add(launches, std::memory_order_relaxed);
+    };
+    // weights transposed for the dgrad GEMMs (K-major B operands), Wr for dx
+    go(moe::launch_transpose_bf16(W2, E, d, f, W2T, stream), 1);
+    go(moe::launch_transpose_bf16(W1, E, 2 * f, d, W1T, stream), 1);
+    go(moe::launch_transpose_f32(Wr, 1, d, E, WrT, stream), 1);
+    // combine and router
+    go(moe::launch_combine_bwd(dy, y_perm, row_of, topk_w, T, K, d, dw, dy_perm, stream), 1);
+    go(moe::launch_router_bwd(topk_w, dw, row_of, T, K, dl, dl_row, stream), 1);
+    // GEMM2 dgrad: dh = dy_perm . W2[e]
+    go(moe::launch_grouped_gemm(false, dy_perm, TK, d, W2T, E, f, offsets, dh, g, ds->status, kWaitLimitNs, stream), 1);
+    // GEMM1 pre-activations again, then SwiGLU backward
+    go(moe::launch_grouped_gemm(false, x_perm, TK, d, W1, E, 2 * f, offsets, a, g, ds->status, kWaitLimitNs, stream), 1);
+    go(moe::launch_swiglu_bwd(a, dh, TK, f, da, stream), 1);
+    // GEMM1 dgrad: dx_perm = da . W1[e]
+    go(moe::launch_grouped_gemm(false, da, TK, 2 * f, W1T, E, d, offsets, dx_perm, g, ds->status, kWaitLimitNs,
+                                stream),
+       1);
+    // weight gradients over each expert's rows
+    go(moe::launch_transpose_grouped(dy_perm, offsets, E, TK, d, Rp, dyT, stream), 1);
+    go(moe::launch_transpose_grouped(h, offsets, E, TK, f, Rp, hT, stream), 1);
+    go(moe::launch_wgrad(dyT, hT, d, f, Rp, offsets, E, TK, dW2, ds->num_sms, ds->status, kWaitLimitNs, stream), 1);
+    go(moe::launch_transpose_grouped(da, offsets, E, TK, 2 * f, Rp, daT, stream), 1);
+    go(moe::launch_transpose_grouped(x_perm, offsets, E, TK, d, Rp, xT, stream), 1);
+    go(moe::launch_wgrad(daT, xT, 2 * f, d, Rp, offsets, E, TK, dW1, ds->num_sms, ds->status, kWaitLimitNs, stream),
+       1);
+    // router weights and the input gradient
+    go(moe::launch_router_wgrad(x_perm, dl_row, offsets, E, TK, d, dWr, dbias, stream), 1);
+    go(moe::launch_dx(dx_perm, WrT, row_of, topk_idx, dl, T, K, E, d, dx, stream), 1);
+    return cuda_status(e);
 }
 
 moe_status_t moe_check_bounded_wait(uint64_t limit_ns, cudaStream_t stream) {

@@ -267,6 +267,31 @@ moe_status_t moe_forward_mxfp8(const uint16_t *x, const float *Wr, const float *
                                int E, int K, int f, uint16_t *y, void *workspace, size_t workspace_bytes,
                                cudaStream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * Backward of the layer (the pages are about MoE training; they give no
+ * backward formula, so these are the gradients of the forward's definition
+ * for an output gradient dy: no gradient through the choice of the K
+ * experts, softmax over the K selected logits).
+ *   dx [T, d] bf16; dWr [d, E], dbias [E], dW1 [E, 2f, d], dW2 [E, d, f]
+ *   fp32 (every expert's entries written, zeros for experts without tokens).
+ * `fwd_workspace` is the workspace of a moe_forward call on the same x and
+ * weights (it holds the routing, x_perm, h and y_perm the backward reuses);
+ * `workspace` holds moe_backward_workspace_size() bytes of scratch
+ * (moe_backward_views() gives its regions).  The dgrad GEMMs run on the
+ * forward's grouped GEMM with transposed weights, the weight gradients on a
+ * grouped GEMM whose reduction runs over each expert's own rows.  All sums
+ * have a fixed order: the gradients are deterministic.  17 kernel launches.  */
+size_t moe_backward_workspace_size(int T, int d, int E, int K, int f);
+typedef struct {
+    size_t dw, dl, dl_row, dy_perm, dh, a, da, dx_perm, W1T, W2T, WrT, dyT, hT, daT, xT, total;
+} moe_backward_layout_t;
+moe_status_t moe_backward_views(int T, int d, int E, int K, int f, moe_backward_layout_t *layout);
+moe_status_t moe_backward(const uint16_t *x, const float *Wr, const float *bias, const uint16_t *W1,
+                          const uint16_t *W2, int T, int d, int E, int K, int f, const uint16_t *dy,
+                          const void *fwd_workspace, size_t fwd_workspace_bytes, uint16_t *dx,
+                          float *dWr, float *dbias, float *dW1, float *dW2, void *workspace,
+                          size_t workspace_bytes, cudaStream_t stream);
+
 /* Reads and clears the device status word of the current device (0 = OK, or
  * a moe_status_t a kernel recorded).  Synchronous: call outside capture. */
 moe_status_t moe_device_status(int *status_out);
