@@ -477,6 +477,86 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
+def run_train_step(args):
+    """One training step of the layer: moe_forward then moe_backward with a
+    seeded output gradient, timed together (kernels: forward, backward)."""
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    import __graft_entry__
+    if rank == 0 or ws == 1:
+        __graft_entry__.build()
+    _barrier(ws)
+    import dropless_moe_expert_gb300 as moe
+
+    s = shape(args.config)
+    T, d, E, K, f = s.T, s.d, s.E, s.K, s.f
+    TK = T * K
+    dev = torch.device("cuda", local)
+    w = make_weights(s, seed=0, device=dev)
+    x = make_tokens(s, seed=replica_seed(rank), device=dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(7 + rank)
+    dy = torch.randn((T, d), generator=g, device=dev).to(torch.bfloat16)
+    layer = moe.MoELayer(w.Wr, w.bias, w.W1, w.W2, K, T)
+    y = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
+    layer(x, out=y)
+    grads = layer.backward(x, dy)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        layer(x, out=y)
+        if ev is not None:
+            ev[1].record(stream)
+        layer.backward(x, dy, grads=grads, workspace=layer.bw_workspace)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert moe.device_status() == 0
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    sampler = ClockSampler(local) if rank == 0 else None
+    _barrier(ws)
+    torch.cuda.synchronize()
+    l0 = moe.launch_count()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    end.record(stream)
+    torch.cuda.synchronize()
+    _barrier(ws)
+    launches = moe.launch_count() - l0
+    clocks = sampler.stop() if sampler else None
+    assert moe.device_status() == 0
+    elapsed_ms = _max_over_ranks(start.elapsed_time(end), ws)
+    fwd_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
+    bwd_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps
+    # useful work: forward 6 TK d f, backward 12 TK d f (data and weight
+    # gradients of both GEMMs); the recomputed pre-activations do not count
+    flops_step = 18.0 * TK * d * f
+    value = aggregate(flops_step, ws, args.steps, elapsed_ms) / 1e12
+    if rank == 0:
+        line = {
+            "metric": "MoE layer training step (fwd + bwd) useful TFLOPS (18*T*K*d*f per step) at 1 GB300",
+            "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) tokens and output gradient)",
+            "config": dict(_config(args.config, s, ws), step="forward + backward",
+                           grads="dx bf16; dWr, dbias, dW1, dW2 fp32"),
+            "kernels": {"forward": {"ms": fwd_ms, "TFLOP/s": 6.0 * TK * d * f / (fwd_ms * 1e-3) / 1e12},
+                        "backward": {"ms": bwd_ms, "TFLOP/s": 12.0 * TK * d * f / (bwd_ms * 1e-3) / 1e12}},
+            "gpu_launches": launches, "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -488,6 +568,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--fused-combine", action="store_true",
                     help="fuse the combine into GEMM2's epilogue (bf16 path)")
+    ap.add_argument("--backward", action="store_true",
+                    help="time a training step of the layer (forward + backward) instead of the forward")
     ap.add_argument("--precision", default="bf16", choices=["bf16", "mxfp8"],
                     help="expert matmuls in bf16 or MXFP8 (E4M3, UE8M0 scale per 32)")
     args = ap.parse_args()
@@ -495,6 +577,8 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.backward:
+        run_train_step(args)
     else:
         run_gpu(args)
 
