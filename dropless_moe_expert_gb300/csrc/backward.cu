@@ -65,6 +65,63 @@ transpose_kernel(const T *__restrict__ src, int B, int R, int C, T *__restrict__
     }
 }
 
+// bf16 transpose with 64 x 64 tiles: 16-byte loads of source rows and
+// 16-byte stores of destination rows (both coalesced); shared-memory rows of
+// 66 elements keep the column reads conflict-free.  dst[b][c][r] =
+// src[b][r][c]; with `offsets` given, batches (experts) without rows are
+// skipped (their transposed weights are never read).
+__global__ void __launch_bounds__(256)
+transpose64_kernel(const uint16_t *__restrict__ src, int R, int C, const int32_t *__restrict__ offsets,
+                   uint16_t *__restrict__ dst) {
+    __shared__ uint16_t tile[64][66];
+    const int b = blockIdx.z;
+    if (offsets && offsets[b + 1] <= offsets[b]) return;
+    const int r0 = blockIdx.y * 64, c0 = blockIdx.x * 64;
+    const uint16_t *s = src + static_cast<size_t>(b) * R * C;
+    uint16_t *d = dst + static_cast<size_t>(b) * R * C;
+    const bool vec = (C % 8 == 0) && (R % 8 == 0);
+    for (int i = threadIdx.x; i < 64 * 8; i += 256) {
+        const int rr = i >> 3, cc = (i & 7) * 8;
+        const int r = r0 + rr, c = c0 + cc;
+        uint16_t v[8];
+        if (vec && r < R && c + 7 < C) {
+            const uint4 u = *reinterpret_cast<const uint4 *>(s + static_cast<size_t>(r) * C + c);
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                v[2 * q] = static_cast<uint16_t>(w[q] & 0xffffu);
+                v[2 * q + 1] = static_cast<uint16_t>(w[q] >> 16);
+            }
+        } else {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) v[q] = (r < R && c + q < C) ? s[static_cast<size_t>(r) * C + c + q] : 0;
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) tile[rr][cc + q] = v[q];
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < 64 * 8; i += 256) {
+        const int cc = i >> 3, rr = (i & 7) * 8;
+        const int c = c0 + cc, r = r0 + rr;
+        if (c >= C) continue;
+        uint16_t v[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) v[q] = tile[rr + q][cc];
+        if (vec && r + 7 < R) {
+            uint4 u;
+            u.x = v[0] | (static_cast<uint32_t>(v[1]) << 16);
+            u.y = v[2] | (static_cast<uint32_t>(v[3]) << 16);
+            u.z = v[4] | (static_cast<uint32_t>(v[5]) << 16);
+            u.w = v[6] | (static_cast<uint32_t>(v[7]) << 16);
+            *reinterpret_cast<uint4 *>(d + static_cast<size_t>(c) * R + r) = u;
+        } else {
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                if (r + q < R) d[static_cast<size_t>(c) * R + r + q] = v[q];
+        }
+    }
+}
+
 // Grouped, padded transpose of rows grouped by expert: dst [C, Rp] with
 // dst[c][pstart[e] + r - offsets[e]] = src[r][c]; pstart[e] = sum over
 // e' < e of round_up(count[e'], 64).  Padding columns are written as zeros
@@ -72,7 +129,7 @@ transpose_kernel(const T *__restrict__ src, int B, int R, int C, T *__restrict__
 __global__ void __launch_bounds__(256)
 transpose_grouped_kernel(const uint16_t *__restrict__ src, const int32_t *__restrict__ offsets, int E, int TK, int C,
                          int Rp, uint16_t *__restrict__ dst) {
-    __shared__ uint16_t tile[32][34];
+    __shared__ uint16_t tile[64][66];
     __shared__ int s_off[MAX_E + 1];
     __shared__ int s_pst[MAX_E + 1];
     if (threadIdx.x < 32) {
@@ -102,29 +159,50 @@ transpose_grouped_kernel(const uint16_t *__restrict__ src, const int32_t *__rest
         }
     }
     __syncthreads();
-    // this block: destination columns j0..j0+31 (padded row index), source
-    // columns c0..c0+31
-    const int j0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
-    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-    for (int i = ty; i < 32; i += 8) {
-        const int j = j0 + i;
-        // expert owning padded position j: the last e with s_pst[e] <= j
-        int lo = 0, hi = E - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (s_pst[mid] <= j) lo = mid; else hi = mid - 1;
+    // this block: padded positions j0..j0+63 (one group, since groups start on
+    // 64-boundaries) and source columns c0..c0+63
+    const int j0 = blockIdx.y * 64, c0 = blockIdx.x * 64;
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_pst[mid] <= j0) lo = mid; else hi = mid - 1;
+    }
+    const int rbase = s_off[lo] + (j0 - s_pst[lo]);  // source row of position j0
+    const int rend = (j0 < s_pst[E]) ? s_off[lo + 1] : rbase;  // the group's rows end here
+    const bool vec = (C % 8 == 0);
+    for (int i = threadIdx.x; i < 64 * 8; i += 256) {
+        const int jj = i >> 3, cc = (i & 7) * 8;
+        const int r = rbase + jj, c = c0 + cc;
+        uint16_t v[8];
+        if (r < rend && vec && c + 7 < C) {
+            const uint4 u = *reinterpret_cast<const uint4 *>(src + static_cast<size_t>(r) * C + c);
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                v[2 * q] = static_cast<uint16_t>(w[q] & 0xffffu);
+                v[2 * q + 1] = static_cast<uint16_t>(w[q] >> 16);
+            }
+        } else {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) v[q] = (r < rend && c + q < C) ? src[static_cast<size_t>(r) * C + c + q] : 0;
         }
-        const int r = s_off[lo] + (j - s_pst[lo]);
-        const bool real = j < s_pst[E] && r < s_off[lo + 1];
-        const int c = c0 + tx;
-        uint16_t v = 0;
-        if (real && c < C) v = src[static_cast<size_t>(r) * C + c];
-        tile[i][tx] = v;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) tile[jj][cc + q] = v[q];
     }
     __syncthreads();
-    for (int i = ty; i < 32; i += 8) {
-        const int c = c0 + i, j = j0 + tx;
-        if (c < C && j < Rp) dst[static_cast<size_t>(c) * Rp + j] = tile[tx][i];
+    for (int i = threadIdx.x; i < 64 * 8; i += 256) {
+        const int cc = i >> 3, jj = (i & 7) * 8;
+        const int c = c0 + cc, j = j0 + jj;
+        if (c >= C || j >= Rp) continue;
+        uint16_t v[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) v[q] = tile[jj + q][cc];
+        uint4 u;
+        u.x = v[0] | (static_cast<uint32_t>(v[1]) << 16);
+        u.y = v[2] | (static_cast<uint32_t>(v[3]) << 16);
+        u.z = v[4] | (static_cast<uint32_t>(v[5]) << 16);
+        u.w = v[6] | (static_cast<uint32_t>(v[7]) << 16);
+        *reinterpret_cast<uint4 *>(dst + static_cast<size_t>(c) * Rp + j) = u;  // Rp is a multiple of 64
     }
 }
 
@@ -202,36 +280,54 @@ swiglu_bwd_kernel(const uint4 *__restrict__ a, const uint4 *__restrict__ dh, int
     }
 }
 
-// dWr[:, e] and dbias[e]: sums over expert e's rows in group order (x_perm
-// rows are the tokens' rows).  Thread (e, 8-column chunk); one extra thread
-// per expert for dbias.
+// dWr[:, e] and dbias[e]: sums over expert e's rows.  One block per (expert,
+// 256-column chunk): lane l of warp w owns 8 columns and the rows
+// w, w + 8, w + 16, ... of the group; the 8 warps' partial sums are then
+// added in warp order.  The order of every addition is fixed: deterministic.
 __global__ void __launch_bounds__(256)
 router_wgrad_kernel(const uint4 *__restrict__ x_perm, const float *__restrict__ dl_row,
                     const int32_t *__restrict__ offsets, int E, int TK, int d, float *__restrict__ dWr,
                     float *__restrict__ dbias) {
+    __shared__ float part[8][256 + 1];
+    __shared__ float bpart[8];
+    const int e = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nvec = d / 8;
-    const int per = nvec + 1;
-    const int gid = blockIdx.x * blockDim.x + threadIdx.x;
-    if (gid >= E * per) return;
-    const int e = gid / per, v = gid % per;
+    const int v = blockIdx.x * 32 + lane;  // 8-column vector index
     const int o0 = min(max(offsets[e], 0), TK);
     const int o1 = min(max(offsets[e + 1], o0), TK);
-    if (v == nvec) {
-        float s = 0.0f;
-        for (int r = o0; r < o1; ++r) s += dl_row[r];
-        dbias[e] = s;
-        return;
-    }
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int r = o0; r < o1; ++r) {
+    float bsum = 0.0f;
+    for (int r = o0 + warp; r < o1; r += 8) {
         const float g = dl_row[r];
-        float xv[8];
-        unpack8(__ldg(x_perm + static_cast<size_t>(r) * nvec + v), xv);
+        bsum += g;
+        if (v < nvec) {
+            float xv[8];
+            unpack8(__ldg(x_perm + static_cast<size_t>(r) * nvec + v), xv);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = __fmaf_rn(g, xv[i], acc[i]);
+            for (int i = 0; i < 8; ++i) acc[i] = __fmaf_rn(g, xv[i], acc[i]);
+        }
     }
 #pragma unroll
-    for (int i = 0; i < 8; ++i) dWr[static_cast<size_t>(v * 8 + i) * E + e] = acc[i];
+    for (int i = 0; i < 8; ++i) part[warp][lane * 8 + i] = acc[i];
+    if (lane == 0) bpart[warp] = bsum;
+    __syncthreads();
+    // warp 0 adds the 8 partial sums in warp order and writes
+    if (warp == 0) {
+        if (v < nvec) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                float t = 0.0f;
+                for (int w = 0; w < 8; ++w) t += part[w][lane * 8 + i];
+                dWr[static_cast<size_t>(v * 8 + i) * E + e] = t;
+            }
+        }
+        if (blockIdx.x == 0 && lane == 0) {
+            float t = 0.0f;
+            for (int w = 0; w < 8; ++w) t += bpart[w];
+            dbias[e] = t;
+        }
+    }
 }
 
 // dx[t] = sum_k dx_perm[row_of[t,k]] + sum_k dl[t,k] Wr^T[idx[t,k]]; one warp
@@ -273,9 +369,10 @@ int warps_grid(int n) { return std::max(1, std::min((n + 7) / 8, 152 * 8)); }
 
 }  // namespace bw
 
-cudaError_t launch_transpose_bf16(const uint16_t *src, int B, int R, int C, uint16_t *dst, cudaStream_t s) {
-    dim3 grid((C + 31) / 32, (R + 31) / 32, B);
-    bw::transpose_kernel<uint16_t><<<grid, 256, 0, s>>>(src, B, R, C, dst);
+cudaError_t launch_transpose_bf16(const uint16_t *src, int B, int R, int C, const int32_t *skip_empty_offsets,
+                                  uint16_t *dst, cudaStream_t s) {
+    dim3 grid((C + 63) / 64, (R + 63) / 64, B);
+    bw::transpose64_kernel<<<grid, 256, 0, s>>>(src, R, C, skip_empty_offsets, dst);
     return cudaGetLastError();
 }
 
@@ -287,7 +384,7 @@ cudaError_t launch_transpose_f32(const float *src, int B, int R, int C, float *d
 
 cudaError_t launch_transpose_grouped(const uint16_t *src, const int32_t *offsets, int E, int TK, int C, int Rp,
                                      uint16_t *dst, cudaStream_t s) {
-    dim3 grid((C + 31) / 32, (Rp + 31) / 32);
+    dim3 grid((C + 63) / 64, (Rp + 63) / 64);
     bw::transpose_grouped_kernel<<<grid, 256, 0, s>>>(src, offsets, E, TK, C, Rp, dst);
     return cudaGetLastError();
 }
@@ -317,9 +414,9 @@ cudaError_t launch_swiglu_bwd(const uint16_t *a, const uint16_t *dh, int TK, int
 
 cudaError_t launch_router_wgrad(const uint16_t *x_perm, const float *dl_row, const int32_t *offsets, int E, int TK,
                                 int d, float *dWr, float *dbias, cudaStream_t s) {
-    const int n = E * (d / 8 + 1);
-    bw::router_wgrad_kernel<<<(n + 255) / 256, 256, 0, s>>>(reinterpret_cast<const uint4 *>(x_perm), dl_row, offsets, E,
-                                                           TK, d, dWr, dbias);
+    dim3 grid((d / 8 + 31) / 32, E);
+    bw::router_wgrad_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4 *>(x_perm), dl_row, offsets, E, TK, d,
+                                                dWr, dbias);
     return cudaGetLastError();
 }
 

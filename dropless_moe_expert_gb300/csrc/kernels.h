@@ -58,7 +58,9 @@ cudaError_t launch_grouped_gemm_mx(bool swiglu, const uint8_t *A, const uint8_t 
                                    const struct GemmLaunch &cfg, int *status, uint64_t timeout_ns, cudaStream_t stream);
 
 // Backward (backward.cu, wgrad.cu).
-cudaError_t launch_transpose_bf16(const uint16_t *src, int B, int R, int C, uint16_t *dst, cudaStream_t s);
+// dst[b] = src[b]^T; with skip_empty_offsets [B+1], batches without rows are skipped
+cudaError_t launch_transpose_bf16(const uint16_t *src, int B, int R, int C, const int32_t *skip_empty_offsets,
+                                  uint16_t *dst, cudaStream_t s);
 cudaError_t launch_transpose_f32(const float *src, int B, int R, int C, float *dst, cudaStream_t s);
 // rows grouped by expert -> [C, Rp], each group from a 64-aligned column, zeros between
 cudaError_t launch_transpose_grouped(const uint16_t *src, const int32_t *offsets, int E, int TK, int C, int Rp,

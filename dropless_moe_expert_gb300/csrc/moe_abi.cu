@@ -584,8 +584,8 @@ moe_status_t moe_backward(const uint16_t *x, const float *Wr, const float *bias,
         g_launches.fetch_add(launches, std::memory_order_relaxed);
     };
     // weights transposed for the dgrad GEMMs (K-major B operands), Wr for dx
-    go(moe::launch_transpose_bf16(W2, E, d, f, W2T, stream), 1);
-    go(moe::launch_transpose_bf16(W1, E, 2 * f, d, W1T, stream), 1);
+    go(moe::launch_transpose_bf16(W2, E, d, f, offsets, W2T, stream), 1);
+    go(moe::launch_transpose_bf16(W1, E, 2 * f, d, offsets, W1T, stream), 1);
     go(moe::launch_transpose_f32(Wr, 1, d, E, WrT, stream), 1);
     // combine and router
     go(moe::launch_combine_bwd(dy, y_perm, row_of, topk_w, T, K, d, dw, dy_perm, stream), 1);
