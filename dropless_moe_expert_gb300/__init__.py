@@ -48,8 +48,7 @@ class _Layout(ctypes.Structure):
 
 class _LayoutBW(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in (
-        "dw", "dl", "dl_row", "dy_perm", "dh", "a", "da", "dx_perm", "W1T", "W2T", "WrT", "dyT", "hT", "daT",
-        "xT", "total")]
+        "dw", "dl", "dl_row", "dy_perm", "dh", "a", "da", "dx_perm", "WrT", "total")]
 
 
 class _LayoutMX(ctypes.Structure):

@@ -22,8 +22,6 @@
 namespace moe {
 namespace bw {
 
-constexpr int MAX_E = 256;
-
 __device__ __forceinline__ void unpack8(const uint4 &u, float *o) {
     const uint32_t p[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
@@ -43,8 +41,7 @@ __device__ __forceinline__ uint4 pack8(const float *v) {
     return make_uint4(p[0], p[1], p[2], p[3]);
 }
 
-// dst[b][c][r] = src[b][r][c] for bf16 (esize 2) or fp32 (esize 4) elements:
-// 32 x 32 tiles through shared memory.
+// dst[b][c][r] = src[b][r][c]: 32 x 32 tiles through shared memory.
 template <typename T>
 __global__ void __launch_bounds__(256)
 transpose_kernel(const T *__restrict__ src, int B, int R, int C, T *__restrict__ dst) {
@@ -62,147 +59,6 @@ transpose_kernel(const T *__restrict__ src, int B, int R, int C, T *__restrict__
     for (int i = ty; i < 32; i += 8) {
         const int c = c0 + i, r = r0 + tx;
         if (r < R && c < C) d[static_cast<size_t>(c) * R + r] = tile[tx][i];
-    }
-}
-
-// bf16 transpose with 64 x 64 tiles: 16-byte loads of source rows and
-// 16-byte stores of destination rows (both coalesced); shared-memory rows of
-// 66 elements keep the column reads conflict-free.  dst[b][c][r] =
-// src[b][r][c]; with `offsets` given, batches (experts) without rows are
-// skipped (their transposed weights are never read).
-__global__ void __launch_bounds__(256)
-transpose64_kernel(const uint16_t *__restrict__ src, int R, int C, const int32_t *__restrict__ offsets,
-                   uint16_t *__restrict__ dst) {
-    __shared__ uint16_t tile[64][66];
-    const int b = blockIdx.z;
-    if (offsets && offsets[b + 1] <= offsets[b]) return;
-    const int r0 = blockIdx.y * 64, c0 = blockIdx.x * 64;
-    const uint16_t *s = src + static_cast<size_t>(b) * R * C;
-    uint16_t *d = dst + static_cast<size_t>(b) * R * C;
-    const bool vec = (C % 8 == 0) && (R % 8 == 0);
-    for (int i = threadIdx.x; i < 64 * 8; i += 256) {
-        const int rr = i >> 3, cc = (i & 7) * 8;
-        const int r = r0 + rr, c = c0 + cc;
-        uint16_t v[8];
-        if (vec && r < R && c + 7 < C) {
-            const uint4 u = *reinterpret_cast<const uint4 *>(s + static_cast<size_t>(r) * C + c);
-            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                v[2 * q] = static_cast<uint16_t>(w[q] & 0xffffu);
-                v[2 * q + 1] = static_cast<uint16_t>(w[q] >> 16);
-            }
-        } else {
-#pragma unroll
-            for (int q = 0; q < 8; ++q) v[q] = (r < R && c + q < C) ? s[static_cast<size_t>(r) * C + c + q] : 0;
-        }
-#pragma unroll
-        for (int q = 0; q < 8; ++q) tile[rr][cc + q] = v[q];
-    }
-    __syncthreads();
-    for (int i = threadIdx.x; i < 64 * 8; i += 256) {
-        const int cc = i >> 3, rr = (i & 7) * 8;
-        const int c = c0 + cc, r = r0 + rr;
-        if (c >= C) continue;
-        uint16_t v[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) v[q] = tile[rr + q][cc];
-        if (vec && r + 7 < R) {
-            uint4 u;
-            u.x = v[0] | (static_cast<uint32_t>(v[1]) << 16);
-            u.y = v[2] | (static_cast<uint32_t>(v[3]) << 16);
-            u.z = v[4] | (static_cast<uint32_t>(v[5]) << 16);
-            u.w = v[6] | (static_cast<uint32_t>(v[7]) << 16);
-            *reinterpret_cast<uint4 *>(d + static_cast<size_t>(c) * R + r) = u;
-        } else {
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-                if (r + q < R) d[static_cast<size_t>(c) * R + r + q] = v[q];
-        }
-    }
-}
-
-// Grouped, padded transpose of rows grouped by expert: dst [C, Rp] with
-// dst[c][pstart[e] + r - offsets[e]] = src[r][c]; pstart[e] = sum over
-// e' < e of round_up(count[e'], 64).  Padding columns are written as zeros
-// by the blocks that own them.
-__global__ void __launch_bounds__(256)
-transpose_grouped_kernel(const uint16_t *__restrict__ src, const int32_t *__restrict__ offsets, int E, int TK, int C,
-                         int Rp, uint16_t *__restrict__ dst) {
-    __shared__ uint16_t tile[64][66];
-    __shared__ int s_off[MAX_E + 1];
-    __shared__ int s_pst[MAX_E + 1];
-    if (threadIdx.x < 32) {
-        const int lane = threadIdx.x;
-        int carry = 0;
-        for (int base = 0; base < E; base += 32) {
-            const int e = base + lane;
-            int v = 0;
-            if (e < E) {
-                const int o0 = min(max(offsets[e], 0), TK);
-                const int o1 = min(max(offsets[e + 1], o0), TK);
-                s_off[e] = o0;
-                v = (o1 - o0 + 63) / 64 * 64;
-            }
-            int incl = v;
-#pragma unroll
-            for (int s = 1; s < 32; s <<= 1) {
-                const int n = __shfl_up_sync(0xffffffffu, incl, s);
-                if (lane >= s) incl += n;
-            }
-            if (e < E) s_pst[e] = carry + incl - v;
-            carry += __shfl_sync(0xffffffffu, incl, 31);
-        }
-        if (lane == 0) {
-            s_off[E] = TK;
-            s_pst[E] = carry;
-        }
-    }
-    __syncthreads();
-    // this block: padded positions j0..j0+63 (one group, since groups start on
-    // 64-boundaries) and source columns c0..c0+63
-    const int j0 = blockIdx.y * 64, c0 = blockIdx.x * 64;
-    int lo = 0, hi = E - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (s_pst[mid] <= j0) lo = mid; else hi = mid - 1;
-    }
-    const int rbase = s_off[lo] + (j0 - s_pst[lo]);  // source row of position j0
-    const int rend = (j0 < s_pst[E]) ? s_off[lo + 1] : rbase;  // the group's rows end here
-    const bool vec = (C % 8 == 0);
-    for (int i = threadIdx.x; i < 64 * 8; i += 256) {
-        const int jj = i >> 3, cc = (i & 7) * 8;
-        const int r = rbase + jj, c = c0 + cc;
-        uint16_t v[8];
-        if (r < rend && vec && c + 7 < C) {
-            const uint4 u = *reinterpret_cast<const uint4 *>(src + static_cast<size_t>(r) * C + c);
-            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                v[2 * q] = static_cast<uint16_t>(w[q] & 0xffffu);
-                v[2 * q + 1] = static_cast<uint16_t>(w[q] >> 16);
-            }
-        } else {
-#pragma unroll
-            for (int q = 0; q < 8; ++q) v[q] = (r < rend && c + q < C) ? src[static_cast<size_t>(r) * C + c + q] : 0;
-        }
-#pragma unroll
-        for (int q = 0; q < 8; ++q) tile[jj][cc + q] = v[q];
-    }
-    __syncthreads();
-    for (int i = threadIdx.x; i < 64 * 8; i += 256) {
-        const int cc = i >> 3, jj = (i & 7) * 8;
-        const int c = c0 + cc, j = j0 + jj;
-        if (c >= C || j >= Rp) continue;
-        uint16_t v[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) v[q] = tile[jj + q][cc];
-        uint4 u;
-        u.x = v[0] | (static_cast<uint32_t>(v[1]) << 16);
-        u.y = v[2] | (static_cast<uint32_t>(v[3]) << 16);
-        u.z = v[4] | (static_cast<uint32_t>(v[5]) << 16);
-        u.w = v[6] | (static_cast<uint32_t>(v[7]) << 16);
-        *reinterpret_cast<uint4 *>(dst + static_cast<size_t>(c) * Rp + j) = u;  // Rp is a multiple of 64
     }
 }
 
@@ -369,23 +225,9 @@ int warps_grid(int n) { return std::max(1, std::min((n + 7) / 8, 152 * 8)); }
 
 }  // namespace bw
 
-cudaError_t launch_transpose_bf16(const uint16_t *src, int B, int R, int C, const int32_t *skip_empty_offsets,
-                                  uint16_t *dst, cudaStream_t s) {
-    dim3 grid((C + 63) / 64, (R + 63) / 64, B);
-    bw::transpose64_kernel<<<grid, 256, 0, s>>>(src, R, C, skip_empty_offsets, dst);
-    return cudaGetLastError();
-}
-
 cudaError_t launch_transpose_f32(const float *src, int B, int R, int C, float *dst, cudaStream_t s) {
     dim3 grid((C + 31) / 32, (R + 31) / 32, B);
     bw::transpose_kernel<float><<<grid, 256, 0, s>>>(src, B, R, C, dst);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_transpose_grouped(const uint16_t *src, const int32_t *offsets, int E, int TK, int C, int Rp,
-                                     uint16_t *dst, cudaStream_t s) {
-    dim3 grid((C + 63) / 64, (Rp + 63) / 64);
-    bw::transpose_grouped_kernel<<<grid, 256, 0, s>>>(src, offsets, E, TK, C, Rp, dst);
     return cudaGetLastError();
 }
 

@@ -8,7 +8,11 @@
 //
 //   GEMM1 (SWIGLU = true):  h[r, n]      = bf16( silu(x_perm[r].W1[e,n]) * (x_perm[r].W1[e,f+n]) )
 //   GEMM2 (SWIGLU = false): y_perm[r, n] = bf16( h[r].W2[e,n] )
-// for every row r of expert e's group offsets[e]..offsets[e+1]-1.
+// for every row r of expert e's group offsets[e]..offsets[e+1]-1.  With
+// BT = true (plain GEMM only) the weights are read as stored [E, K, N], i.e.
+// out[r, n] = bf16( sum_k A[r,k] W[e,k,n] ): the layer backward's dgrad
+// products dy_perm.W2[e] and da.W1[e] without transposing the weights.  The
+// B tile then comes as MN-major 64 x 64 boxes and the MMAs read it MN-major.
 //
 // Design (both variants):
 //  * Persistent over a device-side tile list.  Every CTA reads offsets[] (E+1
@@ -56,7 +60,8 @@ constexpr int BK = 64;
 constexpr int UMMA_K = 16;
 constexpr int TMEM_COLS = 2 * BN_ACC;
 constexpr int THREADS = 192;
-constexpr int BOX_ROWS = 128;  // every TMA box is 128 rows x 64 bf16
+constexpr int BOX_ROWS = 128;  // every K-major TMA box is 128 rows x 64 bf16
+constexpr int BT_BOX = 64 * 64 * 2;  // MN-major B box: 64 K rows x 64 columns
 
 // single-CTA variant
 constexpr int BM = 128;
@@ -96,11 +101,12 @@ using L2 = Layout<P_STAGES, P_STAGE_BYTES>;
 constexpr int SMEM_BYTES = L1::BYTES;
 constexpr int P_SMEM_BYTES = L2::BYTES;
 static_assert(SMEM_BYTES <= 227 * 1024 && P_SMEM_BYTES <= 227 * 1024, "shared memory budget");
+static_assert(B_BYTES == (BN_ACC / 64) * BT_BOX && P_B_BYTES == 2 * BT_BOX, "MN-major B boxes fill the B slot");
 
 // ======================================================================
 // single-CTA variant
 // ======================================================================
-template <bool SWIGLU>
+template <bool SWIGLU, bool BT>
 __global__ void __launch_bounds__(THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmOut, const Params p) {
@@ -163,6 +169,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             for (int k = 0, tile = round_position(0, blockIdx.x, gridDim.x, mix); ok && tile < total_tiles;
                  ++k, tile = round_position(k, blockIdx.x, gridDim.x, mix)) {
                 const Tile t = decode_tile<BM, BAND>(visit_order(tile, total_tiles, mix), s_pre, s_off, s_end, E, NT);
+                static_assert(!(SWIGLU && BT), "the transposed-weight form is a plain GEMM");
                 int brow0, brow1;
                 if (SWIGLU) {
                     brow0 = t.e * p.w_rows + t.n_blk * (BN_ACC / 2);
@@ -177,8 +184,16 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     uint8_t *sb = sa + A_BYTES;
                     mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
                     tma_load_2d(sa, &tmA, &full[stage], kb * BK, t.row0);
-                    tma_load_2d(sb, &tmB, &full[stage], kb * BK, brow0);
-                    tma_load_2d(sb + B_BYTES / 2, &tmB, &full[stage], kb * BK, brow1);
+                    if (BT) {
+                        // W[e] rows kb*64.., columns of the 256-wide block in 64-wide boxes
+                        const int krow = t.e * p.Kdim + kb * BK;
+#pragma unroll
+                        for (int j = 0; j < BN_ACC / 64; ++j)
+                            tma_load_2d(sb + j * BT_BOX, &tmB, &full[stage], t.n_blk * BN_ACC + 64 * j, krow);
+                    } else {
+                        tma_load_2d(sb, &tmB, &full[stage], kb * BK, brow0);
+                        tma_load_2d(sb + B_BYTES / 2, &tmB, &full[stage], kb * BK, brow1);
+                    }
                     armed_phase[stage] = static_cast<int>(phase);
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
@@ -193,7 +208,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16_f32(BM, BN_ACC);
+            constexpr uint32_t idesc = idesc_bf16_f32(BM, BN_ACC, false, BT);
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
             bool ok = true;
             bool issued = false;
@@ -207,11 +222,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     tc_fence_after();
                     const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
                     const uint64_t adesc = smem_desc_kmajor_sw128(sa);
-                    const uint64_t bdesc = smem_desc_kmajor_sw128(sa + A_BYTES);
+                    const uint64_t bdesc = BT ? smem_desc_mnmajor_sw128(sa + A_BYTES, BT_BOX)
+                                              : smem_desc_kmajor_sw128(sa + A_BYTES);
 #pragma unroll
                     for (int j = 0; j < BK / UMMA_K; ++j) {
-                        // advance 16 elements (32 bytes) along K inside the swizzled row
-                        umma_bf16(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, (kb | j) != 0);
+                        // advance 16 elements along K: 32 bytes inside a K-major swizzled
+                        // row, 16 rows (2048 bytes) of an MN-major box
+                        umma_bf16(d_tmem, adesc + 2 * j, bdesc + (BT ? 128 : 2) * j, idesc, (kb | j) != 0);
                     }
                     issued = true;
                     umma_commit(&empty[stage]);
@@ -260,7 +277,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 // ======================================================================
 // CTA-pair variant (cluster of 2)
 // ======================================================================
-template <bool SWIGLU>
+template <bool SWIGLU, bool BT>
 __global__ void __launch_bounds__(THREADS, 1)
 grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                          const __grid_constant__ CUtensorMap tmOut, const Params p) {
@@ -344,7 +361,15 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
                     uint8_t *sb = sa + P_A_BYTES;
                     if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * P_STAGE_BYTES);
                     tma_load_2d_pair(sa, &tmA, full0 + 8u * stage, kb * BK, a_row);
-                    tma_load_2d_pair(sb, &tmB, full0 + 8u * stage, kb * BK, brow);
+                    if (BT) {
+                        // CTA r: columns 128r..128r+127 of the 256-wide block, two 64-wide boxes
+                        const int krow = t.e * p.Kdim + kb * BK;
+                        const int n0 = t.n_blk * BN_ACC + static_cast<int>(rank) * (BN_ACC / 2);
+                        tma_load_2d_pair(sb, &tmB, full0 + 8u * stage, n0, krow);
+                        tma_load_2d_pair(sb + BT_BOX, &tmB, full0 + 8u * stage, n0 + 64, krow);
+                    } else {
+                        tma_load_2d_pair(sb, &tmB, full0 + 8u * stage, kb * BK, brow);
+                    }
                     armed_phase[stage] = static_cast<int>(phase);
                     if (++stage == P_STAGES) { stage = 0; phase ^= 1u; }
                 }
@@ -365,7 +390,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
         }
     } else if (warp == 1) {
         if (lane == 0 && rank == 0) {
-            constexpr uint32_t idesc = idesc_bf16_f32(P_BM, BN_ACC);
+            constexpr uint32_t idesc = idesc_bf16_f32(P_BM, BN_ACC, false, BT);
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
             bool ok = true;
             bool issued = false;
@@ -379,10 +404,11 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
                     tc_fence_after();
                     const uint32_t sa = smem_u32(smem + stage * P_STAGE_BYTES);
                     const uint64_t adesc = smem_desc_kmajor_sw128(sa);
-                    const uint64_t bdesc = smem_desc_kmajor_sw128(sa + P_A_BYTES);
+                    const uint64_t bdesc = BT ? smem_desc_mnmajor_sw128(sa + P_A_BYTES, BT_BOX)
+                                              : smem_desc_kmajor_sw128(sa + P_A_BYTES);
 #pragma unroll
                     for (int j = 0; j < BK / UMMA_K; ++j)
-                        umma_bf16_pair(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, (kb | j) != 0);
+                        umma_bf16_pair(d_tmem, adesc + 2 * j, bdesc + (BT ? 128 : 2) * j, idesc, (kb | j) != 0);
                     issued = true;
                     umma_commit_pair_multicast(&empty[stage], 0x3);
                     if (++stage == P_STAGES) { stage = 0; phase ^= 1u; }
@@ -437,7 +463,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
 // ------------------------------------------------------------------ host side
 namespace {
 
-template <bool SWIGLU>
+template <bool SWIGLU, bool BT>
 cudaError_t launch_pair(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmOut,
                         const gg::Params &p, int grid, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
@@ -452,7 +478,7 @@ cudaError_t launch_pair(const CUtensorMap &tmA, const CUtensorMap &tmB, const CU
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gg::grouped_gemm_pair_kernel<SWIGLU>, tmA, tmB, tmOut, p);
+    return cudaLaunchKernelEx(&cfg, gg::grouped_gemm_pair_kernel<SWIGLU, BT>, tmA, tmB, tmOut, p);
 }
 
 template <bool SWIGLU>
@@ -469,7 +495,7 @@ int max_pairs() {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gg::grouped_gemm_pair_kernel<SWIGLU>, &cfg) != cudaSuccess) return 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gg::grouped_gemm_pair_kernel<SWIGLU, false>, &cfg) != cudaSuccess) return 0;
     return n;
 }
 
@@ -482,13 +508,20 @@ bool grouped_gemm_use_pair(int TK, int E) {
 
 cudaError_t launch_grouped_gemm(bool swiglu, const void *A, int TK, int Kdim, const void *W, int E, int n_out,
                                 const int32_t *offsets, void *out, const GemmLaunch &cfg, int *status,
-                                uint64_t timeout_ns, cudaStream_t stream, const CombineArgs *comb) {
+                                uint64_t timeout_ns, cudaStream_t stream, const CombineArgs *comb, bool b_trans) {
     CUtensorMap tmA, tmB;
+    if (b_trans && (swiglu || comb)) return cudaErrorInvalidValue;
     const int w_rows = swiglu ? 2 * n_out : n_out;
     if (!make_tmap(&tmA, A, static_cast<uint64_t>(TK), static_cast<uint64_t>(Kdim), gg::BOX_ROWS, gg::BK))
         return cudaErrorInvalidValue;
-    if (!make_tmap(&tmB, W, static_cast<uint64_t>(E) * w_rows, static_cast<uint64_t>(Kdim), gg::BOX_ROWS, gg::BK))
+    if (b_trans) {
+        // W as stored: [E * Kdim, n_out], 64 x 64 boxes
+        if (!make_tmap(&tmB, W, static_cast<uint64_t>(E) * Kdim, static_cast<uint64_t>(n_out), 64, 64))
+            return cudaErrorInvalidValue;
+    } else if (!make_tmap(&tmB, W, static_cast<uint64_t>(E) * w_rows, static_cast<uint64_t>(Kdim), gg::BOX_ROWS,
+                          gg::BK)) {
         return cudaErrorInvalidValue;
+    }
     CUtensorMap tmOut;
     if (!make_tmap(&tmOut, out, static_cast<uint64_t>(TK), static_cast<uint64_t>(n_out), 32, 32,
                    CU_TENSOR_MAP_SWIZZLE_64B))
@@ -516,34 +549,40 @@ cudaError_t launch_grouped_gemm(bool swiglu, const void *A, int TK, int Kdim, co
     p.timeout_ns = timeout_ns;
     const int pairs = swiglu ? cfg.pairs_swiglu : cfg.pairs_plain;
     if (grouped_gemm_use_pair(TK, E) && pairs > 0) {
-        return swiglu ? launch_pair<true>(tmA, tmB, tmOut, p, 2 * pairs, stream)
-                      : launch_pair<false>(tmA, tmB, tmOut, p, 2 * pairs, stream);
+        return swiglu    ? launch_pair<true, false>(tmA, tmB, tmOut, p, 2 * pairs, stream)
+               : b_trans ? launch_pair<false, true>(tmA, tmB, tmOut, p, 2 * pairs, stream)
+                         : launch_pair<false, false>(tmA, tmB, tmOut, p, 2 * pairs, stream);
     }
     if (swiglu)
-        gg::grouped_gemm_kernel<true><<<cfg.num_sms, gg::THREADS, gg::SMEM_BYTES, stream>>>(tmA, tmB, tmOut, p);
+        gg::grouped_gemm_kernel<true, false><<<cfg.num_sms, gg::THREADS, gg::SMEM_BYTES, stream>>>(tmA, tmB, tmOut, p);
+    else if (b_trans)
+        gg::grouped_gemm_kernel<false, true><<<cfg.num_sms, gg::THREADS, gg::SMEM_BYTES, stream>>>(tmA, tmB, tmOut, p);
     else
-        gg::grouped_gemm_kernel<false><<<cfg.num_sms, gg::THREADS, gg::SMEM_BYTES, stream>>>(tmA, tmB, tmOut, p);
+        gg::grouped_gemm_kernel<false, false><<<cfg.num_sms, gg::THREADS, gg::SMEM_BYTES, stream>>>(tmA, tmB, tmOut, p);
     return cudaGetLastError();
 }
 
 cudaError_t grouped_gemm_setup(int num_sms, GemmLaunch *cfg) {
     cudaError_t e;
-    if ((e = cudaFuncSetAttribute(gg::grouped_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  gg::SMEM_BYTES)) != cudaSuccess)
-        return e;
-    if ((e = cudaFuncSetAttribute(gg::grouped_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  gg::SMEM_BYTES)) != cudaSuccess)
-        return e;
-    if ((e = cudaFuncSetAttribute(gg::grouped_gemm_pair_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  gg::P_SMEM_BYTES)) != cudaSuccess)
-        return e;
-    if ((e = cudaFuncSetAttribute(gg::grouped_gemm_pair_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  gg::P_SMEM_BYTES)) != cudaSuccess)
-        return e;
+    const void *single[3] = {reinterpret_cast<const void *>(gg::grouped_gemm_kernel<true, false>),
+                             reinterpret_cast<const void *>(gg::grouped_gemm_kernel<false, false>),
+                             reinterpret_cast<const void *>(gg::grouped_gemm_kernel<false, true>)};
+    const void *pair[3] = {reinterpret_cast<const void *>(gg::grouped_gemm_pair_kernel<true, false>),
+                           reinterpret_cast<const void *>(gg::grouped_gemm_pair_kernel<false, false>),
+                           reinterpret_cast<const void *>(gg::grouped_gemm_pair_kernel<false, true>)};
+    for (int i = 0; i < 3; ++i) {
+        if ((e = cudaFuncSetAttribute(single[i], cudaFuncAttributeMaxDynamicSharedMemorySize, gg::SMEM_BYTES)) !=
+            cudaSuccess)
+            return e;
+        if ((e = cudaFuncSetAttribute(pair[i], cudaFuncAttributeMaxDynamicSharedMemorySize, gg::P_SMEM_BYTES)) !=
+            cudaSuccess)
+            return e;
+    }
     cfg->num_sms = num_sms;
     // every pair must be resident at once (the kernel is persistent): never
     // launch more pairs than fit, nor more CTAs than SMs
     cfg->pairs_swiglu = std::min(max_pairs<true>(), num_sms / 2);
+    // (the transposed-weight form has the plain form's resources)
     cfg->pairs_plain = std::min(max_pairs<false>(), num_sms / 2);
     cudaGetLastError();  // a failed occupancy query leaves pairs = 0: single-CTA kernels only
     return cudaSuccess;

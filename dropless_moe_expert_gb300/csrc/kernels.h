@@ -58,13 +58,8 @@ cudaError_t launch_grouped_gemm_mx(bool swiglu, const uint8_t *A, const uint8_t 
                                    const struct GemmLaunch &cfg, int *status, uint64_t timeout_ns, cudaStream_t stream);
 
 // Backward (backward.cu, wgrad.cu).
-// dst[b] = src[b]^T; with skip_empty_offsets [B+1], batches without rows are skipped
-cudaError_t launch_transpose_bf16(const uint16_t *src, int B, int R, int C, const int32_t *skip_empty_offsets,
-                                  uint16_t *dst, cudaStream_t s);
+// dst[b] = src[b]^T (fp32)
 cudaError_t launch_transpose_f32(const float *src, int B, int R, int C, float *dst, cudaStream_t s);
-// rows grouped by expert -> [C, Rp], each group from a 64-aligned column, zeros between
-cudaError_t launch_transpose_grouped(const uint16_t *src, const int32_t *offsets, int E, int TK, int C, int Rp,
-                                     uint16_t *dst, cudaStream_t s);
 cudaError_t launch_combine_bwd(const uint16_t *dy, const uint16_t *y_perm, const int32_t *row_of, const float *topk_w,
                                int T, int K, int d, float *dw, uint16_t *dy_perm, cudaStream_t s);
 cudaError_t launch_router_bwd(const float *topk_w, const float *dw, const int32_t *row_of, int T, int K, float *dl,
@@ -74,12 +69,10 @@ cudaError_t launch_router_wgrad(const uint16_t *x_perm, const float *dl_row, con
                                 int d, float *dWr, float *dbias, cudaStream_t s);
 cudaError_t launch_dx(const uint16_t *dx_perm, const float *WrT, const int32_t *row_of, const int32_t *topk_idx,
                       const float *dl, int T, int K, int E, int d, uint16_t *dx, cudaStream_t s);
-// padded row count of the grouped transposes (every group a multiple of 64)
-size_t wgrad_padded_rows(int TK, int E);
 cudaError_t wgrad_setup();
-// D[e] [M, N] fp32 = At[:, group e] . Bt[:, group e]^T over the padded groups
-cudaError_t launch_wgrad(const uint16_t *At, const uint16_t *Bt, int M, int N, int Rp, const int32_t *offsets, int E,
-                         int TK, float *D, int num_sms, int *status, uint64_t timeout_ns, cudaStream_t stream);
+// D[e] [M, N] fp32 = A[group e]^T . B[group e] for rows grouped by expert, A [TK, M], B [TK, N]
+cudaError_t launch_wgrad(const uint16_t *A, const uint16_t *B, int M, int N, const int32_t *offsets, int E, int TK,
+                         float *D, int num_sms, int *status, uint64_t timeout_ns, cudaStream_t stream);
 
 // Per-device launch shape of the grouped GEMM: SM count, and how many CTA
 // pairs of the pair kernel can be resident at once (0: single-CTA only).
@@ -105,9 +98,11 @@ struct CombineArgs {
     void *y;
 };
 // swiglu: GEMM1 (out [TK, n_out=f], W [E, 2f, Kdim=d]); else GEMM2 (out [TK, n_out=d], W [E, d, Kdim=f]).
+// b_trans (plain only): W is [E, Kdim, n_out] and out = A . W[e] (no transpose in memory).
 cudaError_t launch_grouped_gemm(bool swiglu, const void *A, int TK, int Kdim, const void *W, int E, int n_out,
                                 const int32_t *offsets, void *out, const GemmLaunch &cfg, int *status,
-                                uint64_t timeout_ns, cudaStream_t stream, const CombineArgs *comb = nullptr);
+                                uint64_t timeout_ns, cudaStream_t stream, const CombineArgs *comb = nullptr,
+                                bool b_trans = false);
 
 // A kernel whose only wait never completes: it times out after limit_ns and
 // records MOE_ERR_DEVICE_TIMEOUT in *status.

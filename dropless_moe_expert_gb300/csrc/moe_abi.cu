@@ -124,7 +124,6 @@ bool forward_mxfp8_layout(int T, int d, int E, int K, int f, moe_forward_mxfp8_l
 
 bool backward_layout(int T, int d, int E, int K, int f, moe_backward_layout_t *L) {
     const size_t TK = static_cast<size_t>(T) * K;
-    const size_t Rp = moe::wgrad_padded_rows(static_cast<int>(TK), E);
     size_t o = 0;
     auto take = [&](size_t bytes) {
         const size_t at = o;
@@ -139,13 +138,7 @@ bool backward_layout(int T, int d, int E, int K, int f, moe_backward_layout_t *L
     L->a = take(TK * 2 * f * 2);
     L->da = take(TK * 2 * f * 2);
     L->dx_perm = take(TK * d * 2);
-    L->W1T = take(static_cast<size_t>(E) * 2 * f * d * 2);
-    L->W2T = take(static_cast<size_t>(E) * f * d * 2);
     L->WrT = take(static_cast<size_t>(E) * d * 4);
-    L->dyT = take(static_cast<size_t>(d) * Rp * 2);
-    L->hT = take(static_cast<size_t>(f) * Rp * 2);
-    L->daT = take(static_cast<size_t>(2 * f) * Rp * 2);
-    L->xT = take(static_cast<size_t>(d) * Rp * 2);
     L->total = o;
     return true;
 }
@@ -185,7 +178,7 @@ const char *moe_status_string(int status) {
     }
 }
 
-int moe_abi_version(void) { return 200; }
+int moe_abi_version(void) { return 201; }
 
 uint64_t moe_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
@@ -568,44 +561,33 @@ moe_status_t moe_backward(const uint16_t *x, const float *Wr, const float *bias,
     uint16_t *a = reinterpret_cast<uint16_t *>(bv(B.a));
     uint16_t *da = reinterpret_cast<uint16_t *>(bv(B.da));
     uint16_t *dx_perm = reinterpret_cast<uint16_t *>(bv(B.dx_perm));
-    uint16_t *W1T = reinterpret_cast<uint16_t *>(bv(B.W1T));
-    uint16_t *W2T = reinterpret_cast<uint16_t *>(bv(B.W2T));
     float *WrT = reinterpret_cast<float *>(bv(B.WrT));
-    uint16_t *dyT = reinterpret_cast<uint16_t *>(bv(B.dyT));
-    uint16_t *hT = reinterpret_cast<uint16_t *>(bv(B.hT));
-    uint16_t *daT = reinterpret_cast<uint16_t *>(bv(B.daT));
-    uint16_t *xT = reinterpret_cast<uint16_t *>(bv(B.xT));
     const int TK = T * K;
-    const int Rp = static_cast<int>(moe::wgrad_padded_rows(TK, E));
     const moe::GemmLaunch &g = ds->gemm;
     cudaError_t e = cudaSuccess;
     auto go = [&](cudaError_t r, int launches) {
         if (e == cudaSuccess) e = r;
         g_launches.fetch_add(launches, std::memory_order_relaxed);
     };
-    // weights transposed for the dgrad GEMMs (K-major B operands), Wr for dx
-    go(moe::launch_transpose_bf16(W2, E, d, f, offsets, W2T, stream), 1);
-    go(moe::launch_transpose_bf16(W1, E, 2 * f, d, offsets, W1T, stream), 1);
+    // Wr transposed for dx (the dgrad GEMMs read W1 and W2 as stored, MN-major)
     go(moe::launch_transpose_f32(Wr, 1, d, E, WrT, stream), 1);
     // combine and router
     go(moe::launch_combine_bwd(dy, y_perm, row_of, topk_w, T, K, d, dw, dy_perm, stream), 1);
     go(moe::launch_router_bwd(topk_w, dw, row_of, T, K, dl, dl_row, stream), 1);
     // GEMM2 dgrad: dh = dy_perm . W2[e]
-    go(moe::launch_grouped_gemm(false, dy_perm, TK, d, W2T, E, f, offsets, dh, g, ds->status, kWaitLimitNs, stream), 1);
+    go(moe::launch_grouped_gemm(false, dy_perm, TK, d, W2, E, f, offsets, dh, g, ds->status, kWaitLimitNs, stream,
+                                nullptr, true),
+       1);
     // GEMM1 pre-activations again, then SwiGLU backward
     go(moe::launch_grouped_gemm(false, x_perm, TK, d, W1, E, 2 * f, offsets, a, g, ds->status, kWaitLimitNs, stream), 1);
     go(moe::launch_swiglu_bwd(a, dh, TK, f, da, stream), 1);
     // GEMM1 dgrad: dx_perm = da . W1[e]
-    go(moe::launch_grouped_gemm(false, da, TK, 2 * f, W1T, E, d, offsets, dx_perm, g, ds->status, kWaitLimitNs,
-                                stream),
+    go(moe::launch_grouped_gemm(false, da, TK, 2 * f, W1, E, d, offsets, dx_perm, g, ds->status, kWaitLimitNs,
+                                stream, nullptr, true),
        1);
-    // weight gradients over each expert's rows
-    go(moe::launch_transpose_grouped(dy_perm, offsets, E, TK, d, Rp, dyT, stream), 1);
-    go(moe::launch_transpose_grouped(h, offsets, E, TK, f, Rp, hT, stream), 1);
-    go(moe::launch_wgrad(dyT, hT, d, f, Rp, offsets, E, TK, dW2, ds->num_sms, ds->status, kWaitLimitNs, stream), 1);
-    go(moe::launch_transpose_grouped(da, offsets, E, TK, 2 * f, Rp, daT, stream), 1);
-    go(moe::launch_transpose_grouped(x_perm, offsets, E, TK, d, Rp, xT, stream), 1);
-    go(moe::launch_wgrad(daT, xT, 2 * f, d, Rp, offsets, E, TK, dW1, ds->num_sms, ds->status, kWaitLimitNs, stream),
+    // weight gradients over each expert's rows: dW2[e] = dy_perm[e]^T h[e], dW1[e] = da[e]^T x_perm[e]
+    go(moe::launch_wgrad(dy_perm, h, d, f, offsets, E, TK, dW2, ds->num_sms, ds->status, kWaitLimitNs, stream), 1);
+    go(moe::launch_wgrad(da, x_perm, 2 * f, d, offsets, E, TK, dW1, ds->num_sms, ds->status, kWaitLimitNs, stream),
        1);
     // router weights and the input gradient
     go(moe::launch_router_wgrad(x_perm, dl_row, offsets, E, TK, d, dWr, dbias, stream), 1);

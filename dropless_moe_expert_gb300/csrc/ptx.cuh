@@ -322,12 +322,30 @@ __device__ __forceinline__ uint64_t smem_desc_kmajor_sw128(uint32_t saddr) {
     return d;
 }
 
-// Instruction descriptor of tcgen05.mma kind::f16: D fp32, A and B bf16, both
-// K-major, shape M x N.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+// Shared-memory matrix descriptor of an MN-major bf16 tile: the M (or N)
+// extent in blocks of 64 consecutive elements, each block one SWIZZLE_128B TMA
+// box of K rows x 128 bytes; within a block, 8-row K groups are 1024 bytes
+// apart (stride byte offset), and the blocks are `mn_block_bytes` apart
+// (leading byte offset).  Advancing K by 16 moves the start by 2048 bytes.
+__device__ __forceinline__ uint64_t smem_desc_mnmajor_sw128(uint32_t saddr, uint32_t mn_block_bytes) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>((mn_block_bytes & 0x3FFFFu) >> 4) << 16;
+    d |= static_cast<uint64_t>(1024u >> 4) << 32;
+    d |= static_cast<uint64_t>(1u) << 46;
+    d |= static_cast<uint64_t>(2u) << 61;
+    return d;
+}
+
+// Instruction descriptor of tcgen05.mma kind::f16: D fp32, A and B bf16,
+// shape M x N; each operand K-major unless `a_mn` / `b_mn` marks it MN-major
+// (the transpose bits 15 and 16).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn = false, bool b_mn = false) {
     return (1u << 4)                                   // D format: f32
            | (1u << 7)                                 // A format: bf16
            | (1u << 10)                                // B format: bf16
+           | ((a_mn ? 1u : 0u) << 15)                  // A MN-major
+           | ((b_mn ? 1u : 0u) << 16)                  // B MN-major
            | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
            | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }

@@ -1,5 +1,5 @@
 // Weight gradients of the grouped GEMMs: for every expert e,
-//     D[e] = A^T[:, group e] . B^T[:, group e]^T    (M x N, fp32)
+//     D[e] = A[group e]^T . B[group e]    (M x N, fp32)
 // i.e. dW2[e] = dy_perm[e]^T h[e] (M = d, N = f) and dW1[e] = da[e]^T x_perm[e]
 // (M = 2f, N = d): a sum over the expert's own rows, a ragged reduction
 // length per expert.
@@ -9,19 +9,20 @@
 // Transformer Engine"); its weight gradients reduce over each expert's actual
 // token rows, again without padding to a capacity.
 //
-// Operands are the transposed activations, K-major: A^T [M, Rp] and B^T
-// [N, Rp] bf16, in which group e occupies columns pstart[e] ..
-// pstart[e] + count[e] - 1 with pstart[e] = sum over e' < e of
-// round_up(count[e'], 64) and zeros in the padding columns.  Every TMA K
-// coordinate is then a multiple of 64 (16-byte aligned) and the padding adds
-// nothing to the sums.
+// Operands are the activations as the forward and backward leave them: rows
+// grouped by expert, A [TK, M] and B [TK, N] bf16, row-major.  The reduction
+// runs along the rows, so both operands are MN-major: a stage holds 64 rows
+// (K) of A's 128 columns and B's 256 columns as 64 x 64 TMA boxes (128-byte
+// swizzle), and the MMAs read them with MN-major descriptors -- no transposed
+// copy in memory.  A group's K blocks start at its first row; in its last
+// block the rows past the group (the next expert's rows, or TMA zero fill
+// past TK) are zeroed in shared memory before the MMAs, so they add nothing.
 //
 // Persistent kernel, one CTA per SM: tiles (e, 128-row block, 256-column
-// block) of every expert; a 4-stage ring of 64-wide K slices (A 128 x 64,
-// B 2 x 128 x 64, 128-byte swizzle); tcgen05.mma M=128 N=256 K=16 into two
-// 256-column TMEM accumulators, so a tile's epilogue (fp32 stores, masked at
-// M and N) overlaps the next tile's mainloop.  Experts without rows get their
-// tiles written as zeros.  Bounded waits as in the forward GEMMs.
+// block) of every expert; a 3-stage ring; tcgen05.mma M=128 N=256 K=16 into
+// two 256-column TMEM accumulators, so a tile's epilogue (fp32 by TMA stores
+// of 32 x 32 boxes) overlaps the next tile's mainloop.  Experts without rows
+// get their tiles written as zeros.  Bounded waits as in the forward GEMMs.
 #include "kernels.h"
 #include "ptx.cuh"
 #include "tmap.h"
@@ -34,19 +35,24 @@ constexpr int BN = 256;
 constexpr int BK = 64;
 constexpr int UMMA_K = 16;
 constexpr int THREADS = 192;
-constexpr int STAGES = 4;
+constexpr int STAGES = 3;
 constexpr int MAX_E = 256;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
 constexpr int STAGE = A_BYTES + B_BYTES;
 constexpr int TMEM_COLS = 2 * BN;
-constexpr int OFF_BARS = STAGES * STAGE;
+// epilogue staging: per epilogue warp two 32 x 32 fp32 boxes (128-byte swizzle)
+constexpr int EPI_BUF = 32 * 32 * 4;
+constexpr int OFF_EPI = STAGES * STAGE;
+constexpr int OFF_BARS = OFF_EPI + 4 * 2 * EPI_BUF;
 constexpr int NUM_BARS = 2 * STAGES + 5;  // full, empty, tfull[2], tempty[2], drain
 constexpr int OFF_TMEM = OFF_BARS + NUM_BARS * 8;
 constexpr int OFF_ABORT = OFF_TMEM + 4;
-constexpr int OFF_PST = OFF_ABORT + 4;
-constexpr int OFF_PCNT = OFF_PST + MAX_E * 4;
-constexpr int SMEM_BYTES = OFF_PCNT + MAX_E * 4 + 1024;
+constexpr int OFF_GOFF = OFF_ABORT + 4;
+constexpr int OFF_GCNT = OFF_GOFF + MAX_E * 4;
+constexpr int SMEM_BYTES = OFF_GCNT + MAX_E * 4 + 1024;
+constexpr int BOX = 64 * 64 * 2;  // one 64-row x 64-column bf16 box
+static_assert(A_BYTES == 2 * BOX && B_BYTES == 4 * BOX, "a stage is six boxes");
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 
 struct Params {
@@ -57,26 +63,14 @@ struct Params {
     uint64_t timeout_ns;
 };
 
-// Padded group starts and K lengths from offsets (clamped to [0, TK]); one warp.
-__device__ __forceinline__ void padded_groups(const Params &p, int lane, int *s_pst, int *s_pcnt) {
-    int carry = 0;
-    for (int base = 0; base < p.E; base += 32) {
-        const int e = base + lane;
-        int v = 0;
-        if (e < p.E) {
-            const int o0 = min(max(p.offsets[e], 0), p.TK);
-            const int o1 = min(max(p.offsets[e + 1], o0), p.TK);
-            v = (o1 - o0 + BK - 1) / BK * BK;
-            s_pcnt[e] = v;
-        }
-        int incl = v;
-#pragma unroll
-        for (int s = 1; s < 32; s <<= 1) {
-            const int n = __shfl_up_sync(0xffffffffu, incl, s);
-            if (lane >= s) incl += n;
-        }
-        if (e < p.E) s_pst[e] = carry + incl - v;
-        carry += __shfl_sync(0xffffffffu, incl, 31);
+// Group starts and row counts from offsets, clamped to [0, TK] (so no content
+// of offsets sends a load outside the activations); one warp.
+__device__ __forceinline__ void groups(const Params &p, int lane, int *s_goff, int *s_gcnt) {
+    for (int e = lane; e < p.E; e += 32) {
+        const int o0 = min(max(p.offsets[e], 0), p.TK);
+        const int o1 = min(max(p.offsets[e + 1], o0), p.TK);
+        s_goff[e] = o0;
+        s_gcnt[e] = o1 - o0;
     }
 }
 
@@ -95,12 +89,16 @@ __device__ __forceinline__ Tile decode(const Params &p, int tile) {
     return t;
 }
 
-// One warp's 32 rows of a tile: fp32 out, masked at M and N.  `zero`: the
-// expert has no rows, the accumulator is not read.
-__device__ __forceinline__ void epilogue(const Params &p, const Tile &t, uint32_t tbase, int q, int lane, bool zero) {
-    const int m = t.m0 + q * 32 + lane;
-    const bool row_ok = m < p.M;
-    float *row = p.D + (static_cast<size_t>(t.e) * p.M + m) * p.N;
+// One warp's 32 rows of a tile, 32 columns at a time: the fp32 values go to
+// shared memory (128-byte swizzle: 16-byte chunk j of row i at j ^ (i & 7))
+// and one TMA store writes the 32 x 32 box as full lines (L2 evict-first:
+// the gradients are not read again here).  M and N are multiples of 32, so
+// boxes are whole; a warp whose 32 rows lie past M stores nothing.  `zero`:
+// the expert has no rows, the accumulator is not read.
+__device__ __forceinline__ void epilogue(const Params &p, const CUtensorMap *tm_out, const Tile &t, uint32_t tbase,
+                                         int q, int lane, bool zero, uint8_t *stage, uint32_t &sbuf) {
+    const int m0 = t.m0 + q * 32;
+    if (m0 >= p.M) return;  // warp-uniform
 #pragma unroll 1
     for (int c = 0; c < BN; c += 32) {
         const int n = t.n0 + c;
@@ -113,25 +111,26 @@ __device__ __forceinline__ void epilogue(const Params &p, const Tile &t, uint32_
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = 0u;
         }
-        if (row_ok) {
-            if (n + 32 <= p.N && (p.N % 4) == 0) {
+        uint8_t *buf = stage + sbuf * EPI_BUF;
+        if (lane == 0) bulk_wait_read<1>();  // this buffer's store from two chunks ago has read it
+        __syncwarp();
 #pragma unroll
-                for (int i = 0; i < 32; i += 4)
-                    *reinterpret_cast<float4 *>(row + n + i) = make_float4(
-                        __uint_as_float(v[i]), __uint_as_float(v[i + 1]), __uint_as_float(v[i + 2]),
-                        __uint_as_float(v[i + 3]));
-            } else {
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    if (n + i < p.N) row[n + i] = __uint_as_float(v[i]);
-            }
+        for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<uint4 *>(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+                make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d_evict_first(tm_out, buf, n, t.e * p.M + m0, l2_policy_evict_first());
+            bulk_commit();
         }
-        __syncwarp();  // converged before the next tcgen05.ld
+        sbuf ^= 1u;
     }
 }
 
 __global__ void __launch_bounds__(THREADS, 1)
-wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Params p) {
+wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+             const __grid_constant__ CUtensorMap tmD, const Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_BARS);
@@ -142,8 +141,8 @@ wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
     uint64_t *drain = tfull + 4;
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(smem + OFF_TMEM);
     volatile int *s_abort = reinterpret_cast<volatile int *>(smem + OFF_ABORT);
-    int *s_pst = reinterpret_cast<int *>(smem + OFF_PST);
-    int *s_pcnt = reinterpret_cast<int *>(smem + OFF_PCNT);
+    int *s_goff = reinterpret_cast<int *>(smem + OFF_GOFF);
+    int *s_gcnt = reinterpret_cast<int *>(smem + OFF_GCNT);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -166,7 +165,7 @@ wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
         tmem_alloc(s_tmem, TMEM_COLS);
         tmem_relinquish();
     }
-    if (warp == 2) padded_groups(p, lane, s_pst, s_pcnt);
+    if (warp == 2) groups(p, lane, s_goff, s_gcnt);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -182,16 +181,19 @@ wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
                 const Tile t = decode(p, tile);
-                const int KB = s_pcnt[t.e] / BK;
-                const int k0 = s_pst[t.e];
+                const int KB = (s_gcnt[t.e] + BK - 1) / BK;
+                const int r0 = s_goff[t.e];
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, s_abort, p.status, p.timeout_ns)) { ok = false; break; }
                     uint8_t *sa = smem + stage * STAGE;
                     uint8_t *sb = sa + A_BYTES;
+                    const int row = r0 + kb * BK;
                     mbar_arrive_expect_tx(&full[stage], STAGE);
-                    tma_load_2d(sa, &tmA, &full[stage], k0 + kb * BK, t.m0);
-                    tma_load_2d(sb, &tmB, &full[stage], k0 + kb * BK, t.n0);
-                    tma_load_2d(sb + B_BYTES / 2, &tmB, &full[stage], k0 + kb * BK, t.n0 + BN / 2);
+                    // columns past M or N read TMA zero fill
+                    tma_load_2d(sa, &tmA, &full[stage], t.m0, row);
+                    tma_load_2d(sa + BOX, &tmA, &full[stage], t.m0 + 64, row);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) tma_load_2d(sb + j * BOX, &tmB, &full[stage], t.n0 + 64 * j, row);
                     armed_phase[stage] = static_cast<int>(phase);
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
@@ -204,55 +206,81 @@ wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
-            uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
-            bool ok = true, issued = false;
-            for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-                const Tile t = decode(p, tile);
-                const int KB = s_pcnt[t.e] / BK;
-                if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, s_abort, p.status, p.timeout_ns)) { ok = false; break; }
+        // The whole warp follows the ring: lane 0 waits and issues, all lanes
+        // zero the rows past a group in its last K block.
+        constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, true, true);
+        uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+        bool ok = true, issued = false;
+        for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+            const Tile t = decode(p, tile);
+            const int cnt = s_gcnt[t.e];
+            const int KB = (cnt + BK - 1) / BK;
+            int w = 1;
+            if (lane == 0) w = mbar_wait(&tempty[acc], acc_phase ^ 1u, s_abort, p.status, p.timeout_ns);
+            if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + acc * BN;
+            for (int kb = 0; kb < KB; ++kb) {
+                if (lane == 0) w = mbar_wait(&full[stage], phase, s_abort, p.status, p.timeout_ns);
+                if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + acc * BN;
-                for (int kb = 0; kb < KB; ++kb) {
-                    if (!mbar_wait(&full[stage], phase, s_abort, p.status, p.timeout_ns)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint32_t sa = smem_u32(smem + stage * STAGE);
-                    const uint64_t adesc = smem_desc_kmajor_sw128(sa);
-                    const uint64_t bdesc = smem_desc_kmajor_sw128(sa + A_BYTES);
-#pragma unroll
-                    for (int j = 0; j < BK / UMMA_K; ++j)
-                        umma_bf16(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, (kb | j) != 0);
-                    issued = true;
-                    umma_commit(&empty[stage]);
-                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                uint8_t *sa = smem + stage * STAGE;
+                const int valid = cnt - kb * BK;  // warp-uniform
+                if (valid < BK) {
+                    // rows valid..63 of each of the six boxes: one contiguous
+                    // byte range per box (a 128-byte row holds all its swizzled chunks)
+                    const int zbytes = (BK - valid) * 128;
+#pragma unroll 1
+                    for (int b = 0; b < 6; ++b) {
+                        uint8_t *z = sa + b * BOX + valid * 128;
+                        for (int o = lane * 16; o < zbytes; o += 32 * 16)
+                            *reinterpret_cast<uint4 *>(z + o) = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
                 }
-                if (!ok) break;
-                umma_commit(&tfull[acc]);  // with no MMAs (empty expert) it arrives at once
-                acc ^= 1u;
-                if (acc == 0) acc_phase ^= 1u;
+                if (lane == 0) {
+                    const uint32_t a_addr = smem_u32(sa);
+                    const uint64_t adesc = smem_desc_mnmajor_sw128(a_addr, BOX);
+                    const uint64_t bdesc = smem_desc_mnmajor_sw128(a_addr + A_BYTES, BOX);
+#pragma unroll
+                    for (int j = 0; j < BK / UMMA_K; ++j)  // 16 rows of K: 2048 bytes further
+                        umma_bf16(d_tmem, adesc + 128 * j, bdesc + 128 * j, idesc, (kb | j) != 0);
+                    umma_commit(&empty[stage]);
+                }
+                issued = true;
+                __syncwarp();
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
-            if (!ok && issued) {
-                volatile int no_abort = 0;
-                umma_commit(drain);
-                mbar_wait(drain, 0, &no_abort, p.status, p.timeout_ns);
-            }
+            if (!ok) break;
+            if (lane == 0) umma_commit(&tfull[acc]);  // with no MMAs (empty expert) it arrives at once
+            __syncwarp();
+            acc ^= 1u;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+        if (!ok && issued && lane == 0) {
+            volatile int no_abort = 0;
+            umma_commit(drain);
+            mbar_wait(drain, 0, &no_abort, p.status, p.timeout_ns);
         }
     } else {
         const int q = warp & 3;
+        uint8_t *stage = smem + OFF_EPI + (warp - 2) * 2 * EPI_BUF;
+        uint32_t sbuf = 0;
         uint32_t acc = 0, acc_phase = 0;
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
             const Tile t = decode(p, tile);
             if (!mbar_wait(&tfull[acc], acc_phase, s_abort, p.status, p.timeout_ns)) break;
             tc_fence_after();
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
-            epilogue(p, t, tbase, q, lane, s_pcnt[t.e] == 0);
+            epilogue(p, &tmD, t, tbase, q, lane, s_gcnt[t.e] == 0, stage, sbuf);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[acc]);
             acc ^= 1u;
             if (acc == 0) acc_phase ^= 1u;
         }
+        if (lane == 0) bulk_wait_all();  // stores done before the CTA's shared memory goes away
     }
 
     tc_fence_before();
@@ -265,24 +293,22 @@ wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
 
 }  // namespace wg
 
-size_t wgrad_padded_rows(int TK, int E) {
-    // every group padded to a multiple of 64 rows, and the total a multiple
-    // of 64 (16-byte row strides for TMA)
-    return (static_cast<size_t>(TK) + 63) / 64 * 64 + static_cast<size_t>(E) * wg::BK;
-}
-
 cudaError_t wgrad_setup() {
     return cudaFuncSetAttribute(wg::wgrad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, wg::SMEM_BYTES);
 }
 
-cudaError_t launch_wgrad(const uint16_t *At, const uint16_t *Bt, int M, int N, int Rp, const int32_t *offsets, int E,
-                         int TK, float *D, int num_sms, int *status, uint64_t timeout_ns, cudaStream_t stream) {
-    CUtensorMap tmA, tmB;
-    if (!make_tmap(&tmA, At, static_cast<uint64_t>(M), static_cast<uint64_t>(Rp), wg::BM, wg::BK))
+cudaError_t launch_wgrad(const uint16_t *A, const uint16_t *B, int M, int N, const int32_t *offsets, int E, int TK,
+                         float *D, int num_sms, int *status, uint64_t timeout_ns, cudaStream_t stream) {
+    CUtensorMap tmA, tmB, tmD;
+    if (M % 64 != 0 || N % 64 != 0 || TK < 1) return cudaErrorInvalidValue;
+    // A [TK, M] and B [TK, N] with 64-row x 64-column boxes
+    if (!make_tmap(&tmA, A, static_cast<uint64_t>(TK), static_cast<uint64_t>(M), 64, 64)) return cudaErrorInvalidValue;
+    if (!make_tmap(&tmB, B, static_cast<uint64_t>(TK), static_cast<uint64_t>(N), 64, 64)) return cudaErrorInvalidValue;
+    // D as [E * M, N] fp32, 32 x 32 boxes of 128-byte rows
+    if (!make_tmap_2d(&tmD, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, static_cast<uint64_t>(E) * M,
+                      static_cast<uint64_t>(N), 32, 32, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
-    if (!make_tmap(&tmB, Bt, static_cast<uint64_t>(N), static_cast<uint64_t>(Rp), wg::BN / 2, wg::BK))
-        return cudaErrorInvalidValue;
-    wg::Params p;
+    wg::Params p = {};
     p.offsets = offsets;
     p.E = E;
     p.TK = TK;
@@ -293,7 +319,7 @@ cudaError_t launch_wgrad(const uint16_t *At, const uint16_t *Bt, int M, int N, i
     p.D = D;
     p.status = status;
     p.timeout_ns = timeout_ns;
-    wg::wgrad_kernel<<<num_sms, wg::THREADS, wg::SMEM_BYTES, stream>>>(tmA, tmB, p);
+    wg::wgrad_kernel<<<num_sms, wg::THREADS, wg::SMEM_BYTES, stream>>>(tmA, tmB, tmD, p);
     return cudaGetLastError();
 }
 

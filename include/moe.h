@@ -278,12 +278,13 @@ moe_status_t moe_forward_mxfp8(const uint16_t *x, const float *Wr, const float *
  * weights (it holds the routing, x_perm, h and y_perm the backward reuses);
  * `workspace` holds moe_backward_workspace_size() bytes of scratch
  * (moe_backward_views() gives its regions).  The dgrad GEMMs run on the
- * forward's grouped GEMM with transposed weights, the weight gradients on a
- * grouped GEMM whose reduction runs over each expert's own rows.  All sums
- * have a fixed order: the gradients are deterministic.  17 kernel launches.  */
+ * forward's grouped GEMM reading W1 and W2 as stored (MN-major operands),
+ * the weight gradients on a grouped GEMM whose reduction runs over each
+ * expert's own rows, read from the grouped activations in place.  All sums
+ * have a fixed order: the gradients are deterministic.  11 kernel launches.  */
 size_t moe_backward_workspace_size(int T, int d, int E, int K, int f);
 typedef struct {
-    size_t dw, dl, dl_row, dy_perm, dh, a, da, dx_perm, W1T, W2T, WrT, dyT, hT, daT, xT, total;
+    size_t dw, dl, dl_row, dy_perm, dh, a, da, dx_perm, WrT, total;
 } moe_backward_layout_t;
 moe_status_t moe_backward_views(int T, int d, int E, int K, int f, moe_backward_layout_t *layout);
 moe_status_t moe_backward(const uint16_t *x, const float *Wr, const float *bias, const uint16_t *W1,
