@@ -499,14 +499,16 @@ def run_train_step(args):
     dy = torch.randn((T, d), generator=g, device=dev).to(torch.bfloat16)
     layer = moe.MoELayer(w.Wr, w.bias, w.W1, w.W2, K, T)
     y = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
-    layer(x, out=y)
+    layer(x, out=y, save_preact=True)
     grads = layer.backward(x, dy)
     stream = torch.cuda.current_stream()
 
     def step(ev=None):
+        # the forward keeps GEMM1's pre-activations for the backward (as a
+        # training framework stores its saved activations)
         if ev is not None:
             ev[0].record(stream)
-        layer(x, out=y)
+        layer(x, out=y, save_preact=True)
         if ev is not None:
             ev[1].record(stream)
         layer.backward(x, dy, grads=grads, workspace=layer.bw_workspace)
@@ -546,7 +548,8 @@ def run_train_step(args):
             "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) tokens and output gradient)",
             "config": dict(_config(args.config, s, ws), step="forward + backward",
-                           grads="dx bf16; dWr, dbias, dW1, dW2 fp32"),
+                           grads="dx bf16; dWr, dbias, dW1, dW2 fp32",
+                           saved="GEMM1 pre-activations [T*K, 2f] bf16, stored by the forward"),
             "kernels": {"forward": {"ms": fwd_ms, "TFLOP/s": 6.0 * TK * d * f / (fwd_ms * 1e-3) / 1e12},
                         "backward": {"ms": bwd_ms, "TFLOP/s": 12.0 * TK * d * f / (bwd_ms * 1e-3) / 1e12}},
             "gpu_launches": launches, "clocks": clocks,

@@ -76,11 +76,13 @@ def _load():
         "moe_permute": (I, [P, P, I, I, I, P, P]),
         "moe_grouped_mlp": (I, [P, P, I, I, I, I, P, P, P, P, P]),
         "moe_grouped_gemm1_swiglu": (I, [P, P, I, I, I, I, P, P, P]),
+        "moe_grouped_gemm1_swiglu_preact": (I, [P, P, I, I, I, I, P, P, P, P]),
         "moe_grouped_gemm2": (I, [P, P, I, I, I, I, P, P, P]),
         "moe_unpermute": (I, [P, P, P, I, I, I, P, P]),
         "moe_forward_workspace_size": (S, [I, I, I, I, I]),
         "moe_forward_views": (I, [I, I, I, I, I, ctypes.POINTER(_Layout)]),
         "moe_forward": (I, [P, P, P, P, P, I, I, I, I, I, P, P, S, P]),
+        "moe_forward_train": (I, [P, P, P, P, P, I, I, I, I, I, P, P, S, P, P]),
         "moe_forward_host": (I, [P, P, P, P, P, I, I, I, I, I, P, P, S, P]),
         "moe_mxfp8_scales_size": (S, [I, I]),
         "moe_mxfp8_quantize": (I, [P, I, I, P, P, P]),
@@ -93,7 +95,7 @@ def _load():
         "moe_forward_mxfp8": (I, [P, P, P, P, P, P, P, I, I, I, I, I, P, P, S, P]),
         "moe_backward_workspace_size": (S, [I, I, I, I, I]),
         "moe_backward_views": (I, [I, I, I, I, I, ctypes.POINTER(_LayoutBW)]),
-        "moe_backward": (I, [P, P, P, P, P, I, I, I, I, I, P, P, S, P, P, P, P, P, P, S, P]),
+        "moe_backward": (I, [P, P, P, P, P, I, I, I, I, I, P, P, S, P, P, P, P, P, P, P, S, P]),
         "moe_combine_counters_size": (S, [I, I]),
         "moe_grouped_gemm2_combine": (I, [P, P, I, I, I, I, P, P, P, P, I, I, P, P, S, P, P]),
         "moe_device_status": (I, [ctypes.POINTER(I)]),
@@ -219,14 +221,20 @@ def _mlp_shapes(x_perm, offsets, W1=None, W2=None):
     return TK, d, E, f
 
 
-def grouped_gemm1_swiglu(x_perm, offsets, W1, h=None, stream=None):
+def grouped_gemm1_swiglu(x_perm, offsets, W1, h=None, preact=None, stream=None):
+    """h [TK, f]; with ``preact`` ([TK, 2f] bf16) the pre-activations are stored too."""
     TK, d, E, f = _mlp_shapes(x_perm, offsets, W1=W1)
     _need(x_perm, torch.bfloat16, (TK, d), "x_perm")
     _need(offsets, torch.int32, (E + 1,), "offsets")
     _need(W1, torch.bfloat16, (E, 2 * f, d), "W1")
     h = _empty((TK, f), torch.bfloat16, x_perm) if h is None else _need(h, torch.bfloat16, (TK, f), "h")
-    _check(lib.moe_grouped_gemm1_swiglu(_ptr(x_perm), _ptr(offsets), E, TK, d, f, _ptr(W1), _ptr(h),
-                                        _stream(stream)), "moe_grouped_gemm1_swiglu")
+    if preact is None:
+        _check(lib.moe_grouped_gemm1_swiglu(_ptr(x_perm), _ptr(offsets), E, TK, d, f, _ptr(W1), _ptr(h),
+                                            _stream(stream)), "moe_grouped_gemm1_swiglu")
+    else:
+        _need(preact, torch.bfloat16, (TK, 2 * f), "preact")
+        _check(lib.moe_grouped_gemm1_swiglu_preact(_ptr(x_perm), _ptr(offsets), E, TK, d, f, _ptr(W1), _ptr(h),
+                                                   _ptr(preact), _stream(stream)), "moe_grouped_gemm1_swiglu_preact")
     return h
 
 
@@ -314,8 +322,10 @@ def _weights_check(x, Wr, bias, W1, W2, K):
     return T, d, E, f
 
 
-def forward(x, Wr, bias, W1, W2, K: int, out=None, workspace=None, stream=None):
-    """The whole layer in one C-ABI call (9 kernel launches, no host sync)."""
+def forward(x, Wr, bias, W1, W2, K: int, out=None, workspace=None, stream=None, preact=None):
+    """The whole layer in one C-ABI call (9 kernel launches, no host sync).
+    With ``preact`` ([T*K, 2f] bf16) GEMM1 also stores the pre-activations
+    for a backward pass (moe_forward_train)."""
     T, d, E, f = _weights_check(x, Wr, bias, W1, W2, K)
     _need(x, torch.bfloat16, (T, d), "x")
     nbytes = forward_workspace_size(T, d, E, K, f)
@@ -324,8 +334,14 @@ def forward(x, Wr, bias, W1, W2, K: int, out=None, workspace=None, stream=None):
     if workspace is None:
         workspace = _empty((nbytes,), torch.uint8, x)
     out = _empty((T, d), torch.bfloat16, x) if out is None else _need(out, torch.bfloat16, (T, d), "y")
-    _check(lib.moe_forward(_ptr(x), _ptr(Wr), _ptr(bias), _ptr(W1), _ptr(W2), T, d, E, K, f, _ptr(out),
-                           _ptr(workspace), workspace.numel(), _stream(stream)), "moe_forward")
+    if preact is None:
+        _check(lib.moe_forward(_ptr(x), _ptr(Wr), _ptr(bias), _ptr(W1), _ptr(W2), T, d, E, K, f, _ptr(out),
+                               _ptr(workspace), workspace.numel(), _stream(stream)), "moe_forward")
+    else:
+        _need(preact, torch.bfloat16, (T * K, 2 * f), "preact")
+        _check(lib.moe_forward_train(_ptr(x), _ptr(Wr), _ptr(bias), _ptr(W1), _ptr(W2), T, d, E, K, f, _ptr(out),
+                                     _ptr(workspace), workspace.numel(), _ptr(preact), _stream(stream)),
+               "moe_forward_train")
     return out
 
 
@@ -379,17 +395,32 @@ class MoELayer:
         if n == 0:
             raise MoEError(2, "moe_forward_workspace_size")
         self.workspace = torch.empty((n,), dtype=torch.uint8, device=W1.device)
+        self._preact_buf = None
+        self.preact = None
 
-    def __call__(self, x, out=None, stream=None):
+    def __call__(self, x, out=None, stream=None, save_preact=False):
+        """y = layer(x).  ``save_preact``: also keep GEMM1's pre-activations
+        ([T*K, 2f] bf16, held by the layer) for the next backward(), which
+        then skips recomputing them."""
         if x.shape[0] > self.T_max:
             raise ValueError("more tokens than the workspace was sized for")
+        pre = None
+        if save_preact:
+            n = x.shape[0] * self.K * 2 * self.f
+            if self._preact_buf is None or self._preact_buf.numel() < n:
+                self._preact_buf = torch.empty((self.T_max * self.K * 2 * self.f,), dtype=torch.bfloat16,
+                                               device=x.device)
+            pre = self._preact_buf[:n].view(x.shape[0] * self.K, 2 * self.f)
+        self.preact = pre
         return forward(x, self.Wr, self.bias, self.W1, self.W2, self.K, out=out, workspace=self.workspace,
-                       stream=stream)
+                       stream=stream, preact=pre)
 
     def backward(self, x, dy, grads=None, workspace=None, stream=None):
         """Gradients of sum(dy * y) for the last call (same x): dict of dx
-        [T,d] bf16 and dWr, dbias, dW1, dW2 (fp32, shaped like the weights)."""
+        [T,d] bf16 and dWr, dbias, dW1, dW2 (fp32, shaped like the weights).
+        Uses the pre-activations the last call saved, if it did."""
         T, d = x.shape
+        pre = self.preact if self.preact is not None and self.preact.shape[0] == T * self.K else None
         _need(x, torch.bfloat16, (T, d), "x")
         _need(dy, torch.bfloat16, (T, d), "dy")
         n = int(lib.moe_backward_workspace_size(T, d, self.E, self.K, self.f))
@@ -404,7 +435,7 @@ class MoELayer:
                          dW1=torch.empty(self.W1.shape, **f32), dW2=torch.empty(self.W2.shape, **f32))
         _check(lib.moe_backward(_ptr(x), _ptr(self.Wr), _ptr(self.bias), _ptr(self.W1), _ptr(self.W2), T, d, self.E,
                                 self.K, self.f, _ptr(dy), _ptr(self.workspace), self.workspace.numel(),
-                                _ptr(grads["dx"]), _ptr(grads["dWr"]), _ptr(grads["dbias"]), _ptr(grads["dW1"]),
+                                _ptr(pre), _ptr(grads["dx"]), _ptr(grads["dWr"]), _ptr(grads["dbias"]), _ptr(grads["dW1"]),
                                 _ptr(grads["dW2"]), _ptr(workspace), workspace.numel(), _stream(stream)),
                "moe_backward")
         self.bw_workspace = workspace

@@ -42,6 +42,7 @@ struct Params {
     int w_rows;     // weight rows per expert (2f or d)
     int NT;         // column blocks per row block
     __nv_bfloat16 *out;  // [TK, n_out]
+    __nv_bfloat16 *preact;  // GEMM1 only, nullable: [TK, 2 n_out] gate | up pre-activations, bf16
     int *status;
     uint64_t timeout_ns;
     Combine comb;
@@ -220,9 +221,9 @@ __device__ __forceinline__ void combine_arrive(const Params &p, int n_blk, int g
 // crosses the group's end falls back to masked 16-byte stores per row.
 // `sbuf` alternates the warp's two staging buffers across chunks and tiles.
 template <bool SWIGLU>
-__device__ __forceinline__ void epilogue_tile(const Params &p, const CUtensorMap *tm_out, uint8_t *stage,
-                                              uint32_t &sbuf, uint32_t tbase, int n_blk, int wrow0, int lane,
-                                              int grp_end) {
+__device__ __forceinline__ void epilogue_tile(const Params &p, const CUtensorMap *tm_out, const CUtensorMap *tm_pre,
+                                              uint8_t *stage, uint32_t &sbuf, uint32_t tbase, int n_blk, int wrow0,
+                                              int lane, int grp_end) {
     if (wrow0 >= grp_end) return;  // whole slice outside the group (warp-uniform)
     const bool full = wrow0 + 31 < grp_end;
     const int grow = wrow0 + lane;
@@ -252,9 +253,9 @@ __device__ __forceinline__ void epilogue_tile(const Params &p, const CUtensorMap
         return;
     }
     constexpr int NCOL = SWIGLU ? BN_ACC / 2 : BN_ACC;
-    auto emit = [&](int c, const uint32_t (&packed)[16]) {
-        const int col = n_blk * NCOL + c;
-        if (col >= p.n_out) return;  // column tail (uniform)
+    // 32 columns of the warp's 32 rows into `dst` (row length ld, its tensor
+    // map `tm`) at column col
+    auto put = [&](const CUtensorMap *tm, __nv_bfloat16 *dst, int ld, int col, const uint32_t (&packed)[16]) {
         if (full) {
             uint8_t *buf = stage + sbuf * EPI_BUF;
             if (lane == 0) bulk_wait_read<1>();  // this buffer's store from two chunks ago has read it
@@ -270,13 +271,18 @@ __device__ __forceinline__ void epilogue_tile(const Params &p, const CUtensorMap
             if (lane == 0) {
                 // the output is not read again by this kernel: let L2 evict it
                 // before the operand tiles that other CTAs still share
-                tma_store_2d_evict_first(tm_out, buf, col, wrow0, l2_policy_evict_first());
+                tma_store_2d_evict_first(tm, buf, col, wrow0, l2_policy_evict_first());
                 bulk_commit();
             }
             sbuf ^= 1u;
         } else if (row_ok) {
-            store_row32(p.out + static_cast<size_t>(grow) * p.n_out + col, packed);
+            store_row32(dst + static_cast<size_t>(grow) * ld + col, packed);
         }
+    };
+    auto emit = [&](int c, const uint32_t (&packed)[16]) {
+        const int col = n_blk * NCOL + c;
+        if (col >= p.n_out) return;  // column tail (uniform)
+        put(tm_out, p.out, p.n_out, col, packed);
     };
     if (SWIGLU) {
 #pragma unroll 1
@@ -298,6 +304,18 @@ __device__ __forceinline__ void epilogue_tile(const Params &p, const CUtensorMap
                 packed[i] = pack_bf16x2(h2[0], h2[1]);
             }
             emit(c, packed);
+            const int col = n_blk * NCOL + c;
+            if (p.preact != nullptr && col < p.n_out) {
+                // the pre-activations the backward needs, rounded to bf16
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    packed[i] = pack_bf16x2(__uint_as_float(g[2 * i]), __uint_as_float(g[2 * i + 1]));
+                put(tm_pre, p.preact, 2 * p.n_out, col, packed);
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    packed[i] = pack_bf16x2(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1]));
+                put(tm_pre, p.preact, 2 * p.n_out, p.n_out + col, packed);
+            }
         }
     } else {
         // two 32-column loads per wait, so TMEM latency is paid 4 times per tile, not 8

@@ -109,7 +109,8 @@ static_assert(B_BYTES == (BN_ACC / 64) * BT_BOX && P_B_BYTES == 2 * BT_BOX, "MN-
 template <bool SWIGLU, bool BT>
 __global__ void __launch_bounds__(THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const __grid_constant__ CUtensorMap tmOut, const Params p) {
+                    const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ CUtensorMap tmPre,
+                    const Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L1::OFF_BARS);
@@ -256,7 +257,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             if (!mbar_wait(&tfull[acc], acc_phase, s_abort, p.status, p.timeout_ns)) break;
             tc_fence_after();
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN_ACC;
-            epilogue_tile<SWIGLU>(p, &tmOut, stage, sbuf, tbase, t.n_blk, t.row0 + q * 32, lane, t.grp_end);
+            epilogue_tile<SWIGLU>(p, &tmOut, &tmPre, stage, sbuf, tbase, t.n_blk, t.row0 + q * 32, lane, t.grp_end);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[acc]);
@@ -280,7 +281,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 template <bool SWIGLU, bool BT>
 __global__ void __launch_bounds__(THREADS, 1)
 grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                         const __grid_constant__ CUtensorMap tmOut, const Params p) {
+                         const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ CUtensorMap tmPre,
+                         const Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L2::OFF_BARS);
@@ -437,7 +439,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
             tc_fence_after();
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN_ACC;
             const int wrow0 = t.row0 + 128 * static_cast<int>(rank) + q * 32;
-            epilogue_tile<SWIGLU>(p, &tmOut, stage, sbuf, tbase, t.n_blk, wrow0, lane, t.grp_end);
+            epilogue_tile<SWIGLU>(p, &tmOut, &tmPre, stage, sbuf, tbase, t.n_blk, wrow0, lane, t.grp_end);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(tempty0 + 8u * acc);
@@ -465,7 +467,7 @@ namespace {
 
 template <bool SWIGLU, bool BT>
 cudaError_t launch_pair(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmOut,
-                        const gg::Params &p, int grid, cudaStream_t stream) {
+                        const CUtensorMap &tmPre, const gg::Params &p, int grid, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);
     cfg.blockDim = dim3(gg::THREADS, 1, 1);
@@ -478,7 +480,7 @@ cudaError_t launch_pair(const CUtensorMap &tmA, const CUtensorMap &tmB, const CU
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gg::grouped_gemm_pair_kernel<SWIGLU, BT>, tmA, tmB, tmOut, p);
+    return cudaLaunchKernelEx(&cfg, gg::grouped_gemm_pair_kernel<SWIGLU, BT>, tmA, tmB, tmOut, tmPre, p);
 }
 
 template <bool SWIGLU>
@@ -508,9 +510,11 @@ bool grouped_gemm_use_pair(int TK, int E) {
 
 cudaError_t launch_grouped_gemm(bool swiglu, const void *A, int TK, int Kdim, const void *W, int E, int n_out,
                                 const int32_t *offsets, void *out, const GemmLaunch &cfg, int *status,
-                                uint64_t timeout_ns, cudaStream_t stream, const CombineArgs *comb, bool b_trans) {
+                                uint64_t timeout_ns, cudaStream_t stream, const CombineArgs *comb, bool b_trans,
+                                void *preact) {
     CUtensorMap tmA, tmB;
     if (b_trans && (swiglu || comb)) return cudaErrorInvalidValue;
+    if (preact && !swiglu) return cudaErrorInvalidValue;
     const int w_rows = swiglu ? 2 * n_out : n_out;
     if (!make_tmap(&tmA, A, static_cast<uint64_t>(TK), static_cast<uint64_t>(Kdim), gg::BOX_ROWS, gg::BK))
         return cudaErrorInvalidValue;
@@ -522,10 +526,18 @@ cudaError_t launch_grouped_gemm(bool swiglu, const void *A, int TK, int Kdim, co
                           gg::BK)) {
         return cudaErrorInvalidValue;
     }
-    CUtensorMap tmOut;
+    CUtensorMap tmOut, tmPre;
     if (!make_tmap(&tmOut, out, static_cast<uint64_t>(TK), static_cast<uint64_t>(n_out), 32, 32,
                    CU_TENSOR_MAP_SWIZZLE_64B))
         return cudaErrorInvalidValue;
+    // the pre-activations [TK, 2 n_out] (GEMM1 only); otherwise an unused copy of tmOut
+    if (preact) {
+        if (!make_tmap(&tmPre, preact, static_cast<uint64_t>(TK), 2 * static_cast<uint64_t>(n_out), 32, 32,
+                       CU_TENSOR_MAP_SWIZZLE_64B))
+            return cudaErrorInvalidValue;
+    } else {
+        tmPre = tmOut;
+    }
     gg::Params p = {};
     if (comb && !swiglu) {
         p.comb.src_tok = comb->src_tok;
@@ -545,20 +557,23 @@ cudaError_t launch_grouped_gemm(bool swiglu, const void *A, int TK, int Kdim, co
     p.w_rows = w_rows;
     p.NT = swiglu ? (n_out + gg::BN_ACC / 2 - 1) / (gg::BN_ACC / 2) : (n_out + gg::BN_ACC - 1) / gg::BN_ACC;
     p.out = static_cast<__nv_bfloat16 *>(out);
+    p.preact = static_cast<__nv_bfloat16 *>(preact);
     p.status = status;
     p.timeout_ns = timeout_ns;
     const int pairs = swiglu ? cfg.pairs_swiglu : cfg.pairs_plain;
     if (grouped_gemm_use_pair(TK, E) && pairs > 0) {
-        return swiglu    ? launch_pair<true, false>(tmA, tmB, tmOut, p, 2 * pairs, stream)
-               : b_trans ? launch_pair<false, true>(tmA, tmB, tmOut, p, 2 * pairs, stream)
-                         : launch_pair<false, false>(tmA, tmB, tmOut, p, 2 * pairs, stream);
+        return swiglu    ? launch_pair<true, false>(tmA, tmB, tmOut, tmPre, p, 2 * pairs, stream)
+               : b_trans ? launch_pair<false, true>(tmA, tmB, tmOut, tmPre, p, 2 * pairs, stream)
+                         : launch_pair<false, false>(tmA, tmB, tmOut, tmPre, p, 2 * pairs, stream);
     }
+    const dim3 grid(cfg.num_sms);
     if (swiglu)
-        gg::grouped_gemm_kernel<true, false><<<cfg.num_sms, gg::THREADS, gg::SMEM_BYTES, stream>>>(tmA, tmB, tmOut, p);
+        gg::grouped_gemm_kernel<true, false><<<grid, gg::THREADS, gg::SMEM_BYTES, stream>>>(tmA, tmB, tmOut, tmPre, p);
     else if (b_trans)
-        gg::grouped_gemm_kernel<false, true><<<cfg.num_sms, gg::THREADS, gg::SMEM_BYTES, stream>>>(tmA, tmB, tmOut, p);
+        gg::grouped_gemm_kernel<false, true><<<grid, gg::THREADS, gg::SMEM_BYTES, stream>>>(tmA, tmB, tmOut, tmPre, p);
     else
-        gg::grouped_gemm_kernel<false, false><<<cfg.num_sms, gg::THREADS, gg::SMEM_BYTES, stream>>>(tmA, tmB, tmOut, p);
+        gg::grouped_gemm_kernel<false, false><<<grid, gg::THREADS, gg::SMEM_BYTES, stream>>>(tmA, tmB, tmOut, tmPre,
+                                                                                            p);
     return cudaGetLastError();
 }
 

@@ -299,7 +299,7 @@ grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
             if (SWIGLU)
                 epilogue_swiglu_mx(mp, tbase, t, q, half, lane, s_pre[t.e] / NT + t.m_blk);
             else
-                gg::epilogue_tile<false>(p, &tmOut, stage_buf, sbuf, tbase, t.n_blk, t.row0 + q * 32, lane,
+                gg::epilogue_tile<false>(p, &tmOut, nullptr, stage_buf, sbuf, tbase, t.n_blk, t.row0 + q * 32, lane,
                                          t.grp_end);
             tc_fence_before();
             __syncwarp();

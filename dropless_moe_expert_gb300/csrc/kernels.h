@@ -99,10 +99,11 @@ struct CombineArgs {
 };
 // swiglu: GEMM1 (out [TK, n_out=f], W [E, 2f, Kdim=d]); else GEMM2 (out [TK, n_out=d], W [E, d, Kdim=f]).
 // b_trans (plain only): W is [E, Kdim, n_out] and out = A . W[e] (no transpose in memory).
+// preact (GEMM1 only, nullable): also store the bf16 pre-activations [TK, 2 n_out] (gate | up).
 cudaError_t launch_grouped_gemm(bool swiglu, const void *A, int TK, int Kdim, const void *W, int E, int n_out,
                                 const int32_t *offsets, void *out, const GemmLaunch &cfg, int *status,
                                 uint64_t timeout_ns, cudaStream_t stream, const CombineArgs *comb = nullptr,
-                                bool b_trans = false);
+                                bool b_trans = false, void *preact = nullptr);
 
 // A kernel whose only wait never completes: it times out after limit_ns and
 // records MOE_ERR_DEVICE_TIMEOUT in *status.

@@ -151,7 +151,7 @@ moe_status_t check_mx_shape(int T, int d, int E, int K, int f) {
 }
 
 moe_status_t run_gemm(bool swiglu, const void *A, const int32_t *offsets, int E, int TK, int d, int f,
-                      const void *W, void *out, cudaStream_t stream) {
+                      const void *W, void *out, cudaStream_t stream, void *preact = nullptr) {
     DeviceState *ds = nullptr;
     moe_status_t st = device_state(&ds);
     if (st != MOE_OK) return st;
@@ -159,7 +159,7 @@ moe_status_t run_gemm(bool swiglu, const void *A, const int32_t *offsets, int E,
     const int n_out = swiglu ? f : d;
     g_launches.fetch_add(1, std::memory_order_relaxed);
     return cuda_status(moe::launch_grouped_gemm(swiglu, A, TK, Kdim, W, E, n_out, offsets, out, ds->gemm,
-                                                ds->status, kWaitLimitNs, stream));
+                                                ds->status, kWaitLimitNs, stream, nullptr, false, preact));
 }
 
 }  // namespace
@@ -178,7 +178,7 @@ const char *moe_status_string(int status) {
     }
 }
 
-int moe_abi_version(void) { return 201; }
+int moe_abi_version(void) { return 300; }
 
 uint64_t moe_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
@@ -243,6 +243,18 @@ moe_status_t moe_grouped_gemm1_swiglu(const uint16_t *x_perm, const int32_t *off
     moe_status_t st = check_shape(TK, d, E, 1, f, true, true);
     if (st != MOE_OK) return st;
     return run_gemm(true, x_perm, offsets, E, TK, d, f, W1, h, stream);
+}
+
+moe_status_t moe_grouped_gemm1_swiglu_preact(const uint16_t *x_perm, const int32_t *offsets, int E, int TK, int d,
+                                             int f, const uint16_t *W1, uint16_t *h, uint16_t *preact,
+                                             cudaStream_t stream) {
+    if (!x_perm || !offsets || !W1 || !h || !preact) return MOE_ERR_INVALID_ARG;
+    if (!aligned(x_perm, 16) || !aligned(W1, 16) || !aligned(h, 16) || !aligned(preact, 16) ||
+        !aligned(offsets, 4))
+        return MOE_ERR_INVALID_ARG;
+    moe_status_t st = check_shape(TK, d, E, 1, f, true, true);
+    if (st != MOE_OK) return st;
+    return run_gemm(true, x_perm, offsets, E, TK, d, f, W1, h, stream, preact);
 }
 
 moe_status_t moe_grouped_gemm2(const uint16_t *h, const int32_t *offsets, int E, int TK, int d, int f,
@@ -318,10 +330,11 @@ moe_status_t moe_forward_views(int T, int d, int E, int K, int f, moe_forward_la
     return MOE_OK;
 }
 
-moe_status_t moe_forward(const uint16_t *x, const float *Wr, const float *bias, const uint16_t *W1,
-                         const uint16_t *W2, int T, int d, int E, int K, int f, uint16_t *y, void *workspace,
-                         size_t workspace_bytes, cudaStream_t stream) {
+moe_status_t moe_forward_train(const uint16_t *x, const float *Wr, const float *bias, const uint16_t *W1,
+                               const uint16_t *W2, int T, int d, int E, int K, int f, uint16_t *y, void *workspace,
+                               size_t workspace_bytes, uint16_t *preact, cudaStream_t stream) {
     if (!x || !Wr || !W1 || !W2 || !y || !workspace) return MOE_ERR_INVALID_ARG;
+    if (preact && !aligned(preact, 16)) return MOE_ERR_INVALID_ARG;
     if (!aligned(x, 16) || !aligned(W1, 16) || !aligned(W2, 16) || !aligned(y, 16) || !aligned(workspace, 16) ||
         !aligned(Wr, 4) || (bias && !aligned(bias, 4)))
         return MOE_ERR_INVALID_ARG;
@@ -350,8 +363,19 @@ moe_status_t moe_forward(const uint16_t *x, const float *Wr, const float *bias, 
                         L.router_ws - L.route_ws, stream)) != MOE_OK)
         return st;
     if ((st = moe_permute(x, row_of, T, K, d, x_perm, stream)) != MOE_OK) return st;
-    if ((st = moe_grouped_mlp(x_perm, offsets, E, TK, d, f, W1, W2, h, y_perm, stream)) != MOE_OK) return st;
+    if (preact)
+        st = moe_grouped_gemm1_swiglu_preact(x_perm, offsets, E, TK, d, f, W1, h, preact, stream);
+    else
+        st = moe_grouped_gemm1_swiglu(x_perm, offsets, E, TK, d, f, W1, h, stream);
+    if (st != MOE_OK) return st;
+    if ((st = moe_grouped_gemm2(h, offsets, E, TK, d, f, W2, y_perm, stream)) != MOE_OK) return st;
     return moe_unpermute(y_perm, row_of, w, T, K, d, y, stream);
+}
+
+moe_status_t moe_forward(const uint16_t *x, const float *Wr, const float *bias, const uint16_t *W1,
+                         const uint16_t *W2, int T, int d, int E, int K, int f, uint16_t *y, void *workspace,
+                         size_t workspace_bytes, cudaStream_t stream) {
+    return moe_forward_train(x, Wr, bias, W1, W2, T, d, E, K, f, y, workspace, workspace_bytes, nullptr, stream);
 }
 
 moe_status_t moe_forward_host(const uint16_t *x_host, const float *Wr, const float *bias, const uint16_t *W1,
@@ -523,15 +547,15 @@ moe_status_t moe_backward_views(int T, int d, int E, int K, int f, moe_backward_
 
 moe_status_t moe_backward(const uint16_t *x, const float *Wr, const float *bias, const uint16_t *W1,
                           const uint16_t *W2, int T, int d, int E, int K, int f, const uint16_t *dy,
-                          const void *fwd_workspace, size_t fwd_workspace_bytes, uint16_t *dx, float *dWr,
-                          float *dbias, float *dW1, float *dW2, void *workspace, size_t workspace_bytes,
-                          cudaStream_t stream) {
+                          const void *fwd_workspace, size_t fwd_workspace_bytes, const uint16_t *preact,
+                          uint16_t *dx, float *dWr, float *dbias, float *dW1, float *dW2, void *workspace,
+                          size_t workspace_bytes, cudaStream_t stream) {
     (void)bias;  // the bias enters the gradients only through the routing recorded by the forward
     if (!x || !Wr || !W1 || !W2 || !dy || !fwd_workspace || !dx || !dWr || !dbias || !dW1 || !dW2 || !workspace)
         return MOE_ERR_INVALID_ARG;
     if (!aligned(x, 16) || !aligned(W1, 16) || !aligned(W2, 16) || !aligned(dy, 16) || !aligned(dx, 16) ||
         !aligned(fwd_workspace, 16) || !aligned(workspace, 16) || !aligned(Wr, 4) || !aligned(dWr, 4) ||
-        !aligned(dbias, 4) || !aligned(dW1, 16) || !aligned(dW2, 16))
+        !aligned(dbias, 4) || !aligned(dW1, 16) || !aligned(dW2, 16) || (preact && !aligned(preact, 16)))
         return MOE_ERR_INVALID_ARG;
     moe_status_t st = check_shape(T, d, E, K, f, true, true);
     if (st != MOE_OK) return st;
@@ -578,9 +602,12 @@ moe_status_t moe_backward(const uint16_t *x, const float *Wr, const float *bias,
     go(moe::launch_grouped_gemm(false, dy_perm, TK, d, W2, E, f, offsets, dh, g, ds->status, kWaitLimitNs, stream,
                                 nullptr, true),
        1);
-    // GEMM1 pre-activations again, then SwiGLU backward
-    go(moe::launch_grouped_gemm(false, x_perm, TK, d, W1, E, 2 * f, offsets, a, g, ds->status, kWaitLimitNs, stream), 1);
-    go(moe::launch_swiglu_bwd(a, dh, TK, f, da, stream), 1);
+    // GEMM1 pre-activations: as the forward saved them, else computed again; then SwiGLU backward
+    if (!preact)
+        go(moe::launch_grouped_gemm(false, x_perm, TK, d, W1, E, 2 * f, offsets, a, g, ds->status, kWaitLimitNs,
+                                    stream),
+           1);
+    go(moe::launch_swiglu_bwd(preact ? preact : a, dh, TK, f, da, stream), 1);
     // GEMM1 dgrad: dx_perm = da . W1[e]
     go(moe::launch_grouped_gemm(false, da, TK, 2 * f, W1, E, d, offsets, dx_perm, g, ds->status, kWaitLimitNs,
                                 stream, nullptr, true),

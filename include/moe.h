@@ -156,6 +156,13 @@ moe_status_t moe_grouped_gemm1_swiglu(const uint16_t *x_perm, const int32_t *off
 moe_status_t moe_grouped_gemm2(const uint16_t *h, const int32_t *offsets, int E, int TK,
                                int d, int f, const uint16_t *W2, uint16_t *y_perm,
                                cudaStream_t stream);
+/* GEMM1 that also stores the pre-activations for a backward pass:
+ * preact [TK, 2f] bf16 (caller-owned, 16-byte aligned), row r holding
+ * bf16(g) in columns 0..f-1 and bf16(u) in columns f..2f-1, rows grouped by
+ * expert like h.  One kernel launch.  */
+moe_status_t moe_grouped_gemm1_swiglu_preact(const uint16_t *x_perm, const int32_t *offsets,
+                                             int E, int TK, int d, int f, const uint16_t *W1,
+                                             uint16_t *h, uint16_t *preact, cudaStream_t stream);
 
 /* Steps a5 + a6 in one kernel (the combine fused into GEMM2's epilogue;
  * "Optimization 2": a naive dispatch/combine reads and writes the data many
@@ -194,6 +201,14 @@ moe_status_t moe_forward(const uint16_t *x, const float *Wr, const float *bias,
                          const uint16_t *W1, const uint16_t *W2, int T, int d, int E, int K,
                          int f, uint16_t *y, void *workspace, size_t workspace_bytes,
                          cudaStream_t stream);
+/* moe_forward for training: GEMM1 also stores the pre-activations into
+ * `preact` [T*K, 2f] bf16 (see moe_grouped_gemm1_swiglu_preact; nullable, then
+ * identical to moe_forward), which moe_backward then reads instead of
+ * recomputing them.  Same 9 launches.  */
+moe_status_t moe_forward_train(const uint16_t *x, const float *Wr, const float *bias,
+                               const uint16_t *W1, const uint16_t *W2, int T, int d, int E, int K,
+                               int f, uint16_t *y, void *workspace, size_t workspace_bytes,
+                               uint16_t *preact, cudaStream_t stream);
 
 /* moe_forward with the activations in HOST memory (pinned memory makes the
  * copies asynchronous): copies x_host [T, d] bf16 into the workspace,
@@ -276,12 +291,15 @@ moe_status_t moe_forward_mxfp8(const uint16_t *x, const float *Wr, const float *
  *   fp32 (every expert's entries written, zeros for experts without tokens).
  * `fwd_workspace` is the workspace of a moe_forward call on the same x and
  * weights (it holds the routing, x_perm, h and y_perm the backward reuses);
- * `workspace` holds moe_backward_workspace_size() bytes of scratch
- * (moe_backward_views() gives its regions).  The dgrad GEMMs run on the
+ * `preact` (nullable) the pre-activations a moe_forward_train call saved --
+ * when null they are computed again (one more grouped GEMM, into the
+ * workspace region `a`); `workspace` holds moe_backward_workspace_size()
+ * bytes of scratch (moe_backward_views() gives its regions).  The dgrad GEMMs run on the
  * forward's grouped GEMM reading W1 and W2 as stored (MN-major operands),
  * the weight gradients on a grouped GEMM whose reduction runs over each
  * expert's own rows, read from the grouped activations in place.  All sums
- * have a fixed order: the gradients are deterministic.  11 kernel launches.  */
+ * have a fixed order: the gradients are deterministic.  10 kernel launches
+ * (11 without `preact`).  */
 size_t moe_backward_workspace_size(int T, int d, int E, int K, int f);
 typedef struct {
     size_t dw, dl, dl_row, dy_perm, dh, a, da, dx_perm, WrT, total;
@@ -289,8 +307,9 @@ typedef struct {
 moe_status_t moe_backward_views(int T, int d, int E, int K, int f, moe_backward_layout_t *layout);
 moe_status_t moe_backward(const uint16_t *x, const float *Wr, const float *bias, const uint16_t *W1,
                           const uint16_t *W2, int T, int d, int E, int K, int f, const uint16_t *dy,
-                          const void *fwd_workspace, size_t fwd_workspace_bytes, uint16_t *dx,
-                          float *dWr, float *dbias, float *dW1, float *dW2, void *workspace,
+                          const void *fwd_workspace, size_t fwd_workspace_bytes,
+                          const uint16_t *preact, uint16_t *dx, float *dWr, float *dbias,
+                          float *dW1, float *dW2, void *workspace,
                           size_t workspace_bytes, cudaStream_t stream);
 
 /* Reads and clears the device status word of the current device (0 = OK, or

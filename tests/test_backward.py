@@ -113,13 +113,20 @@ def _case(s, seed):
     return x, w, dy
 
 
+@pytest.mark.parametrize("save", [False, True], ids=["recompute", "saved_preact"])
 @pytest.mark.parametrize("s", CASES, ids=lambda s: f"T{s.T}_d{s.d}_E{s.E}_K{s.K}_f{s.f}")
-def test_backward_matches_oracle(s):
+def test_backward_matches_oracle(s, save):
     import dropless_moe_expert_gb300 as moe
     x, w, dy = _case(s, seed=s.T + 1)
     wd = type(w)(*(t.to(DEV) for t in (w.Wr, w.bias, w.W1, w.W2)))
     xd = x.to(DEV)
     y, v, layer = run_layer(xd, wd, s.K)
+    if save:
+        # the same forward again, GEMM1 storing its pre-activations
+        layer.preact = None
+        y2 = layer(xd, save_preact=True)
+        assert layer.preact is not None
+        assert torch.equal(y2.view(torch.int16), y.view(torch.int16))
     grads = layer.backward(xd, dy.to(DEV))
     grads2 = layer.backward(xd, dy.to(DEV))
     torch.cuda.synchronize()
@@ -151,3 +158,27 @@ def test_backward_matches_oracle(s):
     for e in empty:
         assert not grads["dW1"][int(e)].any() and not grads["dW2"][int(e)].any()
     print(s, {k: f"rel {v[0]:.1e}, worst/bound {v[1]:.2f}" for k, v in report.items()})
+
+
+@pytest.mark.parametrize("s", [CASES[0], CASES[4], CASES[5]], ids=lambda s: f"T{s.T}_d{s.d}_E{s.E}_K{s.K}_f{s.f}")
+def test_saved_preact_matches_recomputed(s):
+    """GEMM1's stored pre-activations against the backward's own recompute
+    (a plain grouped GEMM over the 2f stacked rows): the same bf16 rounding
+    of fp32 sums over the same K slices, so at most one bf16 step apart;
+    every row written (the buffer starts as NaN)."""
+    import dropless_moe_expert_gb300 as moe
+    x, w, dy = _case(s, seed=s.T + 2)
+    wd = type(w)(*(t.to(DEV) for t in (w.Wr, w.bias, w.W1, w.W2)))
+    xd = x.to(DEV)
+    _, _, layer = run_layer(xd, wd, s.K)
+    layer.backward(xd, dy.to(DEV))              # recompute path: fills the region `a`
+    a = layer.backward_views(s.T)["a"].float().clone()
+    layer._preact_buf = torch.full((s.T * s.K * 2 * s.f,), float("nan"), dtype=torch.bfloat16, device=DEV)
+    layer(xd, save_preact=True)
+    torch.cuda.synchronize()
+    assert moe.device_status() == 0
+    pre = layer.preact.float()
+    assert torch.isfinite(pre).all()
+    diff = (pre - a).abs()
+    assert (diff <= 2.0 ** -7 * a.abs() + 1e-30).all()
+    print(s, f"bit-identical fraction {(pre == a).float().mean().item():.6f}")
