@@ -69,10 +69,10 @@ cudaError_t launch_router_wgrad(const uint16_t *x_perm, const float *dl_row, con
                                 int d, float *dWr, float *dbias, cudaStream_t s);
 cudaError_t launch_dx(const uint16_t *dx_perm, const float *WrT, const int32_t *row_of, const int32_t *topk_idx,
                       const float *dl, int T, int K, int E, int d, uint16_t *dx, cudaStream_t s);
-cudaError_t wgrad_setup();
+cudaError_t wgrad_setup(struct GemmLaunch *cfg);
 // D[e] [M, N] fp32 = A[group e]^T . B[group e] for rows grouped by expert, A [TK, M], B [TK, N]
 cudaError_t launch_wgrad(const uint16_t *A, const uint16_t *B, int M, int N, const int32_t *offsets, int E, int TK,
-                         float *D, int num_sms, int *status, uint64_t timeout_ns, cudaStream_t stream);
+                         float *D, const struct GemmLaunch &lc, int *status, uint64_t timeout_ns, cudaStream_t stream);
 
 // Per-device launch shape of the grouped GEMM: SM count, and how many CTA
 // pairs of the pair kernel can be resident at once (0: single-CTA only).
@@ -80,6 +80,7 @@ struct GemmLaunch {
     int num_sms = 0;
     int pairs_swiglu = 0;
     int pairs_plain = 0;
+    int wgrad_pairs = 0;  // resident CTA pairs of the weight-gradient pair kernel
 };
 // Kernel attributes and occupancy queries; once per device, before any capture.
 cudaError_t grouped_gemm_setup(int num_sms, GemmLaunch *cfg);

@@ -44,7 +44,7 @@ moe_status_t device_state(DeviceState **out) {
         if (moe::grouped_gemm_setup(s.num_sms, &s.gemm) != cudaSuccess) return MOE_ERR_CUDA;
         if (moe::router_setup() != cudaSuccess) return MOE_ERR_CUDA;
         if (moe::grouped_gemm_mx_setup() != cudaSuccess) return MOE_ERR_CUDA;
-        if (moe::wgrad_setup() != cudaSuccess) return MOE_ERR_CUDA;
+        if (moe::wgrad_setup(&s.gemm) != cudaSuccess) return MOE_ERR_CUDA;
         if (cudaGetSymbolAddress(reinterpret_cast<void **>(&s.status), g_device_status) != cudaSuccess)
             return MOE_ERR_CUDA;
         s.ready = true;
@@ -613,9 +613,8 @@ moe_status_t moe_backward(const uint16_t *x, const float *Wr, const float *bias,
                                 stream, nullptr, true),
        1);
     // weight gradients over each expert's rows: dW2[e] = dy_perm[e]^T h[e], dW1[e] = da[e]^T x_perm[e]
-    go(moe::launch_wgrad(dy_perm, h, d, f, offsets, E, TK, dW2, ds->num_sms, ds->status, kWaitLimitNs, stream), 1);
-    go(moe::launch_wgrad(da, x_perm, 2 * f, d, offsets, E, TK, dW1, ds->num_sms, ds->status, kWaitLimitNs, stream),
-       1);
+    go(moe::launch_wgrad(dy_perm, h, d, f, offsets, E, TK, dW2, g, ds->status, kWaitLimitNs, stream), 1);
+    go(moe::launch_wgrad(da, x_perm, 2 * f, d, offsets, E, TK, dW1, g, ds->status, kWaitLimitNs, stream), 1);
     // router weights and the input gradient
     go(moe::launch_router_wgrad(x_perm, dl_row, offsets, E, TK, d, dWr, dbias, stream), 1);
     go(moe::launch_dx(dx_perm, WrT, row_of, topk_idx, dl, T, K, E, d, dx, stream), 1);

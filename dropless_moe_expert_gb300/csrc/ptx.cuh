@@ -114,6 +114,10 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// The same for shared memory that a CTA pair's MMA (issued by the peer) reads.
+__device__ __forceinline__ void fence_proxy_async_smem_cluster() {
+    asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
+}
 // TMA store of one box from shared memory, tracked by the bulk-group counter.
 __device__ __forceinline__ void tma_store_2d(const void *tmap, const void *src, int c_inner, int c_outer) {
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(tmap),
@@ -157,6 +161,10 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
 }
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// 16 zero bytes at a shared::cluster address (possibly in the peer CTA).
+__device__ __forceinline__ void st_cluster_zero16(uint32_t cluster_addr) {
+    asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(cluster_addr), "r"(0u) : "memory");
 }
 // Arrive on an mbarrier given by its shared::cluster address (possibly in the peer CTA).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {

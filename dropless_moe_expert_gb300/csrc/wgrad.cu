@@ -18,11 +18,22 @@
 // block the rows past the group (the next expert's rows, or TMA zero fill
 // past TK) are zeroed in shared memory before the MMAs, so they add nothing.
 //
-// Persistent kernel, one CTA per SM: tiles (e, 128-row block, 256-column
-// block) of every expert; a 3-stage ring; tcgen05.mma M=128 N=256 K=16 into
-// two 256-column TMEM accumulators, so a tile's epilogue (fp32 by TMA stores
-// of 32 x 32 boxes) overlaps the next tile's mainloop.  Experts without rows
-// get their tiles written as zeros.  Bounded waits as in the forward GEMMs.
+// Persistent kernels, one CTA per SM, over tiles (e, row block of D, 256-column
+// block) of every expert, with two 256-column TMEM accumulators so a tile's
+// epilogue (fp32 by TMA stores of 32 x 32 boxes) overlaps the next tile's
+// mainloop.  Experts without rows get their tiles written as zeros.  Bounded
+// waits as in the forward GEMMs.
+//  * wgrad_kernel: 128-row tiles, tcgen05.mma M=128 N=256 K=16, a 3-stage
+//    ring of 48 KB.
+//  * wgrad_pair_kernel: clusters of 2 CTAs share 256-row tiles through
+//    cta_group::2 MMAs (M=256): each CTA loads 128 columns of A and 128 of B
+//    per stage (32 KB instead of 48 KB for the same MMA work per SM), 5
+//    stages.  Both CTAs' copies complete on CTA 0's full barrier; in a
+//    group's last K block CTA 0's MMA warp zeroes the tail rows in both
+//    CTAs' shared memory (the peer's through shared::cluster stores) before
+//    it issues.
+#include <algorithm>
+
 #include "kernels.h"
 #include "ptx.cuh"
 #include "tmap.h"
@@ -55,6 +66,19 @@ constexpr int BOX = 64 * 64 * 2;  // one 64-row x 64-column bf16 box
 static_assert(A_BYTES == 2 * BOX && B_BYTES == 4 * BOX, "a stage is six boxes");
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 
+// CTA-pair variant (per CTA)
+constexpr int P_STAGES = 5;
+constexpr int P_STAGE = 4 * BOX;  // 128 columns of A + 128 columns of B, 64 rows
+constexpr int P_OFF_EPI = P_STAGES * P_STAGE;
+constexpr int P_OFF_BARS = P_OFF_EPI + 4 * 2 * EPI_BUF;
+constexpr int P_NUM_BARS = 2 * P_STAGES + 5;  // full (CTA 0), empty, tfull[2], tempty[2], drain
+constexpr int P_OFF_TMEM = P_OFF_BARS + P_NUM_BARS * 8;
+constexpr int P_OFF_ABORT = P_OFF_TMEM + 4;
+constexpr int P_OFF_GOFF = P_OFF_ABORT + 4;
+constexpr int P_OFF_GCNT = P_OFF_GOFF + MAX_E * 4;
+constexpr int P_SMEM_BYTES = P_OFF_GCNT + MAX_E * 4 + 1024;
+static_assert(P_SMEM_BYTES <= 227 * 1024, "shared memory budget");
+
 struct Params {
     const int32_t *offsets;  // [E+1]
     int E, TK, M, N, MT, NT;
@@ -78,15 +102,29 @@ struct Tile {
     int e, m0, n0;
 };
 
+// Tile -> (expert, first row of D, first column of D); p.MT row blocks of RB.
+template <int RB>
 __device__ __forceinline__ Tile decode(const Params &p, int tile) {
     Tile t;
     const int per = p.MT * p.NT;
     t.e = tile / per;
     const int rem = tile - t.e * per;
     // column blocks vary fastest: neighbouring CTAs share the A rows in L2
-    t.m0 = (rem / p.NT) * BM;
+    t.m0 = (rem / p.NT) * RB;
     t.n0 = (rem % p.NT) * BN;
     return t;
+}
+
+// Zeroes rows valid..63 of `nbox` consecutive 64 x 64 boxes (one contiguous
+// byte range per box: a 128-byte row holds all its swizzled chunks); one warp.
+__device__ __forceinline__ void zero_tail(uint8_t *boxes, int nbox, int valid, int lane) {
+    const int zbytes = (BK - valid) * 128;
+#pragma unroll 1
+    for (int b = 0; b < nbox; ++b) {
+        uint8_t *z = boxes + b * BOX + valid * 128;
+        for (int o = lane * 16; o < zbytes; o += 32 * 16)
+            *reinterpret_cast<uint4 *>(z + o) = make_uint4(0u, 0u, 0u, 0u);
+    }
 }
 
 // One warp's 32 rows of a tile, 32 columns at a time: the fp32 values go to
@@ -180,7 +218,7 @@ wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
             uint32_t stage = 0, phase = 0;
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-                const Tile t = decode(p, tile);
+                const Tile t = decode<BM>(p, tile);
                 const int KB = (s_gcnt[t.e] + BK - 1) / BK;
                 const int r0 = s_goff[t.e];
                 for (int kb = 0; kb < KB; ++kb) {
@@ -212,7 +250,7 @@ wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
         uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
         bool ok = true, issued = false;
         for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-            const Tile t = decode(p, tile);
+            const Tile t = decode<BM>(p, tile);
             const int cnt = s_gcnt[t.e];
             const int KB = (cnt + BK - 1) / BK;
             int w = 1;
@@ -227,15 +265,7 @@ wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
                 uint8_t *sa = smem + stage * STAGE;
                 const int valid = cnt - kb * BK;  // warp-uniform
                 if (valid < BK) {
-                    // rows valid..63 of each of the six boxes: one contiguous
-                    // byte range per box (a 128-byte row holds all its swizzled chunks)
-                    const int zbytes = (BK - valid) * 128;
-#pragma unroll 1
-                    for (int b = 0; b < 6; ++b) {
-                        uint8_t *z = sa + b * BOX + valid * 128;
-                        for (int o = lane * 16; o < zbytes; o += 32 * 16)
-                            *reinterpret_cast<uint4 *>(z + o) = make_uint4(0u, 0u, 0u, 0u);
-                    }
+                    zero_tail(sa, 6, valid, lane);
                     fence_proxy_async_smem();
                     __syncwarp();
                 }
@@ -269,7 +299,7 @@ wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
         uint32_t sbuf = 0;
         uint32_t acc = 0, acc_phase = 0;
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-            const Tile t = decode(p, tile);
+            const Tile t = decode<BM>(p, tile);
             if (!mbar_wait(&tfull[acc], acc_phase, s_abort, p.status, p.timeout_ns)) break;
             tc_fence_after();
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
@@ -291,14 +321,242 @@ wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
     }
 }
 
+// ======================================================================
+// CTA-pair variant (cluster of 2): 256-row tiles, CTA r owns rows
+// m0 + 128 r .. m0 + 128 r + 127 of D and supplies columns n0 + 128 r ..
+// n0 + 128 r + 127 of B; CTA 0 issues the cta_group::2 MMAs.
+// ======================================================================
+__global__ void __launch_bounds__(THREADS, 1)
+wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                  const __grid_constant__ CUtensorMap tmD, const Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + P_OFF_BARS);
+    uint64_t *full = bars;                  // CTA 0: both CTAs' bytes
+    uint64_t *empty = bars + P_STAGES;      // both CTAs: freed by CTA 0's MMA commits
+    uint64_t *tfull = bars + 2 * P_STAGES;  // both CTAs
+    uint64_t *tempty = tfull + 2;           // CTA 0: 4 epilogue warps x 2 CTAs
+    uint64_t *drain = tfull + 4;
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(smem + P_OFF_TMEM);
+    volatile int *s_abort = reinterpret_cast<volatile int *>(smem + P_OFF_ABORT);
+    int *s_goff = reinterpret_cast<int *>(smem + P_OFF_GOFF);
+    int *s_gcnt = reinterpret_cast<int *>(smem + P_OFF_GCNT);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const int pair = blockIdx.x >> 1;
+    const int npairs = gridDim.x >> 1;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < P_STAGES; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&tfull[i], 1);
+            mbar_init(&tempty[i], 8);
+        }
+        mbar_init(drain, 1);
+        *s_abort = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 2) groups(p, lane, s_goff, s_gcnt);
+    __syncthreads();
+    // both CTAs' barriers exist before anything crosses the pair, and before
+    // the collective TMEM allocation
+    cluster_sync();
+    if (warp == 1) {
+        tmem_alloc_pair(s_tmem, TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *s_tmem;
+    const int total = p.E * p.MT * p.NT;
+    const int half = static_cast<int>(rank) * 128;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // both CTAs' copies signal CTA 0's full barriers
+            const uint32_t full0 = mapa_shared(smem_u32(&full[0]), 0);
+            int armed_phase[P_STAGES];
+#pragma unroll
+            for (int i = 0; i < P_STAGES; ++i) armed_phase[i] = -1;
+            uint32_t stage = 0, phase = 0;
+            bool ok = true;
+            for (int tile = pair; ok && tile < total; tile += npairs) {
+                const Tile t = decode<2 * BM>(p, tile);
+                const int KB = (s_gcnt[t.e] + BK - 1) / BK;
+                const int r0 = s_goff[t.e];
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!mbar_wait<true>(&empty[stage], phase ^ 1u, s_abort, p.status, p.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *sa = smem + stage * P_STAGE;
+                    const int row = r0 + kb * BK;
+                    const uint32_t bar = full0 + 8u * stage;
+                    if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * P_STAGE);
+                    // columns past M or N read TMA zero fill
+                    tma_load_2d_pair(sa, &tmA, bar, t.m0 + half, row);
+                    tma_load_2d_pair(sa + BOX, &tmA, bar, t.m0 + half + 64, row);
+                    tma_load_2d_pair(sa + 2 * BOX, &tmB, bar, t.n0 + half, row);
+                    tma_load_2d_pair(sa + 3 * BOX, &tmB, bar, t.n0 + half + 64, row);
+                    armed_phase[stage] = static_cast<int>(phase);
+                    if (++stage == P_STAGES) { stage = 0; phase ^= 1u; }
+                }
+            }
+            if (!ok) {
+                volatile int no_abort = 0;
+                if (rank == 0) {
+                    for (int i = 0; i < P_STAGES; ++i)
+                        if (armed_phase[i] >= 0)
+                            mbar_wait<true>(&full[i], static_cast<uint32_t>(armed_phase[i]), &no_abort, p.status,
+                                            p.timeout_ns);
+                } else {
+                    // this CTA's copies signal CTA 0's barriers: give them time to land
+                    const uint64_t t0 = global_timer_ns();
+                    while (global_timer_ns() - t0 < 200000ull) __nanosleep(1000);
+                }
+            }
+        }
+    } else if (warp == 1 && rank == 0) {
+        // Waits for both CTAs' bytes, zeroes the rows past a group in its last
+        // K block (in both CTAs), issues the MMAs.  The whole warp takes part.
+        constexpr uint32_t idesc = idesc_bf16_f32(2 * BM, BN, true, true);
+        const uint32_t peer_base = mapa_shared(smem_u32(smem), 1);
+        uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+        bool ok = true, issued = false;
+        for (int tile = pair; ok && tile < total; tile += npairs) {
+            const Tile t = decode<2 * BM>(p, tile);
+            const int cnt = s_gcnt[t.e];
+            const int KB = (cnt + BK - 1) / BK;
+            int w = 1;
+            if (lane == 0) w = mbar_wait<true>(&tempty[acc], acc_phase ^ 1u, s_abort, p.status, p.timeout_ns);
+            if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + acc * BN;
+            for (int kb = 0; kb < KB; ++kb) {
+                if (lane == 0) w = mbar_wait<true>(&full[stage], phase, s_abort, p.status, p.timeout_ns);
+                if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
+                tc_fence_after();
+                uint8_t *sa = smem + stage * P_STAGE;
+                const int valid = cnt - kb * BK;  // warp-uniform
+                if (valid < BK) {
+                    zero_tail(sa, 4, valid, lane);
+                    // the same rows of the peer's four boxes
+                    const int zbytes = (BK - valid) * 128;
+                    const uint32_t peer = peer_base + static_cast<uint32_t>(stage * P_STAGE + valid * 128);
+#pragma unroll 1
+                    for (int b = 0; b < 4; ++b)
+                        for (int o = lane * 16; o < zbytes; o += 32 * 16)
+                            st_cluster_zero16(peer + static_cast<uint32_t>(b * BOX + o));
+                    fence_proxy_async_smem_cluster();
+                    __syncwarp();
+                }
+                if (lane == 0) {
+                    const uint32_t a_addr = smem_u32(sa);
+                    const uint64_t adesc = smem_desc_mnmajor_sw128(a_addr, BOX);
+                    const uint64_t bdesc = smem_desc_mnmajor_sw128(a_addr + 2 * BOX, BOX);
+#pragma unroll
+                    for (int j = 0; j < BK / UMMA_K; ++j)
+                        umma_bf16_pair(d_tmem, adesc + 128 * j, bdesc + 128 * j, idesc, (kb | j) != 0);
+                    umma_commit_pair_multicast(&empty[stage], 0x3);
+                }
+                issued = true;
+                __syncwarp();
+                if (++stage == P_STAGES) { stage = 0; phase ^= 1u; }
+            }
+            if (!ok) break;
+            if (lane == 0) umma_commit_pair_multicast(&tfull[acc], 0x3);
+            __syncwarp();
+            acc ^= 1u;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+        if (!ok && issued && lane == 0) {
+            volatile int no_abort = 0;
+            umma_commit_pair_multicast(drain, 0x1);
+            mbar_wait<true>(drain, 0, &no_abort, p.status, p.timeout_ns);
+        }
+    } else if (warp == 1) {
+        // CTA 1's MMA warp has no role after the allocation
+    } else {
+        const int q = warp & 3;
+        uint8_t *stage = smem + P_OFF_EPI + (warp - 2) * 2 * EPI_BUF;
+        uint32_t sbuf = 0;
+        const uint32_t tempty0 = mapa_shared(smem_u32(&tempty[0]), 0);
+        uint32_t acc = 0, acc_phase = 0;
+        for (int tile = pair; tile < total; tile += npairs) {
+            Tile t = decode<2 * BM>(p, tile);
+            if (!mbar_wait<true>(&tfull[acc], acc_phase, s_abort, p.status, p.timeout_ns)) break;
+            tc_fence_after();
+            const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+            t.m0 += half;  // this CTA's 128 rows of the tile
+            epilogue(p, &tmD, t, tbase, q, lane, s_gcnt[t.e] == 0, stage, sbuf);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(tempty0 + 8u * acc);
+            acc ^= 1u;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+        if (lane == 0) bulk_wait_all();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    // neither CTA leaves (or frees TMEM) while its peer may still touch its
+    // shared memory or tensor memory
+    cluster_sync();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    }
+}
+
 }  // namespace wg
 
-cudaError_t wgrad_setup() {
-    return cudaFuncSetAttribute(wg::wgrad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, wg::SMEM_BYTES);
+namespace {
+
+cudaLaunchConfig_t pair_config(int grid, cudaStream_t stream, cudaLaunchAttribute *attr) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(wg::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = wg::P_SMEM_BYTES;
+    cfg.stream = stream;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cfg;
+}
+
+}  // namespace
+
+cudaError_t wgrad_setup(GemmLaunch *cfg) {
+    cudaError_t e;
+    if ((e = cudaFuncSetAttribute(wg::wgrad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, wg::SMEM_BYTES)) !=
+        cudaSuccess)
+        return e;
+    if ((e = cudaFuncSetAttribute(wg::wgrad_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  wg::P_SMEM_BYTES)) != cudaSuccess)
+        return e;
+    // every pair of the persistent kernel must be resident at once
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t lc = pair_config(2, nullptr, attr);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, wg::wgrad_pair_kernel, &lc) != cudaSuccess) n = 0;
+    cudaGetLastError();  // a failed query leaves 0 pairs: single-CTA kernel only
+    cfg->wgrad_pairs = std::min(n, cfg->num_sms / 2);
+    return cudaSuccess;
 }
 
 cudaError_t launch_wgrad(const uint16_t *A, const uint16_t *B, int M, int N, const int32_t *offsets, int E, int TK,
-                         float *D, int num_sms, int *status, uint64_t timeout_ns, cudaStream_t stream) {
+                         float *D, const GemmLaunch &lc, int *status, uint64_t timeout_ns, cudaStream_t stream) {
     CUtensorMap tmA, tmB, tmD;
     if (M % 64 != 0 || N % 64 != 0 || TK < 1) return cudaErrorInvalidValue;
     // A [TK, M] and B [TK, N] with 64-row x 64-column boxes
@@ -314,12 +572,23 @@ cudaError_t launch_wgrad(const uint16_t *A, const uint16_t *B, int M, int N, con
     p.TK = TK;
     p.M = M;
     p.N = N;
-    p.MT = (M + wg::BM - 1) / wg::BM;
+    // CTA pairs for D blocks of 256 rows, when D has that many and the
+    // groups are long (the forward GEMMs' rule): with short groups most K
+    // blocks are a group's last, and zeroing the tail in both CTAs costs more
+    // than the pair saves (measured on groups of 128 rows on average)
+    const bool use_pair = lc.wgrad_pairs > 0 && M >= 2 * wg::BM && grouped_gemm_use_pair(TK, E);
+    const int rb = use_pair ? 2 * wg::BM : wg::BM;
+    p.MT = (M + rb - 1) / rb;
     p.NT = (N + wg::BN - 1) / wg::BN;
     p.D = D;
     p.status = status;
     p.timeout_ns = timeout_ns;
-    wg::wgrad_kernel<<<num_sms, wg::THREADS, wg::SMEM_BYTES, stream>>>(tmA, tmB, tmD, p);
+    if (use_pair) {
+        cudaLaunchAttribute attr[1];
+        cudaLaunchConfig_t cfg = pair_config(2 * lc.wgrad_pairs, stream, attr);
+        return cudaLaunchKernelEx(&cfg, wg::wgrad_pair_kernel, tmA, tmB, tmD, p);
+    }
+    wg::wgrad_kernel<<<lc.num_sms, wg::THREADS, wg::SMEM_BYTES, stream>>>(tmA, tmB, tmD, p);
     return cudaGetLastError();
 }
 

@@ -32,8 +32,12 @@ CASES = [
     Shape(T=1000, d=192, E=8, K=1, f=320),
     Shape(T=517, d=320, E=16, K=4, f=448, bias="normal_0.5"),
     Shape(T=129, d=128, E=256, K=8, f=64),
-    Shape(T=2048, d=256, E=4, K=2, f=256),       # CTA-pair dgrad GEMMs, long groups
+    Shape(T=2048, d=256, E=4, K=2, f=256),       # CTA-pair dgrad and weight-gradient GEMMs, long groups
     Shape(T=600, d=128, E=8, K=2, f=192, bias="skew"),
+    # long groups: CTA-pair weight gradients, with partial 256-row blocks of D
+    # (d = 320, 2f = 384) and partial 256-column blocks
+    Shape(T=1500, d=320, E=2, K=1, f=192),
+    Shape(T=3000, d=128, E=4, K=2, f=384, bias="skew"),
 ]
 
 
