@@ -136,53 +136,134 @@ swiglu_bwd_kernel(const uint4 *__restrict__ a, const uint4 *__restrict__ dh, int
     }
 }
 
-// dWr[:, e] and dbias[e]: sums over expert e's rows.  One block per (expert,
-// 256-column chunk): lane l of warp w owns 8 columns and the rows
-// w, w + 8, w + 16, ... of the group; the 8 warps' partial sums are then
-// added in warp order.  The order of every addition is fixed: deterministic.
+// dWr[:, e] and dbias[e]: sums over expert e's rows, in two passes so that
+// a heavy expert's rows spread over many blocks.  Each expert's rows are cut
+// into slices of RW_SLICE rows (slice w of all experts in order: the prefix
+// s_pre over experts of ceil(count / RW_SLICE)); pass 1 sums one slice per
+// block into part[w], pass 2 adds an expert's slices in slice order.  Every
+// addition has a fixed order: deterministic.
+constexpr int RW_SLICE = 256;
+constexpr int RW_MAX_E = 256;
+
+// Group starts, counts (clamped to [0, TK]) and the slice prefix; one warp.
+__device__ __forceinline__ void slice_prefix(const int32_t *offsets, int E, int TK, int lane, int *s_off, int *s_cnt,
+                                             int *s_pre) {
+    int carry = 0;
+    for (int base = 0; base < E; base += 32) {
+        const int e = base + lane;
+        int v = 0;
+        if (e < E) {
+            const int o0 = min(max(offsets[e], 0), TK);
+            const int o1 = min(max(offsets[e + 1], o0), TK);
+            s_off[e] = o0;
+            s_cnt[e] = o1 - o0;
+            v = (o1 - o0 + RW_SLICE - 1) / RW_SLICE;
+        }
+        int incl = v;
+#pragma unroll
+        for (int sh = 1; sh < 32; sh <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, incl, sh);
+            if (lane >= sh) incl += n;
+        }
+        if (e < E) s_pre[e] = carry + incl - v;
+        carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) s_pre[E] = carry;
+}
+
+// Pass 1: block (column chunk of 256, slice w).  Lane l of warp q owns 8
+// columns and the slice's rows q, q + 8, q + 16, ... (four loads in flight);
+// the 8 warps' sums are added in warp order into part[w][cols]; the chunk-0
+// block also writes the slice's sum of dl into bpart[w].
 __global__ void __launch_bounds__(256)
-router_wgrad_kernel(const uint4 *__restrict__ x_perm, const float *__restrict__ dl_row,
-                    const int32_t *__restrict__ offsets, int E, int TK, int d, float *__restrict__ dWr,
-                    float *__restrict__ dbias) {
-    __shared__ float part[8][256 + 1];
-    __shared__ float bpart[8];
-    const int e = blockIdx.y;
+router_wgrad_partial_kernel(const uint4 *__restrict__ x_perm, const float *__restrict__ dl_row,
+                            const int32_t *__restrict__ offsets, int E, int TK, int d, float *__restrict__ part,
+                            float *__restrict__ bpart) {
+    __shared__ int s_off[RW_MAX_E], s_cnt[RW_MAX_E], s_pre[RW_MAX_E + 1];
+    __shared__ float red[8][256 + 1];
+    __shared__ float bred[8];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp == 0) slice_prefix(offsets, E, TK, lane, s_off, s_cnt, s_pre);
+    __syncthreads();
+    const int w = blockIdx.y;
+    if (w >= s_pre[E]) return;  // block-uniform
+    int lo = 0, hi = E - 1;     // the expert whose slices hold w
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_pre[mid] <= w) lo = mid; else hi = mid - 1;
+    }
+    const int e = lo;
+    const int r0 = s_off[e] + (w - s_pre[e]) * RW_SLICE;
+    const int r1 = min(r0 + RW_SLICE, s_off[e] + s_cnt[e]);
     const int nvec = d / 8;
     const int v = blockIdx.x * 32 + lane;  // 8-column vector index
-    const int o0 = min(max(offsets[e], 0), TK);
-    const int o1 = min(max(offsets[e + 1], o0), TK);
+    const bool col_ok = v < nvec;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     float bsum = 0.0f;
-    for (int r = o0 + warp; r < o1; r += 8) {
-        const float g = dl_row[r];
-        bsum += g;
-        if (v < nvec) {
-            float xv[8];
-            unpack8(__ldg(x_perm + static_cast<size_t>(r) * nvec + v), xv);
+    for (int r = r0 + warp; r < r1; r += 32) {
+        uint4 xr[4];
+        float g[4];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) acc[i] = __fmaf_rn(g, xv[i], acc[i]);
+        for (int j = 0; j < 4; ++j) {
+            const int rr = r + 8 * j;
+            const bool ok = rr < r1;
+            g[j] = ok ? dl_row[rr] : 0.0f;
+            xr[j] = (ok && col_ok) ? __ldg(x_perm + static_cast<size_t>(rr) * nvec + v) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (r + 8 * j >= r1) break;
+            bsum += g[j];
+            float xv[8];
+            unpack8(xr[j], xv);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i] = __fmaf_rn(g[j], xv[i], acc[i]);
         }
     }
 #pragma unroll
-    for (int i = 0; i < 8; ++i) part[warp][lane * 8 + i] = acc[i];
-    if (lane == 0) bpart[warp] = bsum;
+    for (int i = 0; i < 8; ++i) red[warp][lane * 8 + i] = acc[i];
+    if (lane == 0) bred[warp] = bsum;
     __syncthreads();
-    // warp 0 adds the 8 partial sums in warp order and writes
     if (warp == 0) {
-        if (v < nvec) {
+        if (col_ok) {
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 float t = 0.0f;
-                for (int w = 0; w < 8; ++w) t += part[w][lane * 8 + i];
-                dWr[static_cast<size_t>(v * 8 + i) * E + e] = t;
+                for (int q = 0; q < 8; ++q) t += red[q][lane * 8 + i];
+                part[static_cast<size_t>(w) * d + v * 8 + i] = t;
             }
         }
         if (blockIdx.x == 0 && lane == 0) {
             float t = 0.0f;
-            for (int w = 0; w < 8; ++w) t += bpart[w];
-            dbias[e] = t;
+            for (int q = 0; q < 8; ++q) t += bred[q];
+            bpart[w] = t;
         }
+    }
+}
+
+// Pass 2: block (column chunk of 256, expert e): dWr[col, e] = the expert's
+// slices' partial sums added in slice order (0 for an expert without rows).
+__global__ void __launch_bounds__(256)
+router_wgrad_reduce_kernel(const float *__restrict__ part, const float *__restrict__ bpart,
+                           const int32_t *__restrict__ offsets, int E, int TK, int d, int W, float *__restrict__ dWr,
+                           float *__restrict__ dbias) {
+    __shared__ int s_off[RW_MAX_E], s_cnt[RW_MAX_E], s_pre[RW_MAX_E + 1];
+    if (threadIdx.x < 32) slice_prefix(offsets, E, TK, threadIdx.x, s_off, s_cnt, s_pre);
+    __syncthreads();
+    const int e = blockIdx.y;
+    // (clamped to the W slices pass 1 had: offsets that are not monotone
+    // cannot send a read past `part`)
+    const int w0 = min(s_pre[e], W), w1 = min(s_pre[e + 1], W);
+    const int col = blockIdx.x * 256 + threadIdx.x;
+    if (col < d) {
+        float t = 0.0f;
+        for (int w = w0; w < w1; ++w) t += part[static_cast<size_t>(w) * d + col];
+        dWr[static_cast<size_t>(col) * E + e] = t;
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        float t = 0.0f;
+        for (int w = w0; w < w1; ++w) t += bpart[w];
+        dbias[e] = t;
     }
 }
 
@@ -254,11 +335,24 @@ cudaError_t launch_swiglu_bwd(const uint16_t *a, const uint16_t *dh, int TK, int
     return cudaGetLastError();
 }
 
+size_t router_wgrad_slices(int TK, int E) {
+    return (static_cast<size_t>(TK) + bw::RW_SLICE - 1) / bw::RW_SLICE + static_cast<size_t>(E);
+}
+
 cudaError_t launch_router_wgrad(const uint16_t *x_perm, const float *dl_row, const int32_t *offsets, int E, int TK,
-                                int d, float *dWr, float *dbias, cudaStream_t s) {
-    dim3 grid((d / 8 + 31) / 32, E);
-    bw::router_wgrad_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4 *>(x_perm), dl_row, offsets, E, TK, d,
-                                                dWr, dbias);
+                                int d, float *part, float *dWr, float *dbias, cudaStream_t s) {
+    if (E > bw::RW_MAX_E) return cudaErrorInvalidValue;
+    const int chunks = (d / 8 + 31) / 32;
+    const size_t Ws = router_wgrad_slices(TK, E);  // at least the slices of all experts
+    if (Ws > 65535) return cudaErrorInvalidValue;   // grid.y
+    const int W = static_cast<int>(Ws);
+    float *bpart = part + static_cast<size_t>(W) * d;
+    bw::router_wgrad_partial_kernel<<<dim3(chunks, W), 256, 0, s>>>(reinterpret_cast<const uint4 *>(x_perm), dl_row,
+                                                                   offsets, E, TK, d, part, bpart);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    bw::router_wgrad_reduce_kernel<<<dim3((d + 255) / 256, E), 256, 0, s>>>(part, bpart, offsets, E, TK, d, W, dWr,
+                                                                           dbias);
     return cudaGetLastError();
 }
 

@@ -65,8 +65,10 @@ cudaError_t launch_combine_bwd(const uint16_t *dy, const uint16_t *y_perm, const
 cudaError_t launch_router_bwd(const float *topk_w, const float *dw, const int32_t *row_of, int T, int K, float *dl,
                               float *dl_row, cudaStream_t s);
 cudaError_t launch_swiglu_bwd(const uint16_t *a, const uint16_t *dh, int TK, int f, uint16_t *da, cudaStream_t s);
+// scratch `part` holds router_wgrad_slices(TK, E) * (d + 1) floats; two launches
+size_t router_wgrad_slices(int TK, int E);
 cudaError_t launch_router_wgrad(const uint16_t *x_perm, const float *dl_row, const int32_t *offsets, int E, int TK,
-                                int d, float *dWr, float *dbias, cudaStream_t s);
+                                int d, float *part, float *dWr, float *dbias, cudaStream_t s);
 cudaError_t launch_dx(const uint16_t *dx_perm, const float *WrT, const int32_t *row_of, const int32_t *topk_idx,
                       const float *dl, int T, int K, int E, int d, uint16_t *dx, cudaStream_t s);
 cudaError_t wgrad_setup(struct GemmLaunch *cfg);
