@@ -377,36 +377,41 @@ def run_gpu(args):
     value = aggregate(flops_step, ws, args.steps, elapsed_ms) / 1e12
     tokens_s = aggregate(T, ws, args.steps, elapsed_ms)
 
-    # ---- end to end through the public API with host buffers (pinned): the
-    # host->device copy of x and the device->host copy of y inside the timed region
-    x_host = x.cpu().pin_memory()
-    y_host = torch.empty((T, d), dtype=torch.bfloat16, pin_memory=True)
+    # ---- end to end through the public API with host buffers (pinned): every
+    # batch's host->device copy of x and device->host copy of y run inside
+    # the timed region, on the library's copy streams, overlapped with the
+    # compute of the neighbouring batches (moe_forward_host_pipelined).  Two
+    # host input and two host output buffers are cycled over the K batches.
+    x_hosts_buf = [x.cpu().pin_memory(),
+                   make_tokens(s, seed=replica_seed(rank) + 1, device="cpu").pin_memory()]
+    y_hosts_buf = [torch.empty((T, d), dtype=torch.bfloat16, pin_memory=True) for _ in range(2)]
     if mxfp8:
         del x_perm, h, sfa, sfh
-        nbytes = int(L.moe_forward_mxfp8_workspace_size(T, d, E, K, f))
-        ws_mx = torch.empty((nbytes,), dtype=torch.uint8, device=dev)
-        x_dev = torch.empty_like(x)
+        nbytes = int(L.moe_forward_mxfp8_host_pipelined_workspace_size(T, d, E, K, f))
+        ws_pipe = torch.empty((nbytes,), dtype=torch.uint8, device=dev)
 
-        def e2e_step():
-            x_dev.copy_(x_host, non_blocking=True)
-            moe.forward_mxfp8(x_dev, w.Wr, w.bias, W1q, W1s, W2q, W2s, K, out=y, workspace=ws_mx)
-            y_host.copy_(y, non_blocking=True)
+        def e2e_run(n):
+            moe.forward_mxfp8_host_pipelined([x_hosts_buf[i % 2] for i in range(n)],
+                                             [y_hosts_buf[i % 2] for i in range(n)], w.Wr, w.bias, W1q, W1s, W2q,
+                                             W2s, K, workspace=ws_pipe)
     else:
-        layer = moe.MoELayer(w.Wr, w.bias, w.W1, w.W2, K, T)
+        nbytes = int(L.moe_forward_host_pipelined_workspace_size(T, d, E, K, f))
+        ws_pipe = torch.empty((nbytes,), dtype=torch.uint8, device=dev)
 
-        def e2e_step():
-            moe.forward_host(x_host, w.Wr, w.bias, w.W1, w.W2, K, y_host=y_host, workspace=layer.workspace)
-    for _ in range(max(1, args.warmup)):
-        e2e_step()
+        def e2e_run(n):
+            moe.forward_host_pipelined([x_hosts_buf[i % 2] for i in range(n)],
+                                       [y_hosts_buf[i % 2] for i in range(n)], w.Wr, w.bias, w.W1, w.W2, K,
+                                       workspace=ws_pipe)
+    e2e_run(max(3, args.warmup))
     torch.cuda.synchronize()
     _barrier(ws)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
+    e2e_run(args.steps)
     e1.record(stream)
     torch.cuda.synchronize()
+    assert moe.device_status() == 0
     e2e_ms = _max_over_ranks(e0.elapsed_time(e1), ws)
     e2e_value = aggregate(flops_step, ws, args.steps, e2e_ms) / 1e12
 
@@ -467,7 +472,9 @@ def run_gpu(args):
                 "once before the timed region" if mxfp8 else "bf16, fp32 accumulate")),
             "tokens_per_s": tokens_s, "kernels": kernels, "roofline": roofline, "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": T * d * 2,
-                    "d2h_bytes_per_step": T * d * 2, "ms_per_step": e2e_ms / args.steps},
+                    "d2h_bytes_per_step": T * d * 2, "ms_per_step": e2e_ms / args.steps,
+                    "copies": "every batch's copies inside the timed region, overlapped with the neighbouring "
+                              "batches' compute (moe_forward_host_pipelined)"},
             "gpu_launches": launches, "clocks": clocks,
             "routing": {"empty_experts": int((counts == 0).sum().item()), "max_group": int(counts.max().item())},
         }

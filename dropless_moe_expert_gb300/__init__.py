@@ -83,6 +83,10 @@ def _load():
         "moe_forward_views": (I, [I, I, I, I, I, ctypes.POINTER(_Layout)]),
         "moe_forward": (I, [P, P, P, P, P, I, I, I, I, I, P, P, S, P]),
         "moe_forward_train": (I, [P, P, P, P, P, I, I, I, I, I, P, P, S, P, P]),
+        "moe_forward_host_pipelined_workspace_size": (S, [I, I, I, I, I]),
+        "moe_forward_host_pipelined": (I, [P, P, I, P, P, P, P, I, I, I, I, I, P, S, P]),
+        "moe_forward_mxfp8_host_pipelined_workspace_size": (S, [I, I, I, I, I]),
+        "moe_forward_mxfp8_host_pipelined": (I, [P, P, I, P, P, P, P, P, P, I, I, I, I, I, P, S, P]),
         "moe_forward_host": (I, [P, P, P, P, P, I, I, I, I, I, P, P, S, P]),
         "moe_mxfp8_scales_size": (S, [I, I]),
         "moe_mxfp8_quantize": (I, [P, I, I, P, P, P]),
@@ -362,6 +366,56 @@ def forward_host(x_host, Wr, bias, W1, W2, K: int, y_host=None, workspace=None, 
                                 _ptr(y_host), _ptr(workspace), workspace.numel(), _stream(stream)),
            "moe_forward_host")
     return y_host
+
+
+def _host_batches(x_hosts, y_hosts, T, d):
+    """Pointer arrays of the host batches (checked: contiguous CPU bf16 [T, d])."""
+    if len(x_hosts) != len(y_hosts) or not x_hosts:
+        raise ValueError("x_hosts and y_hosts must be non-empty and of equal length")
+    for t in list(x_hosts) + list(y_hosts):
+        if t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous() or tuple(t.shape) != (T, d):
+            raise ValueError("host batches must be contiguous CPU bf16 [T, d] tensors")
+    xp = (ctypes.c_void_p * len(x_hosts))(*[t.data_ptr() for t in x_hosts])
+    yp = (ctypes.c_void_p * len(y_hosts))(*[t.data_ptr() for t in y_hosts])
+    return xp, yp
+
+
+def forward_host_pipelined(x_hosts, y_hosts, Wr, bias, W1, W2, K: int, workspace=None, stream=None):
+    """The layer over a list of host batches (pinned [T,d] bf16 CPU tensors;
+    entries may repeat), y_hosts[i] written from x_hosts[i]; host<->device
+    copies overlap the compute of neighbouring batches.  Synchronize the
+    stream before reading y_hosts."""
+    T, d = x_hosts[0].shape
+    _, _, E, f = _weights_check(x_hosts[0], Wr, bias, W1, W2, K)
+    xp, yp = _host_batches(x_hosts, y_hosts, T, d)
+    nbytes = int(lib.moe_forward_host_pipelined_workspace_size(T, d, E, K, f))
+    if nbytes == 0:
+        raise MoEError(2, "moe_forward_host_pipelined_workspace_size")
+    if workspace is None:
+        workspace = torch.empty((nbytes,), dtype=torch.uint8, device=W1.device)
+    _check(lib.moe_forward_host_pipelined(xp, yp, len(x_hosts), _ptr(Wr), _ptr(bias), _ptr(W1), _ptr(W2), T, d, E,
+                                          K, f, _ptr(workspace), workspace.numel(), _stream(stream)),
+           "moe_forward_host_pipelined")
+    return y_hosts
+
+
+def forward_mxfp8_host_pipelined(x_hosts, y_hosts, Wr, bias, W1q, W1s, W2q, W2s, K: int, workspace=None,
+                                 stream=None):
+    """forward_host_pipelined with the MXFP8 expert matmuls (weights quantised)."""
+    T, d = x_hosts[0].shape
+    E, two_f, _ = W1q.shape
+    f = two_f // 2
+    xp, yp = _host_batches(x_hosts, y_hosts, T, d)
+    nbytes = int(lib.moe_forward_mxfp8_host_pipelined_workspace_size(T, d, E, K, f))
+    if nbytes == 0:
+        raise MoEError(2, "moe_forward_mxfp8_host_pipelined_workspace_size")
+    if workspace is None:
+        workspace = torch.empty((nbytes,), dtype=torch.uint8, device=W1q.device)
+    _check(lib.moe_forward_mxfp8_host_pipelined(xp, yp, len(x_hosts), _ptr(Wr), _ptr(bias), _ptr(W1q), _ptr(W1s),
+                                                _ptr(W2q), _ptr(W2s), T, d, E, K, f, _ptr(workspace),
+                                                workspace.numel(), _stream(stream)),
+           "moe_forward_mxfp8_host_pipelined")
+    return y_hosts
 
 
 def device_status() -> int:

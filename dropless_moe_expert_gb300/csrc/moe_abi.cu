@@ -163,6 +163,53 @@ moe_status_t run_gemm(bool swiglu, const void *A, const int32_t *offsets, int E,
                                                 ds->status, kWaitLimitNs, stream, nullptr, false, preact));
 }
 
+// Runs n batches through `compute(x_dev, y_dev)` on `stream` with
+// double-buffered device copies: batch i's host->device copy (copy stream
+// `cin`) and batch i-1's device->host copy (copy stream `cout`) overlap
+// batch i-1's and batch i's compute.  Buffer b = i % 2 is refilled only after
+// the compute of batch i-2 that read it, and recomputed only after the copy
+// out of batch i-2 that read it.  `stream` ends waiting for the last copy out,
+// so its completion means every y_hosts[i] is written.  The copy streams and
+// events belong to the call (destroyed once their work is done).
+template <typename F>
+moe_status_t run_pipelined(const uint16_t *const *x_hosts, uint16_t *const *y_hosts, int n, size_t bytes,
+                           uint16_t *const xbuf[2], uint16_t *const ybuf[2], cudaStream_t stream, F compute) {
+    cudaStream_t cin = nullptr, cout = nullptr;
+    cudaEvent_t ev[7] = {};
+    moe_status_t st = MOE_OK;
+    bool ok = cudaStreamCreateWithFlags(&cin, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&cout, cudaStreamNonBlocking) == cudaSuccess;
+    for (int i = 0; ok && i < 7; ++i) ok = cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming) == cudaSuccess;
+    if (!ok) st = MOE_ERR_CUDA;
+    cudaEvent_t entry = ev[0], *xready = ev + 1, *done = ev + 3, *yfree = ev + 5;
+    auto chk = [&](cudaError_t e) {
+        if (st == MOE_OK && e != cudaSuccess) st = MOE_ERR_CUDA;
+        return st == MOE_OK;
+    };
+    // the copies start after the work the caller queued before this call
+    if (st == MOE_OK && chk(cudaEventRecord(entry, stream)) && chk(cudaStreamWaitEvent(cin, entry, 0)))
+        chk(cudaStreamWaitEvent(cout, entry, 0));
+    for (int i = 0; st == MOE_OK && i < n; ++i) {
+        const int b = i & 1;
+        if (i >= 2 && !chk(cudaStreamWaitEvent(cin, done[b], 0))) break;
+        if (!chk(cudaMemcpyAsync(xbuf[b], x_hosts[i], bytes, cudaMemcpyHostToDevice, cin))) break;
+        if (!chk(cudaEventRecord(xready[b], cin))) break;
+        if (!chk(cudaStreamWaitEvent(stream, xready[b], 0))) break;
+        if (i >= 2 && !chk(cudaStreamWaitEvent(stream, yfree[b], 0))) break;
+        if ((st = compute(xbuf[b], ybuf[b])) != MOE_OK) break;
+        if (!chk(cudaEventRecord(done[b], stream))) break;
+        if (!chk(cudaStreamWaitEvent(cout, done[b], 0))) break;
+        if (!chk(cudaMemcpyAsync(y_hosts[i], ybuf[b], bytes, cudaMemcpyDeviceToHost, cout))) break;
+        if (!chk(cudaEventRecord(yfree[b], cout))) break;
+    }
+    if (st == MOE_OK && n > 0) chk(cudaStreamWaitEvent(stream, yfree[(n - 1) & 1], 0));
+    for (int i = 0; i < 7; ++i)
+        if (ev[i]) cudaEventDestroy(ev[i]);
+    if (cin) cudaStreamDestroy(cin);
+    if (cout) cudaStreamDestroy(cout);
+    return st;
+}
+
 }  // namespace
 
 extern "C" {
@@ -399,6 +446,38 @@ moe_status_t moe_forward_host(const uint16_t *x_host, const float *Wr, const flo
     return cuda_status(cudaMemcpyAsync(y_host, y_dev, bytes, cudaMemcpyDeviceToHost, stream));
 }
 
+size_t moe_forward_host_pipelined_workspace_size(int T, int d, int E, int K, int f) {
+    if (check_shape(T, d, E, K, f, true, true) != MOE_OK) return 0;
+    moe_forward_layout_t L;
+    forward_layout(T, d, E, K, f, &L);
+    // a second x and y buffer after the layer's workspace
+    return L.total + 2 * align_up(static_cast<size_t>(T) * d * 2, 256);
+}
+
+moe_status_t moe_forward_host_pipelined(const uint16_t *const *x_hosts, uint16_t *const *y_hosts, int n_batches,
+                                        const float *Wr, const float *bias, const uint16_t *W1, const uint16_t *W2,
+                                        int T, int d, int E, int K, int f, void *workspace, size_t workspace_bytes,
+                                        cudaStream_t stream) {
+    if (!x_hosts || !y_hosts || n_batches < 1 || !workspace) return MOE_ERR_INVALID_ARG;
+    for (int i = 0; i < n_batches; ++i)
+        if (!x_hosts[i] || !y_hosts[i]) return MOE_ERR_INVALID_ARG;
+    if (!aligned(workspace, 256)) return MOE_ERR_INVALID_ARG;
+    moe_status_t st = check_shape(T, d, E, K, f, true, true);
+    if (st != MOE_OK) return st;
+    if (workspace_bytes < moe_forward_host_pipelined_workspace_size(T, d, E, K, f)) return MOE_ERR_WORKSPACE;
+    moe_forward_layout_t L;
+    forward_layout(T, d, E, K, f, &L);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const size_t bytes = static_cast<size_t>(T) * d * 2;
+    const size_t extra = align_up(bytes, 256);
+    uint16_t *const xbuf[2] = {reinterpret_cast<uint16_t *>(ws + L.x_dev), reinterpret_cast<uint16_t *>(ws + L.total)};
+    uint16_t *const ybuf[2] = {reinterpret_cast<uint16_t *>(ws + L.y_dev),
+                               reinterpret_cast<uint16_t *>(ws + L.total + extra)};
+    return run_pipelined(x_hosts, y_hosts, n_batches, bytes, xbuf, ybuf, stream, [&](uint16_t *xd, uint16_t *yd) {
+        return moe_forward(xd, Wr, bias, W1, W2, T, d, E, K, f, yd, workspace, workspace_bytes, stream);
+    });
+}
+
 size_t moe_mxfp8_scales_size(int rows, int K) {
     if (rows < 1 || K < 128 || K % 128 != 0) return 0;
     return moe::mxfp8_scales_bytes(rows, K);
@@ -529,6 +608,40 @@ moe_status_t moe_forward_mxfp8(const uint16_t *x, const float *Wr, const float *
         MOE_OK)
         return st;
     return moe_unpermute(y_perm, row_of, w, T, K, d, y, stream);
+}
+
+size_t moe_forward_mxfp8_host_pipelined_workspace_size(int T, int d, int E, int K, int f) {
+    if (check_mx_shape(T, d, E, K, f) != MOE_OK) return 0;
+    moe_forward_mxfp8_layout_t L;
+    forward_mxfp8_layout(T, d, E, K, f, &L);
+    // two x and two y buffers after the layer's workspace
+    return L.total + 4 * align_up(static_cast<size_t>(T) * d * 2, 256);
+}
+
+moe_status_t moe_forward_mxfp8_host_pipelined(const uint16_t *const *x_hosts, uint16_t *const *y_hosts,
+                                              int n_batches, const float *Wr, const float *bias,
+                                              const uint8_t *W1q, const uint8_t *W1s, const uint8_t *W2q,
+                                              const uint8_t *W2s, int T, int d, int E, int K, int f,
+                                              void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    if (!x_hosts || !y_hosts || n_batches < 1 || !workspace) return MOE_ERR_INVALID_ARG;
+    for (int i = 0; i < n_batches; ++i)
+        if (!x_hosts[i] || !y_hosts[i]) return MOE_ERR_INVALID_ARG;
+    if (!aligned(workspace, 256)) return MOE_ERR_INVALID_ARG;
+    moe_status_t st = check_mx_shape(T, d, E, K, f);
+    if (st != MOE_OK) return st;
+    if (workspace_bytes < moe_forward_mxfp8_host_pipelined_workspace_size(T, d, E, K, f)) return MOE_ERR_WORKSPACE;
+    moe_forward_mxfp8_layout_t L;
+    forward_mxfp8_layout(T, d, E, K, f, &L);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const size_t bytes = static_cast<size_t>(T) * d * 2;
+    const size_t extra = align_up(bytes, 256);
+    uint16_t *const xbuf[2] = {reinterpret_cast<uint16_t *>(ws + L.total),
+                               reinterpret_cast<uint16_t *>(ws + L.total + extra)};
+    uint16_t *const ybuf[2] = {reinterpret_cast<uint16_t *>(ws + L.total + 2 * extra),
+                               reinterpret_cast<uint16_t *>(ws + L.total + 3 * extra)};
+    return run_pipelined(x_hosts, y_hosts, n_batches, bytes, xbuf, ybuf, stream, [&](uint16_t *xd, uint16_t *yd) {
+        return moe_forward_mxfp8(xd, Wr, bias, W1q, W1s, W2q, W2s, T, d, E, K, f, yd, workspace, L.total, stream);
+    });
 }
 
 size_t moe_backward_workspace_size(int T, int d, int E, int K, int f) {

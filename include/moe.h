@@ -37,7 +37,7 @@
  * Conventions for every entry point:
  *   - All pointers except those of *_host calls are device pointers owned by
  *     the caller.  The library allocates no memory and performs no
- *     host<->device copy, except moe_forward_host (stated there).
+ *     host<->device copy, except the *_host calls (stated there).
  *   - Calls are asynchronous on `stream` and never synchronize; no value flows
  *     from device to host, so a sequence of calls can be captured in a CUDA
  *     graph and replayed for any routing.  (The first call on a device also
@@ -220,6 +220,24 @@ moe_status_t moe_forward_host(const uint16_t *x_host, const float *Wr, const flo
                               int K, int f, uint16_t *y_host, void *workspace,
                               size_t workspace_bytes, cudaStream_t stream);
 
+/* moe_forward over a sequence of n_batches batches in HOST memory, with the
+ * copies overlapped: batch i's host->device copy and batch i-1's
+ * device->host copy run on two copy streams of the call while the layer of
+ * batch i-1 / i runs on `stream` (double-buffered device copies of x and y).
+ * x_hosts[i], y_hosts[i]: [T, d] bf16 host buffers (pinned, or the copies
+ * are not asynchronous), which may repeat; y_hosts[i] is written from batch
+ * i.  `workspace` (256-byte aligned) holds
+ * moe_forward_host_pipelined_workspace_size() bytes: the layer's workspace
+ * (moe_forward_views) followed by the second x and y buffers.  All of the
+ * call's work -- every copy included -- is complete when `stream` is.
+ * 9 kernel launches per batch.  */
+size_t moe_forward_host_pipelined_workspace_size(int T, int d, int E, int K, int f);
+moe_status_t moe_forward_host_pipelined(const uint16_t *const *x_hosts, uint16_t *const *y_hosts,
+                                        int n_batches, const float *Wr, const float *bias,
+                                        const uint16_t *W1, const uint16_t *W2, int T, int d, int E,
+                                        int K, int f, void *workspace, size_t workspace_bytes,
+                                        cudaStream_t stream);
+
 /* ---------------------------------------------------------------------------
  * MXFP8 path ("Optimization 1: Grouped GEMM": on Blackwell the expert
  * matmuls run with MXFP8 block scaling, fed by grouped quantisation).
@@ -281,6 +299,16 @@ moe_status_t moe_forward_mxfp8(const uint16_t *x, const float *Wr, const float *
                                const uint8_t *W1s, const uint8_t *W2q, const uint8_t *W2s, int T, int d,
                                int E, int K, int f, uint16_t *y, void *workspace, size_t workspace_bytes,
                                cudaStream_t stream);
+/* The same over n_batches host batches with overlapped copies (see
+ * moe_forward_host_pipelined): the layer's MXFP8 workspace followed by two x
+ * and two y buffers.  */
+size_t moe_forward_mxfp8_host_pipelined_workspace_size(int T, int d, int E, int K, int f);
+moe_status_t moe_forward_mxfp8_host_pipelined(const uint16_t *const *x_hosts, uint16_t *const *y_hosts,
+                                              int n_batches, const float *Wr, const float *bias,
+                                              const uint8_t *W1q, const uint8_t *W1s,
+                                              const uint8_t *W2q, const uint8_t *W2s, int T, int d,
+                                              int E, int K, int f, void *workspace,
+                                              size_t workspace_bytes, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
  * Backward of the layer (the pages are about MoE training; they give no

@@ -130,6 +130,29 @@ def test_mxfp8_entry_points_reject_bad_arguments(moe):
     assert list(v.values()) == sorted(v.values())
 
 
+def test_pipelined_host_runners_reject_bad_arguments(moe):
+    import ctypes
+    L = moe.lib
+    one = (ctypes.c_void_p * 1)(FAKE)
+    nul = (ctypes.c_void_p * 1)(None)
+    n = L.moe_forward_host_pipelined_workspace_size(64, 64, 8, 2, 64)
+    assert n >= L.moe_forward_workspace_size(64, 64, 8, 2, 64) + 2 * 64 * 64 * 2
+    args = (FAKE, None, FAKE, FAKE, 64, 64, 8, 2, 64)
+    assert L.moe_forward_host_pipelined(one, one, 0, *args, FAKE, n, None) == 1       # no batch
+    assert L.moe_forward_host_pipelined(nul, one, 1, *args, FAKE, n, None) == 1       # null batch pointer
+    assert L.moe_forward_host_pipelined(None, one, 1, *args, FAKE, n, None) == 1
+    assert L.moe_forward_host_pipelined(one, one, 1, *args, FAKE + 16, n, None) == 1  # workspace alignment
+    assert L.moe_forward_host_pipelined(one, one, 1, *args, FAKE, n - 1, None) == 3
+    assert L.moe_forward_host_pipelined(one, one, 1, FAKE, None, FAKE, FAKE, 64, 64, 8, 2, 60, FAKE, n,
+                                        None) == 2                                     # f % 64
+    m = L.moe_forward_mxfp8_host_pipelined_workspace_size(64, 256, 8, 2, 256)
+    assert m >= L.moe_forward_mxfp8_workspace_size(64, 256, 8, 2, 256) + 4 * 64 * 256 * 2
+    assert L.moe_forward_mxfp8_host_pipelined_workspace_size(64, 192, 8, 2, 256) == 0
+    mx = (FAKE, None, FAKE, FAKE, FAKE, FAKE, 64, 256, 8, 2, 256)
+    assert L.moe_forward_mxfp8_host_pipelined(one, one, 0, *mx, FAKE, m, None) == 1
+    assert L.moe_forward_mxfp8_host_pipelined(one, one, 1, *mx, FAKE, m - 1, None) == 3
+
+
 def test_no_launch_happened(moe):
     # every call above was rejected on the host
     assert moe.launch_count() == 0
