@@ -415,6 +415,37 @@ def run_gpu(args):
     e2e_ms = _max_over_ranks(e0.elapsed_time(e1), ws)
     e2e_value = aggregate(flops_step, ws, args.steps, e2e_ms) / 1e12
 
+    # ---- the whole layer (one moe_forward call) captured once as a CUDA graph
+    # and replayed: the launch-overhead-free time of a step
+    graph = None
+    if not mxfp8 and not args.fused_combine:
+        layer_g = moe.MoELayer(w.Wr, w.bias, w.W1, w.W2, K, T)
+        y_g = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
+        gs = torch.cuda.Stream()
+        gs.wait_stream(stream)
+        with torch.cuda.stream(gs):
+            layer_g(x, out=y_g)  # warm the library's per-device state outside capture
+        gs.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=gs):
+            layer_g(x, out=y_g)
+        for _ in range(max(3, args.warmup)):
+            g.replay()
+        torch.cuda.synchronize()
+        _barrier(ws)
+        g0 = torch.cuda.Event(enable_timing=True)
+        g1 = torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for _ in range(args.steps):
+            g.replay()
+        g1.record(stream)
+        torch.cuda.synchronize()
+        assert moe.device_status() == 0
+        g_ms = _max_over_ranks(g0.elapsed_time(g1), ws)
+        graph = {"value": aggregate(flops_step, ws, args.steps, g_ms) / 1e12, "unit": "TFLOP/s",
+                 "ms_per_step": g_ms / args.steps, "note": "moe_forward captured once, replayed K times"}
+        del g, layer_g
+
     # ---- roofline of the dominant kernel
     peaks, peak_src = _peaks()
     dom = max(("grouped_gemm1_swiglu", "grouped_gemm2"), key=lambda n: kmean[n])
@@ -431,7 +462,10 @@ def run_gpu(args):
                 "traffic": (tr["dram_bytes_per_launch"] if tr else None),
                 "traffic_note": (tr.get("note") if tr else "no ncu counters for the current source")}
     share = {n: kmean[n] / sum(kmean.values()) for n in STEP_NAMES}
+    chunks = (T + 63) // 64
     hbm_bytes = {
+        # logits read; topk_idx, topk_w, row_of written; two [chunks, E] tables written and read
+        "route": 4.0 * T * E + 12.0 * TK + 16.0 * chunks * E,
         "permute": 2.0 * T * d + 2.0 * TK * d + 4.0 * TK,
         "unpermute": 2.0 * TK * d + 2.0 * T * d + 8.0 * TK,
     }
@@ -475,7 +509,7 @@ def run_gpu(args):
                     "d2h_bytes_per_step": T * d * 2, "ms_per_step": e2e_ms / args.steps,
                     "copies": "every batch's copies inside the timed region, overlapped with the neighbouring "
                               "batches' compute (moe_forward_host_pipelined)"},
-            "gpu_launches": launches, "clocks": clocks,
+            "gpu_launches": launches, "clocks": clocks, "graph": graph,
             "routing": {"empty_experts": int((counts == 0).sum().item()), "max_group": int(counts.max().item())},
         }
         print(json.dumps(line), flush=True)
