@@ -58,16 +58,16 @@ def _peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
-def _traffic_record(kernel: str):
-    """DRAM bytes per launch from the committed ncu summary, if the kernel's
-    source has not changed since the counters were taken."""
+def _traffic_record(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    this workload and the kernel's source has not changed since."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as fh:
         d = json.load(fh)
     rec = d.get(kernel)
-    if not rec:
+    if not rec or rec.get("workload") != workload:
         return None
     # the hash covers every source file the kernel is built from
     srcs = rec["source"] if isinstance(rec["source"], list) else [rec["source"]]
@@ -450,17 +450,40 @@ def run_gpu(args):
     peaks, peak_src = _peaks()
     dom = max(("grouped_gemm1_swiglu", "grouped_gemm2"), key=lambda n: kmean[n])
     dom_flops = (4.0 if dom == "grouped_gemm1_swiglu" else 2.0) * TK * d * f
-    achieved = dom_flops / (kmean[dom] * 1e-3) / 1e12
     peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
     peak_src_note = f"{peak_src} bf16_tflops_sustained"
+    eb = 1.0 if mxfp8 else 2.0  # bytes per weight / activation element
     if mxfp8:
         peak *= 2.0
         peak_src_note += " x 2 (nominal fp8 / bf16 dense tensor ratio, 4.5 / 2.25 PFLOP/s)"
-    tr = _traffic_record(dom + ("_mxfp8" if mxfp8 else ""))
-    roofline = {"kernel": dom + ("_mxfp8" if mxfp8 else ""), "bound": "tensor", "achieved": achieved, "peak": peak,
-                "unit": "TFLOP/s", "frac": achieved / peak, "peak_source": peak_src_note,
-                "traffic": (tr["dram_bytes_per_launch"] if tr else None),
-                "traffic_note": (tr.get("note") if tr else "no ncu counters for the current source")}
+    # algorithmic bytes of one launch: the live experts' weights, the
+    # activations read and the output written (scales of the MXFP8 operands
+    # add 1/32 of their codes)
+    live = int((counts > 0).sum().item())
+    sc = (1.0 + 1.0 / 32.0) if mxfp8 else 1.0
+    if dom == "grouped_gemm1_swiglu":
+        dom_bytes = sc * eb * (live * 2.0 * f * d + TK * d) + sc * eb * TK * f
+    else:
+        dom_bytes = sc * eb * (live * 1.0 * d * f + TK * f) + 2.0 * TK * d
+    t_dom = kmean[dom] * 1e-3
+    hbm_peak = float(peaks["hbm_gbs"])
+    # the binding resource: the larger of the two floors
+    tensor_floor, hbm_floor = dom_flops / (peak * 1e12), dom_bytes / (hbm_peak * 1e9)
+    tr = _traffic_record(dom + ("_mxfp8" if mxfp8 else ""), s_name)
+    common = {"kernel": dom + ("_mxfp8" if mxfp8 else ""),
+              "traffic": (tr["dram_bytes_per_launch"] if tr else None),
+              "traffic_note": (tr.get("note") if tr else
+                               "no ncu counters for this kernel source on this workload"),
+              "algorithmic": {"flop": dom_flops, "bytes": dom_bytes, "live_experts": live,
+                              "tensor_floor_ms": tensor_floor * 1e3, "hbm_floor_ms": hbm_floor * 1e3}}
+    if hbm_floor > tensor_floor:
+        achieved = dom_bytes / t_dom / 1e9
+        roofline = dict(bound="hbm", achieved=achieved, peak=hbm_peak, unit="GB/s", frac=achieved / hbm_peak,
+                        peak_source=f"{peak_src} hbm_gbs", **common)
+    else:
+        achieved = dom_flops / t_dom / 1e12
+        roofline = dict(bound="tensor", achieved=achieved, peak=peak, unit="TFLOP/s", frac=achieved / peak,
+                        peak_source=peak_src_note, **common)
     share = {n: kmean[n] / sum(kmean.values()) for n in STEP_NAMES}
     chunks = (T + 63) // 64
     hbm_bytes = {
