@@ -55,3 +55,45 @@ def test_graph_replay_with_new_routing(s):
         check_output(to_np(y_static)[same], ref["y"][same], f"y (replay seed {seed})")
         seen_counts.append(tuple(ref["counts"].tolist()))
     assert len(set(seen_counts)) == len(seen_counts), "replays should see different routings"
+
+
+def test_training_step_graph_replays_match_eager():
+    """The training step -- moe_forward_train (saving the pre-activations) then
+    moe_backward -- captured once and replayed with new tokens and output
+    gradients: the gradients equal an eager run's bit for bit (the backward
+    reads every count on the device too)."""
+    s = Shape(T=300, d=256, E=16, K=4, f=128, bias="normal_0.5")
+    w = make_weights(s, seed=0, device="cpu")
+    wd = [t.cuda() for t in (w.Wr, w.bias, w.W1, w.W2)]
+    layer = moe.MoELayer(*wd, s.K, s.T)
+    x_static = make_tokens(s, seed=0, device="cpu").cuda()
+    dy_static = torch.randn((s.T, s.d), device="cuda").to(torch.bfloat16)
+    y_static = torch.empty_like(x_static)
+    layer(x_static, out=y_static, save_preact=True)   # set-up (buffers, library state) outside capture
+    grads = layer.backward(x_static, dy_static)
+    ws = layer.bw_workspace
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        layer(x_static, out=y_static, save_preact=True)
+        layer.backward(x_static, dy_static, grads=grads, workspace=ws)
+    eager = moe.MoELayer(*wd, s.K, s.T)
+    for seed in (1, 2, 3):
+        x_new = make_tokens(s, seed=seed, device="cpu").cuda()
+        g = torch.Generator(device="cuda").manual_seed(seed)
+        dy_new = torch.randn((s.T, s.d), device="cuda", generator=g).to(torch.bfloat16)
+        x_static.copy_(x_new)
+        dy_static.copy_(dy_new)
+        for t in grads.values():
+            t.fill_(float("nan"))
+        graph.replay()
+        y_e = eager(x_new, save_preact=True)
+        g_e = eager.backward(x_new, dy_new)
+        torch.cuda.synchronize()
+        assert moe.device_status() == 0
+        assert torch.equal(y_static.view(torch.int16), y_e.view(torch.int16))
+        for k in g_e:
+            a, b = grads[k], g_e[k]
+            if a.dtype == torch.bfloat16:
+                a, b = a.view(torch.int16), b.view(torch.int16)
+            assert torch.equal(a, b), (seed, k)
