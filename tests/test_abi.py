@@ -153,6 +153,39 @@ def test_pipelined_host_runners_reject_bad_arguments(moe):
     assert L.moe_forward_mxfp8_host_pipelined(one, one, 1, *mx, FAKE, m - 1, None) == 3
 
 
+def test_backward_entry_points_reject_bad_arguments(moe):
+    import ctypes
+    L = moe.lib
+    T, d, E, K, f = 64, 128, 8, 2, 64
+    nb = L.moe_backward_workspace_size(T, d, E, K, f)
+    nf = L.moe_forward_workspace_size(T, d, E, K, f)
+    assert nb > 0 and L.moe_backward_workspace_size(T, 96, E, K, f) == 0   # d % 64
+    # layout: ordered regions, each large enough
+    lay = moe._LayoutBW()
+    assert L.moe_backward_views(T, d, E, K, f, ctypes.byref(lay)) == 0
+    offs = [getattr(lay, n) for n, _ in moe._LayoutBW._fields_]
+    assert offs == sorted(offs) and offs[-1] == nb
+    TK = T * K
+    assert lay.dy_perm - lay.dl_row >= TK * 4 and lay.da - lay.a >= TK * 2 * f * 2
+    assert lay.rw_part - lay.WrT >= d * E * 4
+
+    def bwd(*, x=FAKE, Wr=FAKE, W1=FAKE, dy=FAKE, fws=FAKE, fbytes=nf, pre=None, dx=FAKE, dWr=FAKE, ws=FAKE,
+            wbytes=nb, f_=f):
+        return L.moe_backward(x, Wr, None, W1, FAKE, T, d, E, K, f_, dy, fws, fbytes, pre, dx, dWr, FAKE, FAKE,
+                              FAKE, ws, wbytes, None)
+    assert bwd(x=None) == 1 and bwd(dy=None) == 1 and bwd(fws=None) == 1 and bwd(dx=None) == 1
+    assert bwd(W1=FAKE + 8) == 1          # 16-byte alignment
+    assert bwd(Wr=FAKE + 2) == 1          # 4-byte alignment
+    assert bwd(pre=FAKE + 8) == 1         # saved pre-activations: 16-byte alignment
+    assert bwd(f_=60) == 2                # f % 64
+    assert bwd(fbytes=nf - 1) == 3 and bwd(wbytes=nb - 1) == 3
+    # the training forward and GEMM1 with saved pre-activations
+    assert L.moe_forward_train(FAKE, FAKE, None, FAKE, FAKE, T, d, E, K, f, FAKE, FAKE, nf, FAKE + 8, None) == 1
+    assert L.moe_forward_train(FAKE, FAKE, None, FAKE, FAKE, T, d, E, K, f, FAKE, FAKE, nf - 1, FAKE, None) == 3
+    assert L.moe_grouped_gemm1_swiglu_preact(FAKE, FAKE, E, TK, d, f, FAKE, FAKE, None, None) == 1
+    assert L.moe_grouped_gemm1_swiglu_preact(FAKE, FAKE, E, TK, d, 96, FAKE, FAKE, FAKE, None) == 2
+
+
 def test_no_launch_happened(moe):
     # every call above was rejected on the host
     assert moe.launch_count() == 0
