@@ -127,42 +127,48 @@ __device__ __forceinline__ void zero_tail(uint8_t *boxes, int nbox, int valid, i
     }
 }
 
-// One warp's 32 rows of a tile, 32 columns at a time: the fp32 values go to
-// shared memory (128-byte swizzle: 16-byte chunk j of row i at j ^ (i & 7))
-// and one TMA store writes the 32 x 32 box as full lines (L2 evict-first:
-// the gradients are not read again here).  M and N are multiples of 32, so
-// boxes are whole; a warp whose 32 rows lie past M stores nothing.  `zero`:
-// the expert has no rows, the accumulator is not read.
+// One warp's 32 rows of a tile, 64 columns at a time: two TMEM loads per
+// wait, the fp32 values of each 32 columns go to one of the warp's two
+// staging buffers (128-byte swizzle: 16-byte chunk j of row i at j ^ (i & 7)),
+// then one proxy fence and two TMA stores of 32 x 32 boxes write full lines
+// (L2 evict-first: the gradients are not read again here).  M and N are
+// multiples of 32, so boxes are whole; a warp whose 32 rows lie past M stores
+// nothing.  `zero`: the expert has no rows, the accumulator is not read.
 __device__ __forceinline__ void epilogue(const Params &p, const CUtensorMap *tm_out, const Tile &t, uint32_t tbase,
-                                         int q, int lane, bool zero, uint8_t *stage, uint32_t &sbuf) {
+                                         int q, int lane, bool zero, uint8_t *stage) {
     const int m0 = t.m0 + q * 32;
     if (m0 >= p.M) return;  // warp-uniform
 #pragma unroll 1
-    for (int c = 0; c < BN; c += 32) {
+    for (int c = 0; c < BN; c += 64) {
         const int n = t.n0 + c;
         if (n >= p.N) break;  // uniform
-        uint32_t v[32];
+        uint32_t v[2][32];
         if (!zero) {
-            tmem_ld_32x32b_x32(tbase + c, v);
+            tmem_ld_32x32b_x32(tbase + c, v[0]);
+            tmem_ld_32x32b_x32(tbase + c + 32, v[1]);
             tmem_ld_wait();
         } else {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = 0u;
+            for (int i = 0; i < 32; ++i) v[0][i] = v[1][i] = 0u;
         }
-        uint8_t *buf = stage + sbuf * EPI_BUF;
-        if (lane == 0) bulk_wait_read<1>();  // this buffer's store from two chunks ago has read it
+        if (lane == 0) bulk_wait_read<0>();  // the previous stores have read both buffers
         __syncwarp();
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-            *reinterpret_cast<uint4 *>(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) =
-                make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        for (int b = 0; b < 2; ++b) {
+            uint8_t *buf = stage + b * EPI_BUF;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                *reinterpret_cast<uint4 *>(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+                    make_uint4(v[b][4 * j], v[b][4 * j + 1], v[b][4 * j + 2], v[b][4 * j + 3]);
+        }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-            tma_store_2d_evict_first(tm_out, buf, n, t.e * p.M + m0, l2_policy_evict_first());
+            const uint64_t pol = l2_policy_evict_first();
+            tma_store_2d_evict_first(tm_out, stage, n, t.e * p.M + m0, pol);
+            if (n + 32 < p.N) tma_store_2d_evict_first(tm_out, stage + EPI_BUF, n + 32, t.e * p.M + m0, pol);
             bulk_commit();
         }
-        sbuf ^= 1u;
     }
 }
 
@@ -296,14 +302,13 @@ wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
     } else {
         const int q = warp & 3;
         uint8_t *stage = smem + OFF_EPI + (warp - 2) * 2 * EPI_BUF;
-        uint32_t sbuf = 0;
         uint32_t acc = 0, acc_phase = 0;
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
             const Tile t = decode<BM>(p, tile);
             if (!mbar_wait(&tfull[acc], acc_phase, s_abort, p.status, p.timeout_ns)) break;
             tc_fence_after();
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
-            epilogue(p, &tmD, t, tbase, q, lane, s_gcnt[t.e] == 0, stage, sbuf);
+            epilogue(p, &tmD, t, tbase, q, lane, s_gcnt[t.e] == 0, stage);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[acc]);
@@ -486,7 +491,6 @@ wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     } else {
         const int q = warp & 3;
         uint8_t *stage = smem + P_OFF_EPI + (warp - 2) * 2 * EPI_BUF;
-        uint32_t sbuf = 0;
         const uint32_t tempty0 = mapa_shared(smem_u32(&tempty[0]), 0);
         uint32_t acc = 0, acc_phase = 0;
         for (int tile = pair; tile < total; tile += npairs) {
@@ -495,7 +499,7 @@ wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             tc_fence_after();
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
             t.m0 += half;  // this CTA's 128 rows of the tile
-            epilogue(p, &tmD, t, tbase, q, lane, s_gcnt[t.e] == 0, stage, sbuf);
+            epilogue(p, &tmD, t, tbase, q, lane, s_gcnt[t.e] == 0, stage);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(tempty0 + 8u * acc);
