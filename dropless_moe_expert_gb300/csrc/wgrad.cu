@@ -15,8 +15,10 @@
 // (K) of A's 128 columns and B's 256 columns as 64 x 64 TMA boxes (128-byte
 // swizzle), and the MMAs read them with MN-major descriptors -- no transposed
 // copy in memory.  A group's K blocks start at its first row; in its last
-// block the rows past the group (the next expert's rows, or TMA zero fill
-// past TK) are zeroed in shared memory before the MMAs, so they add nothing.
+// block the MMAs cover only the 16-row K steps that hold the group's rows,
+// and the rows past the group inside the last step (the next expert's rows,
+// or TMA zero fill past TK) are zeroed in shared memory first, so they add
+// nothing.
 //
 // Persistent kernels, one CTA per SM, over tiles (e, row block of D, 256-column
 // block) of every expert, with two 256-column TMEM accumulators so a tile's
@@ -115,10 +117,11 @@ __device__ __forceinline__ Tile decode(const Params &p, int tile) {
     return t;
 }
 
-// Zeroes rows valid..63 of `nbox` consecutive 64 x 64 boxes (one contiguous
-// byte range per box: a 128-byte row holds all its swizzled chunks); one warp.
-__device__ __forceinline__ void zero_tail(uint8_t *boxes, int nbox, int valid, int lane) {
-    const int zbytes = (BK - valid) * 128;
+// Zeroes rows valid..upto-1 of `nbox` consecutive 64 x 64 boxes (one
+// contiguous byte range per box: a 128-byte row holds all its swizzled
+// chunks); one warp.
+__device__ __forceinline__ void zero_tail(uint8_t *boxes, int nbox, int valid, int upto, int lane) {
+    const int zbytes = (upto - valid) * 128;
 #pragma unroll 1
     for (int b = 0; b < nbox; ++b) {
         uint8_t *z = boxes + b * BOX + valid * 128;
@@ -269,9 +272,12 @@ wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
                 if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
                 tc_fence_after();
                 uint8_t *sa = smem + stage * STAGE;
-                const int valid = cnt - kb * BK;  // warp-uniform
-                if (valid < BK) {
-                    zero_tail(sa, 6, valid, lane);
+                // a group's last block: MMAs only over the 16-row K steps that
+                // hold its rows, the rows past it up to the next step zeroed
+                const int valid = min(cnt - kb * BK, BK);  // warp-uniform
+                const int ksteps = (valid + UMMA_K - 1) / UMMA_K;
+                if (valid < ksteps * UMMA_K) {
+                    zero_tail(sa, 6, valid, ksteps * UMMA_K, lane);
                     fence_proxy_async_smem();
                     __syncwarp();
                 }
@@ -279,8 +285,7 @@ wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
                     const uint32_t a_addr = smem_u32(sa);
                     const uint64_t adesc = smem_desc_mnmajor_sw128(a_addr, BOX);
                     const uint64_t bdesc = smem_desc_mnmajor_sw128(a_addr + A_BYTES, BOX);
-#pragma unroll
-                    for (int j = 0; j < BK / UMMA_K; ++j)  // 16 rows of K: 2048 bytes further
+                    for (int j = 0; j < ksteps; ++j)  // 16 rows of K: 2048 bytes further
                         umma_bf16(d_tmem, adesc + 128 * j, bdesc + 128 * j, idesc, (kb | j) != 0);
                     umma_commit(&empty[stage]);
                 }
@@ -449,11 +454,12 @@ wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
                 tc_fence_after();
                 uint8_t *sa = smem + stage * P_STAGE;
-                const int valid = cnt - kb * BK;  // warp-uniform
-                if (valid < BK) {
-                    zero_tail(sa, 4, valid, lane);
+                const int valid = min(cnt - kb * BK, BK);  // warp-uniform
+                const int ksteps = (valid + UMMA_K - 1) / UMMA_K;
+                if (valid < ksteps * UMMA_K) {
+                    zero_tail(sa, 4, valid, ksteps * UMMA_K, lane);
                     // the same rows of the peer's four boxes
-                    const int zbytes = (BK - valid) * 128;
+                    const int zbytes = (ksteps * UMMA_K - valid) * 128;
                     const uint32_t peer = peer_base + static_cast<uint32_t>(stage * P_STAGE + valid * 128);
 #pragma unroll 1
                     for (int b = 0; b < 4; ++b)
@@ -466,8 +472,7 @@ wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     const uint32_t a_addr = smem_u32(sa);
                     const uint64_t adesc = smem_desc_mnmajor_sw128(a_addr, BOX);
                     const uint64_t bdesc = smem_desc_mnmajor_sw128(a_addr + 2 * BOX, BOX);
-#pragma unroll
-                    for (int j = 0; j < BK / UMMA_K; ++j)
+                    for (int j = 0; j < ksteps; ++j)
                         umma_bf16_pair(d_tmem, adesc + 128 * j, bdesc + 128 * j, idesc, (kb | j) != 0);
                     umma_commit_pair_multicast(&empty[stage], 0x3);
                 }
