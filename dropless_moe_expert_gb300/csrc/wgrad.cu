@@ -15,10 +15,8 @@
 // (K) of A's 128 columns and B's 256 columns as 64 x 64 TMA boxes (128-byte
 // swizzle), and the MMAs read them with MN-major descriptors -- no transposed
 // copy in memory.  A group's K blocks start at its first row; in its last
-// block the MMAs cover only the 16-row K steps that hold the group's rows,
-// and the rows past the group inside the last step (the next expert's rows,
-// or TMA zero fill past TK) are zeroed in shared memory first, so they add
-// nothing.
+// block the rows past the group (the next expert's rows, or TMA zero fill
+// past TK) are zeroed in shared memory before the MMAs, so they add nothing.
 //
 // Persistent kernels, one CTA per SM, over tiles (e, row block of D, 256-column
 // block) of every expert, with two 256-column TMEM accumulators so a tile's
@@ -117,11 +115,10 @@ __device__ __forceinline__ Tile decode(const Params &p, int tile) {
     return t;
 }
 
-// Zeroes rows valid..upto-1 of `nbox` consecutive 64 x 64 boxes (one
-// contiguous byte range per box: a 128-byte row holds all its swizzled
-// chunks); one warp.
-__device__ __forceinline__ void zero_tail(uint8_t *boxes, int nbox, int valid, int upto, int lane) {
-    const int zbytes = (upto - valid) * 128;
+// Zeroes rows valid..63 of `nbox` consecutive 64 x 64 boxes (one contiguous
+// byte range per box: a 128-byte row holds all its swizzled chunks); one warp.
+__device__ __forceinline__ void zero_tail(uint8_t *boxes, int nbox, int valid, int lane) {
+    const int zbytes = (BK - valid) * 128;
 #pragma unroll 1
     for (int b = 0; b < nbox; ++b) {
         uint8_t *z = boxes + b * BOX + valid * 128;
@@ -130,48 +127,42 @@ __device__ __forceinline__ void zero_tail(uint8_t *boxes, int nbox, int valid, i
     }
 }
 
-// One warp's 32 rows of a tile, 64 columns at a time: two TMEM loads per
-// wait, the fp32 values of each 32 columns go to one of the warp's two
-// staging buffers (128-byte swizzle: 16-byte chunk j of row i at j ^ (i & 7)),
-// then one proxy fence and two TMA stores of 32 x 32 boxes write full lines
-// (L2 evict-first: the gradients are not read again here).  M and N are
-// multiples of 32, so boxes are whole; a warp whose 32 rows lie past M stores
-// nothing.  `zero`: the expert has no rows, the accumulator is not read.
+// One warp's 32 rows of a tile, 32 columns at a time: the fp32 values go to
+// shared memory (128-byte swizzle: 16-byte chunk j of row i at j ^ (i & 7))
+// and one TMA store writes the 32 x 32 box as full lines (L2 evict-first:
+// the gradients are not read again here).  M and N are multiples of 32, so
+// boxes are whole; a warp whose 32 rows lie past M stores nothing.  `zero`:
+// the expert has no rows, the accumulator is not read.
 __device__ __forceinline__ void epilogue(const Params &p, const CUtensorMap *tm_out, const Tile &t, uint32_t tbase,
-                                         int q, int lane, bool zero, uint8_t *stage) {
+                                         int q, int lane, bool zero, uint8_t *stage, uint32_t &sbuf) {
     const int m0 = t.m0 + q * 32;
     if (m0 >= p.M) return;  // warp-uniform
 #pragma unroll 1
-    for (int c = 0; c < BN; c += 64) {
+    for (int c = 0; c < BN; c += 32) {
         const int n = t.n0 + c;
         if (n >= p.N) break;  // uniform
-        uint32_t v[2][32];
+        uint32_t v[32];
         if (!zero) {
-            tmem_ld_32x32b_x32(tbase + c, v[0]);
-            tmem_ld_32x32b_x32(tbase + c + 32, v[1]);
+            tmem_ld_32x32b_x32(tbase + c, v);
             tmem_ld_wait();
         } else {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[0][i] = v[1][i] = 0u;
+            for (int i = 0; i < 32; ++i) v[i] = 0u;
         }
-        if (lane == 0) bulk_wait_read<0>();  // the previous stores have read both buffers
+        uint8_t *buf = stage + sbuf * EPI_BUF;
+        if (lane == 0) bulk_wait_read<1>();  // this buffer's store from two chunks ago has read it
         __syncwarp();
 #pragma unroll
-        for (int b = 0; b < 2; ++b) {
-            uint8_t *buf = stage + b * EPI_BUF;
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                *reinterpret_cast<uint4 *>(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) =
-                    make_uint4(v[b][4 * j], v[b][4 * j + 1], v[b][4 * j + 2], v[b][4 * j + 3]);
-        }
+        for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<uint4 *>(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+                make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-            const uint64_t pol = l2_policy_evict_first();
-            tma_store_2d_evict_first(tm_out, stage, n, t.e * p.M + m0, pol);
-            if (n + 32 < p.N) tma_store_2d_evict_first(tm_out, stage + EPI_BUF, n + 32, t.e * p.M + m0, pol);
+            tma_store_2d_evict_first(tm_out, buf, n, t.e * p.M + m0, l2_policy_evict_first());
             bulk_commit();
         }
+        sbuf ^= 1u;
     }
 }
 
@@ -272,12 +263,9 @@ wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
                 if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
                 tc_fence_after();
                 uint8_t *sa = smem + stage * STAGE;
-                // a group's last block: MMAs only over the 16-row K steps that
-                // hold its rows, the rows past it up to the next step zeroed
-                const int valid = min(cnt - kb * BK, BK);  // warp-uniform
-                const int ksteps = (valid + UMMA_K - 1) / UMMA_K;
-                if (valid < ksteps * UMMA_K) {
-                    zero_tail(sa, 6, valid, ksteps * UMMA_K, lane);
+                const int valid = cnt - kb * BK;  // warp-uniform
+                if (valid < BK) {
+                    zero_tail(sa, 6, valid, lane);
                     fence_proxy_async_smem();
                     __syncwarp();
                 }
@@ -285,7 +273,8 @@ wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
                     const uint32_t a_addr = smem_u32(sa);
                     const uint64_t adesc = smem_desc_mnmajor_sw128(a_addr, BOX);
                     const uint64_t bdesc = smem_desc_mnmajor_sw128(a_addr + A_BYTES, BOX);
-                    for (int j = 0; j < ksteps; ++j)  // 16 rows of K: 2048 bytes further
+#pragma unroll
+                    for (int j = 0; j < BK / UMMA_K; ++j)  // 16 rows of K: 2048 bytes further
                         umma_bf16(d_tmem, adesc + 128 * j, bdesc + 128 * j, idesc, (kb | j) != 0);
                     umma_commit(&empty[stage]);
                 }
@@ -307,13 +296,14 @@ wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
     } else {
         const int q = warp & 3;
         uint8_t *stage = smem + OFF_EPI + (warp - 2) * 2 * EPI_BUF;
+        uint32_t sbuf = 0;
         uint32_t acc = 0, acc_phase = 0;
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
             const Tile t = decode<BM>(p, tile);
             if (!mbar_wait(&tfull[acc], acc_phase, s_abort, p.status, p.timeout_ns)) break;
             tc_fence_after();
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
-            epilogue(p, &tmD, t, tbase, q, lane, s_gcnt[t.e] == 0, stage);
+            epilogue(p, &tmD, t, tbase, q, lane, s_gcnt[t.e] == 0, stage, sbuf);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[acc]);
@@ -454,12 +444,11 @@ wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
                 tc_fence_after();
                 uint8_t *sa = smem + stage * P_STAGE;
-                const int valid = min(cnt - kb * BK, BK);  // warp-uniform
-                const int ksteps = (valid + UMMA_K - 1) / UMMA_K;
-                if (valid < ksteps * UMMA_K) {
-                    zero_tail(sa, 4, valid, ksteps * UMMA_K, lane);
+                const int valid = cnt - kb * BK;  // warp-uniform
+                if (valid < BK) {
+                    zero_tail(sa, 4, valid, lane);
                     // the same rows of the peer's four boxes
-                    const int zbytes = (ksteps * UMMA_K - valid) * 128;
+                    const int zbytes = (BK - valid) * 128;
                     const uint32_t peer = peer_base + static_cast<uint32_t>(stage * P_STAGE + valid * 128);
 #pragma unroll 1
                     for (int b = 0; b < 4; ++b)
@@ -472,7 +461,8 @@ wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     const uint32_t a_addr = smem_u32(sa);
                     const uint64_t adesc = smem_desc_mnmajor_sw128(a_addr, BOX);
                     const uint64_t bdesc = smem_desc_mnmajor_sw128(a_addr + 2 * BOX, BOX);
-                    for (int j = 0; j < ksteps; ++j)
+#pragma unroll
+                    for (int j = 0; j < BK / UMMA_K; ++j)
                         umma_bf16_pair(d_tmem, adesc + 128 * j, bdesc + 128 * j, idesc, (kb | j) != 0);
                     umma_commit_pair_multicast(&empty[stage], 0x3);
                 }
@@ -496,6 +486,7 @@ wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     } else {
         const int q = warp & 3;
         uint8_t *stage = smem + P_OFF_EPI + (warp - 2) * 2 * EPI_BUF;
+        uint32_t sbuf = 0;
         const uint32_t tempty0 = mapa_shared(smem_u32(&tempty[0]), 0);
         uint32_t acc = 0, acc_phase = 0;
         for (int tile = pair; tile < total; tile += npairs) {
@@ -504,7 +495,7 @@ wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             tc_fence_after();
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
             t.m0 += half;  // this CTA's 128 rows of the tile
-            epilogue(p, &tmD, t, tbase, q, lane, s_gcnt[t.e] == 0, stage);
+            epilogue(p, &tmD, t, tbase, q, lane, s_gcnt[t.e] == 0, stage, sbuf);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(tempty0 + 8u * acc);
