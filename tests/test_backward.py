@@ -38,6 +38,11 @@ CASES = [
     # (d = 320, 2f = 384) and partial 256-column blocks
     Shape(T=1500, d=320, E=2, K=1, f=192),
     Shape(T=3000, d=128, E=4, K=2, f=384, bias="skew"),
+    # degenerate cases: one token; one expert (a dense FFN, no router gradient);
+    # K = E (every expert on every token); the smallest widths
+    Shape(T=1, d=128, E=4, K=2, f=64),
+    Shape(T=200, d=128, E=1, K=1, f=128),
+    Shape(T=64, d=64, E=8, K=8, f=64),
 ]
 
 
