@@ -76,7 +76,8 @@ combine_bwd_kernel(const uint4 *__restrict__ dy, const uint4 *__restrict__ y_per
             const int r = row_of[static_cast<size_t>(t) * K + k];
             const float w = topk_w[static_cast<size_t>(t) * K + k];
             float dot = 0.0f;
-            for (int v = lane; v < nvec; v += 32) {
+            const bool row_ok = r >= 0 && r < T * K;  // outside the contract: no access, dw = 0
+            for (int v = lane; row_ok && v < nvec; v += 32) {
                 float a[8], b[8];
                 unpack8(__ldg(dy + static_cast<size_t>(t) * nvec + v), a);
                 unpack8(__ldg(y_perm + static_cast<size_t>(r) * nvec + v), b);
@@ -268,7 +269,8 @@ router_wgrad_reduce_kernel(const float *__restrict__ part, const float *__restri
 }
 
 // dx[t] = sum_k dx_perm[row_of[t,k]] + sum_k dl[t,k] Wr^T[idx[t,k]]; one warp
-// per token, fp32 in ascending k, then bf16.
+// per token, fp32 in ascending k, then bf16.  Lane k holds the token's k-th
+// row, expert and dl (K <= 32), handed to every lane by shuffles.
 __global__ void __launch_bounds__(256)
 dx_kernel(const uint4 *__restrict__ dx_perm, const float *__restrict__ WrT, const int32_t *__restrict__ row_of,
           const int32_t *__restrict__ topk_idx, const float *__restrict__ dl, int T, int K, int E, int TK, int nvec,
@@ -277,27 +279,38 @@ dx_kernel(const uint4 *__restrict__ dx_perm, const float *__restrict__ WrT, cons
     const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int nw = (gridDim.x * blockDim.x) >> 5;
     for (int t = gw; t < T; t += nw) {
-        for (int v = lane; v < nvec; v += 32) {
+        int my_r = -1, my_e = -1;
+        float my_g = 0.0f;
+        if (lane < K) {
+            my_r = row_of[static_cast<size_t>(t) * K + lane];
+            my_e = topk_idx[static_cast<size_t>(t) * K + lane];
+            my_g = dl[static_cast<size_t>(t) * K + lane];
+        }
+        // the loop is warp-uniform (the shuffles need every lane); lanes past
+        // the row's end load and store nothing
+        for (int v0 = 0; v0 < nvec; v0 += 32) {
+            const int v = v0 + lane;
+            const bool col_ok = v < nvec;
             float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
             for (int k = 0; k < K; ++k) {
-                const int r = row_of[static_cast<size_t>(t) * K + k];
-                if (r < 0 || r >= TK) continue;
+                const int r = __shfl_sync(0xffffffffu, my_r, k);
+                if (r < 0 || r >= TK || !col_ok) continue;
                 float xv[8];
                 unpack8(__ldg(dx_perm + static_cast<size_t>(r) * nvec + v), xv);
 #pragma unroll
                 for (int i = 0; i < 8; ++i) acc[i] += xv[i];
             }
             for (int k = 0; k < K; ++k) {
-                const int e = topk_idx[static_cast<size_t>(t) * K + k];
-                if (e < 0 || e >= E) continue;
-                const float g = dl[static_cast<size_t>(t) * K + k];
+                const int e = __shfl_sync(0xffffffffu, my_e, k);
+                const float g = __shfl_sync(0xffffffffu, my_g, k);
+                if (e < 0 || e >= E || !col_ok) continue;
                 const float4 *wr = reinterpret_cast<const float4 *>(WrT + static_cast<size_t>(e) * nvec * 8) + 2 * v;
                 const float4 w0 = __ldg(wr), w1 = __ldg(wr + 1);
                 const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
                 for (int i = 0; i < 8; ++i) acc[i] = __fmaf_rn(g, wv[i], acc[i]);
             }
-            dx[static_cast<size_t>(t) * nvec + v] = pack8(acc);
+            if (col_ok) dx[static_cast<size_t>(t) * nvec + v] = pack8(acc);
         }
     }
 }

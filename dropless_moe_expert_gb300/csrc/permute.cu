@@ -41,6 +41,7 @@ permute_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ row_of, 
             }
             for (int k = 0; k < K; ++k) {
                 const int r = __shfl_sync(0xffffffffu, my_row, k);
+                if (r < 0 || r >= T * K) continue;  // outside the contract: no write (warp-uniform)
                 uint4 *dst = x_perm + static_cast<size_t>(r) * nvec;
 #pragma unroll
                 for (int u = 0; u < UV; ++u) {
@@ -93,11 +94,13 @@ unpermute_kernel(const uint4 *__restrict__ y_perm, const int32_t *__restrict__ r
                 uint4 buf[KT > 0 ? KT : 1][UVK];
 #pragma unroll
                 for (int k = 0; k < KT; ++k) {
-                    const uint4 *src = y_perm + static_cast<size_t>(__shfl_sync(0xffffffffu, my_row, k)) * nvec;
+                    const int r = __shfl_sync(0xffffffffu, my_row, k);
+                    const bool row_ok = r >= 0 && r < T * K;  // outside the contract: read as zeros
+                    const uint4 *src = y_perm + static_cast<size_t>(row_ok ? r : 0) * nvec;
 #pragma unroll
                     for (int u = 0; u < UVK; ++u) {
                         const int v = v0 + u * 32 + lane;
-                        buf[k][u] = v < nvec ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
+                        buf[k][u] = (row_ok && v < nvec) ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
                     }
                 }
 #pragma unroll
@@ -110,12 +113,13 @@ unpermute_kernel(const uint4 *__restrict__ y_perm, const int32_t *__restrict__ r
                 for (int k = 0; k < K; ++k) {
                     const int r = __shfl_sync(0xffffffffu, my_row, k);
                     const float w = __shfl_sync(0xffffffffu, my_w, k);
-                    const uint4 *src = y_perm + static_cast<size_t>(r) * nvec;
+                    const bool row_ok = r >= 0 && r < T * K;  // outside the contract: read as zeros
+                    const uint4 *src = y_perm + static_cast<size_t>(row_ok ? r : 0) * nvec;
                     uint4 buf[UVK];
 #pragma unroll
                     for (int u = 0; u < UVK; ++u) {
                         const int v = v0 + u * 32 + lane;
-                        buf[u] = v < nvec ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
+                        buf[u] = (row_ok && v < nvec) ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
                     }
 #pragma unroll
                     for (int u = 0; u < UVK; ++u) fma_bf16x8(acc[u], w, buf[u]);
