@@ -1,9 +1,10 @@
 /*
- * moe.h -- C ABI of a dropless Mixture-of-Experts SwiGLU FFN layer forward on
- * one NVIDIA GB300 (sm_103a).
+ * moe.h -- C ABI of a dropless Mixture-of-Experts SwiGLU FFN layer on one
+ * NVIDIA GB300 (sm_103a): the forward (bf16, and MXFP8 expert matmuls) and the
+ * backward of a training step.
  *
  * The operation follows "Accelerating dropless MoE training in JAX with NVIDIA
- * Transformer Engine" (aihot.vn/items/70e24b30eb05130d):
+ * Transformer Engine":
  *   - introduction: a learned router activates the Top-K experts per token;
  *   - "How is dropless MoE different from capacity-based MoE?": every token is
  *     processed by its chosen experts whatever the load (no drop, no padding);

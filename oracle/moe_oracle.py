@@ -6,7 +6,7 @@ and reference legs may import it.  It shares no code with the CUDA library
 and never imports it.
 
 Source page: "Accelerating dropless MoE training in JAX with NVIDIA Transformer
-Engine" (aihot.vn/items/70e24b30eb05130d).  Passages followed:
+Engine".  Passages followed:
   * introduction -- a learned router picks the Top-K experts of each token;
   * "How is dropless MoE different from capacity-based MoE?" -- every token is
     processed by the experts it chose, whatever the load: no drop, no padding;

@@ -2,8 +2,8 @@
  * Oracle (test infrastructure only): fp32 router logits of a dropless MoE layer.
  *
  * Source: "Accelerating dropless MoE training in JAX with NVIDIA Transformer
- * Engine" (aihot.vn/items/70e24b30eb05130d), introduction: a learned router
- * scores every expert for every token and the Top-K experts are activated;
+ * Engine", introduction: a learned router scores every expert for every
+ * token and the Top-K experts are activated;
  * section "What are the challenges of MoE training?": the router is a learned
  * component.  The page fixes no arithmetic for the scores; the layer this
  * oracle checks takes fp32 logits, so the score is defined here as the fp32
