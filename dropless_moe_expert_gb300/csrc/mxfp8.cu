@@ -131,11 +131,16 @@ permute_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ topk_idx
             my_r = __ldg(row_of + static_cast<size_t>(t) * K + lane);
             my_e = __ldg(topk_idx + static_cast<size_t>(t) * K + lane);
         }
+        // the next 256 columns' load is in flight while these are quantised and stored
+        const uint4 *xrow = x + static_cast<size_t>(t) * d / 8;
+        uint4 nxt = 8 * lane < d ? __ldg(xrow + lane) : make_uint4(0u, 0u, 0u, 0u);
         for (int c0 = 0; c0 < d; c0 += 256) {
             const bool valid = c0 + 8 * lane < d;  // d is a multiple of 128: whole blocks
+            const uint4 cur = nxt;
+            if (c0 + 256 + 8 * lane < d) nxt = __ldg(xrow + (c0 + 256) / 8 + lane);
             float v[8];
             if (valid) {
-                unpack_bf16x8(__ldg(x + (static_cast<size_t>(t) * d + c0 + 8 * lane) / 8), v);
+                unpack_bf16x8(cur, v);
             } else {
 #pragma unroll
                 for (int i = 0; i < 8; ++i) v[i] = 0.0f;
