@@ -270,7 +270,10 @@ router_wgrad_reduce_kernel(const float *__restrict__ part, const float *__restri
 
 // dx[t] = sum_k dx_perm[row_of[t,k]] + sum_k dl[t,k] Wr^T[idx[t,k]]; one warp
 // per token, fp32 in ascending k, then bf16.  Lane k holds the token's k-th
-// row, expert and dl (K <= 32), handed to every lane by shuffles.
+// row, expert and dl (K <= 32), handed to every lane by shuffles.  KT > 0: K
+// is KT and the K rows' vectors are all loaded before they are summed (KT
+// loads in flight per lane); KT == 0: any K.
+template <int KT>
 __global__ void __launch_bounds__(256)
 dx_kernel(const uint4 *__restrict__ dx_perm, const float *__restrict__ WrT, const int32_t *__restrict__ row_of,
           const int32_t *__restrict__ topk_idx, const float *__restrict__ dl, int T, int K, int E, int TK, int nvec,
@@ -278,13 +281,14 @@ dx_kernel(const uint4 *__restrict__ dx_perm, const float *__restrict__ WrT, cons
     const int lane = threadIdx.x & 31;
     const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int nw = (gridDim.x * blockDim.x) >> 5;
+    const int k_n = KT > 0 ? KT : K;
     for (int t = gw; t < T; t += nw) {
         int my_r = -1, my_e = -1;
         float my_g = 0.0f;
-        if (lane < K) {
-            my_r = row_of[static_cast<size_t>(t) * K + lane];
-            my_e = topk_idx[static_cast<size_t>(t) * K + lane];
-            my_g = dl[static_cast<size_t>(t) * K + lane];
+        if (lane < k_n) {
+            my_r = row_of[static_cast<size_t>(t) * k_n + lane];
+            my_e = topk_idx[static_cast<size_t>(t) * k_n + lane];
+            my_g = dl[static_cast<size_t>(t) * k_n + lane];
         }
         // the loop is warp-uniform (the shuffles need every lane); lanes past
         // the row's end load and store nothing
@@ -292,15 +296,32 @@ dx_kernel(const uint4 *__restrict__ dx_perm, const float *__restrict__ WrT, cons
             const int v = v0 + lane;
             const bool col_ok = v < nvec;
             float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            for (int k = 0; k < K; ++k) {
-                const int r = __shfl_sync(0xffffffffu, my_r, k);
-                if (r < 0 || r >= TK || !col_ok) continue;
-                float xv[8];
-                unpack8(__ldg(dx_perm + static_cast<size_t>(r) * nvec + v), xv);
+            if (KT > 0) {
+                uint4 buf[KT > 0 ? KT : 1];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) acc[i] += xv[i];
+                for (int k = 0; k < KT; ++k) {
+                    const int r = __shfl_sync(0xffffffffu, my_r, k);
+                    const bool ok = col_ok && r >= 0 && r < TK;
+                    buf[k] = ok ? __ldg(dx_perm + static_cast<size_t>(r) * nvec + v) : make_uint4(0u, 0u, 0u, 0u);
+                }
+#pragma unroll
+                for (int k = 0; k < KT; ++k) {
+                    float xv[8];
+                    unpack8(buf[k], xv);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) acc[i] += xv[i];
+                }
+            } else {
+                for (int k = 0; k < k_n; ++k) {
+                    const int r = __shfl_sync(0xffffffffu, my_r, k);
+                    if (r < 0 || r >= TK || !col_ok) continue;
+                    float xv[8];
+                    unpack8(__ldg(dx_perm + static_cast<size_t>(r) * nvec + v), xv);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) acc[i] += xv[i];
+                }
             }
-            for (int k = 0; k < K; ++k) {
+            for (int k = 0; k < k_n; ++k) {
                 const int e = __shfl_sync(0xffffffffu, my_e, k);
                 const float g = __shfl_sync(0xffffffffu, my_g, k);
                 if (e < 0 || e >= E || !col_ok) continue;
@@ -371,8 +392,17 @@ cudaError_t launch_router_wgrad(const uint16_t *x_perm, const float *dl_row, con
 
 cudaError_t launch_dx(const uint16_t *dx_perm, const float *WrT, const int32_t *row_of, const int32_t *topk_idx,
                       const float *dl, int T, int K, int E, int d, uint16_t *dx, cudaStream_t s) {
-    bw::dx_kernel<<<bw::warps_grid(T), 256, 0, s>>>(reinterpret_cast<const uint4 *>(dx_perm), WrT, row_of, topk_idx,
-                                                   dl, T, K, E, T * K, d / 8, reinterpret_cast<uint4 *>(dx));
+    const auto *src = reinterpret_cast<const uint4 *>(dx_perm);
+    auto *dst = reinterpret_cast<uint4 *>(dx);
+    const int g = bw::warps_grid(T), TK = T * K, nv = d / 8;
+    switch (K) {
+        case 1: bw::dx_kernel<1><<<g, 256, 0, s>>>(src, WrT, row_of, topk_idx, dl, T, K, E, TK, nv, dst); break;
+        case 2: bw::dx_kernel<2><<<g, 256, 0, s>>>(src, WrT, row_of, topk_idx, dl, T, K, E, TK, nv, dst); break;
+        case 4: bw::dx_kernel<4><<<g, 256, 0, s>>>(src, WrT, row_of, topk_idx, dl, T, K, E, TK, nv, dst); break;
+        case 6: bw::dx_kernel<6><<<g, 256, 0, s>>>(src, WrT, row_of, topk_idx, dl, T, K, E, TK, nv, dst); break;
+        case 8: bw::dx_kernel<8><<<g, 256, 0, s>>>(src, WrT, row_of, topk_idx, dl, T, K, E, TK, nv, dst); break;
+        default: bw::dx_kernel<0><<<g, 256, 0, s>>>(src, WrT, row_of, topk_idx, dl, T, K, E, TK, nv, dst); break;
+    }
     return cudaGetLastError();
 }
 

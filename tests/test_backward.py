@@ -43,6 +43,9 @@ CASES = [
     Shape(T=1, d=128, E=4, K=2, f=64),
     Shape(T=200, d=128, E=1, K=1, f=128),
     Shape(T=64, d=64, E=8, K=8, f=64),
+    # K values without a specialised input-gradient kernel (3) and with one (6)
+    Shape(T=300, d=128, E=16, K=3, f=128),
+    Shape(T=257, d=192, E=12, K=6, f=128),
 ]
 
 
