@@ -10,4 +10,4 @@ from .moe_oracle import (combine, dispatch_order, expert_counts, expert_ffn, for
                          router_logits_fp64, silu, topk_route)
 from .mxfp8 import (e4m3_decode, e4m3_encode, e4m3_round, forward_mxfp8, mx_dequantize,  # noqa: F401
                     mx_quantize, mx_scale_exponent)
-from .backward import backward, forward_fp64  # noqa: F401
+from .backward import backward, backward_sampled, forward_fp64  # noqa: F401

@@ -117,3 +117,99 @@ def backward(x, Wr, bias, W1, W2, K: int, dy, routing):
         dx += dx_perm[row_of[:, k]]
     return dict(dx=dx, dWr=dWr, dbias=dbias, dW1=dW1, dW2=dW2, dw=dw, dy_perm=dy_perm, dh=dh, da=da,
                 dx_perm=dx_perm, dL=dL, a=a, h=h, y_perm=y_perm)
+
+
+def backward_sampled(x, Wr, bias, W1, W2, K: int, dy, routing, dW1_at=(), dW2_at=(), dx_at=()):
+    """Selected elements of backward()'s gradients, each evaluated from the
+    same definitions with only the rows it needs, for checks at sizes where
+    the full backward is too slow: dW1[e, i, j] for (e, i, j) in dW1_at,
+    dW2[e, i, j] for (e, i, j) in dW2_at and dx[t] for t in dx_at.
+
+    With every value comes S, the sum of the magnitudes of its terms carried
+    through each intermediate that is itself a sum (dh from |dy_perm|·|W2|,
+    the two terms of silu' separately, dw from |dy|·|y_perm|, dl from the
+    softmax's terms), for an error bound that scales with the terms rather
+    than with a result that cancels.  fp64; W1, W2 may be given in fp32.
+    Returns dict(dW1=[(value, S)], dW2=[...], dx=[(row [d], S row [d])])."""
+    x = np.asarray(x, np.float64)
+    Wr = np.asarray(Wr, np.float64)
+    dy = np.asarray(dy, np.float64)
+    idx, w = np.asarray(routing["idx"]), np.asarray(routing["w"], np.float64)
+    offsets, src_tok, row_of = routing["offsets"], routing["src_tok"], routing["row_of"]
+    E, two_f, d = W1.shape
+    f = two_f // 2
+    # the slot k of each row r: row_of[t, k] = r
+    slot = np.zeros(len(src_tok), np.int64)
+    for k in range(K):
+        slot[row_of[:, k]] = k
+
+    def group(e):
+        rows = np.arange(offsets[e], offsets[e + 1])
+        toks = src_tok[rows]
+        return toks, w[toks, slot[rows]]            # the tokens of the group and their gate weights
+
+    out = dict(dW1=[], dW2=[], dx=[])
+    for e, i, j in dW2_at:                           # dW2[e, i, j] = sum_r dy_perm[r, i] h[r, j]
+        toks, wr = group(e)
+        g = x[toks] @ np.asarray(W1[e][j], np.float64)
+        u = x[toks] @ np.asarray(W1[e][f + j], np.float64)
+        h = silu(g) * u
+        dyp = wr * dy[toks, i]
+        out["dW2"].append((float(np.sum(dyp * h)), float(np.sum(np.abs(dyp) * np.abs(h)))))
+    for e, i, j in dW1_at:                           # dW1[e, i, j] = sum_r da[r, i] x_perm[r, j]
+        toks, wr = group(e)
+        c = i % f                                    # the feature of the gate (i < f) or up (i >= f) row
+        g = x[toks] @ np.asarray(W1[e][c], np.float64)
+        u = x[toks] @ np.asarray(W1[e][f + c], np.float64)
+        s = 1.0 / (1.0 + np.exp(-g))
+        dyp = wr[:, None] * dy[toks]                 # dy_perm rows [n, d]
+        w2c = np.asarray(W2[e][:, c], np.float64)
+        dh = dyp @ w2c
+        dh_mag = np.abs(dyp) @ np.abs(w2c)
+        if i < f:
+            da = dh * u * (s + g * s * (1.0 - s))
+            da_mag = dh_mag * np.abs(u) * (np.abs(s) + np.abs(g * s * (1.0 - s)))
+        else:
+            da = dh * g * s
+            da_mag = dh_mag * np.abs(g * s)
+        xj = x[toks, j]
+        out["dW1"].append((float(np.sum(da * xj)), float(np.sum(da_mag * np.abs(xj)))))
+    expert_cache = {}
+
+    def expert(e):                                   # an expert's weights in fp64, converted once
+        if e not in expert_cache:
+            expert_cache[e] = (np.asarray(W1[e], np.float64), np.asarray(W2[e], np.float64))
+        return expert_cache[e]
+
+    for t in dx_at:                                  # dx[t] = sum_k dx_perm[row_of[t,k]] + sum_k dl[t,k] Wr[:, idx[t,k]]
+        dxt = np.zeros(d)
+        sdx = np.zeros(d)
+        dw = np.zeros(K)
+        dw_mag = np.zeros(K)
+        for k in range(K):
+            e = int(idx[t, k])
+            W1e, W2e = expert(e)
+            a = W1e @ x[t]
+            g, u = a[:f], a[f:]
+            s = 1.0 / (1.0 + np.exp(-g))
+            h = silu(g) * u
+            yp = W2e @ h
+            dw[k] = float(dy[t] @ yp)
+            dw_mag[k] = float(np.abs(dy[t]) @ np.abs(yp))
+            dyp = w[t, k] * dy[t]
+            dh = W2e.T @ dyp
+            dh_mag = np.abs(W2e.T) @ np.abs(dyp)
+            da = np.concatenate([dh * u * (s + g * s * (1.0 - s)), dh * g * s])
+            da_mag = np.concatenate([dh_mag * np.abs(u) * (np.abs(s) + np.abs(g * s * (1.0 - s))),
+                                     dh_mag * np.abs(g * s)])
+            dxt += da @ W1e
+            sdx += da_mag @ np.abs(W1e)
+        wt = w[t]
+        dl = wt * (dw - np.sum(wt * dw))
+        dl_mag = wt * (dw_mag + np.sum(wt * dw_mag))
+        for k in range(K):
+            e = int(idx[t, k])
+            dxt += dl[k] * Wr[:, e]
+            sdx += dl_mag[k] * np.abs(Wr[:, e])
+        out["dx"].append((dxt, sdx))
+    return out

@@ -105,3 +105,28 @@ def test_forward_fp64_matches_forward():
     y64 = oracle.forward_fp64(x, Wr, bias, W1, W2, K)
     y = oracle.forward(x.astype(np.float32), Wr.astype(np.float32), bias.astype(np.float32), W1, W2, K)["y"]
     assert np.allclose(y64, y, rtol=1e-5, atol=1e-5)
+
+
+@pytest.mark.parametrize("K", [1, 2, 3])
+def test_sampled_elements_equal_the_full_backward(K):
+    """backward_sampled() evaluates single elements from the definitions with
+    only the rows they need; on a case small enough for backward() every
+    sampled element must equal it, and each S must bound its |value|."""
+    args = _case(T=40, d=16, E=5, K=K, f=12, seed=7)
+    x, Wr, bias, W1, W2, K_, dy = args
+    routing, _ = _routing(x, Wr, bias, K_)
+    full = oracle.backward(x, Wr, bias, W1, W2, K_, dy, routing)
+    f = W1.shape[1] // 2
+    dW1_at = [(e, i, j) for e in range(5) for i in (0, f - 1, f, 2 * f - 1) for j in (0, 15)]
+    dW2_at = [(e, i, j) for e in range(5) for i in (0, 15) for j in (0, f - 1)]
+    dx_at = [0, 17, 39]
+    got = oracle.backward_sampled(x, Wr, bias, W1, W2, K_, dy, routing, dW1_at, dW2_at, dx_at)
+    for (e, i, j), (v, S) in zip(dW1_at, got["dW1"]):
+        assert v == pytest.approx(full["dW1"][e, i, j], rel=1e-10, abs=1e-12)
+        assert S >= abs(v) - 1e-12
+    for (e, i, j), (v, S) in zip(dW2_at, got["dW2"]):
+        assert v == pytest.approx(full["dW2"][e, i, j], rel=1e-10, abs=1e-12)
+        assert S >= abs(v) - 1e-12
+    for t, (v, S) in zip(dx_at, got["dx"]):
+        np.testing.assert_allclose(v, full["dx"][t], rtol=1e-10, atol=1e-12)
+        assert np.all(S >= np.abs(v) - 1e-12)
