@@ -83,20 +83,36 @@ def mx_scale_exponent(amax) -> np.ndarray:
     return np.clip(e, -127, 127).astype(np.int64)
 
 
-def mx_quantize(V):
-    """Blocks of 32 along the last axis of V [..., K] (K a multiple of 32).
-    Returns (codes uint8 [..., K], scale codes uint8 [..., K/32], dequantised
-    fp64 [..., K])."""
-    V = np.asarray(V, np.float64)
-    K = V.shape[-1]
-    assert K % BLOCK == 0
-    blocks = V.reshape(V.shape[:-1] + (K // BLOCK, BLOCK))
+def _mx_quantize_rows(V):
+    """mx_quantize of a 2-D block of rows [R, K]."""
+    R, K = V.shape
+    blocks = V.reshape(R, K // BLOCK, BLOCK)
     e = mx_scale_exponent(np.max(np.abs(blocks), axis=-1))
     X = np.ldexp(1.0, e)[..., None]
     q = e4m3_round(blocks / X)
-    codes = e4m3_encode(q).reshape(V.shape)
-    deq = (q * X).reshape(V.shape)
-    return codes, (e + 127).astype(np.uint8), deq
+    return e4m3_encode(q).reshape(R, K), (e + 127).astype(np.uint8), (q * X).reshape(R, K)
+
+
+def mx_quantize(V):
+    """Blocks of 32 along the last axis of V [..., K] (K a multiple of 32).
+    Returns (codes uint8 [..., K], scale codes uint8 [..., K/32], dequantised
+    fp64 [..., K]).  Every block lies within one row, so the rows are taken a
+    few thousand elements' worth at a time (the same values; only the size of
+    numpy's temporaries changes)."""
+    V = np.asarray(V, np.float64)
+    K = V.shape[-1]
+    assert K % BLOCK == 0
+    lead = V.shape[:-1]
+    V2 = V.reshape(-1, K)
+    R = V2.shape[0]
+    codes = np.empty((R, K), np.uint8)
+    scales = np.empty((R, K // BLOCK), np.uint8)
+    deq = np.empty((R, K), np.float64)
+    step = max(1, (1 << 20) // max(K, 1))
+    for r0 in range(0, R, step):
+        r1 = min(R, r0 + step)
+        codes[r0:r1], scales[r0:r1], deq[r0:r1] = _mx_quantize_rows(V2[r0:r1])
+    return codes.reshape(V.shape), scales.reshape(lead + (K // BLOCK,)), deq.reshape(V.shape)
 
 
 def mx_dequantize(codes, scale_codes) -> np.ndarray:
@@ -106,6 +122,45 @@ def mx_dequantize(codes, scale_codes) -> np.ndarray:
     s = np.asarray(scale_codes, np.uint8).astype(np.int64) - 127
     vals = e4m3_decode(c).reshape(c.shape[:-1] + (K // BLOCK, BLOCK))
     return (vals * np.ldexp(1.0, s)[..., None]).reshape(c.shape)
+
+
+def expert_ffn_mxfp8(x_rows, W1d_e, W2d_e):
+    """One expert's MXFP8 SwiGLU FFN on a few of its token rows, for checks at
+    full size.  x_rows [n, d] (bf16 values), W1d_e [2f, d] and W2d_e [d, f]
+    the expert's dequantised MXFP8 weights (mx_quantize(...)[2]).  A row's
+    result depends only on its own token and the expert: the token row is
+    quantised in blocks of 32 along d, h = silu(g) * u in fp64 from the
+    dequantised operands, h quantised in blocks of 32 along f, and
+    y_perm = dequantised h times W2d_e^T in fp64.  Returns a dict with xq, xs,
+    h, hq, hs, hd and y_perm."""
+    f = np.asarray(W1d_e).shape[0] // 2
+    xq, xs, xd = mx_quantize(np.asarray(x_rows, np.float32))
+    a = xd @ np.asarray(W1d_e, np.float64).T
+    h = silu(a[:, :f]) * a[:, f:]
+    hq, hs, hd = mx_quantize(h)
+    y_perm = hd @ np.asarray(W2d_e, np.float64).T
+    return dict(xq=xq, xs=xs, h=h, hq=hq, hs=hs, hd=hd, y_perm=y_perm)
+
+
+def forward_mxfp8_tokens(x_rows, L_rows, K: int, expert_weights):
+    """y with MXFP8 expert matmuls for a few tokens, from their own fp32
+    logits L_rows [n, E] and activations x_rows [n, d]; expert_weights(e) ->
+    (W1d_e, W2d_e) dequantised.  Returns (idx, w, per-slot results
+    [n][K] of expert_ffn_mxfp8 for one row, y [n, d])."""
+    idx, w = topk_route(L_rows, K)
+    n = idx.shape[0]
+    slots = [[None] * K for _ in range(n)]
+    for e in sorted(set(int(v) for v in np.asarray(idx).ravel())):
+        W1d_e, W2d_e = expert_weights(e)
+        at = [(i, k) for i in range(n) for k in range(K) if idx[i, k] == e]
+        res = expert_ffn_mxfp8(np.asarray(x_rows)[[i for i, _ in at]], W1d_e, W2d_e)
+        for j, (i, k) in enumerate(at):
+            slots[i][k] = {name: val[j] for name, val in res.items()}
+    y = np.zeros((n, np.asarray(x_rows).shape[1]))
+    for i in range(n):
+        for k in range(K):
+            y[i] += w[i, k] * slots[i][k]["y_perm"]
+    return idx, w, slots, y
 
 
 def forward_mxfp8(x, Wr, bias, W1, W2, K: int, nthreads: int | None = None):

@@ -206,3 +206,53 @@ def compare_small(x, w, K):
     check_rounded(to_np(v["h"])[rg], ref["h"][ro], "h")
     check_output(to_np(v["y_perm"])[rg], ref["y_perm"][ro], "y_perm")
     return check_output(to_np(y)[same], ref["y"][same], "y")
+
+
+# ------------------------------------------------------------ MXFP8 scale atoms
+def unpack_plain_atoms(buf, R, K):
+    """Scale bytes [R, K/32] of a plain matrix from its 512-byte atoms (128
+    rows x 4 scale columns each; row r's 4 bytes at (r % 32) * 16 +
+    ((r % 128) // 32) * 4)."""
+    ns = K // 128
+    r = np.arange(R)
+    out = np.zeros((R, K // 32), np.uint8)
+    for ks in range(ns):
+        base = ((r // 128) * ns + ks) * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4
+        for b in range(4):
+            out[:, ks * 4 + b] = buf[base + b]
+    return out
+
+
+def unpack_group_atoms(buf, offsets, K, rows=None):
+    """Scale bytes [len(rows), K/32] of rows grouped by expert (each group's
+    row blocks start at its first row); all TK rows when rows is None."""
+    ns = K // 128
+    offsets = np.asarray(offsets, np.int64)
+    counts = np.diff(offsets)
+    rbp = np.concatenate([[0], np.cumsum((counts + 127) // 128)])[:-1]
+    r = np.arange(int(offsets[-1])) if rows is None else np.asarray(rows, np.int64)
+    e = np.searchsorted(offsets, r, side="right") - 1
+    i = r - offsets[e]
+    rb = rbp[e] + i // 128
+    j = i % 128
+    out = np.zeros((r.shape[0], K // 32), np.uint8)
+    for ks in range(ns):
+        base = (rb * ns + ks) * 512 + (j % 32) * 16 + (j // 32) * 4
+        for b in range(4):
+            out[:, ks * 4 + b] = buf[base + b]
+    return out
+
+
+def check_mx_rounded(hd_gpu, h_ref, hs_ref, what="h"):
+    """A value computed in fp32 and stored as MXFP8 (hd_gpu, dequantised)
+    against the oracle's fp64 value before its quantisation: within half an
+    E4M3 ulp of its block (2^-4 relative in the normal range, 2^-10 of the
+    block scale below it, the scale allowed one binade above the oracle's
+    scale code hs_ref)."""
+    hd_gpu = np.asarray(hd_gpu, np.float64)
+    h_ref = np.asarray(h_ref, np.float64)
+    assert np.all(np.isfinite(hd_gpu)), f"{what}: non-finite values"
+    X = np.repeat(np.ldexp(1.0, np.asarray(hs_ref).astype(np.int64) - 127), 32, axis=-1)
+    bound = 2.0 ** -4 * np.abs(h_ref) * (1 + 1e-4) + 2.0 ** -9 * X + 1e-6 * np.sqrt(np.mean(h_ref ** 2))
+    excess = np.abs(hd_gpu - h_ref) - bound
+    assert np.all(excess <= 0), f"{what}: {int((excess > 0).sum())} elements beyond the E4M3 rounding bound"

@@ -17,42 +17,11 @@ import torch
 import oracle
 from workloads import Shape, make_tokens, make_weights
 
-from _helpers import check_logits, check_output, check_routing, to_np
+from _helpers import (check_logits, check_mx_rounded, check_output, check_routing, to_np, unpack_group_atoms,
+                      unpack_plain_atoms)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
-
-
-def unpack_plain_atoms(buf, R, K):
-    """Scale bytes [R, K/32] of a plain matrix from its 512-byte atoms."""
-    ns = K // 128
-    r = np.arange(R)
-    out = np.zeros((R, K // 32), np.uint8)
-    for ks in range(ns):
-        base = ((r // 128) * ns + ks) * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4
-        for b in range(4):
-            out[:, ks * 4 + b] = buf[base + b]
-    return out
-
-
-def unpack_group_atoms(buf, offsets, K):
-    """Scale bytes [TK, K/32] of rows grouped by expert (row blocks from each
-    group's first row)."""
-    ns = K // 128
-    counts = np.diff(offsets)
-    rbp = np.concatenate([[0], np.cumsum((counts + 127) // 128)])[:-1]
-    TK = int(offsets[-1])
-    r = np.arange(TK)
-    e = np.searchsorted(offsets, r, side="right") - 1
-    i = r - offsets[e]
-    rb = rbp[e] + i // 128
-    j = i % 128
-    out = np.zeros((TK, K // 32), np.uint8)
-    for ks in range(ns):
-        base = (rb * ns + ks) * 512 + (j % 32) * 16 + (j // 32) * 4
-        for b in range(4):
-            out[:, ks * 4 + b] = buf[base + b]
-    return out
 
 
 @pytest.mark.parametrize("R,K", [(300, 256), (128, 128), (1, 384), (257, 512)])
@@ -118,11 +87,7 @@ def test_layer_matches_mxfp8_oracle(s):
     hs = unpack_group_atoms(to_np(v["sfh"]), offs, s.f)
     hd = oracle.mx_dequantize(to_np(v["hq"]), hs)[rg]
     h = ref["h"][ro]
-    assert np.all(np.isfinite(hd))
-    X = np.repeat(np.ldexp(1.0, ref["hs"][ro].astype(np.int64) - 127), 32, axis=1)
-    bound = 2.0 ** -4 * np.abs(h) * (1 + 1e-4) + 2.0 ** -9 * X + 1e-6 * np.sqrt(np.mean(h ** 2))
-    excess = np.abs(hd - h) - bound
-    assert np.all(excess <= 0), f"h: {int((excess > 0).sum())} elements beyond the E4M3 rounding bound"
+    check_mx_rounded(hd, h, ref["hs"][ro])
     codes_equal = np.mean(to_np(v["hq"])[rg] == ref["hq"][ro])
     check_output(to_np(v["y_perm"])[rg], ref["y_perm"][ro], "y_perm")
     r = check_output(to_np(y)[same], ref["y"][same], "y")

@@ -138,3 +138,37 @@ def test_forward_error_against_the_bf16_oracle_is_the_quantisation_error():
     y = oracle.forward_mxfp8(x, Wr, bias, W1, W2, K)["y"]
     rel = np.linalg.norm(y - ref) / np.linalg.norm(ref)
     assert 1e-3 < rel < 0.1       # E4M3 keeps 3 mantissa bits: a few percent, never zero
+
+
+def test_quantize_in_row_chunks_equals_one_pass():
+    # 70000 rows of 32: three chunks, the last one partial, and a 3-D shape
+    g = np.random.default_rng(4)
+    V = g.standard_normal((2, 35000, 32)) * np.exp(2 * g.standard_normal((2, 35000, 1)))
+    codes, scales, deq = oracle.mx_quantize(V)
+    c1, s1, d1 = mx._mx_quantize_rows(V.reshape(-1, 32))
+    assert codes.shape == V.shape and scales.shape == (2, 35000, 1)
+    assert np.array_equal(codes.reshape(-1, 32), c1)
+    assert np.array_equal(scales.reshape(-1, 1), s1)
+    assert np.array_equal(deq.reshape(-1, 32), d1)
+
+
+@pytest.mark.parametrize("K", [1, 2, 4])
+def test_per_token_evaluation_equals_the_whole_forward(K):
+    x, Wr, bias, W1, W2, _ = _tiny_case(False)
+    ref = oracle.forward_mxfp8(x, Wr, bias, W1, W2, K)
+    _, _, W1d = oracle.mx_quantize(W1)
+    _, _, W2d = oracle.mx_quantize(W2)
+    toks = np.array([0, 3, x.shape[0] - 1])
+    idx, w, slots, y = oracle.forward_mxfp8_tokens(x[toks], ref["logits"][toks], K, lambda e: (W1d[e], W2d[e]))
+    assert np.array_equal(idx, ref["idx"][toks])
+    assert np.array_equal(w, ref["w"][toks])
+    for i, t in enumerate(toks):
+        assert np.array_equal(slots[i][0]["xq"], ref["xq"][t])
+        assert np.array_equal(slots[i][0]["xs"], ref["xs"][t])
+        for k in range(K):
+            r = ref["row_of"][t, k]
+            assert np.allclose(slots[i][k]["h"], ref["h"][r], rtol=1e-12, atol=1e-12)
+            assert np.array_equal(slots[i][k]["hq"], ref["hq"][r])
+            assert np.array_equal(slots[i][k]["hs"], ref["hs"][r])
+            assert np.allclose(slots[i][k]["y_perm"], ref["y_perm"][r], rtol=1e-12, atol=1e-12)
+    assert np.allclose(y, ref["y"][toks], rtol=1e-12, atol=1e-12)
