@@ -299,7 +299,7 @@ __device__ __forceinline__ void epilogue_tile(const Params &p, const CUtensorMap
                 for (int k = 0; k < 2; ++k) {
                     const float gv = __uint_as_float(g[2 * i + k]);
                     const float uv = __uint_as_float(u[2 * i + k]);
-                    h2[k] = gv * __frcp_rn(1.0f + __expf(-gv)) * uv;
+                    h2[k] = __fdividef(gv, 1.0f + __expf(-gv)) * uv;  // silu(g) * u
                 }
                 packed[i] = pack_bf16x2(h2[0], h2[1]);
             }
