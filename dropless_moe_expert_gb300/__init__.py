@@ -48,7 +48,7 @@ class _Layout(ctypes.Structure):
 
 class _LayoutBW(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in (
-        "dw", "dl", "dl_row", "dy_perm", "dh", "a", "da", "dx_perm", "WrT", "rw_part", "total")]
+        "dw", "dl", "dl_row", "dy_perm", "dh", "a", "da", "dx_perm", "WrT", "rw_part", "tmaps", "total")]
 
 
 class _LayoutMX(ctypes.Structure):

@@ -72,9 +72,12 @@ cudaError_t launch_router_wgrad(const uint16_t *x_perm, const float *dl_row, con
 cudaError_t launch_dx(const uint16_t *dx_perm, const float *WrT, const int32_t *row_of, const int32_t *topk_idx,
                       const float *dl, int T, int K, int E, int d, uint16_t *dx, cudaStream_t s);
 cudaError_t wgrad_setup(struct GemmLaunch *cfg);
-// D[e] [M, N] fp32 = A[group e]^T . B[group e] for rows grouped by expert, A [TK, M], B [TK, N]
+// D[e] [M, N] fp32 = A[group e]^T . B[group e] for rows grouped by expert, A [TK, M], B [TK, N];
+// `maps` (128-byte aligned) is scratch for WGRAD_MAP_BYTES * E bytes of per-expert tensor maps.  Two launches.
+constexpr size_t WGRAD_MAP_BYTES = 2 * 128;
 cudaError_t launch_wgrad(const uint16_t *A, const uint16_t *B, int M, int N, const int32_t *offsets, int E, int TK,
-                         float *D, const struct GemmLaunch &lc, int *status, uint64_t timeout_ns, cudaStream_t stream);
+                         float *D, void *maps, const struct GemmLaunch &lc, int *status, uint64_t timeout_ns,
+                         cudaStream_t stream);
 
 // Per-device launch shape of the grouped GEMM: SM count, and how many CTA
 // pairs of the pair kernel can be resident at once (0: single-CTA only).

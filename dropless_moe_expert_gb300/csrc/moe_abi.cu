@@ -140,6 +140,7 @@ bool backward_layout(int T, int d, int E, int K, int f, moe_backward_layout_t *L
     L->dx_perm = take(TK * d * 2);
     L->WrT = take(static_cast<size_t>(E) * d * 4);
     L->rw_part = take(moe::router_wgrad_slices(static_cast<int>(TK), E) * (static_cast<size_t>(d) + 1) * 4);
+    L->tmaps = take(moe::WGRAD_MAP_BYTES * static_cast<size_t>(E));
     L->total = o;
     return true;
 }
@@ -226,7 +227,7 @@ const char *moe_status_string(int status) {
     }
 }
 
-int moe_abi_version(void) { return 400; }
+int moe_abi_version(void) { return 410; }
 
 uint64_t moe_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
@@ -701,6 +702,7 @@ moe_status_t moe_backward(const uint16_t *x, const float *Wr, const float *bias,
     uint16_t *dx_perm = reinterpret_cast<uint16_t *>(bv(B.dx_perm));
     float *WrT = reinterpret_cast<float *>(bv(B.WrT));
     float *rw_part = reinterpret_cast<float *>(bv(B.rw_part));
+    void *tmaps = bv(B.tmaps);
     const int TK = T * K;
     const moe::GemmLaunch &g = ds->gemm;
     cudaError_t e = cudaSuccess;
@@ -728,8 +730,9 @@ moe_status_t moe_backward(const uint16_t *x, const float *Wr, const float *bias,
                                 stream, nullptr, true),
        1);
     // weight gradients over each expert's rows: dW2[e] = dy_perm[e]^T h[e], dW1[e] = da[e]^T x_perm[e]
-    go(moe::launch_wgrad(dy_perm, h, d, f, offsets, E, TK, dW2, g, ds->status, kWaitLimitNs, stream), 1);
-    go(moe::launch_wgrad(da, x_perm, 2 * f, d, offsets, E, TK, dW1, g, ds->status, kWaitLimitNs, stream), 1);
+    // (the two share the per-expert tensor-map scratch: stream order separates them)
+    go(moe::launch_wgrad(dy_perm, h, d, f, offsets, E, TK, dW2, tmaps, g, ds->status, kWaitLimitNs, stream), 2);
+    go(moe::launch_wgrad(da, x_perm, 2 * f, d, offsets, E, TK, dW1, tmaps, g, ds->status, kWaitLimitNs, stream), 2);
     // router weights and the input gradient
     go(moe::launch_router_wgrad(x_perm, dl_row, offsets, E, TK, d, rw_part, dWr, dbias, stream), 2);
     go(moe::launch_dx(dx_perm, WrT, row_of, topk_idx, dl, T, K, E, d, dx, stream), 1);

@@ -100,6 +100,23 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const void *tmap, uint64_
         : "memory");
 }
 
+// Tensor maps edited on the device: a copy of a host-encoded map in global
+// memory gets another base address and another extent of dimension 1 (rows),
+// and is then published to the tensor-map proxy (release by the writer,
+// acquire by each thread that loads through it).
+__device__ __forceinline__ void tmap_set_base(void *map, const void *base) {
+    asm volatile("tensormap.replace.tile.global_address.global.b1024.b64 [%0], %1;" ::"l"(map), "l"(base) : "memory");
+}
+__device__ __forceinline__ void tmap_set_rows(void *map, int rows) {
+    asm volatile("tensormap.replace.tile.global_dim.global.b1024.b32 [%0], 1, %1;" ::"l"(map), "r"(rows) : "memory");
+}
+__device__ __forceinline__ void fence_tmap_release() {
+    asm volatile("fence.proxy.tensormap::generic.release.gpu;" ::: "memory");
+}
+__device__ __forceinline__ void fence_tmap_acquire(const void *map) {
+    asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(map) : "memory");
+}
+
 // Non-tensor bulk copy global -> shared (both 16-byte aligned, bytes a
 // multiple of 16) that completes `bytes` of transaction on an mbarrier.
 __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
@@ -113,10 +130,6 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
 // async proxy (TMA stores, tensor-core operand reads).
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-// The same for shared memory that a CTA pair's MMA (issued by the peer) reads.
-__device__ __forceinline__ void fence_proxy_async_smem_cluster() {
-    asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
 }
 // TMA store of one box from shared memory, tracked by the bulk-group counter.
 __device__ __forceinline__ void tma_store_2d(const void *tmap, const void *src, int c_inner, int c_outer) {
@@ -161,10 +174,6 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
 }
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// 16 zero bytes at a shared::cluster address (possibly in the peer CTA).
-__device__ __forceinline__ void st_cluster_zero16(uint32_t cluster_addr) {
-    asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(cluster_addr), "r"(0u) : "memory");
 }
 // Arrive on an mbarrier given by its shared::cluster address (possibly in the peer CTA).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {

@@ -14,9 +14,12 @@
 // runs along the rows, so both operands are MN-major: a stage holds 64 rows
 // (K) of A's 128 columns and B's 256 columns as 64 x 64 TMA boxes (128-byte
 // swizzle), and the MMAs read them with MN-major descriptors -- no transposed
-// copy in memory.  A group's K blocks start at its first row; in its last
-// block the rows past the group (the next expert's rows, or TMA zero fill
-// past TK) are zeroed in shared memory before the MMAs, so they add nothing.
+// copy in memory.  Every expert has its own pair of tensor maps, copies of
+// the host-encoded ones that a one-block kernel moves on the device to the
+// group's first row and cuts to the group's row count (the host never sees
+// the counts).  A group's K blocks then start at row 0 of its maps, and in
+// its last block TMA fills the rows past the group with zeros, so they add
+// nothing and no thread touches the staged tiles.
 //
 // Persistent kernels, one CTA per SM, over tiles (e, row block of D, 256-column
 // block) of every expert, with two 256-column TMEM accumulators so a tile's
@@ -28,10 +31,8 @@
 //  * wgrad_pair_kernel: clusters of 2 CTAs share 256-row tiles through
 //    cta_group::2 MMAs (M=256): each CTA loads 128 columns of A and 128 of B
 //    per stage (32 KB instead of 48 KB for the same MMA work per SM), 5
-//    stages.  Both CTAs' copies complete on CTA 0's full barrier; in a
-//    group's last K block CTA 0's MMA warp zeroes the tail rows in both
-//    CTAs' shared memory (the peer's through shared::cluster stores) before
-//    it issues.
+//    stages.  Both CTAs' copies complete on CTA 0's full barrier, and CTA
+//    0 issues the MMAs.
 #include <algorithm>
 
 #include "kernels.h"
@@ -59,8 +60,7 @@ constexpr int OFF_BARS = OFF_EPI + 4 * 2 * EPI_BUF;
 constexpr int NUM_BARS = 2 * STAGES + 5;  // full, empty, tfull[2], tempty[2], drain
 constexpr int OFF_TMEM = OFF_BARS + NUM_BARS * 8;
 constexpr int OFF_ABORT = OFF_TMEM + 4;
-constexpr int OFF_GOFF = OFF_ABORT + 4;
-constexpr int OFF_GCNT = OFF_GOFF + MAX_E * 4;
+constexpr int OFF_GCNT = OFF_ABORT + 4;
 constexpr int SMEM_BYTES = OFF_GCNT + MAX_E * 4 + 1024;
 constexpr int BOX = 64 * 64 * 2;  // one 64-row x 64-column bf16 box
 static_assert(A_BYTES == 2 * BOX && B_BYTES == 4 * BOX, "a stage is six boxes");
@@ -74,26 +74,25 @@ constexpr int P_OFF_BARS = P_OFF_EPI + 4 * 2 * EPI_BUF;
 constexpr int P_NUM_BARS = 2 * P_STAGES + 5;  // full (CTA 0), empty, tfull[2], tempty[2], drain
 constexpr int P_OFF_TMEM = P_OFF_BARS + P_NUM_BARS * 8;
 constexpr int P_OFF_ABORT = P_OFF_TMEM + 4;
-constexpr int P_OFF_GOFF = P_OFF_ABORT + 4;
-constexpr int P_OFF_GCNT = P_OFF_GOFF + MAX_E * 4;
+constexpr int P_OFF_GCNT = P_OFF_ABORT + 4;
 constexpr int P_SMEM_BYTES = P_OFF_GCNT + MAX_E * 4 + 1024;
 static_assert(P_SMEM_BYTES <= 227 * 1024, "shared memory budget");
 
 struct Params {
     const int32_t *offsets;  // [E+1]
+    const CUtensorMap *maps; // [2E] per expert: A's rows, then B's rows of its group
     int E, TK, M, N, MT, NT;
     float *D;                // [E, M, N]
     int *status;
     uint64_t timeout_ns;
 };
 
-// Group starts and row counts from offsets, clamped to [0, TK] (so no content
-// of offsets sends a load outside the activations); one warp.
-__device__ __forceinline__ void groups(const Params &p, int lane, int *s_goff, int *s_gcnt) {
+// Group row counts from offsets, clamped to [0, TK] as the per-expert maps
+// are; one warp.
+__device__ __forceinline__ void groups(const Params &p, int lane, int *s_gcnt) {
     for (int e = lane; e < p.E; e += 32) {
         const int o0 = min(max(p.offsets[e], 0), p.TK);
         const int o1 = min(max(p.offsets[e + 1], o0), p.TK);
-        s_goff[e] = o0;
         s_gcnt[e] = o1 - o0;
     }
 }
@@ -115,16 +114,35 @@ __device__ __forceinline__ Tile decode(const Params &p, int tile) {
     return t;
 }
 
-// Zeroes rows valid..63 of `nbox` consecutive 64 x 64 boxes (one contiguous
-// byte range per box: a 128-byte row holds all its swizzled chunks); one warp.
-__device__ __forceinline__ void zero_tail(uint8_t *boxes, int nbox, int valid, int lane) {
-    const int zbytes = (BK - valid) * 128;
-#pragma unroll 1
-    for (int b = 0; b < nbox; ++b) {
-        uint8_t *z = boxes + b * BOX + valid * 128;
-        for (int o = lane * 16; o < zbytes; o += 32 * 16)
-            *reinterpret_cast<uint4 *>(z + o) = make_uint4(0u, 0u, 0u, 0u);
+// Per-expert tensor maps: maps[2e] and maps[2e+1] are tmA and tmB moved to
+// the group's first row, with the group's row count as their extent (at
+// least 1 row: an empty group's maps are never used but stay valid).  One
+// thread per expert.
+__global__ void __launch_bounds__(MAX_E)
+wgrad_maps_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                  const uint16_t *A, const uint16_t *B, const int32_t *offsets, int E, int TK, int M, int N,
+                  CUtensorMap *maps) {
+    const int e = threadIdx.x;
+    if (e >= E) return;
+    const int o0 = min(max(offsets[e], 0), TK);
+    const int o1 = min(max(offsets[e + 1], o0), TK);
+    const int start = min(o0, TK - 1);
+    const int rows = max(o1 - o0, 1);
+    CUtensorMap *ma = maps + 2 * e;
+    const uint4 *ta = reinterpret_cast<const uint4 *>(&tmA);
+    const uint4 *tb = reinterpret_cast<const uint4 *>(&tmB);
+    uint4 *da = reinterpret_cast<uint4 *>(ma);
+    uint4 *db = reinterpret_cast<uint4 *>(ma + 1);
+#pragma unroll
+    for (int i = 0; i < static_cast<int>(sizeof(CUtensorMap) / 16); ++i) {
+        da[i] = ta[i];
+        db[i] = tb[i];
     }
+    tmap_set_base(ma, A + static_cast<size_t>(start) * M);
+    tmap_set_rows(ma, rows);
+    tmap_set_base(ma + 1, B + static_cast<size_t>(start) * N);
+    tmap_set_rows(ma + 1, rows);
+    fence_tmap_release();
 }
 
 // One warp's 32 rows of a tile, 32 columns at a time: the fp32 values go to
@@ -167,8 +185,7 @@ __device__ __forceinline__ void epilogue(const Params &p, const CUtensorMap *tm_
 }
 
 __global__ void __launch_bounds__(THREADS, 1)
-wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-             const __grid_constant__ CUtensorMap tmD, const Params p) {
+wgrad_kernel(const __grid_constant__ CUtensorMap tmD, const Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_BARS);
@@ -179,7 +196,6 @@ wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
     uint64_t *drain = tfull + 4;
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(smem + OFF_TMEM);
     volatile int *s_abort = reinterpret_cast<volatile int *>(smem + OFF_ABORT);
-    int *s_goff = reinterpret_cast<int *>(smem + OFF_GOFF);
     int *s_gcnt = reinterpret_cast<int *>(smem + OFF_GCNT);
 
     const int warp = threadIdx.x >> 5;
@@ -196,14 +212,12 @@ wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
         mbar_init(drain, 1);
         *s_abort = 0;
         fence_mbar_init();
-        tma_prefetch_desc(&tmA);
-        tma_prefetch_desc(&tmB);
     }
     if (warp == 1) {
         tmem_alloc(s_tmem, TMEM_COLS);
         tmem_relinquish();
     }
-    if (warp == 2) groups(p, lane, s_goff, s_gcnt);
+    if (warp == 2) groups(p, lane, s_gcnt);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -220,18 +234,23 @@ wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
             for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
                 const Tile t = decode<BM>(p, tile);
                 const int KB = (s_gcnt[t.e] + BK - 1) / BK;
-                const int r0 = s_goff[t.e];
+                const CUtensorMap *ma = p.maps + 2 * t.e;
+                const CUtensorMap *mb = ma + 1;
+                if (KB > 0) {
+                    fence_tmap_acquire(ma);
+                    fence_tmap_acquire(mb);
+                }
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, s_abort, p.status, p.timeout_ns)) { ok = false; break; }
                     uint8_t *sa = smem + stage * STAGE;
                     uint8_t *sb = sa + A_BYTES;
-                    const int row = r0 + kb * BK;
+                    const int row = kb * BK;  // within the group: rows past it read TMA zero fill
                     mbar_arrive_expect_tx(&full[stage], STAGE);
-                    // columns past M or N read TMA zero fill
-                    tma_load_2d(sa, &tmA, &full[stage], t.m0, row);
-                    tma_load_2d(sa + BOX, &tmA, &full[stage], t.m0 + 64, row);
+                    // columns past M or N read TMA zero fill too
+                    tma_load_2d(sa, ma, &full[stage], t.m0, row);
+                    tma_load_2d(sa + BOX, ma, &full[stage], t.m0 + 64, row);
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) tma_load_2d(sb + j * BOX, &tmB, &full[stage], t.n0 + 64 * j, row);
+                    for (int j = 0; j < 4; ++j) tma_load_2d(sb + j * BOX, mb, &full[stage], t.n0 + 64 * j, row);
                     armed_phase[stage] = static_cast<int>(phase);
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
@@ -244,8 +263,7 @@ wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
             }
         }
     } else if (warp == 1) {
-        // The whole warp follows the ring: lane 0 waits and issues, all lanes
-        // zero the rows past a group in its last K block.
+        // The whole warp follows the ring; lane 0 waits and issues.
         constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, true, true);
         uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
         bool ok = true, issued = false;
@@ -263,12 +281,6 @@ wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
                 if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
                 tc_fence_after();
                 uint8_t *sa = smem + stage * STAGE;
-                const int valid = cnt - kb * BK;  // warp-uniform
-                if (valid < BK) {
-                    zero_tail(sa, 6, valid, lane);
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                }
                 if (lane == 0) {
                     const uint32_t a_addr = smem_u32(sa);
                     const uint64_t adesc = smem_desc_mnmajor_sw128(a_addr, BOX);
@@ -327,8 +339,7 @@ wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
 // n0 + 128 r + 127 of B; CTA 0 issues the cta_group::2 MMAs.
 // ======================================================================
 __global__ void __launch_bounds__(THREADS, 1)
-wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                  const __grid_constant__ CUtensorMap tmD, const Params p) {
+wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmD, const Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + P_OFF_BARS);
@@ -339,7 +350,6 @@ wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     uint64_t *drain = tfull + 4;
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(smem + P_OFF_TMEM);
     volatile int *s_abort = reinterpret_cast<volatile int *>(smem + P_OFF_ABORT);
-    int *s_goff = reinterpret_cast<int *>(smem + P_OFF_GOFF);
     int *s_gcnt = reinterpret_cast<int *>(smem + P_OFF_GCNT);
 
     const int warp = threadIdx.x >> 5;
@@ -359,10 +369,8 @@ wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         mbar_init(drain, 1);
         *s_abort = 0;
         fence_mbar_init();
-        tma_prefetch_desc(&tmA);
-        tma_prefetch_desc(&tmB);
     }
-    if (warp == 2) groups(p, lane, s_goff, s_gcnt);
+    if (warp == 2) groups(p, lane, s_gcnt);
     __syncthreads();
     // both CTAs' barriers exist before anything crosses the pair, and before
     // the collective TMEM allocation
@@ -390,21 +398,26 @@ wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             for (int tile = pair; ok && tile < total; tile += npairs) {
                 const Tile t = decode<2 * BM>(p, tile);
                 const int KB = (s_gcnt[t.e] + BK - 1) / BK;
-                const int r0 = s_goff[t.e];
+                const CUtensorMap *ma = p.maps + 2 * t.e;
+                const CUtensorMap *mb = ma + 1;
+                if (KB > 0) {
+                    fence_tmap_acquire(ma);
+                    fence_tmap_acquire(mb);
+                }
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!mbar_wait<true>(&empty[stage], phase ^ 1u, s_abort, p.status, p.timeout_ns)) {
                         ok = false;
                         break;
                     }
                     uint8_t *sa = smem + stage * P_STAGE;
-                    const int row = r0 + kb * BK;
+                    const int row = kb * BK;  // within the group: rows past it read TMA zero fill
                     const uint32_t bar = full0 + 8u * stage;
                     if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * P_STAGE);
-                    // columns past M or N read TMA zero fill
-                    tma_load_2d_pair(sa, &tmA, bar, t.m0 + half, row);
-                    tma_load_2d_pair(sa + BOX, &tmA, bar, t.m0 + half + 64, row);
-                    tma_load_2d_pair(sa + 2 * BOX, &tmB, bar, t.n0 + half, row);
-                    tma_load_2d_pair(sa + 3 * BOX, &tmB, bar, t.n0 + half + 64, row);
+                    // columns past M or N read TMA zero fill too
+                    tma_load_2d_pair(sa, ma, bar, t.m0 + half, row);
+                    tma_load_2d_pair(sa + BOX, ma, bar, t.m0 + half + 64, row);
+                    tma_load_2d_pair(sa + 2 * BOX, mb, bar, t.n0 + half, row);
+                    tma_load_2d_pair(sa + 3 * BOX, mb, bar, t.n0 + half + 64, row);
                     armed_phase[stage] = static_cast<int>(phase);
                     if (++stage == P_STAGES) { stage = 0; phase ^= 1u; }
                 }
@@ -424,10 +437,9 @@ wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             }
         }
     } else if (warp == 1 && rank == 0) {
-        // Waits for both CTAs' bytes, zeroes the rows past a group in its last
-        // K block (in both CTAs), issues the MMAs.  The whole warp takes part.
+        // Waits for both CTAs' bytes and issues the MMAs; the whole warp
+        // follows the ring, lane 0 waits and issues.
         constexpr uint32_t idesc = idesc_bf16_f32(2 * BM, BN, true, true);
-        const uint32_t peer_base = mapa_shared(smem_u32(smem), 1);
         uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
         bool ok = true, issued = false;
         for (int tile = pair; ok && tile < total; tile += npairs) {
@@ -444,19 +456,6 @@ wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
                 tc_fence_after();
                 uint8_t *sa = smem + stage * P_STAGE;
-                const int valid = cnt - kb * BK;  // warp-uniform
-                if (valid < BK) {
-                    zero_tail(sa, 4, valid, lane);
-                    // the same rows of the peer's four boxes
-                    const int zbytes = (BK - valid) * 128;
-                    const uint32_t peer = peer_base + static_cast<uint32_t>(stage * P_STAGE + valid * 128);
-#pragma unroll 1
-                    for (int b = 0; b < 4; ++b)
-                        for (int o = lane * 16; o < zbytes; o += 32 * 16)
-                            st_cluster_zero16(peer + static_cast<uint32_t>(b * BOX + o));
-                    fence_proxy_async_smem_cluster();
-                    __syncwarp();
-                }
                 if (lane == 0) {
                     const uint32_t a_addr = smem_u32(sa);
                     const uint64_t adesc = smem_desc_mnmajor_sw128(a_addr, BOX);
@@ -556,9 +555,11 @@ cudaError_t wgrad_setup(GemmLaunch *cfg) {
 }
 
 cudaError_t launch_wgrad(const uint16_t *A, const uint16_t *B, int M, int N, const int32_t *offsets, int E, int TK,
-                         float *D, const GemmLaunch &lc, int *status, uint64_t timeout_ns, cudaStream_t stream) {
+                         float *D, void *maps, const GemmLaunch &lc, int *status, uint64_t timeout_ns,
+                         cudaStream_t stream) {
     CUtensorMap tmA, tmB, tmD;
-    if (M % 64 != 0 || N % 64 != 0 || TK < 1) return cudaErrorInvalidValue;
+    if (M % 64 != 0 || N % 64 != 0 || TK < 1 || E < 1 || E > wg::MAX_E) return cudaErrorInvalidValue;
+    if (reinterpret_cast<uintptr_t>(maps) % 128 != 0) return cudaErrorInvalidValue;
     // A [TK, M] and B [TK, N] with 64-row x 64-column boxes
     if (!make_tmap(&tmA, A, static_cast<uint64_t>(TK), static_cast<uint64_t>(M), 64, 64)) return cudaErrorInvalidValue;
     if (!make_tmap(&tmB, B, static_cast<uint64_t>(TK), static_cast<uint64_t>(N), 64, 64)) return cudaErrorInvalidValue;
@@ -566,16 +567,21 @@ cudaError_t launch_wgrad(const uint16_t *A, const uint16_t *B, int M, int N, con
     if (!make_tmap_2d(&tmD, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, static_cast<uint64_t>(E) * M,
                       static_cast<uint64_t>(N), 32, 32, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
+    // the per-expert maps first (same stream: the GEMM reads them after)
+    wg::wgrad_maps_kernel<<<1, wg::MAX_E, 0, stream>>>(tmA, tmB, A, B, offsets, E, TK, M, N,
+                                                       static_cast<CUtensorMap *>(maps));
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
     wg::Params p = {};
     p.offsets = offsets;
+    p.maps = static_cast<const CUtensorMap *>(maps);
     p.E = E;
     p.TK = TK;
     p.M = M;
     p.N = N;
     // CTA pairs for D blocks of 256 rows, when D has that many and the
-    // groups are long (the forward GEMMs' rule): with short groups most K
-    // blocks are a group's last, and zeroing the tail in both CTAs costs more
-    // than the pair saves (measured on groups of 128 rows on average)
+    // groups are long (the forward GEMMs' rule): on groups of 128 rows on
+    // average the pair measured slower (each tile's K loop is a few blocks)
     const bool use_pair = lc.wgrad_pairs > 0 && M >= 2 * wg::BM && grouped_gemm_use_pair(TK, E);
     const int rb = use_pair ? 2 * wg::BM : wg::BM;
     p.MT = (M + rb - 1) / rb;
@@ -586,9 +592,9 @@ cudaError_t launch_wgrad(const uint16_t *A, const uint16_t *B, int M, int N, con
     if (use_pair) {
         cudaLaunchAttribute attr[1];
         cudaLaunchConfig_t cfg = pair_config(2 * lc.wgrad_pairs, stream, attr);
-        return cudaLaunchKernelEx(&cfg, wg::wgrad_pair_kernel, tmA, tmB, tmD, p);
+        return cudaLaunchKernelEx(&cfg, wg::wgrad_pair_kernel, tmD, p);
     }
-    wg::wgrad_kernel<<<lc.num_sms, wg::THREADS, wg::SMEM_BYTES, stream>>>(tmA, tmB, tmD, p);
+    wg::wgrad_kernel<<<lc.num_sms, wg::THREADS, wg::SMEM_BYTES, stream>>>(tmD, p);
     return cudaGetLastError();
 }
 

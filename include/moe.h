@@ -327,11 +327,11 @@ moe_status_t moe_forward_mxfp8_host_pipelined(const uint16_t *const *x_hosts, ui
  * forward's grouped GEMM reading W1 and W2 as stored (MN-major operands),
  * the weight gradients on a grouped GEMM whose reduction runs over each
  * expert's own rows, read from the grouped activations in place.  All sums
- * have a fixed order: the gradients are deterministic.  11 kernel launches
- * (12 without `preact`).  */
+ * have a fixed order: the gradients are deterministic.  13 kernel launches
+ * (14 without `preact`).  */
 size_t moe_backward_workspace_size(int T, int d, int E, int K, int f);
 typedef struct {
-    size_t dw, dl, dl_row, dy_perm, dh, a, da, dx_perm, WrT, rw_part, total;
+    size_t dw, dl, dl_row, dy_perm, dh, a, da, dx_perm, WrT, rw_part, tmaps, total;
 } moe_backward_layout_t;
 moe_status_t moe_backward_views(int T, int d, int E, int K, int f, moe_backward_layout_t *layout);
 moe_status_t moe_backward(const uint16_t *x, const float *Wr, const float *bias, const uint16_t *W1,
