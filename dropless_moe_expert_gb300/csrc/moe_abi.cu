@@ -669,7 +669,7 @@ moe_status_t moe_backward(const uint16_t *x, const float *Wr, const float *bias,
     if (!x || !Wr || !W1 || !W2 || !dy || !fwd_workspace || !dx || !dWr || !dbias || !dW1 || !dW2 || !workspace)
         return MOE_ERR_INVALID_ARG;
     if (!aligned(x, 16) || !aligned(W1, 16) || !aligned(W2, 16) || !aligned(dy, 16) || !aligned(dx, 16) ||
-        !aligned(fwd_workspace, 16) || !aligned(workspace, 16) || !aligned(Wr, 4) || !aligned(dWr, 4) ||
+        !aligned(fwd_workspace, 16) || !aligned(workspace, 128) || !aligned(Wr, 4) || !aligned(dWr, 4) ||
         !aligned(dbias, 4) || !aligned(dW1, 16) || !aligned(dW2, 16) || (preact && !aligned(preact, 16)))
         return MOE_ERR_INVALID_ARG;
     moe_status_t st = check_shape(T, d, E, K, f, true, true);

@@ -322,8 +322,10 @@ moe_status_t moe_forward_mxfp8_host_pipelined(const uint16_t *const *x_hosts, ui
  * weights (it holds the routing, x_perm, h and y_perm the backward reuses);
  * `preact` (nullable) the pre-activations a moe_forward_train call saved --
  * when null they are computed again (one more grouped GEMM, into the
- * workspace region `a`); `workspace` holds moe_backward_workspace_size()
- * bytes of scratch (moe_backward_views() gives its regions).  The dgrad GEMMs run on the
+ * workspace region `a`); `workspace` (128-byte aligned) holds
+ * moe_backward_workspace_size() bytes of scratch (moe_backward_views() gives
+ * its regions; `tmaps` holds 256 bytes per expert of tensor maps that the
+ * weight-gradient GEMMs build on the device, one pair per expert group).  The dgrad GEMMs run on the
  * forward's grouped GEMM reading W1 and W2 as stored (MN-major operands),
  * the weight gradients on a grouped GEMM whose reduction runs over each
  * expert's own rows, read from the grouped activations in place.  All sums

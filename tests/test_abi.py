@@ -168,6 +168,7 @@ def test_backward_entry_points_reject_bad_arguments(moe):
     TK = T * K
     assert lay.dy_perm - lay.dl_row >= TK * 4 and lay.da - lay.a >= TK * 2 * f * 2
     assert lay.rw_part - lay.WrT >= d * E * 4
+    assert lay.total - lay.tmaps >= 256 * E and lay.tmaps % 128 == 0   # two 128-byte tensor maps per expert
 
     def bwd(*, x=FAKE, Wr=FAKE, W1=FAKE, dy=FAKE, fws=FAKE, fbytes=nf, pre=None, dx=FAKE, dWr=FAKE, ws=FAKE,
             wbytes=nb, f_=f):
@@ -177,6 +178,7 @@ def test_backward_entry_points_reject_bad_arguments(moe):
     assert bwd(W1=FAKE + 8) == 1          # 16-byte alignment
     assert bwd(Wr=FAKE + 2) == 1          # 4-byte alignment
     assert bwd(pre=FAKE + 8) == 1         # saved pre-activations: 16-byte alignment
+    assert bwd(ws=FAKE + 16) == 1         # workspace: 128-byte alignment (the tensor maps in it)
     assert bwd(f_=60) == 2                # f % 64
     assert bwd(fbytes=nf - 1) == 3 and bwd(wbytes=nb - 1) == 3
     # the training forward and GEMM1 with saved pre-activations
