@@ -50,6 +50,7 @@ CASES = [
     Shape(T=129, d=128, E=256, K=8, f=128),
     Shape(T=2048, d=256, E=4, K=1, f=256),     # groups of several 128-row blocks
     Shape(T=1500, d=128, E=3, K=2, f=640, bias="skew"),
+    Shape(T=300, d=256, E=4, K=2, f=1664),     # GEMM2 reduction long enough for 256-column tiles
 ]
 
 
