@@ -43,6 +43,12 @@ CASES = [
     Shape(T=1, d=128, E=4, K=2, f=64),
     Shape(T=200, d=128, E=1, K=1, f=128),
     Shape(T=64, d=64, E=8, K=8, f=64),
+    # K = E fixes every group at T rows: groups ending exactly on a 64-row K
+    # block, and groups with a single row in their last block (single-CTA
+    # kernels; then CTA pairs, TK >= 384 E)
+    Shape(T=128, d=128, E=2, K=2, f=128),
+    Shape(T=129, d=128, E=2, K=2, f=128),
+    Shape(T=449, d=256, E=2, K=2, f=256),
     # K values without a specialised input-gradient kernel (3) and with one (6)
     Shape(T=300, d=128, E=16, K=3, f=128),
     Shape(T=257, d=192, E=12, K=6, f=128),
