@@ -36,8 +36,15 @@
 //  * Every wait is bounded: on expiry the kernel records a timeout, drains its
 //    copies and MMAs, frees TMEM and returns.
 //
-// Single-CTA variant (grouped_gemm_kernel): 128-row tiles, M=128 x N=256 MMAs,
-// 4 stages of 48 KB.  Used when groups are small (about one row block).
+// Single-CTA variant (grouped_gemm_kernel), used when groups are small (a
+// few row blocks): tiles of up to two 128-row blocks of one group.  A tile
+// with more than 128 rows left in its group takes both row blocks: per K
+// slice two M=128 x N=256 MMAs share the B tile, one into each TMEM
+// accumulator, so the SM moves 64 KB per slice for twice the work (its
+// epilogue then runs after the mainloop, both accumulators being in use).  A
+// tile with at most 128 rows takes one accumulator, and consecutive such
+// tiles alternate, so their epilogues overlap the next mainloop.  3 stages of
+// 64 KB.
 //
 // CTA-pair variant (grouped_gemm_pair_kernel): clusters of 2 CTAs on 2 SMs
 // share a 256-row tile through cta_group::2 MMAs (M=256 x N=256).  Each CTA
@@ -64,10 +71,12 @@ constexpr int BOX_ROWS = 128;  // every K-major TMA box is 128 rows x 64 bf16
 constexpr int BT_BOX = 64 * 64 * 2;  // MN-major B box: 64 K rows x 64 columns
 
 // single-CTA variant
-constexpr int BM = 128;
-constexpr int BAND = 16;       // row blocks per raster band
-constexpr int STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2;
+constexpr int BM = 128;        // rows of one MMA and one accumulator
+constexpr int TILE_ROWS = 2 * BM;
+constexpr int BAND = 8;        // tiles per raster band
+constexpr int STAGES = 3;
+constexpr int A_BLOCK = BM * BK * 2;
+constexpr int A_BYTES = 2 * A_BLOCK;
 constexpr int B_BYTES = BN_ACC * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 
@@ -150,7 +159,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         tmem_alloc(s_tmem, TMEM_COLS);
         tmem_relinquish();
     }
-    if (warp == 2) build_groups<BM>(p, lane, s_off, s_end, s_pre, s_mix);
+    if (warp == 2) build_groups<TILE_ROWS>(p, lane, s_off, s_end, s_pre, s_mix);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -169,7 +178,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             bool ok = true;
             for (int k = 0, tile = round_position(0, blockIdx.x, gridDim.x, mix); ok && tile < total_tiles;
                  ++k, tile = round_position(k, blockIdx.x, gridDim.x, mix)) {
-                const Tile t = decode_tile<BM, BAND>(visit_order(tile, total_tiles, mix), s_pre, s_off, s_end, E, NT);
+                const Tile t =
+                    decode_tile<TILE_ROWS, BAND>(visit_order(tile, total_tiles, mix), s_pre, s_off, s_end, E, NT);
+                const bool two = t.grp_end - t.row0 > BM;  // both row blocks of the tile hold rows
                 static_assert(!(SWIGLU && BT), "the transposed-weight form is a plain GEMM");
                 int brow0, brow1;
                 if (SWIGLU) {
@@ -183,8 +194,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     if (!mbar_wait(&empty[stage], phase ^ 1u, s_abort, p.status, p.timeout_ns)) { ok = false; break; }
                     uint8_t *sa = smem + stage * STAGE_BYTES;
                     uint8_t *sb = sa + A_BYTES;
-                    mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
+                    mbar_arrive_expect_tx(&full[stage], (two ? 2 : 1) * A_BLOCK + B_BYTES);
                     tma_load_2d(sa, &tmA, &full[stage], kb * BK, t.row0);
+                    if (two) tma_load_2d(sa + A_BLOCK, &tmA, &full[stage], kb * BK, t.row0 + BM);
                     if (BT) {
                         // W[e] rows kb*64.., columns of the 256-wide block in 64-wide boxes
                         const int krow = t.e * p.Kdim + kb * BK;
@@ -210,35 +222,54 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     } else if (warp == 1) {
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_bf16_f32(BM, BN_ACC, false, BT);
-            uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+            // acc: the accumulator the next tile starts in; ph[i]: parity of
+            // accumulator i's next use.  A two-block tile takes acc and acc ^ 1
+            // (in that order, as the epilogue drains them) and leaves acc as it
+            // is; a one-block tile takes acc and moves it on.
+            uint32_t stage = 0, phase = 0, acc = 0;
+            uint32_t ph[2] = {0u, 0u};
             bool ok = true;
             bool issued = false;
             for (int k = 0, tile = round_position(0, blockIdx.x, gridDim.x, mix); ok && tile < total_tiles;
                  ++k, tile = round_position(k, blockIdx.x, gridDim.x, mix)) {
-                if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, s_abort, p.status, p.timeout_ns)) { ok = false; break; }
+                const Tile t =
+                    decode_tile<TILE_ROWS, BAND>(visit_order(tile, total_tiles, mix), s_pre, s_off, s_end, E, NT);
+                const bool two = t.grp_end - t.row0 > BM;
+                const uint32_t a0 = acc, a1 = acc ^ 1u;
+                if (!mbar_wait(&tempty[a0], ph[a0] ^ 1u, s_abort, p.status, p.timeout_ns)) { ok = false; break; }
+                if (two && !mbar_wait(&tempty[a1], ph[a1] ^ 1u, s_abort, p.status, p.timeout_ns)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + acc * BN_ACC;
+                const uint32_t d0 = tmem_base + a0 * BN_ACC;
+                const uint32_t d1 = tmem_base + a1 * BN_ACC;
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!mbar_wait(&full[stage], phase, s_abort, p.status, p.timeout_ns)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
-                    const uint64_t adesc = smem_desc_kmajor_sw128(sa);
+                    const uint64_t adesc0 = smem_desc_kmajor_sw128(sa);
+                    const uint64_t adesc1 = smem_desc_kmajor_sw128(sa + A_BLOCK);
                     const uint64_t bdesc = BT ? smem_desc_mnmajor_sw128(sa + A_BYTES, BT_BOX)
                                               : smem_desc_kmajor_sw128(sa + A_BYTES);
 #pragma unroll
                     for (int j = 0; j < BK / UMMA_K; ++j) {
                         // advance 16 elements along K: 32 bytes inside a K-major swizzled
                         // row, 16 rows (2048 bytes) of an MN-major box
-                        umma_bf16(d_tmem, adesc + 2 * j, bdesc + (BT ? 128 : 2) * j, idesc, (kb | j) != 0);
+                        const uint64_t bj = bdesc + (BT ? 128 : 2) * j;
+                        umma_bf16(d0, adesc0 + 2 * j, bj, idesc, (kb | j) != 0);
+                        if (two) umma_bf16(d1, adesc1 + 2 * j, bj, idesc, (kb | j) != 0);
                     }
                     issued = true;
                     umma_commit(&empty[stage]);
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
-                umma_commit(&tfull[acc]);
-                acc ^= 1u;
-                if (acc == 0) acc_phase ^= 1u;
+                umma_commit(&tfull[a0]);
+                ph[a0] ^= 1u;
+                if (two) {
+                    umma_commit(&tfull[a1]);
+                    ph[a1] ^= 1u;
+                } else {
+                    acc = a1;
+                }
             }
             if (!ok && issued) {
                 volatile int no_abort = 0;
@@ -250,19 +281,27 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         const int q = warp & 3;  // TMEM lane quarter this warp may access
         uint8_t *stage = smem + L1::OFF_EPI + (warp - 2) * 2 * EPI_BUF;
         uint32_t sbuf = 0;
-        uint32_t acc = 0, acc_phase = 0;
-        for (int k = 0, tile = round_position(0, blockIdx.x, gridDim.x, mix); tile < total_tiles;
+        uint32_t acc = 0;
+        uint32_t ph[2] = {0u, 0u};  // the MMA thread's accumulator order, mirrored
+        bool ok = true;
+        for (int k = 0, tile = round_position(0, blockIdx.x, gridDim.x, mix); ok && tile < total_tiles;
              ++k, tile = round_position(k, blockIdx.x, gridDim.x, mix)) {
-            const Tile t = decode_tile<BM, BAND>(visit_order(tile, total_tiles, mix), s_pre, s_off, s_end, E, NT);
-            if (!mbar_wait(&tfull[acc], acc_phase, s_abort, p.status, p.timeout_ns)) break;
-            tc_fence_after();
-            const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN_ACC;
-            epilogue_tile<SWIGLU>(p, &tmOut, &tmPre, stage, sbuf, tbase, t.n_blk, t.row0 + q * 32, lane, t.grp_end);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&tempty[acc]);
-            acc ^= 1u;
-            if (acc == 0) acc_phase ^= 1u;
+            const Tile t =
+                decode_tile<TILE_ROWS, BAND>(visit_order(tile, total_tiles, mix), s_pre, s_off, s_end, E, NT);
+            const int nblk = t.grp_end - t.row0 > BM ? 2 : 1;
+            for (int b = 0; b < nblk; ++b) {
+                const uint32_t a = acc ^ static_cast<uint32_t>(b);
+                if (!mbar_wait(&tfull[a], ph[a], s_abort, p.status, p.timeout_ns)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + a * BN_ACC;
+                epilogue_tile<SWIGLU>(p, &tmOut, &tmPre, stage, sbuf, tbase, t.n_blk, t.row0 + b * BM + q * 32, lane,
+                                      t.grp_end);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tempty[a]);
+                ph[a] ^= 1u;
+            }
+            if (nblk == 1) acc ^= 1u;
         }
         if (lane == 0) bulk_wait_all();  // stores done before the CTA's shared memory goes away
     }
