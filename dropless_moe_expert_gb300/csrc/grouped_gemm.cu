@@ -29,7 +29,8 @@
 //    cross the end of the group).
 //  * Shared-memory ring of bf16 tiles (64-wide K slices, 128-byte swizzle)
 //    with full/empty mbarriers; two 256-column fp32 accumulators in TMEM (512
-//    columns) so the epilogue of tile i overlaps the mainloop of tile i+1.
+//    columns) so the epilogue of tile i overlaps the mainloop of tile i+1
+//    (except after a single-CTA tile of two row blocks, which uses both).
 //  * Tiles are ordered expert by expert; inside an expert, bands of row
 //    blocks sweep all column blocks, so concurrent CTAs share each weight tile
 //    through L2 and the band's activation rows stay L2-resident.
