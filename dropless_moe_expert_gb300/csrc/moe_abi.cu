@@ -227,7 +227,7 @@ const char *moe_status_string(int status) {
     }
 }
 
-int moe_abi_version(void) { return 410; }
+int moe_abi_version(void) { return 401; }
 
 uint64_t moe_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 

@@ -44,7 +44,7 @@ def test_status_strings(moe):
         s = moe.lib.moe_status_string(code).decode()
         assert s.startswith("MOE_")
     assert moe.lib.moe_status_string(99).decode() == "unknown moe_status_t"
-    assert moe.lib.moe_abi_version() == 410
+    assert moe.lib.moe_abi_version() == 401
 
 
 def test_workspace_sizes(moe):
