@@ -131,12 +131,6 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
-// TMA store of one box from shared memory, tracked by the bulk-group counter.
-__device__ __forceinline__ void tma_store_2d(const void *tmap, const void *src, int c_inner, int c_outer) {
-    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(tmap),
-                 "r"(smem_u32(src)), "r"(c_inner), "r"(c_outer)
-                 : "memory");
-}
 // L2 policy that marks lines first in line for eviction.
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     uint64_t pol;
