@@ -97,3 +97,35 @@ def test_training_step_graph_replays_match_eager():
             if a.dtype == torch.bfloat16:
                 a, b = a.view(torch.int16), b.view(torch.int16)
             assert torch.equal(a, b), (seed, k)
+
+
+def test_full_size_skew_graph_replays_match_eager():
+    """The skew workload at full size (T=32768, d=4096, E=64, K=6, f=1536):
+    one captured graph replayed on re-seeded tokens, each replay bitwise equal
+    to an eager call on the same tokens (the eager layer is checked against
+    the oracle at this size in test_parity.py), with different routings."""
+    from workloads import shape
+    s = shape("skew")
+    w = make_weights(s, seed=0, device="cuda")
+    layer = moe.MoELayer(w.Wr, w.bias, w.W1, w.W2, s.K, s.T)
+    eager = moe.MoELayer(w.Wr, w.bias, w.W1, w.W2, s.K, s.T)
+    x_static = make_tokens(s, seed=0, device="cuda")
+    y_static = torch.empty_like(x_static)
+    layer(x_static, out=y_static)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        layer(x_static, out=y_static)
+    counts = []
+    for seed in (1, 2, 3):
+        x = make_tokens(s, seed=seed, device="cuda")
+        x_static.copy_(x)
+        layer.workspace.fill_(0xFF)
+        y_static.fill_(float("nan"))
+        graph.replay()
+        y_eager = eager(x)
+        torch.cuda.synchronize()
+        assert moe.device_status() == 0
+        assert torch.equal(y_static.view(torch.int16), y_eager.view(torch.int16)), f"replay seed {seed}"
+        counts.append(tuple(layer.views(s.T)["counts"].cpu().tolist()))
+    assert len(set(counts)) == len(counts), "replays should see different routings"
