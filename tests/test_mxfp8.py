@@ -118,3 +118,38 @@ def test_rejects_dims_not_multiple_of_128():
     assert moe.lib.moe_forward_mxfp8_workspace_size(64, 192, 8, 2, 256) == 0
     assert moe.lib.moe_forward_mxfp8_workspace_size(64, 256, 8, 2, 192) == 0
     assert moe.mxfp8_scales_size(10, 64) == 0
+
+
+@pytest.mark.parametrize("s", [Shape(T=1500, d=128, E=16, K=2, f=256, bias="skew"), "qwen"],
+                         ids=["skew_small", "qwen_full"])
+def test_graph_replays_match_eager(s):
+    """The MXFP8 layer captured once in a CUDA graph and replayed on re-seeded
+    tokens: each replay is bitwise equal to an eager call on the same tokens
+    (no routing-dependent value frozen at capture), with different routings."""
+    import dropless_moe_expert_gb300 as moe
+    from workloads import shape
+    s = shape(s)
+    w = make_weights(s, seed=0, device=DEV)
+    wd = (w.Wr, w.bias, w.W1, w.W2)
+    layer = moe.MoELayerMXFP8(*wd, s.K, s.T)
+    eager = moe.MoELayerMXFP8(*wd, s.K, s.T)
+    x_static = make_tokens(s, seed=0, device=DEV)
+    y_static = torch.empty_like(x_static)
+    layer(x_static, out=y_static)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        layer(x_static, out=y_static)
+    counts = []
+    for seed in (1, 2, 3):
+        x = make_tokens(s, seed=seed, device=DEV)
+        x_static.copy_(x)
+        layer.workspace.fill_(0xFF)
+        y_static.fill_(float("nan"))
+        graph.replay()
+        y_eager = eager(x)
+        torch.cuda.synchronize()
+        assert moe.device_status() == 0
+        assert torch.equal(y_static.view(torch.int16), y_eager.view(torch.int16)), f"replay seed {seed}"
+        counts.append(tuple(layer.views(s.T)["counts"].cpu().tolist()))
+    assert len(set(counts)) == len(counts), "replays should see different routings"
