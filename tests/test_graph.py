@@ -57,16 +57,20 @@ def test_graph_replay_with_new_routing(s):
     assert len(set(seen_counts)) == len(seen_counts), "replays should see different routings"
 
 
-def test_training_step_graph_replays_match_eager():
+@pytest.mark.parametrize("name", ["small", "dsv3", "mixtral"])
+def test_training_step_graph_replays_match_eager(name):
     """The training step -- moe_forward_train (saving the pre-activations) then
     moe_backward -- captured once and replayed with new tokens and output
     gradients: the gradients equal an eager run's bit for bit (the backward
-    reads every count on the device too)."""
-    s = Shape(T=300, d=256, E=16, K=4, f=128, bias="normal_0.5")
-    w = make_weights(s, seed=0, device="cpu")
-    wd = [t.cuda() for t in (w.Wr, w.bias, w.W1, w.W2)]
+    reads every count on the device too, and rebuilds its per-expert tensor
+    maps on the device every replay).  At a small shape and at the full
+    DSv3- and Mixtral-shaped workloads (single-CTA and CTA-pair kernels)."""
+    from workloads import shape
+    s = Shape(T=300, d=256, E=16, K=4, f=128, bias="normal_0.5") if name == "small" else shape(name)
+    w = make_weights(s, seed=0, device="cuda")
+    wd = [w.Wr, w.bias, w.W1, w.W2]
     layer = moe.MoELayer(*wd, s.K, s.T)
-    x_static = make_tokens(s, seed=0, device="cpu").cuda()
+    x_static = make_tokens(s, seed=0, device="cuda")
     dy_static = torch.randn((s.T, s.d), device="cuda").to(torch.bfloat16)
     y_static = torch.empty_like(x_static)
     layer(x_static, out=y_static, save_preact=True)   # set-up (buffers, library state) outside capture
@@ -79,7 +83,7 @@ def test_training_step_graph_replays_match_eager():
         layer.backward(x_static, dy_static, grads=grads, workspace=ws)
     eager = moe.MoELayer(*wd, s.K, s.T)
     for seed in (1, 2, 3):
-        x_new = make_tokens(s, seed=seed, device="cpu").cuda()
+        x_new = make_tokens(s, seed=seed, device="cuda")
         g = torch.Generator(device="cuda").manual_seed(seed)
         dy_new = torch.randn((s.T, s.d), device="cuda", generator=g).to(torch.bfloat16)
         x_static.copy_(x_new)
