@@ -60,3 +60,20 @@ def test_pipelined_mxfp8_matches_forward():
     for x, y in zip(xs, ys):
         ref = layer(x.to(DEV)).cpu()
         assert torch.equal(y.view(torch.int16), ref.view(torch.int16))
+
+
+def test_pipelined_full_size_skew():
+    """The skew workload at full size (T=32768, d=4096: 268 MB of x and of y
+    per batch), three batches: each equal to the device forward bit for bit."""
+    import dropless_moe_expert_gb300 as moe
+    from workloads import shape
+    s = shape("skew")
+    w = make_weights(s, seed=0, device=DEV)
+    xs = [make_tokens(s, seed=40 + i, device=DEV).cpu().pin_memory() for i in range(3)]
+    ys = [torch.full((s.T, s.d), float("nan"), dtype=torch.bfloat16).pin_memory() for _ in xs]
+    moe.forward_host_pipelined(xs, ys, w.Wr, w.bias, w.W1, w.W2, s.K)
+    torch.cuda.synchronize()
+    assert moe.device_status() == 0
+    for x, y in zip(xs, ys):
+        ref = moe.forward(x.to(DEV), w.Wr, w.bias, w.W1, w.W2, s.K).cpu()
+        assert torch.equal(y.view(torch.int16), ref.view(torch.int16))
