@@ -2,20 +2,28 @@
 """Benchmark of the dropless MoE layer forward on GB300.
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
-                [--config mixtral|dsv3|qwen|skew|tiny] [--precision bf16|mxfp8]
+                [--config skew|mixtral|dsv3|qwen|tiny] [--extra-configs LIST]
+                [--precision bf16|mxfp8] [--backward] [--fused-combine]
 
 One step = one pass of the whole forward (router logits, top-K routing +
 histogram/scan/dispatch order, permute, grouped GEMM1 + SwiGLU, grouped GEMM2,
 weighted unpermute/combine) over one batch of T tokens, through the C ABI.
-Default workload: the Mixtral-8x7B-shaped layer (T=8192, d=4096, E=8, K=2,
-f=14336), seeded synthetic bf16 data.  Under torchrun every rank runs an
-independent replica on its own tokens (the forward has no cross-token
-dependency, so there is no collective): weak scaling.
+The steps alternate between two resident token batches, so consecutive steps
+route differently.  Default workload: the extreme-skew layer (T=32768,
+d=4096, E=64, K=6, f=1536), the one with the most work per step; the
+Mixtral-, DeepSeek-V3- and Qwen-shaped layers are then timed on the device in
+the same run and reported under `other_configs`.  Seeded synthetic bf16
+data.  Under torchrun every rank runs an independent replica on its own
+tokens (the forward has no cross-token dependency, so there is no
+collective): weak scaling.
 
 Prints one JSON line (rank 0).  `value` is useful TFLOP/s = 6*T*K*d*f per
 step (only the valid rows of the two grouped GEMMs count), aggregated over
 ranks; per-kernel durations come from CUDA events on the launching stream
-inside the timed region.  `--impl reference` times the oracle (plain CPU
+inside the timed region.  Clocks are sampled through NVML's query calls
+inside the timed region.  The roofline fraction of the dominant GEMM is
+given against both measured bf16 peaks; `frac` takes the burst figure for a
+timed region under one second and the sustained one otherwise.  `--impl reference` times the oracle (plain CPU
 implementation, fp64) on a bounded sample of the same workload.
 
 `--precision mxfp8` runs the expert matmuls with MXFP8 block scaling (E4M3
@@ -81,51 +89,117 @@ def _traffic_record(kernel: str, workload: str):
 
 
 class ClockSampler:
-    def __init__(self, gpu_index: int):
-        self.proc = None
-        self.path = None
+    """SM clock, power and clock-event reasons sampled DURING the timed region.
+
+    A background thread queries NVML (libnvidia-ml, the driver's library)
+    every `period_s` through read-only calls: nvmlDeviceGetClockInfo,
+    nvmlDeviceGetMaxClockInfo, nvmlDeviceGetPowerUsage and the current
+    clock-event reasons.  No setting of the GPU is changed.  The device is
+    found by its UUID (else PCI bus id, else index), so the sample is of the
+    GPU this process runs on whatever CUDA_VISIBLE_DEVICES holds.  Without
+    NVML it falls back to polling nvidia-smi every 100 ms."""
+
+    # clock-event reason bits (nvml.h): the ones a timing must record
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown"}
+
+    def __init__(self, cuda_index: int, period_s: float = 0.004):
+        import ctypes
+        import threading
+        self.period = period_s
+        self.rows = []          # (sm_mhz, power_w, reason_bits)
+        self.max_mhz = None
+        self.source = None
+        self._stop = threading.Event()
+        self._thread = None
+        self._proc = None
+        self._nvml = None
+        self._h = None
         try:
-            fd, self.path = tempfile.mkstemp(prefix="clocks", suffix=".csv")
-            os.close(fd)
-            self.fh = open(self.path, "w")
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(gpu_index),
-                 "--query-gpu=clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
-                stdout=self.fh, stderr=subprocess.DEVNULL)
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit_v2 failed")
+            h = ctypes.c_void_p()
+            props = torch.cuda.get_device_properties(cuda_index)
+            ok = False
+            uuid = getattr(props, "uuid", None)
+            if uuid is not None:
+                key = str(uuid)
+                key = key if key.startswith("GPU-") else "GPU-" + key
+                ok = nv.nvmlDeviceGetHandleByUUID(key.encode(), ctypes.byref(h)) == 0
+            if not ok and hasattr(props, "pci_bus_id"):
+                bus = "%08x:%02x:%02x.0" % (getattr(props, "pci_domain_id", 0), props.pci_bus_id,
+                                            getattr(props, "pci_device_id", 0))
+                ok = nv.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(h)) == 0
+            if not ok:
+                ok = nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(cuda_index), ctypes.byref(h)) == 0
+            if not ok:
+                raise OSError("no NVML handle for the device")
+            self._reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
+            mx = ctypes.c_uint(0)
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:   # NVML_CLOCK_SM
+                self.max_mhz = float(mx.value)
+            self._nvml, self._h, self._ct = nv, h, ctypes
+            self.source = f"NVML query every {period_s * 1e3:.0f} ms in a thread of the bench process"
         except Exception:
-            self.proc = None
+            self._nvml = None
+
+    def _sample_nvml(self):
+        ct, nv, h = self._ct, self._nvml, self._h
+        mhz, mw, bits = ct.c_uint(0), ct.c_uint(0), ct.c_ulonglong(0)
+        while not self._stop.is_set():
+            if nv.nvmlDeviceGetClockInfo(h, 1, ct.byref(mhz)) == 0:
+                p = mw.value / 1e3 if nv.nvmlDeviceGetPowerUsage(h, ct.byref(mw)) == 0 else None
+                r = bits.value if self._reasons_fn(h, ct.byref(bits)) == 0 else 0
+                self.rows.append((float(mhz.value), p, int(r)))
+            self._stop.wait(self.period)
+
+    def start(self):
+        import threading
+        if self._nvml is not None:
+            self._thread = threading.Thread(target=self._sample_nvml, daemon=True)
+            self._thread.start()
+            return self
+        try:
+            self._proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.source = "nvidia-smi -lms 100"
+        except Exception:
+            self._proc = None
+        return self
 
     def stop(self):
-        if self.proc is None:
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join(timeout=5)
+        elif self._proc is not None:
+            self._proc.terminate()
+            try:
+                out, _ = self._proc.communicate(timeout=5)
+            except Exception:
+                self._proc.kill()
+                out = ""
+            for line in out.splitlines():
+                parts = [q.strip() for q in line.split(",")]
+                try:
+                    self.max_mhz = float(parts[1])
+                    self.rows.append((float(parts[0]), float(parts[2]), int(parts[3], 16)))
+                except (ValueError, IndexError):
+                    continue
+        else:
             return None
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except Exception:
-            self.proc.kill()
-        self.fh.close()
-        rows = []
-        with open(self.path) as fh:
-            for line in fh:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) >= 8:
-                    rows.append(parts)
-        os.unlink(self.path)
-        if not rows:
+        if not self.rows:
             return None
-        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
-        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
-        reasons = set()
-        for r in rows:
-            for name, val in zip(["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"],
-                                 r[4:8]):
-                if val.lower() == "active":
-                    reasons.add(name)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(rows)}
+        sm = [r[0] for r in self.rows]
+        pw = [r[1] for r in self.rows if r[1] is not None]
+        reasons = sorted({name for r in self.rows for bit, name in self.REASONS.items() if r[2] & bit})
+        counts = {name: sum(1 for r in self.rows if r[2] & bit) for bit, name in self.REASONS.items()}
+        return {"sm_mhz": statistics.median(sm), "sm_mhz_min": min(sm), "sm_max_mhz": self.max_mhz,
+                "power_w_max": max(pw) if pw else None, "reasons": reasons,
+                "reason_samples": {k: v for k, v in counts.items() if v}, "samples": len(self.rows),
+                "source": self.source}
 
 
 def _dist():
@@ -237,7 +311,7 @@ def run_reference(args):
         "impl": "reference", "metric": _metric(s), "value": value, "unit": "TFLOP/s", "n_gpus": ws,
         "steps": steps, "warmup": warm, "ms_per_step": total / steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
-        "config": _config(args.config, s, ws),
+        "config": _config(args.config, s, ws, args),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": nthreads, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -248,30 +322,117 @@ def _metric(s):
     return "MoE layer fwd useful TFLOPS (6*T*K*d*f per layer) at 1 GB300"
 
 
-def _config(name, s, ws):
+def _config(name, s, ws, args):
+    mxfp8 = getattr(args, "precision", "bf16") == "mxfp8"
     return {"workload": DESCRIPTIONS.get(name, f"MoE layer fwd T={s.T} d={s.d} E={s.E} K={s.K} f={s.f}"),
             "T": s.T, "d": s.d, "E": s.E, "K": s.K, "f": s.f, "bias": s.bias,
             "tokens_per_gpu": s.T, "parallelism": f"replicas{ws}" if ws > 1 else "single",
-            "l2": "inputs larger than L2 (expert weights stream from HBM every step)"}
+            "l2": "inputs larger than L2 (expert weights stream from HBM every step)",
+            "fused_combine": bool(getattr(args, "fused_combine", False)),
+            "precision": ("mxfp8: E4M3 elements, UE8M0 scale per 32 along K, fp32 accumulate; expert weights "
+                          "quantised once before the timed region" if mxfp8 else "bf16, fp32 accumulate")}
 
 
 # ------------------------------------------------------------------ GPU arm
-def run_gpu(args):
-    ws, rank, local = _dist()
-    torch.cuda.set_device(local)
-    import __graft_entry__
-    if rank == 0 or ws == 1:
-        __graft_entry__.build()
-    _barrier(ws)
-    import dropless_moe_expert_gb300 as moe
+# A timed region shorter than this runs at the clocks of a burst (the bench's
+# regions are tens of ms); longer ones settle where the sustained peak was
+# measured (a seconds-long loop under the power cap).
+BURST_REGION_S = 1.0
 
-    s = shape(args.config)
-    s_name = args.config
+
+def _dominant_roofline(s, s_name, kmean, counts, mxfp8, region_s):
+    """Roofline of the dominant grouped GEMM: its binding resource (the
+    larger of the tensor and HBM floors), achieved rate from the event-timed
+    mean launch, and the fraction of both measured bf16 peaks, the one that
+    applies named by the length of the timed region."""
+    T, d, E, K, f = s.T, s.d, s.E, s.K, s.f
+    TK = T * K
+    peaks, peak_src = _peaks()
+    dom = max(("grouped_gemm1_swiglu", "grouped_gemm2"), key=lambda n: kmean[n])
+    dom_flops = (4.0 if dom == "grouped_gemm1_swiglu" else 2.0) * TK * d * f
+    burst = float(peaks.get("bf16_tflops", 1900.0))
+    sustained = float(peaks.get("bf16_tflops_sustained", burst))
+    ratio = 2.0 if mxfp8 else 1.0      # nominal dense fp8 / bf16 tensor ratio (4.5 / 2.25 PFLOP/s)
+    use_burst = region_s < BURST_REGION_S
+    peak = (burst if use_burst else sustained) * ratio
+    peak_src_note = (f"{peak_src} bf16_tflops ({'burst' if use_burst else 'sustained'}: the timed region "
+                     f"lasted {region_s:.3f} s, {'under' if use_burst else 'over'} {BURST_REGION_S:.0f} s)")
+    if not use_burst:
+        peak_src_note = peak_src_note.replace("bf16_tflops (", "bf16_tflops_sustained (")
+    if mxfp8:
+        peak_src_note += " x 2 (nominal fp8 / bf16 dense tensor ratio, 4.5 / 2.25 PFLOP/s)"
+    eb = 1.0 if mxfp8 else 2.0  # bytes per weight / activation element
+    # algorithmic bytes of one launch: the live experts' weights, the
+    # activations read and the output written (scales of the MXFP8 operands
+    # add 1/32 of their codes)
+    live = int((counts > 0).sum().item())
+    sc = (1.0 + 1.0 / 32.0) if mxfp8 else 1.0
+    if dom == "grouped_gemm1_swiglu":
+        dom_bytes = sc * eb * (live * 2.0 * f * d + TK * d) + sc * eb * TK * f
+    else:
+        dom_bytes = sc * eb * (live * 1.0 * d * f + TK * f) + 2.0 * TK * d
+    t_dom = kmean[dom] * 1e-3
+    hbm_peak = float(peaks["hbm_gbs"])
+    tensor_floor, hbm_floor = dom_flops / (peak * 1e12), dom_bytes / (hbm_peak * 1e9)
+    tr = _traffic_record(dom + ("_mxfp8" if mxfp8 else ""), s_name)
+    tflops = dom_flops / t_dom / 1e12
+    common = {"kernel": dom + ("_mxfp8" if mxfp8 else ""),
+              "traffic": (tr["dram_bytes_per_launch"] if tr else None),
+              "traffic_note": (tr.get("note") if tr else
+                               "no ncu counters for this kernel source on this workload"),
+              "algorithmic": {"flop": dom_flops, "bytes": dom_bytes, "live_experts": live,
+                              "tensor_floor_ms": tensor_floor * 1e3, "hbm_floor_ms": hbm_floor * 1e3},
+              "frac_of_bf16_burst": tflops / (burst * ratio),
+              "frac_of_bf16_sustained": tflops / (sustained * ratio),
+              "frac_of_hbm": dom_bytes / t_dom / 1e9 / hbm_peak}
+    if hbm_floor > tensor_floor:
+        achieved = dom_bytes / t_dom / 1e9
+        return dict(bound="hbm", achieved=achieved, peak=hbm_peak, unit="GB/s", frac=achieved / hbm_peak,
+                    peak_source=f"{peak_src} hbm_gbs", **common)
+    return dict(bound="tensor", achieved=tflops, peak=peak, unit="TFLOP/s", frac=tflops / peak,
+                peak_source=peak_src_note, **common)
+
+
+def _kernel_table(s, kmean, mxfp8):
+    T, d, E, K, f = s.T, s.d, s.E, s.K, s.f
+    TK = T * K
+    peaks, _ = _peaks()
+    share = {n: kmean[n] / sum(kmean.values()) for n in STEP_NAMES}
+    chunks = (T + 63) // 64
+    hbm_bytes = {
+        # logits read; topk_idx, topk_w, row_of written; two [chunks, E] tables written and read
+        "route": 4.0 * T * E + 12.0 * TK + 16.0 * chunks * E,
+        "permute": 2.0 * T * d + 2.0 * TK * d + 4.0 * TK,
+        "unpermute": 2.0 * TK * d + 2.0 * T * d + 8.0 * TK,
+    }
+    if mxfp8:
+        # E4M3 codes: x read as bf16 once, codes written K times, scales beside them
+        hbm_bytes["permute"] = 2.0 * T * d + 1.0 * TK * d + TK * d / 32.0 + 8.0 * TK
+    kernels = {n: {"ms": kmean[n], "share": share[n]} for n in STEP_NAMES}
+    for n, b in hbm_bytes.items():
+        kernels[n]["GB/s"] = b / (kmean[n] * 1e-3) / 1e9
+        kernels[n]["frac_of_hbm"] = kernels[n]["GB/s"] / float(peaks["hbm_gbs"])
+    # router: bf16 tensor-core work of the three-piece split, 3 x 2*T*d*E
+    kernels["router_logits"]["TFLOP/s"] = 6.0 * T * d * E / (kmean["router_logits"] * 1e-3) / 1e12
+    for n in ("grouped_gemm1_swiglu", "grouped_gemm2"):
+        fl = (4.0 if n == "grouped_gemm1_swiglu" else 2.0) * TK * d * f
+        kernels[n]["TFLOP/s"] = fl / (kmean[n] * 1e-3) / 1e12
+    return kernels
+
+
+def measure_forward(moe, s_name, args, ws, rank, local, full=True):
+    """Times K steps of the layer forward on workload `s_name` through the C
+    ABI (one event pair per kernel on the launching stream).  The steps
+    alternate between two resident token batches (two seeds), so that
+    consecutive steps route differently.  With `full`, also the end-to-end
+    host-buffer rate, the graph replays and the CPU baseline."""
+    s = shape(s_name)
     T, d, E, K, f = s.T, s.d, s.E, s.K, s.f
     TK = T * K
     dev = torch.device("cuda", local)
     w = make_weights(s, seed=0, device=dev)
-    x = make_tokens(s, seed=replica_seed(rank), device=dev)
+    xs = [make_tokens(s, seed=replica_seed(rank), device=dev),
+          make_tokens(s, seed=replica_seed(rank) + 1, device=dev)]
 
     # persistent buffers of the step (granular C-ABI calls so that each
     # kernel can be bracketed by events on the launching stream)
@@ -297,18 +458,18 @@ def run_gpu(args):
     y = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
     counters = torch.empty((max(1, int(moe.lib.moe_combine_counters_size(T, d)) // 4),), dtype=torch.int32,
                            device=dev)
-    if args.fused_combine and args.precision != "bf16":
-        raise SystemExit("--fused-combine is a bf16-path option")
     L = moe.lib
     stream = torch.cuda.current_stream()
     sp = stream.cuda_stream
     P = lambda t: t.data_ptr()  # noqa: E731
     bias_p = P(w.bias)
 
-    def step(ev=None):
-        def rec(i):
+    def step(i, ev=None):
+        x = xs[i % 2]
+
+        def rec(j):
             if ev is not None:
-                ev[i].record(stream)
+                ev[j].record(stream)
         rec(0)
         st = L.moe_router_logits(P(x), P(w.Wr), bias_p, T, d, E, P(logits), P(router_ws), router_ws.numel(), sp)
         rec(1)
@@ -344,13 +505,13 @@ def run_gpu(args):
         if st != 0:
             raise RuntimeError(f"C ABI returned {st}")
 
-    for _ in range(args.warmup):
-        step()
+    for i in range(args.warmup):
+        step(i)
     torch.cuda.synchronize()
     assert moe.device_status() == 0
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(args.steps)]
-    sampler = ClockSampler(local) if rank == 0 else None
+    sampler = ClockSampler(local).start() if rank == 0 else None
     _barrier(ws)
     torch.cuda.synchronize()
     l0 = moe.launch_count()
@@ -358,12 +519,12 @@ def run_gpu(args):
     end = torch.cuda.Event(enable_timing=True)
     start.record(stream)
     for i in range(args.steps):
-        step(evs[i])
+        step(i, evs[i])
     end.record(stream)
     torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
     _barrier(ws)
     launches = moe.launch_count() - l0
-    clocks = sampler.stop() if sampler else None
     assert moe.device_status() == 0
     elapsed_ms = start.elapsed_time(end)
     elapsed_ms = _max_over_ranks(elapsed_ms, ws)
@@ -374,16 +535,24 @@ def run_gpu(args):
     kmean = {n: sum(v) / len(v) for n, v in per_kernel.items()}
     ms_per_step = elapsed_ms / args.steps
     flops_step = 6.0 * TK * d * f
-    value = aggregate(flops_step, ws, args.steps, elapsed_ms) / 1e12
-    tokens_s = aggregate(T, ws, args.steps, elapsed_ms)
+    res = {
+        "config": s_name, "s": s, "value": aggregate(flops_step, ws, args.steps, elapsed_ms) / 1e12,
+        "tokens_per_s": aggregate(T, ws, args.steps, elapsed_ms), "ms_per_step": ms_per_step,
+        "launches": launches, "clocks": clocks, "timed_region_s": elapsed_ms * 1e-3,
+        "kernels": _kernel_table(s, kmean, mxfp8),
+        "roofline": _dominant_roofline(s, s_name, kmean, counts, mxfp8, elapsed_ms * 1e-3),
+        "routing": {"empty_experts": int((counts == 0).sum().item()), "max_group": int(counts.max().item()),
+                    "batches": "two resident token batches (seeds r, r+1), alternating step by step"},
+    }
+    if not full:
+        return res
 
     # ---- end to end through the public API with host buffers (pinned): every
     # batch's host->device copy of x and device->host copy of y run inside
     # the timed region, on the library's copy streams, overlapped with the
     # compute of the neighbouring batches (moe_forward_host_pipelined).  Two
     # host input and two host output buffers are cycled over the K batches.
-    x_hosts_buf = [x.cpu().pin_memory(),
-                   make_tokens(s, seed=replica_seed(rank) + 1, device="cpu").pin_memory()]
+    x_hosts_buf = [xs[0].cpu().pin_memory(), xs[1].cpu().pin_memory()]
     y_hosts_buf = [torch.empty((T, d), dtype=torch.bfloat16, pin_memory=True) for _ in range(2)]
     if mxfp8:
         del x_perm, h, sfa, sfh
@@ -413,11 +582,16 @@ def run_gpu(args):
     torch.cuda.synchronize()
     assert moe.device_status() == 0
     e2e_ms = _max_over_ranks(e0.elapsed_time(e1), ws)
-    e2e_value = aggregate(flops_step, ws, args.steps, e2e_ms) / 1e12
+    res["e2e"] = {"value": aggregate(flops_step, ws, args.steps, e2e_ms) / 1e12, "unit": "TFLOP/s",
+                  "h2d_bytes_per_step": T * d * 2, "d2h_bytes_per_step": T * d * 2,
+                  "ms_per_step": e2e_ms / args.steps,
+                  "copies": "every batch's copies inside the timed region, overlapped with the neighbouring "
+                            "batches' compute (moe_forward_host_pipelined)"}
+    del ws_pipe
 
     # ---- the whole layer (one moe_forward call) captured once as a CUDA graph
     # and replayed: the launch-overhead-free time of a step
-    graph = None
+    res["graph"] = None
     if not mxfp8 and not args.fused_combine:
         # The graph reads its tokens from one static buffer; before every
         # replay a fresh batch is copied into it (two seeded batches,
@@ -426,8 +600,8 @@ def run_gpu(args):
         # own pair of events; the copies fall outside those intervals.
         layer_g = moe.MoELayer(w.Wr, w.bias, w.W1, w.W2, K, T)
         y_g = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
-        pool = [x, make_tokens(s, seed=replica_seed(rank) + 2, device=dev)]
-        x_g = x.clone()
+        pool = [xs[0], make_tokens(s, seed=replica_seed(rank) + 2, device=dev)]
+        x_g = xs[0].clone()
         gs = torch.cuda.Stream()
         gs.wait_stream(stream)
         with torch.cuda.stream(gs):
@@ -450,101 +624,66 @@ def run_gpu(args):
         torch.cuda.synchronize()
         assert moe.device_status() == 0
         g_ms = _max_over_ranks(sum(a.elapsed_time(b) for a, b in gev), ws)
-        graph = {"value": aggregate(flops_step, ws, args.steps, g_ms) / 1e12, "unit": "TFLOP/s",
-                 "ms_per_step": g_ms / args.steps,
-                 "note": "moe_forward captured once and replayed K times; before each replay a new token batch "
-                         "(two seeds, alternating) is copied into the graph's input, so every replay routes "
-                         "differently; only the replays are timed"}
+        res["graph"] = {"value": aggregate(flops_step, ws, args.steps, g_ms) / 1e12, "unit": "TFLOP/s",
+                        "ms_per_step": g_ms / args.steps,
+                        "note": "moe_forward captured once and replayed K times; before each replay a new token "
+                                "batch (two seeds, alternating) is copied into the graph's input, so every replay "
+                                "routes differently; only the replays are timed"}
         del g, layer_g, pool, x_g
 
-    # ---- roofline of the dominant kernel
-    peaks, peak_src = _peaks()
-    dom = max(("grouped_gemm1_swiglu", "grouped_gemm2"), key=lambda n: kmean[n])
-    dom_flops = (4.0 if dom == "grouped_gemm1_swiglu" else 2.0) * TK * d * f
-    peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
-    peak_src_note = f"{peak_src} bf16_tflops_sustained"
-    eb = 1.0 if mxfp8 else 2.0  # bytes per weight / activation element
-    if mxfp8:
-        peak *= 2.0
-        peak_src_note += " x 2 (nominal fp8 / bf16 dense tensor ratio, 4.5 / 2.25 PFLOP/s)"
-    # algorithmic bytes of one launch: the live experts' weights, the
-    # activations read and the output written (scales of the MXFP8 operands
-    # add 1/32 of their codes)
-    live = int((counts > 0).sum().item())
-    sc = (1.0 + 1.0 / 32.0) if mxfp8 else 1.0
-    if dom == "grouped_gemm1_swiglu":
-        dom_bytes = sc * eb * (live * 2.0 * f * d + TK * d) + sc * eb * TK * f
-    else:
-        dom_bytes = sc * eb * (live * 1.0 * d * f + TK * f) + 2.0 * TK * d
-    t_dom = kmean[dom] * 1e-3
-    hbm_peak = float(peaks["hbm_gbs"])
-    # the binding resource: the larger of the two floors
-    tensor_floor, hbm_floor = dom_flops / (peak * 1e12), dom_bytes / (hbm_peak * 1e9)
-    tr = _traffic_record(dom + ("_mxfp8" if mxfp8 else ""), s_name)
-    common = {"kernel": dom + ("_mxfp8" if mxfp8 else ""),
-              "traffic": (tr["dram_bytes_per_launch"] if tr else None),
-              "traffic_note": (tr.get("note") if tr else
-                               "no ncu counters for this kernel source on this workload"),
-              "algorithmic": {"flop": dom_flops, "bytes": dom_bytes, "live_experts": live,
-                              "tensor_floor_ms": tensor_floor * 1e3, "hbm_floor_ms": hbm_floor * 1e3}}
-    if hbm_floor > tensor_floor:
-        achieved = dom_bytes / t_dom / 1e9
-        roofline = dict(bound="hbm", achieved=achieved, peak=hbm_peak, unit="GB/s", frac=achieved / hbm_peak,
-                        peak_source=f"{peak_src} hbm_gbs", **common)
-    else:
-        achieved = dom_flops / t_dom / 1e12
-        roofline = dict(bound="tensor", achieved=achieved, peak=peak, unit="TFLOP/s", frac=achieved / peak,
-                        peak_source=peak_src_note, **common)
-    share = {n: kmean[n] / sum(kmean.values()) for n in STEP_NAMES}
-    chunks = (T + 63) // 64
-    hbm_bytes = {
-        # logits read; topk_idx, topk_w, row_of written; two [chunks, E] tables written and read
-        "route": 4.0 * T * E + 12.0 * TK + 16.0 * chunks * E,
-        "permute": 2.0 * T * d + 2.0 * TK * d + 4.0 * TK,
-        "unpermute": 2.0 * TK * d + 2.0 * T * d + 8.0 * TK,
-    }
-    kernels = {n: {"ms": kmean[n], "share": share[n]} for n in STEP_NAMES}
-    for n, b in hbm_bytes.items():
-        kernels[n]["GB/s"] = b / (kmean[n] * 1e-3) / 1e9
-        kernels[n]["frac_of_hbm"] = kernels[n]["GB/s"] / float(peaks["hbm_gbs"])
-    # router: bf16 tensor-core work of the three-piece split, 3 x 2*T*d*E
-    kernels["router_logits"]["TFLOP/s"] = 6.0 * T * d * E / (kmean["router_logits"] * 1e-3) / 1e12
-    if mxfp8:
-        # E4M3 codes: x read as bf16 once, codes written K times, scales beside them
-        hbm_bytes["permute"] = 2.0 * T * d + 1.0 * TK * d + TK * d / 32.0 + 8.0 * TK
-        kernels["permute"]["GB/s"] = hbm_bytes["permute"] / (kmean["permute"] * 1e-3) / 1e9
-        kernels["permute"]["frac_of_hbm"] = kernels["permute"]["GB/s"] / float(peaks["hbm_gbs"])
-    for n in ("grouped_gemm1_swiglu", "grouped_gemm2"):
-        fl = (4.0 if n == "grouped_gemm1_swiglu" else 2.0) * TK * d * f
-        kernels[n]["TFLOP/s"] = fl / (kmean[n] * 1e-3) / 1e12
-
     # ---- CPU baseline: the oracle on a bounded sample (rank 0, N=1 only)
-    cpu = None
+    res["cpu_baseline"] = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline and not mxfp8:
         import oracle
-        inputs = _oracle_inputs(s, x, w)
+        inputs = _oracle_inputs(s, xs[0], w)
         nthreads = oracle.host_threads()
         n, t = _oracle_rate(s, inputs, args.cpu_budget, nthreads)
-        cpu = {"value": 6.0 * n * K * d * f / t / 1e12, "unit": "TFLOP/s", "cores": nthreads, "kind": "oracle",
-               "sample": f"first {n} of {T} tokens, oracle.forward (all {E} experts' weights as {inputs[5]}), "
-                         f"{t:.1f} s"}
+        res["cpu_baseline"] = {
+            "value": 6.0 * n * K * d * f / t / 1e12, "unit": "TFLOP/s", "cores": nthreads, "kind": "oracle",
+            "sample": f"first {n} of {T} tokens, oracle.forward (all {E} experts' weights as {inputs[5]}), "
+                      f"{t:.1f} s"}
+    return res
 
+
+def run_gpu(args):
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    import __graft_entry__
+    if rank == 0 or ws == 1:
+        __graft_entry__.build()
+    _barrier(ws)
+    import dropless_moe_expert_gb300 as moe
+
+    mxfp8 = args.precision == "mxfp8"
+    r = measure_forward(moe, args.config, args, ws, rank, local, full=True)
+    # the other large workloads, device-timed the same way (no e2e or
+    # baseline legs), so that one run reports every configuration
+    others = {}
+    for name in [c for c in args.extra_configs.split(",") if c and c != args.config]:
+        torch.cuda.empty_cache()
+        o = measure_forward(moe, name, args, ws, rank, local, full=False)
+        others[name] = {"workload": DESCRIPTIONS.get(name, name), "value": o["value"], "unit": "TFLOP/s",
+                        "tokens_per_s": o["tokens_per_s"], "ms_per_step": o["ms_per_step"],
+                        "kernels": {n: {"ms": k["ms"], **({"TFLOP/s": k["TFLOP/s"]} if "TFLOP/s" in k else {}),
+                                        **({"frac_of_hbm": k["frac_of_hbm"]} if "frac_of_hbm" in k else {})}
+                                    for n, k in o["kernels"].items()},
+                        "roofline": {kk: o["roofline"][kk] for kk in (
+                            "bound", "kernel", "achieved", "peak", "unit", "frac", "frac_of_bf16_burst",
+                            "frac_of_bf16_sustained", "frac_of_hbm")},
+                        "routing": o["routing"], "clocks": o["clocks"], "gpu_launches": o["launches"]}
+        r["launches"] += o["launches"]
+    s = r["s"]
     if rank == 0:
         line = {
-            "metric": _metric(s), "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "metric": _metric(s), "value": r["value"], "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": r["ms_per_step"], "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "mxfp8" if mxfp8 else "bf16",
             "data": "synthetic (seeded N(0,1) tokens, N(0,1/fan_in) weights)",
-            "config": dict(_config(s_name, s, ws), fused_combine=bool(args.fused_combine), precision=(
-                "mxfp8: E4M3 elements, UE8M0 scale per 32 along K, fp32 accumulate; expert weights quantised "
-                "once before the timed region" if mxfp8 else "bf16, fp32 accumulate")),
-            "tokens_per_s": tokens_s, "kernels": kernels, "roofline": roofline, "cpu_baseline": cpu,
-            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": T * d * 2,
-                    "d2h_bytes_per_step": T * d * 2, "ms_per_step": e2e_ms / args.steps,
-                    "copies": "every batch's copies inside the timed region, overlapped with the neighbouring "
-                              "batches' compute (moe_forward_host_pipelined)"},
-            "gpu_launches": launches, "clocks": clocks, "graph": graph,
-            "routing": {"empty_experts": int((counts == 0).sum().item()), "max_group": int(counts.max().item())},
+            "config": _config(args.config, s, ws, args),
+            "tokens_per_s": r["tokens_per_s"], "kernels": r["kernels"], "roofline": r["roofline"],
+            "cpu_baseline": r["cpu_baseline"], "e2e": r["e2e"], "gpu_launches": r["launches"],
+            "clocks": r["clocks"], "timed_region_s": r["timed_region_s"], "graph": r["graph"],
+            "routing": r["routing"], "other_configs": others or None,
         }
         print(json.dumps(line), flush=True)
     if ws > 1:
@@ -595,7 +734,7 @@ def run_train_step(args):
     torch.cuda.synchronize()
     assert moe.device_status() == 0
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    sampler = ClockSampler(local) if rank == 0 else None
+    sampler = ClockSampler(local).start() if rank == 0 else None
     _barrier(ws)
     torch.cuda.synchronize()
     l0 = moe.launch_count()
@@ -622,7 +761,7 @@ def run_train_step(args):
             "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) tokens and output gradient)",
-            "config": dict(_config(args.config, s, ws), step="forward + backward",
+            "config": dict(_config(args.config, s, ws, args), step="forward + backward",
                            grads="dx bf16; dWr, dbias, dW1, dW2 fp32",
                            saved="GEMM1 pre-activations [T*K, 2f] bf16, stored by the forward"),
             "kernels": {"forward": {"ms": fwd_ms, "TFLOP/s": 6.0 * TK * d * f / (fwd_ms * 1e-3) / 1e12},
@@ -641,7 +780,10 @@ def main():
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--config", default="mixtral")
+    ap.add_argument("--config", default="skew",
+                    help="headline workload (default: the extreme-skew layer, the most work per step)")
+    ap.add_argument("--extra-configs", default="mixtral,dsv3,qwen",
+                    help="other workloads timed on the device in the same run (comma list, '' for none)")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--fused-combine", action="store_true",

@@ -22,7 +22,7 @@ __all__ = [
     "MoEError", "lib", "router_logits", "router_workspace_size", "route", "route_workspace_size", "permute",
     "grouped_mlp",
     "grouped_gemm1_swiglu", "grouped_gemm2", "unpermute", "forward", "forward_workspace_size",
-    "forward_views", "forward_host", "device_status", "launch_count", "MoELayer",
+    "forward_views", "forward_host", "device_status", "last_device_status", "launch_count", "MoELayer",
     "mxfp8_quantize", "mxfp8_scales_size", "mxfp8_act_scales_size", "permute_mxfp8",
     "grouped_gemm1_swiglu_mxfp8", "grouped_gemm2_mxfp8", "forward_mxfp8", "forward_mxfp8_views", "MoELayerMXFP8",
     "grouped_gemm2_combine",
@@ -103,6 +103,7 @@ def _load():
         "moe_combine_counters_size": (S, [I, I]),
         "moe_grouped_gemm2_combine": (I, [P, P, I, I, I, I, P, P, P, P, I, I, P, P, S, P, P]),
         "moe_device_status": (I, [ctypes.POINTER(I)]),
+        "moe_last_device_status": (I, [P, P]),
         "moe_check_bounded_wait": (I, [U64, P]),
     }
     for name, (res, args) in sig.items():
@@ -422,6 +423,18 @@ def device_status() -> int:
     v = ctypes.c_int(0)
     _check(lib.moe_device_status(ctypes.byref(v)), "moe_device_status")
     return v.value
+
+
+def last_device_status(out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Queues a read-and-clear of the device status word on the stream into
+    ``out`` (one int32 on the device, allocated when None), without
+    synchronizing: capture-safe.  Read ``out`` after the stream has run."""
+    if out is None:
+        out = torch.empty((1,), dtype=torch.int32, device="cuda")
+    if out.dtype != torch.int32 or not out.is_cuda or out.numel() < 1:
+        raise ValueError("out must be an int32 CUDA tensor with at least one element")
+    _check(lib.moe_last_device_status(out.data_ptr(), _stream(stream)), "moe_last_device_status")
+    return out
 
 
 def check_bounded_wait(limit_ns: int = 2_000_000, stream=None) -> None:

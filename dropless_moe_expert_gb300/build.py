@@ -72,7 +72,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
             if log.strip():
                 print(f"== {os.path.basename(obj)}\n{log}", file=sys.stderr)
     tmp = out + f".tmp{os.getpid()}"
-    cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *[o for o, _ in results]]
+    cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *[o for o, _ in results], "-ldl"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

@@ -6,8 +6,11 @@
 #include "../../include/moe.h"
 #include "kernels.h"
 
+#include <nvtx3/nvToolsExt.h>
+
 #include <atomic>
 #include <mutex>
+#include <vector>
 
 namespace {
 
@@ -18,6 +21,13 @@ constexpr uint64_t kWaitLimitNs = 1000000000ull;  // bounded device waits: 1 s
 std::atomic<uint64_t> g_launches{0};
 
 __device__ int g_device_status = 0;
+
+// Copies the device status word into the caller's word and clears it, in
+// stream order: it sees what every kernel queued before it on the stream
+// recorded.  One thread; the exchange clears the word atomically, so a
+// kernel on another stream that records a timeout meanwhile is not lost
+// (it shows in the next read).
+__global__ void read_status_kernel(int32_t *out) { *out = atomicExch(&g_device_status, 0); }
 
 struct DeviceState {
     bool ready = false;
@@ -54,6 +64,64 @@ moe_status_t device_state(DeviceState **out) {
 }
 
 inline bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// One NVTX range per C-ABI call, named after the entry point, so that a
+// profiler's timeline shows which call queued which kernels.  Without a
+// profiler attached the push and pop return at once.
+struct Range {
+    explicit Range(const char *name) { nvtxRangePushA(name); }
+    ~Range() { nvtxRangePop(); }
+    Range(const Range &) = delete;
+    Range &operator=(const Range &) = delete;
+};
+#define MOE_RANGE() Range moe_nvtx_range_(__func__)
+
+// Copy streams and events of the pipelined host runner, created once and
+// reused: a call takes a set from its device's pool (or creates one) and
+// gives it back once everything is queued.  Reusing them is safe: every wait
+// a call queues refers to an event recorded earlier in the same call, and a
+// later record of the same event does not change a wait already queued.
+struct Runner {
+    int dev = -1;
+    cudaStream_t cin = nullptr, cout = nullptr;
+    cudaEvent_t ev[7] = {};
+};
+std::vector<Runner> g_runners;
+std::mutex g_runner_mu;
+
+bool acquire_runner(Runner *r) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    {
+        std::lock_guard<std::mutex> lock(g_runner_mu);
+        for (size_t i = 0; i < g_runners.size(); ++i) {
+            if (g_runners[i].dev == dev) {
+                *r = g_runners[i];
+                g_runners.erase(g_runners.begin() + static_cast<std::ptrdiff_t>(i));
+                return true;
+            }
+        }
+    }
+    Runner n;
+    n.dev = dev;
+    bool ok = cudaStreamCreateWithFlags(&n.cin, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&n.cout, cudaStreamNonBlocking) == cudaSuccess;
+    for (int i = 0; ok && i < 7; ++i) ok = cudaEventCreateWithFlags(&n.ev[i], cudaEventDisableTiming) == cudaSuccess;
+    if (!ok) {
+        for (int i = 0; i < 7; ++i)
+            if (n.ev[i]) cudaEventDestroy(n.ev[i]);
+        if (n.cin) cudaStreamDestroy(n.cin);
+        if (n.cout) cudaStreamDestroy(n.cout);
+        return false;
+    }
+    *r = n;
+    return true;
+}
+
+void release_runner(const Runner &r) {
+    std::lock_guard<std::mutex> lock(g_runner_mu);
+    g_runners.push_back(r);
+}
 
 moe_status_t check_shape(int T, int d, int E, int K, int f, bool need_d, bool need_f) {
     if (T < 1 || E < 1 || K < 1 || K > E) return MOE_ERR_INVALID_ARG;
@@ -171,24 +239,22 @@ moe_status_t run_gemm(bool swiglu, const void *A, const int32_t *offsets, int E,
 // the compute of batch i-2 that read it, and recomputed only after the copy
 // out of batch i-2 that read it.  `stream` ends waiting for the last copy out,
 // so its completion means every y_hosts[i] is written.  The copy streams and
-// events belong to the call (destroyed once their work is done).
+// events come from the device's runner pool (created on first use, reused).
 template <typename F>
 moe_status_t run_pipelined(const uint16_t *const *x_hosts, uint16_t *const *y_hosts, int n, size_t bytes,
                            uint16_t *const xbuf[2], uint16_t *const ybuf[2], cudaStream_t stream, F compute) {
-    cudaStream_t cin = nullptr, cout = nullptr;
-    cudaEvent_t ev[7] = {};
+    Runner run;
+    if (!acquire_runner(&run)) return MOE_ERR_CUDA;
+    cudaStream_t cin = run.cin, cout = run.cout;
+    cudaEvent_t *ev = run.ev;
     moe_status_t st = MOE_OK;
-    bool ok = cudaStreamCreateWithFlags(&cin, cudaStreamNonBlocking) == cudaSuccess &&
-              cudaStreamCreateWithFlags(&cout, cudaStreamNonBlocking) == cudaSuccess;
-    for (int i = 0; ok && i < 7; ++i) ok = cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming) == cudaSuccess;
-    if (!ok) st = MOE_ERR_CUDA;
     cudaEvent_t entry = ev[0], *xready = ev + 1, *done = ev + 3, *yfree = ev + 5;
     auto chk = [&](cudaError_t e) {
         if (st == MOE_OK && e != cudaSuccess) st = MOE_ERR_CUDA;
         return st == MOE_OK;
     };
     // the copies start after the work the caller queued before this call
-    if (st == MOE_OK && chk(cudaEventRecord(entry, stream)) && chk(cudaStreamWaitEvent(cin, entry, 0)))
+    if (chk(cudaEventRecord(entry, stream)) && chk(cudaStreamWaitEvent(cin, entry, 0)))
         chk(cudaStreamWaitEvent(cout, entry, 0));
     for (int i = 0; st == MOE_OK && i < n; ++i) {
         const int b = i & 1;
@@ -204,10 +270,7 @@ moe_status_t run_pipelined(const uint16_t *const *x_hosts, uint16_t *const *y_ho
         if (!chk(cudaEventRecord(yfree[b], cout))) break;
     }
     if (st == MOE_OK && n > 0) chk(cudaStreamWaitEvent(stream, yfree[(n - 1) & 1], 0));
-    for (int i = 0; i < 7; ++i)
-        if (ev[i]) cudaEventDestroy(ev[i]);
-    if (cin) cudaStreamDestroy(cin);
-    if (cout) cudaStreamDestroy(cout);
+    release_runner(run);
     return st;
 }
 
@@ -227,7 +290,7 @@ const char *moe_status_string(int status) {
     }
 }
 
-int moe_abi_version(void) { return 401; }
+int moe_abi_version(void) { return 402; }
 
 uint64_t moe_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
@@ -238,6 +301,7 @@ size_t moe_router_workspace_size(int d, int E) {
 
 moe_status_t moe_router_logits(const uint16_t *x, const float *Wr, const float *bias, int T, int d, int E,
                                float *logits, void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    MOE_RANGE();
     if (!x || !Wr || !logits || !workspace) return MOE_ERR_INVALID_ARG;
     if (!aligned(x, 16) || !aligned(Wr, 4) || !aligned(logits, 4) || (bias && !aligned(bias, 4)) ||
         !aligned(workspace, 16))
@@ -261,6 +325,7 @@ size_t moe_route_workspace_size(int T, int E, int K) {
 moe_status_t moe_route(const float *logits, int T, int E, int K, int32_t *topk_idx, float *topk_w,
                        int32_t *counts, int32_t *offsets, int32_t *row_of, int32_t *src_tok, void *workspace,
                        size_t workspace_bytes, cudaStream_t stream) {
+    MOE_RANGE();
     if (!logits || !topk_idx || !topk_w || !counts || !offsets || !row_of || !src_tok || !workspace)
         return MOE_ERR_INVALID_ARG;
     if (!aligned(logits, 4) || !aligned(topk_idx, 4) || !aligned(topk_w, 4) || !aligned(counts, 4) ||
@@ -276,6 +341,7 @@ moe_status_t moe_route(const float *logits, int T, int E, int K, int32_t *topk_i
 
 moe_status_t moe_permute(const uint16_t *x, const int32_t *row_of, int T, int K, int d, uint16_t *x_perm,
                          cudaStream_t stream) {
+    MOE_RANGE();
     if (!x || !row_of || !x_perm) return MOE_ERR_INVALID_ARG;
     if (!aligned(x, 16) || !aligned(x_perm, 16) || !aligned(row_of, 4)) return MOE_ERR_INVALID_ARG;
     moe_status_t st = check_shape(T, d, K, K, 64, true, false);
@@ -286,6 +352,7 @@ moe_status_t moe_permute(const uint16_t *x, const int32_t *row_of, int T, int K,
 
 moe_status_t moe_grouped_gemm1_swiglu(const uint16_t *x_perm, const int32_t *offsets, int E, int TK, int d, int f,
                                       const uint16_t *W1, uint16_t *h, cudaStream_t stream) {
+    MOE_RANGE();
     if (!x_perm || !offsets || !W1 || !h) return MOE_ERR_INVALID_ARG;
     if (!aligned(x_perm, 16) || !aligned(W1, 16) || !aligned(h, 16) || !aligned(offsets, 4))
         return MOE_ERR_INVALID_ARG;
@@ -297,6 +364,7 @@ moe_status_t moe_grouped_gemm1_swiglu(const uint16_t *x_perm, const int32_t *off
 moe_status_t moe_grouped_gemm1_swiglu_preact(const uint16_t *x_perm, const int32_t *offsets, int E, int TK, int d,
                                              int f, const uint16_t *W1, uint16_t *h, uint16_t *preact,
                                              cudaStream_t stream) {
+    MOE_RANGE();
     if (!x_perm || !offsets || !W1 || !h || !preact) return MOE_ERR_INVALID_ARG;
     if (!aligned(x_perm, 16) || !aligned(W1, 16) || !aligned(h, 16) || !aligned(preact, 16) ||
         !aligned(offsets, 4))
@@ -308,6 +376,7 @@ moe_status_t moe_grouped_gemm1_swiglu_preact(const uint16_t *x_perm, const int32
 
 moe_status_t moe_grouped_gemm2(const uint16_t *h, const int32_t *offsets, int E, int TK, int d, int f,
                                const uint16_t *W2, uint16_t *y_perm, cudaStream_t stream) {
+    MOE_RANGE();
     if (!h || !offsets || !W2 || !y_perm) return MOE_ERR_INVALID_ARG;
     if (!aligned(h, 16) || !aligned(W2, 16) || !aligned(y_perm, 16) || !aligned(offsets, 4))
         return MOE_ERR_INVALID_ARG;
@@ -325,6 +394,7 @@ moe_status_t moe_grouped_gemm2_combine(const uint16_t *h, const int32_t *offsets
                                        const uint16_t *W2, const int32_t *src_tok, const int32_t *row_of,
                                        const float *topk_w, int T, int K, uint16_t *y_perm, int32_t *counters,
                                        size_t counters_bytes, uint16_t *y, cudaStream_t stream) {
+    MOE_RANGE();
     if (!h || !offsets || !W2 || !src_tok || !row_of || !topk_w || !y_perm || !counters || !y)
         return MOE_ERR_INVALID_ARG;
     if (!aligned(h, 16) || !aligned(W2, 16) || !aligned(y_perm, 16) || !aligned(y, 16) || !aligned(offsets, 4) ||
@@ -347,6 +417,7 @@ moe_status_t moe_grouped_gemm2_combine(const uint16_t *h, const int32_t *offsets
 moe_status_t moe_grouped_mlp(const uint16_t *x_perm, const int32_t *offsets, int E, int TK, int d, int f,
                              const uint16_t *W1, const uint16_t *W2, uint16_t *h, uint16_t *y_perm,
                              cudaStream_t stream) {
+    MOE_RANGE();
     if (!W2 || !y_perm || !aligned(W2, 16) || !aligned(y_perm, 16)) return MOE_ERR_INVALID_ARG;
     moe_status_t st = moe_grouped_gemm1_swiglu(x_perm, offsets, E, TK, d, f, W1, h, stream);
     if (st != MOE_OK) return st;
@@ -355,6 +426,7 @@ moe_status_t moe_grouped_mlp(const uint16_t *x_perm, const int32_t *offsets, int
 
 moe_status_t moe_unpermute(const uint16_t *y_perm, const int32_t *row_of, const float *topk_w, int T, int K, int d,
                            uint16_t *y, cudaStream_t stream) {
+    MOE_RANGE();
     if (!y_perm || !row_of || !topk_w || !y) return MOE_ERR_INVALID_ARG;
     if (!aligned(y_perm, 16) || !aligned(y, 16) || !aligned(row_of, 4) || !aligned(topk_w, 4))
         return MOE_ERR_INVALID_ARG;
@@ -372,6 +444,7 @@ size_t moe_forward_workspace_size(int T, int d, int E, int K, int f) {
 }
 
 moe_status_t moe_forward_views(int T, int d, int E, int K, int f, moe_forward_layout_t *layout) {
+    MOE_RANGE();
     if (!layout) return MOE_ERR_INVALID_ARG;
     moe_status_t st = check_shape(T, d, E, K, f, true, true);
     if (st != MOE_OK) return st;
@@ -382,6 +455,7 @@ moe_status_t moe_forward_views(int T, int d, int E, int K, int f, moe_forward_la
 moe_status_t moe_forward_train(const uint16_t *x, const float *Wr, const float *bias, const uint16_t *W1,
                                const uint16_t *W2, int T, int d, int E, int K, int f, uint16_t *y, void *workspace,
                                size_t workspace_bytes, uint16_t *preact, cudaStream_t stream) {
+    MOE_RANGE();
     if (!x || !Wr || !W1 || !W2 || !y || !workspace) return MOE_ERR_INVALID_ARG;
     if (preact && !aligned(preact, 16)) return MOE_ERR_INVALID_ARG;
     if (!aligned(x, 16) || !aligned(W1, 16) || !aligned(W2, 16) || !aligned(y, 16) || !aligned(workspace, 16) ||
@@ -424,12 +498,14 @@ moe_status_t moe_forward_train(const uint16_t *x, const float *Wr, const float *
 moe_status_t moe_forward(const uint16_t *x, const float *Wr, const float *bias, const uint16_t *W1,
                          const uint16_t *W2, int T, int d, int E, int K, int f, uint16_t *y, void *workspace,
                          size_t workspace_bytes, cudaStream_t stream) {
+    MOE_RANGE();
     return moe_forward_train(x, Wr, bias, W1, W2, T, d, E, K, f, y, workspace, workspace_bytes, nullptr, stream);
 }
 
 moe_status_t moe_forward_host(const uint16_t *x_host, const float *Wr, const float *bias, const uint16_t *W1,
                               const uint16_t *W2, int T, int d, int E, int K, int f, uint16_t *y_host,
                               void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    MOE_RANGE();
     if (!x_host || !y_host || !workspace) return MOE_ERR_INVALID_ARG;
     moe_status_t st = check_shape(T, d, E, K, f, true, true);
     if (st != MOE_OK) return st;
@@ -459,6 +535,7 @@ moe_status_t moe_forward_host_pipelined(const uint16_t *const *x_hosts, uint16_t
                                         const float *Wr, const float *bias, const uint16_t *W1, const uint16_t *W2,
                                         int T, int d, int E, int K, int f, void *workspace, size_t workspace_bytes,
                                         cudaStream_t stream) {
+    MOE_RANGE();
     if (!x_hosts || !y_hosts || n_batches < 1 || !workspace) return MOE_ERR_INVALID_ARG;
     for (int i = 0; i < n_batches; ++i)
         if (!x_hosts[i] || !y_hosts[i]) return MOE_ERR_INVALID_ARG;
@@ -486,6 +563,7 @@ size_t moe_mxfp8_scales_size(int rows, int K) {
 
 moe_status_t moe_mxfp8_quantize(const uint16_t *src, int rows, int K, uint8_t *codes, uint8_t *scales,
                                 cudaStream_t stream) {
+    MOE_RANGE();
     if (!src || !codes || !scales) return MOE_ERR_INVALID_ARG;
     if (!aligned(src, 16) || !aligned(codes, 16) || !aligned(scales, 16)) return MOE_ERR_INVALID_ARG;
     if (rows < 1 || K < 1) return MOE_ERR_INVALID_ARG;
@@ -502,6 +580,7 @@ size_t moe_mxfp8_act_scales_size(int TK, int E, int K) {
 moe_status_t moe_permute_mxfp8(const uint16_t *x, const int32_t *topk_idx, const int32_t *row_of,
                                const int32_t *offsets, int T, int K, int d, int E, uint8_t *xq_perm, uint8_t *sfa,
                                size_t sfa_bytes, cudaStream_t stream) {
+    MOE_RANGE();
     if (!x || !topk_idx || !row_of || !offsets || !xq_perm || !sfa) return MOE_ERR_INVALID_ARG;
     if (!aligned(x, 16) || !aligned(xq_perm, 16) || !aligned(sfa, 16) || !aligned(topk_idx, 4) ||
         !aligned(row_of, 4) || !aligned(offsets, 4))
@@ -518,6 +597,7 @@ moe_status_t moe_grouped_gemm1_swiglu_mxfp8(const uint8_t *xq_perm, const uint8_
                                             const int32_t *offsets, int E, int TK, int d, int f, const uint8_t *W1q,
                                             const uint8_t *W1s, uint8_t *hq, uint8_t *sfh, size_t sfh_bytes,
                                             cudaStream_t stream) {
+    MOE_RANGE();
     if (!xq_perm || !sfa || !offsets || !W1q || !W1s || !hq || !sfh) return MOE_ERR_INVALID_ARG;
     if (!aligned(xq_perm, 16) || !aligned(sfa, 16) || !aligned(W1q, 16) || !aligned(W1s, 16) || !aligned(hq, 16) ||
         !aligned(sfh, 16) || !aligned(offsets, 4))
@@ -537,6 +617,7 @@ moe_status_t moe_grouped_gemm1_swiglu_mxfp8(const uint8_t *xq_perm, const uint8_
 moe_status_t moe_grouped_gemm2_mxfp8(const uint8_t *hq, const uint8_t *sfh, size_t sfh_bytes, const int32_t *offsets,
                                      int E, int TK, int d, int f, const uint8_t *W2q, const uint8_t *W2s,
                                      uint16_t *y_perm, cudaStream_t stream) {
+    MOE_RANGE();
     if (!hq || !sfh || !offsets || !W2q || !W2s || !y_perm) return MOE_ERR_INVALID_ARG;
     if (!aligned(hq, 16) || !aligned(sfh, 16) || !aligned(W2q, 16) || !aligned(W2s, 16) || !aligned(y_perm, 16) ||
         !aligned(offsets, 4))
@@ -560,6 +641,7 @@ size_t moe_forward_mxfp8_workspace_size(int T, int d, int E, int K, int f) {
 }
 
 moe_status_t moe_forward_mxfp8_views(int T, int d, int E, int K, int f, moe_forward_mxfp8_layout_t *layout) {
+    MOE_RANGE();
     if (!layout) return MOE_ERR_INVALID_ARG;
     moe_status_t st = check_mx_shape(T, d, E, K, f);
     if (st != MOE_OK) return st;
@@ -570,6 +652,7 @@ moe_status_t moe_forward_mxfp8_views(int T, int d, int E, int K, int f, moe_forw
 moe_status_t moe_forward_mxfp8(const uint16_t *x, const float *Wr, const float *bias, const uint8_t *W1q,
                                const uint8_t *W1s, const uint8_t *W2q, const uint8_t *W2s, int T, int d, int E, int K,
                                int f, uint16_t *y, void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    MOE_RANGE();
     if (!x || !Wr || !W1q || !W1s || !W2q || !W2s || !y || !workspace) return MOE_ERR_INVALID_ARG;
     if (!aligned(x, 16) || !aligned(y, 16) || !aligned(workspace, 16) || !aligned(Wr, 4) ||
         (bias && !aligned(bias, 4)))
@@ -624,6 +707,7 @@ moe_status_t moe_forward_mxfp8_host_pipelined(const uint16_t *const *x_hosts, ui
                                               const uint8_t *W1q, const uint8_t *W1s, const uint8_t *W2q,
                                               const uint8_t *W2s, int T, int d, int E, int K, int f,
                                               void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    MOE_RANGE();
     if (!x_hosts || !y_hosts || n_batches < 1 || !workspace) return MOE_ERR_INVALID_ARG;
     for (int i = 0; i < n_batches; ++i)
         if (!x_hosts[i] || !y_hosts[i]) return MOE_ERR_INVALID_ARG;
@@ -653,6 +737,7 @@ size_t moe_backward_workspace_size(int T, int d, int E, int K, int f) {
 }
 
 moe_status_t moe_backward_views(int T, int d, int E, int K, int f, moe_backward_layout_t *layout) {
+    MOE_RANGE();
     if (!layout) return MOE_ERR_INVALID_ARG;
     moe_status_t st = check_shape(T, d, E, K, f, true, true);
     if (st != MOE_OK) return st;
@@ -665,6 +750,7 @@ moe_status_t moe_backward(const uint16_t *x, const float *Wr, const float *bias,
                           const void *fwd_workspace, size_t fwd_workspace_bytes, const uint16_t *preact,
                           uint16_t *dx, float *dWr, float *dbias, float *dW1, float *dW2, void *workspace,
                           size_t workspace_bytes, cudaStream_t stream) {
+    MOE_RANGE();
     (void)bias;  // the bias enters the gradients only through the routing recorded by the forward
     if (!x || !Wr || !W1 || !W2 || !dy || !fwd_workspace || !dx || !dWr || !dbias || !dW1 || !dW2 || !workspace)
         return MOE_ERR_INVALID_ARG;
@@ -740,6 +826,7 @@ moe_status_t moe_backward(const uint16_t *x, const float *Wr, const float *bias,
 }
 
 moe_status_t moe_check_bounded_wait(uint64_t limit_ns, cudaStream_t stream) {
+    MOE_RANGE();
     if (limit_ns < 1000ull || limit_ns > kWaitLimitNs) return MOE_ERR_INVALID_ARG;
     DeviceState *ds = nullptr;
     moe_status_t st = device_state(&ds);
@@ -748,7 +835,19 @@ moe_status_t moe_check_bounded_wait(uint64_t limit_ns, cudaStream_t stream) {
     return cuda_status(moe::launch_bounded_wait_probe(ds->status, limit_ns, stream));
 }
 
+moe_status_t moe_last_device_status(int32_t *dev_status_word, cudaStream_t stream) {
+    MOE_RANGE();
+    if (!dev_status_word || !aligned(dev_status_word, 4)) return MOE_ERR_INVALID_ARG;
+    DeviceState *ds = nullptr;
+    moe_status_t st = device_state(&ds);
+    if (st != MOE_OK) return st;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    read_status_kernel<<<1, 1, 0, stream>>>(dev_status_word);
+    return cuda_status(cudaGetLastError());
+}
+
 moe_status_t moe_device_status(int *status_out) {
+    MOE_RANGE();
     if (!status_out) return MOE_ERR_INVALID_ARG;
     DeviceState *ds = nullptr;
     moe_status_t st = device_state(&ds);

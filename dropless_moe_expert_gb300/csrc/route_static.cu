@@ -1,10 +1,9 @@
 // moe_route_static: the routing step without a caller-provided workspace.
 //
 // Some callers cannot allocate device memory at the point where they route:
-// an inference-engine plugin whose enqueue step must not allocate, code that
-// runs while a stream is captured in global capture mode (where cudaMalloc is
-// not permitted), or a runtime that owns all device memory in a fixed pool
-// and forbids any other allocation.  For them this entry point keeps the
+// an inference-engine plugin whose enqueue step must not allocate, or a
+// runtime that owns all device memory in a fixed pool and forbids any other
+// allocation.  For them this entry point keeps the
 // routing scratch (per-chunk expert counts and bases) in a fixed-size array
 // of device memory that belongs to the library itself.
 //
@@ -12,7 +11,9 @@
 // library holds it until the process exits.  In host code its name is only a
 // host-side stand-in, not a device address: the address a kernel may use is
 // fetched once per device with cudaGetSymbolAddress, with that device
-// current, by the first call on that device.
+// current, by the first call on that device; make that first call before
+// any stream capture.  Every call shares the one array, and calls whose
+// kernels overlap on the GPU race on it: serialize them.
 #include "../../include/moe.h"
 #include "kernels.h"
 

@@ -50,7 +50,8 @@
  *   - Device-side waits are bounded (about one second).  A kernel whose wait
  *     expires records MOE_ERR_DEVICE_TIMEOUT in a device status word, drains
  *     its own copies, frees its tensor memory and returns; read the word with
- *     moe_device_status().
+ *     moe_device_status() (synchronous) or moe_last_device_status() (on a
+ *     stream, capture-safe).
  *   - Inputs are assumed finite; NaN or Inf logits are outside the contract.
  */
 #ifndef MOE_GB300_H
@@ -112,9 +113,8 @@ moe_status_t moe_route(const float *logits, int T, int E, int K,
 
 /* moe_route without a workspace argument, for callers that cannot allocate
  * device memory where they route: an inference-engine plugin whose enqueue
- * step must not allocate, code running while a stream is captured in global
- * capture mode (cudaMalloc is not permitted there), or a runtime that owns
- * all device memory in a fixed pool.  The page has no counterpart: this is
+ * step must not allocate, or a runtime that owns all device memory in a
+ * fixed pool and forbids any other allocation.  The page has no counterpart: this is
  * a packaging variant of moe_route, with identical outputs.
  *   - Scratch lives in a library-owned static device array of
  *     MOE_ROUTE_STATIC_MAX_SCRATCH_BYTES (1 MiB) on every GPU that loads
@@ -346,6 +346,20 @@ moe_status_t moe_backward(const uint16_t *x, const float *Wr, const float *bias,
 /* Reads and clears the device status word of the current device (0 = OK, or
  * a moe_status_t a kernel recorded).  Synchronous: call outside capture. */
 moe_status_t moe_device_status(int *status_out);
+
+/* The same read, asynchronous and capture-safe ("What specialized
+ * optimizations are needed for dropless MoE?": no value may cross to the CPU
+ * inside a captured step, so that CUDA graphs work): one kernel on `stream`
+ * copies the device status word of the current device into the caller's
+ * device word `dev_status_word` (int32, 4-byte aligned, caller-owned) and
+ * clears the status word, atomically.  Queued after a layer's kernels on the
+ * same stream, it reports what they recorded (0, or MOE_ERR_DEVICE_TIMEOUT);
+ * it can be captured into a CUDA graph with them and replayed.  The status
+ * word is shared by every stream of the device, so a read also reports and
+ * clears what kernels of other streams recorded before it ran.  Returns
+ * MOE_ERR_INVALID_ARG for a null or misaligned pointer (nothing launched),
+ * MOE_ERR_CUDA if the launch fails.  One kernel launch.  */
+moe_status_t moe_last_device_status(int32_t *dev_status_word, cudaStream_t stream);
 
 /* Exercises the failure path of the device-side waits: launches one kernel
  * whose single wait can never complete.  After limit_ns (1 us .. 1 s) it

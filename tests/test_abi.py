@@ -29,7 +29,8 @@ def test_header_declares_the_boundary():
     names = _declared()
     for n in ["moe_router_logits", "moe_router_workspace_size", "moe_route", "moe_permute", "moe_grouped_mlp",
               "moe_unpermute",
-              "moe_route_workspace_size", "moe_status_string", "moe_forward", "moe_device_status"]:
+              "moe_route_workspace_size", "moe_status_string", "moe_forward", "moe_device_status",
+              "moe_last_device_status"]:
         assert n in names
 
 
@@ -44,7 +45,7 @@ def test_status_strings(moe):
         s = moe.lib.moe_status_string(code).decode()
         assert s.startswith("MOE_")
     assert moe.lib.moe_status_string(99).decode() == "unknown moe_status_t"
-    assert moe.lib.moe_abi_version() == 401
+    assert moe.lib.moe_abi_version() == 402
 
 
 def test_workspace_sizes(moe):
@@ -87,6 +88,9 @@ def test_forward_rejects_bad_shapes(moe, args, code):
 
 def test_null_and_misaligned_pointers_rejected(moe):
     L = moe.lib
+    # the status read checks its pointer before it touches CUDA
+    assert L.moe_last_device_status(None, None) == 1
+    assert L.moe_last_device_status(FAKE + 2, None) == 1
     assert L.moe_forward(None, FAKE, None, FAKE, FAKE, 8, 64, 8, 2, 64, FAKE, FAKE, 1 << 40, None) == 1
     assert L.moe_forward(FAKE + 2, FAKE, None, FAKE, FAKE, 8, 64, 8, 2, 64, FAKE, FAKE, 1 << 40, None) == 1
     assert L.moe_router_logits(FAKE, FAKE, None, 8, 64, 8, None, FAKE, 1 << 20, None) == 1

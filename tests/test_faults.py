@@ -47,6 +47,36 @@ def test_context_usable_after_timeout():
     check_output(to_np(y), ref["y"])
 
 
+def test_status_read_inside_a_captured_graph():
+    """The capture-safe status read: a graph holding a wait that times out
+    and then moe_last_device_status reports MOE_ERR_DEVICE_TIMEOUT in the
+    caller's device word on every replay, with no synchronous read; a graph
+    holding only the read, replayed next, reports 0 (the word was cleared)."""
+    assert moe.device_status() == 0
+    word = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    clean = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        moe.last_device_status(clean)          # the per-device set-up happens outside capture
+    s.synchronize()
+    g_wait, g_read = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_wait, stream=s):
+        moe.check_bounded_wait(limit_ns=2_000_000)
+        moe.last_device_status(word)
+    with torch.cuda.graph(g_read, stream=s):
+        moe.last_device_status(clean)
+    for _ in range(2):
+        word.fill_(-1)
+        clean.fill_(-1)
+        g_wait.replay()
+        g_read.replay()
+        torch.cuda.synchronize()
+        assert int(word.item()) == MOE_ERR_DEVICE_TIMEOUT
+        assert int(clean.item()) == 0
+    assert moe.device_status() == 0
+
+
 def test_bounded_wait_rejects_out_of_range_limits():
     with pytest.raises(moe.MoEError):
         moe.check_bounded_wait(limit_ns=10)

@@ -45,6 +45,39 @@ def test_random_small_shapes(s):
     compare_small(x, w, s.K)
 
 
+# Medium shapes on which every CTA (or CTA pair) of the persistent grouped
+# GEMMs takes several tiles, compared element by element (every row of h,
+# y_perm and y): the pair kernel's accumulator alternation, phase flips and
+# epilogue overlap across tiles, and the single-CTA kernel's two-block tiles
+# over several waves.  Tiles per launch (GEMM1 / GEMM2) are about:
+#   pair, mild skew          540 / 270 on 76 pairs
+#   pair, interleaved order  440 / 220 on 76 pairs (one expert holds ~T rows)
+#   single-CTA, two-block    380 / 380 on 152 CTAs (groups of 204..332 rows)
+#   single-CTA, interleaved  670 / 330 on 152 CTAs (Zipf-skewed groups)
+MEDIUM_CASES = [
+    Shape(T=8192, d=1024, E=8, K=2, f=1024, bias="normal_0.5"),
+    Shape(T=4096, d=512, E=64, K=6, f=512, bias="skew"),
+    Shape(T=8192, d=1024, E=64, K=2, f=512, bias="zero"),
+    Shape(T=2048, d=512, E=128, K=8, f=512, bias="zipf_1.1"),
+]
+
+
+@pytest.mark.parametrize("s", MEDIUM_CASES, ids=lambda s: f"T{s.T}_d{s.d}_E{s.E}_K{s.K}_f{s.f}_{s.bias}")
+def test_medium_multi_tile_shapes(s):
+    x, w = _cpu_case(s, seed=s.T + s.E, bias_std=0)
+    TK = s.T * s.K
+    pair = TK >= 384 * s.E     # the grouped GEMMs' host-side choice of variant
+    _, v, _ = run_layer(x, w, s.K)
+    counts = to_np(v["counts"])
+    rb = 256
+    tiles1 = int(np.sum((counts + rb - 1) // rb)) * ((s.f + 127) // 128)
+    workers = 76 if pair else 152
+    assert tiles1 >= 2 * workers, f"{tiles1} GEMM1 tiles do not give each worker several"
+    r = compare_small(x, w, s.K)
+    print(f"{'pair' if pair else 'single'}: {tiles1} GEMM1 tiles, y rel_l2={r[0]:.2e} max/rms={r[1]:.2e}, "
+          f"largest group {counts.max()}, empty {(counts == 0).sum()}")
+
+
 def test_single_expert_single_token():
     s = Shape(T=1, d=64, E=1, K=1, f=64)
     x, w = _cpu_case(s)
@@ -175,6 +208,49 @@ def test_host_buffers_entry_point():
 
 
 # ---------------------------------------------------------------- full size
+def _stratified_rows(offsets, seed=0, block=128):
+    """Rows in the oracle's grouped numbering: one random row of every
+    block-row slice of every non-empty group (slices counted from the
+    group's first row, as the GEMM tiles are), plus each group's first and
+    last row."""
+    g = np.random.default_rng(seed)
+    rows = []
+    E = len(offsets) - 1
+    for e in range(E):
+        r0, r1 = int(offsets[e]), int(offsets[e + 1])
+        if r1 == r0:
+            continue
+        rows += [r0, r1 - 1]
+        for b0 in range(r0, r1, block):
+            rows.append(int(g.integers(b0, min(b0 + block, r1))))
+    return np.unique(np.array(rows, np.int64))
+
+
+def _check_stratified_rows(v, xs, idx, offsets, src_tok, same, W1, W2):
+    """h and y_perm of the stratified rows against the expert FFN evaluated
+    from the definition on the oracle's routing (rows of tokens routed
+    identically on both sides)."""
+    rows_o = _stratified_rows(offsets)
+    tok = np.asarray(src_tok)[rows_o]
+    keep = same[tok]
+    rows_o, tok = rows_o[keep], tok[keep]
+    e_of = np.searchsorted(offsets, rows_o, side="right") - 1
+    k_of = np.argmax(idx[tok] == e_of[:, None], axis=1)
+    assert np.all(idx[tok, k_of] == e_of)
+    rows_g = to_np(v["row_of"])[tok, k_of]
+    sel = torch.from_numpy(rows_g).to(DEV)
+    h_g = to_np(v["h"][sel])
+    yp_g = to_np(v["y_perm"][sel])
+    h_ref = np.zeros(h_g.shape)
+    yp_ref = np.zeros(yp_g.shape)
+    for e in np.unique(e_of):
+        m = e_of == e
+        h_ref[m], yp_ref[m] = oracle.expert_ffn(xs[tok[m]], to_np(W1[int(e)]), to_np(W2[int(e)]))
+    check_rounded(h_g, h_ref, "h (stratified rows)")
+    check_output(yp_g, yp_ref, "y_perm (stratified rows)")
+    return len(rows_o), len(np.unique(e_of))
+
+
 def _sample_tokens(T, v, K, n=24, seed=0):
     g = np.random.default_rng(seed)
     toks = set(g.choice(T, size=min(n, T), replace=False).tolist()) | {0, T - 1}
@@ -234,6 +310,10 @@ def test_full_size_workload(name):
     assert torch.equal(v["x_perm"].view(torch.int16), x.view(torch.int16)[st])
     del st
 
+    # one row of every 128-row slice of every live group, and each group's
+    # first and last rows, from the definition
+    nrows, nexp = _check_stratified_rows(v, xs, idx, offsets, src_tok, same, w.W1, w.W2)
+
     # sampled tokens through the oracle, one by one
     toks = _sample_tokens(s.T, v, s.K)
     toks = toks[same[toks]]
@@ -250,5 +330,6 @@ def test_full_size_workload(name):
     # every output row was written and is finite
     assert bool(torch.isfinite(y.float()).all())
     print(f"{name}: logits err/scale {lerr:.2e}, tokens routed differently (near ties) {int((~same).sum())}; "
+          f"stratified rows {nrows} of {nexp} experts; "
           f"sampled {len(toks)} tokens rel_l2={r[0]:.2e} max/rms={r[1]:.2e}; "
           f"experts with no token: {(counts == 0).sum()}, largest group {counts.max()}")
