@@ -329,6 +329,7 @@ def _config(name, s, ws, args):
             "tokens_per_gpu": s.T, "parallelism": f"replicas{ws}" if ws > 1 else "single",
             "l2": "inputs larger than L2 (expert weights stream from HBM every step)",
             "fused_combine": bool(getattr(args, "fused_combine", False)),
+            "permute": getattr(args, "permute", "auto"),
             "precision": ("mxfp8: E4M3 elements, UE8M0 scale per 32 along K, fp32 accumulate; expert weights "
                           "quantised once before the timed region" if mxfp8 else "bf16, fp32 accumulate")}
 
@@ -393,7 +394,7 @@ def _dominant_roofline(s, s_name, kmean, counts, mxfp8, region_s):
                 peak_source=peak_src_note, **common)
 
 
-def _kernel_table(s, kmean, mxfp8):
+def _kernel_table(s, kmean, mxfp8, fused_permute=False):
     T, d, E, K, f = s.T, s.d, s.E, s.K, s.f
     TK = T * K
     peaks, _ = _peaks()
@@ -409,6 +410,10 @@ def _kernel_table(s, kmean, mxfp8):
         # E4M3 codes: x read as bf16 once, codes written K times, scales beside them
         hbm_bytes["permute"] = 2.0 * T * d + 1.0 * TK * d + TK * d / 32.0 + 8.0 * TK
     kernels = {n: {"ms": kmean[n], "share": share[n]} for n in STEP_NAMES}
+    if fused_permute:
+        # no permute kernel: GEMM1 gathers its rows from x
+        del hbm_bytes["permute"]
+        kernels["permute"]["fused_into"] = "grouped_gemm1_swiglu"
     for n, b in hbm_bytes.items():
         kernels[n]["GB/s"] = b / (kmean[n] * 1e-3) / 1e9
         kernels[n]["frac_of_hbm"] = kernels[n]["GB/s"] / float(peaks["hbm_gbs"])
@@ -463,6 +468,8 @@ def measure_forward(moe, s_name, args, ws, rank, local, full=True):
     sp = stream.cuda_stream
     P = lambda t: t.data_ptr()  # noqa: E731
     bias_p = P(w.bias)
+    fuse_permute = not mxfp8 and (args.permute == "fused" or (
+        args.permute == "auto" and moe.forward_fuses_permute(T, d, E, K, f)))
 
     def step(i, ev=None):
         x = xs[i % 2]
@@ -487,9 +494,15 @@ def measure_forward(moe, s_name, args, ws, rank, local, full=True):
                                             P(y_perm), sp)
             rec(5)
         else:
-            st |= L.moe_permute(P(x), P(row_of), T, K, d, P(x_perm), sp)
-            rec(3)
-            st |= L.moe_grouped_gemm1_swiglu(P(x_perm), P(offsets), E, TK, d, f, P(w.W1), P(h), sp)
+            if fuse_permute:
+                # the permute fused into GEMM1's operand load; the permute step is empty
+                rec(3)
+                st |= L.moe_grouped_gemm1_swiglu_gather(P(x), P(src_tok), P(offsets), T, E, TK, d, f, P(w.W1), P(h),
+                                                        sp)
+            else:
+                st |= L.moe_permute(P(x), P(row_of), T, K, d, P(x_perm), sp)
+                rec(3)
+                st |= L.moe_grouped_gemm1_swiglu(P(x_perm), P(offsets), E, TK, d, f, P(w.W1), P(h), sp)
             rec(4)
             if args.fused_combine:
                 # GEMM2 and the combine in one kernel; the combine step below is empty
@@ -537,9 +550,10 @@ def measure_forward(moe, s_name, args, ws, rank, local, full=True):
     flops_step = 6.0 * TK * d * f
     res = {
         "config": s_name, "s": s, "value": aggregate(flops_step, ws, args.steps, elapsed_ms) / 1e12,
+        "fused_permute": bool(fuse_permute),
         "tokens_per_s": aggregate(T, ws, args.steps, elapsed_ms), "ms_per_step": ms_per_step,
         "launches": launches, "clocks": clocks, "timed_region_s": elapsed_ms * 1e-3,
-        "kernels": _kernel_table(s, kmean, mxfp8),
+        "kernels": _kernel_table(s, kmean, mxfp8, fuse_permute),
         "roofline": _dominant_roofline(s, s_name, kmean, counts, mxfp8, elapsed_ms * 1e-3),
         "routing": {"empty_experts": int((counts == 0).sum().item()), "max_group": int(counts.max().item()),
                     "batches": "two resident token batches (seeds r, r+1), alternating step by step"},
@@ -592,7 +606,7 @@ def measure_forward(moe, s_name, args, ws, rank, local, full=True):
     # ---- the whole layer (one moe_forward call) captured once as a CUDA graph
     # and replayed: the launch-overhead-free time of a step
     res["graph"] = None
-    if not mxfp8 and not args.fused_combine:
+    if not mxfp8 and not args.fused_combine and args.permute == "auto":
         # The graph reads its tokens from one static buffer; before every
         # replay a fresh batch is copied into it (two seeded batches,
         # alternating), so each replay routes differently and the graph is
@@ -670,7 +684,8 @@ def run_gpu(args):
                         "roofline": {kk: o["roofline"][kk] for kk in (
                             "bound", "kernel", "achieved", "peak", "unit", "frac", "frac_of_bf16_burst",
                             "frac_of_bf16_sustained", "frac_of_hbm")},
-                        "routing": o["routing"], "clocks": o["clocks"], "gpu_launches": o["launches"]}
+                        "routing": o["routing"], "clocks": o["clocks"], "gpu_launches": o["launches"],
+                        "fused_permute": o["fused_permute"]}
         r["launches"] += o["launches"]
     s = r["s"]
     if rank == 0:
@@ -683,7 +698,7 @@ def run_gpu(args):
             "tokens_per_s": r["tokens_per_s"], "kernels": r["kernels"], "roofline": r["roofline"],
             "cpu_baseline": r["cpu_baseline"], "e2e": r["e2e"], "gpu_launches": r["launches"],
             "clocks": r["clocks"], "timed_region_s": r["timed_region_s"], "graph": r["graph"],
-            "routing": r["routing"], "other_configs": others or None,
+            "routing": r["routing"], "fused_permute": r["fused_permute"], "other_configs": others or None,
         }
         print(json.dumps(line), flush=True)
     if ws > 1:
@@ -788,6 +803,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--fused-combine", action="store_true",
                     help="fuse the combine into GEMM2's epilogue (bf16 path)")
+    ap.add_argument("--permute", default="auto", choices=["auto", "fused", "separate"],
+                    help="bf16 path: fuse the permute into GEMM1's operand load, or run it as its own kernel; "
+                         "auto = moe_forward's choice for the shape (moe_forward_fuses_permute)")
     ap.add_argument("--backward", action="store_true",
                     help="time a training step of the layer (forward + backward) instead of the forward")
     ap.add_argument("--precision", default="bf16", choices=["bf16", "mxfp8"],
@@ -795,6 +813,8 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if (args.permute == "fused" or args.fused_combine) and args.precision != "bf16":
+        raise SystemExit("--permute fused and --fused-combine are bf16-path options")
     if args.impl == "reference":
         run_reference(args)
     elif args.backward:

@@ -25,7 +25,7 @@ __all__ = [
     "forward_views", "forward_host", "device_status", "last_device_status", "launch_count", "MoELayer",
     "mxfp8_quantize", "mxfp8_scales_size", "mxfp8_act_scales_size", "permute_mxfp8",
     "grouped_gemm1_swiglu_mxfp8", "grouped_gemm2_mxfp8", "forward_mxfp8", "forward_mxfp8_views", "MoELayerMXFP8",
-    "grouped_gemm2_combine",
+    "grouped_gemm2_combine", "grouped_gemm1_swiglu_gather", "last_device_status", "forward_fuses_permute",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -77,9 +77,11 @@ def _load():
         "moe_grouped_mlp": (I, [P, P, I, I, I, I, P, P, P, P, P]),
         "moe_grouped_gemm1_swiglu": (I, [P, P, I, I, I, I, P, P, P]),
         "moe_grouped_gemm1_swiglu_preact": (I, [P, P, I, I, I, I, P, P, P, P]),
+        "moe_grouped_gemm1_swiglu_gather": (I, [P, P, P, I, I, I, I, I, P, P, P]),
         "moe_grouped_gemm2": (I, [P, P, I, I, I, I, P, P, P]),
         "moe_unpermute": (I, [P, P, P, I, I, I, P, P]),
         "moe_forward_workspace_size": (S, [I, I, I, I, I]),
+        "moe_forward_fuses_permute": (I, [I, I, I, I, I]),
         "moe_forward_views": (I, [I, I, I, I, I, ctypes.POINTER(_Layout)]),
         "moe_forward": (I, [P, P, P, P, P, I, I, I, I, I, P, P, S, P]),
         "moe_forward_train": (I, [P, P, P, P, P, I, I, I, I, I, P, P, S, P, P]),
@@ -240,6 +242,24 @@ def grouped_gemm1_swiglu(x_perm, offsets, W1, h=None, preact=None, stream=None):
         _need(preact, torch.bfloat16, (TK, 2 * f), "preact")
         _check(lib.moe_grouped_gemm1_swiglu_preact(_ptr(x_perm), _ptr(offsets), E, TK, d, f, _ptr(W1), _ptr(h),
                                                    _ptr(preact), _stream(stream)), "moe_grouped_gemm1_swiglu_preact")
+    return h
+
+
+def grouped_gemm1_swiglu_gather(x, src_tok, offsets, W1, h=None, stream=None):
+    """GEMM1 + SwiGLU with the permute fused into its operand load: row r of
+    expert e's group is read as x[src_tok[r]]; h [TK, f] equals
+    grouped_gemm1_swiglu(permute(x, row_of), offsets, W1) bit for bit."""
+    T, d = x.shape
+    TK = src_tok.shape[0]
+    E = offsets.shape[0] - 1
+    f = W1.shape[1] // 2
+    _need(x, torch.bfloat16, (T, d), "x")
+    _need(src_tok, torch.int32, (TK,), "src_tok")
+    _need(offsets, torch.int32, (E + 1,), "offsets")
+    _need(W1, torch.bfloat16, (E, 2 * f, d), "W1")
+    h = _empty((TK, f), torch.bfloat16, x) if h is None else _need(h, torch.bfloat16, (TK, f), "h")
+    _check(lib.moe_grouped_gemm1_swiglu_gather(_ptr(x), _ptr(src_tok), _ptr(offsets), T, E, TK, d, f, _ptr(W1),
+                                               _ptr(h), _stream(stream)), "moe_grouped_gemm1_swiglu_gather")
     return h
 
 
@@ -443,6 +463,12 @@ def check_bounded_wait(limit_ns: int = 2_000_000, stream=None) -> None:
     _check(lib.moe_check_bounded_wait(limit_ns, _stream(stream)), "moe_check_bounded_wait")
 
 
+def forward_fuses_permute(T: int, d: int, E: int, K: int, f: int) -> bool:
+    """True when moe_forward fuses the permute into GEMM1 for these sizes
+    (then its workspace region x_perm is left unwritten)."""
+    return bool(lib.moe_forward_fuses_permute(T, d, E, K, f))
+
+
 def launch_count() -> int:
     return int(lib.moe_launch_count())
 
@@ -479,6 +505,9 @@ class MoELayer:
                                                device=x.device)
             pre = self._preact_buf[:n].view(x.shape[0] * self.K, 2 * self.f)
         self.preact = pre
+        # moe_forward may fuse the permute into GEMM1 and leave x_perm
+        # unwritten; the training forward (save_preact) always writes it
+        self._x_perm_written = save_preact or not forward_fuses_permute(x.shape[0], self.d, self.E, self.K, self.f)
         return forward(x, self.Wr, self.bias, self.W1, self.W2, self.K, out=out, workspace=self.workspace,
                        stream=stream, preact=pre)
 
@@ -495,6 +524,12 @@ class MoELayer:
             raise MoEError(2, "moe_backward_workspace_size")
         if workspace is None:
             workspace = torch.empty((n,), dtype=torch.uint8, device=x.device)
+        if not getattr(self, "_x_perm_written", True):
+            # the last forward fused the permute: write the grouped rows the
+            # backward reads (one permute kernel)
+            v = self.views(T)
+            permute(x, v["row_of"], out=v["x_perm"], stream=stream)
+            self._x_perm_written = True
         if grads is None:
             f32 = dict(dtype=torch.float32, device=x.device)
             grads = dict(dx=torch.empty((T, d), dtype=torch.bfloat16, device=x.device),

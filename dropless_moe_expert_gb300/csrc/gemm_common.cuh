@@ -46,6 +46,11 @@ struct Params {
     int *status;
     uint64_t timeout_ns;
     Combine comb;
+    // GEMM1 with the permute fused into its operand load (single-CTA kernel
+    // only): row r of A is gather_x[gather_src[r], :], gather_x [gather_T, Kdim]
+    const int32_t *gather_src;
+    const __nv_bfloat16 *gather_x;
+    int gather_T;
 };
 
 struct Tile {

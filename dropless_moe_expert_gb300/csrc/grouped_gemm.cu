@@ -47,6 +47,15 @@
 // tiles alternate, so their epilogues overlap the next mainloop.  3 stages of
 // 64 KB.
 //
+// Fused permute (GATHER, single-CTA GEMM1 only; "Optimization 2" of the page:
+// a naive dispatch writes and reads the tokens again): four more warps copy
+// the A rows straight from the token matrix x, row r being x[src_tok[r]],
+// with 16-byte cp.async into the same 128-byte-swizzled layout TMA writes.
+// Each gathering lane arrives on the stage's full barrier once its copies
+// have landed, beside the producer's transaction count for B; the MMA thread
+// fences the async proxy before the tensor core reads the rows.  The MMAs
+// see the same operand bytes as after a separate permute, so h is identical.
+//
 // CTA-pair variant (grouped_gemm_pair_kernel): clusters of 2 CTAs on 2 SMs
 // share a 256-row tile through cta_group::2 MMAs (M=256 x N=256).  Each CTA
 // loads its 128 A rows and half of the B columns (GEMM1: CTA 0 the gate rows,
@@ -69,6 +78,11 @@ constexpr int UMMA_K = 16;
 constexpr int TMEM_COLS = 2 * BN_ACC;
 constexpr int THREADS = 192;
 constexpr int BOX_ROWS = 128;  // every K-major TMA box is 128 rows x 64 bf16
+constexpr int GATHER_WARPS = 4;  // fused permute: warps 6..9 copy the A rows
+template <bool GATHER>
+constexpr int threads_of() {
+    return GATHER ? THREADS + 32 * GATHER_WARPS : THREADS;
+}
 constexpr int BT_BOX = 64 * 64 * 2;  // MN-major B box: 64 K rows x 64 columns
 
 // single-CTA variant
@@ -113,11 +127,44 @@ constexpr int P_SMEM_BYTES = L2::BYTES;
 static_assert(SMEM_BYTES <= 227 * 1024 && P_SMEM_BYTES <= 227 * 1024, "shared memory budget");
 static_assert(B_BYTES == (BN_ACC / 64) * BT_BOX && P_B_BYTES == 2 * BT_BOX, "MN-major B boxes fill the B slot");
 
+// Fused permute: the 8 rows of a 128-row block starting at row0 that this
+// lane copies, as pointers to their token rows in x, and a bit per row that
+// lies inside the group.  Lane l copies 16-byte chunk l % 8 of rows
+// 32 gw + 4 i + l / 8 (i = 0..7), so eight lanes move one whole 128-byte
+// line.  Rows past the group's end are not copied: row i of A reaches only
+// row i of the accumulator, which the epilogue masks, so whatever their
+// slot holds cannot reach a stored value.  A token index outside [0, T) is
+// clamped (outside the contract, but never read out of bounds).
+__device__ __forceinline__ uint32_t gather_sources(const Params &p, int row0, int grp_end, int gw, int lane,
+                                                   const __nv_bfloat16 *(&src)[8]) {
+    uint32_t valid = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int row = row0 + 32 * gw + 4 * i + (lane >> 3);
+        const int r = min(row, grp_end - 1);
+        const int tok = min(max(p.gather_src[r], 0), p.gather_T - 1);
+        src[i] = p.gather_x + static_cast<size_t>(tok) * p.Kdim + (lane & 7) * 8;
+        valid |= (row < grp_end ? 1u : 0u) << i;
+    }
+    return valid;
+}
+// Copies K slice kb of those rows into a 128-row A block `slot` (128-byte
+// swizzle: 16-byte chunk j of row r sits at chunk j ^ (r % 8) of its line).
+__device__ __forceinline__ void gather_block(uint8_t *slot, const __nv_bfloat16 *const (&src)[8], uint32_t valid,
+                                             int gw, int kb, int lane) {
+    const int j = lane & 7;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int r = 32 * gw + 4 * i + (lane >> 3);
+        if (valid & (1u << i)) cp_async_16(slot + r * (BK * 2) + ((j ^ (r & 7)) << 4), src[i] + kb * BK);
+    }
+}
+
 // ======================================================================
 // single-CTA variant
 // ======================================================================
-template <bool SWIGLU, bool BT>
-__global__ void __launch_bounds__(THREADS, 1)
+template <bool SWIGLU, bool BT, bool GATHER>
+__global__ void __launch_bounds__(threads_of<GATHER>(), 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ CUtensorMap tmPre,
                     const Params p) {
@@ -141,9 +188,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     const int E = p.E;
     const int NT = p.NT;
 
+    static_assert(!GATHER || (SWIGLU && !BT), "the fused permute feeds GEMM1 only");
     if (threadIdx.x == 0) {
         for (int i = 0; i < STAGES; ++i) {
-            mbar_init(&full[i], 1);
+            // fused permute: + one cp.async arrival per gathering lane
+            mbar_init(&full[i], GATHER ? 1 + 32 * GATHER_WARPS : 1);
             mbar_init(&empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -195,9 +244,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     if (!mbar_wait(&empty[stage], phase ^ 1u, s_abort, p.status, p.timeout_ns)) { ok = false; break; }
                     uint8_t *sa = smem + stage * STAGE_BYTES;
                     uint8_t *sb = sa + A_BYTES;
-                    mbar_arrive_expect_tx(&full[stage], (two ? 2 : 1) * A_BLOCK + B_BYTES);
-                    tma_load_2d(sa, &tmA, &full[stage], kb * BK, t.row0);
-                    if (two) tma_load_2d(sa + A_BLOCK, &tmA, &full[stage], kb * BK, t.row0 + BM);
+                    mbar_arrive_expect_tx(&full[stage], (GATHER ? 0 : (two ? 2 : 1) * A_BLOCK) + B_BYTES);
+                    if (!GATHER) {
+                        tma_load_2d(sa, &tmA, &full[stage], kb * BK, t.row0);
+                        if (two) tma_load_2d(sa + A_BLOCK, &tmA, &full[stage], kb * BK, t.row0 + BM);
+                    }
                     if (BT) {
                         // W[e] rows kb*64.., columns of the 256-wide block in 64-wide boxes
                         const int krow = t.e * p.Kdim + kb * BK;
@@ -244,6 +295,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 const uint32_t d1 = tmem_base + a1 * BN_ACC;
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!mbar_wait(&full[stage], phase, s_abort, p.status, p.timeout_ns)) { ok = false; break; }
+                    if (GATHER) fence_proxy_async_smem();  // cp.async rows -> tensor-core reads
                     tc_fence_after();
                     const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
                     const uint64_t adesc0 = smem_desc_kmajor_sw128(sa);
@@ -278,6 +330,31 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 mbar_wait(drain, 0, &no_abort, p.status, p.timeout_ns);
             }
         }
+    } else if (GATHER && warp >= 6) {
+        // fused permute: this warp's 32 rows of each A block of every stage
+        const int gw = warp - 6;
+        uint32_t stage = 0, phase = 0;
+        bool ok = true;
+        for (int k = 0, tile = round_position(0, blockIdx.x, gridDim.x, mix); ok && tile < total_tiles;
+             ++k, tile = round_position(k, blockIdx.x, gridDim.x, mix)) {
+            const Tile t =
+                decode_tile<TILE_ROWS, BAND>(visit_order(tile, total_tiles, mix), s_pre, s_off, s_end, E, NT);
+            const bool two = t.grp_end - t.row0 > BM;
+            const __nv_bfloat16 *src0[8], *src1[8];
+            const uint32_t v0 = gather_sources(p, t.row0, t.grp_end, gw, lane, src0);
+            const uint32_t v1 = two ? gather_sources(p, t.row0 + BM, t.grp_end, gw, lane, src1) : 0u;
+            for (int kb = 0; kb < KB; ++kb) {
+                int got = 1;
+                if (lane == 0) got = mbar_wait(&empty[stage], phase ^ 1u, s_abort, p.status, p.timeout_ns) ? 1 : 0;
+                if (!__shfl_sync(0xffffffffu, got, 0)) { ok = false; break; }
+                uint8_t *sa = smem + stage * STAGE_BYTES;
+                if (v0) gather_block(sa, src0, v0, gw, kb, lane);
+                if (v1) gather_block(sa + A_BLOCK, src1, v1, gw, kb, lane);
+                cp_async_arrive_noinc(&full[stage]);
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            }
+        }
+        cp_async_wait_all();  // this lane's copies have landed before the CTA's shared memory goes away
     } else {
         const int q = warp & 3;  // TMEM lane quarter this warp may access
         uint8_t *stage = smem + L1::OFF_EPI + (warp - 2) * 2 * EPI_BUF;
@@ -548,15 +625,29 @@ bool grouped_gemm_use_pair(int TK, int E) {
     return static_cast<int64_t>(TK) >= static_cast<int64_t>(E) * 384;
 }
 
+bool grouped_gemm1_prefers_gather(int TK, int E, int f) {
+    // The fused permute runs on the single-CTA kernel.  Where that kernel is
+    // chosen anyway, the fusion only removes the permute's x_perm round trip.
+    // Where the pair kernel would run, GEMM1 loses about 5-9% to the
+    // single-CTA kernel, while the permute's share of GEMM1's time falls as
+    // 1/f (its bytes are 4*TK*d, GEMM1's work 4*TK*d*f): measured on GB300,
+    // the fusion wins at f = 768 and 1536 and loses at f = 14336.
+    return !grouped_gemm_use_pair(TK, E) || f <= 4096;
+}
+
 cudaError_t launch_grouped_gemm(bool swiglu, const void *A, int TK, int Kdim, const void *W, int E, int n_out,
                                 const int32_t *offsets, void *out, const GemmLaunch &cfg, int *status,
                                 uint64_t timeout_ns, cudaStream_t stream, const CombineArgs *comb, bool b_trans,
-                                void *preact) {
+                                void *preact, const GatherArgs *gather) {
     CUtensorMap tmA, tmB;
     if (b_trans && (swiglu || comb)) return cudaErrorInvalidValue;
     if (preact && !swiglu) return cudaErrorInvalidValue;
+    if (gather && (!swiglu || b_trans || comb || gather->T < 1)) return cudaErrorInvalidValue;
     const int w_rows = swiglu ? 2 * n_out : n_out;
-    if (!make_tmap(&tmA, A, static_cast<uint64_t>(TK), static_cast<uint64_t>(Kdim), gg::BOX_ROWS, gg::BK))
+    // with the fused permute A is the token matrix [T, Kdim]; its rows are
+    // copied by the gather warps and the map goes unused
+    const uint64_t a_rows = gather ? static_cast<uint64_t>(gather->T) : static_cast<uint64_t>(TK);
+    if (!make_tmap(&tmA, A, a_rows, static_cast<uint64_t>(Kdim), gg::BOX_ROWS, gg::BK))
         return cudaErrorInvalidValue;
     if (b_trans) {
         // W as stored: [E * Kdim, n_out], 64 x 64 boxes
@@ -600,39 +691,51 @@ cudaError_t launch_grouped_gemm(bool swiglu, const void *A, int TK, int Kdim, co
     p.preact = static_cast<__nv_bfloat16 *>(preact);
     p.status = status;
     p.timeout_ns = timeout_ns;
+    const dim3 grid(cfg.num_sms);
+    if (gather) {
+        // the fused permute runs on the single-CTA kernel for every shape
+        p.gather_src = gather->src_tok;
+        p.gather_x = static_cast<const __nv_bfloat16 *>(A);
+        p.gather_T = gather->T;
+        gg::grouped_gemm_kernel<true, false, true>
+            <<<grid, gg::threads_of<true>(), gg::SMEM_BYTES, stream>>>(tmA, tmB, tmOut, tmPre, p);
+        return cudaGetLastError();
+    }
     const int pairs = swiglu ? cfg.pairs_swiglu : cfg.pairs_plain;
     if (grouped_gemm_use_pair(TK, E) && pairs > 0) {
         return swiglu    ? launch_pair<true, false>(tmA, tmB, tmOut, tmPre, p, 2 * pairs, stream)
                : b_trans ? launch_pair<false, true>(tmA, tmB, tmOut, tmPre, p, 2 * pairs, stream)
                          : launch_pair<false, false>(tmA, tmB, tmOut, tmPre, p, 2 * pairs, stream);
     }
-    const dim3 grid(cfg.num_sms);
     if (swiglu)
-        gg::grouped_gemm_kernel<true, false><<<grid, gg::THREADS, gg::SMEM_BYTES, stream>>>(tmA, tmB, tmOut, tmPre, p);
+        gg::grouped_gemm_kernel<true, false, false>
+            <<<grid, gg::THREADS, gg::SMEM_BYTES, stream>>>(tmA, tmB, tmOut, tmPre, p);
     else if (b_trans)
-        gg::grouped_gemm_kernel<false, true><<<grid, gg::THREADS, gg::SMEM_BYTES, stream>>>(tmA, tmB, tmOut, tmPre, p);
+        gg::grouped_gemm_kernel<false, true, false>
+            <<<grid, gg::THREADS, gg::SMEM_BYTES, stream>>>(tmA, tmB, tmOut, tmPre, p);
     else
-        gg::grouped_gemm_kernel<false, false><<<grid, gg::THREADS, gg::SMEM_BYTES, stream>>>(tmA, tmB, tmOut, tmPre,
-                                                                                            p);
+        gg::grouped_gemm_kernel<false, false, false>
+            <<<grid, gg::THREADS, gg::SMEM_BYTES, stream>>>(tmA, tmB, tmOut, tmPre, p);
     return cudaGetLastError();
 }
 
 cudaError_t grouped_gemm_setup(int num_sms, GemmLaunch *cfg) {
     cudaError_t e;
-    const void *single[3] = {reinterpret_cast<const void *>(gg::grouped_gemm_kernel<true, false>),
-                             reinterpret_cast<const void *>(gg::grouped_gemm_kernel<false, false>),
-                             reinterpret_cast<const void *>(gg::grouped_gemm_kernel<false, true>)};
+    const void *single[4] = {reinterpret_cast<const void *>(gg::grouped_gemm_kernel<true, false, false>),
+                             reinterpret_cast<const void *>(gg::grouped_gemm_kernel<false, false, false>),
+                             reinterpret_cast<const void *>(gg::grouped_gemm_kernel<false, true, false>),
+                             reinterpret_cast<const void *>(gg::grouped_gemm_kernel<true, false, true>)};
     const void *pair[3] = {reinterpret_cast<const void *>(gg::grouped_gemm_pair_kernel<true, false>),
                            reinterpret_cast<const void *>(gg::grouped_gemm_pair_kernel<false, false>),
                            reinterpret_cast<const void *>(gg::grouped_gemm_pair_kernel<false, true>)};
-    for (int i = 0; i < 3; ++i) {
+    for (int i = 0; i < 4; ++i)
         if ((e = cudaFuncSetAttribute(single[i], cudaFuncAttributeMaxDynamicSharedMemorySize, gg::SMEM_BYTES)) !=
             cudaSuccess)
             return e;
+    for (int i = 0; i < 3; ++i)
         if ((e = cudaFuncSetAttribute(pair[i], cudaFuncAttributeMaxDynamicSharedMemorySize, gg::P_SMEM_BYTES)) !=
             cudaSuccess)
             return e;
-    }
     cfg->num_sms = num_sms;
     // every pair must be resident at once (the kernel is persistent): never
     // launch more pairs than fit, nor more CTAs than SMs

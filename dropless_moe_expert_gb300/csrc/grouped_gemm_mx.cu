@@ -25,9 +25,11 @@
 //    after its stage's MMAs completed (the shared-memory stage was freed by
 //    their commit), so the ring needs no further synchronisation.
 //  * One accumulator (256 columns); the other 256 TMEM columns hold the
-//    scale ring.  The epilogue of a tile therefore runs between mainloops
-//    (the TMA producer keeps filling the ring meanwhile), and GEMM1's, which
-//    forms and quantises h, is spread over eight warps.
+//    scale ring.  GEMM1's epilogue, which forms and quantises h, is spread
+//    over eight warps; each thread loads its 128 accumulator values first
+//    and hands the accumulator back before the arithmetic and the stores, so
+//    those overlap the next tile's mainloop.  GEMM2's epilogue (256 columns
+//    per row) holds the accumulator until its last TMEM load.
 //  * Scale atoms are addressed by 128-row blocks: A and h by the tile's row
 //    block (rb = row blocks of earlier experts + the tile's block inside its
 //    expert), the weights by their global row / 128.  Every atom index is
@@ -106,31 +108,42 @@ __device__ __forceinline__ size_t clamp_atom(size_t a, size_t n) { return a < n 
 
 // GEMM1 epilogue of one warp: 32 rows and half (64) of the tile's 128 output
 // columns of h (gate columns 0..127 and up columns 128..255 of the
-// accumulator).  Each thread owns one row: per 32-column block it forms h,
-// quantises it and stores 32 code bytes; its two blocks' scale bytes are one
-// half-word of the row's word in the h atom for this row block and slice.
+// accumulator).  Each thread owns one row.  It first loads all 128 of its
+// accumulator values (the gate and up halves of its 64 columns) and then
+// releases the accumulator (`release`: fence, warp sync, arrive on tempty),
+// so the next tile's MMAs start while it forms h, quantises it per 32-column
+// block and stores the codes; its two blocks' scale bytes are one half-word
+// of the row's word in the h atom for this row block and slice.
+template <typename Release>
 __device__ __forceinline__ void epilogue_swiglu_mx(const MxParams &mp, uint32_t tbase, const gg::Tile &t, int q,
-                                                   int half, int lane, int rb) {
+                                                   int half, int lane, int rb, Release release) {
     const gg::Params &p = mp.g;
     const int wrow0 = t.row0 + q * 32;
-    if (wrow0 >= t.grp_end) return;  // warp-uniform
+    if (wrow0 >= t.grp_end) {  // warp-uniform: nothing of this warp's rows to store
+        release();
+        return;
+    }
     const int grow = wrow0 + lane;
     const bool row_ok = grow < t.grp_end;
+    uint32_t g[2][32], u[2][32];
+    tmem_ld_32x32b_x32(tbase + half * 64, g[0]);
+    tmem_ld_32x32b_x32(tbase + BN_ACC / 2 + half * 64, u[0]);
+    tmem_ld_32x32b_x32(tbase + half * 64 + 32, g[1]);
+    tmem_ld_32x32b_x32(tbase + BN_ACC / 2 + half * 64 + 32, u[1]);
+    tmem_ld_wait();
+    release();
     uint32_t scales = 0;
-#pragma unroll 1
-    for (int c = half * 64; c < half * 64 + 64; c += 32) {
-        uint32_t g[32], u[32];
-        tmem_ld_32x32b_x32(tbase + c, g);
-        tmem_ld_32x32b_x32(tbase + BN_ACC / 2 + c, u);
-        tmem_ld_wait();
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+        const int c = half * 64 + 32 * b;
         float h[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-            const float gv = __uint_as_float(g[i]);
-            h[i] = __fdividef(gv, 1.0f + __expf(-gv)) * __uint_as_float(u[i]);  // silu(g) * u
+            const float gv = __uint_as_float(g[b][i]);
+            h[i] = __fdividef(gv, 1.0f + __expf(-gv)) * __uint_as_float(u[b][i]);  // silu(g) * u
         }
         uint32_t packed[8];
-        scales |= mx::quant_block(h, packed) << (8 * ((c / 32) & 1));
+        scales |= mx::quant_block(h, packed) << (8 * b);
         if (row_ok) {
             uint4 *dst = reinterpret_cast<uint4 *>(mp.hq + static_cast<size_t>(grow) * p.n_out + t.n_blk * 128 + c);
             dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
@@ -296,14 +309,20 @@ grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
             if (!mbar_wait(tfull, acc_phase, s_abort, p.status, p.timeout_ns)) break;
             tc_fence_after();
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-            if (SWIGLU)
-                epilogue_swiglu_mx(mp, tbase, t, q, half, lane, s_pre[t.e] / NT + t.m_blk);
-            else
+            // hands the accumulator back to the MMA thread (after this warp's
+            // TMEM loads have completed)
+            auto release = [&]() {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty);
+            };
+            if (SWIGLU) {
+                epilogue_swiglu_mx(mp, tbase, t, q, half, lane, s_pre[t.e] / NT + t.m_blk, release);
+            } else {
                 gg::epilogue_tile<false>(p, &tmOut, nullptr, stage_buf, sbuf, tbase, t.n_blk, t.row0 + q * 32, lane,
                                          t.grp_end);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(tempty);
+                release();
+            }
             acc_phase ^= 1u;
         }
         if (lane == 0) bulk_wait_all();  // stores done before the CTA's shared memory goes away

@@ -92,6 +92,9 @@ cudaError_t grouped_gemm_setup(int num_sms, GemmLaunch *cfg);
 // True when the CTA-pair kernel is used for this shape (decided on host
 // sizes only, so the choice is the same for every routing).
 bool grouped_gemm_use_pair(int TK, int E);
+// True when the whole-layer forward fuses the permute into GEMM1 for this
+// shape (host sizes only).
+bool grouped_gemm1_prefers_gather(int TK, int E, int f);
 // GEMM2 with the combine fused into its epilogue: y [T, n_out] bf16 from the
 // rows it stores in `out` (then scratch); counters [T, ceil(n_out / 256)]
 // int32 must be zero at launch.
@@ -103,13 +106,20 @@ struct CombineArgs {
     int *counters;
     void *y;
 };
+// GEMM1 with the permute fused into its operand load: A is the token matrix
+// x [T, Kdim] and row r of the grouped operand is x[src_tok[r]].
+struct GatherArgs {
+    const int32_t *src_tok;  // [TK]
+    int T;
+};
 // swiglu: GEMM1 (out [TK, n_out=f], W [E, 2f, Kdim=d]); else GEMM2 (out [TK, n_out=d], W [E, d, Kdim=f]).
 // b_trans (plain only): W is [E, Kdim, n_out] and out = A . W[e] (no transpose in memory).
 // preact (GEMM1 only, nullable): also store the bf16 pre-activations [TK, 2 n_out] (gate | up).
+// gather (GEMM1 only, nullable): the fused permute (single-CTA kernel for every shape).
 cudaError_t launch_grouped_gemm(bool swiglu, const void *A, int TK, int Kdim, const void *W, int E, int n_out,
                                 const int32_t *offsets, void *out, const GemmLaunch &cfg, int *status,
                                 uint64_t timeout_ns, cudaStream_t stream, const CombineArgs *comb = nullptr,
-                                bool b_trans = false, void *preact = nullptr);
+                                bool b_trans = false, void *preact = nullptr, const GatherArgs *gather = nullptr);
 
 // A kernel whose only wait never completes: it times out after limit_ns and
 // records MOE_ERR_DEVICE_TIMEOUT in *status.

@@ -290,7 +290,7 @@ const char *moe_status_string(int status) {
     }
 }
 
-int moe_abi_version(void) { return 402; }
+int moe_abi_version(void) { return 403; }
 
 uint64_t moe_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
@@ -385,6 +385,24 @@ moe_status_t moe_grouped_gemm2(const uint16_t *h, const int32_t *offsets, int E,
     return run_gemm(false, h, offsets, E, TK, d, f, W2, y_perm, stream);
 }
 
+moe_status_t moe_grouped_gemm1_swiglu_gather(const uint16_t *x, const int32_t *src_tok, const int32_t *offsets,
+                                             int T, int E, int TK, int d, int f, const uint16_t *W1, uint16_t *h,
+                                             cudaStream_t stream) {
+    MOE_RANGE();
+    if (!x || !src_tok || !offsets || !W1 || !h) return MOE_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(W1, 16) || !aligned(h, 16) || !aligned(src_tok, 4) || !aligned(offsets, 4))
+        return MOE_ERR_INVALID_ARG;
+    moe_status_t st = check_shape(TK, d, E, 1, f, true, true);
+    if (st != MOE_OK) return st;
+    if (T < 1) return MOE_ERR_INVALID_ARG;
+    DeviceState *ds = nullptr;
+    if ((st = device_state(&ds)) != MOE_OK) return st;
+    const moe::GatherArgs g{src_tok, T};
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return cuda_status(moe::launch_grouped_gemm(true, x, TK, d, W1, E, f, offsets, h, ds->gemm, ds->status,
+                                                kWaitLimitNs, stream, nullptr, false, nullptr, &g));
+}
+
 size_t moe_combine_counters_size(int T, int d) {
     if (T < 1 || d < 64 || d % 64 != 0) return 0;
     return static_cast<size_t>(T) * ((d + 255) / 256) * sizeof(int32_t);
@@ -452,10 +470,16 @@ moe_status_t moe_forward_views(int T, int d, int E, int K, int f, moe_forward_la
     return MOE_OK;
 }
 
-moe_status_t moe_forward_train(const uint16_t *x, const float *Wr, const float *bias, const uint16_t *W1,
-                               const uint16_t *W2, int T, int d, int E, int K, int f, uint16_t *y, void *workspace,
-                               size_t workspace_bytes, uint16_t *preact, cudaStream_t stream) {
-    MOE_RANGE();
+}  // extern "C"
+
+namespace {
+
+// The forward of moe_forward and moe_forward_train.  `fuse_permute`: GEMM1
+// reads its rows straight from x (the permute fused into its operand load)
+// and x_perm is not written.
+moe_status_t forward_impl(const uint16_t *x, const float *Wr, const float *bias, const uint16_t *W1,
+                          const uint16_t *W2, int T, int d, int E, int K, int f, uint16_t *y, void *workspace,
+                          size_t workspace_bytes, uint16_t *preact, bool fuse_permute, cudaStream_t stream) {
     if (!x || !Wr || !W1 || !W2 || !y || !workspace) return MOE_ERR_INVALID_ARG;
     if (preact && !aligned(preact, 16)) return MOE_ERR_INVALID_ARG;
     if (!aligned(x, 16) || !aligned(W1, 16) || !aligned(W2, 16) || !aligned(y, 16) || !aligned(workspace, 16) ||
@@ -485,21 +509,43 @@ moe_status_t moe_forward_train(const uint16_t *x, const float *Wr, const float *
     if ((st = moe_route(logits, T, E, K, idx, w, counts, offsets, row_of, src_tok, at(L.route_ws),
                         L.router_ws - L.route_ws, stream)) != MOE_OK)
         return st;
-    if ((st = moe_permute(x, row_of, T, K, d, x_perm, stream)) != MOE_OK) return st;
-    if (preact)
-        st = moe_grouped_gemm1_swiglu_preact(x_perm, offsets, E, TK, d, f, W1, h, preact, stream);
-    else
-        st = moe_grouped_gemm1_swiglu(x_perm, offsets, E, TK, d, f, W1, h, stream);
+    if (fuse_permute) {
+        st = moe_grouped_gemm1_swiglu_gather(x, src_tok, offsets, T, E, TK, d, f, W1, h, stream);
+    } else {
+        if ((st = moe_permute(x, row_of, T, K, d, x_perm, stream)) != MOE_OK) return st;
+        if (preact)
+            st = moe_grouped_gemm1_swiglu_preact(x_perm, offsets, E, TK, d, f, W1, h, preact, stream);
+        else
+            st = moe_grouped_gemm1_swiglu(x_perm, offsets, E, TK, d, f, W1, h, stream);
+    }
     if (st != MOE_OK) return st;
     if ((st = moe_grouped_gemm2(h, offsets, E, TK, d, f, W2, y_perm, stream)) != MOE_OK) return st;
     return moe_unpermute(y_perm, row_of, w, T, K, d, y, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_forward_fuses_permute(int T, int d, int E, int K, int f) {
+    if (check_shape(T, d, E, K, f, true, true) != MOE_OK) return 0;
+    return moe::grouped_gemm1_prefers_gather(T * K, E, f) ? 1 : 0;
+}
+
+moe_status_t moe_forward_train(const uint16_t *x, const float *Wr, const float *bias, const uint16_t *W1,
+                               const uint16_t *W2, int T, int d, int E, int K, int f, uint16_t *y, void *workspace,
+                               size_t workspace_bytes, uint16_t *preact, cudaStream_t stream) {
+    MOE_RANGE();
+    // the backward reads x_perm: the training forward always writes it
+    return forward_impl(x, Wr, bias, W1, W2, T, d, E, K, f, y, workspace, workspace_bytes, preact, false, stream);
 }
 
 moe_status_t moe_forward(const uint16_t *x, const float *Wr, const float *bias, const uint16_t *W1,
                          const uint16_t *W2, int T, int d, int E, int K, int f, uint16_t *y, void *workspace,
                          size_t workspace_bytes, cudaStream_t stream) {
     MOE_RANGE();
-    return moe_forward_train(x, Wr, bias, W1, W2, T, d, E, K, f, y, workspace, workspace_bytes, nullptr, stream);
+    return forward_impl(x, Wr, bias, W1, W2, T, d, E, K, f, y, workspace, workspace_bytes, nullptr,
+                        moe_forward_fuses_permute(T, d, E, K, f) != 0, stream);
 }
 
 moe_status_t moe_forward_host(const uint16_t *x_host, const float *Wr, const float *bias, const uint16_t *W1,

@@ -126,6 +126,19 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
         : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared (both 16-byte aligned), through
+// L2 only (.cg).
+__device__ __forceinline__ void cp_async_16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+// Arrives on `bar` once every cp.async this thread issued before it has
+// landed.  .noinc: the arrival counts against the barrier's expected count,
+// which must include one per arriving thread.
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // Makes this thread's generic-proxy shared-memory writes visible to the
 // async proxy (TMA stores, tensor-core operand reads).
 __device__ __forceinline__ void fence_proxy_async_smem() {

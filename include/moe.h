@@ -165,6 +165,21 @@ moe_status_t moe_grouped_gemm1_swiglu_preact(const uint16_t *x_perm, const int32
                                              int E, int TK, int d, int f, const uint16_t *W1,
                                              uint16_t *h, uint16_t *preact, cudaStream_t stream);
 
+/* Steps a3 + a4 in one kernel (the permute fused into GEMM1's operand load;
+ * "Optimization 2": a naive dispatch reads and writes the tokens again).
+ * Computes h exactly as moe_permute followed by moe_grouped_gemm1_swiglu
+ * (bit-identical), without x_perm: row r of expert e's group is read as
+ * x[src_tok[r], :] (x [T, d] bf16, src_tok [TK] from moe_route).  It runs the
+ * single-CTA kernel for every shape, so on shapes whose average group holds
+ * 384 rows or more it is slower than the unfused pair; on the small-group
+ * shapes it trades the permute's x_perm round trip for row gathers.
+ * src_tok values outside [0, T) are outside the contract (they are clamped,
+ * never read out of bounds).  One kernel launch.  */
+moe_status_t moe_grouped_gemm1_swiglu_gather(const uint16_t *x, const int32_t *src_tok,
+                                             const int32_t *offsets, int T, int E, int TK, int d,
+                                             int f, const uint16_t *W1, uint16_t *h,
+                                             cudaStream_t stream);
+
 /* Steps a5 + a6 in one kernel (the combine fused into GEMM2's epilogue;
  * "Optimization 2": a naive dispatch/combine reads and writes the data many
  * times, TE fuses them into one pipeline).  Computes y exactly as
@@ -188,10 +203,20 @@ moe_status_t moe_grouped_gemm2_combine(const uint16_t *h, const int32_t *offsets
 moe_status_t moe_unpermute(const uint16_t *y_perm, const int32_t *row_of, const float *topk_w,
                            int T, int K, int d, uint16_t *y, cudaStream_t stream);
 
-/* The whole layer, a0..a6 in order on `stream` (9 kernel launches).
+/* The whole layer, a0..a6 in order on `stream` (9 kernel launches, or 8
+ * when the permute is fused into GEMM1).
  * `workspace` (16-byte aligned, moe_forward_workspace_size() bytes) holds
  * every intermediate; moe_forward_views() gives their byte offsets so that a
- * caller can inspect them after the call.  */
+ * caller can inspect them after the call.  Whether moe_forward fuses the
+ * permute into GEMM1 (moe_grouped_gemm1_swiglu_gather; the region x_perm is
+ * then left unwritten, and every other output is bit-identical) is decided
+ * on the sizes alone, so it is the same for every routing:
+ * moe_forward_fuses_permute() returns 1 for the shapes where it does, which
+ * are those whose grouped GEMMs run single-CTA tiles (average group under
+ * 384 rows) and those with f <= 4096, where the permute's round trip costs
+ * more than the CTA-pair kernel saves.  moe_forward_train never fuses it:
+ * the backward reads x_perm.  */
+int moe_forward_fuses_permute(int T, int d, int E, int K, int f);
 size_t moe_forward_workspace_size(int T, int d, int E, int K, int f);
 typedef struct {
     size_t logits, topk_idx, topk_w, counts, offsets, row_of, src_tok, route_ws,
@@ -318,8 +343,11 @@ moe_status_t moe_forward_mxfp8_host_pipelined(const uint16_t *const *x_hosts, ui
  * experts, softmax over the K selected logits).
  *   dx [T, d] bf16; dWr [d, E], dbias [E], dW1 [E, 2f, d], dW2 [E, d, f]
  *   fp32 (every expert's entries written, zeros for experts without tokens).
- * `fwd_workspace` is the workspace of a moe_forward call on the same x and
- * weights (it holds the routing, x_perm, h and y_perm the backward reuses);
+ * `fwd_workspace` is the workspace of a moe_forward_train call on the same
+ * x and weights (it holds the routing, x_perm, h and y_perm the backward
+ * reuses), or of a moe_forward call on sizes for which
+ * moe_forward_fuses_permute() is 0 (elsewhere moe_forward leaves x_perm
+ * unwritten: run moe_permute into its x_perm region first);
  * `preact` (nullable) the pre-activations a moe_forward_train call saved --
  * when null they are computed again (one more grouped GEMM, into the
  * workspace region `a`); `workspace` (128-byte aligned) holds

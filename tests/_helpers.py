@@ -153,6 +153,55 @@ def check_rounded(h_gpu, h_ref, what="h"):
     return r
 
 
+def stratified_rows(offsets, seed=0, block=128):
+    """Rows in the oracle's grouped numbering: one random row of every
+    block-row slice of every non-empty group (slices counted from the
+    group's first row, as the GEMM tiles are), plus each group's first and
+    last row."""
+    g = np.random.default_rng(seed)
+    rows = []
+    E = len(offsets) - 1
+    for e in range(E):
+        r0, r1 = int(offsets[e]), int(offsets[e + 1])
+        if r1 == r0:
+            continue
+        rows += [r0, r1 - 1]
+        for b0 in range(r0, r1, block):
+            rows.append(int(g.integers(b0, min(b0 + block, r1))))
+    return np.unique(np.array(rows, np.int64))
+
+
+def check_stratified_rows(h, y_perm, row_of, xs, idx, offsets, src_tok, same, W1, W2):
+    """h (and y_perm, unless None) of the stratified rows against the expert
+    FFN evaluated from the definition on the oracle's routing (idx, offsets,
+    src_tok), for rows of tokens routed identically on both sides (`same`).
+    h, y_perm, row_of: the GPU's tensors; W1, W2: the layer's weights (any
+    device).  Returns (rows checked, experts touched)."""
+    rows_o = stratified_rows(offsets)
+    tok = np.asarray(src_tok)[rows_o]
+    keep = same[tok]
+    rows_o, tok = rows_o[keep], tok[keep]
+    e_of = np.searchsorted(offsets, rows_o, side="right") - 1
+    k_of = np.argmax(idx[tok] == e_of[:, None], axis=1)
+    assert np.all(idx[tok, k_of] == e_of)
+    rows_g = to_np(row_of)[tok, k_of]
+    sel = torch.from_numpy(rows_g).to(h.device)
+    h_g = to_np(h[sel])
+    yp_g = to_np(y_perm[sel]) if y_perm is not None else None
+    h_ref = np.zeros(h_g.shape)
+    yp_ref = np.zeros(yp_g.shape) if yp_g is not None else None
+    for e in np.unique(e_of):
+        m = e_of == e
+        he, ye = oracle.expert_ffn(xs[tok[m]], to_np(W1[int(e)]), to_np(W2[int(e)]))
+        h_ref[m] = he
+        if yp_ref is not None:
+            yp_ref[m] = ye
+    check_rounded(h_g, h_ref, "h (stratified rows)")
+    if yp_g is not None:
+        check_output(yp_g, yp_ref, "y_perm (stratified rows)")
+    return len(rows_o), len(np.unique(e_of))
+
+
 def run_layer(x, w, K, fill_nan=True):
     """Runs the whole layer with moe.MoELayer on the tensors' device; the
     workspace is filled with 0xFF bytes first (NaN in bf16 and fp32, -1 in
@@ -198,8 +247,11 @@ def compare_small(x, w, K):
     else:
         check_dispatch_valid(v, T, K, E)
     src_tok = to_np(v["src_tok"])
-    xp = v["x_perm"].view(torch.int16).cpu().numpy()
-    assert np.array_equal(xp, x.view(torch.int16).cpu().numpy()[src_tok]), "x_perm"
+    import dropless_moe_expert_gb300 as moe
+    if not moe.forward_fuses_permute(T, xs.shape[1], E, K, W1.shape[1] // 2):
+        # the layer wrote x_perm (else GEMM1 read the rows straight from x)
+        xp = v["x_perm"].view(torch.int16).cpu().numpy()
+        assert np.array_equal(xp, x.view(torch.int16).cpu().numpy()[src_tok]), "x_perm"
     # rows of the equally routed tokens, matched through each side's row_of
     rg = to_np(v["row_of"])[same].ravel()
     ro = ref["row_of"][same].ravel()

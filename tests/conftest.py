@@ -11,6 +11,11 @@ if ROOT not in sys.path:
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a)")
     config.addinivalue_line("markers", "slow: full-size workload (minutes)")
+    # the test modules import the package, which loads the in-tree CUDA
+    # library: bring it (and the oracle's C part) up to date first (a no-op
+    # when nothing changed since the last build)
+    import __graft_entry__
+    __graft_entry__.build()
 
 
 def pytest_collection_modifyitems(config, items):

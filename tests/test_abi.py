@@ -45,7 +45,7 @@ def test_status_strings(moe):
         s = moe.lib.moe_status_string(code).decode()
         assert s.startswith("MOE_")
     assert moe.lib.moe_status_string(99).decode() == "unknown moe_status_t"
-    assert moe.lib.moe_abi_version() == 402
+    assert moe.lib.moe_abi_version() == 403
 
 
 def test_workspace_sizes(moe):
@@ -88,6 +88,11 @@ def test_forward_rejects_bad_shapes(moe, args, code):
 
 def test_null_and_misaligned_pointers_rejected(moe):
     L = moe.lib
+    # the fused-permute GEMM1: null, misaligned and bad sizes
+    assert L.moe_grouped_gemm1_swiglu_gather(None, FAKE, FAKE, 8, 8, 16, 64, 64, FAKE, FAKE, None) == 1
+    assert L.moe_grouped_gemm1_swiglu_gather(FAKE + 2, FAKE, FAKE, 8, 8, 16, 64, 64, FAKE, FAKE, None) == 1
+    assert L.moe_grouped_gemm1_swiglu_gather(FAKE, FAKE, FAKE, 0, 8, 16, 64, 64, FAKE, FAKE, None) == 1
+    assert L.moe_grouped_gemm1_swiglu_gather(FAKE, FAKE, FAKE, 8, 8, 16, 96, 64, FAKE, FAKE, None) == 2
     # the status read checks its pointer before it touches CUDA
     assert L.moe_last_device_status(None, None) == 1
     assert L.moe_last_device_status(FAKE + 2, None) == 1

@@ -14,7 +14,7 @@ import oracle
 from workloads import LayerWeights, Shape, make_tokens, make_weights, random_shape_cases, shape
 
 from _helpers import (W_TOL, check_dispatch_valid, check_logits, check_output, check_rounded, check_routing,
-                      compare_small, run_layer, to_np, weight_tol)
+                      check_stratified_rows, compare_small, run_layer, to_np, weight_tol)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -182,6 +182,31 @@ def test_route_ties_and_signed_zeros_direct():
     assert np.array_equal(to_np(r.src_tok), src_tok)
 
 
+@pytest.mark.parametrize("s", [Shape(T=517, d=320, E=16, K=4, f=448), Shape(T=2048, d=256, E=4, K=1, f=256),
+                               Shape(T=1024, d=256, E=2, K=2, f=4160)],
+                         ids=["single_cta", "pair_small_f", "pair_large_f"])
+def test_forward_permute_choice_is_bit_identical(s):
+    """moe_forward fuses the permute into GEMM1 on some shapes (sizes alone
+    decide); its output equals the unfused step-by-step path's bit for bit
+    either way, and the training forward (which keeps x_perm) gives the same y."""
+    import dropless_moe_expert_gb300 as moe
+    x, w = _cpu_case(s, seed=12)
+    fused = moe.forward_fuses_permute(s.T, s.d, s.E, s.K, s.f)
+    TK = s.T * s.K
+    assert fused == ((TK < 384 * s.E) or s.f <= 4096)
+    y_one, v, layer = run_layer(x, w, s.K)
+    L = moe.router_logits(x, w.Wr, w.bias)
+    r = moe.route(L, s.K)
+    y = moe.unpermute(moe.grouped_gemm2(moe.grouped_gemm1_swiglu(moe.permute(x, r.row_of), r.offsets, w.W1),
+                                        r.offsets, w.W2), r.row_of, r.topk_w)
+    y_train = torch.empty_like(y)
+    layer(x, out=y_train, save_preact=True)
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int16), y_one.view(torch.int16))
+    assert torch.equal(y_train.view(torch.int16), y_one.view(torch.int16))
+    assert torch.equal(layer.views(s.T)["x_perm"].view(torch.int16), x.view(torch.int16)[r.src_tok.long()])
+
+
 def test_step_by_step_api_matches_single_call():
     import dropless_moe_expert_gb300 as moe
     s = Shape(T=517, d=320, E=16, K=4, f=448)
@@ -208,49 +233,6 @@ def test_host_buffers_entry_point():
 
 
 # ---------------------------------------------------------------- full size
-def _stratified_rows(offsets, seed=0, block=128):
-    """Rows in the oracle's grouped numbering: one random row of every
-    block-row slice of every non-empty group (slices counted from the
-    group's first row, as the GEMM tiles are), plus each group's first and
-    last row."""
-    g = np.random.default_rng(seed)
-    rows = []
-    E = len(offsets) - 1
-    for e in range(E):
-        r0, r1 = int(offsets[e]), int(offsets[e + 1])
-        if r1 == r0:
-            continue
-        rows += [r0, r1 - 1]
-        for b0 in range(r0, r1, block):
-            rows.append(int(g.integers(b0, min(b0 + block, r1))))
-    return np.unique(np.array(rows, np.int64))
-
-
-def _check_stratified_rows(v, xs, idx, offsets, src_tok, same, W1, W2):
-    """h and y_perm of the stratified rows against the expert FFN evaluated
-    from the definition on the oracle's routing (rows of tokens routed
-    identically on both sides)."""
-    rows_o = _stratified_rows(offsets)
-    tok = np.asarray(src_tok)[rows_o]
-    keep = same[tok]
-    rows_o, tok = rows_o[keep], tok[keep]
-    e_of = np.searchsorted(offsets, rows_o, side="right") - 1
-    k_of = np.argmax(idx[tok] == e_of[:, None], axis=1)
-    assert np.all(idx[tok, k_of] == e_of)
-    rows_g = to_np(v["row_of"])[tok, k_of]
-    sel = torch.from_numpy(rows_g).to(DEV)
-    h_g = to_np(v["h"][sel])
-    yp_g = to_np(v["y_perm"][sel])
-    h_ref = np.zeros(h_g.shape)
-    yp_ref = np.zeros(yp_g.shape)
-    for e in np.unique(e_of):
-        m = e_of == e
-        h_ref[m], yp_ref[m] = oracle.expert_ffn(xs[tok[m]], to_np(W1[int(e)]), to_np(W2[int(e)]))
-    check_rounded(h_g, h_ref, "h (stratified rows)")
-    check_output(yp_g, yp_ref, "y_perm (stratified rows)")
-    return len(rows_o), len(np.unique(e_of))
-
-
 def _sample_tokens(T, v, K, n=24, seed=0):
     g = np.random.default_rng(seed)
     toks = set(g.choice(T, size=min(n, T), replace=False).tolist()) | {0, T - 1}
@@ -305,14 +287,17 @@ def test_full_size_workload(name):
         assert np.array_equal(to_np(v["src_tok"]), src_tok)
     else:
         check_dispatch_valid(v, s.T, s.K, s.E)
-    # every permuted row is its token's row (checked on the device, bit patterns)
-    st = v["src_tok"].long()
-    assert torch.equal(v["x_perm"].view(torch.int16), x.view(torch.int16)[st])
-    del st
+    # every permuted row is its token's row (checked on the device, bit
+    # patterns), where the layer wrote x_perm rather than fusing the permute
+    if not moe.forward_fuses_permute(s.T, s.d, s.E, s.K, s.f):
+        st = v["src_tok"].long()
+        assert torch.equal(v["x_perm"].view(torch.int16), x.view(torch.int16)[st])
+        del st
 
     # one row of every 128-row slice of every live group, and each group's
     # first and last rows, from the definition
-    nrows, nexp = _check_stratified_rows(v, xs, idx, offsets, src_tok, same, w.W1, w.W2)
+    nrows, nexp = check_stratified_rows(v["h"], v["y_perm"], v["row_of"], xs, idx, offsets, src_tok, same,
+                                        w.W1, w.W2)
 
     # sampled tokens through the oracle, one by one
     toks = _sample_tokens(s.T, v, s.K)
