@@ -45,6 +45,10 @@ struct Params {
     __nv_bfloat16 *preact;  // GEMM1 only, nullable: [TK, 2 n_out] gate | up pre-activations, bf16
     int *status;
     uint64_t timeout_ns;
+    // Dynamic tile order (nullable: static round-robin): two ints, zero at
+    // launch, shared by every CTA of the launch -- [0] the next ticket, [1]
+    // the CTAs done; the last CTA to finish sets both back to zero.
+    int *sched;
     Combine comb;
     // GEMM1 with the permute fused into its operand load (single-CTA kernel
     // only): row r of A is gather_x[gather_src[r], :], gather_x [gather_T, Kdim]
@@ -141,6 +145,50 @@ __device__ __forceinline__ int visit_order(int p, int N, int mix) {
 // operands in L2) close together even when workers drift apart.
 __device__ __forceinline__ int round_position(int k, int c, int G, int mix) {
     return k * G + ((mix && (k & 1)) ? G - 1 - c : c);
+}
+
+// ------------------------------------------------------------ tile queue
+// The producer thread decides the CTA's (or CTA pair's) next tile and hands it
+// to the CTA's other roles through a ring of shared-memory slots: slot j % Q
+// holds the j-th tile, and its `full` barrier takes the producer's arrival
+// after the store.  The next tile is the static round-robin position
+// (Params::sched == nullptr) or a ticket drawn from the launch's global
+// counter: a CTA that finishes early then takes the next tile in visit order,
+// so no worker falls behind the others by more than a tile, and the tiles in
+// flight stay a contiguous window of the visit order (neighbours share
+// operands in L2).  A slot holds -1 after the last tile.
+//
+// No reader frees its slot: the pipeline itself bounds how far the producer
+// can run ahead of every reader.  The producer publishes tile k + 1 when it
+// starts loading tile k's stages, which needs the stages of S ring positions
+// earlier to have been consumed by the MMAs, so the MMAs are at most S tiles
+// behind (S stages of one slice each in the worst case); the MMAs of tile m
+// need the accumulator of tile m - 2 drained, so the epilogue is at most two
+// tiles behind them; the loaders of the other operand (gather warps, the
+// second CTA of a pair) complete the MMAs' stages, so they are within S
+// stages of the producer.  At most S + 3 published tiles are unread at any
+// time, and a ring of Q >= S + 4 slots is never overwritten before it is read.
+__host__ __device__ constexpr int queue_slots(int stages) { return stages + 4 <= 8 ? 8 : 16; }
+
+// First position (round 0) of worker c of G.
+__device__ __forceinline__ int first_position(const Params &p, int c, int G, int mix) {
+    return p.sched ? atomicAdd(p.sched, 1) : round_position(0, c, G, mix);
+}
+// Position of round k + 1, drawn while round k's tile is being loaded.
+__device__ __forceinline__ int next_position(const Params &p, int k, int c, int G, int mix) {
+    return p.sched ? atomicAdd(p.sched, 1) : round_position(k + 1, c, G, mix);
+}
+// End of the launch for a CTA (one thread, after the CTA's last use of the
+// counter): the last of the launch's CTAs resets it for the next launch,
+// which stream order places after this one.
+__device__ __forceinline__ void sched_retire(const Params &p) {
+    if (!p.sched) return;
+    __threadfence();
+    if (atomicAdd(p.sched + 1, 1) == static_cast<int>(gridDim.x) - 1) {
+        atomicExch(p.sched, 0);
+        atomicExch(p.sched + 1, 0);
+        __threadfence();
+    }
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

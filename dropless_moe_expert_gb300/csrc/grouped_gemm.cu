@@ -64,6 +64,7 @@
 // signal its full barrier, its commits free both CTAs' stages, and both CTAs'
 // epilogues release its accumulator.
 #include <algorithm>
+#include <atomic>
 
 #include "gemm_common.cuh"
 #include "kernels.h"
@@ -108,16 +109,20 @@ constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
 
 template <int NSTAGES, int STAGE>
 struct Layout {
+    static constexpr int TQ = queue_slots(NSTAGES);
+    static_assert(TQ >= NSTAGES + 4, "tile queue shorter than the pipeline's lead");
     static constexpr int OFF_EPI = NSTAGES * STAGE;  // 1024-aligned: the ring is whole KBs
     static constexpr int OFF_BARS = OFF_EPI + EPI_BYTES;
-    static constexpr int NUM_BARS = 2 * NSTAGES + 5;  // full, empty, tfull[2], tempty[2], drain
+    // full, empty, tfull[2], tempty[2], drain, qfull[TQ]
+    static constexpr int NUM_BARS = 2 * NSTAGES + 5 + TQ;
     static constexpr int OFF_TMEM = OFF_BARS + NUM_BARS * 8;
     static constexpr int OFF_ABORT = OFF_TMEM + 4;
     static constexpr int OFF_OFFS = OFF_ABORT + 4;
     static constexpr int OFF_ENDS = OFF_OFFS + MAX_E * 4;
     static constexpr int OFF_PRE = OFF_ENDS + MAX_E * 4;
     static constexpr int OFF_MIX = OFF_PRE + (MAX_E + 1) * 4;
-    static constexpr int USED = OFF_MIX + 4;
+    static constexpr int OFF_TQ = OFF_MIX + 4;  // tile-queue slots
+    static constexpr int USED = OFF_TQ + TQ * 4;
     static constexpr int BYTES = USED + 1024;  // slack for 1024-byte alignment
 };
 using L1 = Layout<STAGES, STAGE_BYTES>;
@@ -163,7 +168,7 @@ __device__ __forceinline__ void gather_block(uint8_t *slot, const __nv_bfloat16 
 // ======================================================================
 // single-CTA variant
 // ======================================================================
-template <bool SWIGLU, bool BT, bool GATHER>
+template <bool SWIGLU, bool BT, bool GATHER, bool DYN>
 __global__ void __launch_bounds__(threads_of<GATHER>(), 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ CUtensorMap tmPre,
@@ -176,6 +181,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     uint64_t *tfull = bars + 2 * STAGES;
     uint64_t *tempty = bars + 2 * STAGES + 2;
     uint64_t *drain = bars + 2 * STAGES + 4;
+    constexpr int TQ = L1::TQ;
+    uint64_t *qfull = bars + 2 * STAGES + 5;
+    volatile int *s_tq = reinterpret_cast<volatile int *>(smem + L1::OFF_TQ);
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(smem + L1::OFF_TMEM);
     volatile int *s_abort = reinterpret_cast<volatile int *>(smem + L1::OFF_ABORT);
     int *s_off = reinterpret_cast<int *>(smem + L1::OFF_OFFS);
@@ -189,6 +197,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     const int NT = p.NT;
 
     static_assert(!GATHER || (SWIGLU && !BT), "the fused permute feeds GEMM1 only");
+    static_assert(!(GATHER && DYN), "the fused-permute kernel keeps the static order");
     if (threadIdx.x == 0) {
         for (int i = 0; i < STAGES; ++i) {
             // fused permute: + one cp.async arrival per gathering lane
@@ -200,6 +209,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             mbar_init(&tempty[i], 4);
         }
         mbar_init(drain, 1);
+        for (int i = 0; i < TQ; ++i) mbar_init(&qfull[i], 1);
         *s_abort = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmA);
@@ -225,9 +235,30 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 #pragma unroll
             for (int i = 0; i < STAGES; ++i) armed_phase[i] = -1;
             uint32_t stage = 0, phase = 0;
-            bool ok = true;
-            for (int k = 0, tile = round_position(0, blockIdx.x, gridDim.x, mix); ok && tile < total_tiles;
-                 ++k, tile = round_position(k, blockIdx.x, gridDim.x, mix)) {
+            // Tiles are handed to the other roles one ahead of this thread's
+            // own loads, and drawn two ahead: tile k + 1 is published when tile
+            // k's loads begin, and the position of tile k + 2 drawn then, its
+            // latency hidden behind those loads.
+            auto publish = [&](int k, int tile) {
+                s_tq[k % TQ] = tile;
+                mbar_arrive(&qfull[k % TQ]);
+                return true;
+            };
+            // (static order, !DYN: every role computes the positions itself)
+            int cur = DYN ? first_position(p, blockIdx.x, gridDim.x, mix) : round_position(0, blockIdx.x, gridDim.x, mix);
+            cur = cur < total_tiles ? cur : -1;
+            int nxt = (DYN && cur >= 0) ? next_position(p, 0, blockIdx.x, gridDim.x, mix) : total_tiles;
+            bool ok = DYN ? publish(0, cur) : true;
+            for (int k = 0; ok && cur >= 0; ++k) {
+                const int tile = cur;
+                if (DYN) {
+                    cur = nxt < total_tiles ? nxt : -1;
+                    if (!publish(k + 1, cur)) { ok = false; break; }
+                    if (cur >= 0) nxt = next_position(p, k + 1, blockIdx.x, gridDim.x, mix);
+                } else {
+                    cur = round_position(k + 1, blockIdx.x, gridDim.x, mix);
+                    cur = cur < total_tiles ? cur : -1;
+                }
                 const Tile t =
                     decode_tile<TILE_ROWS, BAND>(visit_order(tile, total_tiles, mix), s_pre, s_off, s_end, E, NT);
                 const bool two = t.grp_end - t.row0 > BM;  // both row blocks of the tile hold rows
@@ -282,8 +313,16 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             uint32_t ph[2] = {0u, 0u};
             bool ok = true;
             bool issued = false;
-            for (int k = 0, tile = round_position(0, blockIdx.x, gridDim.x, mix); ok && tile < total_tiles;
-                 ++k, tile = round_position(k, blockIdx.x, gridDim.x, mix)) {
+            for (int k = 0; ok; ++k) {
+                int tile;
+                if (DYN) {
+                    if (!mbar_wait(&qfull[k % TQ], (k / TQ) & 1u, s_abort, p.status, p.timeout_ns)) { ok = false; break; }
+                    tile = s_tq[k % TQ];
+                    if (tile < 0) break;
+                } else {
+                    tile = round_position(k, blockIdx.x, gridDim.x, mix);
+                    if (tile >= total_tiles) break;
+                }
                 const Tile t =
                     decode_tile<TILE_ROWS, BAND>(visit_order(tile, total_tiles, mix), s_pre, s_off, s_end, E, NT);
                 const bool two = t.grp_end - t.row0 > BM;
@@ -335,8 +374,16 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         const int gw = warp - 6;
         uint32_t stage = 0, phase = 0;
         bool ok = true;
-        for (int k = 0, tile = round_position(0, blockIdx.x, gridDim.x, mix); ok && tile < total_tiles;
-             ++k, tile = round_position(k, blockIdx.x, gridDim.x, mix)) {
+        for (int k = 0; ok; ++k) {
+            int tile;
+            if (DYN) {
+                if (!mbar_wait(&qfull[k % TQ], (k / TQ) & 1u, s_abort, p.status, p.timeout_ns)) break;
+                tile = s_tq[k % TQ];
+                if (tile < 0) break;
+            } else {
+                tile = round_position(k, blockIdx.x, gridDim.x, mix);
+                if (tile >= total_tiles) break;
+            }
             const Tile t =
                 decode_tile<TILE_ROWS, BAND>(visit_order(tile, total_tiles, mix), s_pre, s_off, s_end, E, NT);
             const bool two = t.grp_end - t.row0 > BM;
@@ -362,8 +409,16 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         uint32_t acc = 0;
         uint32_t ph[2] = {0u, 0u};  // the MMA thread's accumulator order, mirrored
         bool ok = true;
-        for (int k = 0, tile = round_position(0, blockIdx.x, gridDim.x, mix); ok && tile < total_tiles;
-             ++k, tile = round_position(k, blockIdx.x, gridDim.x, mix)) {
+        for (int k = 0; ok; ++k) {
+            int tile;
+            if (DYN) {
+                if (!mbar_wait(&qfull[k % TQ], (k / TQ) & 1u, s_abort, p.status, p.timeout_ns)) break;
+                tile = s_tq[k % TQ];
+                if (tile < 0) break;
+            } else {
+                tile = round_position(k, blockIdx.x, gridDim.x, mix);
+                if (tile >= total_tiles) break;
+            }
             const Tile t =
                 decode_tile<TILE_ROWS, BAND>(visit_order(tile, total_tiles, mix), s_pre, s_off, s_end, E, NT);
             const int nblk = t.grp_end - t.row0 > BM ? 2 : 1;
@@ -390,12 +445,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         tc_fence_after();
         tmem_dealloc(tmem_base, TMEM_COLS);
     }
+    if (threadIdx.x == 0) sched_retire(p);
 }
 
 // ======================================================================
 // CTA-pair variant (cluster of 2)
 // ======================================================================
-template <bool SWIGLU, bool BT>
+template <bool SWIGLU, bool BT, bool DYN>
 __global__ void __launch_bounds__(THREADS, 1)
 grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                          const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ CUtensorMap tmPre,
@@ -408,6 +464,9 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
     uint64_t *tfull = bars + 2 * P_STAGES;       // both CTAs
     uint64_t *tempty = bars + 2 * P_STAGES + 2;  // CTA 0 only: 4 warps x 2 CTAs arrive
     uint64_t *drain = bars + 2 * P_STAGES + 4;
+    constexpr int TQ = L2::TQ;
+    uint64_t *qfull = bars + 2 * P_STAGES + 5;   // both CTAs
+    volatile int *s_tq = reinterpret_cast<volatile int *>(smem + L2::OFF_TQ);
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(smem + L2::OFF_TMEM);
     volatile int *s_abort = reinterpret_cast<volatile int *>(smem + L2::OFF_ABORT);
     int *s_off = reinterpret_cast<int *>(smem + L2::OFF_OFFS);
@@ -433,6 +492,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
             mbar_init(&tempty[i], 8);
         }
         mbar_init(drain, 1);
+        for (int i = 0; i < TQ; ++i) mbar_init(&qfull[i], 1);
         *s_abort = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmA);
@@ -466,8 +526,47 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
             for (int i = 0; i < P_STAGES; ++i) armed_phase[i] = -1;
             uint32_t stage = 0, phase = 0;
             bool ok = true;
-            for (int k = 0, tile = round_position(0, pair, npairs, mix); ok && tile < total_tiles;
-                 ++k, tile = round_position(k, pair, npairs, mix)) {
+            // CTA 0 decides the pair's tiles and writes each into both CTAs' queue
+            const uint32_t tq_peer = mapa_shared(smem_u32(const_cast<int *>(s_tq)), 1);
+            const uint32_t qfull_peer = mapa_shared(smem_u32(&qfull[0]), 1);
+            // DYN: CTA 0 publishes tile k + 1 to both CTAs when its loads of
+            // tile k begin, and draws the position of tile k + 2 then (see the
+            // single-CTA kernel), so CTA 1 learns each tile well before its
+            // stages free up.  Otherwise both CTAs follow the static order.
+            auto publish = [&](int k, int tile) {
+                s_tq[k % TQ] = tile;
+                st_shared_cluster(tq_peer + 4u * (k % TQ), tile);
+                mbar_arrive(&qfull[k % TQ]);
+                mbar_arrive_cluster(qfull_peer + 8u * (k % TQ));
+                return true;
+            };
+            int cur = -1, nxt = total_tiles;
+            if (DYN && rank == 0) {
+                cur = first_position(p, pair, npairs, mix);
+                cur = cur < total_tiles ? cur : -1;
+                nxt = cur >= 0 ? next_position(p, 0, pair, npairs, mix) : total_tiles;
+                ok = publish(0, cur);
+            }
+            for (int k = 0; ok; ++k) {
+                int tile;
+                if (!DYN) {
+                    // static order: both CTAs compute the pair's positions themselves
+                    tile = round_position(k, pair, npairs, mix);
+                    if (tile >= total_tiles) break;
+                } else if (rank == 0) {
+                    tile = cur;
+                    if (tile < 0) break;
+                    cur = nxt < total_tiles ? nxt : -1;
+                    if (!publish(k + 1, cur)) { ok = false; break; }
+                    if (cur >= 0) nxt = next_position(p, k + 1, pair, npairs, mix);
+                } else {
+                    if (!mbar_wait<true>(&qfull[k % TQ], (k / TQ) & 1u, s_abort, p.status, p.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    tile = s_tq[k % TQ];
+                    if (tile < 0) break;
+                }
                 const Tile t = decode_tile<P_BM, P_BAND>(visit_order(tile, total_tiles, mix), s_pre, s_off, s_end, E, NT);
                 const int a_row = t.row0 + 128 * static_cast<int>(rank);
                 // GEMM1: CTA 0 loads the gate rows, CTA 1 the up rows (f rows later);
@@ -513,8 +612,13 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
             bool ok = true;
             bool issued = false;
-            for (int k = 0, tile = round_position(0, pair, npairs, mix); ok && tile < total_tiles;
-                 ++k, tile = round_position(k, pair, npairs, mix)) {
+            for (int k = 0; ok; ++k) {
+                if (DYN) {
+                    if (!mbar_wait(&qfull[k % TQ], (k / TQ) & 1u, s_abort, p.status, p.timeout_ns)) { ok = false; break; }
+                    if (s_tq[k % TQ] < 0) break;
+                } else if (round_position(k, pair, npairs, mix) >= total_tiles) {
+                    break;
+                }
                 if (!mbar_wait<true>(&tempty[acc], acc_phase ^ 1u, s_abort, p.status, p.timeout_ns)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN_ACC;
@@ -549,8 +653,16 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
         uint32_t sbuf = 0;
         const uint32_t tempty0 = mapa_shared(smem_u32(&tempty[0]), 0);
         uint32_t acc = 0, acc_phase = 0;
-        for (int k = 0, tile = round_position(0, pair, npairs, mix); tile < total_tiles;
-             ++k, tile = round_position(k, pair, npairs, mix)) {
+        for (int k = 0;; ++k) {
+            int tile;
+            if (DYN) {
+                if (!mbar_wait<true>(&qfull[k % TQ], (k / TQ) & 1u, s_abort, p.status, p.timeout_ns)) break;
+                tile = s_tq[k % TQ];
+                if (tile < 0) break;
+            } else {
+                tile = round_position(k, pair, npairs, mix);
+                if (tile >= total_tiles) break;
+            }
             const Tile t = decode_tile<P_BM, P_BAND>(visit_order(tile, total_tiles, mix), s_pre, s_off, s_end, E, NT);
             if (!mbar_wait<true>(&tfull[acc], acc_phase, s_abort, p.status, p.timeout_ns)) break;
             tc_fence_after();
@@ -575,6 +687,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
         tc_fence_after();
         tmem_dealloc_pair(tmem_base, TMEM_COLS);
     }
+    if (threadIdx.x == 0) sched_retire(p);
 }
 
 }  // namespace gg
@@ -582,7 +695,39 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
 // ------------------------------------------------------------------ host side
 namespace {
 
-template <bool SWIGLU, bool BT>
+// Counters of the dynamic tile order (Params::sched), two ints per slot, in a
+// library-owned table on every device that loads the library (zero at load;
+// each launch leaves its slot at zero).  An eager launch takes the next slot
+// of a ring of kEagerSlots, so only kernels of launches kEagerSlots apart
+// could share one, and those are never in flight together.  A launch being
+// captured into a CUDA graph takes a slot of its own that no later launch
+// reuses: every replay of the graph uses it, and replays of one graph run one
+// after another.  Once the captured slots are used up, captured launches fall
+// back to the static order (sched == nullptr).
+constexpr int kEagerSlots = 2048;
+constexpr int kCapturedSlots = 14336;
+__device__ int g_sched_slots[2 * (kEagerSlots + kCapturedSlots)];
+constexpr int kMaxDev = 64;
+std::atomic<uint32_t> g_eager_next[kMaxDev];
+std::atomic<uint32_t> g_captured_next[kMaxDev];
+
+int *sched_slot(const GemmLaunch &cfg, cudaStream_t stream) {
+    if (cfg.sched_base == nullptr || cfg.device < 0 || cfg.device >= kMaxDev) return nullptr;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    if (cs == cudaStreamCaptureStatusActive) {
+        const uint32_t i = g_captured_next[cfg.device].fetch_add(1, std::memory_order_relaxed);
+        if (i >= static_cast<uint32_t>(kCapturedSlots)) return nullptr;
+        return cfg.sched_base + 2 * (kEagerSlots + static_cast<int>(i));
+    }
+    const uint32_t i = g_eager_next[cfg.device].fetch_add(1, std::memory_order_relaxed) % kEagerSlots;
+    return cfg.sched_base + 2 * static_cast<int>(i);
+}
+
+template <bool SWIGLU, bool BT, bool DYN>
 cudaError_t launch_pair(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmOut,
                         const CUtensorMap &tmPre, const gg::Params &p, int grid, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
@@ -597,7 +742,7 @@ cudaError_t launch_pair(const CUtensorMap &tmA, const CUtensorMap &tmB, const CU
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gg::grouped_gemm_pair_kernel<SWIGLU, BT>, tmA, tmB, tmOut, tmPre, p);
+    return cudaLaunchKernelEx(&cfg, gg::grouped_gemm_pair_kernel<SWIGLU, BT, DYN>, tmA, tmB, tmOut, tmPre, p);
 }
 
 template <bool SWIGLU>
@@ -614,7 +759,8 @@ int max_pairs() {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gg::grouped_gemm_pair_kernel<SWIGLU, false>, &cfg) != cudaSuccess) return 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gg::grouped_gemm_pair_kernel<SWIGLU, false, true>, &cfg) != cudaSuccess)
+        return 0;
     return n;
 }
 
@@ -692,51 +838,77 @@ cudaError_t launch_grouped_gemm(bool swiglu, const void *A, int TK, int Kdim, co
     p.status = status;
     p.timeout_ns = timeout_ns;
     const dim3 grid(cfg.num_sms);
+    const int pairs = swiglu ? cfg.pairs_swiglu : cfg.pairs_plain;
+    const bool use_pair = !gather && grouped_gemm_use_pair(TK, E) && pairs > 0;
+    // Dynamic tile order (measured on GB300 against the static order):
+    //  - the CTA-pair kernel with long reductions (Kdim >= 4096): 2-5% faster
+    //    and half the DRAM traffic on the Mixtral shape (GEMM1 3.2 GB per
+    //    launch against 2.48 GB algorithmic, from 6.1 GB);
+    //  - the CTA-pair kernel with short ones: 5-10% slower (the Qwen- and
+    //    skew-shaped GEMM2s, Kdim = 768 and 1536): per tile, CTA 0 must hand
+    //    the tile to CTA 1, which the static order does not need;
+    //  - the single-CTA kernel: 5% faster on the DSv3-shaped GEMM2, but 5%
+    //    slower on its fused-permute GEMM1, which keeps the static order.
+    p.sched = (gather || (use_pair && Kdim < 4096)) ? nullptr : sched_slot(cfg, stream);
     if (gather) {
         // the fused permute runs on the single-CTA kernel for every shape
         p.gather_src = gather->src_tok;
         p.gather_x = static_cast<const __nv_bfloat16 *>(A);
         p.gather_T = gather->T;
-        gg::grouped_gemm_kernel<true, false, true>
+        gg::grouped_gemm_kernel<true, false, true, false>
             <<<grid, gg::threads_of<true>(), gg::SMEM_BYTES, stream>>>(tmA, tmB, tmOut, tmPre, p);
         return cudaGetLastError();
     }
-    const int pairs = swiglu ? cfg.pairs_swiglu : cfg.pairs_plain;
-    if (grouped_gemm_use_pair(TK, E) && pairs > 0) {
-        return swiglu    ? launch_pair<true, false>(tmA, tmB, tmOut, tmPre, p, 2 * pairs, stream)
-               : b_trans ? launch_pair<false, true>(tmA, tmB, tmOut, tmPre, p, 2 * pairs, stream)
-                         : launch_pair<false, false>(tmA, tmB, tmOut, tmPre, p, 2 * pairs, stream);
+    if (use_pair) {
+        const int g = 2 * pairs;
+        if (p.sched)
+            return swiglu    ? launch_pair<true, false, true>(tmA, tmB, tmOut, tmPre, p, g, stream)
+                   : b_trans ? launch_pair<false, true, true>(tmA, tmB, tmOut, tmPre, p, g, stream)
+                             : launch_pair<false, false, true>(tmA, tmB, tmOut, tmPre, p, g, stream);
+        return swiglu    ? launch_pair<true, false, false>(tmA, tmB, tmOut, tmPre, p, g, stream)
+               : b_trans ? launch_pair<false, true, false>(tmA, tmB, tmOut, tmPre, p, g, stream)
+                         : launch_pair<false, false, false>(tmA, tmB, tmOut, tmPre, p, g, stream);
     }
-    if (swiglu)
-        gg::grouped_gemm_kernel<true, false, false>
-            <<<grid, gg::THREADS, gg::SMEM_BYTES, stream>>>(tmA, tmB, tmOut, tmPre, p);
-    else if (b_trans)
-        gg::grouped_gemm_kernel<false, true, false>
-            <<<grid, gg::THREADS, gg::SMEM_BYTES, stream>>>(tmA, tmB, tmOut, tmPre, p);
-    else
-        gg::grouped_gemm_kernel<false, false, false>
-            <<<grid, gg::THREADS, gg::SMEM_BYTES, stream>>>(tmA, tmB, tmOut, tmPre, p);
-    return cudaGetLastError();
+    auto single = [&](auto kernel) {
+        kernel<<<grid, gg::THREADS, gg::SMEM_BYTES, stream>>>(tmA, tmB, tmOut, tmPre, p);
+        return cudaGetLastError();
+    };
+    if (p.sched)
+        return swiglu    ? single(gg::grouped_gemm_kernel<true, false, false, true>)
+               : b_trans ? single(gg::grouped_gemm_kernel<false, true, false, true>)
+                         : single(gg::grouped_gemm_kernel<false, false, false, true>);
+    return swiglu    ? single(gg::grouped_gemm_kernel<true, false, false, false>)
+           : b_trans ? single(gg::grouped_gemm_kernel<false, true, false, false>)
+                     : single(gg::grouped_gemm_kernel<false, false, false, false>);
 }
 
 cudaError_t grouped_gemm_setup(int num_sms, GemmLaunch *cfg) {
     cudaError_t e;
-    const void *single[4] = {reinterpret_cast<const void *>(gg::grouped_gemm_kernel<true, false, false>),
-                             reinterpret_cast<const void *>(gg::grouped_gemm_kernel<false, false, false>),
-                             reinterpret_cast<const void *>(gg::grouped_gemm_kernel<false, true, false>),
-                             reinterpret_cast<const void *>(gg::grouped_gemm_kernel<true, false, true>)};
-    const void *pair[3] = {reinterpret_cast<const void *>(gg::grouped_gemm_pair_kernel<true, false>),
-                           reinterpret_cast<const void *>(gg::grouped_gemm_pair_kernel<false, false>),
-                           reinterpret_cast<const void *>(gg::grouped_gemm_pair_kernel<false, true>)};
-    for (int i = 0; i < 4; ++i)
+    const void *single[7] = {reinterpret_cast<const void *>(gg::grouped_gemm_kernel<true, false, false, false>),
+                             reinterpret_cast<const void *>(gg::grouped_gemm_kernel<false, false, false, false>),
+                             reinterpret_cast<const void *>(gg::grouped_gemm_kernel<false, true, false, false>),
+                             reinterpret_cast<const void *>(gg::grouped_gemm_kernel<true, false, false, true>),
+                             reinterpret_cast<const void *>(gg::grouped_gemm_kernel<false, false, false, true>),
+                             reinterpret_cast<const void *>(gg::grouped_gemm_kernel<false, true, false, true>),
+                             reinterpret_cast<const void *>(gg::grouped_gemm_kernel<true, false, true, false>)};
+    const void *pair[6] = {reinterpret_cast<const void *>(gg::grouped_gemm_pair_kernel<true, false, false>),
+                           reinterpret_cast<const void *>(gg::grouped_gemm_pair_kernel<false, false, false>),
+                           reinterpret_cast<const void *>(gg::grouped_gemm_pair_kernel<false, true, false>),
+                           reinterpret_cast<const void *>(gg::grouped_gemm_pair_kernel<true, false, true>),
+                           reinterpret_cast<const void *>(gg::grouped_gemm_pair_kernel<false, false, true>),
+                           reinterpret_cast<const void *>(gg::grouped_gemm_pair_kernel<false, true, true>)};
+    for (int i = 0; i < 7; ++i)
         if ((e = cudaFuncSetAttribute(single[i], cudaFuncAttributeMaxDynamicSharedMemorySize, gg::SMEM_BYTES)) !=
             cudaSuccess)
             return e;
-    for (int i = 0; i < 3; ++i)
+    for (int i = 0; i < 6; ++i)
         if ((e = cudaFuncSetAttribute(pair[i], cudaFuncAttributeMaxDynamicSharedMemorySize, gg::P_SMEM_BYTES)) !=
             cudaSuccess)
             return e;
     cfg->num_sms = num_sms;
+    if ((e = cudaGetDevice(&cfg->device)) != cudaSuccess) return e;
+    if ((e = cudaGetSymbolAddress(reinterpret_cast<void **>(&cfg->sched_base), g_sched_slots)) != cudaSuccess)
+        return e;
     // every pair must be resident at once (the kernel is persistent): never
     // launch more pairs than fit, nor more CTAs than SMs
     cfg->pairs_swiglu = std::min(max_pairs<true>(), num_sms / 2);

@@ -86,6 +86,8 @@ struct GemmLaunch {
     int pairs_swiglu = 0;
     int pairs_plain = 0;
     int wgrad_pairs = 0;  // resident CTA pairs of the weight-gradient pair kernel
+    int device = -1;
+    int *sched_base = nullptr;  // device address of the dynamic tile order's counter table
 };
 // Kernel attributes and occupancy queries; once per device, before any capture.
 cudaError_t grouped_gemm_setup(int num_sms, GemmLaunch *cfg);

@@ -38,7 +38,17 @@
  * Conventions for every entry point:
  *   - All pointers except those of *_host calls are device pointers owned by
  *     the caller.  The library allocates no memory and performs no
- *     host<->device copy, except the *_host calls (stated there).
+ *     host<->device copy, except the *_host calls (stated there).  It keeps
+ *     two small tables of its own in static device memory on every GPU that
+ *     loads it: the device status word, and 128 KB of counters through which
+ *     the CTAs of one bf16 grouped-GEMM launch hand out its tiles in order
+ *     (dynamic scheduling).  Each launch takes a counter slot on the host:
+ *     eager launches from a ring of 2048 (so only launches 2048 apart could
+ *     share one, and those are never in flight together), launches captured
+ *     into a CUDA graph a slot of their own, kept for every replay (the
+ *     replays of one graph run one after another; a capture instantiated
+ *     twice must not run both instances at once).  After 14336 captured
+ *     launches, later captures use a static tile order instead.
  *   - Calls are asynchronous on `stream` and never synchronize; no value flows
  *     from device to host, so a sequence of calls can be captured in a CUDA
  *     graph and replayed for any routing.  (The first call on a device also

@@ -54,11 +54,14 @@ def test_random_small_shapes(s):
 #   pair, interleaved order  440 / 220 on 76 pairs (one expert holds ~T rows)
 #   single-CTA, two-block    380 / 380 on 152 CTAs (groups of 204..332 rows)
 #   single-CTA, interleaved  670 / 330 on 152 CTAs (Zipf-skewed groups)
+#   pair, long reductions    ~300 / ~130 on 76 pairs (d = 4096 and f = 4160:
+#                            both GEMMs take the dynamic tile order)
 MEDIUM_CASES = [
     Shape(T=8192, d=1024, E=8, K=2, f=1024, bias="normal_0.5"),
     Shape(T=4096, d=512, E=64, K=6, f=512, bias="skew"),
     Shape(T=8192, d=1024, E=64, K=2, f=512, bias="zero"),
     Shape(T=2048, d=512, E=128, K=8, f=512, bias="zipf_1.1"),
+    Shape(T=1024, d=4096, E=3, K=2, f=4160, bias="normal_0.5"),
 ]
 
 

@@ -52,6 +52,10 @@ CONFIGS = {
     # (so the same tile shapes and K lengths) with 2 experts and 2048 rows
     # each, about 1 GB of weights
     "mixtral_e2": dict(T=2048, d=4096, E=2, K=1, f=14336, bias="zero"),
+    # profiling-size stand-in for the skew layer: the same d, f, E, K and bias
+    # rule with an eighth of the tokens (the same GEMM kernels and tile
+    # shapes), about 3 GB on the device
+    "skew_t4096": dict(T=4096, d=4096, E=64, K=6, f=1536, bias="skew"),
 }
 
 DESCRIPTIONS = {
@@ -62,6 +66,7 @@ DESCRIPTIONS = {
     "skew": "Extreme-skew MoE layer fwd T=32768 d=4096 E=64 K=6 f=1536",
     "dsv3_e32": "DeepSeek-V3-shaped layer, 32 experts (profiling size) T=512 d=7168 E=32 K=8 f=2048",
     "mixtral_e2": "Mixtral-shaped expert GEMMs, 2 experts (profiling size) T=2048 d=4096 E=2 K=1 f=14336",
+    "skew_t4096": "Extreme-skew MoE layer, 4096 tokens (profiling size) T=4096 d=4096 E=64 K=6 f=1536",
 }
 
 
