@@ -74,7 +74,7 @@ def _traffic_record(kernel: str, workload: str):
         return None
     with open(p) as fh:
         d = json.load(fh)
-    rec = d.get(kernel)
+    rec = d.get(f"{kernel}@{workload}")
     if not rec or rec.get("workload") != workload:
         return None
     # the hash covers every source file the kernel is built from
@@ -341,7 +341,7 @@ def _config(name, s, ws, args):
 BURST_REGION_S = 1.0
 
 
-def _dominant_roofline(s, s_name, kmean, counts, mxfp8, region_s):
+def _dominant_roofline(s, s_name, kmean, counts, mxfp8, region_s, fused_permute=False):
     """Roofline of the dominant grouped GEMM: its binding resource (the
     larger of the tensor and HBM floors), achieved rate from the event-timed
     mean launch, and the fraction of both measured bf16 peaks, the one that
@@ -369,7 +369,9 @@ def _dominant_roofline(s, s_name, kmean, counts, mxfp8, region_s):
     live = int((counts > 0).sum().item())
     sc = (1.0 + 1.0 / 32.0) if mxfp8 else 1.0
     if dom == "grouped_gemm1_swiglu":
-        dom_bytes = sc * eb * (live * 2.0 * f * d + TK * d) + sc * eb * TK * f
+        # A: the permuted rows, or (permute fused) each token row once
+        a_rows = T if fused_permute else TK
+        dom_bytes = sc * eb * (live * 2.0 * f * d + a_rows * d) + sc * eb * TK * f
     else:
         dom_bytes = sc * eb * (live * 1.0 * d * f + TK * f) + 2.0 * TK * d
     t_dom = kmean[dom] * 1e-3
@@ -554,7 +556,7 @@ def measure_forward(moe, s_name, args, ws, rank, local, full=True):
         "tokens_per_s": aggregate(T, ws, args.steps, elapsed_ms), "ms_per_step": ms_per_step,
         "launches": launches, "clocks": clocks, "timed_region_s": elapsed_ms * 1e-3,
         "kernels": _kernel_table(s, kmean, mxfp8, fuse_permute),
-        "roofline": _dominant_roofline(s, s_name, kmean, counts, mxfp8, elapsed_ms * 1e-3),
+        "roofline": _dominant_roofline(s, s_name, kmean, counts, mxfp8, elapsed_ms * 1e-3, fuse_permute),
         "routing": {"empty_experts": int((counts == 0).sum().item()), "max_group": int(counts.max().item()),
                     "batches": "two resident token batches (seeds r, r+1), alternating step by step"},
     }
