@@ -268,15 +268,18 @@ __device__ __forceinline__ void combine_arrive(const Params &p, int n_blk, int g
 
 // Epilogue of one accumulator for one warp: 32 TMEM lanes = 32 output rows
 // wrow0..wrow0+31 (this thread's row is wrow0 + lane), tbase points at the
-// warp's lane quarter of the accumulator.  Each 32-column chunk is converted
-// to bf16 and, when all 32 rows belong to the group, staged in shared memory
-// (64-byte swizzle) and written by one TMA store of full lines; a slice that
-// crosses the group's end falls back to masked 16-byte stores per row.
-// `sbuf` alternates the warp's two staging buffers across chunks and tiles.
-template <bool SWIGLU>
+// warp's lane quarter of the accumulator.  The warp covers output columns
+// [c_begin, c_end) of the tile (all of them, or half where two warps share a
+// lane quarter).  Each 32-column chunk is converted to bf16 and, when all 32
+// rows belong to the group, staged in shared memory (64-byte swizzle) and
+// written by one TMA store of full lines; a slice that crosses the group's
+// end falls back to masked 16-byte stores per row.  `sbuf` cycles through
+// the warp's NBUF staging buffers across chunks and tiles.
+template <bool SWIGLU, int NBUF = 2>
 __device__ __forceinline__ void epilogue_tile(const Params &p, const CUtensorMap *tm_out, const CUtensorMap *tm_pre,
                                               uint8_t *stage, uint32_t &sbuf, uint32_t tbase, int n_blk, int wrow0,
-                                              int lane, int grp_end) {
+                                              int lane, int grp_end, int c_begin = 0,
+                                              int c_end = SWIGLU ? BN_ACC / 2 : BN_ACC) {
     if (wrow0 >= grp_end) return;  // whole slice outside the group (warp-uniform)
     const bool full = wrow0 + 31 < grp_end;
     const int grow = wrow0 + lane;
@@ -285,7 +288,7 @@ __device__ __forceinline__ void epilogue_tile(const Params &p, const CUtensorMap
         // fused combine: rows stored directly (generic proxy), so that a fence
         // orders them before the token's count
 #pragma unroll 1
-        for (int c = 0; c < BN_ACC; c += 64) {
+        for (int c = c_begin; c < c_end; c += 64) {
             const int col = n_blk * BN_ACC + c;
             if (col >= p.n_out) break;  // column tail (uniform)
             uint32_t v[2][32];
@@ -311,7 +314,7 @@ __device__ __forceinline__ void epilogue_tile(const Params &p, const CUtensorMap
     auto put = [&](const CUtensorMap *tm, __nv_bfloat16 *dst, int ld, int col, const uint32_t (&packed)[16]) {
         if (full) {
             uint8_t *buf = stage + sbuf * EPI_BUF;
-            if (lane == 0) bulk_wait_read<1>();  // this buffer's store from two chunks ago has read it
+            if (lane == 0) bulk_wait_read<NBUF - 1>();  // this buffer's store from NBUF chunks ago has read it
             __syncwarp();
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -327,7 +330,7 @@ __device__ __forceinline__ void epilogue_tile(const Params &p, const CUtensorMap
                 tma_store_2d_evict_first(tm, buf, col, wrow0, l2_policy_evict_first());
                 bulk_commit();
             }
-            sbuf ^= 1u;
+            sbuf = (sbuf + 1 == NBUF) ? 0u : sbuf + 1;
         } else if (row_ok) {
             store_row32(dst + static_cast<size_t>(grow) * ld + col, packed);
         }
@@ -339,7 +342,7 @@ __device__ __forceinline__ void epilogue_tile(const Params &p, const CUtensorMap
     };
     if (SWIGLU) {
 #pragma unroll 1
-        for (int c = 0; c < NCOL; c += 32) {
+        for (int c = c_begin; c < c_end; c += 32) {
             uint32_t g[32], u[32];
             tmem_ld_32x32b_x32(tbase + c, g);
             tmem_ld_32x32b_x32(tbase + BN_ACC / 2 + c, u);
@@ -373,7 +376,7 @@ __device__ __forceinline__ void epilogue_tile(const Params &p, const CUtensorMap
     } else {
         // two 32-column loads per wait, so TMEM latency is paid 4 times per tile, not 8
 #pragma unroll 1
-        for (int c = 0; c < NCOL; c += 64) {
+        for (int c = c_begin; c < c_end; c += 64) {
             uint32_t v[2][32];
             tmem_ld_32x32b_x32(tbase + c, v[0]);
             tmem_ld_32x32b_x32(tbase + c + 32, v[1]);

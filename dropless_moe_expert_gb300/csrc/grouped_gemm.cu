@@ -79,10 +79,19 @@ constexpr int UMMA_K = 16;
 constexpr int TMEM_COLS = 2 * BN_ACC;
 constexpr int THREADS = 192;
 constexpr int BOX_ROWS = 128;  // every K-major TMA box is 128 rows x 64 bf16
-constexpr int GATHER_WARPS = 4;  // fused permute: warps 6..9 copy the A rows
-template <bool GATHER>
-constexpr int threads_of() {
-    return GATHER ? THREADS + 32 * GATHER_WARPS : THREADS;
+constexpr int GATHER_WARPS = 4;  // fused permute: the last four warps copy the A rows
+// Epilogue warps of the single-CTA kernel.  GEMM1 (SwiGLU) takes two per TMEM
+// lane quarter, each storing half of the tile's 128 h columns through one
+// staging buffer: its tiles of two row blocks use both accumulators, so
+// their epilogue runs between mainloops and its length counts in full.  The
+// plain GEMMs keep one per quarter, with two staging buffers each.
+template <bool SWIGLU>
+__host__ __device__ constexpr int epi_warps() {
+    return SWIGLU ? 8 : 4;
+}
+template <bool SWIGLU, bool GATHER>
+__host__ __device__ constexpr int threads_of() {
+    return 64 + 32 * epi_warps<SWIGLU>() + (GATHER ? 32 * GATHER_WARPS : 0);
 }
 constexpr int BT_BOX = 64 * 64 * 2;  // MN-major B box: 64 K rows x 64 columns
 
@@ -169,7 +178,7 @@ __device__ __forceinline__ void gather_block(uint8_t *slot, const __nv_bfloat16 
 // single-CTA variant
 // ======================================================================
 template <bool SWIGLU, bool BT, bool GATHER, bool DYN>
-__global__ void __launch_bounds__(threads_of<GATHER>(), 1)
+__global__ void __launch_bounds__(threads_of<SWIGLU, GATHER>(), 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ CUtensorMap tmPre,
                     const Params p) {
@@ -206,7 +215,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&tfull[i], 1);
-            mbar_init(&tempty[i], 4);
+            mbar_init(&tempty[i], epi_warps<SWIGLU>());
         }
         mbar_init(drain, 1);
         for (int i = 0; i < TQ; ++i) mbar_init(&qfull[i], 1);
@@ -369,9 +378,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 mbar_wait(drain, 0, &no_abort, p.status, p.timeout_ns);
             }
         }
-    } else if (GATHER && warp >= 6) {
+    } else if (GATHER && warp >= 2 + epi_warps<SWIGLU>()) {
         // fused permute: this warp's 32 rows of each A block of every stage
-        const int gw = warp - 6;
+        const int gw = warp - 2 - epi_warps<SWIGLU>();
         uint32_t stage = 0, phase = 0;
         bool ok = true;
         for (int k = 0; ok; ++k) {
@@ -404,7 +413,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         cp_async_wait_all();  // this lane's copies have landed before the CTA's shared memory goes away
     } else {
         const int q = warp & 3;  // TMEM lane quarter this warp may access
-        uint8_t *stage = smem + L1::OFF_EPI + (warp - 2) * 2 * EPI_BUF;
+        constexpr int NBUF = SWIGLU ? 1 : 2;  // staging buffers per epilogue warp
+        static_assert(epi_warps<SWIGLU>() * NBUF * EPI_BUF == EPI_BYTES, "epilogue staging");
+        // GEMM1: the two warps of a lane quarter split the tile's 128 h columns
+        const int c_begin = SWIGLU ? ((warp - 2) >> 2) * (BN_ACC / 4) : 0;
+        const int c_end = SWIGLU ? c_begin + BN_ACC / 4 : BN_ACC;
+        uint8_t *stage = smem + L1::OFF_EPI + (warp - 2) * NBUF * EPI_BUF;
         uint32_t sbuf = 0;
         uint32_t acc = 0;
         uint32_t ph[2] = {0u, 0u};  // the MMA thread's accumulator order, mirrored
@@ -427,8 +441,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 if (!mbar_wait(&tfull[a], ph[a], s_abort, p.status, p.timeout_ns)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + a * BN_ACC;
-                epilogue_tile<SWIGLU>(p, &tmOut, &tmPre, stage, sbuf, tbase, t.n_blk, t.row0 + b * BM + q * 32, lane,
-                                      t.grp_end);
+                epilogue_tile<SWIGLU, NBUF>(p, &tmOut, &tmPre, stage, sbuf, tbase, t.n_blk, t.row0 + b * BM + q * 32,
+                                            lane, t.grp_end, c_begin, c_end);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&tempty[a]);
@@ -856,7 +870,7 @@ cudaError_t launch_grouped_gemm(bool swiglu, const void *A, int TK, int Kdim, co
         p.gather_x = static_cast<const __nv_bfloat16 *>(A);
         p.gather_T = gather->T;
         gg::grouped_gemm_kernel<true, false, true, false>
-            <<<grid, gg::threads_of<true>(), gg::SMEM_BYTES, stream>>>(tmA, tmB, tmOut, tmPre, p);
+            <<<grid, gg::threads_of<true, true>(), gg::SMEM_BYTES, stream>>>(tmA, tmB, tmOut, tmPre, p);
         return cudaGetLastError();
     }
     if (use_pair) {
@@ -870,7 +884,8 @@ cudaError_t launch_grouped_gemm(bool swiglu, const void *A, int TK, int Kdim, co
                          : launch_pair<false, false, false>(tmA, tmB, tmOut, tmPre, p, g, stream);
     }
     auto single = [&](auto kernel) {
-        kernel<<<grid, gg::THREADS, gg::SMEM_BYTES, stream>>>(tmA, tmB, tmOut, tmPre, p);
+        kernel<<<grid, swiglu ? gg::threads_of<true, false>() : gg::threads_of<false, false>(), gg::SMEM_BYTES,
+                 stream>>>(tmA, tmB, tmOut, tmPre, p);
         return cudaGetLastError();
     };
     if (p.sched)
