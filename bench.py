@@ -688,7 +688,6 @@ def run_gpu(args):
                             "frac_of_bf16_sustained", "frac_of_hbm")},
                         "routing": o["routing"], "clocks": o["clocks"], "gpu_launches": o["launches"],
                         "fused_permute": o["fused_permute"]}
-        r["launches"] += o["launches"]
     s = r["s"]
     if rank == 0:
         line = {
