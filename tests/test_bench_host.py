@@ -44,7 +44,7 @@ def test_short_region_takes_the_burst_peak_long_region_the_sustained(monkeypatch
     assert r["peak"] == 4000.0
 
 
-def test_weight_streaming_shape_is_judged_against_hbm(monkeypatch):
+def test_weight_streaming_shape_is_bound_by_hbm(monkeypatch):
     _peaks(monkeypatch)
     s = shape("dsv3")
     counts = torch.zeros(s.E, dtype=torch.int64)
