@@ -30,6 +30,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <atomic>
 
 namespace moe {
 namespace mx {
@@ -80,9 +81,10 @@ quantize_kernel(const uint4 *__restrict__ src, int R, int K, uint4 *__restrict__
 }
 
 // Row-block prefix of the expert groups, from offsets[E+1] (clamped to
-// [0, TK] like the GEMMs do), into shared memory; one warp.
+// [0, TK] like the GEMMs do), into shared memory; one warp.  Group e holds
+// rows [s_off[e], s_end[e]) and its scale atoms start at row block s_rb[e].
 __device__ __forceinline__ void row_block_prefix(const int32_t *__restrict__ offsets, int E, int TK, int lane,
-                                                 int *s_off, int *s_rb) {
+                                                 int *s_off, int *s_end, int *s_rb) {
     int carry = 0;
     for (int base = 0; base < E; base += 32) {
         const int e = base + lane;
@@ -91,6 +93,7 @@ __device__ __forceinline__ void row_block_prefix(const int32_t *__restrict__ off
             const int o0 = min(max(offsets[e], 0), TK);
             const int o1 = min(max(offsets[e + 1], o0), TK);
             s_off[e] = o0;
+            s_end[e] = o1;
             cnt = (o1 - o0 + 127) / 128;
         }
         int v = cnt;
@@ -104,74 +107,162 @@ __device__ __forceinline__ void row_block_prefix(const int32_t *__restrict__ off
     }
 }
 
-// Permute + quantise: one warp per token.  The warp walks the row in chunks
-// of 256 elements, lane l holding elements 8l..8l+7 (one 16-byte load, so the
-// warp reads 512 contiguous bytes); a block of 32 elements is 4 lanes, which
-// combine their maxima with two shuffles.  Each lane writes its 8 codes (8
-// bytes: 256 contiguous bytes per warp) to every row of x_perm the token
-// occupies, and lane 16 s (s = 0, 1) gathers the 4 scale bytes of the chunk's
-// s-th 128-element slice and writes them as one word of that row's atom.
-__global__ void __launch_bounds__(256)
+constexpr int PERMUTE_WARPS = 8;
+constexpr int MAX_K = 16;
+
+// Where one of a token's rows goes: its row r of x_perm (-1 for a row
+// outside the contract, a row index outside [0, TK) or outside its expert's
+// group, which is skipped) and its scale word in the atom of its group's row
+// block at K slice 0 (slice ks adds 128 words).
+struct RowDest {
+    int row;
+    int sf;
+};
+
+// 16 consecutive elements (32 bytes of bf16) of one lane, zeros past d.
+__device__ __forceinline__ void load16(const uint4 *__restrict__ row, int c, int d, uint4 &a, uint4 &b) {
+    if (c < d) {
+        a = __ldg(row + c / 8);
+        b = __ldg(row + c / 8 + 1);
+    } else {
+        a = b = make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+
+// Lane k < K: the destination of the token's k-th row (row r, expert e).
+__device__ __forceinline__ RowDest row_dest(int r, int e, int E, int ns, const int *s_off, const int *s_end,
+                                            const int *s_rb) {
+    RowDest rd;
+    rd.row = -1;
+    rd.sf = 0;
+    if (e >= 0 && e < E && r >= s_off[e] && r < s_end[e]) {
+        const int local = r - s_off[e];
+        rd.row = r;
+        rd.sf = static_cast<int>(atom_word(s_rb[e] + local / 128, 0, ns, local % 128));
+    }
+    return rd;
+}
+
+// Permute + quantise.  A token row is cut into chunks of 512 elements.
+// With W warps in the grid, warp w first takes whole tokens w, w + W, ...
+// for R = floor(T / W) rounds, so that the warps sweep the tokens in order;
+// the chunks of the last T - R W tokens are then cut into W equal
+// contiguous runs, one per warp, so that the warps also end together.  In
+// a chunk lane l holds elements 16l..16l+15 (two 16-byte loads; the warp
+// reads 1 KB contiguous), so a 32-element block is a lane pair, whose maxima
+// meet in one shuffle, and its 16 codes are one 16-byte store per
+// destination row (512 contiguous bytes per warp).  Lane 8 s (s = 0..3)
+// collects the 4 scale bytes of the chunk's s-th 128-element slice from
+// lanes 8s, 8s+2, 8s+4, 8s+6 and writes them as one word of the row's atom.
+// When a warp reaches a new token, lanes k < K work out its K destinations
+// into shared memory, read back as one broadcast per row and chunk (the
+// next row's read issued before this row's stores).  The next chunk and the
+// next token's routing are loaded while the current chunk is quantised and
+// stored.
+__global__ void __launch_bounds__(32 * PERMUTE_WARPS, 5)
 permute_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ topk_idx, const int32_t *__restrict__ row_of,
-               const int32_t *__restrict__ offsets, int T, int K, int d, int E, uint2 *__restrict__ xq,
+               const int32_t *__restrict__ offsets, int T, int K, int d, int E, uint8_t *__restrict__ xq,
                uint32_t *__restrict__ sf) {
     __shared__ int s_off[MAX_E];
+    __shared__ int s_end[MAX_E];
     __shared__ int s_rb[MAX_E];
+    __shared__ RowDest s_dst[PERMUTE_WARPS][MAX_K];
     const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
     const int TK = T * K;
-    if (threadIdx.x < 32) row_block_prefix(offsets, E, TK, lane, s_off, s_rb);
+    if (threadIdx.x < 32) row_block_prefix(offsets, E, TK, lane, s_off, s_end, s_rb);
     __syncthreads();
     const int ns = d / 128;
-    const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int nw = (gridDim.x * blockDim.x) >> 5;
-    for (int t = gw; t < T; t += nw) {
-        // lanes k < K hold the token's k-th row and expert
-        int my_r = -1, my_e = -1;
-        if (lane < K) {
-            my_r = __ldg(row_of + static_cast<size_t>(t) * K + lane);
-            my_e = __ldg(topk_idx + static_cast<size_t>(t) * K + lane);
+    const int nch = (d + 511) / 512;
+    const int W = gridDim.x * PERMUTE_WARPS;
+    const int w = blockIdx.x * PERMUTE_WARPS + warp;
+    const int R = T / W;
+    const int tail0 = R * W;  // first token of the tail
+    const long long tail_chunks = static_cast<long long>(T - tail0) * nch;
+    const long long q0 = tail_chunks * w / W, q1 = tail_chunks * (w + 1) / W;
+    const int tail_t = tail0 + static_cast<int>(q0 / nch);  // this warp's run of the tail
+    const int tail_c = static_cast<int>(q0 % nch) * 512;
+    const int tail_last = tail0 + static_cast<int>((q1 - 1) / nch);  // used only when q1 > q0
+    int left = R * nch + static_cast<int>(q1 - q0);                  // chunks this warp quantises
+    if (left == 0) return;
+    // the token after tt in this warp's sequence (T when there is none)
+    auto after = [&](int tt) -> int {
+        if (tt < tail0) return tt + W < tail0 ? tt + W : (q1 > q0 ? tail_t : T);
+        return tt < tail_last ? tt + 1 : T;
+    };
+    int t = R > 0 ? w : tail_t;
+    int c0 = R > 0 ? 0 : tail_c;
+    int t_next = after(t);
+    RowDest *dst = s_dst[warp];
+    int my_r = -1, my_e = -1;
+    if (lane < K) {
+        my_r = __ldg(row_of + static_cast<size_t>(t) * K + lane);
+        my_e = __ldg(topk_idx + static_cast<size_t>(t) * K + lane);
+        dst[lane] = row_dest(my_r, my_e, E, ns, s_off, s_end, s_rb);
+        if (t_next < T) {
+            my_r = __ldg(row_of + static_cast<size_t>(t_next) * K + lane);
+            my_e = __ldg(topk_idx + static_cast<size_t>(t_next) * K + lane);
         }
-        // the next 256 columns' load is in flight while these are quantised and stored
-        const uint4 *xrow = x + static_cast<size_t>(t) * d / 8;
-        uint4 nxt = 8 * lane < d ? __ldg(xrow + lane) : make_uint4(0u, 0u, 0u, 0u);
-        for (int c0 = 0; c0 < d; c0 += 256) {
-            const bool valid = c0 + 8 * lane < d;  // d is a multiple of 128: whole blocks
-            const uint4 cur = nxt;
-            if (c0 + 256 + 8 * lane < d) nxt = __ldg(xrow + (c0 + 256) / 8 + lane);
-            float v[8];
-            if (valid) {
-                unpack_bf16x8(cur, v);
-            } else {
+    }
+    uint4 na, nb;
+    load16(x + static_cast<size_t>(t) * d / 8, c0 + 16 * lane, d, na, nb);
+    __syncwarp();
+    const bool scale_lane = (lane & 7) == 0;
+    for (; left > 0; --left) {
+        const bool more = left > 1;
+        const int c = c0 + 16 * lane;
+        const bool valid = c < d;  // d is a multiple of 128: whole slices
+        const uint4 a = na, b = nb;
+        int tn = t, cn = c0 + 512;
+        if (cn >= d) {
+            tn = t_next;
+            cn = (t < tail0 && tn == tail_t) ? tail_c : 0;
+        }
+        if (more) load16(x + static_cast<size_t>(tn) * d / 8, cn + 16 * lane, d, na, nb);
+        float v[16];
+        unpack_bf16x8(a, v);
+        unpack_bf16x8(b, v + 8);
+        float amax = 0.0f;
 #pragma unroll
-                for (int i = 0; i < 8; ++i) v[i] = 0.0f;
-            }
-            float amax = 0.0f;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
-            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-            const uint32_t sbyte = scale_byte(amax);
-            const float inv = __uint_as_float((254u - sbyte) << 23);  // 2^-(s-127)
-            uint2 code;
-            code.x = pack4(v[0] * inv, v[1] * inv, v[2] * inv, v[3] * inv);
-            code.y = pack4(v[4] * inv, v[5] * inv, v[6] * inv, v[7] * inv);
-            // the chunk's two slices: bytes of blocks 0..3 from lanes 0, 4, 8, 12
-            // (slice 0) and 16, 20, 24, 28 (slice 1)
-            const uint32_t b1 = __shfl_down_sync(0xffffffffu, sbyte, 4);
-            const uint32_t b2 = __shfl_down_sync(0xffffffffu, sbyte, 8);
-            const uint32_t b3 = __shfl_down_sync(0xffffffffu, sbyte, 12);
-            const uint32_t word = sbyte | (b1 << 8) | (b2 << 16) | (b3 << 24);
-            const int ks = c0 / 128 + (lane >> 4);
-            for (int k = 0; k < K; ++k) {
-                const int r = __shfl_sync(0xffffffffu, my_r, k);
-                const int e = __shfl_sync(0xffffffffu, my_e, k);
-                if (r < 0 || r >= TK || e < 0 || e >= E) continue;  // outside the contract: skip (warp-uniform)
-                const int local = r - s_off[e];
-                if (local < 0) continue;
-                if (valid) xq[(static_cast<size_t>(r) * d + c0 + 8 * lane) / 8] = code;
-                if ((lane & 15) == 0 && valid) sf[atom_word(s_rb[e] + local / 128, ks, ns, local % 128)] = word;
+        for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        const uint32_t sbyte = scale_byte(amax);
+        const float inv = __uint_as_float((254u - sbyte) << 23);  // 2^-(s-127)
+        uint4 code;
+        code.x = pack4(v[0] * inv, v[1] * inv, v[2] * inv, v[3] * inv);
+        code.y = pack4(v[4] * inv, v[5] * inv, v[6] * inv, v[7] * inv);
+        code.z = pack4(v[8] * inv, v[9] * inv, v[10] * inv, v[11] * inv);
+        code.w = pack4(v[12] * inv, v[13] * inv, v[14] * inv, v[15] * inv);
+        const uint32_t b1 = __shfl_down_sync(0xffffffffu, sbyte, 2);
+        const uint32_t b2 = __shfl_down_sync(0xffffffffu, sbyte, 4);
+        const uint32_t b3 = __shfl_down_sync(0xffffffffu, sbyte, 6);
+        const uint32_t word = sbyte | (b1 << 8) | (b2 << 16) | (b3 << 24);
+        const int sf_col = (c0 / 128 + (lane >> 3)) * 128;
+        uint8_t *xq_c = xq + c;
+        RowDest nxt = dst[0];
+        for (int k = 0; k < K; ++k) {
+            const RowDest rd = nxt;
+            if (k + 1 < K) nxt = dst[k + 1];
+            if (rd.row >= 0 && valid) {  // rd is warp-uniform
+                *reinterpret_cast<uint4 *>(xq_c + static_cast<size_t>(rd.row) * d) = code;
+                if (scale_lane) sf[rd.sf + sf_col] = word;
             }
         }
+        if (tn != t && more) {
+            // next token: its destinations from the routing loaded a token ago
+            __syncwarp();
+            t_next = after(tn);
+            if (lane < K) {
+                dst[lane] = row_dest(my_r, my_e, E, ns, s_off, s_end, s_rb);
+                if (t_next < T) {
+                    my_r = __ldg(row_of + static_cast<size_t>(t_next) * K + lane);
+                    my_e = __ldg(topk_idx + static_cast<size_t>(t_next) * K + lane);
+                }
+            }
+            __syncwarp();
+        }
+        t = tn;
+        c0 = cn;
     }
 }
 
@@ -198,11 +289,26 @@ cudaError_t launch_mxfp8_quantize(const uint16_t *src, int rows, int K, uint8_t 
 cudaError_t launch_permute_mxfp8(const uint16_t *x, const int32_t *topk_idx, const int32_t *row_of,
                                  const int32_t *offsets, int T, int K, int d, int E, uint8_t *xq, uint8_t *sfa,
                                  cudaStream_t stream) {
-    const int warps = 8;
-    const int blocks = std::max(1, std::min((T + warps - 1) / warps, 152 * 8));
-    mx::permute_kernel<<<blocks, 32 * warps, 0, stream>>>(reinterpret_cast<const uint4 *>(x), topk_idx, row_of,
-                                                         offsets, T, K, d, E, reinterpret_cast<uint2 *>(xq),
-                                                         reinterpret_cast<uint32_t *>(sfa));
+    // one wave of resident blocks, worked out once per device
+    static std::atomic<int> resident[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    int wave = resident[dev].load(std::memory_order_relaxed);
+    if (wave == 0) {
+        int sms = 0, per_sm = 0;
+        cudaError_t err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (err == cudaSuccess)
+            err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, mx::permute_kernel, 32 * mx::PERMUTE_WARPS, 0);
+        if (err != cudaSuccess) return err;
+        wave = std::max(1, sms * std::max(1, per_sm));
+        resident[dev].store(wave, std::memory_order_relaxed);
+    }
+    const long long chunks = static_cast<long long>(T) * ((d + 511) / 512);
+    const int blocks = static_cast<int>(std::max(1LL, std::min((chunks + mx::PERMUTE_WARPS - 1) / mx::PERMUTE_WARPS,
+                                                                static_cast<long long>(wave))));
+    mx::permute_kernel<<<blocks, 32 * mx::PERMUTE_WARPS, 0, stream>>>(reinterpret_cast<const uint4 *>(x), topk_idx,
+                                                                      row_of, offsets, T, K, d, E, xq,
+                                                                      reinterpret_cast<uint32_t *>(sfa));
     return cudaGetLastError();
 }
 

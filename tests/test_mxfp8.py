@@ -153,3 +153,32 @@ def test_graph_replays_match_eager(s):
         assert torch.equal(y_static.view(torch.int16), y_eager.view(torch.int16)), f"replay seed {seed}"
         counts.append(tuple(layer.views(s.T)["counts"].cpu().tolist()))
     assert len(set(counts)) == len(counts), "replays should see different routings"
+
+
+@pytest.mark.parametrize("s", [
+    Shape(T=100, d=4096, E=8, K=2, f=128),                       # fewer tokens than warps: the chunks split evenly
+    Shape(T=7000, d=640, E=16, K=3, f=128),                      # one round of whole tokens, then a split tail;
+                                                                 # a 128-column last chunk
+    Shape(T=13000, d=1152, E=64, K=2, f=128, bias="zipf_1.1"),   # two rounds, a tail, empty experts
+], ids=lambda s: f"T{s.T}_d{s.d}_E{s.E}_K{s.K}")
+def test_permute_quantise_every_row_bit_exact(s):
+    """The quantising permute hands a grid of warps whole tokens in rounds
+    while every warp still gets one, then splits the remaining tokens'
+    512-column chunks into equal runs.  Every row of x_perm (codes and scale
+    bytes) is compared with the oracle's quantisation of the token it came
+    from, placed by the GPU's own routing; on a 152-SM GB300 the shapes take
+    zero, one and two rounds before the split tail."""
+    import dropless_moe_expert_gb300 as moe
+    w = make_weights(s, seed=5, device=DEV)
+    x = make_tokens(s, seed=5, device=DEV)
+    r = moe.route(moe.router_logits(x, w.Wr, w.bias), s.K)
+    xq, sfa = moe.permute_mxfp8(x, r)
+    torch.cuda.synchronize()
+    assert moe.device_status() == 0
+    codes, scales, _ = oracle.mx_quantize(to_np(x))
+    row_of = to_np(r.row_of).astype(np.int64)
+    tok = np.repeat(np.arange(s.T), s.K)
+    rows = row_of.ravel()
+    assert np.array_equal(np.sort(rows), np.arange(s.T * s.K))
+    assert np.array_equal(to_np(xq)[rows], codes[tok])
+    assert np.array_equal(unpack_group_atoms(to_np(sfa), to_np(r.offsets), s.d, rows), scales[tok])
