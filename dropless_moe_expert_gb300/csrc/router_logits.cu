@@ -16,19 +16,29 @@
 //     L[t, e] = sum_p sum_i x[t, i] * Wp[e, i],   p in {hi, mid, lo},
 // is one bf16 contraction of depth 3d with exact products and fp32
 // accumulation: the same operands and precision as the fp32 dot product,
-// summed in the tensor core's order instead of index order.  The result is
-// deterministic (fixed tile shapes, no atomics, no split reduction).
+// summed in the tensor core's order instead of index order (each piece's
+// sum in its own fp32 accumulator, the three added at the end).  The result
+// is deterministic (fixed tile shapes, no atomics, no split reduction).  A
+// one-hot token gives every weight exactly: hi + mid is representable in
+// fp32, and adding lo restores w.
 //
 // Two kernels:
 //   router_split_kernel : Wr [d, E] fp32 -> Ws [3][E][d] bf16 (hi, mid, lo,
 //                         each K-major, i.e. transposed) in caller scratch;
 //   router_gemm_kernel  : one 128-token x BN-expert tile per CTA; per 64-wide
 //                         K slice TMA brings the x tile and the three weight
-//                         pieces' tiles (128-byte swizzle), one thread issues
-//                         3 x 4 tcgen05.mma (M=128, N=BN, K=16) into one fp32
-//                         TMEM accumulator, and four warps add the bias and
-//                         store fp32 rows.  Expert rows past E and token rows
-//                         past T come from TMA zero fill and are not stored.
+//                         pieces' tiles (128-byte swizzle), which lie one
+//                         after the other in shared memory and so form one
+//                         K-major B operand of 3 BN rows.  One thread issues
+//                         4 tcgen05.mma (M=128, N=3 BN, K=16): TMEM columns
+//                         [0, BN) accumulate x.hi, [BN, 2BN) x.mid and
+//                         [2BN, 3BN) x.lo, each in fp32.  Four warps form
+//                         L = (x.hi + x.mid) + x.lo + bias and store fp32
+//                         rows.  (Three MMAs of N = BN per K step measured
+//                         2-3x slower: small-N MMAs are bound by their issue
+//                         cost, not by the tensor pipe.)  Expert rows past E
+//                         and token rows past T come from TMA zero fill and
+//                         are not stored.
 #include "kernels.h"
 #include "ptx.cuh"
 #include "tmap.h"
@@ -54,8 +64,8 @@ struct Cfg {
     static constexpr int OFF_TMEM = OFF_BARS + NUM_BARS * 8;
     static constexpr int OFF_ABORT = OFF_TMEM + 4;
     static constexpr int BYTES = OFF_ABORT + 4 + 1024;  // slack for 1024-byte alignment
-    static constexpr int TMEM_COLS = BN;                // a power of two >= 32
-    static_assert(BN == 32 || BN == 64 || BN == 128, "accumulator width");
+    static constexpr int TMEM_COLS = BN == 32 ? 128 : 256;  // 3 BN columns, rounded up to a power of two
+    static_assert(BN == 32 || BN == 64, "accumulator width: 3 BN <= 256 for one MMA");
     static_assert(STAGES >= 2 && BYTES <= 227 * 1024, "shared memory budget");
     static_assert(B_PIECE % 1024 == 0, "swizzled tiles must stay 1024-byte aligned");
 };
@@ -176,7 +186,7 @@ router_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
         }
     } else if (warp == 1 && lane == 0) {
         // MMA issuer: per K slice, the hi, mid and lo pieces in turn
-        constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+        constexpr uint32_t idesc = idesc_bf16_f32(BM, 3 * BN);
         uint32_t stage = 0, phase = 0;
         bool ok = true, issued = false;
         for (int kb = 0; kb < KB; ++kb) {
@@ -184,13 +194,10 @@ router_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
             tc_fence_after();
             const uint32_t sa = smem_u32(smem + stage * C::STAGE);
             const uint64_t adesc = smem_desc_kmajor_sw128(sa);
+            const uint64_t bdesc = smem_desc_kmajor_sw128(sa + A_BYTES);  // hi, mid, lo rows: 3 BN
 #pragma unroll
-            for (int pc = 0; pc < 3; ++pc) {
-                const uint64_t bdesc = smem_desc_kmajor_sw128(sa + A_BYTES + pc * C::B_PIECE);
-#pragma unroll
-                for (int j = 0; j < BK / UMMA_K; ++j)
-                    umma_bf16(tmem_base, adesc + 2 * j, bdesc + 2 * j, idesc, (kb | pc | j) != 0);
-            }
+            for (int j = 0; j < BK / UMMA_K; ++j)
+                umma_bf16(tmem_base, adesc + 2 * j, bdesc + 2 * j, idesc, (kb | j) != 0);
             issued = true;
             umma_commit(&empty[stage]);
             if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
@@ -215,8 +222,10 @@ router_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
         float *Lrow = p.L + static_cast<size_t>(row) * p.E;
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
-            uint32_t v[32];
-            tmem_ld_32x32b_x32(tbase + c, v);
+            uint32_t vh[32], vm[32], vl[32];
+            tmem_ld_32x32b_x32(tbase + c, vh);
+            tmem_ld_32x32b_x32(tbase + BN + c, vm);
+            tmem_ld_32x32b_x32(tbase + 2 * BN + c, vl);
             tmem_ld_wait();
             const int e0 = n0 + c;
             if (row < p.T && e0 < p.E) {
@@ -224,7 +233,8 @@ router_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
                 const int e = e0 + i;
-                const float a = __uint_as_float(v[i]);
+                const float a = __fadd_rn(__fadd_rn(__uint_as_float(vh[i]), __uint_as_float(vm[i])),
+                                          __uint_as_float(vl[i]));
                 o[i] = (p.bias && e < p.E) ? __fadd_rn(a, p.bias[e]) : a;
             }
             if (p.vec4) {
@@ -268,7 +278,7 @@ size_t router_workspace_bytes(int d, int E) { return static_cast<size_t>(3) * E 
 int router_tile_n(int T, int E) {
     // widest accumulator that still gives about one wave of tiles
     const int mt = (T + rt::BM - 1) / rt::BM;
-    int bn = E <= 32 ? 32 : (E <= 64 ? 64 : 128);
+    int bn = E <= 32 ? 32 : 64;
     while (bn > 32 && static_cast<int64_t>(mt) * ((E + bn - 1) / bn) < 120) bn /= 2;
     return bn;
 }
@@ -278,11 +288,8 @@ cudaError_t router_setup() {
     if ((e = cudaFuncSetAttribute(rt::router_gemm_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   rt::Cfg<32>::BYTES)) != cudaSuccess)
         return e;
-    if ((e = cudaFuncSetAttribute(rt::router_gemm_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  rt::Cfg<64>::BYTES)) != cudaSuccess)
-        return e;
-    return cudaFuncSetAttribute(rt::router_gemm_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                rt::Cfg<128>::BYTES);
+    return cudaFuncSetAttribute(rt::router_gemm_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                rt::Cfg<64>::BYTES);
 }
 
 cudaError_t launch_router_logits(const uint16_t *x, const float *Wr, const float *bias, int T, int d, int E,
@@ -313,11 +320,7 @@ cudaError_t launch_router_logits(const uint16_t *x, const float *Wr, const float
     p.status = status;
     p.timeout_ns = timeout_ns;
     const int tiles = ((T + rt::BM - 1) / rt::BM) * p.NT;
-    switch (bn) {
-        case 32: return rt::launch_gemm<32>(tmX, tmW, p, tiles, stream);
-        case 64: return rt::launch_gemm<64>(tmX, tmW, p, tiles, stream);
-        default: return rt::launch_gemm<128>(tmX, tmW, p, tiles, stream);
-    }
+    return bn == 32 ? rt::launch_gemm<32>(tmX, tmW, p, tiles, stream) : rt::launch_gemm<64>(tmX, tmW, p, tiles, stream);
 }
 
 }  // namespace moe
