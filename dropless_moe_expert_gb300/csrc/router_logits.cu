@@ -30,7 +30,8 @@
 //                         pieces' tiles (128-byte swizzle), which lie one
 //                         after the other in shared memory and so form one
 //                         K-major B operand of 3 BN rows.  One thread issues
-//                         4 tcgen05.mma (M=128, N=3 BN, K=16): TMEM columns
+//                         4 tcgen05.mma (M=128, N=3 BN, K=16; for BN = 128
+//                         two per K step, N = 256 and 128): TMEM columns
 //                         [0, BN) accumulate x.hi, [BN, 2BN) x.mid and
 //                         [2BN, 3BN) x.lo, each in fp32.  Four warps form
 //                         L = (x.hi + x.mid) + x.lo + bias and store fp32
@@ -64,8 +65,11 @@ struct Cfg {
     static constexpr int OFF_TMEM = OFF_BARS + NUM_BARS * 8;
     static constexpr int OFF_ABORT = OFF_TMEM + 4;
     static constexpr int BYTES = OFF_ABORT + 4 + 1024;  // slack for 1024-byte alignment
-    static constexpr int TMEM_COLS = BN == 32 ? 128 : 256;  // 3 BN columns, rounded up to a power of two
-    static_assert(BN == 32 || BN == 64, "accumulator width: 3 BN <= 256 for one MMA");
+    static constexpr int TMEM_COLS = BN == 32 ? 128 : (BN == 64 ? 256 : 512);  // 3 BN, rounded up to a power of two
+    // one MMA of N = 3 BN where that fits (N <= 256); for BN = 128 two, of
+    // N = 256 (hi and mid) and N = 128 (lo)
+    static constexpr bool SPLIT_MMA = 3 * BN > 256;
+    static_assert(BN == 32 || BN == 64 || BN == 128, "accumulator width");
     static_assert(STAGES >= 2 && BYTES <= 227 * 1024, "shared memory budget");
     static_assert(B_PIECE % 1024 == 0, "swizzled tiles must stay 1024-byte aligned");
 };
@@ -186,7 +190,8 @@ router_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
         }
     } else if (warp == 1 && lane == 0) {
         // MMA issuer: per K slice, the hi, mid and lo pieces in turn
-        constexpr uint32_t idesc = idesc_bf16_f32(BM, 3 * BN);
+        constexpr uint32_t idesc = idesc_bf16_f32(BM, C::SPLIT_MMA ? 2 * BN : 3 * BN);
+        constexpr uint32_t idesc_lo = idesc_bf16_f32(BM, BN);
         uint32_t stage = 0, phase = 0;
         bool ok = true, issued = false;
         for (int kb = 0; kb < KB; ++kb) {
@@ -195,9 +200,13 @@ router_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
             const uint32_t sa = smem_u32(smem + stage * C::STAGE);
             const uint64_t adesc = smem_desc_kmajor_sw128(sa);
             const uint64_t bdesc = smem_desc_kmajor_sw128(sa + A_BYTES);  // hi, mid, lo rows: 3 BN
+            const uint64_t bdesc_lo = smem_desc_kmajor_sw128(sa + A_BYTES + 2 * C::B_PIECE);
 #pragma unroll
-            for (int j = 0; j < BK / UMMA_K; ++j)
+            for (int j = 0; j < BK / UMMA_K; ++j) {
                 umma_bf16(tmem_base, adesc + 2 * j, bdesc + 2 * j, idesc, (kb | j) != 0);
+                if (C::SPLIT_MMA)
+                    umma_bf16(tmem_base + 2 * BN, adesc + 2 * j, bdesc_lo + 2 * j, idesc_lo, (kb | j) != 0);
+            }
             issued = true;
             umma_commit(&empty[stage]);
             if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
@@ -278,7 +287,7 @@ size_t router_workspace_bytes(int d, int E) { return static_cast<size_t>(3) * E 
 int router_tile_n(int T, int E) {
     // widest accumulator that still gives about one wave of tiles
     const int mt = (T + rt::BM - 1) / rt::BM;
-    int bn = E <= 32 ? 32 : 64;
+    int bn = E <= 32 ? 32 : (E <= 64 ? 64 : 128);
     while (bn > 32 && static_cast<int64_t>(mt) * ((E + bn - 1) / bn) < 120) bn /= 2;
     return bn;
 }
@@ -288,8 +297,11 @@ cudaError_t router_setup() {
     if ((e = cudaFuncSetAttribute(rt::router_gemm_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   rt::Cfg<32>::BYTES)) != cudaSuccess)
         return e;
-    return cudaFuncSetAttribute(rt::router_gemm_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                rt::Cfg<64>::BYTES);
+    if ((e = cudaFuncSetAttribute(rt::router_gemm_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  rt::Cfg<64>::BYTES)) != cudaSuccess)
+        return e;
+    return cudaFuncSetAttribute(rt::router_gemm_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                rt::Cfg<128>::BYTES);
 }
 
 cudaError_t launch_router_logits(const uint16_t *x, const float *Wr, const float *bias, int T, int d, int E,
@@ -320,7 +332,11 @@ cudaError_t launch_router_logits(const uint16_t *x, const float *Wr, const float
     p.status = status;
     p.timeout_ns = timeout_ns;
     const int tiles = ((T + rt::BM - 1) / rt::BM) * p.NT;
-    return bn == 32 ? rt::launch_gemm<32>(tmX, tmW, p, tiles, stream) : rt::launch_gemm<64>(tmX, tmW, p, tiles, stream);
+    switch (bn) {
+        case 32: return rt::launch_gemm<32>(tmX, tmW, p, tiles, stream);
+        case 64: return rt::launch_gemm<64>(tmX, tmW, p, tiles, stream);
+        default: return rt::launch_gemm<128>(tmX, tmW, p, tiles, stream);
+    }
 }
 
 }  // namespace moe
