@@ -5,7 +5,31 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <algorithm>
+#include <atomic>
+
 namespace moe {
+
+// Blocks of `kernel` (launched with `threads` threads and no dynamic shared
+// memory) that are resident on the current device at once: one wave.
+// Worked out on the first call per device and kept in `cache`, one slot per
+// device (at most 64 devices).
+template <class Kernel>
+cudaError_t one_wave(Kernel kernel, int threads, std::atomic<int> (&cache)[64], int *blocks) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    int wave = cache[dev].load(std::memory_order_relaxed);
+    if (wave == 0) {
+        int sms = 0, per_sm = 0;
+        cudaError_t err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (err == cudaSuccess) err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0);
+        if (err != cudaSuccess) return err;
+        wave = std::max(1, sms * std::max(1, per_sm));
+        cache[dev].store(wave, std::memory_order_relaxed);
+    }
+    *blocks = wave;
+    return cudaSuccess;
+}
 
 // Tokens per routing chunk: the unit of the per-chunk histograms that make the
 // dispatch order deterministic.

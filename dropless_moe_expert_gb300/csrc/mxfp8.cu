@@ -289,20 +289,10 @@ cudaError_t launch_mxfp8_quantize(const uint16_t *src, int rows, int K, uint8_t 
 cudaError_t launch_permute_mxfp8(const uint16_t *x, const int32_t *topk_idx, const int32_t *row_of,
                                  const int32_t *offsets, int T, int K, int d, int E, uint8_t *xq, uint8_t *sfa,
                                  cudaStream_t stream) {
-    // one wave of resident blocks, worked out once per device
     static std::atomic<int> resident[64];
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    int wave = resident[dev].load(std::memory_order_relaxed);
-    if (wave == 0) {
-        int sms = 0, per_sm = 0;
-        cudaError_t err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (err == cudaSuccess)
-            err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, mx::permute_kernel, 32 * mx::PERMUTE_WARPS, 0);
-        if (err != cudaSuccess) return err;
-        wave = std::max(1, sms * std::max(1, per_sm));
-        resident[dev].store(wave, std::memory_order_relaxed);
-    }
+    int wave = 0;
+    const cudaError_t err = one_wave(mx::permute_kernel, 32 * mx::PERMUTE_WARPS, resident, &wave);
+    if (err != cudaSuccess) return err;
     const long long chunks = static_cast<long long>(T) * ((d + 511) / 512);
     const int blocks = static_cast<int>(std::max(1LL, std::min((chunks + mx::PERMUTE_WARPS - 1) / mx::PERMUTE_WARPS,
                                                                 static_cast<long long>(wave))));

@@ -224,19 +224,9 @@ cudaError_t launch_unpermute(const uint16_t *y_perm, const int32_t *row_of, cons
             // DSv3-shaped combine 88.7 -> 79.7 us, the Qwen-shaped 99.6 -> 91.3
             // us; for K = 2 and 6 the per-token form stays faster)
             static std::atomic<int> resident[64];
-            int dev = 0;
-            if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-            int wave = resident[dev].load(std::memory_order_relaxed);
-            if (wave == 0) {
-                int sms = 0, per_sm = 0;
-                cudaError_t err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-                if (err == cudaSuccess)
-                    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pm::unpermute_unit_kernel<8>,
-                                                                        pm::THREADS, 0);
-                if (err != cudaSuccess) return err;
-                wave = std::max(1, sms * std::max(1, per_sm));
-                resident[dev].store(wave, std::memory_order_relaxed);
-            }
+            int wave = 0;
+            const cudaError_t err = one_wave(pm::unpermute_unit_kernel<8>, pm::THREADS, resident, &wave);
+            if (err != cudaSuccess) return err;
             const long long units = static_cast<long long>(T) * ((nvec + 31) / 32);
             const int blocks = static_cast<int>(std::max(1LL, std::min((units + 7) / 8, static_cast<long long>(wave))));
             pm::unpermute_unit_kernel<8><<<blocks, pm::THREADS, 0, stream>>>(src, row_of, topk_w, T, nvec, dst);

@@ -180,6 +180,7 @@ def random_shape_cases():
         Shape(T=129, d=128, E=256, K=8, f=64),
         Shape(T=1000, d=512, E=8, K=1, f=320),
         Shape(T=517, d=320, E=16, K=4, f=448),
+        Shape(T=333, d=320, E=16, K=8, f=192),   # K = 8 with a ragged 256-column round of the combine
         # average group >= 384 rows: the grouped GEMMs take their CTA-pair
         # (256-row tile) path; ragged tails inside the pair tiles
         Shape(T=2048, d=256, E=4, K=1, f=256),
