@@ -56,16 +56,16 @@ constexpr int BM = 128;
 constexpr int BK = 128;          // elements (= bytes) of K per stage
 constexpr int UMMA_K = 32;
 constexpr int BAND = 16;
-// warps 0 and 1: TMA producer and MMA issuer; then the epilogue warps: GEMM1
-// (whose tiles are short and whose epilogue forms and quantises h) uses two
-// per TMEM lane quarter, each owning half of the tile's h columns), GEMM2
-// one (bf16 rows written by TMA stores of full lines, which measured faster
-// than eight warps of direct 16-byte row stores).  With a single accumulator
-// the epilogue is not overlapped with the next mainloop, so its length
-// counts in full.
+// warps 0 and 1: TMA producer and MMA issuer; then eight epilogue warps, two
+// per TMEM lane quarter, each owning half of the tile's columns (GEMM1: 64 of
+// its 128 h columns, GEMM2: 128 of its 256 output columns).  With a single
+// accumulator the epilogue would hold the next tile's MMAs for its whole
+// length, so each thread first loads all of its accumulator values and hands
+// the accumulator back, then forms and stores its outputs beside the next
+// tile's mainloop.
 template <bool SWIGLU>
 struct Roles {
-    static constexpr int EPI_WARPS = SWIGLU ? 8 : 4;
+    static constexpr int EPI_WARPS = 8;
     static constexpr int THREADS = 64 + 32 * EPI_WARPS;
 };
 constexpr int STAGES = 4;
@@ -155,6 +155,59 @@ __device__ __forceinline__ void epilogue_swiglu_mx(const MxParams &mp, uint32_t 
         const size_t atom = clamp_atom(static_cast<size_t>(rb) * ns + t.n_blk, mp.sfh_atoms);
         const size_t word = atom * 128 + ((grow - t.row0) & 31) * 4 + ((grow - t.row0) >> 5);
         reinterpret_cast<uint16_t *>(mp.sfh)[2 * word + half] = static_cast<uint16_t>(scales);
+    }
+}
+
+// GEMM2 epilogue of one warp: 32 rows and half (128) of the tile's 256
+// output columns.  Each thread owns one row; it loads its 128 accumulator
+// values, releases the accumulator (`release`), then converts them to bf16
+// 32 columns at a time.  A chunk whose 32 rows all belong to the group is
+// staged in the warp's shared-memory buffer (64-byte swizzle) and written by
+// one TMA store of full lines; one that crosses the group's end is written
+// by masked 16-byte stores per row.
+template <typename Release>
+__device__ __forceinline__ void epilogue_plain_mx(const gg::Params &p, const CUtensorMap *tm_out, uint8_t *buf,
+                                                  uint32_t tbase, const gg::Tile &t, int q, int half, int lane,
+                                                  Release release) {
+    const int wrow0 = t.row0 + q * 32;
+    if (wrow0 >= t.grp_end) {  // warp-uniform: nothing of this warp's rows to store
+        release();
+        return;
+    }
+    const bool full = wrow0 + 31 < t.grp_end;
+    const int grow = wrow0 + lane;
+    const bool row_ok = grow < t.grp_end;
+    uint32_t v[4][32];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) tmem_ld_32x32b_x32(tbase + half * 128 + 32 * j, v[j]);
+    tmem_ld_wait();
+    release();
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int col = t.n_blk * BN_ACC + half * 128 + 32 * j;
+        if (col >= p.n_out) break;  // column tail (uniform)
+        uint32_t packed[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            packed[i] = gg::pack_bf16x2(__uint_as_float(v[j][2 * i]), __uint_as_float(v[j][2 * i + 1]));
+        if (full) {
+            if (lane == 0) bulk_wait_read<0>();  // the previous chunk's store has read the buffer
+            __syncwarp();
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int kk = k ^ ((lane >> 1) & 3);
+                *reinterpret_cast<uint4 *>(buf + lane * 64 + kk * 16) =
+                    make_uint4(packed[4 * k], packed[4 * k + 1], packed[4 * k + 2], packed[4 * k + 3]);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                tma_store_2d_evict_first(tm_out, buf, col, wrow0, l2_policy_evict_first());
+                bulk_commit();
+            }
+        } else if (row_ok) {
+            gg::store_row32(p.out + static_cast<size_t>(grow) * p.n_out + col, packed);
+        }
     }
 }
 
@@ -298,9 +351,9 @@ grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
         }
     } else {
         const int q = warp & 3;  // TMEM lane quarter this warp may access
-        const int half = (warp - 2) / 4;  // GEMM1: which 64 of the tile's 128 h columns
-        uint8_t *stage_buf = smem + OFF_EPI + ((warp - 2) & 3) * 2 * EPI_BUF;
-        uint32_t sbuf = 0;
+        const int half = (warp - 2) / 4;  // which half of the tile's columns
+        static_assert(Roles<SWIGLU>::EPI_WARPS * EPI_BUF <= EPI_BYTES, "epilogue staging");
+        uint8_t *stage_buf = smem + OFF_EPI + (warp - 2) * EPI_BUF;
         uint32_t acc_phase = 0;
         for (int k = 0, tile = gg::round_position(0, blockIdx.x, gridDim.x, mix); tile < total_tiles;
              ++k, tile = gg::round_position(k, blockIdx.x, gridDim.x, mix)) {
@@ -319,9 +372,7 @@ grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
             if (SWIGLU) {
                 epilogue_swiglu_mx(mp, tbase, t, q, half, lane, s_pre[t.e] / NT + t.m_blk, release);
             } else {
-                gg::epilogue_tile<false>(p, &tmOut, nullptr, stage_buf, sbuf, tbase, t.n_blk, t.row0 + q * 32, lane,
-                                         t.grp_end);
-                release();
+                epilogue_plain_mx(p, &tmOut, stage_buf, tbase, t, q, half, lane, release);
             }
             acc_phase ^= 1u;
         }
