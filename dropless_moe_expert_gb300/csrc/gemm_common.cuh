@@ -266,6 +266,54 @@ __device__ __forceinline__ void combine_arrive(const Params &p, int n_blk, int g
     }
 }
 
+// One 32-column chunk of a warp's 32 rows, 16 words of packed bf16 pairs per
+// lane, into dst (row length ld, tensor map tm) at column col.  When all 32
+// rows belong to the group (`full`) the chunk is staged in the warp's buffer
+// `sbuf` of NBUF (64-byte swizzle) and written by one TMA store of full lines;
+// otherwise each lane whose row lies in the group stores its 64 bytes.
+template <int NBUF>
+__device__ __forceinline__ void put_chunk32(const CUtensorMap *tm, __nv_bfloat16 *dst, int ld, int col,
+                                            const uint32_t (&packed)[16], bool full, bool row_ok, int grow,
+                                            int wrow0, int lane, uint8_t *stage, uint32_t &sbuf) {
+    if (full) {
+        uint8_t *buf = stage + sbuf * EPI_BUF;
+        if (lane == 0) bulk_wait_read<NBUF - 1>();  // this buffer's store from NBUF chunks ago has read it
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int jj = j ^ ((lane >> 1) & 3);
+            *reinterpret_cast<uint4 *>(buf + lane * 64 + jj * 16) =
+                make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            // the output is not read again by this kernel: let L2 evict it
+            // before the operand tiles that other CTAs still share
+            tma_store_2d_evict_first(tm, buf, col, wrow0, l2_policy_evict_first());
+            bulk_commit();
+        }
+        sbuf = (sbuf + 1 == NBUF) ? 0u : sbuf + 1;
+    } else if (row_ok) {
+        store_row32(dst + static_cast<size_t>(grow) * ld + col, packed);
+    }
+}
+
+// silu(g) * u of 32 gate and up accumulator values, as 16 packed bf16 pairs
+__device__ __forceinline__ void swiglu32(const uint32_t (&g)[32], const uint32_t (&u)[32], uint32_t (&packed)[16]) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        float h2[2];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const float gv = __uint_as_float(g[2 * i + k]);
+            const float uv = __uint_as_float(u[2 * i + k]);
+            h2[k] = __fdividef(gv, 1.0f + __expf(-gv)) * uv;  // silu(g) * u
+        }
+        packed[i] = pack_bf16x2(h2[0], h2[1]);
+    }
+}
+
 // Epilogue of one accumulator for one warp: 32 TMEM lanes = 32 output rows
 // wrow0..wrow0+31 (this thread's row is wrow0 + lane), tbase points at the
 // warp's lane quarter of the accumulator.  The warp covers output columns
@@ -312,28 +360,7 @@ __device__ __forceinline__ void epilogue_tile(const Params &p, const CUtensorMap
     // 32 columns of the warp's 32 rows into `dst` (row length ld, its tensor
     // map `tm`) at column col
     auto put = [&](const CUtensorMap *tm, __nv_bfloat16 *dst, int ld, int col, const uint32_t (&packed)[16]) {
-        if (full) {
-            uint8_t *buf = stage + sbuf * EPI_BUF;
-            if (lane == 0) bulk_wait_read<NBUF - 1>();  // this buffer's store from NBUF chunks ago has read it
-            __syncwarp();
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int jj = j ^ ((lane >> 1) & 3);
-                *reinterpret_cast<uint4 *>(buf + lane * 64 + jj * 16) =
-                    make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                // the output is not read again by this kernel: let L2 evict it
-                // before the operand tiles that other CTAs still share
-                tma_store_2d_evict_first(tm, buf, col, wrow0, l2_policy_evict_first());
-                bulk_commit();
-            }
-            sbuf = (sbuf + 1 == NBUF) ? 0u : sbuf + 1;
-        } else if (row_ok) {
-            store_row32(dst + static_cast<size_t>(grow) * ld + col, packed);
-        }
+        put_chunk32<NBUF>(tm, dst, ld, col, packed, full, row_ok, grow, wrow0, lane, stage, sbuf);
     };
     auto emit = [&](int c, const uint32_t (&packed)[16]) {
         const int col = n_blk * NCOL + c;
@@ -348,17 +375,7 @@ __device__ __forceinline__ void epilogue_tile(const Params &p, const CUtensorMap
             tmem_ld_32x32b_x32(tbase + BN_ACC / 2 + c, u);
             tmem_ld_wait();
             uint32_t packed[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                float h2[2];
-#pragma unroll
-                for (int k = 0; k < 2; ++k) {
-                    const float gv = __uint_as_float(g[2 * i + k]);
-                    const float uv = __uint_as_float(u[2 * i + k]);
-                    h2[k] = __fdividef(gv, 1.0f + __expf(-gv)) * uv;  // silu(g) * u
-                }
-                packed[i] = pack_bf16x2(h2[0], h2[1]);
-            }
+            swiglu32(g, u, packed);
             emit(c, packed);
             const int col = n_blk * NCOL + c;
             if (p.preact != nullptr && col < p.n_out) {
@@ -391,6 +408,104 @@ __device__ __forceinline__ void epilogue_tile(const Params &p, const CUtensorMap
             }
         }
     }
+}
+
+// GEMM1 epilogue of one warp that hands its accumulator back early: 32 rows
+// and the 64 h columns [c_begin, c_begin + 64) of the tile, two 32-column
+// chunks.  The first chunk's gate and up values are loaded and turned into
+// h, the second chunk's are loaded, and then the accumulator is released
+// (`release`: fence, warp sync, arrive) before the second chunk's h is
+// formed and both chunks are stored.  The same arithmetic and stores as
+// epilogue_tile<true> without pre-activations, so h is bit-identical.
+template <typename Release>
+__device__ __forceinline__ void epilogue_swiglu_early(const Params &p, const CUtensorMap *tm_out, uint8_t *stage,
+                                                      uint32_t &sbuf, uint32_t tbase, int n_blk, int wrow0, int lane,
+                                                      int grp_end, int c_begin, Release release) {
+    if (wrow0 >= grp_end) {  // whole slice outside the group (warp-uniform)
+        release();
+        return;
+    }
+    const bool full = wrow0 + 31 < grp_end;
+    const int grow = wrow0 + lane;
+    const bool row_ok = grow < grp_end;
+    constexpr int NCOL = BN_ACC / 2;
+    uint32_t g[32], u[32], h0[16], h1[16];
+    tmem_ld_32x32b_x32(tbase + c_begin, g);
+    tmem_ld_32x32b_x32(tbase + NCOL + c_begin, u);
+    tmem_ld_wait();
+    swiglu32(g, u, h0);
+    tmem_ld_32x32b_x32(tbase + c_begin + 32, g);
+    tmem_ld_32x32b_x32(tbase + NCOL + c_begin + 32, u);
+    tmem_ld_wait();
+    release();
+    swiglu32(g, u, h1);
+    const int col = n_blk * NCOL + c_begin;
+    if (col < p.n_out) put_chunk32<1>(tm_out, p.out, p.n_out, col, h0, full, row_ok, grow, wrow0, lane, stage, sbuf);
+    if (col + 32 < p.n_out)
+        put_chunk32<1>(tm_out, p.out, p.n_out, col + 32, h1, full, row_ok, grow, wrow0, lane, stage, sbuf);
+}
+
+// silu(g) * u of 16 gate and up accumulator values into 8 packed bf16 pairs
+// (the first or second half of a 32-column chunk's packed words)
+__device__ __forceinline__ void swiglu16(const uint32_t (&g)[16], const uint32_t (&u)[16], uint32_t *packed) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        float h2[2];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const float gv = __uint_as_float(g[2 * i + k]);
+            const float uv = __uint_as_float(u[2 * i + k]);
+            h2[k] = __fdividef(gv, 1.0f + __expf(-gv)) * uv;  // silu(g) * u
+        }
+        packed[i] = pack_bf16x2(h2[0], h2[1]);
+    }
+}
+
+// GEMM1 epilogue of one warp over a tile of two row blocks (accumulators at
+// tb0 and tb1, rows wrow0 and wrow0 + 128): the 64 h columns [c_begin,
+// c_begin + 64) of each block are formed 16 columns at a time and kept in
+// registers, each accumulator is released once its last values are loaded,
+// and only then are the four 32-column chunks stored.  Both accumulators go
+// back before any store.  The arithmetic and stores are epilogue_tile<true>'s
+// without pre-activations, so h is bit-identical.  Returns false if the wait
+// for block 1's accumulator gave up.
+template <typename Wait, typename Release>
+__device__ __forceinline__ bool epilogue_swiglu_early2(const Params &p, const CUtensorMap *tm_out, uint8_t *stage,
+                                                       uint32_t &sbuf, uint32_t tb0, uint32_t tb1, int n_blk,
+                                                       int wrow0, int lane, int grp_end, int c_begin, Wait wait1,
+                                                       Release release0, Release release1) {
+    constexpr int NCOL = BN_ACC / 2;
+    uint32_t h[4][16];
+    // the 64 columns of one block, 16 at a time; `release` after the last load
+    auto block = [&](uint32_t tb, uint32_t(*hb)[16], Release release) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            uint32_t g[16], u[16];
+            tmem_ld_32x32b_x16(tb + c_begin + 16 * j, g);
+            tmem_ld_32x32b_x16(tb + NCOL + c_begin + 16 * j, u);
+            tmem_ld_wait();
+            if (j == 3) release();
+            swiglu16(g, u, &hb[j >> 1][8 * (j & 1)]);
+        }
+    };
+    block(tb0, h, release0);  // block 0: its rows start inside the group
+    if (!wait1()) return false;
+    if (wrow0 + 128 < grp_end) block(tb1, h + 2, release1);
+    else release1();
+    const int col = n_blk * NCOL + c_begin;
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+        const int wr = wrow0 + 128 * b;
+        if (wr >= grp_end) break;  // warp-uniform
+        const bool full = wr + 31 < grp_end;
+        const int grow = wr + lane;
+        const bool row_ok = grow < grp_end;
+        if (col < p.n_out)
+            put_chunk32<1>(tm_out, p.out, p.n_out, col, h[2 * b], full, row_ok, grow, wr, lane, stage, sbuf);
+        if (col + 32 < p.n_out)
+            put_chunk32<1>(tm_out, p.out, p.n_out, col + 32, h[2 * b + 1], full, row_ok, grow, wr, lane, stage, sbuf);
+    }
+    return true;
 }
 
 }  // namespace gg

@@ -48,7 +48,7 @@
 // 64 KB.
 //
 // Fused permute (GATHER, single-CTA GEMM1 only; "Optimization 2" of the page:
-// a naive dispatch writes and reads the tokens again): four more warps copy
+// a naive dispatch writes and reads the tokens again): two more warps copy
 // the A rows straight from the token matrix x, row r being x[src_tok[r]],
 // with 16-byte cp.async into the same 128-byte-swizzled layout TMA writes.
 // Each gathering lane arrives on the stage's full barrier once its copies
@@ -79,7 +79,8 @@ constexpr int UMMA_K = 16;
 constexpr int TMEM_COLS = 2 * BN_ACC;
 constexpr int THREADS = 192;
 constexpr int BOX_ROWS = 128;  // every K-major TMA box is 128 rows x 64 bf16
-constexpr int GATHER_WARPS = 4;  // fused permute: the last four warps copy the A rows
+constexpr int GATHER_WARPS = 2;  // fused permute: the last two warps copy the A rows
+constexpr int GATHER_ROWS = 128 / GATHER_WARPS / 4;  // rows of a 128-row block per gathering lane
 // Epilogue warps of the single-CTA kernel.  GEMM1 (SwiGLU) takes two per TMEM
 // lane quarter, each storing half of the tile's 128 h columns through one
 // staging buffer: its tiles of two row blocks use both accumulators, so
@@ -141,20 +142,20 @@ constexpr int P_SMEM_BYTES = L2::BYTES;
 static_assert(SMEM_BYTES <= 227 * 1024 && P_SMEM_BYTES <= 227 * 1024, "shared memory budget");
 static_assert(B_BYTES == (BN_ACC / 64) * BT_BOX && P_B_BYTES == 2 * BT_BOX, "MN-major B boxes fill the B slot");
 
-// Fused permute: the 8 rows of a 128-row block starting at row0 that this
-// lane copies, as pointers to their token rows in x, and a bit per row that
-// lies inside the group.  Lane l copies 16-byte chunk l % 8 of rows
-// 32 gw + 4 i + l / 8 (i = 0..7), so eight lanes move one whole 128-byte
-// line.  Rows past the group's end are not copied: row i of A reaches only
+// Fused permute: the GATHER_ROWS rows of a 128-row block starting at row0
+// that this lane copies, as pointers to their token rows in x, and a bit per
+// row that lies inside the group.  Lane l of gathering warp gw copies 16-byte
+// chunk l % 8 of rows (128 / GATHER_WARPS) gw + 4 i + l / 8, so eight lanes
+// move one whole 128-byte line.  Rows past the group's end are not copied: row i of A reaches only
 // row i of the accumulator, which the epilogue masks, so whatever their
 // slot holds cannot reach a stored value.  A token index outside [0, T) is
 // clamped (outside the contract, but never read out of bounds).
 __device__ __forceinline__ uint32_t gather_sources(const Params &p, int row0, int grp_end, int gw, int lane,
-                                                   const __nv_bfloat16 *(&src)[8]) {
+                                                   const __nv_bfloat16 *(&src)[GATHER_ROWS]) {
     uint32_t valid = 0;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int row = row0 + 32 * gw + 4 * i + (lane >> 3);
+    for (int i = 0; i < GATHER_ROWS; ++i) {
+        const int row = row0 + 4 * GATHER_ROWS * gw + 4 * i + (lane >> 3);
         const int r = min(row, grp_end - 1);
         const int tok = min(max(p.gather_src[r], 0), p.gather_T - 1);
         src[i] = p.gather_x + static_cast<size_t>(tok) * p.Kdim + (lane & 7) * 8;
@@ -164,12 +165,12 @@ __device__ __forceinline__ uint32_t gather_sources(const Params &p, int row0, in
 }
 // Copies K slice kb of those rows into a 128-row A block `slot` (128-byte
 // swizzle: 16-byte chunk j of row r sits at chunk j ^ (r % 8) of its line).
-__device__ __forceinline__ void gather_block(uint8_t *slot, const __nv_bfloat16 *const (&src)[8], uint32_t valid,
-                                             int gw, int kb, int lane) {
+__device__ __forceinline__ void gather_block(uint8_t *slot, const __nv_bfloat16 *const (&src)[GATHER_ROWS],
+                                             uint32_t valid, int gw, int kb, int lane) {
     const int j = lane & 7;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int r = 32 * gw + 4 * i + (lane >> 3);
+    for (int i = 0; i < GATHER_ROWS; ++i) {
+        const int r = 4 * GATHER_ROWS * gw + 4 * i + (lane >> 3);
         if (valid & (1u << i)) cp_async_16(slot + r * (BK * 2) + ((j ^ (r & 7)) << 4), src[i] + kb * BK);
     }
 }
@@ -396,7 +397,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             const Tile t =
                 decode_tile<TILE_ROWS, BAND>(visit_order(tile, total_tiles, mix), s_pre, s_off, s_end, E, NT);
             const bool two = t.grp_end - t.row0 > BM;
-            const __nv_bfloat16 *src0[8], *src1[8];
+            const __nv_bfloat16 *src0[GATHER_ROWS], *src1[GATHER_ROWS];
             const uint32_t v0 = gather_sources(p, t.row0, t.grp_end, gw, lane, src0);
             const uint32_t v1 = two ? gather_sources(p, t.row0 + BM, t.grp_end, gw, lane, src1) : 0u;
             for (int kb = 0; kb < KB; ++kb) {
@@ -436,16 +437,52 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             const Tile t =
                 decode_tile<TILE_ROWS, BAND>(visit_order(tile, total_tiles, mix), s_pre, s_off, s_end, E, NT);
             const int nblk = t.grp_end - t.row0 > BM ? 2 : 1;
+            if (SWIGLU && p.preact == nullptr && nblk == 2 && t.row0 + q * 32 < t.grp_end) {
+                // GEMM1, two blocks: both accumulators go back before any store
+                const uint32_t a0 = acc, a1 = acc ^ 1u;
+                if (!mbar_wait(&tfull[a0], ph[a0], s_abort, p.status, p.timeout_ns)) break;
+                tc_fence_after();
+                const uint32_t tq = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+                auto release_of = [&](uint32_t a) {
+                    return [&, a]() {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&tempty[a]);
+                    };
+                };
+                auto wait1 = [&]() {
+                    if (!mbar_wait(&tfull[a1], ph[a1], s_abort, p.status, p.timeout_ns)) return false;
+                    tc_fence_after();
+                    return true;
+                };
+                if (!epilogue_swiglu_early2(p, &tmOut, stage, sbuf, tq + a0 * BN_ACC, tq + a1 * BN_ACC, t.n_blk,
+                                            t.row0 + q * 32, lane, t.grp_end, c_begin, wait1, release_of(a0),
+                                            release_of(a1)))
+                    break;
+                ph[a0] ^= 1u;
+                ph[a1] ^= 1u;
+                continue;  // a tile of two blocks leaves acc as it is
+            }
             for (int b = 0; b < nblk; ++b) {
                 const uint32_t a = acc ^ static_cast<uint32_t>(b);
                 if (!mbar_wait(&tfull[a], ph[a], s_abort, p.status, p.timeout_ns)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + a * BN_ACC;
-                epilogue_tile<SWIGLU, NBUF>(p, &tmOut, &tmPre, stage, sbuf, tbase, t.n_blk, t.row0 + b * BM + q * 32,
-                                            lane, t.grp_end, c_begin, c_end);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&tempty[a]);
+                // hands accumulator a back to the MMA thread (after this warp's TMEM loads)
+                auto release = [&]() {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&tempty[a]);
+                };
+                if (SWIGLU && p.preact == nullptr) {
+                    // GEMM1: the accumulator goes back once its values are loaded
+                    epilogue_swiglu_early(p, &tmOut, stage, sbuf, tbase, t.n_blk, t.row0 + b * BM + q * 32, lane,
+                                          t.grp_end, c_begin, release);
+                } else {
+                    epilogue_tile<SWIGLU, NBUF>(p, &tmOut, &tmPre, stage, sbuf, tbase, t.n_blk,
+                                                t.row0 + b * BM + q * 32, lane, t.grp_end, c_begin, c_end);
+                    release();
+                }
                 ph[a] ^= 1u;
             }
             if (nblk == 1) acc ^= 1u;
