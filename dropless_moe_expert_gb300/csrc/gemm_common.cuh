@@ -211,15 +211,18 @@ __device__ __forceinline__ void fma_bf16x8(float (&acc)[8], float w, const uint4
     }
 }
 
-// Fused combine, after this warp's 32 rows of y_perm (columns of block
-// n_blk) are stored.  Each row's lane makes its stores visible and counts
-// the row for its token; the lane that brings the count to K is the
-// token's last row in this column block, and the warp then forms
+// Fused combine, after this warp's 32 rows of y_perm (its columns of block
+// n_blk) are stored; `parts` warps share those rows, each storing its share
+// of the block's columns.  Each row's lane makes its stores visible and
+// counts the row for its token; the lane that brings the count to K * parts
+// holds the token's last row (and share) in this column block, and the warp
+// then forms
 //   y[t, cols] = bf16( sum_{k=0..K-1} w[t,k] * y_perm[row_of[t,k], cols] )
 // (fp32 fused multiply-add in ascending k, the unfused combine's
 // arithmetic) from the K stored rows, 8 columns per lane.  Which row comes
 // last does not change the sum, so the result is deterministic.
-__device__ __forceinline__ void combine_arrive(const Params &p, int n_blk, int grow, bool row_ok, int lane) {
+__device__ __forceinline__ void combine_arrive(const Params &p, int n_blk, int grow, bool row_ok, int lane,
+                                               int parts) {
     const Combine &cb = p.comb;
     __threadfence();  // this row's stores before its count
     int tok = -1;
@@ -227,7 +230,7 @@ __device__ __forceinline__ void combine_arrive(const Params &p, int n_blk, int g
     if (row_ok) {
         tok = cb.src_tok[grow];
         if (tok >= 0 && tok < cb.T)
-            last = atomicAdd(&cb.counters[static_cast<size_t>(tok) * cb.nb + n_blk], 1) == cb.K - 1;
+            last = atomicAdd(&cb.counters[static_cast<size_t>(tok) * cb.nb + n_blk], 1) == cb.K * parts - 1;
     }
     unsigned m = __ballot_sync(0xffffffffu, last);
     if (m == 0) return;
@@ -353,7 +356,7 @@ __device__ __forceinline__ void epilogue_tile(const Params &p, const CUtensorMap
                 if (row_ok) store_row32(p.out + static_cast<size_t>(grow) * p.n_out + col + 32 * hlf, packed);
             }
         }
-        combine_arrive(p, n_blk, grow, row_ok, lane);
+        combine_arrive(p, n_blk, grow, row_ok, lane, BN_ACC / (c_end - c_begin));
         return;
     }
     constexpr int NCOL = SWIGLU ? BN_ACC / 2 : BN_ACC;

@@ -81,14 +81,14 @@ constexpr int THREADS = 192;
 constexpr int BOX_ROWS = 128;  // every K-major TMA box is 128 rows x 64 bf16
 constexpr int GATHER_WARPS = 2;  // fused permute: the last two warps copy the A rows
 constexpr int GATHER_ROWS = 128 / GATHER_WARPS / 4;  // rows of a 128-row block per gathering lane
-// Epilogue warps of the single-CTA kernel.  GEMM1 (SwiGLU) takes two per TMEM
-// lane quarter, each storing half of the tile's 128 h columns through one
-// staging buffer: its tiles of two row blocks use both accumulators, so
-// their epilogue runs between mainloops and its length counts in full.  The
-// plain GEMMs keep one per quarter, with two staging buffers each.
+// Epilogue warps of the single-CTA kernel: two per TMEM lane quarter, each
+// owning half of the tile's columns (GEMM1: 64 of its 128 h columns; the
+// plain GEMMs: 128 of 256) and storing through one staging buffer.  Tiles of
+// two row blocks use both accumulators, so their epilogue runs between
+// mainloops and its length counts in full.
 template <bool SWIGLU>
 __host__ __device__ constexpr int epi_warps() {
-    return SWIGLU ? 8 : 4;
+    return 8;
 }
 template <bool SWIGLU, bool GATHER>
 __host__ __device__ constexpr int threads_of() {
@@ -414,11 +414,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         cp_async_wait_all();  // this lane's copies have landed before the CTA's shared memory goes away
     } else {
         const int q = warp & 3;  // TMEM lane quarter this warp may access
-        constexpr int NBUF = SWIGLU ? 1 : 2;  // staging buffers per epilogue warp
+        constexpr int NBUF = 1;  // staging buffers per epilogue warp
         static_assert(epi_warps<SWIGLU>() * NBUF * EPI_BUF == EPI_BYTES, "epilogue staging");
-        // GEMM1: the two warps of a lane quarter split the tile's 128 h columns
-        const int c_begin = SWIGLU ? ((warp - 2) >> 2) * (BN_ACC / 4) : 0;
-        const int c_end = SWIGLU ? c_begin + BN_ACC / 4 : BN_ACC;
+        // the two warps of a lane quarter split the tile's columns
+        constexpr int SHARE = (SWIGLU ? BN_ACC / 2 : BN_ACC) / 2;
+        const int c_begin = ((warp - 2) >> 2) * SHARE;
+        const int c_end = c_begin + SHARE;
         uint8_t *stage = smem + L1::OFF_EPI + (warp - 2) * NBUF * EPI_BUF;
         uint32_t sbuf = 0;
         uint32_t acc = 0;
