@@ -100,6 +100,18 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const void *tmap, uint64_
         : "memory");
 }
 
+// The same box delivered to every CTA of `cta_mask` in the cluster, at the
+// same shared-memory offset in each, completing its bytes on the mbarrier at
+// the same offset in each.
+__device__ __forceinline__ void tma_load_2d_multicast(void *dst, const void *tmap, uint64_t *bar, int c_inner,
+                                                      int c_outer, uint16_t cta_mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
+        "l"(tmap), "r"(smem_u32(bar)), "r"(c_inner), "r"(c_outer), "h"(cta_mask)
+        : "memory");
+}
+
 // Tensor maps edited on the device: a copy of a host-encoded map in global
 // memory gets another base address and another extent of dimension 1 (rows),
 // and is then published to the tensor-map proxy (release by the writer,
@@ -238,6 +250,16 @@ __device__ __forceinline__ void umma_commit(uint64_t *bar) {
                  : "memory");
 }
 
+// Arrives once on the mbarrier at the same offset in every CTA of `cta_mask`
+// when every MMA issued so far by this thread is done.
+__device__ __forceinline__ void umma_commit_multicast(uint64_t *bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"(cta_mask)
+        : "memory");
+}
+
 // The same for a CTA pair (cta_group::2): allocation and release are
 // collective -- one warp of each of the two CTAs executes them.
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t *dst_smem, uint32_t ncols) {
@@ -272,8 +294,8 @@ __device__ __forceinline__ void umma_commit_pair_multicast(uint64_t *bar, uint16
         : "memory");
 }
 
-// 32 TMEM lanes x 32 consecutive 32-bit columns: thread i of the warp gets
-// lane (base lane + i), columns col..col+31 in r[0..31].
+// 32 TMEM lanes x 16 consecutive 32-bit columns: thread i of the warp gets
+// lane (base lane + i), columns col..col+15 in r[0..15].
 __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
@@ -282,6 +304,8 @@ __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)
           "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
 }
+// 32 TMEM lanes x 32 consecutive 32-bit columns: thread i of the warp gets
+// lane (base lane + i), columns col..col+31 in r[0..31].
 __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
