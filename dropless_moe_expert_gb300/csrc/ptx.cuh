@@ -100,18 +100,6 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const void *tmap, uint64_
         : "memory");
 }
 
-// The same box delivered to every CTA of `cta_mask` in the cluster, at the
-// same shared-memory offset in each, completing its bytes on the mbarrier at
-// the same offset in each.
-__device__ __forceinline__ void tma_load_2d_multicast(void *dst, const void *tmap, uint64_t *bar, int c_inner,
-                                                      int c_outer, uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
-        "l"(tmap), "r"(smem_u32(bar)), "r"(c_inner), "r"(c_outer), "h"(cta_mask)
-        : "memory");
-}
-
 // Tensor maps edited on the device: a copy of a host-encoded map in global
 // memory gets another base address and another extent of dimension 1 (rows),
 // and is then published to the tensor-map proxy (release by the writer,
@@ -248,16 +236,6 @@ __device__ __forceinline__ void umma_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                      smem_u32(bar))
                  : "memory");
-}
-
-// Arrives once on the mbarrier at the same offset in every CTA of `cta_mask`
-// when every MMA issued so far by this thread is done.
-__device__ __forceinline__ void umma_commit_multicast(uint64_t *bar, uint16_t cta_mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            smem_u32(bar)),
-        "h"(cta_mask)
-        : "memory");
 }
 
 // The same for a CTA pair (cta_group::2): allocation and release are
