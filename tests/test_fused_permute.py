@@ -7,8 +7,10 @@ Small and medium shapes compare every row of h with the oracle's
 full-size DeepSeek-V3- and Qwen-shaped layers, the small-group workloads this
 path is meant for, compare one row of every 128-row slice of every live
 expert group, and each group's first and last rows, with the expert FFN
-evaluated from the definition.  Every case also checks that h is bit for bit
-the unfused path's, since both feed the tensor cores the same bytes."""
+evaluated from the definition, and so do the skew- and Mixtral-shaped layers,
+whose large groups the unfused path runs on the CTA-pair kernel.  Every case
+also checks that h is bit for bit the unfused path's, since both feed the
+tensor cores the same bytes."""
 import numpy as np
 import pytest
 import torch
@@ -26,6 +28,9 @@ CASES = random_shape_cases() + [
     Shape(T=130, d=192, E=256, K=2, f=128, bias="zipf_1.1"),          # > 100 empty experts
     Shape(T=2048, d=512, E=128, K=8, f=512, bias="zipf_1.1"),         # several tiles per CTA, two-block tiles
     Shape(T=4096, d=512, E=8, K=2, f=256, bias="normal_0.5"),         # pair-sized groups on the single-CTA kernel
+    Shape(T=8192, d=512, E=8, K=2, f=1024, bias="normal_0.5"),        # pair-sized groups, several tiles per CTA
+    Shape(T=4096, d=512, E=16, K=2, f=256, bias="zipf_1.1"),          # pair-sized, empty and <= 128-row groups
+    Shape(T=4096, d=4096, E=4, K=2, f=1024, bias="normal_0.5"),       # pair-sized groups, 4096-deep reduction
 ]
 
 
@@ -76,7 +81,7 @@ def test_fused_permute_repeated_calls_and_token_clamp():
     assert bool(torch.isfinite(c.float()).all())
 
 
-@pytest.mark.parametrize("name", ["dsv3", "qwen"])
+@pytest.mark.parametrize("name", ["dsv3", "qwen", "skew", "mixtral"])
 def test_fused_permute_full_size_sampled_rows(name):
     import dropless_moe_expert_gb300 as moe
     s = shape(name)
