@@ -723,7 +723,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
             epilogue_tile<SWIGLU>(p, &tmOut, &tmPre, stage, sbuf, tbase, t.n_blk, wrow0, lane, t.grp_end);
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(tempty0 + 8u * acc);
+            if (lane == 0) mbar_arrive_cluster_cta(tempty0 + 8u * acc);
             acc ^= 1u;
             if (acc == 0) acc_phase ^= 1u;
         }

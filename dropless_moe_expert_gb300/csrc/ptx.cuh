@@ -190,6 +190,15 @@ __device__ __forceinline__ void st_shared_cluster(uint32_t cluster_addr, int v) 
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
+// Arrive on a (possibly remote) mbarrier with release semantics at CTA
+// scope only: for hand-overs that carry no data in memory, such as an
+// accumulator whose TMEM reads were already waited for and fenced with
+// tcgen05.fence::before_thread_sync.  A cluster-scope release fences this
+// thread's memory operations at cluster scope first and holds the thread
+// until the peer observes the arrival.
+__device__ __forceinline__ void mbar_arrive_cluster_cta(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
 // TMA load into this CTA's shared memory that signals an mbarrier of either CTA
 // of the pair (given by its shared::cluster address).
 __device__ __forceinline__ void tma_load_2d_pair(void *dst, const void *tmap, uint32_t mbar_cluster_addr,
