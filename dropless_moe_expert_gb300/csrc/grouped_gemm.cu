@@ -587,9 +587,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
             // stages free up.  Otherwise both CTAs follow the static order.
             auto publish = [&](int k, int tile) {
                 s_tq[k % TQ] = tile;
-                st_shared_cluster(tq_peer + 4u * (k % TQ), tile);
                 mbar_arrive(&qfull[k % TQ]);
-                mbar_arrive_cluster(qfull_peer + 8u * (k % TQ));
+                send_to_peer(tq_peer + 4u * (k % TQ), tile, qfull_peer + 8u * (k % TQ));
                 return true;
             };
             int cur = -1, nxt = total_tiles;

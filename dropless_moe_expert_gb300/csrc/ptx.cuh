@@ -182,22 +182,27 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-// 32-bit store to a shared::cluster address (possibly in the peer CTA).
-__device__ __forceinline__ void st_shared_cluster(uint32_t cluster_addr, int v) {
-    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
-}
-// Arrive on an mbarrier given by its shared::cluster address (possibly in the peer CTA).
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
-}
-// Arrive on a (possibly remote) mbarrier with release semantics at CTA
-// scope only: for hand-overs that carry no data in memory, such as an
-// accumulator whose TMEM reads were already waited for and fenced with
-// tcgen05.fence::before_thread_sync.  A cluster-scope release fences this
-// thread's memory operations at cluster scope first and holds the thread
-// until the peer observes the arrival.
+// Arrive on an mbarrier given by its shared::cluster address (possibly in
+// the peer CTA), with release semantics at CTA scope only: for hand-overs
+// that carry no data in memory, such as an accumulator whose TMEM reads were
+// already waited for and fenced with tcgen05.fence::before_thread_sync.  A
+// cluster-scope release fences this thread's memory operations at cluster
+// scope first and holds the thread until the peer observes the arrival.
 __device__ __forceinline__ void mbar_arrive_cluster_cta(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+// Hands a 32-bit value to the peer CTA of a pair without waiting: a relaxed
+// arrive that also expects 4 bytes of transaction on the peer's mbarrier,
+// then an asynchronous store of the value to the peer's shared memory that
+// completes those 4 bytes on the same mbarrier.  The barrier's phase cannot
+// complete before the value has landed, so a reader that waits on it reads
+// the value; the sending thread is not held.  Both addresses are
+// shared::cluster addresses in the peer CTA.
+__device__ __forceinline__ void send_to_peer(uint32_t value_addr, int v, uint32_t mbar_addr) {
+    asm volatile("mbarrier.arrive.expect_tx.relaxed.cluster.shared::cluster.b64 _, [%0], 4;" ::"r"(mbar_addr) : "memory");
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(value_addr), "r"(v),
+                 "r"(mbar_addr)
+                 : "memory");
 }
 // TMA load into this CTA's shared memory that signals an mbarrier of either CTA
 // of the pair (given by its shared::cluster address).

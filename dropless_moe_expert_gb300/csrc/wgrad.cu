@@ -497,7 +497,7 @@ wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmD, const Params p) {
             epilogue(p, &tmD, t, tbase, q, lane, s_gcnt[t.e] == 0, stage, sbuf);
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(tempty0 + 8u * acc);
+            if (lane == 0) mbar_arrive_cluster_cta(tempty0 + 8u * acc);
             acc ^= 1u;
             if (acc == 0) acc_phase ^= 1u;
         }
