@@ -592,17 +592,20 @@ def measure_forward(moe, s_name, args, ws, rank, local, full=True):
     _barrier(ws)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    e2e_sampler = ClockSampler(local).start() if rank == 0 else None
     e0.record(stream)
     e2e_run(args.steps)
     e1.record(stream)
     torch.cuda.synchronize()
+    e2e_clocks = e2e_sampler.stop() if e2e_sampler else None
     assert moe.device_status() == 0
     e2e_ms = _max_over_ranks(e0.elapsed_time(e1), ws)
     res["e2e"] = {"value": aggregate(flops_step, ws, args.steps, e2e_ms) / 1e12, "unit": "TFLOP/s",
                   "h2d_bytes_per_step": T * d * 2, "d2h_bytes_per_step": T * d * 2,
                   "ms_per_step": e2e_ms / args.steps,
                   "copies": "every batch's copies inside the timed region, overlapped with the neighbouring "
-                            "batches' compute (moe_forward_host_pipelined)"}
+                            "batches' compute (moe_forward_host_pipelined)",
+                  "clocks": e2e_clocks}
     del ws_pipe
 
     # ---- the whole layer (one moe_forward call) captured once as a CUDA graph
