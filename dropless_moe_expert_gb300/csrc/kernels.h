@@ -72,10 +72,11 @@ cudaError_t launch_permute_mxfp8(const uint16_t *x, const int32_t *topk_idx, con
                                  const int32_t *offsets, int T, int K, int d, int E, uint8_t *xq, uint8_t *sfa,
                                  cudaStream_t stream);
 
-// MXFP8 grouped GEMMs (single-CTA tiles).  swiglu: GEMM1 (A = x codes [TK, d],
+// MXFP8 grouped GEMMs (single-CTA tiles; GEMM2 on CTA pairs where its groups
+// are large and Kdim < 4096).  swiglu: GEMM1 (A = x codes [TK, d],
 // W = W1 codes [E, 2f, d], out = h codes [TK, f], sfo = h scale atoms);
 // else GEMM2 (A = h codes [TK, f], W = W2 codes [E, d, f], out = y_perm bf16).
-cudaError_t grouped_gemm_mx_setup();
+cudaError_t grouped_gemm_mx_setup(struct GemmLaunch *cfg);
 cudaError_t launch_grouped_gemm_mx(bool swiglu, const uint8_t *A, const uint8_t *sfa, size_t sfa_bytes, int TK,
                                    int Kdim, const uint8_t *W, const uint8_t *sfw, size_t sfw_bytes, int E, int n_out,
                                    const int32_t *offsets, void *out, uint8_t *sfo, size_t sfo_bytes,
@@ -110,6 +111,7 @@ struct GemmLaunch {
     int pairs_swiglu = 0;
     int pairs_plain = 0;
     int wgrad_pairs = 0;  // resident CTA pairs of the weight-gradient pair kernel
+    int mx_pairs = 0;  // ... of the MXFP8 GEMM2 pair kernel
     int device = -1;
     int *sched_base = nullptr;  // device address of the dynamic tile order's counter table
 };

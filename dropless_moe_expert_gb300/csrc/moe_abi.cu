@@ -53,7 +53,7 @@ moe_status_t device_state(DeviceState **out) {
         if (major != 10) return MOE_ERR_UNSUPPORTED;  // built for sm_103a only
         if (moe::grouped_gemm_setup(s.num_sms, &s.gemm) != cudaSuccess) return MOE_ERR_CUDA;
         if (moe::router_setup() != cudaSuccess) return MOE_ERR_CUDA;
-        if (moe::grouped_gemm_mx_setup() != cudaSuccess) return MOE_ERR_CUDA;
+        if (moe::grouped_gemm_mx_setup(&s.gemm) != cudaSuccess) return MOE_ERR_CUDA;
         if (moe::wgrad_setup(&s.gemm) != cudaSuccess) return MOE_ERR_CUDA;
         if (cudaGetSymbolAddress(reinterpret_cast<void **>(&s.status), g_device_status) != cudaSuccess)
             return MOE_ERR_CUDA;

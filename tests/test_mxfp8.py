@@ -17,8 +17,8 @@ import torch
 import oracle
 from workloads import Shape, make_tokens, make_weights
 
-from _helpers import (check_logits, check_mx_rounded, check_output, check_routing, to_np, unpack_group_atoms,
-                      unpack_plain_atoms)
+from _helpers import (check_logits, check_mx_rounded, check_output, check_rounded, check_routing, to_np,
+                      unpack_group_atoms, unpack_plain_atoms)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -96,6 +96,27 @@ def test_layer_matches_mxfp8_oracle(s):
     q_err = np.linalg.norm(to_np(y)[same] - y_bf16[same]) / np.linalg.norm(y_bf16[same])
     print(f"{s}: h codes equal {codes_equal:.5f}; y rel_l2 {r[0]:.2e} vs the MXFP8 oracle, "
           f"{q_err:.2e} vs the bf16 oracle")
+
+
+def test_gemm2_pairs_over_device_h_against_oracle():
+    """GEMM2 of pair-sized groups with a short reduction, which runs on the
+    CTA-pair MXFP8 kernel with several tiles per pair: y_perm against the
+    fp64 product of the device's own dequantised h and the oracle's
+    dequantised W2, every element within the bf16 rounding bound.  Taking the
+    device's h isolates GEMM2 from the few h codes that round to the other
+    side of an E4M3 step, which the whole-layer check meets at this size."""
+    s = Shape(T=8192, d=1024, E=8, K=2, f=512, bias="normal_0.5")
+    _, w, _, layer = _run(s, seed=s.T)
+    v = layer.views(s.T)
+    offs = to_np(v["offsets"]).astype(np.int64)
+    hd = oracle.mx_dequantize(to_np(v["hq"]), unpack_group_atoms(to_np(v["sfh"]), offs, s.f))
+    ref = np.zeros((s.T * s.K, s.d))
+    for e in range(s.E):
+        lo, hi = int(offs[e]), int(offs[e + 1])
+        if hi > lo:
+            _, _, W2d = oracle.mx_quantize(w.W2[e].float().numpy())
+            ref[lo:hi] = hd[lo:hi] @ W2d.T
+    check_rounded(to_np(v["y_perm"]), ref, "y_perm (MXFP8 GEMM2 over the device's h)")
 
 
 def test_step_by_step_api_matches_single_call():
