@@ -19,12 +19,13 @@
 //     tokens chose it in a shared bitmap (atomicOr: the final bitmap does not
 //     depend on order), and from it writes the chunk's per-expert count and
 //     every pair's rank inside the chunk.
-//  2. route_scan: one CTA of 1024 threads, each owning one expert and a slice
-//     of chunks; counts = sum over chunks, offsets = exclusive scan over
-//     experts, chunk_base[c][e] = offsets[e] + rows of expert e in earlier
-//     chunks.
-//  3. route_scatter: row_of[t,k] = chunk_base[chunk(t)][e] + rank;
-//     src_tok[row] = t.  Rows of a group are thus in ascending token order.
+//  2. route_scan: one CTA of 1024 threads per 32 experts, each thread owning
+//     one expert and a slice of chunks; counts = sum over chunks,
+//     chunk_base[c][e] = rows of expert e in earlier chunks.
+//  3. route_scatter: every CTA scans counts over the experts (CTA 0 writes
+//     them as offsets); row_of[t,k] = offsets[e] + chunk_base[chunk(t)][e] +
+//     rank; src_tok[row] = t.  Rows of a group are thus in ascending token
+//     order.
 #include "kernels.h"
 
 #include <math.h>
@@ -175,60 +176,42 @@ route_topk_kernel(const float *__restrict__ L, int T, int E, int K, int32_t *__r
     }
 }
 
-// Thread (e, s): expert e < EP (E rounded up to a multiple of 32), slice s of
-// S = SCAN_THREADS / EP consecutive chunk ranges.  Loads of one chunk row are
-// coalesced across the experts of a warp.
+// Per-expert prefix over the chunks, spread over CTAs of SCAN_E experts.
+// Thread (e, s) of a CTA: expert e0 + e, slice s of S = SCAN_THREADS / SCAN_E
+// consecutive chunk ranges, so a warp's loads of one chunk row are coalesced
+// across its experts.  Writes counts[e] and chunk_base[c][e], the rows of
+// expert e in chunks before c (the base within the expert's group; the
+// scatter adds the group's offset).
+constexpr int SCAN_E = 32;
 __global__ void __launch_bounds__(SCAN_THREADS)
 route_scan_kernel(const int32_t *__restrict__ chunk_counts, int C, int E, int32_t *__restrict__ counts,
-                  int32_t *__restrict__ offsets, int32_t *__restrict__ chunk_base) {
-    __shared__ int32_t part[SCAN_THREADS];   // [s][e]: rows of expert e in slice s
-    __shared__ int32_t warp_tot[MAX_E / 32];
-    const int EP = (E + 31) & ~31;
-    const int S = SCAN_THREADS / EP;
-    const int e = threadIdx.x % EP;
-    const int sl = threadIdx.x / EP;
+                  int32_t *__restrict__ chunk_base) {
+    __shared__ int32_t part[SCAN_THREADS];  // [s][e]: rows of expert e in slice s, then the slice's base
+    constexpr int S = SCAN_THREADS / SCAN_E;
+    const int el = threadIdx.x % SCAN_E;
+    const int sl = threadIdx.x / SCAN_E;
+    const int e = blockIdx.x * SCAN_E + el;
     const int CS = (C + S - 1) / S;
     const int c0 = min(C, sl * CS), c1 = min(C, c0 + CS);
     int sum = 0;
-    if (sl < S && e < E) {
+    if (e < E) {
 #pragma unroll 8
         for (int c = c0; c < c1; ++c) sum += chunk_counts[static_cast<size_t>(c) * E + e];
     }
-    if (sl < S) part[sl * EP + e] = sum;
+    part[sl * SCAN_E + el] = sum;
     __syncthreads();
     if (sl == 0) {
-        int cnt = 0;
-        for (int q = 0; q < S; ++q) cnt += part[q * EP + e];
-        // exclusive scan of cnt over experts
-        const int lane = e & 31, warp = e >> 5;
-        int v = cnt;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int n = __shfl_up_sync(0xffffffffu, v, o);
-            if (lane >= o) v += n;
-        }
-        if (lane == 31) warp_tot[warp] = v;
-        __syncwarp();
-        asm volatile("bar.sync 1, %0;" ::"r"(EP) : "memory");  // the EP threads of slice 0
-        int before = 0;
-        for (int w = 0; w < warp; ++w) before += warp_tot[w];
-        const int excl = before + v - cnt;
-        if (e < E) {
-            counts[e] = cnt;
-            offsets[e] = excl;
-            if (e == E - 1) offsets[E] = excl + cnt;
-        }
-        // turn the slice sums into slice bases
-        int run = excl;
+        int run = 0;
         for (int q = 0; q < S; ++q) {
-            const int pq = part[q * EP + e];
-            part[q * EP + e] = run;
+            const int pq = part[q * SCAN_E + el];
+            part[q * SCAN_E + el] = run;
             run += pq;
         }
+        if (e < E) counts[e] = run;
     }
     __syncthreads();
-    if (sl < S && e < E) {
-        int run = part[sl * EP + e];
+    if (e < E) {
+        int run = part[sl * SCAN_E + el];
 #pragma unroll 8
         for (int c = c0; c < c1; ++c) {
             chunk_base[static_cast<size_t>(c) * E + e] = run;
@@ -237,15 +220,40 @@ route_scan_kernel(const int32_t *__restrict__ chunk_counts, int C, int E, int32_
     }
 }
 
+// Every CTA forms the exclusive scan of counts over the experts (E <= 256)
+// in shared memory, and CTA 0 writes it to offsets (E + 1 entries).  Then
+// row_of[t, k] = offsets[e] + chunk_base[chunk of t][e] + (the rank within
+// the chunk that row_of holds on entry), and src_tok of that row is t.
 __global__ void route_scatter_kernel(const int32_t *__restrict__ topk_idx, const int32_t *__restrict__ chunk_base,
-                                     int T, int E, int K, int32_t *__restrict__ row_of,
+                                     const int32_t *__restrict__ counts, int T, int E, int K,
+                                     int32_t *__restrict__ offsets, int32_t *__restrict__ row_of,
                                      int32_t *__restrict__ src_tok) {
+    __shared__ int32_t s_off[MAX_E + 1];
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        int carry = 0;
+        for (int base = 0; base < E; base += 32) {
+            const int v = base + lane < E ? counts[base + lane] : 0;
+            int incl = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int n = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += n;
+            }
+            if (base + lane < E) s_off[base + lane] = carry + incl - v;
+            carry += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) s_off[E] = carry;
+    }
+    __syncthreads();
+    if (blockIdx.x == 0)
+        for (int e = threadIdx.x; e <= E; e += blockDim.x) offsets[e] = s_off[e];
     const size_t TK = static_cast<size_t>(T) * K;
     for (size_t p = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; p < TK;
          p += static_cast<size_t>(gridDim.x) * blockDim.x) {
         const int t = static_cast<int>(p / K);
         const int e = topk_idx[p];
-        const int r = chunk_base[static_cast<size_t>(t / CH) * E + e] + row_of[p];
+        const int r = s_off[e] + chunk_base[static_cast<size_t>(t / CH) * E + e] + row_of[p];
         row_of[p] = r;
         src_tok[r] = t;
     }
@@ -277,12 +285,14 @@ cudaError_t launch_route(const float *logits, int T, int E, int K, int32_t *topk
         rt::route_topk_kernel<32, 8, TOPK_THREADS><<<C, TOPK_THREADS, 0, stream>>>(logits, T, E, K, topk_idx, topk_w, row_of, chunk_counts);
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
-    rt::route_scan_kernel<<<1, rt::SCAN_THREADS, 0, stream>>>(chunk_counts, C, E, counts, offsets, chunk_base);
+    rt::route_scan_kernel<<<(E + rt::SCAN_E - 1) / rt::SCAN_E, rt::SCAN_THREADS, 0, stream>>>(chunk_counts, C, E,
+                                                                                              counts, chunk_base);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     const size_t TK = static_cast<size_t>(T) * K;
     const int blocks = static_cast<int>(std::min<size_t>((TK + 255) / 256, 152 * 8));
-    rt::route_scatter_kernel<<<blocks, 256, 0, stream>>>(topk_idx, chunk_base, T, E, K, row_of, src_tok);
+    rt::route_scatter_kernel<<<blocks, 256, 0, stream>>>(topk_idx, chunk_base, counts, T, E, K, offsets, row_of,
+                                                         src_tok);
     return cudaGetLastError();
 }
 
