@@ -25,15 +25,19 @@
 // Two kernels:
 //   router_split_kernel : Wr [d, E] fp32 -> Ws [3][E][d] bf16 (hi, mid, lo,
 //                         each K-major, i.e. transposed) in caller scratch;
-//   router_gemm_kernel  : one 128-token x BN-expert tile per CTA; per 64-wide
-//                         K slice TMA brings the x tile and the three weight
-//                         pieces' tiles (128-byte swizzle), which lie one
-//                         after the other in shared memory and so form one
-//                         K-major B operand of 3 BN rows.  One thread issues
-//                         4 tcgen05.mma (M=128, N=3 BN, K=16; for BN = 128
-//                         two per K step, N = 256 and 128): TMEM columns
-//                         [0, BN) accumulate x.hi, [BN, 2BN) x.mid and
-//                         [2BN, 3BN) x.lo, each in fp32.  Four warps form
+//   router_gemm_kernel  : one tile of MB x 128 tokens x BN experts per CTA;
+//                         per 64-wide K slice TMA brings the MB x tiles and
+//                         the three weight pieces' tiles (128-byte swizzle),
+//                         which lie one after the other in shared memory and
+//                         so form one K-major B operand of 3 BN rows.  One
+//                         thread issues, per 128-token block, 4 tcgen05.mma
+//                         (M=128, N=3 BN, K=16; for BN = 128 two per K step,
+//                         N = 256 and 128) into the block's accumulator:
+//                         TMEM columns [0, BN) accumulate x.hi, [BN, 2BN)
+//                         x.mid and [2BN, 3BN) x.lo, each in fp32.  Tiles of
+//                         two blocks (MB = 2) share the weight tiles, halving
+//                         their bytes per token; they are used where one-block
+//                         tiles would take more than one wave of the GPU.  Four warps form
 //                         L = (x.hi + x.mid) + x.lo + bias and store fp32
 //                         rows.  (Three MMAs of N = BN per K step measured
 //                         2-3x slower: small-N MMAs are bound by their issue
@@ -55,21 +59,23 @@ constexpr int UMMA_K = 16;
 constexpr int THREADS = 128;
 constexpr int A_BYTES = BM * BK * 2;
 
-template <int BN>
+template <int BN, int MB>
 struct Cfg {
     static constexpr int B_PIECE = BN * BK * 2;
-    static constexpr int STAGE = A_BYTES + 3 * B_PIECE;
+    static constexpr int STAGE = MB * A_BYTES + 3 * B_PIECE;
     static constexpr int STAGES = (200 * 1024) / STAGE < 8 ? (200 * 1024) / STAGE : 8;
     static constexpr int OFF_BARS = STAGES * STAGE;  // whole KBs: tiles stay 1024-aligned
     static constexpr int NUM_BARS = 2 * STAGES + 2;  // full, empty, accumulator full, drain
     static constexpr int OFF_TMEM = OFF_BARS + NUM_BARS * 8;
     static constexpr int OFF_ABORT = OFF_TMEM + 4;
     static constexpr int BYTES = OFF_ABORT + 4 + 1024;  // slack for 1024-byte alignment
-    static constexpr int TMEM_COLS = BN == 32 ? 128 : (BN == 64 ? 256 : 512);  // 3 BN, rounded up to a power of two
+    static constexpr int ACC = BN == 32 ? 128 : (BN == 64 ? 256 : 512);  // 3 BN, rounded up to a power of two
+    static constexpr int TMEM_COLS = MB * ACC;
     // one MMA of N = 3 BN where that fits (N <= 256); for BN = 128 two, of
     // N = 256 (hi and mid) and N = 128 (lo)
     static constexpr bool SPLIT_MMA = 3 * BN > 256;
     static_assert(BN == 32 || BN == 64 || BN == 128, "accumulator width");
+    static_assert(MB == 1 || (MB == 2 && BN <= 64), "accumulators of a tile fit in TMEM");
     static_assert(STAGES >= 2 && BYTES <= 227 * 1024, "shared memory budget");
     static_assert(B_PIECE % 1024 == 0, "swizzled tiles must stay 1024-byte aligned");
 };
@@ -114,12 +120,12 @@ router_split_kernel(const float *__restrict__ Wr, int d, int E, __nv_bfloat16 *_
     }
 }
 
-template <int BN>
+template <int BN, int MB>
 __global__ void __launch_bounds__(THREADS, 1)
 router_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW0,
                    const __grid_constant__ CUtensorMap tmW1, const __grid_constant__ CUtensorMap tmW2,
                    const Params p) {
-    using C = Cfg<BN>;
+    using C = Cfg<BN, MB>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BARS);
@@ -135,7 +141,7 @@ router_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
     const int n_blk = blockIdx.x % p.NT;
     const int m_blk = blockIdx.x / p.NT;  // expert tiles of one token tile are neighbours: x tile shared in L2
     const int n0 = n_blk * BN;
-    const int m0 = m_blk * BM;
+    const int m0 = m_blk * MB * BM;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::STAGES; ++i) {
@@ -172,9 +178,10 @@ router_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
         for (int kb = 0; kb < KB; ++kb) {
             if (!mbar_wait(&empty[stage], phase ^ 1u, s_abort, p.status, p.timeout_ns)) { ok = false; break; }
             uint8_t *sa = smem + stage * C::STAGE;
-            uint8_t *sb = sa + A_BYTES;
+            uint8_t *sb = sa + MB * A_BYTES;
             mbar_arrive_expect_tx(&full[stage], C::STAGE);
-            tma_load_2d(sa, &tmX, &full[stage], kb * BK, m0);
+#pragma unroll
+            for (int b = 0; b < MB; ++b) tma_load_2d(sa + b * A_BYTES, &tmX, &full[stage], kb * BK, m0 + b * BM);
             tma_load_2d(sb, &tmW0, &full[stage], kb * BK, n0);
             tma_load_2d(sb + C::B_PIECE, &tmW1, &full[stage], kb * BK, n0);
             tma_load_2d(sb + 2 * C::B_PIECE, &tmW2, &full[stage], kb * BK, n0);
@@ -198,14 +205,18 @@ router_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
             if (!mbar_wait(&full[stage], phase, s_abort, p.status, p.timeout_ns)) { ok = false; break; }
             tc_fence_after();
             const uint32_t sa = smem_u32(smem + stage * C::STAGE);
-            const uint64_t adesc = smem_desc_kmajor_sw128(sa);
-            const uint64_t bdesc = smem_desc_kmajor_sw128(sa + A_BYTES);  // hi, mid, lo rows: 3 BN
-            const uint64_t bdesc_lo = smem_desc_kmajor_sw128(sa + A_BYTES + 2 * C::B_PIECE);
+            const uint64_t bdesc = smem_desc_kmajor_sw128(sa + MB * A_BYTES);  // hi, mid, lo rows: 3 BN
+            const uint64_t bdesc_lo = smem_desc_kmajor_sw128(sa + MB * A_BYTES + 2 * C::B_PIECE);
 #pragma unroll
-            for (int j = 0; j < BK / UMMA_K; ++j) {
-                umma_bf16(tmem_base, adesc + 2 * j, bdesc + 2 * j, idesc, (kb | j) != 0);
-                if (C::SPLIT_MMA)
-                    umma_bf16(tmem_base + 2 * BN, adesc + 2 * j, bdesc_lo + 2 * j, idesc_lo, (kb | j) != 0);
+            for (int b = 0; b < MB; ++b) {
+                const uint64_t adesc = smem_desc_kmajor_sw128(sa + b * A_BYTES);
+                const uint32_t acc = tmem_base + b * C::ACC;
+#pragma unroll
+                for (int j = 0; j < BK / UMMA_K; ++j) {
+                    umma_bf16(acc, adesc + 2 * j, bdesc + 2 * j, idesc, (kb | j) != 0);
+                    if (C::SPLIT_MMA)
+                        umma_bf16(acc + 2 * BN, adesc + 2 * j, bdesc_lo + 2 * j, idesc_lo, (kb | j) != 0);
+                }
             }
             issued = true;
             umma_commit(&empty[stage]);
@@ -222,12 +233,14 @@ router_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
     }
     __syncwarp();
 
-    // epilogue: warp w owns TMEM lanes 32w..32w+31 = token rows m0+32w..
+    // epilogue: warp w owns TMEM lanes 32w..32w+31 = token rows m0+32w.. of
+    // each 128-token block
     const bool acc_ready = __all_sync(0xffffffffu, mbar_wait(accfull, 0, s_abort, p.status, p.timeout_ns));
     tc_fence_after();
-    if (acc_ready) {
-        const int row = m0 + warp * 32 + lane;
-        const uint32_t tbase = tmem_base + (static_cast<uint32_t>(warp * 32) << 16);
+#pragma unroll 1
+    for (int b = 0; acc_ready && b < MB; ++b) {
+        const int row = m0 + b * BM + warp * 32 + lane;
+        const uint32_t tbase = tmem_base + (static_cast<uint32_t>(warp * 32) << 16) + b * C::ACC;
         float *Lrow = p.L + static_cast<size_t>(row) * p.E;
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
@@ -273,10 +286,10 @@ router_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
     }
 }
 
-template <int BN>
+template <int BN, int MB>
 cudaError_t launch_gemm(const CUtensorMap &tmX, const CUtensorMap (&tmW)[3], const Params &p, int tiles,
                         cudaStream_t s) {
-    router_gemm_kernel<BN><<<tiles, THREADS, Cfg<BN>::BYTES, s>>>(tmX, tmW[0], tmW[1], tmW[2], p);
+    router_gemm_kernel<BN, MB><<<tiles, THREADS, Cfg<BN, MB>::BYTES, s>>>(tmX, tmW[0], tmW[1], tmW[2], p);
     return cudaGetLastError();
 }
 
@@ -294,14 +307,17 @@ int router_tile_n(int T, int E) {
 
 cudaError_t router_setup() {
     cudaError_t e;
-    if ((e = cudaFuncSetAttribute(rt::router_gemm_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  rt::Cfg<32>::BYTES)) != cudaSuccess)
+#define MOE_ROUTER_SMEM(BN, MB)                                                                               \
+    if ((e = cudaFuncSetAttribute(rt::router_gemm_kernel<BN, MB>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                                  rt::Cfg<BN, MB>::BYTES)) != cudaSuccess)                                      \
         return e;
-    if ((e = cudaFuncSetAttribute(rt::router_gemm_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  rt::Cfg<64>::BYTES)) != cudaSuccess)
-        return e;
-    return cudaFuncSetAttribute(rt::router_gemm_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                rt::Cfg<128>::BYTES);
+    MOE_ROUTER_SMEM(32, 1)
+    MOE_ROUTER_SMEM(64, 1)
+    MOE_ROUTER_SMEM(128, 1)
+    MOE_ROUTER_SMEM(32, 2)
+    MOE_ROUTER_SMEM(64, 2)
+#undef MOE_ROUTER_SMEM
+    return cudaSuccess;
 }
 
 cudaError_t launch_router_logits(const uint16_t *x, const float *Wr, const float *bias, int T, int d, int E,
@@ -331,11 +347,21 @@ cudaError_t launch_router_logits(const uint16_t *x, const float *Wr, const float
     p.vec4 = (E % 4 == 0) && (reinterpret_cast<uintptr_t>(logits) % 16 == 0);
     p.status = status;
     p.timeout_ns = timeout_ns;
-    const int tiles = ((T + rt::BM - 1) / rt::BM) * p.NT;
+    // Tiles of two 128-token blocks where one-block tiles would take more
+    // than one wave: the busiest SMs then take in x for 256 tokens and the
+    // weight tiles once, instead of both twice.
+    const int mt = (T + rt::BM - 1) / rt::BM;
+    int dev = 0, sms = 0;
+    if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+    if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return err;
+    const bool two = bn <= 64 && mt * p.NT > sms;
+    const int tiles = (two ? (mt + 1) / 2 : mt) * p.NT;
     switch (bn) {
-        case 32: return rt::launch_gemm<32>(tmX, tmW, p, tiles, stream);
-        case 64: return rt::launch_gemm<64>(tmX, tmW, p, tiles, stream);
-        default: return rt::launch_gemm<128>(tmX, tmW, p, tiles, stream);
+        case 32: return two ? rt::launch_gemm<32, 2>(tmX, tmW, p, tiles, stream)
+                            : rt::launch_gemm<32, 1>(tmX, tmW, p, tiles, stream);
+        case 64: return two ? rt::launch_gemm<64, 2>(tmX, tmW, p, tiles, stream)
+                            : rt::launch_gemm<64, 1>(tmX, tmW, p, tiles, stream);
+        default: return rt::launch_gemm<128, 1>(tmX, tmW, p, tiles, stream);
     }
 }
 

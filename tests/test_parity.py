@@ -108,12 +108,14 @@ def test_every_token_to_one_expert(K):
     compare_small(x, w, K)
 
 
-@pytest.mark.parametrize("E,T", [(8, 300), (64, 300), (200, 300), (200, 16000)])
+@pytest.mark.parametrize("E,T", [(8, 300), (64, 300), (200, 300), (200, 16000), (64, 20000), (20, 40000)])
 def test_router_one_hot_tokens_are_exact(E, T):
     """x[t] = 2^s e_i makes the dot product a single product: the logits must
     be exactly fp32(2^s Wr[i, e]) + bias[e], which holds only if all three
     bf16 pieces of Wr are added back exactly and each lands on its expert.
-    T = 16000 takes 128-column expert tiles (two MMAs per K step)."""
+    T = 16000 takes 128-column expert tiles (two MMAs per K step); T = 20000
+    and 40000 take tiles of two 128-token blocks (more than one wave of
+    one-block tiles), the last one partial or with its second block past T."""
     import dropless_moe_expert_gb300 as moe
     d = 256
     g = np.random.default_rng(E)
@@ -133,10 +135,11 @@ def test_router_one_hot_tokens_are_exact(E, T):
 
 
 # expert tiles of 32, 64 and (at least 120 token tiles) 128 columns, the last
-# two with a partial tile
+# two with a partial tile; tiles of two 128-token blocks (the last two)
 @pytest.mark.parametrize("s", [Shape(T=1000, d=512, E=8, K=2, f=64), Shape(T=300, d=1024, E=256, K=8, f=64),
                                Shape(T=129, d=64, E=100, K=4, f=64), Shape(T=16000, d=128, E=128, K=8, f=64),
-                               Shape(T=15400, d=256, E=130, K=2, f=64)],
+                               Shape(T=15400, d=256, E=130, K=2, f=64), Shape(T=20000, d=256, E=64, K=2, f=64),
+                               Shape(T=40000, d=128, E=20, K=2, f=64)],
                          ids=lambda s: f"T{s.T}_d{s.d}_E{s.E}")
 def test_router_logits_bound_and_deterministic(s):
     import dropless_moe_expert_gb300 as moe
