@@ -393,13 +393,15 @@ grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
 // CTA-pair variant of GEMM2 (cluster of 2): 256-row tiles through
 // cta_group::2 block-scaled MMAs (M = 256).  CTA r loads A rows row0 + 128 r
 // .. + 127 and rows 128 r .. 128 r + 127 of the 256-row column block of W2,
-// so each SM moves 32 KB of operands per 128-wide K slice instead of 48 KB.  Scales: each CTA
-// holds the scale atom of its own 128 A rows and both atoms of the 256 B
-// rows (each CTA's half of D needs all B columns' scales), and the pair copy
-// (tcgen05.cp.cta_group::2, issued by CTA 0) moves each CTA's atoms into its
-// own TMEM.  Every copy of both CTAs -- the atoms too, through 2D tensor maps
-// of 256-byte rows -- completes on CTA 0's full barrier; CTA 0's commits free
-// both CTAs' stages and fill both accumulators.
+// so each SM moves 32 KB of operands per 128-wide K slice instead of 48 KB.
+// Scales: each CTA holds the scale atom of its own 128 A rows and both atoms
+// of the 256 B rows (each CTA's half of D needs all B columns' scales), and
+// the pair copy (tcgen05.cp.cta_group::2, issued by CTA 0) moves each CTA's
+// atoms into its own TMEM.  Every copy of both CTAs -- the atoms too, through
+// 2D tensor maps of 256-byte rows -- completes on CTA 0's full barrier; CTA
+// 0's commits free both CTAs' stages and fill both accumulators.  The eight
+// epilogue warps of each CTA hand CTA 0's accumulator back once their values
+// are loaded.
 // ======================================================================
 constexpr int P_BM = 256;
 constexpr int P_BAND = 8;
