@@ -44,6 +44,8 @@
 //                         cost, not by the tensor pipe.)  Expert rows past E
 //                         and token rows past T come from TMA zero fill and
 //                         are not stored.
+#include <atomic>
+
 #include "kernels.h"
 #include "ptx.cuh"
 #include "tmap.h"
@@ -351,9 +353,15 @@ cudaError_t launch_router_logits(const uint16_t *x, const float *Wr, const float
     // than one wave: the busiest SMs then take in x for 256 tokens and the
     // weight tiles once, instead of both twice.
     const int mt = (T + rt::BM - 1) / rt::BM;
-    int dev = 0, sms = 0;
+    static std::atomic<int> sm_count[64];  // per device, read once
+    int dev = 0;
     if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
-    if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return err;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    int sms = sm_count[dev].load(std::memory_order_relaxed);
+    if (sms == 0) {
+        if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return err;
+        sm_count[dev].store(sms, std::memory_order_relaxed);
+    }
     const bool two = bn <= 64 && mt * p.NT > sms;
     const int tiles = (two ? (mt + 1) / 2 : mt) * p.NT;
     switch (bn) {
